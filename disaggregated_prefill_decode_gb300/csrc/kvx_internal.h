@@ -1,0 +1,123 @@
+// Internal definitions shared by the kvx translation units (not installed; the public ABI is kvx.h).
+#pragma once
+
+#include "kvx.h"
+
+#include <atomic>
+#include <cstdint>
+#include <vector>
+
+namespace kvx {
+
+// One tile of copy work: a CTA moves it for one (layer, plane). Offsets are bytes into the
+// producer / consumer buffer of (layer, plane, shard). Contiguous plans: `n` is a byte count.
+// Strided plans (head-shard remap): `n` rows of CopyArgs::width bytes at the two row pitches.
+struct alignas(16) TileDesc {
+    int64_t src_off;
+    int64_t dst_off;
+    int32_t n;
+    int32_t s_shard;
+    int32_t d_shard;
+    int32_t pad;
+};
+static_assert(sizeof(TileDesc) == 32, "TileDesc is two 16-byte words");
+
+// Kernel arguments of one push launch (passed by value).
+struct CopyArgs {
+    const TileDesc *tiles;
+    const uint8_t *const *src_base;   // [n_layers][n_planes][src_shards] device pointers
+    uint8_t *const *dst_base;         // [n_layers][n_planes][dst_shards]
+    int32_t *err;                     // [n_layers] error words, set only when a tile is out of bounds
+    int64_t src_buf_bytes;
+    int64_t dst_buf_bytes;
+    int64_t src_pitch;                // producer row bytes
+    int64_t dst_pitch;                // consumer row bytes
+    int32_t width;                    // strided: bytes copied per row
+    int32_t n_planes;
+    int32_t src_shards;
+    int32_t dst_shards;
+    int32_t layer0;
+};
+
+struct Geom {
+    int32_t n_layers, n_planes, n_shards, heads_per_shard, head_dim, elem_bytes, block_size;
+    int64_t n_blocks;
+    int64_t head_bytes() const { return (int64_t)head_dim * elem_bytes; }
+    int64_t row_bytes() const { return (int64_t)heads_per_shard * head_bytes(); }
+    int64_t buf_bytes() const { return n_blocks * block_size * row_bytes(); }
+    int32_t n_buffers() const { return n_layers * n_planes * n_shards; }
+};
+
+struct PendingPush {
+    cudaEvent_t done;
+    int32_t layer_begin, layer_end;
+};
+
+// Head-shard pair: the contiguous head range one producer shard shares with one consumer shard, as
+// byte offsets inside a producer row and a consumer row.
+struct Pair { int32_t s, d; int64_t src_seg_off, dst_seg_off; };
+std::vector<Pair> shard_pairs(const Geom &s, const Geom &d);
+
+// Thread-local error text; returns `st` so call sites can `return fail(st, ...)`.
+kvx_status fail(kvx_status st, const char *fmt, ...);
+kvx_status cuda_fail(cudaError_t e, const char *what);
+void count_launch(int64_t n = 1);
+size_t align_up(size_t x, size_t a);
+
+// Device memory from a library-owned stream-ordered pool (one per device; it keeps freed memory
+// for reuse instead of returning it to the driver at every synchronisation).
+kvx_status pool_alloc(void **ptr, size_t bytes, cudaStream_t stream);
+void pool_free(void *ptr);
+// A non-blocking stream per device for the library's own small read-backs.
+kvx_status aux_stream(cudaStream_t *out);
+
+// Launches the tile copy for layers [args.layer0, args.layer0 + n_layers) (kvx_push.cu).
+cudaError_t launch_copy(const CopyArgs &args, int64_t n_tiles, int32_t n_layers, int32_t vec, bool strided,
+                        int32_t threads, cudaStream_t stream);
+
+}  // namespace kvx
+
+// The plan object behind kvx_plan_t.
+struct kvx_plan_s {
+    kvx::Geom src{}, dst{};
+    std::vector<void *> src_base, dst_base;   // host copies of the pools' pointer tables
+
+    // merged token runs (host), rows = block * block_size + slot
+    std::vector<int32_t> run_src_row, run_dst_row, run_ntok;
+
+    // copy shape
+    int32_t strided = 0;
+    int32_t vec = 16;
+    int32_t width = 0;
+    int32_t tile_bytes = 16384;
+    int32_t threads = 256;
+    int64_t n_tiles = 0;                       // per (layer, plane)
+    int64_t bytes_per_layer = 0;
+    std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans
+
+    // device copy: [tiles][src_base][dst_base][err]
+    void *dev = nullptr;
+    size_t dev_bytes = 0;
+    size_t off_tiles = 0, off_src = 0, off_dst = 0, off_err = 0;
+    std::vector<uint8_t> upload_img;           // host image of the uploaded descriptor bytes
+    bool uploaded = false;
+    bool device_built = false;                 // descriptors were written on the device
+    cudaEvent_t upload_evt = nullptr;
+    cudaStream_t upload_stream = nullptr;
+
+    // pushes issued and not yet confirmed by kvx_sync
+    std::vector<kvx::PendingPush> pending;
+    std::vector<cudaEvent_t> free_events;
+    std::vector<int32_t> layer_state;          // kvx_layer_state per layer
+    std::vector<uint8_t> inject;               // host fault injection armed, per layer
+    std::vector<uint8_t> injected_pending;     // injected failure waiting for sync, per layer
+};
+
+namespace kvx {
+// Shared by host-built and device-built plans (kvx_plan.cpp).
+kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl);
+void finish_plan_shape(kvx_plan_s *pl);
+// Device layout and kernel arguments of a plan (kvx_push.cu).
+void plan_layout(kvx_plan_s *pl);
+CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0);
+}  // namespace kvx

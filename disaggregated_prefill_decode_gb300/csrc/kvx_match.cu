@@ -1,0 +1,683 @@
+// Bidirectional reuse on the device: chained block hashes, the resident-block hash table, the
+// per-session match with the recompute threshold, and emission of the decode->prefill copy plan.
+//
+// Follows the bidirectional KV transfer article (spke.com 3845): Figure 1 steps 4-6 (prefill checks
+// the remote reusable KV after applying local cache hits, queues a receive when the reusable tokens
+// reach the threshold, then the transfer moves decode blocks to prefill) and "KV-Recompute-
+// Schwellenwert" (recompute below the threshold, pull at or above it). The block hash is chained
+// 64-bit FNV-1a (Fowler/Noll/Vo): per octet, xor then multiply by the FNV prime.
+#include "kvx_internal.h"
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+namespace kvx {
+
+constexpr uint64_t kFnvBasis = 14695981039346656037ull;
+constexpr uint64_t kFnvPrime = 1099511628211ull;
+
+// ------------------------------------------------------------------------------------------------
+// Hashing
+// ------------------------------------------------------------------------------------------------
+
+// FNV-1a over the 4 octets of one token id, least significant first.
+__device__ __forceinline__ uint64_t fnv_token(uint64_t h, uint32_t v) {
+    h = (h ^ (v & 0xffu)) * kFnvPrime;
+    h = (h ^ ((v >> 8) & 0xffu)) * kFnvPrime;
+    h = (h ^ ((v >> 16) & 0xffu)) * kFnvPrime;
+    h = (h ^ (v >> 24)) * kFnvPrime;
+    return h;
+}
+
+// Hash of one full block: parent hash (8 octets, little endian) then block_size token ids.
+__device__ __forceinline__ uint64_t hash_block(uint64_t parent, const uint32_t *tok, int32_t bs) {
+    uint64_t h = kFnvBasis;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) h = (h ^ ((parent >> (8 * b)) & 0xffull)) * kFnvPrime;
+    int32_t i = 0;
+    for (; i + 4 <= bs; i += 4) {
+        const uint32_t t0 = tok[i], t1 = tok[i + 1], t2 = tok[i + 2], t3 = tok[i + 3];
+        h = fnv_token(h, t0);
+        h = fnv_token(h, t1);
+        h = fnv_token(h, t2);
+        h = fnv_token(h, t3);
+    }
+    for (; i < bs; ++i) h = fnv_token(h, tok[i]);
+    return h;
+}
+
+// One thread per session; a session's chain is sequential by definition.
+__global__ void kvx_hash_sessions(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t bs,
+                                  uint64_t *out, const int64_t *hash_off, int64_t n_tok_total, int32_t *err) {
+    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n_sessions) return;
+    const int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
+    const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
+    if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total || hash_off[s] < 0 || hash_off[s + 1] - hash_off[s] < n_full) {
+        atomicOr(err, 1);
+        return;
+    }
+    uint64_t parent = 0;
+    uint64_t *o = out + hash_off[s];
+    for (int64_t j = 0; j < n_full; ++j) {
+        parent = hash_block(parent, tokens + t0 + j * bs, bs);
+        o[j] = parent;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Resident-block table: open addressing, linear probing, key 0 kept in the header
+// ------------------------------------------------------------------------------------------------
+
+struct TableHeader {
+    int32_t has_zero;
+    int32_t zero_val;
+    int32_t dup;
+    int32_t pad;
+};
+
+struct TableView {
+    const uint64_t *keys;
+    const int32_t *vals;
+    const TableHeader *hdr;
+    uint64_t mask;
+    int32_t shift;
+};
+
+__device__ __forceinline__ uint64_t slot_of(uint64_t key, int32_t shift) {
+    return (key * 0x9E3779B97F4A7C15ull) >> shift;
+}
+
+__global__ void kvx_table_insert(const uint64_t *keys, const int32_t *vals, int64_t n, uint64_t *tkeys, int32_t *tvals,
+                                 TableHeader *hdr, uint64_t mask, int32_t shift) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint64_t k = keys[i];
+    const int32_t v = vals[i];
+    if (k == 0) {
+        if (atomicExch(&hdr->has_zero, 1) == 1) atomicExch(&hdr->dup, 1);
+        hdr->zero_val = v;
+        return;
+    }
+    uint64_t idx = slot_of(k, shift);
+    for (uint64_t probe = 0; probe <= mask; ++probe) {
+        const unsigned long long prev =
+            atomicCAS(reinterpret_cast<unsigned long long *>(tkeys + idx), 0ull, (unsigned long long)k);
+        if (prev == 0ull) { tvals[idx] = v; return; }
+        if (prev == (unsigned long long)k) { atomicExch(&hdr->dup, 1); return; }
+        idx = (idx + 1) & mask;
+    }
+    atomicExch(&hdr->dup, 2);   // table full: cannot happen at load factor <= 1/2
+}
+
+__device__ __forceinline__ int32_t table_find(const TableView &t, uint64_t key) {
+    if (key == 0) return t.hdr->has_zero ? t.hdr->zero_val : -1;
+    uint64_t idx = slot_of(key, t.shift);
+    for (uint64_t probe = 0; probe <= t.mask; ++probe) {
+        const uint64_t k = t.keys[idx];
+        if (k == key) return t.vals[idx];
+        if (k == 0) return -1;
+        idx = (idx + 1) & t.mask;
+    }
+    return -1;
+}
+
+__global__ void kvx_table_lookup_kernel(TableView t, const uint64_t *keys, int64_t n, int32_t *out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = table_find(t, keys[i]);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Match
+// ------------------------------------------------------------------------------------------------
+
+// Per session: hash block by block while either prefix (local hits, agreement with the published
+// remote hashes) is still open; stop once both have ended.
+__global__ void kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t bs,
+                                   TableView table, const uint64_t *remote_hash, const int64_t *rem_off,
+                                   int32_t threshold, int64_t n_tok_total, int64_t n_pub, kvx_match_result *out,
+                                   int64_t *push_blocks, int32_t *err) {
+    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n_sessions) return;
+    int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
+    int64_t r0 = rem_off[s], n_rem = rem_off[s + 1] - r0;
+    // malformed offsets: flag them and treat the session as empty, so no array is read out of range
+    if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total) { atomicOr(err, 1); t0 = 0; n_tok = 0; }
+    if (r0 < 0 || n_rem < 0 || r0 + n_rem > n_pub) { atomicOr(err, 2); r0 = 0; n_rem = 0; }
+    const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
+    int64_t l_loc = 0, l_rem = 0;
+    bool loc_open = true, rem_open = true;
+    uint64_t parent = 0;
+    for (int64_t j = 0; j < n_full && (loc_open || rem_open); ++j) {
+        const uint64_t h = hash_block(parent, tokens + t0 + j * bs, bs);
+        parent = h;
+        if (loc_open) {
+            if (table_find(table, h) >= 0) ++l_loc; else loc_open = false;
+        }
+        if (rem_open) {
+            if (j < n_rem && remote_hash[r0 + j] == h) ++l_rem; else rem_open = false;
+        }
+    }
+    const int64_t missing_blocks = l_rem > l_loc ? l_rem - l_loc : 0;
+    const int64_t missing = missing_blocks * bs;
+    if (missing > (int64_t)INT32_MAX || l_loc > (int64_t)INT32_MAX) atomicOr(err, 4);
+    const int32_t push = (missing > 0 && missing >= threshold) ? 1 : 0;
+    kvx_match_result r;
+    r.local_hit_blocks = (int32_t)l_loc;
+    r.remote_hit_blocks = (int32_t)l_rem;
+    r.missing_tokens = (int32_t)missing;
+    r.push = push;
+    r.dst_start = -1;
+    out[s] = r;
+    push_blocks[s] = push ? missing_blocks : 0;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Scans: warp shuffles inside a warp, warp totals through shared memory, block totals through a
+// second level (reduce-then-scan over 1024-element blocks).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kScanThreads = 1024;
+
+// Inclusive scan of one value per thread across the block; returns it and the block total.
+__device__ __forceinline__ int64_t block_inclusive_scan(int64_t v, int64_t *warp_sums, int64_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < n_warps ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += warp_sums[warp - 1];
+    *total = warp_sums[n_warps - 1];
+    __syncthreads();
+    return v;
+}
+
+// Phase 1: exclusive scan inside each 1024-element block; block totals to partial[].
+// n is *n_dev when n_dev is not NULL, else n_host (the grid covers the host bound).
+__global__ void __launch_bounds__(kScanThreads) kvx_scan_local(const int64_t *in, int64_t *out, int64_t n_host,
+                                                                const int64_t *n_dev, int64_t *partial) {
+    __shared__ int64_t ws[32];
+    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t v = i < n ? in[i] : 0;
+    int64_t total;
+    const int64_t inc = block_inclusive_scan(v, ws, &total);
+    if (i < n) out[i] = inc - v;
+    if (threadIdx.x == 0) partial[blockIdx.x] = total;
+}
+
+// Phase 2: one block scans the partials (any count, in passes of 1024 with a carry); *sum = total.
+__global__ void __launch_bounds__(kScanThreads) kvx_scan_partials(int64_t *partial, int64_t n_part, int64_t *sum) {
+    __shared__ int64_t ws[32];
+    int64_t carry = 0;
+    for (int64_t base = 0; base < n_part; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const int64_t v = i < n_part ? partial[i] : 0;
+        int64_t total;
+        const int64_t inc = block_inclusive_scan(v, ws, &total);
+        if (i < n_part) partial[i] = carry + inc - v;
+        carry += total;
+    }
+    if (threadIdx.x == 0) *sum = carry;
+}
+
+// Phase 3: add each block's offset.
+__global__ void __launch_bounds__(kScanThreads) kvx_scan_add(int64_t *out, int64_t n_host, const int64_t *n_dev,
+                                                              const int64_t *partial) {
+    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] += partial[blockIdx.x];
+}
+
+// Exclusive scan of in[0..n) into out, total into *sum. n_bound is a host upper bound on n.
+static cudaError_t exclusive_scan(const int64_t *in, int64_t *out, int64_t n_bound, const int64_t *n_dev,
+                                  int64_t *partial, int64_t *sum, cudaStream_t st) {
+    const int64_t nb = std::max<int64_t>(1, (n_bound + kScanThreads - 1) / kScanThreads);
+    kvx_scan_local<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, partial);
+    kvx_scan_partials<<<1, kScanThreads, 0, st>>>(partial, nb, sum);
+    kvx_scan_add<<<(unsigned)nb, kScanThreads, 0, st>>>(out, n_bound, n_dev, partial);
+    count_launch(3);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Decode -> prefill plan emission
+// ------------------------------------------------------------------------------------------------
+
+// Scalars: [0] blocks the pushes need, [1] runs, [2] tiles, [4] blocks the plan emits ([0], or 0
+// when the free list is too short).
+struct MatchScratch {
+    int64_t *push_blocks;   // [n_sessions]
+    int64_t *sess_start;    // [n_sessions] exclusive scan of push_blocks
+    int64_t *pair_src;      // [B] decode block of pushed block k
+    int64_t *pair_dst;      // [B] prefill block of pushed block k
+    int64_t *flag;          // [B] 1 where a run starts
+    int64_t *run_idx;       // [B] exclusive scan of flag
+    int64_t *run_start;     // [B] first pushed block of each run
+    int64_t *tile_count;    // [B] tiles of each run
+    int64_t *tile_start;    // [B] exclusive scan of tile_count
+    int64_t *partial;       // scan partials
+    int64_t *scalars;       // [8]
+    int32_t *err;           // [4] error bits
+};
+
+__global__ void kvx_assign_dst(kvx_match_result *out, const int64_t *sess_start, int32_t n_sessions,
+                               int64_t *scalars, int64_t n_free, int32_t *err) {
+    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+    const bool fits = scalars[0] <= n_free;
+    if (s == 0) {
+        scalars[4] = fits ? scalars[0] : 0;
+        if (!fits) atomicOr(err, 8);
+    }
+    if (s < n_sessions && out[s].push) out[s].dst_start = sess_start[s];
+}
+
+// One thread per pushed block k: its session, its (decode, prefill) pair, and whether it starts a
+// run (first block of a session, or either id not its predecessor's + 1).
+__global__ void kvx_emit_pairs(const kvx_match_result *res, const int64_t *sess_start, int32_t n_sessions,
+                               const int32_t *remote_blk, const int64_t *rem_off, const int32_t *free_blocks,
+                               const int64_t *total, int64_t *pair_src, int64_t *pair_dst, int64_t *flag) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= *total) return;
+    // The last session whose range starts at or before k owns k: a pushing session s covers
+    // [sess_start[s], sess_start[s] + n_s) and every later session starts at or after its end.
+    int32_t lo = 0, hi = n_sessions - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (sess_start[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    const int32_t s = lo;
+    const int64_t i = k - sess_start[s];
+    const int64_t base = rem_off[s] + res[s].local_hit_blocks;
+    const int64_t src = remote_blk[base + i];
+    const int64_t dst = free_blocks[k];
+    pair_src[k] = src;
+    pair_dst[k] = dst;
+    int64_t starts = 1;
+    if (i > 0) starts = (src == (int64_t)remote_blk[base + i - 1] + 1 && dst == (int64_t)free_blocks[k - 1] + 1) ? 0 : 1;
+    flag[k] = starts;
+}
+
+__global__ void kvx_run_starts(const int64_t *flag, const int64_t *run_idx, const int64_t *total, int64_t *run_start) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < *total && flag[k]) run_start[run_idx[k]] = k;
+}
+
+struct EmitShape {
+    int64_t src_row_bytes, dst_row_bytes;
+    int32_t bs;
+    int32_t strided;
+    int32_t tile_bytes;
+    int32_t rows_per_tile;
+    int32_t n_pairs;
+    int32_t pad;
+    int32_t pair_s[8], pair_d[8];
+    int64_t pair_soff[8], pair_doff[8];
+};
+
+__global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, EmitShape sh, int64_t *tile_count) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n_runs = scalars[1], total = scalars[4];
+    if (r >= n_runs) return;
+    const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
+    const int64_t ntok = (k1 - run_start[r]) * sh.bs;
+    const int64_t per = sh.strided ? (ntok + sh.rows_per_tile - 1) / sh.rows_per_tile
+                                   : (ntok * sh.src_row_bytes + sh.tile_bytes - 1) / sh.tile_bytes;
+    tile_count[r] = per * sh.n_pairs;
+}
+
+// One thread per run: the run's rows (for host introspection) and its tiles, cut as the host plan
+// builder cuts them.
+__global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_start, const int64_t *scalars,
+                               const int64_t *pair_src, const int64_t *pair_dst, EmitShape sh, TileDesc *tiles,
+                               int64_t tile_cap, int32_t *run_src_row, int32_t *run_dst_row, int32_t *run_ntok,
+                               int32_t *err) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t n_runs = scalars[1], total = scalars[4];
+    if (r >= n_runs) return;
+    const int64_t k0 = run_start[r];
+    const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
+    const int64_t ntok = (k1 - k0) * sh.bs;
+    const int64_t srow = pair_src[k0] * sh.bs, drow = pair_dst[k0] * sh.bs;
+    run_src_row[r] = (int32_t)srow;
+    run_dst_row[r] = (int32_t)drow;
+    run_ntok[r] = (int32_t)ntok;
+    int64_t t = tile_start[r];
+    if (!sh.strided) {
+        const int64_t bytes = ntok * sh.src_row_bytes;
+        const int64_t s0 = srow * sh.src_row_bytes, d0 = drow * sh.dst_row_bytes;
+        for (int64_t o = 0; o < bytes; o += sh.tile_bytes)
+            for (int32_t q = 0; q < sh.n_pairs; ++q, ++t) {
+                if (t >= tile_cap) { atomicOr(err, 16); return; }
+                TileDesc d;
+                d.src_off = s0 + o;
+                d.dst_off = d0 + o;
+                d.n = (int32_t)min((int64_t)sh.tile_bytes, bytes - o);
+                d.s_shard = sh.pair_s[q];
+                d.d_shard = sh.pair_d[q];
+                d.pad = 0;
+                tiles[t] = d;
+            }
+    } else {
+        for (int64_t r0 = 0; r0 < ntok; r0 += sh.rows_per_tile)
+            for (int32_t q = 0; q < sh.n_pairs; ++q, ++t) {
+                if (t >= tile_cap) { atomicOr(err, 16); return; }
+                TileDesc d;
+                d.src_off = (srow + r0) * sh.src_row_bytes + sh.pair_soff[q];
+                d.dst_off = (drow + r0) * sh.dst_row_bytes + sh.pair_doff[q];
+                d.n = (int32_t)min((int64_t)sh.rows_per_tile, ntok - r0);
+                d.s_shard = sh.pair_s[q];
+                d.d_shard = sh.pair_d[q];
+                d.pad = 0;
+                tiles[t] = d;
+            }
+    }
+}
+
+static unsigned grid_for(int64_t n, int threads) {
+    return (unsigned)std::max<int64_t>(1, (n + threads - 1) / threads);
+}
+
+}  // namespace kvx
+
+using namespace kvx;
+
+struct kvx_table_s {
+    void *dev = nullptr;
+    uint64_t *keys = nullptr;
+    int32_t *vals = nullptr;
+    TableHeader *hdr = nullptr;
+    uint64_t capacity = 0;
+    int32_t shift = 0;
+    int64_t n = 0;
+    cudaEvent_t last_use = nullptr;   // recorded after each lookup; destroy waits for it
+    TableView view() const { return TableView{keys, vals, hdr, capacity - 1, shift}; }
+};
+
+extern "C" {
+
+kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t block_size,
+                            uint64_t *out_hash, const int64_t *hash_off, cudaStream_t stream) {
+    if (n_sessions < 0 || block_size < 1) return fail(KVX_EINVAL, "n_sessions >= 0 and block_size >= 1");
+    if (n_sessions == 0) return KVX_OK;
+    if (!tokens || !tok_off || !out_hash || !hash_off) return fail(KVX_EINVAL, "NULL device array");
+    int64_t n_tok_total = 0;
+    cudaError_t e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading tok_off");
+    void *errp = nullptr;
+    kvx_status st = pool_alloc(&errp, sizeof(int32_t), stream);
+    if (st) return st;
+    int32_t *err = static_cast<int32_t *>(errp);
+    e = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
+    if (e == cudaSuccess) {
+        count_launch();
+        kvx_hash_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                       out_hash, hash_off, n_tok_total, err);
+        e = cudaGetLastError();
+    }
+    int32_t h_err = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_err, err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    pool_free(errp);
+    if (e != cudaSuccess) return cuda_fail(e, "kvx_block_hashes");
+    if (h_err) return fail(KVX_ERANGE, "malformed tok_off, or a hash_off range shorter than the session's full blocks");
+    return KVX_OK;
+}
+
+kvx_status kvx_table_build(const uint64_t *keys, const int32_t *vals, int64_t n, cudaStream_t stream, kvx_table_t *out) {
+    if (!out) return fail(KVX_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (n < 0 || (n > 0 && (!keys || !vals))) return fail(KVX_EINVAL, "bad key/value arrays");
+    if (n > ((int64_t)1 << 40)) return fail(KVX_EUNSUPPORTED, "table too large");
+    kvx_table_s *t = new (std::nothrow) kvx_table_s();
+    if (!t) return fail(KVX_ENOMEM, "host allocation failed");
+    uint64_t cap = 16;
+    int32_t bits = 4;
+    while (cap < (uint64_t)(2 * n)) { cap <<= 1; ++bits; }
+    t->capacity = cap;
+    t->shift = 64 - bits;
+    t->n = n;
+    const size_t off_vals = align_up(sizeof(uint64_t) * cap, 256);
+    const size_t off_hdr = off_vals + align_up(sizeof(int32_t) * cap, 256);
+    const size_t bytes = off_hdr + 256;
+    kvx_status st = pool_alloc(&t->dev, bytes, stream);
+    if (st) { delete t; return st; }
+    t->keys = static_cast<uint64_t *>(t->dev);
+    t->vals = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(t->dev) + off_vals);
+    t->hdr = reinterpret_cast<TableHeader *>(static_cast<uint8_t *>(t->dev) + off_hdr);
+    cudaError_t e = cudaMemsetAsync(t->dev, 0, bytes, stream);
+    if (e == cudaSuccess && n > 0) {
+        count_launch();
+        kvx_table_insert<<<grid_for(n, 256), 256, 0, stream>>>(keys, vals, n, t->keys, t->vals, t->hdr, cap - 1,
+                                                               t->shift);
+        e = cudaGetLastError();
+    }
+    TableHeader h = {};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, t->hdr, sizeof(h), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) { pool_free(t->dev); delete t; return cuda_fail(e, "kvx_table_build"); }
+    if (h.dup) { pool_free(t->dev); delete t; return fail(KVX_EINVAL, "duplicate key in table input"); }
+    *out = t;
+    return KVX_OK;
+}
+
+kvx_status kvx_table_lookup(kvx_table_t t, const uint64_t *keys, int64_t n, int32_t *out_vals, cudaStream_t stream) {
+    if (!t) return fail(KVX_EINVAL, "NULL table");
+    if (n < 0 || (n > 0 && (!keys || !out_vals))) return fail(KVX_EINVAL, "bad arrays");
+    if (n == 0) return KVX_OK;
+    count_launch();
+    kvx_table_lookup_kernel<<<grid_for(n, 256), 256, 0, stream>>>(t->view(), keys, n, out_vals);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && !t->last_use) e = cudaEventCreateWithFlags(&t->last_use, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(t->last_use, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvx_table_lookup");
+    return KVX_OK;
+}
+
+kvx_status kvx_table_destroy(kvx_table_t t) {
+    if (!t) return KVX_OK;
+    cudaError_t e = cudaSuccess;
+    if (t->last_use) {
+        e = cudaEventSynchronize(t->last_use);
+        cudaEventDestroy(t->last_use);
+    }
+    if (t->dev) pool_free(t->dev);
+    delete t;
+    if (e != cudaSuccess) return cuda_fail(e, "kvx_table_destroy");
+    return KVX_OK;
+}
+
+kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t block_size,
+                            kvx_table_t table, const uint64_t *remote_hash, const int32_t *remote_blk,
+                            const int64_t *rem_off, int32_t threshold, const int32_t *free_blocks, int64_t n_free,
+                            const kvx_pool *remote_pool, const kvx_pool *local_pool, kvx_match_result *out,
+                            kvx_plan_t *out_plan, cudaStream_t stream) {
+    if (out_plan) *out_plan = nullptr;
+    if (n_sessions < 0 || block_size < 1 || n_free < 0) return fail(KVX_EINVAL, "bad counts");
+    if (!table) return fail(KVX_EINVAL, "NULL table");
+    if (n_sessions > 0 && (!tokens || !tok_off || !rem_off || !out || !remote_hash || !remote_blk))
+        return fail(KVX_EINVAL, "NULL device array");
+    if (n_free > 0 && !free_blocks) return fail(KVX_EINVAL, "NULL free list");
+
+    // the plan's geometry is validated before any device work
+    kvx_plan_s *pl = nullptr;
+    if (out_plan) {
+        pl = new (std::nothrow) kvx_plan_s();
+        if (!pl) return fail(KVX_ENOMEM, "host allocation failed");
+        kvx_status st = init_plan_geometry(remote_pool, local_pool, nullptr, pl);
+        if (st) { delete pl; return st; }
+        if (pl->src.block_size != block_size || pl->dst.block_size != block_size) {
+            delete pl;
+            return fail(KVX_EINVAL, "pool block sizes must equal block_size");
+        }
+        if (std::max(pl->src.n_shards, pl->dst.n_shards) > 8) {
+            delete pl;
+            return fail(KVX_EUNSUPPORTED, "device-built plans support at most 8 shard pairs");
+        }
+        pl->device_built = true;
+    }
+    if (n_sessions == 0) {
+        if (pl) { finish_plan_shape(pl); *out_plan = pl; }
+        return KVX_OK;
+    }
+
+    // host bounds: published blocks (pushed blocks never exceed them) and tokens
+    int64_t n_pub = 0, n_tok_total = 0;
+    cudaError_t e = cudaMemcpyAsync(&n_pub, rem_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) { delete pl; return cuda_fail(e, "reading rem_off / tok_off"); }
+    if (n_pub < 0 || n_tok_total < 0) { delete pl; return fail(KVX_EINVAL, "offsets are not CSR offset arrays"); }
+    const int64_t B = std::max<int64_t>(n_pub, 1);
+    const int64_t n_part = std::max<int64_t>(1, (std::max<int64_t>(B, n_sessions) + kScanThreads - 1) / kScanThreads);
+
+    // scratch, one allocation
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_push = take(sizeof(int64_t) * n_sessions), o_sess = take(sizeof(int64_t) * n_sessions);
+    const size_t o_ps = take(8 * B), o_pd = take(8 * B), o_flag = take(8 * B), o_ridx = take(8 * B);
+    const size_t o_rstart = take(8 * B), o_tcount = take(8 * B), o_tstart = take(8 * B);
+    const size_t o_part = take(8 * n_part), o_scal = take(8 * 8), o_err = take(sizeof(int32_t) * 4);
+    const size_t o_rows = take(sizeof(int32_t) * 3 * B);
+    void *scratch = nullptr;
+    kvx_status st = pool_alloc(&scratch, off, stream);
+    if (st) { delete pl; return st; }
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    MatchScratch m;
+    m.push_blocks = reinterpret_cast<int64_t *>(sb + o_push);
+    m.sess_start = reinterpret_cast<int64_t *>(sb + o_sess);
+    m.pair_src = reinterpret_cast<int64_t *>(sb + o_ps);
+    m.pair_dst = reinterpret_cast<int64_t *>(sb + o_pd);
+    m.flag = reinterpret_cast<int64_t *>(sb + o_flag);
+    m.run_idx = reinterpret_cast<int64_t *>(sb + o_ridx);
+    m.run_start = reinterpret_cast<int64_t *>(sb + o_rstart);
+    m.tile_count = reinterpret_cast<int64_t *>(sb + o_tcount);
+    m.tile_start = reinterpret_cast<int64_t *>(sb + o_tstart);
+    m.partial = reinterpret_cast<int64_t *>(sb + o_part);
+    m.scalars = reinterpret_cast<int64_t *>(sb + o_scal);
+    m.err = reinterpret_cast<int32_t *>(sb + o_err);
+    int32_t *rows = reinterpret_cast<int32_t *>(sb + o_rows);
+
+    auto cleanup = [&](kvx_status s) {
+        cudaStreamSynchronize(stream);   // nothing may still use the buffers below
+        pool_free(scratch);
+        if (pl) { if (pl->dev) pool_free(pl->dev); delete pl; }
+        return s;
+    };
+    auto ok = [&](cudaError_t x) { if (x != cudaSuccess && e == cudaSuccess) e = x; };
+
+    ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8, stream));
+    ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
+    count_launch();
+    kvx_match_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                    table->view(), remote_hash, rem_off, threshold,
+                                                                    n_tok_total, n_pub, out, m.push_blocks, m.err);
+    ok(cudaGetLastError());
+    ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
+    count_launch();
+    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free,
+                                                                  m.err);
+    ok(cudaGetLastError());
+
+    if (pl && e == cudaSuccess) {
+        const std::vector<Pair> pairs = shard_pairs(pl->src, pl->dst);
+        EmitShape sh = {};
+        sh.src_row_bytes = pl->src.row_bytes();
+        sh.dst_row_bytes = pl->dst.row_bytes();
+        sh.bs = block_size;
+        sh.strided = pl->strided;
+        sh.tile_bytes = pl->tile_bytes;
+        sh.rows_per_tile = pl->strided ? std::max<int32_t>(1, pl->tile_bytes / pl->width) : 1;
+        sh.n_pairs = (int32_t)pairs.size();
+        for (size_t q = 0; q < pairs.size(); ++q) {
+            sh.pair_s[q] = pairs[q].s;
+            sh.pair_d[q] = pairs[q].d;
+            sh.pair_soff[q] = pairs[q].src_seg_off;
+            sh.pair_doff[q] = pairs[q].dst_seg_off;
+        }
+        // a run of L blocks has at most L times the tiles of one block
+        const int64_t per_block = pl->strided ? (block_size + sh.rows_per_tile - 1) / sh.rows_per_tile
+                                              : ((int64_t)block_size * sh.src_row_bytes + pl->tile_bytes - 1) / pl->tile_bytes;
+        const int64_t tile_cap = B * per_block * sh.n_pairs;
+        pl->n_tiles = tile_cap;   // sizes the layout; the real count comes back below
+        plan_layout(pl);
+        st = pool_alloc(&pl->dev, pl->dev_bytes, stream);
+        if (st) return cleanup(st);
+        pl->upload_img.assign(pl->off_err - pl->off_src, 0);
+        memcpy(pl->upload_img.data(), pl->src_base.data(), sizeof(void *) * pl->src_base.size());
+        memcpy(pl->upload_img.data() + (pl->off_dst - pl->off_src), pl->dst_base.data(),
+               sizeof(void *) * pl->dst_base.size());
+        uint8_t *dev = static_cast<uint8_t *>(pl->dev);
+        ok(cudaMemcpyAsync(dev + pl->off_src, pl->upload_img.data(), pl->upload_img.size(), cudaMemcpyHostToDevice,
+                           stream));
+        ok(cudaMemsetAsync(dev + pl->off_err, 0, sizeof(int32_t) * (size_t)pl->src.n_layers, stream));
+        TileDesc *tiles = reinterpret_cast<TileDesc *>(dev + pl->off_tiles);
+
+        count_launch(4);
+        kvx_emit_pairs<<<grid_for(B, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, remote_blk, rem_off,
+                                                             free_blocks, &m.scalars[4], m.pair_src, m.pair_dst, m.flag);
+        ok(cudaGetLastError());
+        ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.partial, &m.scalars[1], stream));
+        kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start);
+        ok(cudaGetLastError());
+        kvx_run_tiles<<<grid_for(B, 256), 256, 0, stream>>>(m.run_start, m.scalars, sh, m.tile_count);
+        ok(cudaGetLastError());
+        ok(exclusive_scan(m.tile_count, m.tile_start, B, &m.scalars[1], m.partial, &m.scalars[2], stream));
+        kvx_emit_tiles<<<grid_for(B, 128), 128, 0, stream>>>(m.run_start, m.tile_start, m.scalars, m.pair_src,
+                                                             m.pair_dst, sh, tiles, tile_cap, rows, rows + B,
+                                                             rows + 2 * B, m.err);
+        ok(cudaGetLastError());
+    }
+    int64_t h_scal[3] = {0, 0, 0};
+    int32_t h_err = 0;
+    ok(cudaMemcpyAsync(h_scal, m.scalars, sizeof(h_scal), cudaMemcpyDeviceToHost, stream));
+    ok(cudaMemcpyAsync(&h_err, m.err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
+    ok(cudaStreamSynchronize(stream));
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "kvx_match_prefix"));
+    if (h_err & ~8) return cleanup(fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err));
+    if (h_err & 8)
+        return cleanup(fail(KVX_ENOMEM, "pushing sessions need %lld blocks, free list has %lld", (long long)h_scal[0],
+                            (long long)n_free));
+    if (pl) {
+        const int64_t n_runs = h_scal[1];
+        pl->n_tiles = h_scal[2];
+        pl->run_src_row.resize((size_t)n_runs);
+        pl->run_dst_row.resize((size_t)n_runs);
+        pl->run_ntok.resize((size_t)n_runs);
+        if (n_runs > 0) {
+            ok(cudaMemcpyAsync(pl->run_src_row.data(), rows, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
+            ok(cudaMemcpyAsync(pl->run_dst_row.data(), rows + B, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
+            ok(cudaMemcpyAsync(pl->run_ntok.data(), rows + 2 * B, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
+            ok(cudaStreamSynchronize(stream));
+            if (e != cudaSuccess) return cleanup(cuda_fail(e, "reading plan runs"));
+        }
+        finish_plan_shape(pl);
+        e = cudaEventCreateWithFlags(&pl->upload_evt, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventRecord(pl->upload_evt, stream);
+        if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventRecord(plan)"));
+        pl->upload_stream = stream;
+        pl->uploaded = true;
+        *out_plan = pl;
+        pl = nullptr;
+    }
+    pool_free(scratch);
+    return KVX_OK;
+}
+
+}  // extern "C"

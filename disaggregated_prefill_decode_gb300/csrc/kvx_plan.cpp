@@ -1,0 +1,356 @@
+// Host side of kvx: error reporting, plan validation, run merging and tiling. No CUDA calls.
+//
+// Follows the push-mode NIXL connector article (spke.com 3844), section "Threading-Modell" (block ids
+// are mapped to memory descriptors and contiguous blocks merged into larger regions) and
+// "Implementierungsdetails" step 3 (each side maps block positions to its own layout), and the
+// "vLLM MoRIIO KV Connector" notes, section 6 (transfer triples with adjacent blocks merged; rank
+// mapping when one TP size is a multiple of the other).
+#include "kvx_internal.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <numeric>
+
+namespace kvx {
+
+static thread_local char g_err[512] = "";
+static std::atomic<int64_t> g_launches{0};
+
+kvx_status fail(kvx_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kvx_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(KVX_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+void count_launch(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+static kvx_status read_geom(const kvx_pool *p, const char *side, Geom *g, std::vector<void *> *bases) {
+    if (!p) return fail(KVX_EINVAL, "%s pool is NULL", side);
+    if (p->n_layers < 1 || p->n_planes < 1 || p->n_shards < 1 || p->heads_per_shard < 1 || p->head_dim < 1 ||
+        p->elem_bytes < 1 || p->block_size < 1 || p->n_blocks < 0 || p->reserved != 0)
+        return fail(KVX_EINVAL, "%s pool: counts must be >= 1 (n_blocks >= 0, reserved 0)", side);
+    *g = Geom{p->n_layers, p->n_planes, p->n_shards, p->heads_per_shard, p->head_dim, p->elem_bytes,
+              p->block_size, p->n_blocks};
+    // extents stay well inside int64, rows inside int32, buffers inside the int32 launch grid
+    const double bytes = (double)p->n_blocks * p->block_size * p->heads_per_shard * (double)p->head_dim * p->elem_bytes;
+    if (bytes > 9.0e18) return fail(KVX_EUNSUPPORTED, "%s pool buffer size overflows", side);
+    if ((double)p->n_blocks * p->block_size > (double)std::numeric_limits<int32_t>::max())
+        return fail(KVX_EUNSUPPORTED, "%s pool has more than 2^31-1 rows per buffer", side);
+    if ((double)p->n_layers * p->n_planes * p->n_shards > 1.0e7)
+        return fail(KVX_EUNSUPPORTED, "%s pool has too many buffers", side);
+    if (p->n_layers > 65535 || p->n_planes > 65535)
+        return fail(KVX_EUNSUPPORTED, "%s pool: at most 65535 layers and planes", side);
+    if (!p->base) return fail(KVX_EINVAL, "%s pool base table is NULL", side);
+    const int32_t n = g->n_buffers();
+    bases->assign(p->base, p->base + n);
+    for (int32_t i = 0; i < n; ++i)
+        if (!(*bases)[i] && g->buf_bytes() > 0) return fail(KVX_EINVAL, "%s pool buffer %d is NULL", side, i);
+    return KVX_OK;
+}
+
+// A consumer buffer that overlaps a producer buffer or another consumer buffer makes the copy a race.
+static kvx_status check_overlap(const std::vector<void *> &src, int64_t src_bytes, const std::vector<void *> &dst,
+                                int64_t dst_bytes) {
+    struct Iv { uintptr_t lo, hi; int dst; };
+    std::vector<Iv> iv;
+    iv.reserve(src.size() + dst.size());
+    if (src_bytes > 0)
+        for (void *p : src) iv.push_back({(uintptr_t)p, (uintptr_t)p + (uintptr_t)src_bytes, 0});
+    if (dst_bytes > 0)
+        for (void *p : dst) iv.push_back({(uintptr_t)p, (uintptr_t)p + (uintptr_t)dst_bytes, 1});
+    std::sort(iv.begin(), iv.end(), [](const Iv &a, const Iv &b) { return a.lo < b.lo; });
+    // sweep in address order, remembering the furthest end of consumer and producer intervals seen
+    uintptr_t max_dst_hi = 0, max_src_hi = 0;
+    bool any_dst = false, any_src = false;
+    for (const Iv &v : iv) {
+        if (any_dst && v.lo < max_dst_hi) return fail(KVX_EINVAL, "a consumer buffer overlaps another pool buffer");
+        if (v.dst && any_src && v.lo < max_src_hi) return fail(KVX_EINVAL, "a consumer buffer overlaps a producer buffer");
+        if (v.dst) { max_dst_hi = std::max(max_dst_hi, v.hi); any_dst = true; }
+        else { max_src_hi = std::max(max_src_hi, v.hi); any_src = true; }
+    }
+    return KVX_OK;
+}
+
+// Appends the maximal token runs of one request. Walks the segments between consecutive block
+// boundaries of either side (rows inside a segment advance together), and extends the previous run
+// when both sides continue it.
+static void request_runs(int64_t n_tok, int32_t bs_s, const int32_t *sids, int32_t bs_d, const int32_t *dids,
+                         kvx_plan_s *pl) {
+    const size_t first = pl->run_ntok.size();
+    int64_t t = 0;
+    while (t < n_tok) {
+        const int64_t is = t / bs_s, id = t / bs_d;
+        const int64_t end = std::min({(is + 1) * bs_s, (id + 1) * bs_d, n_tok});
+        const int64_t srow = (int64_t)sids[is] * bs_s + (t - is * bs_s);
+        const int64_t drow = (int64_t)dids[id] * bs_d + (t - id * bs_d);
+        const int32_t len = (int32_t)(end - t);
+        const size_t k = pl->run_ntok.size();
+        if (k > first && (int64_t)pl->run_src_row[k - 1] + pl->run_ntok[k - 1] == srow &&
+            (int64_t)pl->run_dst_row[k - 1] + pl->run_ntok[k - 1] == drow) {
+            pl->run_ntok[k - 1] += len;
+        } else {
+            pl->run_src_row.push_back((int32_t)srow);
+            pl->run_dst_row.push_back((int32_t)drow);
+            pl->run_ntok.push_back(len);
+        }
+        t = end;
+    }
+}
+
+// Head-shard pairs: the contiguous head ranges that one producer shard and one consumer shard share.
+std::vector<Pair> shard_pairs(const Geom &s, const Geom &d) {
+    std::vector<Pair> out;
+    const int64_t hb = s.head_bytes();
+    if (s.heads_per_shard == d.heads_per_shard) {
+        for (int32_t i = 0; i < s.n_shards; ++i) out.push_back({i, i, 0, 0});
+    } else if (s.heads_per_shard < d.heads_per_shard) {   // merge: several producer shards per consumer shard
+        for (int32_t i = 0; i < s.n_shards; ++i) {
+            const int32_t g0 = i * s.heads_per_shard;
+            const int32_t ds = g0 / d.heads_per_shard;
+            out.push_back({i, ds, 0, (int64_t)(g0 - ds * d.heads_per_shard) * hb});
+        }
+    } else {                                              // split: several consumer shards per producer shard
+        for (int32_t j = 0; j < d.n_shards; ++j) {
+            const int32_t g0 = j * d.heads_per_shard;
+            const int32_t ss = g0 / s.heads_per_shard;
+            out.push_back({ss, j, (int64_t)(g0 - ss * s.heads_per_shard) * hb, 0});
+        }
+    }
+    return out;
+}
+
+static int64_t gcd64(int64_t a, int64_t b) { return std::gcd(a < 0 ? -a : a, b < 0 ? -b : b); }
+
+// The widest vector (<= 16 bytes) dividing every address, offset and length the copy uses.
+static int32_t vector_bytes(const kvx_plan_s *pl, const std::vector<Pair> &pairs) {
+    int64_t g = 16;
+    for (void *p : pl->src_base) g = gcd64(g, (int64_t)((uintptr_t)p & 15));
+    for (void *p : pl->dst_base) g = gcd64(g, (int64_t)((uintptr_t)p & 15));
+    g = gcd64(g, pl->src.row_bytes());
+    g = gcd64(g, pl->dst.row_bytes());
+    if (pl->strided) {
+        g = gcd64(g, pl->width);
+        for (const Pair &q : pairs) g = gcd64(gcd64(g, q.src_seg_off), q.dst_seg_off);
+    } else {
+        g = gcd64(g, pl->tile_bytes);
+    }
+    return (int32_t)g;   // gcd with 16: one of 16, 8, 4, 2, 1
+}
+
+static void build_tiles(kvx_plan_s *pl, const std::vector<Pair> &pairs) {
+    pl->tiles.clear();
+    const int64_t rb_s = pl->src.row_bytes(), rb_d = pl->dst.row_bytes();
+    const size_t nr = pl->run_ntok.size();
+    if (!pl->strided) {
+        for (size_t r = 0; r < nr; ++r) {
+            const int64_t bytes = (int64_t)pl->run_ntok[r] * rb_s;
+            const int64_t s0 = (int64_t)pl->run_src_row[r] * rb_s, d0 = (int64_t)pl->run_dst_row[r] * rb_d;
+            for (int64_t o = 0; o < bytes; o += pl->tile_bytes)
+                for (const Pair &q : pairs)
+                    pl->tiles.push_back({s0 + o, d0 + o, (int32_t)std::min<int64_t>(pl->tile_bytes, bytes - o),
+                                         q.s, q.d, 0});
+        }
+    } else {
+        const int64_t rpt = std::max<int64_t>(1, pl->tile_bytes / pl->width);
+        for (size_t r = 0; r < nr; ++r)
+            for (int64_t r0 = 0; r0 < pl->run_ntok[r]; r0 += rpt) {
+                const int32_t rows = (int32_t)std::min<int64_t>(rpt, pl->run_ntok[r] - r0);
+                for (const Pair &q : pairs)
+                    pl->tiles.push_back({((int64_t)pl->run_src_row[r] + r0) * rb_s + q.src_seg_off,
+                                         ((int64_t)pl->run_dst_row[r] + r0) * rb_d + q.dst_seg_off, rows, q.s, q.d, 0});
+            }
+    }
+    pl->n_tiles = (int64_t)pl->tiles.size();
+}
+
+kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl) {
+    kvx_status st = read_geom(src, "producer", &pl->src, &pl->src_base);
+    if (st) return st;
+    st = read_geom(dst, "consumer", &pl->dst, &pl->dst_base);
+    if (st) return st;
+    const Geom &s = pl->src, &d = pl->dst;
+    if (s.n_layers != d.n_layers || s.n_planes != d.n_planes)
+        return fail(KVX_EINVAL, "layer/plane counts differ (%d x %d vs %d x %d)", s.n_layers, s.n_planes,
+                    d.n_layers, d.n_planes);
+    if (s.head_dim != d.head_dim || s.elem_bytes != d.elem_bytes) return fail(KVX_EINVAL, "head_dim / elem_bytes differ");
+    if ((int64_t)s.n_shards * s.heads_per_shard != (int64_t)d.n_shards * d.heads_per_shard)
+        return fail(KVX_EINVAL, "total KV heads differ (%d vs %d)", s.n_shards * s.heads_per_shard,
+                    d.n_shards * d.heads_per_shard);
+    if (std::max(s.n_shards, d.n_shards) % std::min(s.n_shards, d.n_shards) != 0)
+        return fail(KVX_EUNSUPPORTED, "shard counts %d and %d do not divide one another", s.n_shards, d.n_shards);
+    st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
+    if (st) return st;
+    if (opts) {
+        for (int i = 0; i < 6; ++i)
+            if (opts->reserved[i]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+        if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
+        if (opts->threads) pl->threads = opts->threads;
+    }
+    if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
+        return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
+    if (pl->threads < 32 || pl->threads > 1024 || pl->threads % 32)
+        return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
+    pl->strided = (s.heads_per_shard != d.heads_per_shard) ? 1 : 0;
+    pl->width = (int32_t)(std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
+    pl->layer_state.assign(s.n_layers, KVX_LAYER_IDLE);
+    pl->inject.assign(s.n_layers, 0);
+    pl->injected_pending.assign(s.n_layers, 0);
+    return KVX_OK;
+}
+
+void finish_plan_shape(kvx_plan_s *pl) {
+    pl->vec = vector_bytes(pl, shard_pairs(pl->src, pl->dst));
+    int64_t toks = 0;
+    for (int32_t n : pl->run_ntok) toks += n;
+    pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
+}
+
+}  // namespace kvx
+
+using namespace kvx;
+
+extern "C" {
+
+const char *kvx_status_str(kvx_status s) {
+    switch (s) {
+        case KVX_OK: return "KVX_OK";
+        case KVX_EINVAL: return "KVX_EINVAL";
+        case KVX_ERANGE: return "KVX_ERANGE";
+        case KVX_EOVERLAP: return "KVX_EOVERLAP";
+        case KVX_EUNSUPPORTED: return "KVX_EUNSUPPORTED";
+        case KVX_ENOMEM: return "KVX_ENOMEM";
+        case KVX_ECUDA: return "KVX_ECUDA";
+        case KVX_ETIMEDOUT: return "KVX_ETIMEDOUT";
+        case KVX_EFAILED: return "KVX_EFAILED";
+    }
+    return "KVX_UNKNOWN";
+}
+
+const char *kvx_last_error(void) { return g_err; }
+
+const char *kvx_version(void) { return "kvx 0.1 (sm_103a)"; }
+
+int64_t kvx_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kvx_status kvx_plan_ex(const kvx_pool *src, const kvx_pool *dst, const kvx_request *reqs, int32_t n_reqs,
+                       const kvx_plan_opts *opts, kvx_plan_t *out) {
+    if (!out) return fail(KVX_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (n_reqs < 0 || (n_reqs > 0 && !reqs)) return fail(KVX_EINVAL, "bad request array");
+    kvx_plan_s *pl = new (std::nothrow) kvx_plan_s();
+    if (!pl) return fail(KVX_ENOMEM, "host allocation failed");
+    kvx_status st = init_plan_geometry(src, dst, opts, pl);
+    if (st) { delete pl; return st; }
+    const Geom &s = pl->src, &d = pl->dst;
+
+    // requests: counts, id ranges, consumer blocks used once
+    std::vector<uint8_t> used((size_t)d.n_blocks, 0);
+    for (int32_t r = 0; r < n_reqs; ++r) {
+        const kvx_request &q = reqs[r];
+        if (q.n_tokens < 0) { delete pl; return fail(KVX_EINVAL, "request %d: n_tokens < 0", r); }
+        const int64_t ns = ceil_div(q.n_tokens, s.block_size), nd = ceil_div(q.n_tokens, d.block_size);
+        if (q.n_src < ns || q.n_dst < nd) {
+            delete pl;
+            return fail(KVX_ERANGE, "request %d: %lld tokens need %lld producer and %lld consumer ids (got %d, %d)", r,
+                        (long long)q.n_tokens, (long long)ns, (long long)nd, q.n_src, q.n_dst);
+        }
+        if ((ns > 0 && !q.src_block_ids) || (nd > 0 && !q.dst_block_ids)) {
+            delete pl;
+            return fail(KVX_EINVAL, "request %d: id array is NULL", r);
+        }
+        for (int64_t i = 0; i < ns; ++i)
+            if (q.src_block_ids[i] < 0 || q.src_block_ids[i] >= s.n_blocks) {
+                delete pl;
+                return fail(KVX_ERANGE, "request %d: producer block id %d outside [0, %lld)", r, q.src_block_ids[i],
+                            (long long)s.n_blocks);
+            }
+        for (int64_t i = 0; i < nd; ++i) {
+            const int32_t b = q.dst_block_ids[i];
+            if (b < 0 || b >= d.n_blocks) {
+                delete pl;
+                return fail(KVX_ERANGE, "request %d: consumer block id %d outside [0, %lld)", r, b, (long long)d.n_blocks);
+            }
+            if (used[(size_t)b]) {
+                delete pl;
+                return fail(KVX_EOVERLAP, "request %d: consumer block %d is written twice", r, b);
+            }
+            used[(size_t)b] = 1;
+        }
+    }
+    for (int32_t r = 0; r < n_reqs; ++r)
+        request_runs(reqs[r].n_tokens, s.block_size, reqs[r].src_block_ids, d.block_size, reqs[r].dst_block_ids, pl);
+    finish_plan_shape(pl);
+    build_tiles(pl, shard_pairs(pl->src, pl->dst));
+    if (pl->n_tiles > std::numeric_limits<int32_t>::max()) {
+        delete pl;
+        return fail(KVX_EUNSUPPORTED, "plan needs more than 2^31-1 tiles per layer; raise tile_bytes");
+    }
+    *out = pl;
+    return KVX_OK;
+}
+
+kvx_status kvx_plan(const kvx_pool *src, const kvx_pool *dst, const kvx_request *reqs, int32_t n_reqs,
+                    kvx_plan_t *out) {
+    return kvx_plan_ex(src, dst, reqs, n_reqs, nullptr, out);
+}
+
+kvx_status kvx_plan_runs(kvx_plan_t pl, int64_t *n_runs, const int32_t **src_row, const int32_t **dst_row,
+                         const int32_t **n_tokens) {
+    if (!pl || !n_runs) return fail(KVX_EINVAL, "NULL argument");
+    *n_runs = (int64_t)pl->run_ntok.size();
+    if (src_row) *src_row = pl->run_src_row.data();
+    if (dst_row) *dst_row = pl->run_dst_row.data();
+    if (n_tokens) *n_tokens = pl->run_ntok.data();
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
+    if (!pl || !out) return fail(KVX_EINVAL, "NULL argument");
+    out->n_runs = (int64_t)pl->run_ntok.size();
+    out->n_tiles = pl->n_tiles;
+    out->bytes_per_layer = pl->bytes_per_layer;
+    out->vec_bytes = pl->vec;
+    out->strided = pl->strided;
+    out->n_layers = pl->src.n_layers;
+    out->n_planes = pl->src.n_planes;
+    out->width = pl->width;
+    out->tile_bytes = pl->tile_bytes;
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_tiles(kvx_plan_t pl, int64_t *n_tiles, const void **tiles) {
+    if (!pl || !n_tiles || !tiles) return fail(KVX_EINVAL, "NULL argument");
+    *n_tiles = (int64_t)pl->tiles.size();
+    *tiles = pl->tiles.data();
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_layer_states(kvx_plan_t pl, int32_t *out, int32_t n_layers) {
+    if (!pl || !out) return fail(KVX_EINVAL, "NULL argument");
+    if (n_layers != pl->src.n_layers) return fail(KVX_EINVAL, "plan has %d layers", pl->src.n_layers);
+    for (int32_t l = 0; l < n_layers; ++l) out[l] = pl->layer_state[l];
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_inject_failure(kvx_plan_t pl, int32_t layer) {
+    if (!pl) return fail(KVX_EINVAL, "NULL plan");
+    if (layer < 0 || layer >= pl->src.n_layers) return fail(KVX_EINVAL, "layer %d out of range", layer);
+    pl->inject[layer] = 1;
+    return KVX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,329 @@
+"""Thin ctypes binding of the kvx C-ABI (include/kvx.h): same names, argument marshalling only.
+
+Every operation runs in libkvx.so (hand-written CUDA for sm_103a). There is no fallback: importing
+this module raises if the library has not been built (``__graft_entry__.build()`` or
+``python disaggregated_prefill_decode_gb300/build.py``). PyTorch is used by callers only to own device
+memory and streams; this module accepts torch tensors / streams / events or raw integer handles.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvx.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"kvx CUDA library not built: {_LIB_PATH} is missing (run __graft_entry__.build())")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+c_i32, c_i64, c_u64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
+
+KVX_OK, KVX_EINVAL, KVX_ERANGE, KVX_EOVERLAP, KVX_EUNSUPPORTED, KVX_ENOMEM, KVX_ECUDA, KVX_ETIMEDOUT, \
+    KVX_EFAILED = range(9)
+KVX_LAYER_IDLE, KVX_LAYER_PENDING, KVX_LAYER_DONE, KVX_LAYER_FAILED = range(4)
+
+
+class kvx_pool(ctypes.Structure):
+    _fields_ = [("n_layers", c_i32), ("n_planes", c_i32), ("n_shards", c_i32), ("heads_per_shard", c_i32),
+                ("head_dim", c_i32), ("elem_bytes", c_i32), ("block_size", c_i32), ("reserved", c_i32),
+                ("n_blocks", c_i64), ("base", ctypes.POINTER(c_vp))]
+
+
+class kvx_request(ctypes.Structure):
+    _fields_ = [("req_id", c_i64), ("n_tokens", c_i64), ("src_block_ids", ctypes.POINTER(c_i32)), ("n_src", c_i32),
+                ("dst_block_ids", ctypes.POINTER(c_i32)), ("n_dst", c_i32)]
+
+
+class kvx_plan_opts(ctypes.Structure):
+    _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("reserved", c_i32 * 6)]
+
+
+class kvx_plan_info(ctypes.Structure):
+    _fields_ = [("n_runs", c_i64), ("n_tiles", c_i64), ("bytes_per_layer", c_i64), ("vec_bytes", c_i32),
+                ("strided", c_i32), ("n_layers", c_i32), ("n_planes", c_i32), ("width", c_i32),
+                ("tile_bytes", c_i32)]
+
+
+class kvx_match_result(ctypes.Structure):
+    _fields_ = [("local_hit_blocks", c_i32), ("remote_hit_blocks", c_i32), ("missing_tokens", c_i32),
+                ("push", c_i32), ("dst_start", c_i64)]
+
+
+MATCH_RESULT_DTYPE = np.dtype([("local_hit_blocks", "<i4"), ("remote_hit_blocks", "<i4"), ("missing_tokens", "<i4"),
+                               ("push", "<i4"), ("dst_start", "<i8")])
+assert MATCH_RESULT_DTYPE.itemsize == ctypes.sizeof(kvx_match_result)
+
+TILE_DTYPE = np.dtype([("src_off", "<i8"), ("dst_off", "<i8"), ("n", "<i4"), ("src_shard", "<i4"),
+                       ("dst_shard", "<i4"), ("pad", "<i4")])
+
+_P = ctypes.POINTER
+_sig = {
+    "kvx_plan": (c_i32, [_P(kvx_pool), _P(kvx_pool), _P(kvx_request), c_i32, _P(c_vp)]),
+    "kvx_plan_ex": (c_i32, [_P(kvx_pool), _P(kvx_pool), _P(kvx_request), c_i32, _P(kvx_plan_opts), _P(c_vp)]),
+    "kvx_plan_runs": (c_i32, [c_vp, _P(c_i64), _P(_P(c_i32)), _P(_P(c_i32)), _P(_P(c_i32))]),
+    "kvx_plan_get_info": (c_i32, [c_vp, _P(kvx_plan_info)]),
+    "kvx_plan_tiles": (c_i32, [c_vp, _P(c_i64), _P(c_vp)]),
+    "kvx_push_layer": (c_i32, [c_vp, c_i32, c_vp, c_vp]),
+    "kvx_push_layers": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp]),
+    "kvx_sync": (c_i32, [c_vp, c_i64]),
+    "kvx_plan_layer_states": (c_i32, [c_vp, _P(c_i32), c_i32]),
+    "kvx_plan_inject_failure": (c_i32, [c_vp, c_i32]),
+    "kvx_plan_destroy": (c_i32, [c_vp]),
+    "kvx_status_str": (ctypes.c_char_p, [c_i32]),
+    "kvx_last_error": (ctypes.c_char_p, []),
+    "kvx_block_hashes": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "kvx_table_build": (c_i32, [c_vp, c_vp, c_i64, c_vp, _P(c_vp)]),
+    "kvx_table_lookup": (c_i32, [c_vp, c_vp, c_i64, c_vp, c_vp]),
+    "kvx_table_destroy": (c_i32, [c_vp]),
+    "kvx_match_prefix": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
+                                 _P(kvx_pool), _P(kvx_pool), c_vp, _P(c_vp), c_vp]),
+    "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp]),
+    "kvx_version": (ctypes.c_char_p, []),
+    "kvx_launch_count": (c_i64, []),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_sig)
+
+
+class KvxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kvx_status_str(status)}: {kvx_last_error()}")
+
+
+def _check(st: int, where: str) -> int:
+    if st != KVX_OK:
+        raise KvxError(st, where)
+    return st
+
+
+def kvx_status_str(status: int) -> str:
+    return _lib.kvx_status_str(status).decode()
+
+
+def kvx_last_error() -> str:
+    return _lib.kvx_last_error().decode()
+
+
+def kvx_version() -> str:
+    return _lib.kvx_version().decode()
+
+
+def kvx_launch_count() -> int:
+    return int(_lib.kvx_launch_count())
+
+
+# ---------------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------------
+
+def _ptr(x) -> int:
+    """Device pointer of a torch tensor, or an int passed through. None -> 0."""
+    if x is None:
+        return 0
+    if isinstance(x, (int, np.integer)):
+        return int(x)
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _event(e) -> int:
+    if e is None:
+        return 0
+    if isinstance(e, int):
+        return e
+    return int(e.cuda_event)
+
+
+class Pool:
+    """A kvx_pool plus the pointer table it references. `geom` has the kvx_pool count fields;
+    `buffers` lists one device buffer (torch tensor or pointer) per (layer, plane, shard)."""
+
+    def __init__(self, geom, buffers: Sequence):
+        n = geom.n_layers * geom.n_planes * geom.n_shards
+        if len(buffers) != n:
+            raise ValueError(f"pool needs {n} buffers, got {len(buffers)}")
+        self.geom = geom
+        self.buffers = list(buffers)
+        self._ptrs = (c_vp * max(n, 1))(*[_ptr(b) for b in buffers])
+        self.struct = kvx_pool(geom.n_layers, geom.n_planes, geom.n_shards, geom.heads_per_shard, geom.head_dim,
+                               geom.elem_bytes, geom.block_size, 0, geom.n_blocks,
+                               ctypes.cast(self._ptrs, _P(c_vp)))
+
+
+class Plan:
+    """Owns a kvx_plan_t handle; call kvx_plan_destroy (or use `with`) to free it."""
+
+    def __init__(self, handle: int, n_layers: int):
+        self.handle = handle
+        self.n_layers = n_layers
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        kvx_plan_destroy(self)
+
+
+class Table:
+    def __init__(self, handle: int):
+        self.handle = handle
+
+
+def _requests(reqs) -> tuple:
+    """reqs: iterable of (n_tokens, src_ids, dst_ids) or (n_tokens, src_ids, dst_ids, req_id)."""
+    keep, arr = [], []
+    for i, r in enumerate(reqs):
+        n_tok, sids, dids = int(r[0]), np.ascontiguousarray(r[1], np.int32), np.ascontiguousarray(r[2], np.int32)
+        rid = int(r[3]) if len(r) > 3 else i
+        keep += [sids, dids]
+        arr.append(kvx_request(rid, n_tok, sids.ctypes.data_as(_P(c_i32)), len(sids),
+                               dids.ctypes.data_as(_P(c_i32)), len(dids)))
+    n = len(arr)
+    carr = (kvx_request * max(n, 1))(*arr)
+    return carr, n, keep
+
+
+def _h(plan) -> int:
+    return plan.handle if isinstance(plan, Plan) else int(plan)
+
+
+# ---------------------------------------------------------------------------------------------
+# C-ABI calls
+# ---------------------------------------------------------------------------------------------
+
+def kvx_plan(src: Pool, dst: Pool, requests: Iterable) -> Plan:
+    return kvx_plan_ex(src, dst, requests, None)
+
+
+def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] = None) -> Plan:
+    carr, n, _keep = _requests(requests)
+    out = c_vp()
+    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0))) if opts else None
+    st = _lib.kvx_plan_ex(ctypes.byref(src.struct), ctypes.byref(dst.struct), carr, n,
+                          ctypes.byref(o) if o is not None else None, ctypes.byref(out))
+    _check(st, "kvx_plan")
+    return Plan(out.value, src.geom.n_layers)
+
+
+def kvx_plan_runs(plan) -> tuple:
+    n = c_i64()
+    s, d, t = _P(c_i32)(), _P(c_i32)(), _P(c_i32)()
+    _check(_lib.kvx_plan_runs(_h(plan), ctypes.byref(n), ctypes.byref(s), ctypes.byref(d), ctypes.byref(t)),
+           "kvx_plan_runs")
+    k = n.value
+    if k == 0:
+        z = np.zeros(0, np.int32)
+        return z, z.copy(), z.copy()
+    return (np.ctypeslib.as_array(s, (k,)).copy(), np.ctypeslib.as_array(d, (k,)).copy(),
+            np.ctypeslib.as_array(t, (k,)).copy())
+
+
+def kvx_plan_get_info(plan) -> dict:
+    info = kvx_plan_info()
+    _check(_lib.kvx_plan_get_info(_h(plan), ctypes.byref(info)), "kvx_plan_get_info")
+    return {f: getattr(info, f) for f, _ in kvx_plan_info._fields_}
+
+
+def kvx_plan_tiles(plan) -> np.ndarray:
+    """Copy of a host-built plan's tile table (structured array of TILE_DTYPE)."""
+    n = c_i64()
+    p = c_vp()
+    _check(_lib.kvx_plan_tiles(_h(plan), ctypes.byref(n), ctypes.byref(p)), "kvx_plan_tiles")
+    if n.value == 0:
+        return np.zeros(0, TILE_DTYPE)
+    raw = (ctypes.c_uint8 * (32 * n.value)).from_address(p.value)
+    return np.frombuffer(bytes(raw), TILE_DTYPE).copy()
+
+
+def kvx_push_layer(plan, layer: int, stream=None, ready=None) -> None:
+    _check(_lib.kvx_push_layer(_h(plan), layer, _stream(stream), _event(ready)), "kvx_push_layer")
+
+
+def kvx_push_layers(plan, layer_begin: int, layer_end: int, stream=None, ready=None) -> None:
+    _check(_lib.kvx_push_layers(_h(plan), layer_begin, layer_end, _stream(stream), _event(ready)), "kvx_push_layers")
+
+
+def kvx_sync(plan, timeout_us: int = -1) -> int:
+    """Returns KVX_OK, KVX_ETIMEDOUT or KVX_EFAILED; raises on any other status."""
+    st = _lib.kvx_sync(_h(plan), int(timeout_us))
+    if st not in (KVX_OK, KVX_ETIMEDOUT, KVX_EFAILED):
+        raise KvxError(st, "kvx_sync")
+    return st
+
+
+def kvx_plan_layer_states(plan) -> np.ndarray:
+    out = np.zeros(plan.n_layers, np.int32)
+    _check(_lib.kvx_plan_layer_states(_h(plan), out.ctypes.data_as(_P(c_i32)), plan.n_layers), "kvx_plan_layer_states")
+    return out
+
+
+def kvx_plan_inject_failure(plan, layer: int) -> None:
+    _check(_lib.kvx_plan_inject_failure(_h(plan), layer), "kvx_plan_inject_failure")
+
+
+def kvx_plan_destroy(plan) -> None:
+    h = _h(plan)
+    if h:
+        _check(_lib.kvx_plan_destroy(h), "kvx_plan_destroy")
+    if isinstance(plan, Plan):
+        plan.handle = 0
+
+
+def kvx_block_hashes(tokens, tok_off, n_sessions: int, block_size: int, out_hash, hash_off, stream=None) -> None:
+    _check(_lib.kvx_block_hashes(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, _ptr(out_hash), _ptr(hash_off),
+                                 _stream(stream)), "kvx_block_hashes")
+
+
+def kvx_table_build(keys, vals, n: int, stream=None) -> Table:
+    out = c_vp()
+    _check(_lib.kvx_table_build(_ptr(keys), _ptr(vals), n, _stream(stream), ctypes.byref(out)), "kvx_table_build")
+    return Table(out.value)
+
+
+def kvx_table_lookup(table: Table, keys, n: int, out_vals, stream=None) -> None:
+    _check(_lib.kvx_table_lookup(table.handle, _ptr(keys), n, _ptr(out_vals), _stream(stream)), "kvx_table_lookup")
+
+
+def kvx_table_destroy(table: Table) -> None:
+    if table.handle:
+        _check(_lib.kvx_table_destroy(table.handle), "kvx_table_destroy")
+    table.handle = 0
+
+
+def kvx_match_prefix(tokens, tok_off, n_sessions: int, block_size: int, table: Table, remote_hash, remote_blk,
+                     rem_off, recompute_threshold_tokens: int, free_blocks, n_free: int, remote_pool: Optional[Pool],
+                     local_pool: Optional[Pool], out, want_plan: bool = True, stream=None):
+    """Returns (status, Plan or None). Status is KVX_OK or KVX_ENOMEM; other statuses raise."""
+    plan = c_vp()
+    st = _lib.kvx_match_prefix(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, table.handle, _ptr(remote_hash),
+                               _ptr(remote_blk), _ptr(rem_off), recompute_threshold_tokens, _ptr(free_blocks), n_free,
+                               ctypes.byref(remote_pool.struct) if remote_pool else None,
+                               ctypes.byref(local_pool.struct) if local_pool else None, _ptr(out),
+                               ctypes.byref(plan) if want_plan else None, _stream(stream))
+    if st not in (KVX_OK, KVX_ENOMEM):
+        raise KvxError(st, "kvx_match_prefix")
+    n_layers = remote_pool.geom.n_layers if remote_pool else 0
+    return st, (Plan(plan.value, n_layers) if plan.value else None)
+
+
+def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed: int = 0, stream=None) -> None:
+    _check(_lib.kvx_fixture_prefill(ctas, iters, _ptr(buf), n_bytes, seed & (2**64 - 1), _stream(stream)),
+           "kvx_fixture_prefill")
+
+
+def library_path() -> str:
+    return _LIB_PATH

@@ -1,0 +1,295 @@
+/*
+ * kvx -- paged KV-cache push between two pools resident in one GPU's HBM (sm_103a).
+ *
+ * The calls below restate, for a single-GPU C library, the data path of the KV connectors described
+ * in three web pages on disaggregated prefill/decode serving:
+ *   [P1] the push-mode NIXL connector article (spke.com, article 3844);
+ *   [P2] the "vLLM MoRIIO KV Connector" notes (single-node PD disaggregation);
+ *   [P3] the bidirectional KV transfer article (spke.com, article 3845).
+ * Section names are the pages' own.
+ *
+ * Conventions shared by every call:
+ *  - Device memory (pools, token and id arrays given as device pointers) belongs to the caller.
+ *    kvx allocates device memory only for plan descriptors, hash tables and the scratch of
+ *    kvx_match_prefix / kvx_block_hashes, and frees it in kvx_plan_destroy / kvx_table_destroy or
+ *    before the call returns.
+ *  - Host arrays passed in are copied before the call returns; the caller may reuse them.
+ *  - Every call returns a kvx_status. On error a one-line reason is stored in a thread-local
+ *    buffer (kvx_last_error); no call aborts the process or traps on the device.
+ *  - A plan or table is used by one host thread at a time. Different plans are independent.
+ *  - Device work runs on the stream the caller passes (plus a library-owned non-blocking stream
+ *    for small status read-backs).
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvx_status {
+    KVX_OK = 0,
+    KVX_EINVAL = 1,        /* malformed argument: null pointer, bad geometry, overlapping buffers  */
+    KVX_ERANGE = 2,        /* block id outside [0, n_blocks) or too few ids for n_tokens          */
+    KVX_EOVERLAP = 3,      /* a consumer block would be written by two requests (or twice)        */
+    KVX_EUNSUPPORTED = 4,  /* layout pair the library does not map (shard counts do not divide)   */
+    KVX_ENOMEM = 5,        /* device or host allocation failed; free list too short               */
+    KVX_ECUDA = 6,         /* a CUDA runtime call failed (text in kvx_last_error)                 */
+    KVX_ETIMEDOUT = 7,     /* kvx_sync deadline passed with pushes still pending                  */
+    KVX_EFAILED = 8        /* a completed push reported FAILED for at least one layer             */
+} kvx_status;
+
+/* Per-layer state of a plan's pushes, [P2] section 6 ("failure handling": the batch state is judged
+ * over all layers' states DONE / FAILED / PENDING, because a middle layer can fail). */
+typedef enum kvx_layer_state {
+    KVX_LAYER_IDLE = 0,     /* not pushed since the plan was built */
+    KVX_LAYER_PENDING = 1,
+    KVX_LAYER_DONE = 2,
+    KVX_LAYER_FAILED = 3
+} kvx_layer_state;
+
+/*
+ * One side's paged KV pool. [P2] section 3 (the one-time handshake exchanges the KV base address,
+ * block size and per-layer tensor strides a peer needs to address the cache) and section 6
+ * ("memory registration": each layer's KV tensor is registered separately).
+ *
+ * The pool is n_layers * n_planes * n_shards separate device buffers; buffer
+ * base[(layer * n_planes + plane) * n_shards + shard] is a dense row-major array
+ *     [n_blocks][block_size][heads_per_shard][head_dim]  of elem_bytes-byte elements.
+ * planes: 2 for separate K and V, 1 for a single latent (MLA). Shard s holds the global KV heads
+ * [s * heads_per_shard, (s + 1) * heads_per_shard), i.e. the tensor-parallel head partition.
+ * Values are moved as opaque bytes; elem_bytes only sizes them. `base` is a host array of device
+ * pointers, copied by kvx_plan.
+ */
+typedef struct kvx_pool {
+    int32_t n_layers;
+    int32_t n_planes;
+    int32_t n_shards;
+    int32_t heads_per_shard;
+    int32_t head_dim;
+    int32_t elem_bytes;
+    int32_t block_size;     /* tokens per block */
+    int32_t reserved;       /* must be 0 */
+    int64_t n_blocks;
+    void *const *base;
+} kvx_pool;
+
+/*
+ * One request: its first n_tokens tokens are copied. Token t lives in producer block
+ * src_block_ids[t / src.block_size] slot t % src.block_size, and goes to consumer block
+ * dst_block_ids[t / dst.block_size] slot t % dst.block_size ([P1] "Implementierungsdetails",
+ * step 3: each side maps block positions to its own physical layout, so block sizes may differ).
+ * Unused slots of a last, partial consumer block keep their bytes. Host arrays.
+ */
+typedef struct kvx_request {
+    int64_t req_id;
+    int64_t n_tokens;
+    const int32_t *src_block_ids;
+    int32_t n_src;           /* >= ceil(n_tokens / src.block_size); extra ids are ignored */
+    const int32_t *dst_block_ids;
+    int32_t n_dst;           /* >= ceil(n_tokens / dst.block_size); extra ids are ignored */
+} kvx_request;
+
+typedef struct kvx_plan_s *kvx_plan_t;
+
+/* Tuning knobs of a plan; zero fields take the defaults. */
+typedef struct kvx_plan_opts {
+    int32_t tile_bytes;       /* bytes one CTA copies per tile (default 16384; multiple of 16)  */
+    int32_t threads;          /* threads per CTA (default 256; multiple of 32, <= 1024)         */
+    int32_t reserved[6];      /* must be 0 */
+} kvx_plan_opts;
+
+/*
+ * kvx_plan -- build the copy plan of a set of requests.
+ * [P1] "Threading-Modell": the block ids of a request are mapped to memory descriptors and
+ * contiguous blocks are merged into larger transfer regions; [P2] section 6 ("memory registration
+ * and offset calculation"): transfers are (local offset, remote offset, size) triples and adjacent
+ * blocks merge; [P2] section 6 ("rank mapping"): the two sides may use different TP sizes when one
+ * is a multiple of the other.
+ *
+ * Runs are merged within each request at token granularity: a run is a maximal token range whose
+ * producer rows (block * block_size + slot) and consumer rows both advance by one per token. Runs
+ * are then cut into tiles of about tile_bytes for the copy kernel. The plan is layer-invariant:
+ * a push for layer l only changes the buffer bases.
+ *
+ * Validation, all before any CUDA call (so kvx_plan runs without a GPU):
+ *   EINVAL        null pointers, counts < 1, n_layers / n_planes / head_dim / elem_bytes differ,
+ *                 total heads differ, null buffer, a consumer buffer overlaps any other buffer;
+ *   EUNSUPPORTED  neither shard count divides the other; more than 2^31-1 rows in a buffer;
+ *   ERANGE        a needed block id is outside [0, n_blocks), n_src or n_dst too small;
+ *   EOVERLAP      a consumer block appears twice among all requests' needed ids.
+ * No device memory is touched by kvx_plan; descriptors go to the device at the first push.
+ * `opts` may be NULL.
+ */
+kvx_status kvx_plan(const kvx_pool *src, const kvx_pool *dst, const kvx_request *reqs, int32_t n_reqs,
+                    kvx_plan_t *out);
+kvx_status kvx_plan_ex(const kvx_pool *src, const kvx_pool *dst, const kvx_request *reqs, int32_t n_reqs,
+                       const kvx_plan_opts *opts, kvx_plan_t *out);
+
+/* Introspection for tests: the plan's merged token runs (host arrays owned by the plan, valid
+ * until kvx_plan_destroy). Rows are block * block_size + slot on each side. */
+kvx_status kvx_plan_runs(kvx_plan_t plan, int64_t *n_runs, const int32_t **src_row,
+                         const int32_t **dst_row, const int32_t **n_tokens);
+
+/* Plan summary: runs, tiles per (layer, plane), bytes moved per layer (read; the same is written),
+ * the vector width the copy kernel uses (16, 8, 4, 2 or 1 bytes), and whether rows are strided
+ * (head-shard remap: each tile copies `n` rows of `width` bytes, stepping by the producer and
+ * consumer row sizes) or contiguous (each tile copies `n` bytes). */
+typedef struct kvx_plan_info {
+    int64_t n_runs;
+    int64_t n_tiles;             /* per (layer, plane) */
+    int64_t bytes_per_layer;     /* read per layer; the same amount is written */
+    int32_t vec_bytes;
+    int32_t strided;
+    int32_t n_layers;
+    int32_t n_planes;
+    int32_t width;               /* strided plans: bytes per row segment */
+    int32_t tile_bytes;
+} kvx_plan_info;
+kvx_status kvx_plan_get_info(kvx_plan_t plan, kvx_plan_info *out);
+
+/* Introspection for tests: the tile table of a host-built plan (host memory owned by the plan).
+ * Entry layout, 32 bytes: { int64 src_off; int64 dst_off; int32 n; int32 src_shard;
+ * int32 dst_shard; int32 pad }. Offsets are bytes into the (layer, plane, shard) buffers; every
+ * layer and plane uses the same table. Device-built plans report 0 entries here. */
+kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles);
+
+/*
+ * kvx_push_layer -- copy layer `layer` of every request of the plan, on `stream`.
+ * [P2] section 3.2 (WRITE mode): after each layer's forward step the write of that layer is queued
+ * to a worker that first synchronises on a CUDA event, so the copy of layer k starts after layer k's
+ * compute and overlaps layer k+1; [P1] "Threading-Modell": the main loop hands the blocks to a
+ * background thread and returns to model execution at once.
+ *
+ * If `ready` is not NULL the stream first waits for it (cudaStreamWaitEvent). The call only
+ * enqueues: it returns before the copy runs. Until kvx_sync returns KVX_OK the producer layer must
+ * not be rewritten and the consumer layer must not be read. The first push of a plan allocates and
+ * uploads its descriptors on `stream`; pushes on other streams wait for that upload. The current
+ * device must be the device of the pools and the stream.
+ * kvx_push_layers does layers [layer_begin, layer_end) in one launch.
+ */
+kvx_status kvx_push_layer(kvx_plan_t plan, int32_t layer, cudaStream_t stream, cudaEvent_t ready);
+kvx_status kvx_push_layers(kvx_plan_t plan, int32_t layer_begin, int32_t layer_end, cudaStream_t stream,
+                           cudaEvent_t ready);
+
+/*
+ * kvx_sync -- wait for every push issued on the plan since the last completed sync.
+ * [P1] "Implementierungsdetails", step 3: the consumer counts one completion per producer write and
+ * treats the KV as received only when all expected completions arrived; [P2] section 3.2
+ * (wait_for_save seals the number of writes actually queued) and section 6 (per-layer batch state).
+ *
+ * The count is sealed at entry: pushes issued so far. timeout_us < 0 waits without a deadline;
+ * otherwise the host polls until the deadline and returns KVX_ETIMEDOUT with the pushes still
+ * pending (a later kvx_sync waits for them again). When all are complete: KVX_EFAILED if any layer
+ * reported FAILED (kvx_plan_layer_states tells which), else KVX_OK.
+ */
+kvx_status kvx_sync(kvx_plan_t plan, int64_t timeout_us);
+
+/* Per-layer states (out: n_layers entries of kvx_layer_state). */
+kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers);
+
+/* Testing hook for host-side fault injection: the next push of `layer` completes normally on the
+ * device but is reported FAILED by kvx_sync. */
+kvx_status kvx_plan_inject_failure(kvx_plan_t plan, int32_t layer);
+
+/* Waits for any pending push, then frees the plan and its device descriptors. NULL is a no-op. */
+kvx_status kvx_plan_destroy(kvx_plan_t plan);
+
+const char *kvx_status_str(kvx_status status);
+const char *kvx_last_error(void);
+
+/* ------------------------------------------------------------------------------------------------
+ * Bidirectional reuse: block hashes, local prefix table, match and decode->prefill plan.
+ * [P3] "Bidirektionaler KV-Transfer", Figure 1 steps 4-6: prefill checks the remote reusable KV
+ * after applying local cache hits, queues a receive when the reusable tokens reach the threshold,
+ * and the same transfer mechanism moves the blocks decode->prefill; [P3] "KV-Recompute-
+ * Schwellenwert": recompute below kv_recompute_threshold, pull at or above it.
+ * ---------------------------------------------------------------------------------------------- */
+
+/*
+ * kvx_block_hashes -- chained block hashes of sessions' token streams, on `stream` (waits for it).
+ * Session s has tokens[tok_off[s] .. tok_off[s+1]) (uint32 ids, device CSR; tok_off is a device
+ * array of n_sessions + 1 int64). For each full block j (block_size tokens), the hash is 64-bit
+ * FNV-1a (offset basis 14695981039346656037, prime 1099511628211; per octet xor then multiply)
+ * over the parent hash as 8 little-endian octets followed by the block's token ids as 4
+ * little-endian octets each; block 0's parent is 0. A trailing partial block is not hashed.
+ * Output for session s goes to out_hash[hash_off[s] ...] (device; hash_off device, n_sessions + 1
+ * int64, each session needing floor(len / block_size) slots). The pages name prefix caching but
+ * not the hash; this chained FNV-1a is the reading this library fixes.
+ */
+kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                            int32_t block_size, uint64_t *out_hash, const int64_t *hash_off,
+                            cudaStream_t stream);
+
+/* Device hash table of the prefill side's resident blocks: hash -> local block id. */
+typedef struct kvx_table_s *kvx_table_t;
+
+/* Builds a table from n device keys / values on `stream` and waits for it. Duplicate keys ->
+ * KVX_EINVAL (no table). n may be 0. */
+kvx_status kvx_table_build(const uint64_t *keys, const int32_t *vals, int64_t n, cudaStream_t stream,
+                           kvx_table_t *out);
+/* Looks up n device keys; out_vals[i] = value or -1 (device). */
+kvx_status kvx_table_lookup(kvx_table_t table, const uint64_t *keys, int64_t n, int32_t *out_vals,
+                            cudaStream_t stream);
+/* Waits for the table's last lookup, then frees it. */
+kvx_status kvx_table_destroy(kvx_table_t table);
+
+/* Per-session decision of kvx_match_prefix (device array, one entry per session). */
+typedef struct kvx_match_result {
+    int32_t local_hit_blocks;   /* L_loc: longest prefix of blocks resident in the local table     */
+    int32_t remote_hit_blocks;  /* L_rem: longest prefix whose hash equals the published hash      */
+    int32_t missing_tokens;     /* max(0, L_rem - L_loc) * block_size                              */
+    int32_t push;               /* 1 iff missing_tokens > 0 and missing_tokens >= threshold        */
+    int64_t dst_start;          /* offset into free_blocks of the session's first block, or -1     */
+} kvx_match_result;
+
+/*
+ * kvx_match_prefix -- decide, per session, whether to pull the decode-held span, and build the
+ * decode->prefill plan.
+ *
+ * Inputs (device unless stated): tokens/tok_off as in kvx_block_hashes; the local table; the
+ * published remote list per session, remote_hash/remote_blk[rem_off[s] .. rem_off[s+1]) (hash and
+ * decode block id of each of the session's blocks, in order); recompute_threshold_tokens (host);
+ * free_blocks[0 .. n_free) (distinct prefill blocks, handed out in order). Pushing sessions, in
+ * session order, take (L_rem - L_loc) consecutive entries of free_blocks; pair k of session s
+ * copies decode block remote_blk[rem_off[s] + L_loc + k] into prefill block
+ * free_blocks[dst_start + k].
+ *
+ * remote_pool is the producer (decode) pool, local_pool the consumer (prefill) pool; their
+ * block_size must equal block_size. If out_plan is not NULL it receives a plan (built on the
+ * device) whose pushes copy those blocks with kvx_push_layer / kvx_sync; NULL computes the
+ * decisions only (the pools may then be NULL). The call waits for `stream` (it reads back the
+ * totals). Block ids outside a pool make the affected layers FAILED at kvx_sync (the copy kernel
+ * skips them). If the pushing sessions need more than n_free blocks the decisions are still
+ * written, no plan is made, and the call returns KVX_ENOMEM.
+ */
+kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                            int32_t block_size, kvx_table_t local_table, const uint64_t *remote_hash,
+                            const int32_t *remote_blk, const int64_t *rem_off,
+                            int32_t recompute_threshold_tokens, const int32_t *free_blocks, int64_t n_free,
+                            const kvx_pool *remote_pool, const kvx_pool *local_pool, kvx_match_result *out,
+                            kvx_plan_t *out_plan, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Synthetic prefill fixture (tests and benchmark only; not part of the transfer path).
+ * Occupies `ctas` CTAs of 128 threads with a dependent integer chain of `iters` steps per thread,
+ * standing in for a layer's forward compute on the main stream. If `buf` is not NULL, the CTAs
+ * then rewrite buf[0 .. n_bytes) (device, 16-byte aligned, n_bytes a multiple of 16) with a pattern
+ * derived from `seed`, so a push that ran before the fixture finished would copy stale bytes.
+ * ---------------------------------------------------------------------------------------------- */
+kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes, uint64_t seed,
+                               cudaStream_t stream);
+
+/* Library version string and the number of kvx kernels launched by this process so far. */
+const char *kvx_version(void);
+int64_t kvx_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_H */

@@ -88,10 +88,14 @@ def dst_side_map(src_geom, src_bufs, dst_geom, dst_bufs, requests):
 
 def random_requests(rng, src_geom, dst_geom, n_reqs, max_tokens):
     """Random request lengths and random (unique-per-side) block ids."""
-    lens = [int(x) for x in rng.integers(0, max_tokens + 1, n_reqs)]
-    need_s = [ceil_div(n, src_geom.block_size) for n in lens]
-    need_d = [ceil_div(n, dst_geom.block_size) for n in lens]
-    assert sum(need_s) <= src_geom.n_blocks and sum(need_d) <= dst_geom.n_blocks
+    for _ in range(1000):   # redraw until both pools can hold every request
+        lens = [int(x) for x in rng.integers(0, max_tokens + 1, n_reqs)]
+        need_s = [ceil_div(n, src_geom.block_size) for n in lens]
+        need_d = [ceil_div(n, dst_geom.block_size) for n in lens]
+        if sum(need_s) <= src_geom.n_blocks and sum(need_d) <= dst_geom.n_blocks:
+            break
+    else:
+        raise ValueError("pools too small for the requested lengths")
     sp = rng.permutation(src_geom.n_blocks).astype(np.int32)
     dp = rng.permutation(dst_geom.n_blocks).astype(np.int32)
     reqs, ps, pd = [], 0, 0

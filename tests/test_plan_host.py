@@ -1,0 +1,210 @@
+"""Host-side tests of libkvx.so (no GPU): exported symbols, plan validation, merged runs against the
+oracle, and the tile table replayed on the CPU with the copy kernel's semantics against the oracle.
+
+kvx_plan makes no CUDA call, so the pools here carry fake, well-separated device addresses; the
+replay uses numpy host buffers addressed by the tile offsets."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kvx_inputs
+import oracle
+from helpers import host_pool, random_requests
+
+kvx = pytest.importorskip("disaggregated_prefill_decode_gb300.kvx")
+
+PoolGeom = kvx_inputs.PoolGeom
+HEADER = os.path.join(os.path.dirname(os.path.abspath(__file__)), "..", "include", "kvx.h")
+
+
+def fake_pool(geom, base, align=256):
+    stride = -(-geom.buffer_bytes // align) * align + align
+    return kvx.Pool(geom, [base + i * stride for i in range(geom.n_buffers)])
+
+
+def pools(sg, dg):
+    return fake_pool(sg, 1 << 40), fake_pool(dg, 1 << 44)
+
+
+def reqs_of(w):
+    return [(r.n_tokens, r.src_ids, r.dst_ids) for r in w.requests]
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return set(re.findall(r"^\s*(?:kvx_status|const char \*|int64_t)\s*(kvx_\w+)\s*\(", text, re.M))
+
+
+def test_every_declared_symbol_is_exported():
+    declared = declared_functions()
+    assert {"kvx_plan", "kvx_push_layer", "kvx_sync", "kvx_match_prefix"} <= declared
+    for name in sorted(declared):
+        assert hasattr(kvx._lib, name), name
+        assert name in kvx.EXPORTED, name
+
+
+def test_status_strings_and_version():
+    assert kvx.kvx_status_str(kvx.KVX_OK) == "KVX_OK"
+    assert kvx.kvx_status_str(kvx.KVX_ETIMEDOUT) == "KVX_ETIMEDOUT"
+    assert "sm_103a" in kvx.kvx_version()
+
+
+def test_runs_match_oracle_on_workloads():
+    orc = oracle.load()
+    for make in (kvx_inputs.tiny, lambda: kvx_inputs.qwen3_32b_single(n_layers=1),
+                 lambda: kvx_inputs.qwen3_32b_batched(n_layers=1),
+                 lambda: kvx_inputs.tp4_to_tp1_remap(n_layers=1)):
+        w = make()
+        sp, dp = pools(w.src, w.dst)
+        plan = kvx.kvx_plan(sp, dp, reqs_of(w))
+        rs, rd, rl = kvx.kvx_plan_runs(plan)
+        want = [orc.token_runs(r.n_tokens, w.src.block_size, r.src_ids, w.dst.block_size, r.dst_ids)
+                for r in w.requests]
+        assert np.array_equal(rs, np.concatenate([x[0] for x in want]))
+        assert np.array_equal(rd, np.concatenate([x[1] for x in want]))
+        assert np.array_equal(rl, np.concatenate([x[2] for x in want]))
+        info = kvx.kvx_plan_get_info(plan)
+        heads = w.src.n_shards * w.src.heads_per_shard
+        assert info["bytes_per_layer"] == sum(r.n_tokens for r in w.requests) * heads * w.src.head_dim * \
+            w.src.elem_bytes * w.src.n_planes
+        assert info["strided"] == (w.name == "tp4_to_tp1_remap")
+        kvx.kvx_plan_destroy(plan)
+
+
+def replay_tiles(plan, sg, src, dg, dst):
+    """The copy kernel's semantics on the CPU: each tile, for each (layer, plane)."""
+    info = kvx.kvx_plan_get_info(plan)
+    tiles = kvx.kvx_plan_tiles(plan)
+    assert len(tiles) == info["n_tiles"]
+    out = [b.copy() for b in dst]
+    for l in range(sg.n_layers):
+        for p in range(sg.n_planes):
+            for t in tiles:
+                sb = src[(l * sg.n_planes + p) * sg.n_shards + t["src_shard"]]
+                db = out[(l * dg.n_planes + p) * dg.n_shards + t["dst_shard"]]
+                so, do, n = int(t["src_off"]), int(t["dst_off"]), int(t["n"])
+                if not info["strided"]:
+                    assert n <= info["tile_bytes"] and n % info["vec_bytes"] == 0
+                    db[do:do + n] = sb[so:so + n]
+                else:
+                    w = info["width"]
+                    for r in range(n):
+                        db[do + r * dg.row_bytes:do + r * dg.row_bytes + w] = \
+                            sb[so + r * sg.row_bytes:so + r * sg.row_bytes + w]
+    return out
+
+
+CASES = {
+    "equal": (PoolGeom(2, 2, 1, 2, 4, 2, 4, 12), PoolGeom(2, 2, 1, 2, 4, 2, 4, 12)),
+    "merge4to1_bs4to8": (PoolGeom(1, 2, 4, 1, 8, 2, 4, 10), PoolGeom(1, 2, 1, 4, 8, 2, 8, 6)),
+    "split1to2_bs8to2": (PoolGeom(1, 1, 1, 4, 8, 2, 8, 5), PoolGeom(1, 1, 2, 2, 8, 2, 2, 20)),
+    "merge2to1_equal_bs": (PoolGeom(1, 2, 2, 2, 16, 2, 4, 9), PoolGeom(1, 2, 1, 4, 16, 2, 4, 9)),
+    "bs1": (PoolGeom(1, 2, 1, 2, 8, 1, 1, 24), PoolGeom(1, 2, 1, 2, 8, 1, 1, 24)),
+    "odd_head_bytes": (PoolGeom(1, 1, 2, 1, 3, 1, 3, 9), PoolGeom(1, 1, 1, 2, 3, 1, 5, 7)),
+    "mla576": (PoolGeom(2, 1, 1, 1, 576, 1, 4, 8), PoolGeom(2, 1, 1, 1, 576, 1, 4, 8)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("tile_bytes", [16, 48, 1024, 16384])
+def test_tile_replay_equals_oracle(name, tile_bytes):
+    sg, dg = CASES[name]
+    rng = np.random.default_rng(len(name) * 7 + tile_bytes)
+    max_tok = min(sg.n_blocks * sg.block_size, dg.n_blocks * dg.block_size) // 3
+    reqs = random_requests(rng, sg, dg, 3, max_tok)
+    sp, dp = pools(sg, dg)
+    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"tile_bytes": tile_bytes})
+    src = host_pool(sg, 5)
+    dst = host_pool(dg, 0, fill=0x3C)
+    got = replay_tiles(plan, sg, src, dg, dst)
+    oracle.load().push(sg, src, dg, dst, reqs)
+    for a, b in zip(got, dst):
+        assert np.array_equal(a, b)
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_tile_replay_tiny_workload():
+    w = kvx_inputs.tiny()
+    sp, dp = pools(w.src, w.dst)
+    plan = kvx.kvx_plan(sp, dp, reqs_of(w))
+    src = host_pool(w.src, 1)
+    dst = host_pool(w.dst, 0, fill=0xAD)
+    got = replay_tiles(plan, w.src, src, w.dst, dst)
+    oracle.load().push(w.src, src, w.dst, dst, reqs_of(w))
+    assert all(np.array_equal(a, b) for a, b in zip(got, dst))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_vector_width_follows_alignment():
+    g = PoolGeom(1, 1, 1, 2, 64, 2, 16, 8)
+    sp, dp = pools(g, g)
+    pl = kvx.kvx_plan(sp, dp, [(20, [0, 1], [2, 3])])
+    assert kvx.kvx_plan_get_info(pl)["vec_bytes"] == 16
+    kvx.kvx_plan_destroy(pl)
+    sp8 = kvx.Pool(g, [(1 << 40) + 8])
+    pl = kvx.kvx_plan(sp8, dp, [(20, [0, 1], [2, 3])])
+    assert kvx.kvx_plan_get_info(pl)["vec_bytes"] == 8
+    kvx.kvx_plan_destroy(pl)
+    g3 = PoolGeom(1, 1, 1, 1, 3, 1, 4, 8)
+    sp, dp = pools(g3, g3)
+    pl = kvx.kvx_plan(sp, dp, [(5, [0, 1], [2, 3])])
+    assert kvx.kvx_plan_get_info(pl)["vec_bytes"] == 1
+    kvx.kvx_plan_destroy(pl)
+
+
+def test_empty_plans():
+    g = PoolGeom(2, 2, 1, 2, 64, 2, 16, 8)
+    sp, dp = pools(g, g)
+    for reqs in ([], [(0, [], [])], [(0, [5], [6])]):
+        pl = kvx.kvx_plan(sp, dp, reqs)
+        info = kvx.kvx_plan_get_info(pl)
+        assert info["n_runs"] == 0 and info["n_tiles"] == 0 and info["bytes_per_layer"] == 0
+        assert kvx.kvx_sync(pl, 0) == kvx.KVX_OK                # nothing pushed: no device call
+        assert kvx.kvx_plan_layer_states(pl).tolist() == [kvx.KVX_LAYER_IDLE] * 2
+        kvx.kvx_plan_destroy(pl)
+
+
+def expect(status, fn):
+    with pytest.raises(kvx.KvxError) as ei:
+        fn()
+    assert ei.value.status == status, str(ei.value)
+    assert kvx.kvx_last_error()
+
+
+def test_validation_errors():
+    g = PoolGeom(2, 2, 1, 2, 64, 2, 16, 8)
+    sp, dp = pools(g, g)
+    ok = (20, np.array([0, 1]), np.array([2, 3]))
+    expect(kvx.KVX_ERANGE, lambda: kvx.kvx_plan(sp, dp, [(20, [0, 8], [2, 3])]))       # id == n_blocks
+    expect(kvx.KVX_ERANGE, lambda: kvx.kvx_plan(sp, dp, [(20, [0, 1], [-1, 3])]))      # negative id
+    expect(kvx.KVX_ERANGE, lambda: kvx.kvx_plan(sp, dp, [(40, [0, 1], [2, 3])]))       # too few ids
+    expect(kvx.KVX_EOVERLAP, lambda: kvx.kvx_plan(sp, dp, [ok, (5, [4], [3])]))        # dst shared
+    expect(kvx.KVX_EOVERLAP, lambda: kvx.kvx_plan(sp, dp, [(20, [0, 1], [5, 5])]))     # dst twice
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, dp, [(-1, [], [])]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, sp, [ok]))                         # same memory
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, kvx.Pool(g, dp.buffers[:3] + [dp.buffers[0]]), [ok]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, fake_pool(g.replace(n_layers=3), 1 << 44), [ok]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, fake_pool(g.replace(heads_per_shard=3), 1 << 44), [ok]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(sp, fake_pool(g.replace(head_dim=32, heads_per_shard=4), 1 << 44),
+                                                [ok]))
+    g6a, g6b = PoolGeom(1, 1, 3, 2, 8, 2, 4, 8), PoolGeom(1, 1, 2, 3, 8, 2, 4, 8)
+    expect(kvx.KVX_EUNSUPPORTED, lambda: kvx.kvx_plan(fake_pool(g6a, 1 << 40), fake_pool(g6b, 1 << 44), [ok]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(fake_pool(g.replace(block_size=0), 1 << 40), dp, [ok]))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"tile_bytes": 24}))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"threads": 48}))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(kvx.Pool(g, [0] * g.n_buffers), dp, [ok]))
+    pl = kvx.kvx_plan(sp, dp, [ok])
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_inject_failure(pl, 2))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_push_layer(pl, 2))                # layer out of range, before CUDA
+    kvx.kvx_plan_destroy(pl)
+
+
+def test_requests_keep_extra_ids_unused():
+    """ids past ceil(n_tokens / block_size) are ignored, so they may repeat."""
+    g = PoolGeom(1, 1, 1, 1, 8, 2, 4, 8)
+    sp, dp = pools(g, g)
+    pl = kvx.kvx_plan(sp, dp, [(4, [0, 0, 0], [1, 1, 1]), (3, [2], [2])])
+    assert kvx.kvx_plan_get_info(pl)["n_runs"] == 2
+    kvx.kvx_plan_destroy(pl)
