@@ -1,0 +1,510 @@
+"""Benchmark of the kvx layer push (and the prefix match) on one GB300, or N independent replicas.
+
+Default workload: the Qwen3-32B-shaped single-request push (64 layers x {K,V}, 8 KV heads x 128 bf16,
+block 16, one 8192-token prompt = 512 blocks, pools of 615 blocks, destination ids chunked). One step
+is the whole hot path once: build the plan on the host, then for each layer run the synthetic prefill
+fixture on the main stream, record its event, push that layer on a high-priority side stream gated
+on the event, and finally kvx_sync. Inputs move 4.3 GB per step (larger than the 129 MB L2), so no
+flush is needed between steps.
+
+Printed: one JSON line (rank 0). value = read+write bytes of all pushes / device time of the timed
+steps (CUDA events on the main stream around all steps), summed over ranks / max over ranks.
+roofline.achieved = the same bytes per push launch / the mean push duration (CUDA events on the side
+stream around each launch). e2e = the same metric with the producer KV starting in pinned host memory
+and the consumer KV read back each step (per-layer copies overlapped with the pushes).
+--impl reference times the CPU oracle instead (rank 0 only), on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import kvx_inputs  # noqa: E402
+
+METRIC = "KV push GB/s (read+write) and % of GB300 HBM roofline; blocks/s; prefix-match ops/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="kvx", choices=["kvx", "reference"])
+    p.add_argument("--workload", default="qwen3_32b_single", choices=sorted(kvx_inputs.PUSH_WORKLOADS))
+    p.add_argument("--tile-bytes", type=int, default=0)
+    p.add_argument("--threads", type=int, default=0)
+    p.add_argument("--fixture-ctas", type=int, default=8)
+    p.add_argument("--fixture-iters", type=int, default=2000)
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-match", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes of the push kernel from a committed ncu summary, if the kernel source is
+    unchanged since the capture (else None)."""
+    src = os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", "kvx_push.cu")
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kvx_push_sha") != sha:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def requests(w):
+    return [(r.n_tokens, r.src_ids, r.dst_ids) for r in w.requests]
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.proc = None
+        self.uuid = device_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# kvx arm
+# ---------------------------------------------------------------------------------------------
+
+def alloc_pool(torch, geom, fill, seed, device):
+    per = -(-geom.buffer_bytes // 512) * 512
+    big = torch.empty(per * geom.n_buffers, dtype=torch.uint8, device=device)
+    if fill == "src":
+        kvx_inputs.fill_bf16_normal(big, seed) if geom.elem_bytes == 2 else kvx_inputs.fill_fp8_bytes(big, seed)
+    else:
+        kvx_inputs.fill_canary(big, "bf16_normal" if geom.elem_bytes == 2 else "fp8_bytes")
+    return [big[i * per:i * per + geom.buffer_bytes] for i in range(geom.n_buffers)], big
+
+
+def run_kvx(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+    from disaggregated_prefill_decode_gb300 import kvx
+
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    w = kvx_inputs.PUSH_WORKLOADS[args.workload]()
+    L = w.src.n_layers
+    src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
+    dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
+    sp, dp = kvx.Pool(w.src, src), kvx.Pool(w.dst, dst)
+    reqs = requests(w)
+    opts = {"tile_bytes": args.tile_bytes, "threads": args.threads}
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(priority=-1)
+
+    probe = kvx.kvx_plan_ex(sp, dp, reqs, opts)
+    info = kvx.kvx_plan_get_info(probe)
+    kvx.kvx_plan_destroy(probe)
+    bytes_step = 2 * info["bytes_per_layer"] * L                       # read + write
+    blocks_step = sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L
+
+    K, W = args.steps, args.warmup
+    ready = [torch.cuda.Event() for _ in range(L)]
+    t_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K * L)]
+
+    def step(timed_idx):
+        plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
+        for layer in range(L):
+            kvx.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, stream=main)
+            ready[layer].record(main)
+            if timed_idx is not None:
+                side.wait_event(ready[layer])
+                t_ev[timed_idx * L + layer][0].record(side)
+            kvx.kvx_push_layer(plan, layer, side, ready[layer])
+            if timed_idx is not None:
+                t_ev[timed_idx * L + layer][1].record(side)
+        st = kvx.kvx_sync(plan, -1)
+        kvx.kvx_plan_destroy(plan)
+        if st != kvx.KVX_OK:
+            raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
+
+    for _ in range(W):
+        step(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = kvx.kvx_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t0.record(main)
+    for k in range(K):
+        step(k)
+    main.wait_stream(side)
+    t1.record(main)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = kvx.kvx_launch_count() - launches0
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    push_ms = [a.elapsed_time(b) for a, b in t_ev]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        n = torch.tensor([launches], dtype=torch.int64, device=device)
+        dist.all_reduce(n)
+        launches = int(n.item())
+        dist.barrier()
+
+    mean_push_ms = statistics.fmean(push_ms)
+    peak, peak_kind = measured_peak()
+    achieved = 2 * info["bytes_per_layer"] / (mean_push_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(world * bytes_step * K / (elapsed_ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(elapsed_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8",
+        "data": "synthetic: seeded bf16 N(0,1) producer KV, consumer canary 0xDEAD, seeded chunked block ids",
+        "config": {
+            "workload": args.workload,
+            "layers": L, "planes": w.src.n_planes,
+            "producer": f"{w.src.n_shards} x [{w.src.n_blocks}][{w.src.block_size}][{w.src.heads_per_shard}][{w.src.head_dim}] x {w.src.elem_bytes} B",
+            "consumer": f"{w.dst.n_shards} x [{w.dst.n_blocks}][{w.dst.block_size}][{w.dst.heads_per_shard}][{w.dst.head_dim}] x {w.dst.elem_bytes} B",
+            "requests": len(reqs), "tokens": int(sum(n for n, _, _ in reqs)),
+            "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
+            "vec_bytes": info["vec_bytes"],
+            "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
+            "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on main stream, "
+                      "event, kvx_push_layer on a priority side stream; plan built and synced every step",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "blocks_per_s": round(world * blocks_step * K / (elapsed_ms * 1e-3), 1),
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "kernel": "kvx_copy_tiles (one launch per layer)",
+            "bytes_per_launch": 2 * info["bytes_per_layer"], "mean_launch_us": round(mean_push_ms * 1e3, 3),
+            "traffic": ncu_traffic(args.workload),
+        },
+        "gpu_launches": launches,
+        "clocks": clk,
+        "host_wall_s": round(wall, 4),
+    }
+    if rank == 0:
+        result["memcpy_ceiling"] = memcpy_ceiling(torch, device)
+        if not args.no_e2e:
+            result["e2e"] = run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world)
+        if not args.no_match:
+            result["match"] = run_match(torch, kvx, device)
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def memcpy_ceiling(torch, device):
+    """cudaMemcpyAsync-class device-to-device copy of 2 GiB (torch copy_), read+write GB/s."""
+    n = 1 << 31
+    a = torch.empty(n, dtype=torch.uint8, device=device)
+    b = torch.empty(n, dtype=torch.uint8, device=device)
+    a.fill_(1)
+    for _ in range(3):
+        b.copy_(a)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(10):
+        s.record()
+        b.copy_(a)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    del a, b
+    return {"value": round(2 * n / (best * 1e-3) / 1e9, 1), "unit": "GB/s", "how": "torch copy_ of 2 GiB, best of 10"}
+
+
+def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world):
+    """Producer KV from pinned host memory, per layer: H2D copy, push, D2H of the consumer layer, on
+    three streams so the copies overlap the pushes; plan built and synced each step."""
+    L, P = w.src.n_layers, w.src.n_planes * w.src.n_shards
+    bb_s = w.src.block_size * w.src.row_bytes
+    bb_d = w.dst.block_size * w.dst.row_bytes
+    s_lo = min(int(r[1][:-(-r[0] // w.src.block_size)].min()) for r in reqs if r[0] > 0)
+    s_hi = max(int(r[1][:-(-r[0] // w.src.block_size)].max()) for r in reqs if r[0] > 0) + 1
+    d_lo = min(int(r[2][:-(-r[0] // w.dst.block_size)].min()) for r in reqs if r[0] > 0)
+    d_hi = max(int(r[2][:-(-r[0] // w.dst.block_size)].max()) for r in reqs if r[0] > 0) + 1
+    s_rng, d_rng = (s_lo * bb_s, s_hi * bb_s), (d_lo * bb_d, d_hi * bb_d)
+    host_src = [torch.empty(s_rng[1] - s_rng[0], dtype=torch.uint8, pin_memory=True) for _ in range(len(src))]
+    host_dst = [torch.empty(d_rng[1] - d_rng[0], dtype=torch.uint8, pin_memory=True) for _ in range(len(dst))]
+    for h, d in zip(host_src, src):
+        h.copy_(d[s_rng[0]:s_rng[1]])
+    h2d, side, d2h = torch.cuda.Stream(), torch.cuda.Stream(priority=-1), torch.cuda.Stream()
+    ev_h = [torch.cuda.Event() for _ in range(L)]
+    ev_p = [torch.cuda.Event() for _ in range(L)]
+    nd = w.dst.n_planes * w.dst.n_shards
+
+    def step():
+        plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
+        for layer in range(L):
+            with torch.cuda.stream(h2d):
+                for i in range(layer * P, (layer + 1) * P):
+                    src[i][s_rng[0]:s_rng[1]].copy_(host_src[i], non_blocking=True)
+                ev_h[layer].record(h2d)
+            kvx.kvx_push_layer(plan, layer, side, ev_h[layer])
+            ev_p[layer].record(side)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_p[layer])
+                for i in range(layer * nd, (layer + 1) * nd):
+                    host_dst[i].copy_(dst[i][d_rng[0]:d_rng[1]], non_blocking=True)
+        st = kvx.kvx_sync(plan, -1)
+        d2h.synchronize()
+        kvx.kvx_plan_destroy(plan)
+        assert st == kvx.KVX_OK
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t) / args.e2e_steps
+    return {"value": round(bytes_step / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(h.numel() for h in host_src),
+            "d2h_bytes_per_step": sum(h.numel() for h in host_dst),
+            "ms_per_step": round(dt * 1e3, 3), "steps": args.e2e_steps,
+            "how": "pinned host producer KV -> H2D per layer -> kvx_push_layer -> D2H consumer layer, 3 streams, "
+                   "host wall clock with device sync on both sides (rank 0)"}
+
+
+def run_match(torch, kvx, device):
+    """Prefix match of the bidirectional workload (256 sessions, 1024 shared + U[2k,32k] history tokens,
+    block 64): decode publishes block hashes (kvx_block_hashes), prefill keeps a Bernoulli(0.4) subset
+    in its table, kvx_match_prefix decides per session and builds the decode->prefill plan, which is
+    then pushed for one layer of the fp8 576-byte latent pool."""
+    w = kvx_inputs.bidir_mla_fp8(n_layers=1)
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        view = {np.uint32: np.int32, np.uint64: np.int64}.get(a.dtype.type, a.dtype.type)
+        return torch.from_numpy(a.view(view)).to(device)
+
+    tokens, tok_off, rem_off = d(w.tokens), d(w.tok_off), d(w.rem_off)
+    n_pub = int(w.rem_off[-1])
+    hashes = torch.empty(n_pub, dtype=torch.int64, device=device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hash_ms = []
+    for _ in range(5):
+        s.record()
+        kvx.kvx_block_hashes(tokens, tok_off, w.n_sessions, 64, hashes, rem_off)
+        e.record()
+        e.synchronize()
+        hash_ms.append(s.elapsed_time(e))
+    resident = torch.from_numpy(w.resident).to(device)
+    keys = torch.unique(hashes[resident])
+    table = kvx.kvx_table_build(keys, torch.arange(keys.numel(), dtype=torch.int32, device=device), keys.numel())
+    out = torch.empty(w.n_sessions * 24, dtype=torch.uint8, device=device)
+    rblk, free = d(w.remote_blk), d(w.free_blocks)
+    src, _ = alloc_pool(torch, w.decode, "src", w.seed, device)
+    dst, _ = alloc_pool(torch, w.prefill, "dst", 0, device)
+    sp, dp = kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst)
+
+    def match(with_plan):
+        return kvx.kvx_match_prefix(tokens, tok_off, w.n_sessions, 64, table, hashes, rblk, rem_off, w.threshold,
+                                    free, len(w.free_blocks), sp, dp, out, want_plan=with_plan)
+
+    match_ms, plan_ms = [], []
+    for i in range(6):
+        t = time.perf_counter()
+        _, plan = match(False)
+        match_ms.append((time.perf_counter() - t) * 1e3)
+        t = time.perf_counter()
+        _, plan = match(True)
+        plan_ms.append((time.perf_counter() - t) * 1e3)
+        if i < 5:
+            kvx.kvx_plan_destroy(plan)
+    res = out.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
+    info = kvx.kvx_plan_get_info(plan)
+    side = torch.cuda.Stream(priority=-1)
+    kvx.kvx_push_layer(plan, 0, side)
+    kvx.kvx_sync(plan, -1)
+    push_ms = []
+    for _ in range(5):
+        s.record(side)
+        kvx.kvx_push_layer(plan, 0, side)
+        e.record(side)
+        kvx.kvx_sync(plan, -1)
+        push_ms.append(s.elapsed_time(e))
+    kvx.kvx_plan_destroy(plan)
+    kvx.kvx_table_destroy(table)
+    compares = int(res["remote_hit_blocks"].sum())
+    m_ms = statistics.median(match_ms[1:])
+    return {
+        "workload": "bidir_mla_fp8: 256 sessions, block 64, threshold 512, fp8 latent 576 B, 1 of 48 layers pushed",
+        "sessions_per_s": round(w.n_sessions / (m_ms * 1e-3), 1),
+        "block_compares_per_s": round(compares / (m_ms * 1e-3), 1),
+        "match_ms": round(m_ms, 3), "match_and_plan_ms": round(statistics.median(plan_ms[1:]), 3),
+        "hash_only_ms": round(statistics.median(hash_ms[1:]), 3),
+        "hashed_blocks": n_pub, "pushing_sessions": int(res["push"].sum()),
+        "push_blocks": int(res["missing_tokens"].sum() // 64), "runs": info["n_runs"],
+        "dp_push_gbs_one_layer": round(2 * info["bytes_per_layer"] / (statistics.median(push_ms) * 1e-3) / 1e9, 1),
+        "how": "host wall clock per kvx_match_prefix call (it waits for its stream); hashes and push with CUDA events",
+    }
+
+
+# ---------------------------------------------------------------------------------------------
+# oracle (CPU) timing: the cpu_baseline leg and the reference arm
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample(w, n_layers):
+    """Host pools for `n_layers` layers of the workload (random bytes: the oracle copies opaque bytes)."""
+    sg, dg = w.src.replace(n_layers=n_layers), w.dst.replace(n_layers=n_layers)
+    rng = np.random.default_rng(w.seed)
+    src = [rng.integers(0, 256, sg.buffer_bytes, dtype=np.uint8) for _ in range(sg.n_buffers)]
+    dst = [np.full(dg.buffer_bytes, 0xAD, np.uint8) for _ in range(dg.n_buffers)]
+    return sg, src, dg, dst
+
+
+def cpu_baseline(w, seconds, n_layers=4):
+    import oracle
+    orc = oracle.load()
+    sg, src, dg, dst = oracle_sample(w, n_layers)
+    reqs = requests(w)
+    per_layer = 2 * sum(n for n, _, _ in reqs) * sg.n_shards * sg.row_bytes * sg.n_planes
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.push(sg, src, dg, dst, reqs)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(per_layer * n_layers * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} oracle pushes of {n_layers} of {w.src.n_layers} layers of {w.name} "
+                      f"(host pools, single thread), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.load()
+    w = kvx_inputs.PUSH_WORKLOADS[args.workload]()
+    n_layers = 2
+    sg, src, dg, dst = oracle_sample(w, n_layers)
+    reqs = requests(w)
+    bytes_step = 2 * sum(n for n, _, _ in reqs) * sg.n_shards * sg.row_bytes * sg.n_planes * n_layers
+    for _ in range(args.warmup):
+        orc.push(sg, src, dg, dst, reqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.push(sg, src, dg, dst, reqs)
+    dt = time.perf_counter() - t0
+    v = round(bytes_step * args.steps / dt / 1e9, 3)
+    sample = f"each step: oracle push of {n_layers} of {w.src.n_layers} layers of {w.name} on host pools, 1 thread"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic: seeded random bytes, same block ids as the kvx arm",
+            "config": {"workload": args.workload, "layers_per_step": n_layers},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_kvx(args, rank, local_rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

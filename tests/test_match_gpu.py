@@ -1,0 +1,276 @@
+"""GPU parity of the bidirectional reuse path through the C-ABI: block hashes, the resident table, the
+per-session match decision, the device-built decode->prefill plan and its push, all against the
+oracle (integer work: bit-exact)."""
+import numpy as np
+import pytest
+
+import kvx_inputs
+import oracle
+from gpu_helpers import canary_host, check_layers, device_pool
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+kvx = pytest.importorskip("disaggregated_prefill_decode_gb300.kvx")
+
+PoolGeom = kvx_inputs.PoolGeom
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    yield
+    torch.cuda.synchronize()
+
+
+def dev(a, dtype):
+    """numpy -> device tensor with the same bits (uint32 / uint64 travel as int32 / int64)."""
+    a = np.ascontiguousarray(a)
+    view = {np.uint32: np.int32, np.uint64: np.int64}.get(a.dtype.type, a.dtype.type)
+    if len(a) == 0:
+        a = np.zeros(1, a.dtype)
+    return torch.from_numpy(a.view(view)).to("cuda")
+
+
+def results(out_t, n):
+    return out_t.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)[:n]
+
+
+# ---------------------------------------------------------------------------------------------
+# hashes and table
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bs", [64, 4, 1])
+def test_block_hashes_match_oracle(bs):
+    rng = np.random.default_rng(bs)
+    lens = [0, 1, bs - 1, bs, 5 * bs + 3, 700, 2 * bs]
+    toks = [rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32) for n in lens]
+    tok_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    nh = [n // bs for n in lens]
+    hash_off = np.concatenate([[0], np.cumsum(nh)]).astype(np.int64)
+    out = torch.zeros(max(int(hash_off[-1]), 1), dtype=torch.int64, device="cuda")
+    kvx.kvx_block_hashes(dev(np.concatenate(toks), np.uint32), dev(tok_off, np.int64), len(lens), bs, out,
+                         dev(hash_off, np.int64))
+    got = out.cpu().numpy().view(np.uint64)
+    orc = oracle.load()
+    for s, t in enumerate(toks):
+        assert np.array_equal(got[hash_off[s]:hash_off[s + 1]], orc.block_hashes(t, bs)), s
+
+
+def test_block_hashes_reject_short_output_range():
+    tok_off = dev(np.array([0, 128], np.int64), np.int64)
+    hash_off = dev(np.array([0, 1], np.int64), np.int64)       # 2 full blocks, room for 1
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    with pytest.raises(kvx.KvxError) as ei:
+        kvx.kvx_block_hashes(dev(np.zeros(128, np.uint32), np.uint32), tok_off, 1, 64, out, hash_off)
+    assert ei.value.status == kvx.KVX_ERANGE
+
+
+def test_table_build_and_lookup():
+    rng = np.random.default_rng(5)
+    keys = np.unique(rng.integers(1, 2**63, 5000, dtype=np.int64).astype(np.uint64))
+    keys = np.concatenate([keys, np.array([0], np.uint64)])      # key 0 is a legal hash
+    vals = rng.integers(0, 10**6, len(keys)).astype(np.int32)
+    table = kvx.kvx_table_build(dev(keys, np.uint64), dev(vals, np.int32), len(keys))
+    probe = np.concatenate([keys, rng.integers(1, 2**63, 3000, dtype=np.int64).astype(np.uint64)])
+    out = torch.empty(len(probe), dtype=torch.int32, device="cuda")
+    kvx.kvx_table_lookup(table, dev(probe, np.uint64), len(probe), out)
+    got = out.cpu().numpy()
+    want = dict(zip(keys.tolist(), vals.tolist()))
+    assert got.tolist() == [want.get(k, -1) for k in probe.tolist()]
+    kvx.kvx_table_destroy(table)
+    with pytest.raises(kvx.KvxError) as ei:
+        kvx.kvx_table_build(dev(np.array([7, 9, 7], np.uint64), np.uint64), dev(np.arange(3, dtype=np.int32), np.int32), 3)
+    assert ei.value.status == kvx.KVX_EINVAL
+    empty = kvx.kvx_table_build(None, None, 0)
+    kvx.kvx_table_lookup(empty, dev(keys[:10], np.uint64), 10, out)
+    assert out[:10].cpu().tolist() == [-1] * 10
+    kvx.kvx_table_destroy(empty)
+
+
+# ---------------------------------------------------------------------------------------------
+# match + device-built plan + push
+# ---------------------------------------------------------------------------------------------
+
+class Case:
+    """A bidirectional workload on the device: published hashes and resident keys from the oracle."""
+
+    def __init__(self, w, flip_frac=0.0, seed=0):
+        orc = oracle.load()
+        self.w = w
+        hs = [orc.block_hashes(w.tokens[w.tok_off[s]:w.tok_off[s + 1]], w.block_size) for s in range(w.n_sessions)]
+        allh = np.concatenate(hs) if hs else np.zeros(0, np.uint64)
+        self.remote_hash = allh.copy()
+        if flip_frac:
+            flip = np.random.default_rng(seed).random(len(allh)) < flip_frac
+            self.remote_hash[flip] ^= np.uint64(1)
+        self.keys = np.unique(allh[w.resident])
+        self.t_tokens = dev(w.tokens, np.uint32)
+        self.t_tok_off = dev(w.tok_off, np.int64)
+        self.t_rh = dev(self.remote_hash, np.uint64)
+        self.t_rb = dev(w.remote_blk, np.int32)
+        self.t_ro = dev(w.rem_off, np.int64)
+        self.t_free = dev(w.free_blocks, np.int32)
+        self.table = kvx.kvx_table_build(dev(self.keys, np.uint64), dev(np.arange(len(self.keys), dtype=np.int32),
+                                                                        np.int32), len(self.keys))
+
+    def oracle_match(self, n_free=None):
+        w = self.w
+        free = w.free_blocks if n_free is None else w.free_blocks[:n_free]
+        return oracle.load().match(w.tokens, w.tok_off, w.block_size, self.keys, self.remote_hash, w.remote_blk,
+                                   w.rem_off, w.threshold, free)
+
+    def match(self, remote_pool=None, local_pool=None, n_free=None, want_plan=True):
+        w = self.w
+        out = torch.zeros(max(w.n_sessions, 1) * 24, dtype=torch.uint8, device="cuda")
+        nf = len(w.free_blocks) if n_free is None else n_free
+        st, plan = kvx.kvx_match_prefix(self.t_tokens, self.t_tok_off, w.n_sessions, w.block_size, self.table, self.t_rh,
+                                        self.t_rb, self.t_ro, w.threshold, self.t_free, nf, remote_pool, local_pool, out,
+                                        want_plan=want_plan)
+        return st, plan, results(out, w.n_sessions)
+
+    def close(self):
+        kvx.kvx_table_destroy(self.table)
+
+
+def assert_decisions(got, want):
+    assert got["local_hit_blocks"].tolist() == want["local_hit"].tolist()
+    assert got["remote_hit_blocks"].tolist() == want["remote_hit"].tolist()
+    assert got["missing_tokens"].tolist() == want["missing"].tolist()
+    assert got["push"].tolist() == want["push"].tolist()
+    assert got["dst_start"].tolist() == want["dst_start"].tolist()
+
+
+def oracle_requests(c, want):
+    """The pushes the oracle's match implies: one request per pushing session."""
+    w, reqs, k = c.w, [], 0
+    for s in range(w.n_sessions):
+        if want["push"][s]:
+            nb = int(want["missing"][s]) // w.block_size
+            reqs.append((nb * w.block_size, want["pair_src"][k:k + nb], want["pair_dst"][k:k + nb]))
+            k += nb
+    return reqs
+
+
+def test_match_decisions_and_plan_runs_reduced():
+    w = kvx_inputs.bidir_mla_fp8(seed=21, n_sessions=24, n_layers=2, system_tokens=256, hist_range=(64, 3000),
+                                 resident_p=0.6, threshold=256)
+    c = Case(w, flip_frac=0.01, seed=3)
+    want = c.oracle_match()
+    assert want["status"] == 0 and want["push"].sum() > 3 and (want["push"] == 0).sum() > 0
+    st, plan, got = c.match(want_plan=False)
+    assert st == kvx.KVX_OK and plan is None
+    assert_decisions(got, want)
+    c.close()
+
+
+def test_match_plan_and_push_reduced():
+    w = kvx_inputs.bidir_mla_fp8(seed=22, n_sessions=16, n_layers=3, system_tokens=256, hist_range=(64, 2500),
+                                 resident_p=0.5, threshold=128)
+    c = Case(w, flip_frac=0.005, seed=4)
+    want = c.oracle_match()
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=5)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    reqs = oracle_requests(c, want)
+    # the device-built runs are the oracle's maximal runs of each pushing session's block pairs
+    orc = oracle.load()
+    wr = [orc.block_runs(r[1], r[2]) for r in reqs]
+    rs, rd, rl = kvx.kvx_plan_runs(plan)
+    assert rs.tolist() == (np.concatenate([x[0] for x in wr]) * 64).tolist()
+    assert rd.tolist() == (np.concatenate([x[1] for x in wr]) * 64).tolist()
+    assert rl.tolist() == (np.concatenate([x[2] for x in wr]) * 64).tolist()
+    side = torch.cuda.Stream(priority=-1)
+    for layer in range(w.decode.n_layers):
+        kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")], reqs,
+                 range(w.decode.n_layers))
+    kvx.kvx_plan_destroy(plan)
+    c.close()
+
+
+def test_match_full_sessions_two_layers():
+    """All 256 sessions of the bidirectional workload (1024 shared + U[2k,32k] history tokens each);
+    the pool has 2 of its 48 layers so the whole push is checked against the oracle."""
+    w = kvx_inputs.bidir_mla_fp8(n_layers=2)
+    c = Case(w)
+    want = c.oracle_match()
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=w.seed)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    assert want["push"].sum() == w.n_sessions                   # every session has > 512 missing tokens
+    side = torch.cuda.Stream(priority=-1)
+    for layer in range(2):
+        kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")],
+                 oracle_requests(c, want), range(2))
+    kvx.kvx_plan_destroy(plan)
+    c.close()
+
+
+@pytest.mark.parametrize("l_rem,want_push", [(511, 0), (512, 1), (513, 1)])
+def test_threshold_edges(l_rem, want_push):
+    bs, n = 1, 600
+    rng = np.random.default_rng(l_rem)
+    toks = rng.integers(0, kvx_inputs.VOCAB, n).astype(np.uint32)
+    h = oracle.load().block_hashes(toks, bs)
+    remote = h.copy()
+    remote[l_rem] ^= np.uint64(9)
+    table = kvx.kvx_table_build(None, None, 0)
+    out = torch.zeros(24, dtype=torch.uint8, device="cuda")
+    st, plan = kvx.kvx_match_prefix(dev(toks, np.uint32), dev(np.array([0, n], np.int64), np.int64), 1, bs, table,
+                                    dev(remote, np.uint64), dev(np.arange(n, dtype=np.int32), np.int32),
+                                    dev(np.array([0, n], np.int64), np.int64), 512,
+                                    dev(np.arange(n, dtype=np.int32), np.int32), n, None, None, out, want_plan=False)
+    r = results(out, 1)[0]
+    assert (r["local_hit_blocks"], r["remote_hit_blocks"], r["missing_tokens"], r["push"]) == (0, l_rem, l_rem, want_push)
+    kvx.kvx_table_destroy(table)
+
+
+def test_free_list_too_short_is_enomem():
+    w = kvx_inputs.bidir_mla_fp8(seed=23, n_sessions=8, n_layers=1, system_tokens=128, hist_range=(600, 1500),
+                                 resident_p=0.3, threshold=64)
+    c = Case(w)
+    full = c.oracle_match()
+    need = int(sum(full["missing"][full["push"] == 1]) // 64)
+    short = c.oracle_match(n_free=need - 1)
+    assert short["status"] == 5
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=1)
+    dst, big = device_pool(w.prefill, "canary_fp8_bytes")
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst), n_free=need - 1)
+    assert st == kvx.KVX_ENOMEM and plan is None
+    assert_decisions(got, short)
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst), n_free=need)
+    assert st == kvx.KVX_OK and plan is not None
+    kvx.kvx_plan_destroy(plan)
+    c.close()
+
+
+def test_bad_free_block_fails_the_layer_without_writing_outside():
+    """A free-list entry outside the prefill pool: the copy kernel's bounds guard skips those tiles and
+    kvx_sync reports the layer FAILED; nothing outside the pool buffers changes."""
+    w = kvx_inputs.bidir_mla_fp8(seed=24, n_sessions=2, n_layers=1, system_tokens=128, hist_range=(600, 900),
+                                 resident_p=0.0, threshold=64)
+    bad_free = w.free_blocks.copy()
+    bad_free[0] = w.prefill.n_blocks + 5
+    w.free_blocks = bad_free
+    c = Case(w)
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=1)
+    per = -(-w.prefill.buffer_bytes // 512) * 512
+    guard = torch.full((per * 3,), 0x55, dtype=torch.uint8, device="cuda")
+    dst = [guard[per:per + w.prefill.buffer_bytes]]
+    dst[0].fill_(kvx_inputs.CANARY_FP8)
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+    assert st == kvx.KVX_OK
+    kvx.kvx_push_layer(plan, 0, torch.cuda.current_stream())
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_EFAILED
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_FAILED]
+    assert bool((guard[:per] == 0x55).all()) and bool((guard[per + w.prefill.buffer_bytes:] == 0x55).all())
+    kvx.kvx_plan_destroy(plan)
+    c.close()

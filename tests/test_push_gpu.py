@@ -1,0 +1,227 @@
+"""GPU parity of the layer push through the C-ABI: the kvx copy on device against the oracle, byte for
+byte (this is pure data movement: bit-exact is the only bar).
+
+Small cases run every layer through the oracle; the full-size workloads (Qwen3-32B-shaped, 64 layers)
+run in the launch configuration the benchmark times (one push per layer on a high-priority side
+stream, gated on an event after the prefill fixture) and check sampled layers whole."""
+import zlib
+
+import numpy as np
+import pytest
+
+import kvx_inputs
+import oracle
+from gpu_helpers import canary_host, check_layers, device_pool, host, layer_buffers
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+kvx = pytest.importorskip("disaggregated_prefill_decode_gb300.kvx")
+
+PoolGeom = kvx_inputs.PoolGeom
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    yield
+    torch.cuda.synchronize()
+
+
+def reqs_of(w):
+    return [(r.n_tokens, r.src_ids, r.dst_ids) for r in w.requests]
+
+
+def push_all_layers(plan, n_layers, fixture_iters=2000, per_layer=True):
+    """The benchmark's launch pattern: fixture on the main stream, event, push on a side stream."""
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(priority=-1)
+    if per_layer:
+        for layer in range(n_layers):
+            kvx.kvx_fixture_prefill(8, fixture_iters, stream=main)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            kvx.kvx_push_layer(plan, layer, side, ev)
+    else:
+        ev = torch.cuda.Event()
+        ev.record(main)
+        kvx.kvx_push_layers(plan, 0, n_layers, side, ev)
+    return kvx.kvx_sync(plan, -1)
+
+
+def run_workload(w, layers_to_check, opts=None, per_layer=True):
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), opts)
+    assert push_all_layers(plan, w.src.n_layers, per_layer=per_layer) == kvx.KVX_OK
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_DONE] * w.src.n_layers
+    per = w.dst.n_planes * w.dst.n_shards
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(per)],
+                 reqs_of(w), layers_to_check)
+    info = kvx.kvx_plan_get_info(plan)
+    kvx.kvx_plan_destroy(plan)
+    return info
+
+
+def test_tiny_all_layers():
+    w = kvx_inputs.tiny()
+    run_workload(w, range(w.src.n_layers))
+
+
+@pytest.mark.parametrize("make", [
+    lambda: kvx_inputs.qwen3_32b_single(n_layers=2),
+    lambda: kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=6),
+    lambda: kvx_inputs.tp4_to_tp1_remap(n_layers=2, n_requests=3),
+], ids=["qwen3_32b_single", "qwen3_32b_batched", "tp4_to_tp1_remap"])
+def test_reduced_workloads_all_layers(make):
+    w = make()
+    info = run_workload(w, range(w.src.n_layers))
+    assert info["vec_bytes"] == 16
+
+
+@pytest.mark.parametrize("name", ["qwen3_32b_single", "qwen3_32b_batched", "tp4_to_tp1_remap"])
+def test_full_size_sampled_layers(name):
+    """Full 64-layer workload in the benchmark's launch pattern; layers 0, 31, 63 checked whole."""
+    w = kvx_inputs.PUSH_WORKLOADS[name]()
+    run_workload(w, [0, 31, 63])
+
+
+def test_all_layers_in_one_launch():
+    w = kvx_inputs.qwen3_32b_batched(n_layers=3, n_requests=4)
+    run_workload(w, range(3), per_layer=False)
+
+
+@pytest.mark.parametrize("tile_bytes,threads", [(16, 32), (4096, 128), (16384, 256), (65536, 1024), (2064, 96)])
+def test_launch_shapes(tile_bytes, threads):
+    w = kvx_inputs.qwen3_32b_batched(n_layers=1, n_requests=3, len_range=(100, 900))
+    run_workload(w, [0], opts={"tile_bytes": tile_bytes, "threads": threads})
+
+
+GEOMS = {
+    # name: (src, dst) -- block sizes 1/16/64, odd head bytes (narrow vectors), merges and splits
+    "bs1": (PoolGeom(2, 2, 1, 2, 64, 2, 1, 300), PoolGeom(2, 2, 1, 2, 64, 2, 1, 300)),
+    "bs64_to_16": (PoolGeom(2, 2, 1, 8, 128, 2, 64, 20), PoolGeom(2, 2, 1, 8, 128, 2, 16, 80)),
+    "head_bytes_6": (PoolGeom(1, 2, 1, 3, 3, 2, 16, 40), PoolGeom(1, 2, 1, 3, 3, 2, 16, 40)),
+    "head_bytes_3_merge": (PoolGeom(1, 1, 2, 1, 3, 1, 4, 50), PoolGeom(1, 1, 1, 2, 3, 1, 8, 25)),
+    "head_bytes_12_split": (PoolGeom(1, 1, 1, 4, 6, 2, 8, 30), PoolGeom(1, 1, 4, 1, 6, 2, 4, 60)),
+    "split1to2": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 40), PoolGeom(2, 2, 2, 4, 128, 2, 16, 40)),
+    "merge8to2": (PoolGeom(1, 2, 8, 1, 64, 2, 16, 40), PoolGeom(1, 2, 2, 4, 64, 2, 32, 20)),
+    "mla576_fp8": (PoolGeom(2, 1, 1, 1, 576, 1, 64, 30), PoolGeom(2, 1, 1, 1, 576, 1, 64, 30)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GEOMS))
+def test_geometry_sweep(name):
+    from helpers import random_requests
+    sg, dg = GEOMS[name]
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    reqs = random_requests(rng, sg, dg, 4, min(sg.n_blocks * sg.block_size, dg.n_blocks * dg.block_size) // 4)
+    kind = "fp8_bytes" if sg.elem_bytes == 1 else "bf16_normal"
+    src, _ = device_pool(sg, kind, seed=7)
+    dst, _ = device_pool(dg, "canary_" + kind)
+    plan = kvx.kvx_plan(kvx.Pool(sg, src), kvx.Pool(dg, dst), reqs)
+    assert push_all_layers(plan, sg.n_layers) == kvx.KVX_OK
+    per = dg.n_planes * dg.n_shards
+    check_layers(sg, src, dg, dst, lambda l: [canary_host(dg, kind) for _ in range(per)], reqs, range(sg.n_layers))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_one_huge_run_equals_one_copy():
+    g = PoolGeom(2, 2, 1, 8, 128, 2, 16, 1100)
+    src, _ = device_pool(g, "bf16_normal", seed=3)
+    dst, _ = device_pool(g, "canary_bf16_normal")
+    n_blk, off = 1000, 50
+    plan = kvx.kvx_plan(kvx.Pool(g, src), kvx.Pool(g, dst), [(n_blk * 16, np.arange(n_blk), np.arange(off, off + n_blk))])
+    assert kvx.kvx_plan_get_info(plan)["n_runs"] == 1
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    bb = 16 * g.row_bytes
+    canary = torch.tensor(kvx_inputs.CANARY_BF16 - 0x10000, dtype=torch.int16, device="cuda")
+    for s, d in zip(src, dst):
+        assert torch.equal(d[off * bb:(off + n_blk) * bb], s[:n_blk * bb])
+        assert bool((d[:off * bb].view(torch.int16) == canary).all())
+        assert bool((d[(off + n_blk) * bb:].view(torch.int16) == canary).all())
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_empty_plan_pushes_nothing():
+    g = PoolGeom(2, 2, 1, 2, 64, 2, 16, 8)
+    src, _ = device_pool(g, "bf16_normal", seed=1)
+    dst, big = device_pool(g, "canary_bf16_normal")
+    before = big.clone()
+    plan = kvx.kvx_plan(kvx.Pool(g, src), kvx.Pool(g, dst), [(0, [], [])])
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    assert torch.equal(big, before)
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_producer_unchanged_and_plan_reusable():
+    w = kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=3)
+    src, sbig = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    s_before = sbig.clone()
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    for _ in range(3):                                  # the same plan pushed three times
+        assert push_all_layers(plan, 2) == kvx.KVX_OK
+    assert torch.equal(sbig, s_before)
+    per = w.dst.n_planes
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(per)],
+                 reqs_of(w), range(2))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_push_ordered_after_prefill_rewrite():
+    """The fixture rewrites each layer's producer KV just before its event; a push that started early
+    would copy the stale bytes. The final consumer must equal the oracle on the final producer."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=4)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(priority=-1)
+    for layer in range(4):
+        for b in layer_buffers(w.src, src, layer):
+            kvx.kvx_fixture_prefill(16, 20000, b, b.numel(), seed=1000 + layer, stream=main)
+        ev = torch.cuda.Event()
+        ev.record(main)
+        kvx.kvx_push_layer(plan, layer, side, ev)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(4))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_sync_timeout_then_completion():
+    """A long (bounded) fixture holds the stream; a 1 ms deadline times out, a later sync completes."""
+    w = kvx_inputs.tiny()
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    side = torch.cuda.Stream()
+    kvx.kvx_fixture_prefill(1, 30_000_000, stream=side)          # ~tens of ms of dependent integer work
+    kvx.kvx_push_layer(plan, 0, side)
+    kvx.kvx_push_layer(plan, 1, side)
+    assert kvx.kvx_sync(plan, 1000) == kvx.KVX_ETIMEDOUT
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_PENDING] * 2
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(2))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_injected_failure_reports_failed_layer():
+    w = kvx_inputs.tiny()
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    kvx.kvx_plan_inject_failure(plan, 1)
+    assert push_all_layers(plan, 2) == kvx.KVX_EFAILED
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_DONE, kvx.KVX_LAYER_FAILED]
+    assert push_all_layers(plan, 2) == kvx.KVX_OK                # the injection fires once
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_DONE] * 2
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_launch_count_grows():
+    n0 = kvx.kvx_launch_count()
+    test_tiny_all_layers()
+    assert kvx.kvx_launch_count() >= n0 + 4                     # 2 fixtures + 2 pushes
