@@ -175,27 +175,45 @@ def run_kvx(args, rank, local_rank, world):
     blocks_step = sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L
 
     K, W = args.steps, args.warmup
+    opts["flags"] = kvx.KVX_PLAN_TIMING
     ready = [torch.cuda.Event() for _ in range(L)]
-    t_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K * L)]
+    for ev in ready:                                  # materialise the events so their handles exist
+        ev.record(main)
+    ready_h = [int(ev.cuda_event) for ev in ready]
+    main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
+    lib = kvx._lib                                    # the C-ABI itself: two calls per layer in the loop
+    push_us = []
 
-    def step(timed_idx):
+    def issue():
+        """One step's plan and its per-layer issue: fixture then gated push, layer by layer."""
         plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
         for layer in range(L):
-            kvx.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, stream=main)
-            ready[layer].record(main)
-            if timed_idx is not None:
-                side.wait_event(ready[layer])
-                t_ev[timed_idx * L + layer][0].record(side)
-            kvx.kvx_push_layer(plan, layer, side, ready[layer])
-            if timed_idx is not None:
-                t_ev[timed_idx * L + layer][1].record(side)
+            st = lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h, ready_h[layer])
+            st |= lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer])
+            if st:
+                raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
+        return plan
+
+    def finish(plan, timed):
         st = kvx.kvx_sync(plan, -1)
-        kvx.kvx_plan_destroy(plan)
         if st != kvx.KVX_OK:
             raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
+        if timed:
+            push_us.extend(kvx.kvx_plan_push_times(plan).tolist())
+        kvx.kvx_plan_destroy(plan)
 
-    for _ in range(W):
-        step(None)
+    def run_steps(n, timed):
+        """n steps, each synced after the next one is issued (one request in flight behind another)."""
+        prev = None
+        for _ in range(n):
+            plan = issue()
+            if prev is not None:
+                finish(prev, timed)
+            prev = plan
+        if prev is not None:
+            finish(prev, timed)
+
+    run_steps(W, False)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -212,8 +230,7 @@ def run_kvx(args, rank, local_rank, world):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     t0.record(main)
-    for k in range(K):
-        step(k)
+    run_steps(K, True)
     main.wait_stream(side)
     t1.record(main)
     torch.cuda.synchronize()
@@ -221,7 +238,8 @@ def run_kvx(args, rank, local_rank, world):
     launches = kvx.kvx_launch_count() - launches0
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    push_ms = [a.elapsed_time(b) for a, b in t_ev]
+    push_ms = [u * 1e-3 for u in push_us]
+    assert len(push_ms) == K * L
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -256,8 +274,9 @@ def run_kvx(args, rank, local_rank, world):
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"],
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
-            "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on main stream, "
-                      "event, kvx_push_layer on a priority side stream; plan built and synced every step",
+            "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on the main stream "
+                      "records the layer's event; kvx_push_layer on a priority side stream waits for it; a plan is "
+                      "built every step and synced after the next step is issued",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "blocks_per_s": round(world * blocks_step * K / (elapsed_ms * 1e-3), 1),
@@ -265,6 +284,8 @@ def run_kvx(args, rank, local_rank, world):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "kernel": "kvx_copy_tiles (one launch per layer)",
+            "launch_us_p50": round(statistics.median(push_us), 3),
+            "timing": "KVX_PLAN_TIMING events around each launch on the side stream, all timed launches",
             "bytes_per_launch": 2 * info["bytes_per_layer"], "mean_launch_us": round(mean_push_ms * 1e3, 3),
             "traffic": ncu_traffic(args.workload),
         },

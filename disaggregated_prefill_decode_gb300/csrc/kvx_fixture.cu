@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(128) kvx_fixture_kernel(int64_t iters, uint4 *
 using namespace kvx;
 
 extern "C" kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes, uint64_t seed,
-                                          cudaStream_t stream) {
+                                          cudaStream_t stream, cudaEvent_t done) {
     if (ctas < 1 || ctas > 65535 || iters < 0) return fail(KVX_EINVAL, "fixture: ctas in [1, 65535], iters >= 0");
     if (buf && (n_bytes < 0 || n_bytes % 16 || ((uintptr_t)buf & 15)))
         return fail(KVX_EINVAL, "fixture: buffer must be 16-byte aligned with a multiple-of-16 size");
@@ -40,5 +40,9 @@ extern "C" kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf
     kvx_fixture_kernel<<<ctas, 128, 0, stream>>>(iters, static_cast<uint4 *>(buf), buf ? n_bytes / 16 : 0, seed);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "fixture launch");
+    if (done) {
+        e = cudaEventRecord(done, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fixture)");
+    }
     return KVX_OK;
 }

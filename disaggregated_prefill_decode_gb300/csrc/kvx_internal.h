@@ -50,6 +50,7 @@ struct Geom {
 
 struct PendingPush {
     cudaEvent_t done;
+    cudaEvent_t start;      // timing plans only
     int32_t layer_begin, layer_end;
 };
 
@@ -91,6 +92,7 @@ struct kvx_plan_s {
     int32_t width = 0;
     int32_t tile_bytes = 16384;
     int32_t threads = 256;
+    int32_t flags = 0;                         // KVX_PLAN_* bits
     int64_t n_tiles = 0;                       // per (layer, plane)
     int64_t bytes_per_layer = 0;
     std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans
@@ -108,6 +110,7 @@ struct kvx_plan_s {
     // pushes issued and not yet confirmed by kvx_sync
     std::vector<kvx::PendingPush> pending;
     std::vector<cudaEvent_t> free_events;
+    std::vector<float> push_us;                // timing plans: durations confirmed by the last sync
     std::vector<int32_t> layer_state;          // kvx_layer_state per layer
     std::vector<uint8_t> inject;               // host fault injection armed, per layer
     std::vector<uint8_t> injected_pending;     // injected failure waiting for sync, per layer

@@ -275,13 +275,17 @@ struct MatchScratch {
     int32_t *err;           // [4] error bits
 };
 
+// B bounds the scratch arrays: overlapping remote ranges (a malformed CSR) could otherwise claim more
+// pushed blocks than there are published ones.
 __global__ void kvx_assign_dst(kvx_match_result *out, const int64_t *sess_start, int32_t n_sessions,
-                               int64_t *scalars, int64_t n_free, int32_t *err) {
+                               int64_t *scalars, int64_t n_free, int64_t B, int32_t *err) {
     const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
     const bool fits = scalars[0] <= n_free;
+    const bool sane = scalars[0] <= B;
     if (s == 0) {
-        scalars[4] = fits ? scalars[0] : 0;
-        if (!fits) atomicOr(err, 8);
+        scalars[4] = (fits && sane) ? scalars[0] : 0;
+        if (!sane) atomicOr(err, 2);
+        else if (!fits) atomicOr(err, 8);
     }
     if (s < n_sessions && out[s].push) out[s].dst_start = sess_start[s];
 }
@@ -591,7 +595,7 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
     ok(cudaGetLastError());
     ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
     count_launch();
-    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free,
+    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free, B,
                                                                   m.err);
     ok(cudaGetLastError());
 

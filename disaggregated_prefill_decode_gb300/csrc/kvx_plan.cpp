@@ -195,10 +195,12 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
     if (st) return st;
     if (opts) {
-        for (int i = 0; i < 6; ++i)
+        for (int i = 0; i < 5; ++i)
             if (opts->reserved[i]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+        if (opts->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
         if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
         if (opts->threads) pl->threads = opts->threads;
+        pl->flags = opts->flags;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
@@ -336,6 +338,14 @@ kvx_status kvx_plan_tiles(kvx_plan_t pl, int64_t *n_tiles, const void **tiles) {
     if (!pl || !n_tiles || !tiles) return fail(KVX_EINVAL, "NULL argument");
     *n_tiles = (int64_t)pl->tiles.size();
     *tiles = pl->tiles.data();
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_push_times(kvx_plan_t pl, float *out_us, int32_t cap, int32_t *n) {
+    if (!pl || !n || (cap > 0 && !out_us)) return fail(KVX_EINVAL, "NULL argument");
+    if (!(pl->flags & KVX_PLAN_TIMING)) return fail(KVX_EINVAL, "plan was built without KVX_PLAN_TIMING");
+    *n = (int32_t)pl->push_us.size();
+    for (int32_t i = 0; i < *n && i < cap; ++i) out_us[i] = pl->push_us[i];
     return KVX_OK;
 }
 

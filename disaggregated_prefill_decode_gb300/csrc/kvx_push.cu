@@ -251,13 +251,15 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     return KVX_OK;
 }
 
+// Timing plans use timing-enabled events for both ends of a push; other plans only need completion.
 static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
     if (!pl->free_events.empty()) {
         *ev = pl->free_events.back();
         pl->free_events.pop_back();
         return KVX_OK;
     }
-    cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    const unsigned flags = (pl->flags & KVX_PLAN_TIMING) ? cudaEventDefault : cudaEventDisableTiming;
+    cudaError_t e = cudaEventCreateWithFlags(ev, flags);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
     return KVX_OK;
 }
@@ -275,8 +277,19 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
         e = cudaStreamWaitEvent(stream, ready, 0);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(ready)");
     }
+    cudaEvent_t start = nullptr;
+    if (pl->flags & KVX_PLAN_TIMING) {
+        st = take_event(pl, &start);
+        if (st) return st;
+        e = cudaEventRecord(start, stream);
+        if (e != cudaSuccess) {
+            pl->free_events.push_back(start);
+            return cuda_fail(e, "cudaEventRecord(push start)");
+        }
+    }
     e = launch_copy(plan_copy_args(pl, l0), pl->n_tiles, l1 - l0, pl->vec, pl->strided != 0, pl->threads, stream);
     if (e != cudaSuccess) {
+        if (start) pl->free_events.push_back(start);
         for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
         return cuda_fail(e, "copy kernel launch");
     }
@@ -286,9 +299,10 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
     e = cudaEventRecord(ev, stream);
     if (e != cudaSuccess) {
         pl->free_events.push_back(ev);
+        if (start) pl->free_events.push_back(start);
         return cuda_fail(e, "cudaEventRecord(push)");
     }
-    pl->pending.push_back({ev, l0, l1});
+    pl->pending.push_back({ev, start, l0, l1});
     for (int32_t l = l0; l < l1; ++l) {
         pl->layer_state[l] = KVX_LAYER_PENDING;
         if (pl->inject[l]) { pl->injected_pending[l] = 1; pl->inject[l] = 0; }
@@ -342,8 +356,16 @@ kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {
         if (e != cudaSuccess) return cuda_fail(e, "clearing push error words");
     }
     bool failed = false;
+    pl->push_us.clear();
     for (size_t i = 0; i < sealed; ++i) {
         const PendingPush &p = pl->pending[i];
+        if (p.start) {
+            float ms = 0.f;
+            e = cudaEventElapsedTime(&ms, p.start, p.done);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime(push)");
+            pl->push_us.push_back(ms * 1000.f);
+            pl->free_events.push_back(p.start);
+        }
         for (int32_t l = p.layer_begin; l < p.layer_end; ++l) {
             const bool bad = err[l] != 0 || pl->injected_pending[l];
             pl->layer_state[l] = bad ? KVX_LAYER_FAILED : KVX_LAYER_DONE;
@@ -364,6 +386,7 @@ kvx_status kvx_plan_destroy(kvx_plan_t pl) {
         cudaError_t e = cudaEventSynchronize(p.done);
         if (e != cudaSuccess && st == KVX_OK) st = cuda_fail(e, "cudaEventSynchronize(destroy)");
         cudaEventDestroy(p.done);
+        if (p.start) cudaEventDestroy(p.start);
     }
     for (cudaEvent_t ev : pl->free_events) cudaEventDestroy(ev);
     if (pl->upload_evt) {

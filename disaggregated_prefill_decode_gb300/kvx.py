@@ -37,7 +37,10 @@ class kvx_request(ctypes.Structure):
 
 
 class kvx_plan_opts(ctypes.Structure):
-    _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("reserved", c_i32 * 6)]
+    _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("flags", c_i32), ("reserved", c_i32 * 5)]
+
+
+KVX_PLAN_TIMING = 1
 
 
 class kvx_plan_info(ctypes.Structure):
@@ -69,6 +72,7 @@ _sig = {
     "kvx_push_layers": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp]),
     "kvx_sync": (c_i32, [c_vp, c_i64]),
     "kvx_plan_layer_states": (c_i32, [c_vp, _P(c_i32), c_i32]),
+    "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), c_i32, _P(c_i32)]),
     "kvx_plan_inject_failure": (c_i32, [c_vp, c_i32]),
     "kvx_plan_destroy": (c_i32, [c_vp]),
     "kvx_status_str": (ctypes.c_char_p, [c_i32]),
@@ -79,7 +83,7 @@ _sig = {
     "kvx_table_destroy": (c_i32, [c_vp]),
     "kvx_match_prefix": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
                                  _P(kvx_pool), _P(kvx_pool), c_vp, _P(c_vp), c_vp]),
-    "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp]),
+    "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp, c_vp]),
     "kvx_version": (ctypes.c_char_p, []),
     "kvx_launch_count": (c_i64, []),
 }
@@ -212,7 +216,8 @@ def kvx_plan(src: Pool, dst: Pool, requests: Iterable) -> Plan:
 def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] = None) -> Plan:
     carr, n, _keep = _requests(requests)
     out = c_vp()
-    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0))) if opts else None
+    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0)), int(opts.get("flags", 0))) \
+        if opts else None
     st = _lib.kvx_plan_ex(ctypes.byref(src.struct), ctypes.byref(dst.struct), carr, n,
                           ctypes.byref(o) if o is not None else None, ctypes.byref(out))
     _check(st, "kvx_plan")
@@ -263,6 +268,15 @@ def kvx_sync(plan, timeout_us: int = -1) -> int:
     if st not in (KVX_OK, KVX_ETIMEDOUT, KVX_EFAILED):
         raise KvxError(st, "kvx_sync")
     return st
+
+
+def kvx_plan_push_times(plan, cap: int = 4096) -> np.ndarray:
+    """Device microseconds of each push confirmed by the last kvx_sync (timing plans)."""
+    out = np.zeros(cap, np.float32)
+    n = c_i32()
+    _check(_lib.kvx_plan_push_times(_h(plan), out.ctypes.data_as(_P(ctypes.c_float)), cap, ctypes.byref(n)),
+           "kvx_plan_push_times")
+    return out[:min(n.value, cap)].copy()
 
 
 def kvx_plan_layer_states(plan) -> np.ndarray:
@@ -320,9 +334,10 @@ def kvx_match_prefix(tokens, tok_off, n_sessions: int, block_size: int, table: T
     return st, (Plan(plan.value, n_layers) if plan.value else None)
 
 
-def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed: int = 0, stream=None) -> None:
-    _check(_lib.kvx_fixture_prefill(ctas, iters, _ptr(buf), n_bytes, seed & (2**64 - 1), _stream(stream)),
-           "kvx_fixture_prefill")
+def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed: int = 0, stream=None,
+                        done=None) -> None:
+    _check(_lib.kvx_fixture_prefill(ctas, iters, _ptr(buf), n_bytes, seed & (2**64 - 1), _stream(stream),
+                                    _event(done)), "kvx_fixture_prefill")
 
 
 def library_path() -> str:

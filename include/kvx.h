@@ -100,8 +100,15 @@ typedef struct kvx_plan_s *kvx_plan_t;
 typedef struct kvx_plan_opts {
     int32_t tile_bytes;       /* bytes one CTA copies per tile (default 16384; multiple of 16)  */
     int32_t threads;          /* threads per CTA (default 256; multiple of 32, <= 1024)         */
-    int32_t reserved[6];      /* must be 0 */
+    int32_t flags;            /* KVX_PLAN_* bits                                                 */
+    int32_t reserved[5];      /* must be 0 */
 } kvx_plan_opts;
+
+/* Record the device time of every push (CUDA events around each launch); read with
+ * kvx_plan_push_times after kvx_sync. This is the per-layer KV transfer time that the
+ * bidirectional article's prefill-duration breakdown ([P3] "Leistungsdaten", Figs. 4 and 6)
+ * separates from recompute time. */
+#define KVX_PLAN_TIMING 1
 
 /*
  * kvx_plan -- build the copy plan of a set of requests.
@@ -188,6 +195,11 @@ kvx_status kvx_push_layers(kvx_plan_t plan, int32_t layer_begin, int32_t layer_e
  * reported FAILED (kvx_plan_layer_states tells which), else KVX_OK.
  */
 kvx_status kvx_sync(kvx_plan_t plan, int64_t timeout_us);
+
+/* Plans built with KVX_PLAN_TIMING: device time in microseconds of each push the last completed
+ * kvx_sync confirmed, in issue order (out: up to cap entries; *n receives the count). Each time
+ * runs from the point the stream passed the push's `ready` wait to the end of its kernel. */
+kvx_status kvx_plan_push_times(kvx_plan_t plan, float *out_us, int32_t cap, int32_t *n);
 
 /* Per-layer states (out: n_layers entries of kvx_layer_state). */
 kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers);
@@ -282,7 +294,7 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
  * derived from `seed`, so a push that ran before the fixture finished would copy stale bytes.
  * ---------------------------------------------------------------------------------------------- */
 kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes, uint64_t seed,
-                               cudaStream_t stream);
+                               cudaStream_t stream, cudaEvent_t done /* recorded after it when not NULL */);
 
 /* Library version string and the number of kvx kernels launched by this process so far. */
 const char *kvx_version(void);

@@ -208,3 +208,16 @@ def test_requests_keep_extra_ids_unused():
     pl = kvx.kvx_plan(sp, dp, [(4, [0, 0, 0], [1, 1, 1]), (3, [2], [2])])
     assert kvx.kvx_plan_get_info(pl)["n_runs"] == 2
     kvx.kvx_plan_destroy(pl)
+
+
+def test_timing_flag_validation():
+    g = PoolGeom(1, 1, 1, 2, 64, 2, 16, 8)
+    sp, dp = pools(g, g)
+    ok = (20, [0, 1], [2, 3])
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"flags": 2}))
+    plain = kvx.kvx_plan(sp, dp, [ok])
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_push_times(plain))
+    kvx.kvx_plan_destroy(plain)
+    timed = kvx.kvx_plan_ex(sp, dp, [ok], {"flags": kvx.KVX_PLAN_TIMING})
+    assert len(kvx.kvx_plan_push_times(timed)) == 0          # nothing synced yet
+    kvx.kvx_plan_destroy(timed)

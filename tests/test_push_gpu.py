@@ -225,3 +225,16 @@ def test_launch_count_grows():
     n0 = kvx.kvx_launch_count()
     test_tiny_all_layers()
     assert kvx.kvx_launch_count() >= n0 + 4                     # 2 fixtures + 2 pushes
+
+
+def test_push_times_of_timing_plan():
+    w = kvx_inputs.qwen3_32b_single(n_layers=4)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"flags": kvx.KVX_PLAN_TIMING})
+    assert push_all_layers(plan, 4) == kvx.KVX_OK
+    t = kvx.kvx_plan_push_times(plan)
+    assert len(t) == 4 and np.all(t > 0) and np.all(t < 1e5)
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(4))
+    kvx.kvx_plan_destroy(plan)
