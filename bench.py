@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--workload", default="qwen3_32b_single", choices=sorted(kvx_inputs.PUSH_WORKLOADS))
     p.add_argument("--tile-bytes", type=int, default=0)
     p.add_argument("--threads", type=int, default=0)
+    p.add_argument("--kernel", type=int, default=0, help="KVX_KERNEL_*: 0 auto, 1 tile, 2 persist, 3 bulk")
+    p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--fixture-ctas", type=int, default=8)
     p.add_argument("--fixture-iters", type=int, default=2000)
     p.add_argument("--e2e-steps", type=int, default=5)
@@ -164,7 +166,8 @@ def run_kvx(args, rank, local_rank, world):
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
     sp, dp = kvx.Pool(w.src, src), kvx.Pool(w.dst, dst)
     reqs = requests(w)
-    opts = {"tile_bytes": args.tile_bytes, "threads": args.threads}
+    opts = {"tile_bytes": args.tile_bytes, "threads": args.threads, "kernel": args.kernel,
+            "ctas_per_sm": args.ctas_per_sm}
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream(priority=-1)
 
@@ -272,7 +275,8 @@ def run_kvx(args, rank, local_rank, world):
             "consumer": f"{w.dst.n_shards} x [{w.dst.n_blocks}][{w.dst.block_size}][{w.dst.heads_per_shard}][{w.dst.head_dim}] x {w.dst.elem_bytes} B",
             "requests": len(reqs), "tokens": int(sum(n for n, _, _ in reqs)),
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
-            "vec_bytes": info["vec_bytes"],
+            "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
+            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "occupancy",
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on the main stream "
                       "records the layer's event; kvx_push_layer on a priority side stream waits for it; a plan is "

@@ -28,6 +28,7 @@ struct CopyArgs {
     const uint8_t *const *src_base;   // [n_layers][n_planes][src_shards] device pointers
     uint8_t *const *dst_base;         // [n_layers][n_planes][dst_shards]
     int32_t *err;                     // [n_layers] error words, set only when a tile is out of bounds
+    int64_t n_tiles;                  // tiles per (layer, plane)
     int64_t src_buf_bytes;
     int64_t dst_buf_bytes;
     int64_t src_pitch;                // producer row bytes
@@ -73,8 +74,15 @@ void pool_free(void *ptr);
 kvx_status aux_stream(cudaStream_t *out);
 
 // Launches the tile copy for layers [args.layer0, args.layer0 + n_layers) (kvx_push.cu).
-cudaError_t launch_copy(const CopyArgs &args, int64_t n_tiles, int32_t n_layers, int32_t vec, bool strided,
-                        int32_t threads, cudaStream_t stream);
+struct LaunchShape {
+    int32_t kernel;        // KVX_KERNEL_TILE / PERSIST / BULK (resolved)
+    int32_t vec;
+    int32_t strided;
+    int32_t threads;
+    int32_t tile_bytes;    // bulk: bytes per stage
+    int32_t ctas_per_sm;   // 0: occupancy limit
+};
+cudaError_t launch_copy(const CopyArgs &args, int32_t n_layers, const LaunchShape &shape, cudaStream_t stream);
 
 }  // namespace kvx
 
@@ -93,6 +101,8 @@ struct kvx_plan_s {
     int32_t tile_bytes = 16384;
     int32_t threads = 256;
     int32_t flags = 0;                         // KVX_PLAN_* bits
+    int32_t kernel = 0;                        // resolved KVX_KERNEL_*
+    int32_t ctas_per_sm = 0;
     int64_t n_tiles = 0;                       // per (layer, plane)
     int64_t bytes_per_layer = 0;
     std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans

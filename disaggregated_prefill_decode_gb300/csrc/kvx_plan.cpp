@@ -195,12 +195,16 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
     if (st) return st;
     if (opts) {
-        for (int i = 0; i < 5; ++i)
+        for (int i = 0; i < 3; ++i)
             if (opts->reserved[i]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
         if (opts->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
         if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
         if (opts->threads) pl->threads = opts->threads;
         pl->flags = opts->flags;
+        if (opts->kernel < 0 || opts->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", opts->kernel);
+        if (opts->ctas_per_sm < 0 || opts->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
+        pl->kernel = opts->kernel;
+        pl->ctas_per_sm = opts->ctas_per_sm;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
@@ -214,8 +218,17 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     return KVX_OK;
 }
 
+// Bulk copies need 16-byte aligned addresses and sizes and a stage that fits shared memory.
+static int32_t resolve_kernel(const kvx_plan_s *pl) {
+    const int32_t k = pl->kernel == KVX_KERNEL_AUTO ? KVX_KERNEL_PERSIST : pl->kernel;
+    if (k == KVX_KERNEL_BULK && (pl->strided || pl->vec != 16 || pl->tile_bytes > (48 << 10)))
+        return KVX_KERNEL_PERSIST;
+    return k;
+}
+
 void finish_plan_shape(kvx_plan_s *pl) {
     pl->vec = vector_bytes(pl, shard_pairs(pl->src, pl->dst));
+    pl->kernel = resolve_kernel(pl);
     int64_t toks = 0;
     for (int32_t n : pl->run_ntok) toks += n;
     pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
@@ -331,6 +344,8 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->n_planes = pl->src.n_planes;
     out->width = pl->width;
     out->tile_bytes = pl->tile_bytes;
+    out->kernel = pl->kernel;
+    out->threads = pl->kernel == KVX_KERNEL_BULK ? 32 : pl->threads;
     return KVX_OK;
 }
 

@@ -10,7 +10,9 @@
 
 #include <chrono>
 #include <cstring>
+#include <algorithm>
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <thread>
 
@@ -29,28 +31,21 @@ template <> struct VecType<1> { using T = uint8_t; };
 
 constexpr int kUnroll = 4;
 
-// One CTA per (tile, plane, layer). Every thread reads the 32-byte tile descriptor (a broadcast
-// load), resolves the (layer, plane, shard) buffer bases, then copies with VEC-byte integer vectors,
-// kUnroll independent loads in flight per thread before their stores. Values are never converted.
-template <int VEC, bool STRIDED>
-__global__ void __launch_bounds__(1024) kvx_copy_tiles(CopyArgs a) {
-    using V = typename VecType<VEC>::T;
-    const TileDesc t = a.tiles[blockIdx.x];
-    const int32_t layer = a.layer0 + (int32_t)blockIdx.z;
-    const int64_t lp = (int64_t)layer * a.n_planes + blockIdx.y;
-
-    // Bounds guard: host-built tables are validated already; device-built ones are checked here.
-    // An out-of-bounds tile sets the layer's error word and is skipped (no trap).
+// Host-validated tables never fail this guard; device-built ones are checked here. An out-of-bounds
+// tile is skipped and its layer's error word set (no trap).
+template <bool STRIDED>
+__device__ __forceinline__ bool tile_in_bounds(const TileDesc &t, const CopyArgs &a) {
     const int64_t src_end = STRIDED ? t.src_off + (int64_t)(t.n - 1) * a.src_pitch + a.width : t.src_off + t.n;
     const int64_t dst_end = STRIDED ? t.dst_off + (int64_t)(t.n - 1) * a.dst_pitch + a.width : t.dst_off + t.n;
-    if (t.n <= 0 || t.src_off < 0 || t.dst_off < 0 || src_end > a.src_buf_bytes || dst_end > a.dst_buf_bytes ||
-        t.s_shard < 0 || t.s_shard >= a.src_shards || t.d_shard < 0 || t.d_shard >= a.dst_shards) {
-        if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
-        return;
-    }
-    const uint8_t *src = a.src_base[lp * a.src_shards + t.s_shard] + t.src_off;
-    uint8_t *dst = a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off;
+    return t.n > 0 && t.src_off >= 0 && t.dst_off >= 0 && src_end <= a.src_buf_bytes && dst_end <= a.dst_buf_bytes &&
+           t.s_shard >= 0 && t.s_shard < a.src_shards && t.d_shard >= 0 && t.d_shard < a.dst_shards;
+}
 
+// Copies one tile with VEC-byte integer vectors, kUnroll independent loads in flight per thread
+// before their stores. Values are never converted.
+template <int VEC, bool STRIDED>
+__device__ __forceinline__ void copy_tile(const TileDesc &t, const uint8_t *src, uint8_t *dst, const CopyArgs &a) {
+    using V = typename VecType<VEC>::T;
     if (!STRIDED) {
         const V *s = reinterpret_cast<const V *>(src);
         V *d = reinterpret_cast<V *>(dst);
@@ -98,26 +93,273 @@ __global__ void __launch_bounds__(1024) kvx_copy_tiles(CopyArgs a) {
     }
 }
 
+// Work item w of a launch: tile w % n_tiles of plane (w / n_tiles) % n_planes of layer
+// layer0 + w / (n_tiles * n_planes). Consecutive items are consecutive tiles of one buffer pair.
+__device__ __forceinline__ void decode_item(const CopyArgs &a, int64_t w, int64_t *tile, int32_t *layer, int64_t *lp) {
+    const int64_t rest = w / a.n_tiles;
+    *tile = w - rest * a.n_tiles;
+    const int32_t plane = (int32_t)(rest % a.n_planes);
+    *layer = a.layer0 + (int32_t)(rest / a.n_planes);
+    *lp = (int64_t)(*layer) * a.n_planes + plane;
+}
+
+// KVX_KERNEL_TILE: one CTA per (tile, plane, layer).
+template <int VEC, bool STRIDED>
+__global__ void __launch_bounds__(1024) kvx_copy_tiles(CopyArgs a) {
+    const TileDesc t = a.tiles[blockIdx.x];
+    const int32_t layer = a.layer0 + (int32_t)blockIdx.z;
+    const int64_t lp = (int64_t)layer * a.n_planes + blockIdx.y;
+    if (!tile_in_bounds<STRIDED>(t, a)) {
+        if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
+        return;
+    }
+    copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
+                            a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
+}
+
+// KVX_KERNEL_PERSIST: a resident grid walks the work items; each CTA loads the next item's
+// descriptor before copying the current one, so the descriptor latency hides behind the copy.
+template <int VEC, bool STRIDED>
+__global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_work) {
+    int64_t w = blockIdx.x;
+    if (w >= n_work) return;
+    TileDesc next = a.tiles[w % a.n_tiles];
+    for (; w < n_work; w += gridDim.x) {
+        const TileDesc t = next;
+        if (w + gridDim.x < n_work) next = a.tiles[(w + gridDim.x) % a.n_tiles];
+        int64_t tile, lp;
+        int32_t layer;
+        decode_item(a, w, &tile, &layer, &lp);
+        if (!tile_in_bounds<STRIDED>(t, a)) {
+            if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
+            continue;
+        }
+        copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
+                                a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// KVX_KERNEL_BULK: bulk asynchronous copies through shared memory (contiguous, 16-byte aligned).
+// One thread per CTA drives a ring of kBulkStages stages: the load of an item lands in its stage
+// and completes the stage's mbarrier (transaction count = bytes); the thread then issues the bulk
+// store of that stage and, once the store before it has finished reading its stage, the load of a
+// later item into that freed stage. Waits are bounded by the global timer.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kBulkStages = 4;
+constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// The single arrival of a stage's phase, announcing `bytes` of incoming transactions (0 for none).
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for a stage's phase; false when the deadline passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_test(bar, parity))
+        if (global_ns() - t0 > kBulkWaitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(void *stage, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(stage)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *stage, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(stage)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+struct BulkItem {
+    const uint8_t *src;
+    uint8_t *dst;
+    uint32_t bytes;    // 0: skipped (out of bounds or misaligned)
+    int32_t layer;
+};
+
+__device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int32_t stage_bytes) {
+    int64_t tile, lp;
+    BulkItem it;
+    decode_item(a, w, &tile, &it.layer, &lp);
+    const TileDesc t = a.tiles[tile];
+    it.src = nullptr;
+    it.dst = nullptr;
+    it.bytes = 0;
+    if (!tile_in_bounds<false>(t, a) || t.n > stage_bytes) {
+        if (t.n != 0) atomicOr(&a.err[it.layer], 1);
+        return it;
+    }
+    it.src = a.src_base[lp * a.src_shards + t.s_shard] + t.src_off;
+    it.dst = a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off;
+    if ((((uintptr_t)it.src) | ((uintptr_t)it.dst) | (uintptr_t)t.n) & 15) {
+        atomicOr(&a.err[it.layer], 1);
+        return it;
+    }
+    it.bytes = (uint32_t)t.n;
+    return it;
+}
+
+__global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, int32_t stage_bytes) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t bar[kBulkStages];
+    if (threadIdx.x != 0) return;
+    for (int s = 0; s < kBulkStages; ++s) mbar_init(&bar[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+    const int64_t n_mine = (int64_t)blockIdx.x < n_work ? (n_work - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    BulkItem items[kBulkStages];
+    // item i of this CTA is work item blockIdx.x + i * gridDim.x, in stage i % kBulkStages
+    auto issue = [&](int64_t i) {
+        const int s = (int)(i % kBulkStages);
+        items[s] = bulk_item(a, blockIdx.x + i * gridDim.x, stage_bytes);
+        mbar_arrive_expect(&bar[s], items[s].bytes);
+        if (items[s].bytes) bulk_load(ring + (size_t)s * stage_bytes, items[s].src, items[s].bytes, &bar[s]);
+    };
+    int64_t issued = 0;
+    for (; issued < n_mine && issued < kBulkStages - 1; ++issued) issue(issued);
+    bool timed_out = false;
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = (int)(i % kBulkStages);
+        if (!mbar_wait(&bar[s], (uint32_t)((i / kBulkStages) & 1))) {
+            atomicOr(&a.err[items[s].layer], 2);
+            timed_out = true;
+            break;
+        }
+        if (items[s].bytes) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            bulk_store(items[s].dst, ring + (size_t)s * stage_bytes, items[s].bytes);
+        }
+        bulk_commit();
+        if (issued < n_mine) {
+            bulk_wait_read_1();   // the store issued one item ago has read the stage the next load reuses
+            issue(issued);
+            ++issued;
+        }
+    }
+    if (timed_out) {
+        // give every load still in flight a bounded chance to land before the ring goes away
+        for (int64_t j = 0; j < kBulkStages && j < issued; ++j) {
+            const int64_t i = issued - 1 - j;
+            mbar_wait(&bar[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1));
+        }
+    }
+    bulk_wait_all();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch
+// ------------------------------------------------------------------------------------------------
+
 template <int VEC>
-static cudaError_t launch_vec(const CopyArgs &a, dim3 grid, int threads, bool strided, cudaStream_t st) {
-    if (strided)
-        kvx_copy_tiles<VEC, true><<<grid, threads, 0, st>>>(a);
-    else
-        kvx_copy_tiles<VEC, false><<<grid, threads, 0, st>>>(a);
+static cudaError_t launch_vec(const CopyArgs &a, int32_t n_layers, const LaunchShape &sh, unsigned grid_persist,
+                              cudaStream_t st) {
+    const int64_t n_work = a.n_tiles * a.n_planes * n_layers;
+    if (sh.kernel == KVX_KERNEL_TILE) {
+        const dim3 grid((unsigned)a.n_tiles, (unsigned)a.n_planes, (unsigned)n_layers);
+        if (sh.strided) kvx_copy_tiles<VEC, true><<<grid, sh.threads, 0, st>>>(a);
+        else kvx_copy_tiles<VEC, false><<<grid, sh.threads, 0, st>>>(a);
+    } else {
+        if (sh.strided) kvx_copy_persist<VEC, true><<<grid_persist, sh.threads, 0, st>>>(a, n_work);
+        else kvx_copy_persist<VEC, false><<<grid_persist, sh.threads, 0, st>>>(a, n_work);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy(const CopyArgs &a, int64_t n_tiles, int32_t n_layers, int32_t vec, bool strided,
-                        int32_t threads, cudaStream_t st) {
-    if (n_tiles <= 0 || n_layers <= 0) return cudaSuccess;
-    const dim3 grid((unsigned)n_tiles, (unsigned)a.n_planes, (unsigned)n_layers);
+// Resident CTAs per SM for a kernel (occupancy query), times the SM count; cached per key.
+static std::mutex g_grid_mu;
+static std::map<std::tuple<int, const void *, int, int>, int> g_resident;
+
+static cudaError_t resident_grid(const void *fn, int threads, int smem, int per_sm_cap, int *grid) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    const auto key = std::make_tuple(dev, fn, threads, smem);
+    auto it = g_resident.find(key);
+    if (it == g_resident.end()) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (smem > 48 * 1024) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+        if (e != cudaSuccess) return e;
+        it = g_resident.emplace(key, sms * 1000 + std::max(per_sm, 1)).first;
+    }
+    const int sms = it->second / 1000, per_sm = it->second % 1000;
+    *grid = sms * (per_sm_cap > 0 ? std::min(per_sm_cap, per_sm) : per_sm);
+    return cudaSuccess;
+}
+
+template <int VEC>
+static const void *persist_fn(bool strided) {
+    return strided ? (const void *)kvx_copy_persist<VEC, true> : (const void *)kvx_copy_persist<VEC, false>;
+}
+
+cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &sh, cudaStream_t st) {
+    if (a.n_tiles <= 0 || n_layers <= 0) return cudaSuccess;
+    const int64_t n_work = a.n_tiles * a.n_planes * n_layers;
     count_launch();
-    switch (vec) {
-        case 16: return launch_vec<16>(a, grid, threads, strided, st);
-        case 8: return launch_vec<8>(a, grid, threads, strided, st);
-        case 4: return launch_vec<4>(a, grid, threads, strided, st);
-        case 2: return launch_vec<2>(a, grid, threads, strided, st);
-        default: return launch_vec<1>(a, grid, threads, strided, st);
+    int grid = 0;
+    cudaError_t e;
+    if (sh.kernel == KVX_KERNEL_BULK) {
+        const int smem = kBulkStages * sh.tile_bytes;
+        e = resident_grid((const void *)kvx_copy_bulk, 32, smem, sh.ctas_per_sm, &grid);
+        if (e != cudaSuccess) return e;
+        kvx_copy_bulk<<<(unsigned)std::min<int64_t>(grid, n_work), 32, smem, st>>>(a, n_work, sh.tile_bytes);
+        return cudaGetLastError();
+    }
+    if (sh.kernel == KVX_KERNEL_PERSIST) {
+        const void *fn = sh.vec == 16 ? persist_fn<16>(sh.strided) : sh.vec == 8 ? persist_fn<8>(sh.strided)
+                       : sh.vec == 4 ? persist_fn<4>(sh.strided) : sh.vec == 2 ? persist_fn<2>(sh.strided)
+                       : persist_fn<1>(sh.strided);
+        e = resident_grid(fn, sh.threads, 0, sh.ctas_per_sm, &grid);
+        if (e != cudaSuccess) return e;
+        grid = (int)std::min<int64_t>(grid, n_work);
+    }
+    switch (sh.vec) {
+        case 16: return launch_vec<16>(a, n_layers, sh, (unsigned)grid, st);
+        case 8: return launch_vec<8>(a, n_layers, sh, (unsigned)grid, st);
+        case 4: return launch_vec<4>(a, n_layers, sh, (unsigned)grid, st);
+        case 2: return launch_vec<2>(a, n_layers, sh, (unsigned)grid, st);
+        default: return launch_vec<1>(a, n_layers, sh, (unsigned)grid, st);
     }
 }
 
@@ -200,6 +442,7 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.src_base = reinterpret_cast<const uint8_t *const *>(base + pl->off_src);
     a.dst_base = reinterpret_cast<uint8_t *const *>(base + pl->off_dst);
     a.err = reinterpret_cast<int32_t *>(base + pl->off_err);
+    a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();
     a.src_pitch = pl->src.row_bytes();
@@ -287,7 +530,8 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
             return cuda_fail(e, "cudaEventRecord(push start)");
         }
     }
-    e = launch_copy(plan_copy_args(pl, l0), pl->n_tiles, l1 - l0, pl->vec, pl->strided != 0, pl->threads, stream);
+    const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm};
+    e = launch_copy(plan_copy_args(pl, l0), l1 - l0, shape, stream);
     if (e != cudaSuccess) {
         if (start) pl->free_events.push_back(start);
         for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;

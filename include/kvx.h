@@ -101,8 +101,19 @@ typedef struct kvx_plan_opts {
     int32_t tile_bytes;       /* bytes one CTA copies per tile (default 16384; multiple of 16)  */
     int32_t threads;          /* threads per CTA (default 256; multiple of 32, <= 1024)         */
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
-    int32_t reserved[5];      /* must be 0 */
+    int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
+    int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM (0: occupancy limit)   */
+    int32_t reserved[3];      /* must be 0 */
 } kvx_plan_opts;
+
+/* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
+ * loading the next descriptor while it copies the current tile. BULK: the same walk with the bulk
+ * asynchronous copy engine (global -> shared -> global through a ring of mbarrier-tracked stages);
+ * contiguous plans with 16-byte alignment only, others fall back to PERSIST. */
+#define KVX_KERNEL_AUTO 0
+#define KVX_KERNEL_TILE 1
+#define KVX_KERNEL_PERSIST 2
+#define KVX_KERNEL_BULK 3
 
 /* Record the device time of every push (CUDA events around each launch); read with
  * kvx_plan_push_times after kvx_sync. This is the per-layer KV transfer time that the
@@ -156,6 +167,8 @@ typedef struct kvx_plan_info {
     int32_t n_planes;
     int32_t width;               /* strided plans: bytes per row segment */
     int32_t tile_bytes;
+    int32_t kernel;              /* the KVX_KERNEL_* the pushes use */
+    int32_t threads;
 } kvx_plan_info;
 kvx_status kvx_plan_get_info(kvx_plan_t plan, kvx_plan_info *out);
 

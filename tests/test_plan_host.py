@@ -221,3 +221,25 @@ def test_timing_flag_validation():
     timed = kvx.kvx_plan_ex(sp, dp, [ok], {"flags": kvx.KVX_PLAN_TIMING})
     assert len(kvx.kvx_plan_push_times(timed)) == 0          # nothing synced yet
     kvx.kvx_plan_destroy(timed)
+
+
+def test_kernel_resolution():
+    g = PoolGeom(1, 2, 1, 8, 128, 2, 16, 8)
+    sp, dp = pools(g, g)
+    ok = (20, [0, 1], [2, 3])
+    def kern(opts, a=sp, b=dp):
+        p = kvx.kvx_plan_ex(a, b, [ok], opts)
+        k = kvx.kvx_plan_get_info(p)["kernel"]
+        kvx.kvx_plan_destroy(p)
+        return k
+    assert kern({}) == kvx.KVX_KERNEL_PERSIST
+    assert kern({"kernel": kvx.KVX_KERNEL_TILE}) == kvx.KVX_KERNEL_TILE
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK}) == kvx.KVX_KERNEL_BULK
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": 65536}) == kvx.KVX_KERNEL_PERSIST   # stage too big
+    sp8 = kvx.Pool(g, [(1 << 40) + 8, (1 << 40) + 8 + (1 << 30)])
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK}, sp8, dp) == kvx.KVX_KERNEL_PERSIST                  # 8-byte aligned
+    gs, gd = PoolGeom(1, 2, 2, 4, 128, 2, 16, 8), PoolGeom(1, 2, 1, 8, 128, 2, 16, 8)
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK}, fake_pool(gs, 1 << 40), fake_pool(gd, 1 << 44)) == \
+        kvx.KVX_KERNEL_PERSIST                                                                       # strided
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"kernel": 9}))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"ctas_per_sm": 99}))

@@ -68,15 +68,29 @@ def test_tiny_all_layers():
     run_workload(w, range(w.src.n_layers))
 
 
+KERNELS = {"tile": 1, "persist": 2, "bulk": 3}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("make", [
     lambda: kvx_inputs.qwen3_32b_single(n_layers=2),
     lambda: kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=6),
     lambda: kvx_inputs.tp4_to_tp1_remap(n_layers=2, n_requests=3),
 ], ids=["qwen3_32b_single", "qwen3_32b_batched", "tp4_to_tp1_remap"])
-def test_reduced_workloads_all_layers(make):
+def test_reduced_workloads_all_layers(make, kernel):
     w = make()
-    info = run_workload(w, range(w.src.n_layers))
+    info = run_workload(w, range(w.src.n_layers), opts={"kernel": KERNELS[kernel]})
     assert info["vec_bytes"] == 16
+    want = KERNELS[kernel] if not (kernel == "bulk" and info["strided"]) else KERNELS["persist"]
+    assert info["kernel"] == want
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+@pytest.mark.parametrize("tile_bytes,ctas", [(4096, 0), (16384, 2), (49152, 1)])
+def test_kernels_launch_shapes(kernel, tile_bytes, ctas):
+    w = kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=4, len_range=(100, 2000))
+    run_workload(w, range(2), opts={"kernel": KERNELS[kernel], "tile_bytes": tile_bytes, "ctas_per_sm": ctas})
+    run_workload(w, range(2), opts={"kernel": KERNELS[kernel], "tile_bytes": tile_bytes}, per_layer=False)
 
 
 @pytest.mark.parametrize("name", ["qwen3_32b_single", "qwen3_32b_batched", "tp4_to_tp1_remap"])
@@ -110,8 +124,9 @@ GEOMS = {
 }
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("name", sorted(GEOMS))
-def test_geometry_sweep(name):
+def test_geometry_sweep(name, kernel):
     from helpers import random_requests
     sg, dg = GEOMS[name]
     rng = np.random.default_rng(zlib.crc32(name.encode()))
@@ -119,7 +134,7 @@ def test_geometry_sweep(name):
     kind = "fp8_bytes" if sg.elem_bytes == 1 else "bf16_normal"
     src, _ = device_pool(sg, kind, seed=7)
     dst, _ = device_pool(dg, "canary_" + kind)
-    plan = kvx.kvx_plan(kvx.Pool(sg, src), kvx.Pool(dg, dst), reqs)
+    plan = kvx.kvx_plan_ex(kvx.Pool(sg, src), kvx.Pool(dg, dst), reqs, {"kernel": KERNELS[kernel]})
     assert push_all_layers(plan, sg.n_layers) == kvx.KVX_OK
     per = dg.n_planes * dg.n_shards
     check_layers(sg, src, dg, dst, lambda l: [canary_host(dg, kind) for _ in range(per)], reqs, range(sg.n_layers))
