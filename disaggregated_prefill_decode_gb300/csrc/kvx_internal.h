@@ -103,6 +103,9 @@ struct kvx_plan_s {
     int32_t flags = 0;                         // KVX_PLAN_* bits
     int32_t kernel = 0;                        // resolved KVX_KERNEL_*
     int32_t ctas_per_sm = 0;
+    int32_t lanes = 2;                         // internal streams pushes fan out over
+    int32_t next_lane = 0;
+    cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
     int64_t n_tiles = 0;                       // per (layer, plane)
     int64_t bytes_per_layer = 0;
     std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans
@@ -120,7 +123,7 @@ struct kvx_plan_s {
     // pushes issued and not yet confirmed by kvx_sync
     std::vector<kvx::PendingPush> pending;
     std::vector<cudaEvent_t> free_events;
-    std::vector<float> push_us;                // timing plans: durations confirmed by the last sync
+    std::vector<float> push_start_us, push_end_us;   // timing plans: confirmed by the last sync
     std::vector<int32_t> layer_state;          // kvx_layer_state per layer
     std::vector<uint8_t> inject;               // host fault injection armed, per layer
     std::vector<uint8_t> injected_pending;     // injected failure waiting for sync, per layer

@@ -195,7 +195,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
     if (st) return st;
     if (opts) {
-        for (int i = 0; i < 3; ++i)
+        for (int i = 0; i < 2; ++i)
             if (opts->reserved[i]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
         if (opts->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
         if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
@@ -203,8 +203,10 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         pl->flags = opts->flags;
         if (opts->kernel < 0 || opts->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", opts->kernel);
         if (opts->ctas_per_sm < 0 || opts->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
+        if (opts->lanes < 0 || opts->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
         pl->kernel = opts->kernel;
         pl->ctas_per_sm = opts->ctas_per_sm;
+        if (opts->lanes) pl->lanes = opts->lanes;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
@@ -346,6 +348,8 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->tile_bytes = pl->tile_bytes;
     out->kernel = pl->kernel;
     out->threads = pl->kernel == KVX_KERNEL_BULK ? 32 : pl->threads;
+    out->lanes = pl->lanes;
+    out->reserved = 0;
     return KVX_OK;
 }
 
@@ -356,11 +360,14 @@ kvx_status kvx_plan_tiles(kvx_plan_t pl, int64_t *n_tiles, const void **tiles) {
     return KVX_OK;
 }
 
-kvx_status kvx_plan_push_times(kvx_plan_t pl, float *out_us, int32_t cap, int32_t *n) {
-    if (!pl || !n || (cap > 0 && !out_us)) return fail(KVX_EINVAL, "NULL argument");
+kvx_status kvx_plan_push_times(kvx_plan_t pl, float *start_us, float *end_us, int32_t cap, int32_t *n) {
+    if (!pl || !n || (cap > 0 && (!start_us || !end_us))) return fail(KVX_EINVAL, "NULL argument");
     if (!(pl->flags & KVX_PLAN_TIMING)) return fail(KVX_EINVAL, "plan was built without KVX_PLAN_TIMING");
-    *n = (int32_t)pl->push_us.size();
-    for (int32_t i = 0; i < *n && i < cap; ++i) out_us[i] = pl->push_us[i];
+    *n = (int32_t)pl->push_start_us.size();
+    for (int32_t i = 0; i < *n && i < cap; ++i) {
+        start_us[i] = pl->push_start_us[i];
+        end_us[i] = pl->push_end_us[i];
+    }
     return KVX_OK;
 }
 

@@ -370,6 +370,28 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
 static std::mutex g_dev_mu;
 static std::map<int, cudaMemPool_t> g_pools;
 static std::map<int, cudaStream_t> g_aux;
+static std::map<int, std::vector<cudaStream_t>> g_lanes;
+
+// Lane `i` of the current device: a non-blocking stream at the device's highest priority, created
+// on first use and kept for the life of the process.
+static kvx_status lane_stream(int32_t i, cudaStream_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    std::vector<cudaStream_t> &v = g_lanes[dev];
+    while ((int32_t)v.size() <= i) {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetStreamPriorityRange");
+        cudaStream_t s;
+        e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate(lane)");
+        v.push_back(s);
+    }
+    *out = v[i];
+    return KVX_OK;
+}
 
 static cudaError_t device_pool(int dev, cudaMemPool_t *out) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -516,6 +538,22 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
     kvx_status st = ensure_device(pl, stream);
     if (st) return st;
     cudaError_t e;
+    if (pl->lanes > 1) {
+        // fork: the lane waits for everything already on the caller's stream (the upload included)
+        if (!pl->fork_evt) {
+            e = cudaEventCreateWithFlags(&pl->fork_evt, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(fork)");
+        }
+        e = cudaEventRecord(pl->fork_evt, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+        cudaStream_t lane = nullptr;
+        st = lane_stream(pl->next_lane, &lane);
+        if (st) return st;
+        pl->next_lane = (pl->next_lane + 1) % pl->lanes;
+        e = cudaStreamWaitEvent(lane, pl->fork_evt, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fork)");
+        stream = lane;
+    }
     if (ready) {
         e = cudaStreamWaitEvent(stream, ready, 0);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(ready)");
@@ -600,16 +638,22 @@ kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {
         if (e != cudaSuccess) return cuda_fail(e, "clearing push error words");
     }
     bool failed = false;
-    pl->push_us.clear();
+    pl->push_start_us.clear();
+    pl->push_end_us.clear();
     for (size_t i = 0; i < sealed; ++i) {
         const PendingPush &p = pl->pending[i];
         if (p.start) {
-            float ms = 0.f;
-            e = cudaEventElapsedTime(&ms, p.start, p.done);
+            float s_ms = 0.f, e_ms = 0.f;
+            e = cudaEventElapsedTime(&s_ms, pl->pending[0].start, p.start);
+            if (e == cudaSuccess) e = cudaEventElapsedTime(&e_ms, pl->pending[0].start, p.done);
             if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime(push)");
-            pl->push_us.push_back(ms * 1000.f);
-            pl->free_events.push_back(p.start);
+            pl->push_start_us.push_back(s_ms * 1000.f);
+            pl->push_end_us.push_back(e_ms * 1000.f);
         }
+    }
+    for (size_t i = 0; i < sealed; ++i) {
+        const PendingPush &p = pl->pending[i];
+        if (p.start) pl->free_events.push_back(p.start);
         for (int32_t l = p.layer_begin; l < p.layer_end; ++l) {
             const bool bad = err[l] != 0 || pl->injected_pending[l];
             pl->layer_state[l] = bad ? KVX_LAYER_FAILED : KVX_LAYER_DONE;
@@ -633,6 +677,7 @@ kvx_status kvx_plan_destroy(kvx_plan_t pl) {
         if (p.start) cudaEventDestroy(p.start);
     }
     for (cudaEvent_t ev : pl->free_events) cudaEventDestroy(ev);
+    if (pl->fork_evt) cudaEventDestroy(pl->fork_evt);
     if (pl->upload_evt) {
         cudaEventSynchronize(pl->upload_evt);
         cudaEventDestroy(pl->upload_evt);

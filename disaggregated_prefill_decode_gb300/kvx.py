@@ -38,7 +38,7 @@ class kvx_request(ctypes.Structure):
 
 class kvx_plan_opts(ctypes.Structure):
     _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("flags", c_i32), ("kernel", c_i32), ("ctas_per_sm", c_i32),
-                ("reserved", c_i32 * 3)]
+                ("lanes", c_i32), ("reserved", c_i32 * 2)]
 
 
 KVX_PLAN_TIMING = 1
@@ -48,7 +48,7 @@ KVX_KERNEL_AUTO, KVX_KERNEL_TILE, KVX_KERNEL_PERSIST, KVX_KERNEL_BULK = range(4)
 class kvx_plan_info(ctypes.Structure):
     _fields_ = [("n_runs", c_i64), ("n_tiles", c_i64), ("bytes_per_layer", c_i64), ("vec_bytes", c_i32),
                 ("strided", c_i32), ("n_layers", c_i32), ("n_planes", c_i32), ("width", c_i32),
-                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32)]
+                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("reserved", c_i32)]
 
 
 class kvx_match_result(ctypes.Structure):
@@ -74,7 +74,7 @@ _sig = {
     "kvx_push_layers": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp]),
     "kvx_sync": (c_i32, [c_vp, c_i64]),
     "kvx_plan_layer_states": (c_i32, [c_vp, _P(c_i32), c_i32]),
-    "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), c_i32, _P(c_i32)]),
+    "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), _P(ctypes.c_float), c_i32, _P(c_i32)]),
     "kvx_plan_inject_failure": (c_i32, [c_vp, c_i32]),
     "kvx_plan_destroy": (c_i32, [c_vp]),
     "kvx_status_str": (ctypes.c_char_p, [c_i32]),
@@ -219,7 +219,8 @@ def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] =
     carr, n, _keep = _requests(requests)
     out = c_vp()
     o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0)), int(opts.get("flags", 0)),
-                      int(opts.get("kernel", 0)), int(opts.get("ctas_per_sm", 0))) if opts else None
+                      int(opts.get("kernel", 0)), int(opts.get("ctas_per_sm", 0)), int(opts.get("lanes", 0))) \
+        if opts else None
     st = _lib.kvx_plan_ex(ctypes.byref(src.struct), ctypes.byref(dst.struct), carr, n,
                           ctypes.byref(o) if o is not None else None, ctypes.byref(out))
     _check(st, "kvx_plan")
@@ -272,13 +273,15 @@ def kvx_sync(plan, timeout_us: int = -1) -> int:
     return st
 
 
-def kvx_plan_push_times(plan, cap: int = 4096) -> np.ndarray:
-    """Device microseconds of each push confirmed by the last kvx_sync (timing plans)."""
-    out = np.zeros(cap, np.float32)
+def kvx_plan_push_times(plan, cap: int = 4096) -> tuple:
+    """(start_us, end_us) of each push confirmed by the last kvx_sync, relative to the first one's
+    start (timing plans)."""
+    s, e = np.zeros(cap, np.float32), np.zeros(cap, np.float32)
     n = c_i32()
-    _check(_lib.kvx_plan_push_times(_h(plan), out.ctypes.data_as(_P(ctypes.c_float)), cap, ctypes.byref(n)),
-           "kvx_plan_push_times")
-    return out[:min(n.value, cap)].copy()
+    _check(_lib.kvx_plan_push_times(_h(plan), s.ctypes.data_as(_P(ctypes.c_float)), e.ctypes.data_as(_P(ctypes.c_float)),
+                                    cap, ctypes.byref(n)), "kvx_plan_push_times")
+    k = min(n.value, cap)
+    return s[:k].copy(), e[:k].copy()
 
 
 def kvx_plan_layer_states(plan) -> np.ndarray:

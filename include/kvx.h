@@ -103,7 +103,8 @@ typedef struct kvx_plan_opts {
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM (0: occupancy limit)   */
-    int32_t reserved[3];      /* must be 0 */
+    int32_t lanes;            /* internal streams pushes fan out over (0: default 2; 1: none)    */
+    int32_t reserved[2];      /* must be 0 */
 } kvx_plan_opts;
 
 /* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
@@ -115,8 +116,8 @@ typedef struct kvx_plan_opts {
 #define KVX_KERNEL_PERSIST 2
 #define KVX_KERNEL_BULK 3
 
-/* Record the device time of every push (CUDA events around each launch); read with
- * kvx_plan_push_times after kvx_sync. This is the per-layer KV transfer time that the
+/* Record when every push starts and ends on the device (CUDA events around each launch); read
+ * with kvx_plan_push_times after kvx_sync. This is the per-layer KV transfer time that the
  * bidirectional article's prefill-duration breakdown ([P3] "Leistungsdaten", Figs. 4 and 6)
  * separates from recompute time. */
 #define KVX_PLAN_TIMING 1
@@ -169,6 +170,8 @@ typedef struct kvx_plan_info {
     int32_t tile_bytes;
     int32_t kernel;              /* the KVX_KERNEL_* the pushes use */
     int32_t threads;
+    int32_t lanes;
+    int32_t reserved;
 } kvx_plan_info;
 kvx_status kvx_plan_get_info(kvx_plan_t plan, kvx_plan_info *out);
 
@@ -185,11 +188,16 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
  * compute and overlaps layer k+1; [P1] "Threading-Modell": the main loop hands the blocks to a
  * background thread and returns to model execution at once.
  *
- * If `ready` is not NULL the stream first waits for it (cudaStreamWaitEvent). The call only
- * enqueues: it returns before the copy runs. Until kvx_sync returns KVX_OK the producer layer must
+ * The push is ordered after everything already enqueued on `stream` and, if `ready` is not NULL,
+ * after `ready`. The call only enqueues: it returns before the copy runs. Completion is what
+ * kvx_sync reports, not stream order: with lanes > 1 (the default, 2) the copy runs on one of the
+ * library's internal high-priority streams ("lanes", forked from `stream` by an event), so
+ * consecutive pushes of different layers can overlap on the GPU, the head of one hiding the tail
+ * of the previous; work enqueued on `stream` later is not ordered after the copy. With lanes = 1
+ * the copy is enqueued on `stream` itself. Until kvx_sync returns KVX_OK the producer layer must
  * not be rewritten and the consumer layer must not be read. The first push of a plan allocates and
- * uploads its descriptors on `stream`; pushes on other streams wait for that upload. The current
- * device must be the device of the pools and the stream.
+ * uploads its descriptors on `stream`. The current device must be the device of the pools and the
+ * stream.
  * kvx_push_layers does layers [layer_begin, layer_end) in one launch.
  */
 kvx_status kvx_push_layer(kvx_plan_t plan, int32_t layer, cudaStream_t stream, cudaEvent_t ready);
@@ -209,10 +217,11 @@ kvx_status kvx_push_layers(kvx_plan_t plan, int32_t layer_begin, int32_t layer_e
  */
 kvx_status kvx_sync(kvx_plan_t plan, int64_t timeout_us);
 
-/* Plans built with KVX_PLAN_TIMING: device time in microseconds of each push the last completed
- * kvx_sync confirmed, in issue order (out: up to cap entries; *n receives the count). Each time
- * runs from the point the stream passed the push's `ready` wait to the end of its kernel. */
-kvx_status kvx_plan_push_times(kvx_plan_t plan, float *out_us, int32_t cap, int32_t *n);
+/* Plans built with KVX_PLAN_TIMING: for each push the last completed kvx_sync confirmed, in issue
+ * order, its start and end in microseconds relative to the start of the first of them (up to cap
+ * entries each; *n receives the count). A push starts when its stream has passed the push's
+ * `ready` wait and ends with its kernel. Pushes on different lanes may overlap. */
+kvx_status kvx_plan_push_times(kvx_plan_t plan, float *start_us, float *end_us, int32_t cap, int32_t *n);
 
 /* Per-layer states (out: n_layers entries of kvx_layer_state). */
 kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers);

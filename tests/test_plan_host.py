@@ -219,7 +219,8 @@ def test_timing_flag_validation():
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_push_times(plain))
     kvx.kvx_plan_destroy(plain)
     timed = kvx.kvx_plan_ex(sp, dp, [ok], {"flags": kvx.KVX_PLAN_TIMING})
-    assert len(kvx.kvx_plan_push_times(timed)) == 0          # nothing synced yet
+    s, e = kvx.kvx_plan_push_times(timed)
+    assert len(s) == 0 and len(e) == 0                       # nothing synced yet
     kvx.kvx_plan_destroy(timed)
 
 
@@ -243,3 +244,7 @@ def test_kernel_resolution():
         kvx.KVX_KERNEL_PERSIST                                                                       # strided
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"kernel": 9}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"ctas_per_sm": 99}))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"lanes": 9}))
+    p = kvx.kvx_plan(sp, dp, [ok])
+    assert kvx.kvx_plan_get_info(p)["lanes"] == 2
+    kvx.kvx_plan_destroy(p)

@@ -85,6 +85,13 @@ def test_reduced_workloads_all_layers(make, kernel):
     assert info["kernel"] == want
 
 
+@pytest.mark.parametrize("lanes", [1, 2, 5])
+def test_lanes(lanes):
+    w = kvx_inputs.qwen3_32b_batched(n_layers=6, n_requests=4, len_range=(500, 3000))
+    info = run_workload(w, range(6), opts={"lanes": lanes})
+    assert info["lanes"] == lanes
+
+
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("tile_bytes,ctas", [(4096, 0), (16384, 2), (49152, 1)])
 def test_kernels_launch_shapes(kernel, tile_bytes, ctas):
@@ -248,8 +255,9 @@ def test_push_times_of_timing_plan():
     dst, _ = device_pool(w.dst, "canary_" + w.values)
     plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"flags": kvx.KVX_PLAN_TIMING})
     assert push_all_layers(plan, 4) == kvx.KVX_OK
-    t = kvx.kvx_plan_push_times(plan)
-    assert len(t) == 4 and np.all(t > 0) and np.all(t < 1e5)
+    s, e = kvx.kvx_plan_push_times(plan)
+    t = e - s
+    assert len(t) == 4 and np.all(t > 0) and np.all(t < 1e5) and s[0] == 0
     check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
                  range(4))
     kvx.kvx_plan_destroy(plan)
