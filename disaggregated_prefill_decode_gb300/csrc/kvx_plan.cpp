@@ -325,6 +325,32 @@ kvx_status kvx_plan(const kvx_pool *src, const kvx_pool *dst, const kvx_request 
     return kvx_plan_ex(src, dst, reqs, n_reqs, nullptr, out);
 }
 
+kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
+    if (!pl || !o) return fail(KVX_EINVAL, "NULL argument");
+    if (!pl->pending.empty()) return fail(KVX_EINVAL, "pushes are pending; kvx_sync first");
+    if (o->tile_bytes && o->tile_bytes != pl->tile_bytes) return fail(KVX_EINVAL, "tile_bytes is fixed once tiles exist");
+    if (o->reserved[0] || o->reserved[1]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+    if (o->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
+    if (o->kernel < 0 || o->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", o->kernel);
+    if (o->ctas_per_sm < 0 || o->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
+    if (o->lanes < 0 || o->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
+    if (o->threads && (o->threads < 32 || o->threads > 1024 || o->threads % 32))
+        return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
+    if ((o->flags ^ pl->flags) & KVX_PLAN_TIMING) {
+        // events are created with or without timing: drop the pooled ones
+        for (cudaEvent_t ev : pl->free_events) cudaEventDestroy(ev);
+        pl->free_events.clear();
+    }
+    pl->flags = o->flags;
+    if (o->threads) pl->threads = o->threads;
+    pl->ctas_per_sm = o->ctas_per_sm;
+    pl->lanes = o->lanes ? o->lanes : 2;
+    pl->next_lane = 0;
+    pl->kernel = o->kernel;
+    pl->kernel = resolve_kernel(pl);
+    return KVX_OK;
+}
+
 kvx_status kvx_plan_runs(kvx_plan_t pl, int64_t *n_runs, const int32_t **src_row, const int32_t **dst_row,
                          const int32_t **n_tokens) {
     if (!pl || !n_runs) return fail(KVX_EINVAL, "NULL argument");

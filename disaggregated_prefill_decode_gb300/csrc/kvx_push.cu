@@ -370,22 +370,19 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
 static std::mutex g_dev_mu;
 static std::map<int, cudaMemPool_t> g_pools;
 static std::map<int, cudaStream_t> g_aux;
-static std::map<int, std::vector<cudaStream_t>> g_lanes;
+static std::map<std::pair<int, int>, std::vector<cudaStream_t>> g_lanes;
 
-// Lane `i` of the current device: a non-blocking stream at the device's highest priority, created
-// on first use and kept for the life of the process.
-static kvx_status lane_stream(int32_t i, cudaStream_t *out) {
+// Lane `i` for the current device at `priority`: a non-blocking stream created on first use and kept
+// for the life of the process.
+static kvx_status lane_stream(int32_t i, int priority, cudaStream_t *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    std::vector<cudaStream_t> &v = g_lanes[dev];
+    std::vector<cudaStream_t> &v = g_lanes[std::make_pair(dev, priority)];
     while ((int32_t)v.size() <= i) {
-        int least = 0, greatest = 0;
-        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetStreamPriorityRange");
         cudaStream_t s;
-        e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest);
+        e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, priority);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate(lane)");
         v.push_back(s);
     }
@@ -531,7 +528,8 @@ static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
 
 extern "C" {
 
-kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t ready) {
+kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t ready,
+                                 cudaEvent_t done) {
     if (!pl) return fail(KVX_EINVAL, "NULL plan");
     if (l0 < 0 || l1 > pl->src.n_layers || l0 >= l1)
         return fail(KVX_EINVAL, "layer range [%d, %d) outside [0, %d)", l0, l1, pl->src.n_layers);
@@ -546,8 +544,11 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
         }
         e = cudaEventRecord(pl->fork_evt, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+        int prio = 0;
+        e = cudaStreamGetPriority(stream, &prio);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetPriority");
         cudaStream_t lane = nullptr;
-        st = lane_stream(pl->next_lane, &lane);
+        st = lane_stream(pl->next_lane, prio, &lane);
         if (st) return st;
         pl->next_lane = (pl->next_lane + 1) % pl->lanes;
         e = cudaStreamWaitEvent(lane, pl->fork_evt, 0);
@@ -584,6 +585,14 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
         if (start) pl->free_events.push_back(start);
         return cuda_fail(e, "cudaEventRecord(push)");
     }
+    if (done) {
+        e = cudaEventRecord(done, stream);
+        if (e != cudaSuccess) {
+            pl->free_events.push_back(ev);
+            if (start) pl->free_events.push_back(start);
+            return cuda_fail(e, "cudaEventRecord(done)");
+        }
+    }
     pl->pending.push_back({ev, start, l0, l1});
     for (int32_t l = l0; l < l1; ++l) {
         pl->layer_state[l] = KVX_LAYER_PENDING;
@@ -592,8 +601,12 @@ kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t s
     return KVX_OK;
 }
 
+kvx_status kvx_push_layers(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t ready) {
+    return kvx_push_layer_notify(pl, l0, l1, stream, ready, nullptr);
+}
+
 kvx_status kvx_push_layer(kvx_plan_t pl, int32_t layer, cudaStream_t stream, cudaEvent_t ready) {
-    return kvx_push_layers(pl, layer, layer + 1, stream, ready);
+    return kvx_push_layer_notify(pl, layer, layer + 1, stream, ready, nullptr);
 }
 
 kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {

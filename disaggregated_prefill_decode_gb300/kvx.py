@@ -67,11 +67,13 @@ _P = ctypes.POINTER
 _sig = {
     "kvx_plan": (c_i32, [_P(kvx_pool), _P(kvx_pool), _P(kvx_request), c_i32, _P(c_vp)]),
     "kvx_plan_ex": (c_i32, [_P(kvx_pool), _P(kvx_pool), _P(kvx_request), c_i32, _P(kvx_plan_opts), _P(c_vp)]),
+    "kvx_plan_set_opts": (c_i32, [c_vp, _P(kvx_plan_opts)]),
     "kvx_plan_runs": (c_i32, [c_vp, _P(c_i64), _P(_P(c_i32)), _P(_P(c_i32)), _P(_P(c_i32))]),
     "kvx_plan_get_info": (c_i32, [c_vp, _P(kvx_plan_info)]),
     "kvx_plan_tiles": (c_i32, [c_vp, _P(c_i64), _P(c_vp)]),
     "kvx_push_layer": (c_i32, [c_vp, c_i32, c_vp, c_vp]),
     "kvx_push_layers": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp]),
+    "kvx_push_layer_notify": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "kvx_sync": (c_i32, [c_vp, c_i64]),
     "kvx_plan_layer_states": (c_i32, [c_vp, _P(c_i32), c_i32]),
     "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), _P(ctypes.c_float), c_i32, _P(c_i32)]),
@@ -227,6 +229,12 @@ def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] =
     return Plan(out.value, src.geom.n_layers)
 
 
+def kvx_plan_set_opts(plan, opts: dict) -> None:
+    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0)), int(opts.get("flags", 0)),
+                      int(opts.get("kernel", 0)), int(opts.get("ctas_per_sm", 0)), int(opts.get("lanes", 0)))
+    _check(_lib.kvx_plan_set_opts(_h(plan), ctypes.byref(o)), "kvx_plan_set_opts")
+
+
 def kvx_plan_runs(plan) -> tuple:
     n = c_i64()
     s, d, t = _P(c_i32)(), _P(c_i32)(), _P(c_i32)()
@@ -263,6 +271,11 @@ def kvx_push_layer(plan, layer: int, stream=None, ready=None) -> None:
 
 def kvx_push_layers(plan, layer_begin: int, layer_end: int, stream=None, ready=None) -> None:
     _check(_lib.kvx_push_layers(_h(plan), layer_begin, layer_end, _stream(stream), _event(ready)), "kvx_push_layers")
+
+
+def kvx_push_layer_notify(plan, layer_begin: int, layer_end: int, stream, ready, done) -> None:
+    _check(_lib.kvx_push_layer_notify(_h(plan), layer_begin, layer_end, _stream(stream), _event(ready), _event(done)),
+           "kvx_push_layer_notify")
 
 
 def kvx_sync(plan, timeout_us: int = -1) -> int:

@@ -149,6 +149,11 @@ kvx_status kvx_plan(const kvx_pool *src, const kvx_pool *dst, const kvx_request 
 kvx_status kvx_plan_ex(const kvx_pool *src, const kvx_pool *dst, const kvx_request *reqs, int32_t n_reqs,
                        const kvx_plan_opts *opts, kvx_plan_t *out);
 
+/* Changes a plan's launch options before or between pushes (no push pending): flags, kernel,
+ * threads, ctas_per_sm and lanes. tile_bytes must be 0 or the plan's own (its tiles are built).
+ * Useful for plans built by kvx_match_prefix, which takes no options. */
+kvx_status kvx_plan_set_opts(kvx_plan_t plan, const kvx_plan_opts *opts);
+
 /* Introspection for tests: the plan's merged token runs (host arrays owned by the plan, valid
  * until kvx_plan_destroy). Rows are block * block_size + slot on each side. */
 kvx_status kvx_plan_runs(kvx_plan_t plan, int64_t *n_runs, const int32_t **src_row,
@@ -193,7 +198,8 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
  * kvx_sync reports, not stream order: with lanes > 1 (the default, 2) the copy runs on one of the
  * library's internal high-priority streams ("lanes", forked from `stream` by an event), so
  * consecutive pushes of different layers can overlap on the GPU, the head of one hiding the tail
- * of the previous; work enqueued on `stream` later is not ordered after the copy. With lanes = 1
+ * of the previous; work enqueued on `stream` later is not ordered after the copy. Lanes run at the
+ * priority of `stream`, so the caller decides whether pushes yield to its compute. With lanes = 1
  * the copy is enqueued on `stream` itself. Until kvx_sync returns KVX_OK the producer layer must
  * not be rewritten and the consumer layer must not be read. The first push of a plan allocates and
  * uploads its descriptors on `stream`. The current device must be the device of the pools and the
@@ -203,6 +209,13 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
 kvx_status kvx_push_layer(kvx_plan_t plan, int32_t layer, cudaStream_t stream, cudaEvent_t ready);
 kvx_status kvx_push_layers(kvx_plan_t plan, int32_t layer_begin, int32_t layer_end, cudaStream_t stream,
                            cudaEvent_t ready);
+
+/* The same, and `done` (the caller's event, not NULL) is recorded right after the copy, on the
+ * stream that runs it: a per-push completion notification ([P1] "Implementierungsdetails", step 3:
+ * each write carries a completion notification). A consumer stream can wait on it before reading
+ * the layer; kvx_sync still reports failures. */
+kvx_status kvx_push_layer_notify(kvx_plan_t plan, int32_t layer_begin, int32_t layer_end, cudaStream_t stream,
+                                 cudaEvent_t ready, cudaEvent_t done);
 
 /*
  * kvx_sync -- wait for every push issued on the plan since the last completed sync.

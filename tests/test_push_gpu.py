@@ -261,3 +261,41 @@ def test_push_times_of_timing_plan():
     check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
                  range(4))
     kvx.kvx_plan_destroy(plan)
+
+
+def test_notify_event_orders_a_consumer_stream():
+    """A consumer stream that waits on the push's notification event sees the pushed layer."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=3)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    side, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in range(3)]
+    copies = []
+    for layer in range(3):
+        kvx.kvx_push_layer_notify(plan, layer, layer + 1, side, None, done[layer])
+        consumer.wait_event(done[layer])
+        with torch.cuda.stream(consumer):
+            copies.append([b.clone() for b in layer_buffers(w.dst, dst, layer)])
+    consumer.synchronize()
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    for layer in range(3):
+        for a, b in zip(copies[layer], layer_buffers(w.dst, dst, layer)):
+            assert torch.equal(a, b)
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_set_opts_on_existing_plan():
+    w = kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=3)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    kvx.kvx_plan_set_opts(plan, {"flags": kvx.KVX_PLAN_TIMING, "kernel": kvx.KVX_KERNEL_BULK, "lanes": 1})
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    s, e = kvx.kvx_plan_push_times(plan)
+    assert len(s) == 2 and np.all(e > s)
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(2))
+    kvx.kvx_plan_destroy(plan)
