@@ -74,18 +74,24 @@ def measured_peak():
 def ncu_traffic(kernel_key):
     """Per-launch DRAM bytes of the push kernel from a committed ncu summary, if the kernel source is
     unchanged since the capture (else None)."""
-    src = os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", "kvx_push.cu")
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    rec = None
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f).get(kernel_key)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kvx_push_sha") != sha:
+    if not rec or rec.get("csrc_sha") != csrc_sha():
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def csrc_sha():
+    """Hash of the copy kernel and plan builder sources (the ncu counters are valid only for these)."""
+    h = hashlib.sha256()
+    for name in ("kvx_push.cu", "kvx_plan.cpp"):
+        with open(os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def requests(w):
@@ -300,7 +306,7 @@ def run_kvx(args, rank, local_rank, world):
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
             "lanes": info["lanes"],
-            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "occupancy",
+            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or 2,
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
                       "stream "

@@ -102,8 +102,8 @@ struct kvx_plan_s {
     int32_t threads = 256;
     int32_t flags = 0;                         // KVX_PLAN_* bits
     int32_t kernel = 0;                        // resolved KVX_KERNEL_*
-    int32_t ctas_per_sm = 0;
-    int32_t lanes = 2;                         // internal streams pushes fan out over
+    int32_t ctas_per_sm = 2;                   // resident CTAs per SM of persistent kernels
+    int32_t lanes = 4;                         // internal streams pushes fan out over
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
     int64_t n_tiles = 0;                       // per (layer, plane)

@@ -205,7 +205,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         if (opts->ctas_per_sm < 0 || opts->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
         if (opts->lanes < 0 || opts->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
         pl->kernel = opts->kernel;
-        pl->ctas_per_sm = opts->ctas_per_sm;
+        if (opts->ctas_per_sm) pl->ctas_per_sm = opts->ctas_per_sm;
         if (opts->lanes) pl->lanes = opts->lanes;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
@@ -343,8 +343,8 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     }
     pl->flags = o->flags;
     if (o->threads) pl->threads = o->threads;
-    pl->ctas_per_sm = o->ctas_per_sm;
-    pl->lanes = o->lanes ? o->lanes : 2;
+    pl->ctas_per_sm = o->ctas_per_sm ? o->ctas_per_sm : 2;
+    pl->lanes = o->lanes ? o->lanes : 4;
     pl->next_lane = 0;
     pl->kernel = o->kernel;
     pl->kernel = resolve_kernel(pl);

@@ -102,8 +102,10 @@ typedef struct kvx_plan_opts {
     int32_t threads;          /* threads per CTA (default 256; multiple of 32, <= 1024)         */
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
-    int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM (0: occupancy limit)   */
-    int32_t lanes;            /* internal streams pushes fan out over (0: default 2; 1: none)    */
+    int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
+                                 limit (0: default 2, which leaves room for the caller's compute
+                                 and for an overlapping push) */
+    int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
     int32_t reserved[2];      /* must be 0 */
 } kvx_plan_opts;
 
@@ -195,7 +197,7 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
  *
  * The push is ordered after everything already enqueued on `stream` and, if `ready` is not NULL,
  * after `ready`. The call only enqueues: it returns before the copy runs. Completion is what
- * kvx_sync reports, not stream order: with lanes > 1 (the default, 2) the copy runs on one of the
+ * kvx_sync reports, not stream order: with lanes > 1 (the default, 4) the copy runs on one of the
  * library's internal high-priority streams ("lanes", forked from `stream` by an event), so
  * consecutive pushes of different layers can overlap on the GPU, the head of one hiding the tail
  * of the previous; work enqueued on `stream` later is not ordered after the copy. Lanes run at the

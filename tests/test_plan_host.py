@@ -246,5 +246,5 @@ def test_kernel_resolution():
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"ctas_per_sm": 99}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"lanes": 9}))
     p = kvx.kvx_plan(sp, dp, [ok])
-    assert kvx.kvx_plan_get_info(p)["lanes"] == 2
+    assert kvx.kvx_plan_get_info(p)["lanes"] == 4
     kvx.kvx_plan_destroy(p)
