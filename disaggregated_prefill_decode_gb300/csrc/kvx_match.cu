@@ -10,6 +10,8 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
 
 namespace kvx {
@@ -685,3 +687,109 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free variant of the match decision.
+//
+// Serving engines usually reserve nearly all free HBM for their paged KV pools at start-up and
+// allow no device allocation on the request path afterwards: a cudaMalloc there can fail once the
+// pools are carved out, and cudaMalloc / cudaFree may synchronise the device and stall every other
+// stream. kvx_match_prefix_static serves such callers. Its scratch (per-session pushed-block
+// counts, their exclusive scan, scan partials, totals and error bits) is the file-scope array
+// below, sized for at most kStaticMaxSessions sessions per call (about 1 MiB, held by every GPU
+// that loads the library until the process exits).
+// ------------------------------------------------------------------------------------------------
+
+namespace kvx {
+
+constexpr int32_t kStaticMaxSessions = 65536;
+constexpr size_t kStaticPushOff = 0;
+constexpr size_t kStaticSessOff = kStaticPushOff + sizeof(int64_t) * kStaticMaxSessions;
+constexpr size_t kStaticPartOff = kStaticSessOff + sizeof(int64_t) * kStaticMaxSessions;
+constexpr size_t kStaticScalOff = kStaticPartOff + sizeof(int64_t) * (kStaticMaxSessions / kScanThreads);
+constexpr size_t kStaticErrOff = kStaticScalOff + sizeof(int64_t) * 8;
+constexpr size_t kStaticBytes = kStaticErrOff + sizeof(int32_t) * 4;
+
+static __device__ __align__(256) unsigned char g_match_scratch[kStaticBytes];
+
+// In host code g_match_scratch names a host-side stand-in, not device memory: the device address
+// is looked up once per device (with that device current) and cached.
+static std::mutex g_static_mu;
+static std::map<int, unsigned char *> g_static_addr;
+
+static kvx_status static_scratch(unsigned char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    auto it = g_static_addr.find(dev);
+    if (it == g_static_addr.end()) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_match_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(match scratch)");
+        it = g_static_addr.emplace(dev, static_cast<unsigned char *>(p)).first;
+    }
+    *out = it->second;
+    return KVX_OK;
+}
+
+}  // namespace kvx
+
+extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                                              int32_t block_size, kvx_table_t table, const uint64_t *remote_hash,
+                                              const int64_t *rem_off, int32_t threshold, int64_t n_free,
+                                              kvx_match_result *out, cudaStream_t stream) {
+    if (n_sessions < 0 || block_size < 1 || n_free < 0) return fail(KVX_EINVAL, "bad counts");
+    if (n_sessions > kStaticMaxSessions)
+        return fail(KVX_EINVAL, "kvx_match_prefix_static takes at most %d sessions per call (got %d); its scratch "
+                                "is a fixed array", kStaticMaxSessions, n_sessions);
+    if (!table) return fail(KVX_EINVAL, "NULL table");
+    if (n_sessions == 0) return KVX_OK;
+    if (!tokens || !tok_off || !rem_off || !remote_hash || !out) return fail(KVX_EINVAL, "NULL device array");
+    unsigned char *sc = nullptr;
+    kvx_status st = static_scratch(&sc);
+    if (st) return st;
+    int64_t *push_blocks = reinterpret_cast<int64_t *>(sc + kStaticPushOff);
+    int64_t *sess_start = reinterpret_cast<int64_t *>(sc + kStaticSessOff);
+    int64_t *partial = reinterpret_cast<int64_t *>(sc + kStaticPartOff);
+    int64_t *scalars = reinterpret_cast<int64_t *>(sc + kStaticScalOff);
+    int32_t *err = reinterpret_cast<int32_t *>(sc + kStaticErrOff);
+
+    // totals of the two CSR arrays bound every read the kernels make
+    int64_t n_pub = 0, n_tok_total = 0;
+    cudaError_t e = cudaMemcpyAsync(&n_pub, rem_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading rem_off / tok_off");
+    if (n_pub < 0 || n_tok_total < 0) return fail(KVX_EINVAL, "offsets are not CSR offset arrays");
+
+    // the array keeps the previous call's contents: the totals and error bits must start at zero
+    e = cudaMemsetAsync(scalars, 0, sizeof(int64_t) * 8, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t) * 4, stream);
+    if (e == cudaSuccess) {
+        count_launch();
+        kvx_match_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                        table->view(), remote_hash, rem_off, threshold,
+                                                                        n_tok_total, n_pub, out, push_blocks, err);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);
+    if (e == cudaSuccess) {
+        count_launch();
+        kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, sess_start, n_sessions, scalars, n_free,
+                                                                      n_pub, err);
+        e = cudaGetLastError();
+    }
+    int64_t need = 0;
+    int32_t h_err = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&need, scalars, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_err, err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvx_match_prefix_static");
+    if (h_err & ~8) return fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err);
+    if (h_err & 8)
+        return fail(KVX_ENOMEM, "pushing sessions need %lld blocks, free list has %lld", (long long)need,
+                    (long long)n_free);
+    return KVX_OK;
+}

@@ -87,6 +87,7 @@ _sig = {
     "kvx_table_destroy": (c_i32, [c_vp]),
     "kvx_match_prefix": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
                                  _P(kvx_pool), _P(kvx_pool), c_vp, _P(c_vp), c_vp]),
+    "kvx_match_prefix_static": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_i64, c_vp, c_vp]),
     "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp, c_vp]),
     "kvx_version": (ctypes.c_char_p, []),
     "kvx_launch_count": (c_i64, []),
@@ -350,6 +351,17 @@ def kvx_match_prefix(tokens, tok_off, n_sessions: int, block_size: int, table: T
         raise KvxError(st, "kvx_match_prefix")
     n_layers = remote_pool.geom.n_layers if remote_pool else 0
     return st, (Plan(plan.value, n_layers) if plan.value else None)
+
+
+def kvx_match_prefix_static(tokens, tok_off, n_sessions: int, block_size: int, table: Table, remote_hash, rem_off,
+                            recompute_threshold_tokens: int, n_free: int, out, stream=None) -> int:
+    """Allocation-free match decision. Returns KVX_OK or KVX_ENOMEM; other statuses raise."""
+    st = _lib.kvx_match_prefix_static(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, table.handle,
+                                      _ptr(remote_hash), _ptr(rem_off), recompute_threshold_tokens, n_free, _ptr(out),
+                                      _stream(stream))
+    if st not in (KVX_OK, KVX_ENOMEM):
+        raise KvxError(st, "kvx_match_prefix_static")
+    return st
 
 
 def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed: int = 0, stream=None,

@@ -323,6 +323,28 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
                             const kvx_pool *remote_pool, const kvx_pool *local_pool, kvx_match_result *out,
                             kvx_plan_t *out_plan, cudaStream_t stream);
 
+/*
+ * kvx_match_prefix_static -- the per-session decision of kvx_match_prefix (the same
+ * kvx_match_result per session, dst_start included) without allocating any memory. The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate device memory on the
+ * request path, typically serving engines that reserve nearly all free HBM for their paged KV
+ * pools at start-up, where a later cudaMalloc can fail and cudaMalloc / cudaFree may synchronise
+ * the device and stall the other streams.
+ *
+ * Arguments as in kvx_match_prefix; no plan is built (free_blocks is not read, n_free only bounds
+ * the assignment). Its scratch is one fixed array of the library (about 1 MiB on every GPU that
+ * loads it, held until the process exits), sized for at most 65536 sessions per call; more
+ * return KVX_EINVAL. The first call on a device looks up that array's device address (make this
+ * first call before any stream capture). Every call reuses the same array and leaves its contents
+ * behind; the call clears what must start at zero. Calls whose device work overlaps (on different
+ * streams or host threads) race on the array. The call waits for `stream`. Returns KVX_OK, or
+ * KVX_ENOMEM with the decisions written when the pushing sessions need more than n_free blocks.
+ */
+kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                                   int32_t block_size, kvx_table_t local_table, const uint64_t *remote_hash,
+                                   const int64_t *rem_off, int32_t recompute_threshold_tokens, int64_t n_free,
+                                   kvx_match_result *out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------------------------------
  * Synthetic prefill fixture (tests and benchmark only; not part of the transfer path).
  * Occupies `ctas` CTAs of 128 threads with a dependent integer chain of `iters` steps per thread,
