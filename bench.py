@@ -274,13 +274,7 @@ def run_kvx(args, rank, local_rank, world):
     mean_push_ms = sum(push_busy_us) / (K * L) * 1e-3
     raw_push_ms = statistics.fmean(push_raw_us) * 1e-3
     if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        n = torch.tensor([launches], dtype=torch.int64, device=device)
-        dist.all_reduce(n)
-        launches = int(n.item())
-        dist.barrier()
+        elapsed_ms, launches = reduce_over_ranks(elapsed_ms, launches, device)
 
     peak, peak_kind = measured_peak()
     achieved = 2 * info["bytes_per_layer"] / (mean_push_ms * 1e-3) / 1e9
@@ -341,6 +335,18 @@ def run_kvx(args, rank, local_rank, world):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def reduce_over_ranks(elapsed_ms, launches, device):
+    """Replicas: the job's time is the slowest rank's, its launches the sum over ranks."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([launches], dtype=torch.int64, device=device)
+    dist.all_reduce(n)
+    dist.barrier()
+    return float(t.item()), int(n.item())
 
 
 def memcpy_ceiling(torch, device):
