@@ -210,7 +210,7 @@ def run_kvx(args, rank, local_rank, world):
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
     lib = kvx._lib                                    # the C-ABI itself: two calls per layer in the loop
-    push_raw_us, push_busy_us = [], []
+    push_raw_us, push_busy_us, issue_us = [], [], []
 
     def issue():
         """One step's plan and its per-layer issue: fixture then gated push, layer by layer."""
@@ -236,7 +236,10 @@ def run_kvx(args, rank, local_rank, world):
         """n steps, each synced after the next one is issued (one request in flight behind another)."""
         prev = None
         for _ in range(n):
+            h0 = time.perf_counter()
             plan = issue()
+            if timed:
+                issue_us.append((time.perf_counter() - h0) * 1e6)
             if prev is not None:
                 finish(prev, timed)
             prev = plan
@@ -322,6 +325,7 @@ def run_kvx(args, rank, local_rank, world):
         "gpu_launches": launches,
         "clocks": clk,
         "host_wall_s": round(wall, 4),
+        "host_issue_us_per_layer": round(statistics.fmean(issue_us) / L, 3),
     }
     if rank == 0:
         result["memcpy_ceiling"] = memcpy_ceiling(torch, device)

@@ -106,6 +106,8 @@ struct kvx_plan_s {
     int32_t lanes = 4;                         // internal streams pushes fan out over
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
+    cudaStream_t lane_src = nullptr;           // caller stream the cached lanes below were chosen for
+    std::vector<cudaStream_t> lane_cache;      // lanes at that stream's priority
     int64_t n_tiles = 0;                       // per (layer, plane)
     int64_t bytes_per_layer = 0;
     std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans

@@ -18,54 +18,99 @@ namespace kvx {
 
 constexpr uint64_t kFnvBasis = 14695981039346656037ull;
 constexpr uint64_t kFnvPrime = 1099511628211ull;
+static_assert(kFnvPrime == (1ull << 40) + 0x1b3u, "fnv_step splits the prime as 2^40 + 0x1b3");
 
 // ------------------------------------------------------------------------------------------------
 // Hashing
 // ------------------------------------------------------------------------------------------------
 
-// FNV-1a over the 4 octets of one token id, least significant first.
-__device__ __forceinline__ uint64_t fnv_token(uint64_t h, uint32_t v) {
-    h = (h ^ (v & 0xffu)) * kFnvPrime;
-    h = (h ^ ((v >> 8) & 0xffu)) * kFnvPrime;
-    h = (h ^ ((v >> 16) & 0xffu)) * kFnvPrime;
-    h = (h ^ (v >> 24)) * kFnvPrime;
-    return h;
+// One FNV-1a step on the hash held as two 32-bit halves. The prime is 2^40 + 0x1b3, so
+// (hi:lo ^ b) * prime mod 2^64 = hi' : lo' with t = lo ^ b, p = t * 0x1b3 (64-bit),
+// lo' = low half of p, hi' = hi * 0x1b3 + high half of p + (t << 8). Only the low half forms a
+// dependent chain of its own; the high half follows it.
+__device__ __forceinline__ void fnv_step(uint32_t &lo, uint32_t &hi, uint32_t byte) {
+    const uint32_t t = lo ^ byte;
+    const uint64_t p = (uint64_t)t * 0x1b3u;
+    hi = hi * 0x1b3u + (uint32_t)(p >> 32) + (t << 8);
+    lo = (uint32_t)p;
 }
 
-// Hash of one full block: parent hash (8 octets, little endian) then block_size token ids.
-__device__ __forceinline__ uint64_t hash_block(uint64_t parent, const uint32_t *tok, int32_t bs) {
-    uint64_t h = kFnvBasis;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) h = (h ^ ((parent >> (8 * b)) & 0xffull)) * kFnvPrime;
-    int32_t i = 0;
-    for (; i + 4 <= bs; i += 4) {
-        const uint32_t t0 = tok[i], t1 = tok[i + 1], t2 = tok[i + 2], t3 = tok[i + 3];
-        h = fnv_token(h, t0);
-        h = fnv_token(h, t1);
-        h = fnv_token(h, t2);
-        h = fnv_token(h, t3);
+__device__ __forceinline__ void fnv_word(uint32_t &lo, uint32_t &hi, uint32_t v) {
+    fnv_step(lo, hi, v & 0xffu);
+    fnv_step(lo, hi, (v >> 8) & 0xffu);
+    fnv_step(lo, hi, (v >> 16) & 0xffu);
+    fnv_step(lo, hi, v >> 24);
+}
+
+constexpr uint32_t kFnvBasisLo = (uint32_t)kFnvBasis, kFnvBasisHi = (uint32_t)(kFnvBasis >> 32);
+constexpr unsigned kFull = 0xffffffffu;
+
+// Walks one session's full blocks with a whole warp. The session's tokens are a flat stream of
+// n_full * bs ids; the warp loads 64 of them at a time (two per lane, coalesced), loading the next 64
+// while the current ones are hashed, and every lane runs the same chain, taking each token from its
+// owner lane by shuffle. After each block every lane holds its hash h and calls on_block(j, h).
+// on_block returns false to stop early. All branches are uniform across the warp.
+template <typename OnBlock>
+__device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, int32_t bs, OnBlock &&on_block) {
+    const int lane = threadIdx.x & 31;
+    const int64_t total = n_full * bs;
+    uint32_t nxt_a = 0, nxt_b = 0;
+    if (2 * lane < total) nxt_a = tok[2 * lane];
+    if (2 * lane + 1 < total) nxt_b = tok[2 * lane + 1];
+    uint32_t lo = kFnvBasisLo, hi = kFnvBasisHi;
+    uint64_t parent = 0;
+    int64_t j = 0;
+    int32_t in_block = 0;
+    for (int64_t base = 0; base < total; base += 64) {
+        const uint32_t a = nxt_a, b = nxt_b;
+        const int64_t nb = base + 64;
+        if (nb + 2 * lane < total) nxt_a = tok[nb + 2 * lane];
+        if (nb + 2 * lane + 1 < total) nxt_b = tok[nb + 2 * lane + 1];
+        const int n_here = (int)min((int64_t)64, total - base);
+#pragma unroll 8
+        for (int i = 0; i < n_here; ++i) {
+            const uint32_t v = __shfl_sync(kFull, (i & 1) ? b : a, i >> 1);
+            if (in_block == 0) {
+                lo = kFnvBasisLo;
+                hi = kFnvBasisHi;
+                fnv_word(lo, hi, (uint32_t)parent);
+                fnv_word(lo, hi, (uint32_t)(parent >> 32));
+            }
+            fnv_word(lo, hi, v);
+            if (++in_block == bs) {
+                in_block = 0;
+                parent = ((uint64_t)hi << 32) | lo;
+                if (!on_block(j, parent)) return;
+                ++j;
+            }
+        }
     }
-    for (; i < bs; ++i) h = fnv_token(h, tok[i]);
-    return h;
 }
 
-// One thread per session; a session's chain is sequential by definition.
-__global__ void kvx_hash_sessions(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t bs,
-                                  uint64_t *out, const int64_t *hash_off, int64_t n_tok_total, int32_t *err) {
-    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per session; hashes go out a window of 32 blocks at a time (lane k writes block k of the
+// window), coalesced.
+__global__ void __launch_bounds__(128) kvx_hash_sessions(const uint32_t *tokens, const int64_t *tok_off,
+                                                         int32_t n_sessions, int32_t bs, uint64_t *out,
+                                                         const int64_t *hash_off, int64_t n_tok_total, int32_t *err) {
+    const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
     if (s >= n_sessions) return;
     const int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
     const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
     if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total || hash_off[s] < 0 || hash_off[s + 1] - hash_off[s] < n_full) {
-        atomicOr(err, 1);
+        if (lane == 0) atomicOr(err, 1);
         return;
     }
-    uint64_t parent = 0;
     uint64_t *o = out + hash_off[s];
-    for (int64_t j = 0; j < n_full; ++j) {
-        parent = hash_block(parent, tokens + t0 + j * bs, bs);
-        o[j] = parent;
-    }
+    uint64_t mine = 0;
+    warp_chain(tokens + t0, n_full, bs, [&](int64_t j, uint64_t h) {
+        if ((j & 31) == lane) mine = h;
+        if ((j & 31) == 31 || j == n_full - 1) {
+            const int64_t w0 = j & ~(int64_t)31;
+            if (w0 + lane <= j) o[w0 + lane] = mine;
+        }
+        return true;
+    });
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -134,33 +179,59 @@ __global__ void kvx_table_lookup_kernel(TableView t, const uint64_t *keys, int64
 // Match
 // ------------------------------------------------------------------------------------------------
 
-// Per session: hash block by block while either prefix (local hits, agreement with the published
-// remote hashes) is still open; stop once both have ended.
-__global__ void kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t bs,
-                                   TableView table, const uint64_t *remote_hash, const int64_t *rem_off,
-                                   int32_t threshold, int64_t n_tok_total, int64_t n_pub, kvx_match_result *out,
-                                   int64_t *push_blocks, int32_t *err) {
-    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per session: hash block by block while either prefix (local hits, agreement with the
+// published remote hashes) is still open; stop once both have ended. Each lane keeps the hash of
+// one block of the current window of 32; at the end of a window the lanes look their blocks up in the
+// table and compare them with the published list in parallel, and ballots extend the two prefixes.
+__global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
+                                                          int32_t n_sessions, int32_t bs, TableView table,
+                                                          const uint64_t *remote_hash, const int64_t *rem_off,
+                                                          int32_t threshold, int64_t n_tok_total, int64_t n_pub,
+                                                          kvx_match_result *out, int64_t *push_blocks, int32_t *err) {
+    const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
     if (s >= n_sessions) return;
     int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
     int64_t r0 = rem_off[s], n_rem = rem_off[s + 1] - r0;
     // malformed offsets: flag them and treat the session as empty, so no array is read out of range
-    if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total) { atomicOr(err, 1); t0 = 0; n_tok = 0; }
-    if (r0 < 0 || n_rem < 0 || r0 + n_rem > n_pub) { atomicOr(err, 2); r0 = 0; n_rem = 0; }
+    if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total) {
+        if (lane == 0) atomicOr(err, 1);
+        t0 = 0;
+        n_tok = 0;
+    }
+    if (r0 < 0 || n_rem < 0 || r0 + n_rem > n_pub) {
+        if (lane == 0) atomicOr(err, 2);
+        r0 = 0;
+        n_rem = 0;
+    }
     const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
     int64_t l_loc = 0, l_rem = 0;
     bool loc_open = true, rem_open = true;
-    uint64_t parent = 0;
-    for (int64_t j = 0; j < n_full && (loc_open || rem_open); ++j) {
-        const uint64_t h = hash_block(parent, tokens + t0 + j * bs, bs);
-        parent = h;
+    uint64_t mine = 0;
+    warp_chain(tokens + t0, n_full, bs, [&](int64_t j, uint64_t h) {
+        if ((j & 31) == lane) mine = h;
+        if ((j & 31) != 31 && j != n_full - 1) return true;
+        const int64_t w0 = j & ~(int64_t)31;
+        const int n_valid = (int)(j - w0 + 1);
+        const int64_t jb = w0 + lane;
+        const bool valid = lane < n_valid;
         if (loc_open) {
-            if (table_find(table, h) >= 0) ++l_loc; else loc_open = false;
+            const bool hit = valid && table_find(table, mine) >= 0;
+            const unsigned miss = ~__ballot_sync(kFull, hit);
+            const int first_miss = __ffs(miss) - 1;             // a lane past n_valid always misses
+            l_loc += min(first_miss, n_valid);
+            loc_open = first_miss >= n_valid;
         }
         if (rem_open) {
-            if (j < n_rem && remote_hash[r0 + j] == h) ++l_rem; else rem_open = false;
+            const bool same = valid && jb < n_rem && remote_hash[r0 + jb] == mine;
+            const unsigned miss = ~__ballot_sync(kFull, same);
+            const int first_miss = __ffs(miss) - 1;
+            l_rem += min(first_miss, n_valid);
+            rem_open = first_miss >= n_valid;
         }
-    }
+        return loc_open || rem_open;
+    });
+    if (lane != 0) return;
     const int64_t missing_blocks = l_rem > l_loc ? l_rem - l_loc : 0;
     const int64_t missing = missing_blocks * bs;
     if (missing > (int64_t)INT32_MAX || l_loc > (int64_t)INT32_MAX) atomicOr(err, 4);
@@ -432,7 +503,7 @@ kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int3
     e = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
     if (e == cudaSuccess) {
         count_launch();
-        kvx_hash_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+        kvx_hash_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                        out_hash, hash_off, n_tok_total, err);
         e = cudaGetLastError();
     }
@@ -591,7 +662,7 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
     ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8, stream));
     ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
     count_launch();
-    kvx_match_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+    kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                     table->view(), remote_hash, rem_off, threshold,
                                                                     n_tok_total, n_pub, out, m.push_blocks, m.err);
     ok(cudaGetLastError());
@@ -769,7 +840,7 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
     if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t) * 4, stream);
     if (e == cudaSuccess) {
         count_launch();
-        kvx_match_sessions<<<grid_for(n_sessions, 64), 64, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+        kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                         table->view(), remote_hash, rem_off, threshold,
                                                                         n_tok_total, n_pub, out, push_blocks, err);
         e = cudaGetLastError();

@@ -346,6 +346,8 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     pl->ctas_per_sm = o->ctas_per_sm ? o->ctas_per_sm : 2;
     pl->lanes = o->lanes ? o->lanes : 4;
     pl->next_lane = 0;
+    pl->lane_cache.clear();
+    pl->lane_src = nullptr;
     pl->kernel = o->kernel;
     pl->kernel = resolve_kernel(pl);
     return KVX_OK;

@@ -544,12 +544,19 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
         }
         e = cudaEventRecord(pl->fork_evt, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
-        int prio = 0;
-        e = cudaStreamGetPriority(stream, &prio);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetPriority");
-        cudaStream_t lane = nullptr;
-        st = lane_stream(pl->next_lane, prio, &lane);
-        if (st) return st;
+        if (pl->lane_src != stream || (int32_t)pl->lane_cache.size() != pl->lanes) {
+            // first push from this stream: look up its priority and the lanes that match it once
+            int prio = 0;
+            e = cudaStreamGetPriority(stream, &prio);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetPriority");
+            pl->lane_cache.assign(pl->lanes, nullptr);
+            for (int32_t i = 0; i < pl->lanes; ++i) {
+                st = lane_stream(i, prio, &pl->lane_cache[i]);
+                if (st) return st;
+            }
+            pl->lane_src = stream;
+        }
+        cudaStream_t lane = pl->lane_cache[pl->next_lane];
         pl->next_lane = (pl->next_lane + 1) % pl->lanes;
         e = cudaStreamWaitEvent(lane, pl->fork_evt, 0);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fork)");
