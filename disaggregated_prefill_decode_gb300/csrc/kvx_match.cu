@@ -218,14 +218,14 @@ __global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens
         if (loc_open) {
             const bool hit = valid && table_find(table, mine) >= 0;
             const unsigned miss = ~__ballot_sync(kFull, hit);
-            const int first_miss = __ffs(miss) - 1;             // a lane past n_valid always misses
+            const int first_miss = miss ? __ffs(miss) - 1 : 32;  // lanes past n_valid always miss
             l_loc += min(first_miss, n_valid);
             loc_open = first_miss >= n_valid;
         }
         if (rem_open) {
             const bool same = valid && jb < n_rem && remote_hash[r0 + jb] == mine;
             const unsigned miss = ~__ballot_sync(kFull, same);
-            const int first_miss = __ffs(miss) - 1;
+            const int first_miss = miss ? __ffs(miss) - 1 : 32;
             l_rem += min(first_miss, n_valid);
             rem_open = first_miss >= n_valid;
         }
