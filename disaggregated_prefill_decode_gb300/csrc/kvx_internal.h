@@ -72,6 +72,10 @@ kvx_status pool_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 void pool_free(void *ptr);
 // A non-blocking stream per device for the library's own small read-backs.
 kvx_status aux_stream(cudaStream_t *out);
+// Library-wide pool of events per (device, timing): plans rebuilt every step reuse them instead of
+// creating and destroying one or two per push.
+kvx_status event_take(bool timing, cudaEvent_t *ev);
+void event_give(bool timing, cudaEvent_t ev);
 
 // Launches the tile copy for layers [args.layer0, args.layer0 + n_layers) (kvx_push.cu).
 struct LaunchShape {
@@ -102,7 +106,7 @@ struct kvx_plan_s {
     int32_t threads = 256;
     int32_t flags = 0;                         // KVX_PLAN_* bits
     int32_t kernel = 0;                        // resolved KVX_KERNEL_*
-    int32_t ctas_per_sm = 2;                   // resident CTAs per SM of persistent kernels
+    int32_t ctas_per_sm = 0;                   // resident CTAs per SM of persistent kernels (0: by size)
     int32_t lanes = 4;                         // internal streams pushes fan out over
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push

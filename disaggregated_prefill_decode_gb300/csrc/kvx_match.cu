@@ -745,8 +745,9 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
             if (e != cudaSuccess) return cleanup(cuda_fail(e, "reading plan runs"));
         }
         finish_plan_shape(pl);
-        e = cudaEventCreateWithFlags(&pl->upload_evt, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventRecord(pl->upload_evt, stream);
+        st = event_take(false, &pl->upload_evt);
+        if (st) return cleanup(st);
+        e = cudaEventRecord(pl->upload_evt, stream);
         if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventRecord(plan)"));
         pl->upload_stream = stream;
         pl->uploaded = true;

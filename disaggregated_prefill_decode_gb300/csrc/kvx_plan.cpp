@@ -337,13 +337,13 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     if (o->threads && (o->threads < 32 || o->threads > 1024 || o->threads % 32))
         return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
     if ((o->flags ^ pl->flags) & KVX_PLAN_TIMING) {
-        // events are created with or without timing: drop the pooled ones
-        for (cudaEvent_t ev : pl->free_events) cudaEventDestroy(ev);
+        // events are created with or without timing: hand the plan's spares back to the pool
+        for (cudaEvent_t ev : pl->free_events) event_give((pl->flags & KVX_PLAN_TIMING) != 0, ev);
         pl->free_events.clear();
     }
     pl->flags = o->flags;
     if (o->threads) pl->threads = o->threads;
-    pl->ctas_per_sm = o->ctas_per_sm ? o->ctas_per_sm : 2;
+    pl->ctas_per_sm = o->ctas_per_sm;
     pl->lanes = o->lanes ? o->lanes : 4;
     pl->next_lane = 0;
     pl->lane_cache.clear();

@@ -341,16 +341,21 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     cudaError_t e;
     if (sh.kernel == KVX_KERNEL_BULK) {
         const int smem = kBulkStages * sh.tile_bytes;
-        e = resident_grid((const void *)kvx_copy_bulk, 32, smem, sh.ctas_per_sm, &grid);
+        const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 2 : 64);
+        e = resident_grid((const void *)kvx_copy_bulk, 32, smem, cap, &grid);
         if (e != cudaSuccess) return e;
         kvx_copy_bulk<<<(unsigned)std::min<int64_t>(grid, n_work), 32, smem, st>>>(a, n_work, sh.tile_bytes);
         return cudaGetLastError();
     }
+    // default resident CTAs: small launches stay small so that they overlap the caller's compute and
+    // the next push; large ones take the whole GPU
+    LaunchShape shape = sh;
+    if (shape.ctas_per_sm == 0) shape.ctas_per_sm = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 2 : 64;
     if (sh.kernel == KVX_KERNEL_PERSIST) {
         const void *fn = sh.vec == 16 ? persist_fn<16>(sh.strided) : sh.vec == 8 ? persist_fn<8>(sh.strided)
                        : sh.vec == 4 ? persist_fn<4>(sh.strided) : sh.vec == 2 ? persist_fn<2>(sh.strided)
                        : persist_fn<1>(sh.strided);
-        e = resident_grid(fn, sh.threads, 0, sh.ctas_per_sm, &grid);
+        e = resident_grid(fn, sh.threads, 0, shape.ctas_per_sm, &grid);
         if (e != cudaSuccess) return e;
         grid = (int)std::min<int64_t>(grid, n_work);
     }
@@ -371,6 +376,37 @@ static std::mutex g_dev_mu;
 static std::map<int, cudaMemPool_t> g_pools;
 static std::map<int, cudaStream_t> g_aux;
 static std::map<std::pair<int, int>, std::vector<cudaStream_t>> g_lanes;
+static std::mutex g_evt_mu;
+static std::map<std::pair<int, bool>, std::vector<cudaEvent_t>> g_events;
+
+kvx_status event_take(bool timing, cudaEvent_t *ev) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    {
+        std::lock_guard<std::mutex> lk(g_evt_mu);
+        std::vector<cudaEvent_t> &v = g_events[std::make_pair(dev, timing)];
+        if (!v.empty()) {
+            *ev = v.back();
+            v.pop_back();
+            return KVX_OK;
+        }
+    }
+    e = cudaEventCreateWithFlags(ev, timing ? cudaEventDefault : cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    return KVX_OK;
+}
+
+// Events go back to the pool of the current device; callers give back events of that device.
+void event_give(bool timing, cudaEvent_t ev) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaEventDestroy(ev);
+        return;
+    }
+    std::lock_guard<std::mutex> lk(g_evt_mu);
+    g_events[std::make_pair(dev, timing)].push_back(ev);
+}
 
 // Lane `i` for the current device at `priority`: a non-blocking stream created on first use and kept
 // for the life of the process.
@@ -504,8 +540,8 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     memcpy(img + pl->off_dst, pl->dst_base.data(), sizeof(void *) * pl->dst_base.size());
     cudaError_t e = cudaMemcpyAsync(pl->dev, img, pl->dev_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan upload)");
-    e = cudaEventCreateWithFlags(&pl->upload_evt, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    st = event_take(false, &pl->upload_evt);
+    if (st) return st;
     e = cudaEventRecord(pl->upload_evt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(upload)");
     pl->upload_stream = stream;
@@ -520,10 +556,7 @@ static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
         pl->free_events.pop_back();
         return KVX_OK;
     }
-    const unsigned flags = (pl->flags & KVX_PLAN_TIMING) ? cudaEventDefault : cudaEventDisableTiming;
-    cudaError_t e = cudaEventCreateWithFlags(ev, flags);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
-    return KVX_OK;
+    return event_take((pl->flags & KVX_PLAN_TIMING) != 0, ev);
 }
 
 extern "C" {
@@ -539,8 +572,8 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
     if (pl->lanes > 1) {
         // fork: the lane waits for everything already on the caller's stream (the upload included)
         if (!pl->fork_evt) {
-            e = cudaEventCreateWithFlags(&pl->fork_evt, cudaEventDisableTiming);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(fork)");
+            st = event_take(false, &pl->fork_evt);
+            if (st) return st;
         }
         e = cudaEventRecord(pl->fork_evt, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
@@ -693,14 +726,15 @@ kvx_status kvx_plan_destroy(kvx_plan_t pl) {
     for (const PendingPush &p : pl->pending) {
         cudaError_t e = cudaEventSynchronize(p.done);
         if (e != cudaSuccess && st == KVX_OK) st = cuda_fail(e, "cudaEventSynchronize(destroy)");
-        cudaEventDestroy(p.done);
-        if (p.start) cudaEventDestroy(p.start);
+        const bool timing = (pl->flags & KVX_PLAN_TIMING) != 0;
+        event_give(timing, p.done);
+        if (p.start) event_give(timing, p.start);
     }
-    for (cudaEvent_t ev : pl->free_events) cudaEventDestroy(ev);
-    if (pl->fork_evt) cudaEventDestroy(pl->fork_evt);
+    for (cudaEvent_t ev : pl->free_events) event_give((pl->flags & KVX_PLAN_TIMING) != 0, ev);
+    if (pl->fork_evt) event_give(false, pl->fork_evt);
     if (pl->upload_evt) {
         cudaEventSynchronize(pl->upload_evt);
-        cudaEventDestroy(pl->upload_evt);
+        event_give(false, pl->upload_evt);
     }
     if (pl->dev) pool_free(pl->dev);
     delete pl;

@@ -103,8 +103,9 @@ typedef struct kvx_plan_opts {
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
-                                 limit (0: default 2, which leaves room for the caller's compute
-                                 and for an overlapping push) */
+                                 limit (0: 2 for launches that read under 128 MiB, leaving room for
+                                 the caller's compute and an overlapping push; the occupancy limit
+                                 for larger launches) */
     int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
     int32_t reserved[2];      /* must be 0 */
 } kvx_plan_opts;
