@@ -24,15 +24,14 @@ static_assert(kFnvPrime == (1ull << 40) + 0x1b3u, "fnv_step splits the prime as 
 // Hashing
 // ------------------------------------------------------------------------------------------------
 
-// One FNV-1a step on the hash held as two 32-bit halves. The prime is 2^40 + 0x1b3, so
-// (hi:lo ^ b) * prime mod 2^64 = hi' : lo' with t = lo ^ b, p = t * 0x1b3 (64-bit),
-// lo' = low half of p, hi' = hi * 0x1b3 + high half of p + (t << 8). Only the low half forms a
-// dependent chain of its own; the high half follows it.
+// One FNV-1a step on the hash held as two 32-bit halves. The prime is 2^40 + 0x1b3, so with
+// t = lo ^ b: (hi:lo ^ b) * prime mod 2^64 = hi':lo' where lo' = t * 0x1b3 mod 2^32 and
+// hi' = hi * 0x1b3 + high word of (t * 0x1b3) + (t << 8) mod 2^32. The low half is the only chain
+// that depends on itself alone (xor, 32-bit multiply); the high half follows it.
 __device__ __forceinline__ void fnv_step(uint32_t &lo, uint32_t &hi, uint32_t byte) {
     const uint32_t t = lo ^ byte;
-    const uint64_t p = (uint64_t)t * 0x1b3u;
-    hi = hi * 0x1b3u + (uint32_t)(p >> 32) + (t << 8);
-    lo = (uint32_t)p;
+    lo = t * 0x1b3u;
+    hi = hi * 0x1b3u + __umulhi(t, 0x1b3u) + (t << 8);
 }
 
 __device__ __forceinline__ void fnv_word(uint32_t &lo, uint32_t &hi, uint32_t v) {
@@ -60,6 +59,33 @@ __device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, 
     uint32_t lo = kFnvBasisLo, hi = kFnvBasisHi;
     uint64_t parent = 0;
     int64_t j = 0;
+    if ((bs & 63) == 0) {
+        // block sizes that are multiples of 64: each chunk of 64 tokens lies inside one block, so the
+        // 256 byte steps of a chunk run without a branch
+        const int64_t per_block = bs >> 6;
+        int64_t chunk_in_block = 0;
+        for (int64_t base = 0; base < total; base += 64) {
+            const uint32_t a = nxt_a, b = nxt_b;
+            const int64_t nb = base + 64;
+            if (nb + 2 * lane < total) nxt_a = tok[nb + 2 * lane];
+            if (nb + 2 * lane + 1 < total) nxt_b = tok[nb + 2 * lane + 1];
+            if (chunk_in_block == 0) {
+                lo = kFnvBasisLo;
+                hi = kFnvBasisHi;
+                fnv_word(lo, hi, (uint32_t)parent);
+                fnv_word(lo, hi, (uint32_t)(parent >> 32));
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) fnv_word(lo, hi, __shfl_sync(kFull, (i & 1) ? b : a, i >> 1));
+            if (++chunk_in_block == per_block) {
+                chunk_in_block = 0;
+                parent = ((uint64_t)hi << 32) | lo;
+                if (!on_block(j, parent)) return;
+                ++j;
+            }
+        }
+        return;
+    }
     int32_t in_block = 0;
     for (int64_t base = 0; base < total; base += 64) {
         const uint32_t a = nxt_a, b = nxt_b;
