@@ -303,7 +303,7 @@ def run_kvx(args, rank, local_rank, world):
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
             "lanes": info["lanes"],
-            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "auto (2 below 128 MiB per launch)",
+            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "auto (1 bulk / 2 persistent below 128 MiB per launch)",
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
                       "stream "

@@ -220,11 +220,12 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     return KVX_OK;
 }
 
-// Bulk copies need 16-byte aligned addresses and sizes and a stage that fits shared memory.
+// Bulk copies need 16-byte aligned addresses and sizes and a stage that fits shared memory; the
+// automatic choice takes them whenever they apply (measured fastest with other work running).
 static int32_t resolve_kernel(const kvx_plan_s *pl) {
-    const int32_t k = pl->kernel == KVX_KERNEL_AUTO ? KVX_KERNEL_PERSIST : pl->kernel;
-    if (k == KVX_KERNEL_BULK && (pl->strided || pl->vec != 16 || pl->tile_bytes > (48 << 10)))
-        return KVX_KERNEL_PERSIST;
+    const bool bulk_ok = !pl->strided && pl->vec == 16 && pl->tile_bytes <= (48 << 10);
+    const int32_t k = pl->kernel == KVX_KERNEL_AUTO ? (bulk_ok ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
+    if (k == KVX_KERNEL_BULK && !bulk_ok) return KVX_KERNEL_PERSIST;
     return k;
 }
 

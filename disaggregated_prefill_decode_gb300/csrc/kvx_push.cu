@@ -341,7 +341,7 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     cudaError_t e;
     if (sh.kernel == KVX_KERNEL_BULK) {
         const int smem = kBulkStages * sh.tile_bytes;
-        const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 2 : 64);
+        const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 1 : 64);
         e = resident_grid((const void *)kvx_copy_bulk, 32, smem, cap, &grid);
         if (e != cudaSuccess) return e;
         kvx_copy_bulk<<<(unsigned)std::min<int64_t>(grid, n_work), 32, smem, st>>>(a, n_work, sh.tile_bytes);

@@ -103,9 +103,9 @@ typedef struct kvx_plan_opts {
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
-                                 limit (0: 2 for launches that read under 128 MiB, leaving room for
-                                 the caller's compute and an overlapping push; the occupancy limit
-                                 for larger launches) */
+                                 limit (0: for launches that read under 128 MiB 1 with BULK and 2
+                                 with PERSIST, leaving room for the caller's compute and an
+                                 overlapping push; the occupancy limit for larger launches) */
     int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
     int32_t reserved[2];      /* must be 0 */
 } kvx_plan_opts;
@@ -113,7 +113,8 @@ typedef struct kvx_plan_opts {
 /* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
  * loading the next descriptor while it copies the current tile. BULK: the same walk with the bulk
  * asynchronous copy engine (global -> shared -> global through a ring of mbarrier-tracked stages);
- * contiguous plans with 16-byte alignment only, others fall back to PERSIST. */
+ * contiguous plans with 16-byte alignment only, others fall back to PERSIST. AUTO picks BULK where it
+ * applies and PERSIST elsewhere. */
 #define KVX_KERNEL_AUTO 0
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2

@@ -233,7 +233,8 @@ def test_kernel_resolution():
         k = kvx.kvx_plan_get_info(p)["kernel"]
         kvx.kvx_plan_destroy(p)
         return k
-    assert kern({}) == kvx.KVX_KERNEL_PERSIST
+    assert kern({}) == kvx.KVX_KERNEL_BULK
+    assert kern({"tile_bytes": 65536}) == kvx.KVX_KERNEL_PERSIST
     assert kern({"kernel": kvx.KVX_KERNEL_TILE}) == kvx.KVX_KERNEL_TILE
     assert kern({"kernel": kvx.KVX_KERNEL_BULK}) == kvx.KVX_KERNEL_BULK
     assert kern({"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": 65536}) == kvx.KVX_KERNEL_PERSIST   # stage too big
