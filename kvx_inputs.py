@@ -266,14 +266,17 @@ def fill_bf16_normal(t, seed: int) -> None:
     flat.normal_(0.0, 1.0, generator=gen)
 
 
-def fill_fp8_bytes(t, seed: int) -> None:
-    """Fill a torch uint8 tensor with bytes uniform over 0x00..0xFE minus 0x7F (no e4m3 NaN codes)."""
+def fill_fp8_bytes(t, seed: int, chunk: int = 1 << 30) -> None:
+    """Fill a torch uint8 tensor with bytes uniform over 0x00..0xFE minus 0x7F (no e4m3 NaN codes),
+    a chunk at a time so that no temporary is as large as the tensor."""
     import torch
     gen = torch.Generator(device=t.device)
     gen.manual_seed(seed)
     flat = t.view(-1)
-    flat.random_(0, 254, generator=gen)
-    flat.add_((flat >= 0x7F).to(torch.uint8))
+    for i in range(0, flat.numel(), chunk):
+        c = flat[i:i + chunk]
+        c.random_(0, 254, generator=gen)
+        c.add_((c >= 0x7F).to(torch.uint8))
 
 
 def fill_canary(t, kind: str) -> None:

@@ -274,3 +274,56 @@ def test_bad_free_block_fails_the_layer_without_writing_outside():
     assert bool((guard[:per] == 0x55).all()) and bool((guard[per + w.prefill.buffer_bytes:] == 0x55).all())
     kvx.kvx_plan_destroy(plan)
     c.close()
+
+
+def test_bidir_full_scale_in_waves():
+    """The full bidirectional workload: 256 sessions, 48 layers of fp8 576-byte latents (decode pool
+    ~130 GB, prefill pool ~85 GB). Sessions are matched and pushed in 4 waves of 64 into one recycled
+    free region; after each wave, layers 0, 23 and 47 are checked whole against the oracle."""
+    orc = oracle.load()
+    w0 = kvx_inputs.bidir_mla_fp8(n_layers=48, free_blocks=1)        # sizes only
+    hs = [orc.block_hashes(w0.tokens[w0.tok_off[s]:w0.tok_off[s + 1]], 64) for s in range(w0.n_sessions)]
+    allh = np.concatenate(hs)
+    keys = np.unique(allh[w0.resident])
+    waves = [range(i, i + 64) for i in range(0, 256, 64)]
+    # free region large enough for the largest wave (decisions from the oracle)
+    need = []
+    for wv in waves:
+        s0, s1 = wv[0], wv[-1] + 1
+        sub = orc.match(w0.tokens[w0.tok_off[s0]:w0.tok_off[s1]], w0.tok_off[s0:s1 + 1] - w0.tok_off[s0], 64, keys,
+                        allh[w0.rem_off[s0]:w0.rem_off[s1]], w0.remote_blk[w0.rem_off[s0]:w0.rem_off[s1]],
+                        w0.rem_off[s0:s1 + 1] - w0.rem_off[s0], w0.threshold, np.zeros(0, np.int32))
+        need.append(int(sub["missing"][sub["push"] == 1].sum() // 64))
+    w = kvx_inputs.bidir_mla_fp8(n_layers=48, free_blocks=max(need))
+    assert np.array_equal(w.tokens, w0.tokens) and np.array_equal(w.remote_blk, w0.remote_blk)
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=w.seed)
+    dst, dbig = device_pool(w.prefill, "canary_fp8_bytes")
+    table = kvx.kvx_table_build(dev(keys, np.uint64), dev(np.arange(len(keys), dtype=np.int32), np.int32), len(keys))
+    sp, dp = kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst)
+    side = torch.cuda.Stream()
+    for wv in waves:
+        s0, s1 = wv[0], wv[-1] + 1
+        t0, t1, r0, r1 = w.tok_off[s0], w.tok_off[s1], w.rem_off[s0], w.rem_off[s1]
+        toks, tok_off = w.tokens[t0:t1], w.tok_off[s0:s1 + 1] - t0
+        rh, rb, rem_off = allh[r0:r1], w.remote_blk[r0:r1], w.rem_off[s0:s1 + 1] - r0
+        want = orc.match(toks, tok_off, 64, keys, rh, rb, rem_off, w.threshold, w.free_blocks)
+        assert want["status"] == 0
+        kvx_inputs.fill_canary(dbig, "fp8_bytes")                       # recycle the free region
+        out = torch.zeros(64 * 24, dtype=torch.uint8, device="cuda")
+        st, plan = kvx.kvx_match_prefix(dev(toks, np.uint32), dev(tok_off, np.int64), 64, 64, table,
+                                        dev(rh, np.uint64), dev(rb, np.int32), dev(rem_off, np.int64), w.threshold,
+                                        dev(w.free_blocks, np.int32), len(w.free_blocks), sp, dp, out)
+        assert st == kvx.KVX_OK
+        assert_decisions(results(out, 64), want)
+        for layer in range(48):
+            kvx.kvx_push_layer(plan, layer, side)
+        assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+        reqs, k = [], 0
+        for s in range(64):
+            if want["push"][s]:
+                nb = int(want["missing"][s]) // 64
+                reqs.append((nb * 64, want["pair_src"][k:k + nb], want["pair_dst"][k:k + nb]))
+                k += nb
+        check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")], reqs, [0, 23, 47])
+        kvx.kvx_plan_destroy(plan)
+    kvx.kvx_table_destroy(table)
