@@ -31,10 +31,14 @@ CANARY_BF16 = 0xDEAD    # fill of every untouched consumer bf16 element
 CANARY_FP8 = 0x7F       # fill of the prefill pool in the fp8 workload: an e4m3 NaN code, never pushed
 
 
+LAYOUT_NHD, LAYOUT_HND = 0, 1
+
+
 @dataclasses.dataclass
 class PoolGeom:
     """Shape of one side's paged pool: n_layers*n_planes*n_shards dense buffers, each
-    [n_blocks][block_size][heads_per_shard][head_dim] elements of elem_bytes."""
+    [n_blocks][block_size][heads_per_shard][head_dim] (layout NHD) or
+    [n_blocks][heads_per_shard][block_size][head_dim] (layout HND) elements of elem_bytes."""
     n_layers: int
     n_planes: int
     n_shards: int
@@ -43,6 +47,7 @@ class PoolGeom:
     elem_bytes: int
     block_size: int
     n_blocks: int
+    layout: int = LAYOUT_NHD
 
     @property
     def n_buffers(self) -> int:

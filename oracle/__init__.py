@@ -49,7 +49,7 @@ class _Pool(ctypes.Structure):
     _fields_ = [
         ("n_layers", ctypes.c_int32), ("n_planes", ctypes.c_int32), ("n_shards", ctypes.c_int32),
         ("heads_per_shard", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-        ("elem_bytes", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("elem_bytes", ctypes.c_int32), ("block_size", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("n_blocks", ctypes.c_int64), ("base", ctypes.POINTER(ctypes.c_void_p)),
     ]
 
@@ -95,7 +95,7 @@ class Oracle:
             ptrs[i] = b.ctypes.data
         keep.append(ptrs)
         return _Pool(geom.n_layers, geom.n_planes, geom.n_shards, geom.heads_per_shard, geom.head_dim,
-                     geom.elem_bytes, geom.block_size, geom.n_blocks,
+                     geom.elem_bytes, geom.block_size, getattr(geom, "layout", 0), geom.n_blocks,
                      ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)))
 
     def push(self, src_geom, src_bufs, dst_geom, dst_bufs, requests: Iterable[Tuple[int, np.ndarray, np.ndarray]]):

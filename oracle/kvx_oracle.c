@@ -25,7 +25,8 @@
  *          14695981039346656037, 64-bit prime 1099511628211; per octet: xor, then multiply.
  *
  * Readings where the pages are silent (all stated again in the design notes):
- *  - each (layer, plane, shard) buffer is dense [n_blocks][block_size][heads][head_dim];
+ *  - each (layer, plane, shard) buffer is dense [n_blocks][block_size][heads][head_dim] ("NHD"),
+ *    or [n_blocks][heads][block_size][head_dim] ("HND") when the pool says so;
  *  - token t of a request lives in block ids[t / block_size], slot t % block_size, on each side;
  *  - only tokens [0, n_tokens) are copied, so unused slots of a last block keep their old bytes;
  *  - shard s owns the global heads [s*heads_per_shard, (s+1)*heads_per_shard);
@@ -45,9 +46,17 @@
 /* One side's pool, as the oracle sees it: host copies of each (layer, plane, shard) buffer. */
 typedef struct {
     int32_t n_layers, n_planes, n_shards, heads_per_shard, head_dim, elem_bytes, block_size;
+    int32_t layout; /* 0: [block][slot][head][dim], 1: [block][head][slot][dim] */
     int64_t n_blocks;
     uint8_t **base; /* [(layer * n_planes + plane) * n_shards + shard] */
 } oracle_pool;
+
+/* Index, in units of one head's bytes, of (block, slot, head) inside one buffer. */
+static int64_t oracle_head_index(const oracle_pool *p, int64_t blk, int64_t slot, int64_t head)
+{
+    if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;
+    return (blk * p->block_size + slot) * p->heads_per_shard + head;
+}
 
 /* ------------------------------------------------------------------------------------------- */
 /* [push] [ranks]: the per-head byte copy, request -> layer -> plane -> token -> shard -> head.  */
@@ -66,17 +75,17 @@ int oracle_push(const oracle_pool *src, const oracle_pool *dst, int32_t n_reqs,
                     int64_t sblk = src_ids[r][t / src->block_size];
                     int64_t dblk = dst_ids[r][t / dst->block_size];
                     if (sblk < 0 || sblk >= src->n_blocks || dblk < 0 || dblk >= dst->n_blocks) return -1;
-                    int64_t src_row = sblk * src->block_size + t % src->block_size;
-                    int64_t dst_row = dblk * dst->block_size + t % dst->block_size;
+                    int64_t src_slot = t % src->block_size;
+                    int64_t dst_slot = t % dst->block_size;
                     for (int32_t s = 0; s < src->n_shards; ++s) {
                         for (int32_t h = 0; h < src->heads_per_shard; ++h) {
                             int32_t g = s * src->heads_per_shard + h;      /* global KV head */
                             int32_t ds = g / dst->heads_per_shard;         /* consumer shard */
                             int32_t dh = g % dst->heads_per_shard;         /* head within it */
                             const uint8_t *from = src->base[((int64_t)l * src->n_planes + p) * src->n_shards + s]
-                                                  + (size_t)(src_row * src->heads_per_shard + h) * head_bytes;
+                                                  + (size_t)oracle_head_index(src, sblk, src_slot, h) * head_bytes;
                             uint8_t *to = dst->base[((int64_t)l * dst->n_planes + p) * dst->n_shards + ds]
-                                          + (size_t)(dst_row * dst->heads_per_shard + dh) * head_bytes;
+                                          + (size_t)oracle_head_index(dst, dblk, dst_slot, dh) * head_bytes;
                             memcpy(to, from, head_bytes);
                         }
                     }

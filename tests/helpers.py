@@ -26,6 +26,13 @@ def host_pool(geom, seed, fill="random"):
     return bufs
 
 
+def nhd_view(geom, buf, hb):
+    """A [block][slot][head][bytes] numpy view of one buffer, whatever its layout (writes go through)."""
+    if getattr(geom, "layout", 0) == 1:
+        return buf.reshape(geom.n_blocks, geom.heads_per_shard, geom.block_size, hb).transpose(0, 2, 1, 3)
+    return buf.reshape(geom.n_blocks, geom.block_size, geom.heads_per_shard, hb)
+
+
 def numpy_route_push(src_geom, src_bufs, dst_geom, dst_bufs, requests):
     """The push written with numpy tensor views; returns new dst buffers."""
     out = [b.copy() for b in dst_bufs]
@@ -38,14 +45,12 @@ def numpy_route_push(src_geom, src_bufs, dst_geom, dst_bufs, requests):
             for p in range(src_geom.n_planes):
                 shards = []
                 for s in range(src_geom.n_shards):
-                    v = src_bufs[(l * src_geom.n_planes + p) * src_geom.n_shards + s].reshape(
-                        src_geom.n_blocks, src_geom.block_size, src_geom.heads_per_shard, hb)
+                    v = nhd_view(src_geom, src_bufs[(l * src_geom.n_planes + p) * src_geom.n_shards + s], hb)
                     shards.append(v[np.asarray(sids[:nbs])].reshape(-1, src_geom.heads_per_shard, hb)[:n])
                 tokens = np.concatenate(shards, axis=1)      # [n, all heads, head bytes]
                 for d in range(dst_geom.n_shards):
                     part = tokens[:, d * dst_geom.heads_per_shard:(d + 1) * dst_geom.heads_per_shard]
-                    v = out[(l * dst_geom.n_planes + p) * dst_geom.n_shards + d].reshape(
-                        dst_geom.n_blocks, dst_geom.block_size, dst_geom.heads_per_shard, hb)
+                    v = nhd_view(dst_geom, out[(l * dst_geom.n_planes + p) * dst_geom.n_shards + d], hb)
                     idx = np.asarray(dids[:nbd])
                     cur = v[idx].reshape(-1, dst_geom.heads_per_shard, hb)
                     cur[:n] = part
@@ -68,8 +73,12 @@ def dst_side_map(src_geom, src_bufs, dst_geom, dst_bufs, requests):
                 buf = out[(l * dst_geom.n_planes + p) * dst_geom.n_shards + d]
                 for byte in range(dst_geom.buffer_bytes):
                     head_slot, within = divmod(byte, hb)
-                    row, hd = divmod(head_slot, dst_geom.heads_per_shard)
-                    blk, slot = divmod(row, dst_geom.block_size)
+                    if getattr(dst_geom, "layout", 0) == 1:
+                        blk_head, slot = divmod(head_slot, dst_geom.block_size)
+                        blk, hd = divmod(blk_head, dst_geom.heads_per_shard)
+                    else:
+                        row, hd = divmod(head_slot, dst_geom.heads_per_shard)
+                        blk, slot = divmod(row, dst_geom.block_size)
                     if blk not in owner:
                         continue
                     r, i = owner[blk]
@@ -80,9 +89,13 @@ def dst_side_map(src_geom, src_bufs, dst_geom, dst_bufs, requests):
                     g = d * dst_geom.heads_per_shard + hd
                     s, hs = divmod(g, src_geom.heads_per_shard)
                     sblk, sslot = divmod(t, src_geom.block_size)
-                    srow = int(sids[sblk]) * src_geom.block_size + sslot
+                    sb = int(sids[sblk])
+                    if getattr(src_geom, "layout", 0) == 1:
+                        sidx = (sb * src_geom.heads_per_shard + hs) * src_geom.block_size + sslot
+                    else:
+                        sidx = (sb * src_geom.block_size + sslot) * src_geom.heads_per_shard + hs
                     sbuf = src_bufs[(l * src_geom.n_planes + p) * src_geom.n_shards + s]
-                    buf[byte] = sbuf[(srow * src_geom.heads_per_shard + hs) * hb + within]
+                    buf[byte] = sbuf[sidx * hb + within]
     return out
 
 

@@ -22,8 +22,7 @@ MUTANTS = [
     ("parent_big_endian", "(uint8_t)(parent >> (8 * b))", "(uint8_t)(parent >> (8 * (7 - b)))"),
     ("token_big_endian", "(uint8_t)(tok >> (8 * b))", "(uint8_t)(tok >> (8 * (3 - b)))"),
     ("no_chaining", "parent = out[j];", "parent = 0;"),
-    ("src_slot_from_dst_bs", "int64_t src_row = sblk * src->block_size + t % src->block_size;",
-     "int64_t src_row = sblk * src->block_size + t % dst->block_size;"),
+    ("src_slot_from_dst_bs", "int64_t src_slot = t % src->block_size;", "int64_t src_slot = t % dst->block_size;"),
     ("dst_shard_mapping", "int32_t ds = g / dst->heads_per_shard;", "int32_t ds = g % dst->n_shards;"),
     ("whole_last_block", "for (int64_t t = 0; t < n_tokens[r]; ++t) {",
      "for (int64_t t = 0; t < (n_tokens[r] + dst->block_size - 1) / dst->block_size * dst->block_size; ++t) {"),
@@ -37,6 +36,10 @@ MUTANTS = [
     ("missing_not_clipped", "l_rem > l_loc ? l_rem - l_loc : 0", "l_rem - l_loc"),
     ("free_list_offset", "free_blocks[out_dst_start[s] + i]", "free_blocks[i]"),
     ("remote_span_start", "remote_blk[rem_off[s] + out_local_hit[s] + i]", "remote_blk[rem_off[s] + i]"),
+    ("hnd_as_nhd", "if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;",
+     "if (p->layout == 1) return (blk * p->block_size + slot) * p->heads_per_shard + head;"),
+    ("hnd_slot_head_swapped", "if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;",
+     "if (p->layout == 1) return (blk * p->heads_per_shard + slot) * p->block_size + head;"),
 ]
 
 CHILD = r"""

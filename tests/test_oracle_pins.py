@@ -110,6 +110,9 @@ GEOMS = {
     "bs1": (PoolGeom(1, 2, 1, 2, 2, 1, 1, 24), PoolGeom(1, 2, 1, 2, 2, 1, 1, 24)),
     "odd_head_bytes": (PoolGeom(1, 1, 2, 1, 3, 1, 3, 9), PoolGeom(1, 1, 1, 2, 3, 1, 5, 7)),
     "mla_like": (PoolGeom(2, 1, 1, 1, 6, 1, 4, 8), PoolGeom(2, 1, 1, 1, 6, 1, 4, 8)),
+    "hnd_equal": (PoolGeom(1, 2, 1, 3, 4, 2, 4, 10, 1), PoolGeom(1, 2, 1, 3, 4, 2, 4, 10, 1)),
+    "nhd_to_hnd_bs4to8": (PoolGeom(1, 1, 2, 2, 4, 2, 4, 10), PoolGeom(1, 1, 1, 4, 4, 2, 8, 6, 1)),
+    "hnd_to_nhd_split": (PoolGeom(1, 2, 1, 4, 2, 2, 8, 5, 1), PoolGeom(1, 2, 2, 2, 2, 2, 4, 10)),
 }
 
 
