@@ -42,7 +42,15 @@ struct CopyArgs {
 
 struct Geom {
     int32_t n_layers, n_planes, n_shards, heads_per_shard, head_dim, elem_bytes, block_size;
+    int32_t layout;                   // KVX_LAYOUT_NHD or KVX_LAYOUT_HND
     int64_t n_blocks;
+    // index of (block, slot, head) inside one buffer, in units of head_bytes()
+    int64_t head_index(int64_t blk, int64_t slot, int64_t head) const {
+        return layout == KVX_LAYOUT_HND ? (blk * heads_per_shard + head) * block_size + slot
+                                        : (blk * block_size + slot) * heads_per_shard + head;
+    }
+    // bytes between consecutive tokens of one head inside a block
+    int64_t token_pitch() const { return layout == KVX_LAYOUT_HND ? head_bytes() : row_bytes(); }
     int64_t head_bytes() const { return (int64_t)head_dim * elem_bytes; }
     int64_t row_bytes() const { return (int64_t)heads_per_shard * head_bytes(); }
     int64_t buf_bytes() const { return n_blocks * block_size * row_bytes(); }
@@ -100,6 +108,8 @@ struct kvx_plan_s {
 
     // copy shape
     int32_t strided = 0;
+    int32_t per_head = 0;                      // tiles are (block segment, head) pieces (an HND side)
+    int64_t src_pitch = 0, dst_pitch = 0;      // strided tiles: row pitches
     int32_t vec = 16;
     int32_t width = 0;
     int32_t tile_bytes = 16384;

@@ -628,6 +628,10 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
             delete pl;
             return fail(KVX_EINVAL, "pool block sizes must equal block_size");
         }
+        if (pl->per_head) {
+            delete pl;
+            return fail(KVX_EUNSUPPORTED, "device-built plans need KVX_LAYOUT_NHD pools");
+        }
         if (std::max(pl->src.n_shards, pl->dst.n_shards) > 8) {
             delete pl;
             return fail(KVX_EUNSUPPORTED, "device-built plans support at most 8 shard pairs");

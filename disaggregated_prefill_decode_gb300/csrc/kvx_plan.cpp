@@ -41,10 +41,12 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static kvx_status read_geom(const kvx_pool *p, const char *side, Geom *g, std::vector<void *> *bases) {
     if (!p) return fail(KVX_EINVAL, "%s pool is NULL", side);
     if (p->n_layers < 1 || p->n_planes < 1 || p->n_shards < 1 || p->heads_per_shard < 1 || p->head_dim < 1 ||
-        p->elem_bytes < 1 || p->block_size < 1 || p->n_blocks < 0 || p->reserved != 0)
-        return fail(KVX_EINVAL, "%s pool: counts must be >= 1 (n_blocks >= 0, reserved 0)", side);
+        p->elem_bytes < 1 || p->block_size < 1 || p->n_blocks < 0)
+        return fail(KVX_EINVAL, "%s pool: counts must be >= 1 (n_blocks >= 0)", side);
+    if (p->layout != KVX_LAYOUT_NHD && p->layout != KVX_LAYOUT_HND)
+        return fail(KVX_EUNSUPPORTED, "%s pool: unknown layout %d", side, p->layout);
     *g = Geom{p->n_layers, p->n_planes, p->n_shards, p->heads_per_shard, p->head_dim, p->elem_bytes,
-              p->block_size, p->n_blocks};
+              p->block_size, p->layout, p->n_blocks};
     // extents stay well inside int64, rows inside int32, buffers inside the int32 launch grid
     const double bytes = (double)p->n_blocks * p->block_size * p->heads_per_shard * (double)p->head_dim * p->elem_bytes;
     if (bytes > 9.0e18) return fail(KVX_EUNSUPPORTED, "%s pool buffer size overflows", side);
@@ -142,7 +144,9 @@ static int32_t vector_bytes(const kvx_plan_s *pl, const std::vector<Pair> &pairs
     for (void *p : pl->dst_base) g = gcd64(g, (int64_t)((uintptr_t)p & 15));
     g = gcd64(g, pl->src.row_bytes());
     g = gcd64(g, pl->dst.row_bytes());
-    if (pl->strided) {
+    if (pl->per_head) {
+        g = gcd64(g, pl->src.head_bytes());   // offsets, pitches and widths are multiples of it
+    } else if (pl->strided) {
         g = gcd64(g, pl->width);
         for (const Pair &q : pairs) g = gcd64(gcd64(g, q.src_seg_off), q.dst_seg_off);
     } else {
@@ -151,8 +155,55 @@ static int32_t vector_bytes(const kvx_plan_s *pl, const std::vector<Pair> &pairs
     return (int32_t)g;   // gcd with 16: one of 16, 8, 4, 2, 1
 }
 
+// Tiles of plans with an HND side: each run is cut at every block boundary of either side, and each
+// such segment is copied head by head (a head's tokens are rows at each side's token pitch). When
+// both sides are HND with the same block size and heads per shard, a stretch of whole blocks is one
+// contiguous span per shard on both sides and is copied as such.
+static void build_head_tiles(kvx_plan_s *pl) {
+    const Geom &s = pl->src, &d = pl->dst;
+    const int64_t hb = s.head_bytes();
+    const int64_t rows_per_tile = std::max<int64_t>(1, pl->tile_bytes / hb);
+    const int32_t heads = s.n_shards * s.heads_per_shard;
+    const bool same_hnd = s.layout == KVX_LAYOUT_HND && d.layout == KVX_LAYOUT_HND && s.block_size == d.block_size &&
+                          s.heads_per_shard == d.heads_per_shard;
+    auto emit = [&](int64_t soff, int64_t doff, int64_t rows, int32_t ss, int32_t ds) {
+        for (int64_t r0 = 0; r0 < rows; r0 += rows_per_tile)
+            pl->tiles.push_back({soff + r0 * pl->src_pitch, doff + r0 * pl->dst_pitch,
+                                 (int32_t)std::min(rows_per_tile, rows - r0), ss, ds, 0});
+    };
+    for (size_t r = 0; r < pl->run_ntok.size(); ++r) {
+        int64_t t = 0;
+        const int64_t n = pl->run_ntok[r];
+        while (t < n) {
+            const int64_t srow = (int64_t)pl->run_src_row[r] + t, drow = (int64_t)pl->run_dst_row[r] + t;
+            const int64_t sblk = srow / s.block_size, sslot = srow % s.block_size;
+            const int64_t dblk = drow / d.block_size, dslot = drow % d.block_size;
+            if (same_hnd && sslot == 0 && dslot == 0 && n - t >= s.block_size) {
+                const int64_t nblk = (n - t) / s.block_size;        // whole blocks, contiguous on both sides
+                for (int32_t sh = 0; sh < s.n_shards; ++sh)
+                    emit(s.head_index(sblk, 0, 0) * hb, d.head_index(dblk, 0, 0) * hb,
+                         nblk * s.block_size * s.heads_per_shard, sh, sh);
+                t += nblk * s.block_size;
+                continue;
+            }
+            const int64_t len = std::min({s.block_size - sslot, d.block_size - dslot, n - t});
+            for (int32_t g = 0; g < heads; ++g) {
+                const int32_t ss = g / s.heads_per_shard, hs = g % s.heads_per_shard;
+                const int32_t ds = g / d.heads_per_shard, hd = g % d.heads_per_shard;
+                emit(s.head_index(sblk, sslot, hs) * hb, d.head_index(dblk, dslot, hd) * hb, len, ss, ds);
+            }
+            t += len;
+        }
+    }
+    pl->n_tiles = (int64_t)pl->tiles.size();
+}
+
 static void build_tiles(kvx_plan_s *pl, const std::vector<Pair> &pairs) {
     pl->tiles.clear();
+    if (pl->per_head) {
+        build_head_tiles(pl);
+        return;
+    }
     const int64_t rb_s = pl->src.row_bytes(), rb_d = pl->dst.row_bytes();
     const size_t nr = pl->run_ntok.size();
     if (!pl->strided) {
@@ -212,8 +263,11 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
     if (pl->threads < 32 || pl->threads > 1024 || pl->threads % 32)
         return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
-    pl->strided = (s.heads_per_shard != d.heads_per_shard) ? 1 : 0;
-    pl->width = (int32_t)(std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
+    pl->per_head = (s.layout == KVX_LAYOUT_HND || d.layout == KVX_LAYOUT_HND) ? 1 : 0;
+    pl->strided = (pl->per_head || s.heads_per_shard != d.heads_per_shard) ? 1 : 0;
+    pl->width = (int32_t)(pl->per_head ? s.head_bytes() : std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
+    pl->src_pitch = pl->per_head ? s.token_pitch() : s.row_bytes();
+    pl->dst_pitch = pl->per_head ? d.token_pitch() : d.row_bytes();
     pl->layer_state.assign(s.n_layers, KVX_LAYER_IDLE);
     pl->inject.assign(s.n_layers, 0);
     pl->injected_pending.assign(s.n_layers, 0);
@@ -379,6 +433,8 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->threads = pl->kernel == KVX_KERNEL_BULK ? 32 : pl->threads;
     out->lanes = pl->lanes;
     out->reserved = 0;
+    out->src_pitch = pl->src_pitch;
+    out->dst_pitch = pl->dst_pitch;
     return KVX_OK;
 }
 

@@ -500,8 +500,8 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();
-    a.src_pitch = pl->src.row_bytes();
-    a.dst_pitch = pl->dst.row_bytes();
+    a.src_pitch = pl->src_pitch;
+    a.dst_pitch = pl->dst_pitch;
     a.width = pl->width;
     a.n_planes = pl->src.n_planes;
     a.src_shards = pl->src.n_shards;

@@ -27,8 +27,11 @@ KVX_LAYER_IDLE, KVX_LAYER_PENDING, KVX_LAYER_DONE, KVX_LAYER_FAILED = range(4)
 
 class kvx_pool(ctypes.Structure):
     _fields_ = [("n_layers", c_i32), ("n_planes", c_i32), ("n_shards", c_i32), ("heads_per_shard", c_i32),
-                ("head_dim", c_i32), ("elem_bytes", c_i32), ("block_size", c_i32), ("reserved", c_i32),
+                ("head_dim", c_i32), ("elem_bytes", c_i32), ("block_size", c_i32), ("layout", c_i32),
                 ("n_blocks", c_i64), ("base", ctypes.POINTER(c_vp))]
+
+
+KVX_LAYOUT_NHD, KVX_LAYOUT_HND = 0, 1
 
 
 class kvx_request(ctypes.Structure):
@@ -48,7 +51,8 @@ KVX_KERNEL_AUTO, KVX_KERNEL_TILE, KVX_KERNEL_PERSIST, KVX_KERNEL_BULK = range(4)
 class kvx_plan_info(ctypes.Structure):
     _fields_ = [("n_runs", c_i64), ("n_tiles", c_i64), ("bytes_per_layer", c_i64), ("vec_bytes", c_i32),
                 ("strided", c_i32), ("n_layers", c_i32), ("n_planes", c_i32), ("width", c_i32),
-                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("reserved", c_i32)]
+                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("reserved", c_i32),
+                ("src_pitch", c_i64), ("dst_pitch", c_i64)]
 
 
 class kvx_match_result(ctypes.Structure):
@@ -169,7 +173,7 @@ class Pool:
         self.buffers = list(buffers)
         self._ptrs = (c_vp * max(n, 1))(*[_ptr(b) for b in buffers])
         self.struct = kvx_pool(geom.n_layers, geom.n_planes, geom.n_shards, geom.heads_per_shard, geom.head_dim,
-                               geom.elem_bytes, geom.block_size, 0, geom.n_blocks,
+                               geom.elem_bytes, geom.block_size, getattr(geom, "layout", 0), geom.n_blocks,
                                ctypes.cast(self._ptrs, _P(c_vp)))
 
 

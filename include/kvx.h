@@ -59,12 +59,17 @@ typedef enum kvx_layer_state {
  *
  * The pool is n_layers * n_planes * n_shards separate device buffers; buffer
  * base[(layer * n_planes + plane) * n_shards + shard] is a dense row-major array
- *     [n_blocks][block_size][heads_per_shard][head_dim]  of elem_bytes-byte elements.
+ *     [n_blocks][block_size][heads_per_shard][head_dim]  (layout KVX_LAYOUT_NHD), or
+ *     [n_blocks][heads_per_shard][block_size][head_dim]  (layout KVX_LAYOUT_HND)
+ * of elem_bytes-byte elements. The two sides may use different layouts.
  * planes: 2 for separate K and V, 1 for a single latent (MLA). Shard s holds the global KV heads
  * [s * heads_per_shard, (s + 1) * heads_per_shard), i.e. the tensor-parallel head partition.
  * Values are moved as opaque bytes; elem_bytes only sizes them. `base` is a host array of device
  * pointers, copied by kvx_plan.
  */
+#define KVX_LAYOUT_NHD 0
+#define KVX_LAYOUT_HND 1
+
 typedef struct kvx_pool {
     int32_t n_layers;
     int32_t n_planes;
@@ -73,7 +78,7 @@ typedef struct kvx_pool {
     int32_t head_dim;
     int32_t elem_bytes;
     int32_t block_size;     /* tokens per block */
-    int32_t reserved;       /* must be 0 */
+    int32_t layout;         /* KVX_LAYOUT_NHD (0) or KVX_LAYOUT_HND (1) */
     int64_t n_blocks;
     void *const *base;
 } kvx_pool;
@@ -143,6 +148,7 @@ typedef struct kvx_plan_opts {
  *   EINVAL        null pointers, counts < 1, n_layers / n_planes / head_dim / elem_bytes differ,
  *                 total heads differ, null buffer, a consumer buffer overlaps any other buffer;
  *   EUNSUPPORTED  neither shard count divides the other; more than 2^31-1 rows in a buffer;
+ *                 an unknown layout;
  *   ERANGE        a needed block id is outside [0, n_blocks), n_src or n_dst too small;
  *   EOVERLAP      a consumer block appears twice among all requests' needed ids.
  * No device memory is touched by kvx_plan; descriptors go to the device at the first push.
@@ -181,6 +187,8 @@ typedef struct kvx_plan_info {
     int32_t threads;
     int32_t lanes;
     int32_t reserved;
+    int64_t src_pitch;           /* strided plans: bytes between consecutive rows of a tile, producer */
+    int64_t dst_pitch;           /* and consumer side */
 } kvx_plan_info;
 kvx_status kvx_plan_get_info(kvx_plan_t plan, kvx_plan_info *out);
 
@@ -311,7 +319,7 @@ typedef struct kvx_match_result {
  * free_blocks[dst_start + k].
  *
  * remote_pool is the producer (decode) pool, local_pool the consumer (prefill) pool; their
- * block_size must equal block_size. If out_plan is not NULL it receives a plan (built on the
+ * block_size must equal block_size and both must use KVX_LAYOUT_NHD. If out_plan is not NULL it receives a plan (built on the
  * device) whose pushes copy those blocks with kvx_push_layer / kvx_sync; NULL computes the
  * decisions only (the pools may then be NULL). The call waits for `stream` (it reads back the
  * totals). Block ids outside a pool make the affected layers FAILED at kvx_sync (the copy kernel

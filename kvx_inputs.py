@@ -153,12 +153,12 @@ def qwen3_32b_single(seed: int = 2, n_layers: int = 64) -> PushWorkload:
 
 
 def qwen3_32b_batched(seed: int = 3, n_layers: int = 64, n_requests: int = 16,
-                      len_range=(1024, 8192)) -> PushWorkload:
+                      len_range=(1024, 8192), layout: int = LAYOUT_NHD) -> PushWorkload:
     rng = np.random.default_rng(seed)
     lens = rng.integers(len_range[0], len_range[1] + 1, n_requests).tolist()
     need = [_ceil_div(n, 16) for n in lens]
     pool = math.ceil(1.2 * sum(need))
-    geom = _qwen3_32b_geom(n_layers, pool)
+    geom = _qwen3_32b_geom(n_layers, pool).replace(layout=layout)
     src = _slice_per_request(chunked_order(rng, pool, mean=2.0), need)
     dst = _slice_per_request(chunked_order(rng, pool, mean=2.0), need)
     reqs = [Request(n, s, d) for n, s, d in zip(lens, src, dst)]
@@ -181,11 +181,19 @@ def tp4_to_tp1_remap(seed: int = 4, n_layers: int = 64, n_requests: int = 8,
     return PushWorkload("tp4_to_tp1_remap", src_geom, dst_geom, reqs, seed, "bf16_normal")
 
 
+def qwen3_32b_batched_hnd(seed: int = 3, n_layers: int = 64) -> PushWorkload:
+    """The batched workload with both pools head-major ([block][head][slot][dim])."""
+    w = qwen3_32b_batched(seed=seed, n_layers=n_layers, layout=LAYOUT_HND)
+    w.name = "qwen3_32b_batched_hnd"
+    return w
+
+
 PUSH_WORKLOADS = {
     "tiny": tiny,
     "qwen3_32b_single": qwen3_32b_single,
     "qwen3_32b_batched": qwen3_32b_batched,
     "tp4_to_tp1_remap": tp4_to_tp1_remap,
+    "qwen3_32b_batched_hnd": qwen3_32b_batched_hnd,
 }
 
 

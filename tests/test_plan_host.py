@@ -89,10 +89,9 @@ def replay_tiles(plan, sg, src, dg, dst):
                     assert n <= info["tile_bytes"] and n % info["vec_bytes"] == 0
                     db[do:do + n] = sb[so:so + n]
                 else:
-                    w = info["width"]
+                    w, sp_, dp_ = info["width"], info["src_pitch"], info["dst_pitch"]
                     for r in range(n):
-                        db[do + r * dg.row_bytes:do + r * dg.row_bytes + w] = \
-                            sb[so + r * sg.row_bytes:so + r * sg.row_bytes + w]
+                        db[do + r * dp_:do + r * dp_ + w] = sb[so + r * sp_:so + r * sp_ + w]
     return out
 
 
@@ -104,6 +103,10 @@ CASES = {
     "bs1": (PoolGeom(1, 2, 1, 2, 8, 1, 1, 24), PoolGeom(1, 2, 1, 2, 8, 1, 1, 24)),
     "odd_head_bytes": (PoolGeom(1, 1, 2, 1, 3, 1, 3, 9), PoolGeom(1, 1, 1, 2, 3, 1, 5, 7)),
     "mla576": (PoolGeom(2, 1, 1, 1, 576, 1, 4, 8), PoolGeom(2, 1, 1, 1, 576, 1, 4, 8)),
+    "hnd_equal": (PoolGeom(1, 2, 2, 3, 8, 2, 4, 10, 1), PoolGeom(1, 2, 2, 3, 8, 2, 4, 10, 1)),
+    "hnd_to_hnd_bs4to8": (PoolGeom(1, 1, 1, 4, 8, 2, 4, 12, 1), PoolGeom(1, 1, 1, 4, 8, 2, 8, 6, 1)),
+    "nhd_to_hnd_merge": (PoolGeom(1, 2, 4, 1, 8, 2, 4, 10), PoolGeom(1, 2, 1, 4, 8, 2, 8, 6, 1)),
+    "hnd_to_nhd_split": (PoolGeom(1, 1, 1, 4, 8, 2, 8, 5, 1), PoolGeom(1, 1, 2, 2, 8, 2, 2, 20)),
 }
 
 
@@ -192,6 +195,7 @@ def test_validation_errors():
     g6a, g6b = PoolGeom(1, 1, 3, 2, 8, 2, 4, 8), PoolGeom(1, 1, 2, 3, 8, 2, 4, 8)
     expect(kvx.KVX_EUNSUPPORTED, lambda: kvx.kvx_plan(fake_pool(g6a, 1 << 40), fake_pool(g6b, 1 << 44), [ok]))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(fake_pool(g.replace(block_size=0), 1 << 40), dp, [ok]))
+    expect(kvx.KVX_EUNSUPPORTED, lambda: kvx.kvx_plan(fake_pool(g.replace(layout=2), 1 << 40), dp, [ok]))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"tile_bytes": 24}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"threads": 48}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(kvx.Pool(g, [0] * g.n_buffers), dp, [ok]))

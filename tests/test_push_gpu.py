@@ -128,6 +128,10 @@ GEOMS = {
     "split1to2": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 40), PoolGeom(2, 2, 2, 4, 128, 2, 16, 40)),
     "merge8to2": (PoolGeom(1, 2, 8, 1, 64, 2, 16, 40), PoolGeom(1, 2, 2, 4, 64, 2, 32, 20)),
     "mla576_fp8": (PoolGeom(2, 1, 1, 1, 576, 1, 64, 30), PoolGeom(2, 1, 1, 1, 576, 1, 64, 30)),
+    "hnd_qwen_equal": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 60, 1), PoolGeom(2, 2, 1, 8, 128, 2, 16, 60, 1)),
+    "hnd_tp4_to_nhd_tp1_bs64": (PoolGeom(1, 2, 4, 2, 128, 2, 16, 60, 1), PoolGeom(1, 2, 1, 8, 128, 2, 64, 15)),
+    "nhd_to_hnd_bs16to32": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 1, 8, 128, 2, 32, 30, 1)),
+    "hnd_odd_heads": (PoolGeom(1, 1, 1, 3, 3, 2, 8, 40, 1), PoolGeom(1, 1, 3, 1, 3, 2, 4, 80, 1)),
 }
 
 
@@ -299,3 +303,10 @@ def test_set_opts_on_existing_plan():
     check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
                  range(2))
     kvx.kvx_plan_destroy(plan)
+
+
+def test_hnd_batched_workload_sampled():
+    """The batched Qwen3-32B-shaped workload with both pools head-major, 64 layers, sampled layers."""
+    w = kvx_inputs.qwen3_32b_batched_hnd()
+    info = run_workload(w, [0, 40, 63])
+    assert info["strided"] == 1 and info["src_pitch"] == 256 and info["dst_pitch"] == 256
