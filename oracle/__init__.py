@@ -78,6 +78,9 @@ class Oracle:
         lib.oracle_match.argtypes = [_I32, _P, _P, _I32, _P, _I64, _P, _P, _P, _I32, _P, _I64,
                                      _P, _P, _P, _P, _P, _P, _P, _P]
         lib.oracle_match.restype = ctypes.c_int
+        lib.oracle_match_ex.argtypes = [_I32, _P, _P, _I32, _P, _I64, _P, _P, _P, _I32, _P, _I64, _I32, _P, _I64,
+                                        _P, _P, _P, _P, _P, _P, _P, _P]
+        lib.oracle_match_ex.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -156,9 +159,12 @@ class Oracle:
         return out[:n].copy()
 
     # -- match ----------------------------------------------------------------------------------
+    FILL_HOLES, KEEP_LAST = 1, 2
+
     def match(self, tokens, tok_off, block_size, local_keys, remote_hash, remote_blk, rem_off, threshold,
-              free_blocks):
-        """Returns dict(local_hit, remote_hit, missing, push, dst_start, pair_src, pair_dst, status)."""
+              free_blocks, flags=0, expiry=None, now=0):
+        """Returns dict(local_hit, remote_hit, missing, push, dst_start, pair_src, pair_dst, status).
+        flags: FILL_HOLES | KEEP_LAST; expiry (per session) with now: retention of the published span."""
         tokens = np.ascontiguousarray(tokens, np.uint32)
         tok_off = np.ascontiguousarray(tok_off, np.int64)
         n_s = len(tok_off) - 1
@@ -175,11 +181,13 @@ class Oracle:
         cap = max(len(rb), 1)
         ps, pd = np.zeros(cap, np.int32), np.zeros(cap, np.int32)
         npairs = ctypes.c_int64(0)
-        rc = self.lib.oracle_match(n_s, tokens_.ctypes.data, tok_off.ctypes.data, block_size,
-                                   keys_.ctypes.data, len(keys), rh_.ctypes.data, rb_.ctypes.data,
-                                   ro.ctypes.data, threshold, fb_.ctypes.data, len(fb),
-                                   lh.ctypes.data, rhit.ctypes.data, miss.ctypes.data, push.ctypes.data,
-                                   dstart.ctypes.data, ps.ctypes.data, pd.ctypes.data, ctypes.byref(npairs))
+        exp = None if expiry is None else np.ascontiguousarray(expiry, np.int64)
+        rc = self.lib.oracle_match_ex(n_s, tokens_.ctypes.data, tok_off.ctypes.data, block_size,
+                                      keys_.ctypes.data, len(keys), rh_.ctypes.data, rb_.ctypes.data,
+                                      ro.ctypes.data, threshold, fb_.ctypes.data, len(fb), int(flags),
+                                      None if exp is None else exp.ctypes.data, int(now),
+                                      lh.ctypes.data, rhit.ctypes.data, miss.ctypes.data, push.ctypes.data,
+                                      dstart.ctypes.data, ps.ctypes.data, pd.ctypes.data, ctypes.byref(npairs))
         if rc < 0:
             raise MemoryError("oracle_match")
         k = npairs.value

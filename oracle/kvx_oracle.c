@@ -35,6 +35,15 @@
  *    (4 bytes each, little endian); the first block's parent is 0; only full blocks are hashed;
  *  - missing = max(0, L_rem - L_loc) * block_size; push iff missing > 0 and missing >= threshold;
  *  - pushing sessions take prefill blocks from the free list in session order.
+ * Options of the match (each off by default):
+ *  - fill holes: blocks of [0, L_rem) that are resident locally are reused even past the first local
+ *    miss (a chained hash certifies the whole prefix before the block), so only the non-resident
+ *    blocks of [0, L_rem) are pulled: missing = that count * block_size;
+ *  - TTL ("Bidirectional KV transfer" article, "Block Retention TTL": a turn arriving after the
+ *    retention time falls back to normal prefill): a session whose published span has expiry <= now
+ *    has nothing published;
+ *  - keep last ("vLLM MoRIIO KV Connector" notes, section 3.1: the last token is always recomputed):
+ *    when L_rem blocks cover every token of the session, L_rem drops by one block.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -205,12 +214,15 @@ static int oracle_is_resident(const uint64_t *sorted, int64_t n, uint64_t key)
  * Returns 0, 5 if the free list is too short (decisions written, no pairs), or -1 on allocation
  * failure.
  */
-int oracle_match(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_off, int32_t block_size,
-                 const uint64_t *local_keys, int64_t n_local, const uint64_t *remote_hash,
-                 const int32_t *remote_blk, const int64_t *rem_off, int32_t threshold,
-                 const int32_t *free_blocks, int64_t n_free, int32_t *out_local_hit,
-                 int32_t *out_remote_hit, int32_t *out_missing, int32_t *out_push, int64_t *out_dst_start,
-                 int32_t *pair_src, int32_t *pair_dst, int64_t *n_pairs)
+#define ORACLE_MATCH_FILL_HOLES 1
+#define ORACLE_MATCH_KEEP_LAST 2
+
+int oracle_match_ex(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_off, int32_t block_size,
+                    const uint64_t *local_keys, int64_t n_local, const uint64_t *remote_hash,
+                    const int32_t *remote_blk, const int64_t *rem_off, int32_t threshold,
+                    const int32_t *free_blocks, int64_t n_free, int32_t flags, const int64_t *expiry, int64_t now,
+                    int32_t *out_local_hit, int32_t *out_remote_hit, int32_t *out_missing, int32_t *out_push,
+                    int64_t *out_dst_start, int32_t *pair_src, int32_t *pair_dst, int64_t *n_pairs)
 {
     uint64_t *sorted = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n_local > 0 ? n_local : 1));
     if (!sorted) return -1;
@@ -228,18 +240,24 @@ int oracle_match(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_
         while (l_loc < n_full && oracle_is_resident(sorted, n_local, h[l_loc])) ++l_loc;
 
         int64_t n_rem = rem_off[s + 1] - rem_off[s];
+        if (expiry && now >= expiry[s]) n_rem = 0;                 /* retention expired */
         int64_t l_rem = 0;
         while (l_rem < n_full && l_rem < n_rem && h[l_rem] == remote_hash[rem_off[s] + l_rem]) ++l_rem;
-        free(h);
+        if ((flags & ORACLE_MATCH_KEEP_LAST) && l_rem > 0 && l_rem * block_size >= n_tok) --l_rem;
 
         int64_t missing_blocks = l_rem > l_loc ? l_rem - l_loc : 0;
+        if (flags & ORACLE_MATCH_FILL_HOLES) {
+            missing_blocks = 0;
+            for (int64_t j = 0; j < l_rem; ++j)
+                if (!oracle_is_resident(sorted, n_local, h[j])) ++missing_blocks;
+        }
+        free(h);
         int64_t missing = missing_blocks * block_size;
         out_local_hit[s] = (int32_t)l_loc;
         out_remote_hit[s] = (int32_t)l_rem;
         out_missing[s] = (int32_t)missing;
         out_push[s] = (missing > 0 && missing >= threshold) ? 1 : 0;
     }
-    free(sorted);
 
     int64_t cursor = 0;
     for (int32_t s = 0; s < n_sessions; ++s) {
@@ -251,12 +269,31 @@ int oracle_match(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_
         }
     }
     if (cursor > n_free) {
+        free(sorted);
         *n_pairs = 0;
         return 5;
     }
     int64_t k = 0;
     for (int32_t s = 0; s < n_sessions; ++s) {
         if (!out_push[s]) continue;
+        if (flags & ORACLE_MATCH_FILL_HOLES) {
+            /* the non-resident blocks of [0, L_rem), in order */
+            int64_t n_tok = tok_off[s + 1] - tok_off[s];
+            int64_t n_full = n_tok / block_size;
+            uint64_t *h = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n_full > 0 ? n_full : 1));
+            if (!h) { free(sorted); return -1; }
+            oracle_block_hashes(tokens + tok_off[s], n_tok, block_size, h);
+            int64_t i = 0;
+            for (int64_t j = 0; j < out_remote_hit[s]; ++j) {
+                if (oracle_is_resident(sorted, n_local, h[j])) continue;
+                pair_src[k] = remote_blk[rem_off[s] + j];
+                pair_dst[k] = free_blocks[out_dst_start[s] + i];
+                ++k;
+                ++i;
+            }
+            free(h);
+            continue;
+        }
         int64_t nb = out_missing[s] / block_size;
         for (int64_t i = 0; i < nb; ++i) {
             pair_src[k] = remote_blk[rem_off[s] + out_local_hit[s] + i];
@@ -264,6 +301,19 @@ int oracle_match(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_
             ++k;
         }
     }
+    free(sorted);
     *n_pairs = k;
     return 0;
+}
+
+int oracle_match(int32_t n_sessions, const uint32_t *tokens, const int64_t *tok_off, int32_t block_size,
+                 const uint64_t *local_keys, int64_t n_local, const uint64_t *remote_hash,
+                 const int32_t *remote_blk, const int64_t *rem_off, int32_t threshold,
+                 const int32_t *free_blocks, int64_t n_free, int32_t *out_local_hit,
+                 int32_t *out_remote_hit, int32_t *out_missing, int32_t *out_push, int64_t *out_dst_start,
+                 int32_t *pair_src, int32_t *pair_dst, int64_t *n_pairs)
+{
+    return oracle_match_ex(n_sessions, tokens, tok_off, block_size, local_keys, n_local, remote_hash, remote_blk,
+                           rem_off, threshold, free_blocks, n_free, 0, NULL, 0, out_local_hit, out_remote_hit,
+                           out_missing, out_push, out_dst_start, pair_src, pair_dst, n_pairs);
 }

@@ -34,8 +34,15 @@ MUTANTS = [
      "for (int64_t q = 0; q < n_full; ++q) l_loc += oracle_is_resident(sorted, n_local, h[q]);"),
     ("threshold_strict", "(missing > 0 && missing >= threshold)", "(missing > 0 && missing > threshold)"),
     ("missing_not_clipped", "l_rem > l_loc ? l_rem - l_loc : 0", "l_rem - l_loc"),
-    ("free_list_offset", "free_blocks[out_dst_start[s] + i]", "free_blocks[i]"),
+    ("free_list_offset", "pair_dst[k] = free_blocks[out_dst_start[s] + i];\n            ++k;\n        }",
+     "pair_dst[k] = free_blocks[i];\n            ++k;\n        }"),
+    ("free_list_offset_holes", "pair_dst[k] = free_blocks[out_dst_start[s] + i];\n                ++k;",
+     "pair_dst[k] = free_blocks[i];\n                ++k;"),
     ("remote_span_start", "remote_blk[rem_off[s] + out_local_hit[s] + i]", "remote_blk[rem_off[s] + i]"),
+    ("holes_counted_from_prefix", "for (int64_t j = 0; j < l_rem; ++j)\n                if (!oracle_is_resident(sorted, n_local, h[j])) ++missing_blocks;",
+     "for (int64_t j = l_loc; j < l_rem; ++j)\n                ++missing_blocks;"),
+    ("ttl_strict", "if (expiry && now >= expiry[s]) n_rem = 0;", "if (expiry && now > expiry[s]) n_rem = 0;"),
+    ("keep_last_always", "&& l_rem > 0 && l_rem * block_size >= n_tok) --l_rem;", "&& l_rem > 0) --l_rem;"),
     ("hnd_as_nhd", "if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;",
      "if (p->layout == 1) return (blk * p->block_size + slot) * p->heads_per_shard + head;"),
     ("hnd_slot_head_swapped", "if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;",

@@ -240,31 +240,41 @@ def test_runs_invariants_random(orc):
 # Match
 # ---------------------------------------------------------------------------------------------
 
-def naive_match(orc, tokens, tok_off, bs, local_keys, remote_hash, remote_blk, rem_off, threshold, free):
+def naive_match(orc, tokens, tok_off, bs, local_keys, remote_hash, remote_blk, rem_off, threshold, free,
+                fill_holes=False, keep_last=False, expiry=None, now=0):
     keys = set(int(k) for k in local_keys)
     res = dict(local_hit=[], remote_hit=[], missing=[], push=[])
+    pulled = []
     for s in range(len(tok_off) - 1):
         h = [int(x) for x in orc.block_hashes(tokens[tok_off[s]:tok_off[s + 1]], bs)]
         rem = [int(x) for x in remote_hash[rem_off[s]:rem_off[s + 1]]]
+        if expiry is not None and now >= expiry[s]:
+            rem = []
         loc = 0
         while loc < len(h) and h[loc] in keys:
             loc += 1
         rh = 0
         while rh < len(h) and rh < len(rem) and h[rh] == rem[rh]:
             rh += 1
-        miss = max(0, rh - loc) * bs
+        if keep_last and rh > 0 and rh * bs >= tok_off[s + 1] - tok_off[s]:
+            rh -= 1
+        if fill_holes:
+            take = [j for j in range(rh) if h[j] not in keys]
+        else:
+            take = list(range(loc, rh))
+        miss = len(take) * bs
         res["local_hit"].append(loc)
         res["remote_hit"].append(rh)
         res["missing"].append(miss)
         res["push"].append(int(miss > 0 and miss >= threshold))
+        pulled.append(take)
     pairs_s, pairs_d, cur = [], [], 0
     for s in range(len(tok_off) - 1):
         if res["push"][s]:
-            loc, nb = res["local_hit"][s], res["missing"][s] // bs
-            for i in range(nb):
-                pairs_s.append(int(remote_blk[rem_off[s] + loc + i]))
+            for i, j in enumerate(pulled[s]):
+                pairs_s.append(int(remote_blk[rem_off[s] + j]))
                 pairs_d.append(int(free[cur + i]))
-            cur += nb
+            cur += len(pulled[s])
     return res, pairs_s, pairs_d
 
 
@@ -354,3 +364,46 @@ def test_match_free_list_order_and_exhaustion(orc):
     short = orc.match(tokens, tok_off, bs, keys, remote, rblk, rem_off, 1, free[:14])
     assert short["status"] == 5 and len(short["pair_src"]) == 0
     assert short["push"].tolist() == [1, 1, 1]
+
+
+@pytest.mark.parametrize("fill_holes,keep_last,ttl", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (1, 1, 1)])
+def test_match_options_equal_naive_loop(orc, fill_holes, keep_last, ttl):
+    w = kvx_inputs.bidir_mla_fp8(seed=40 + fill_holes + 2 * keep_last + 4 * ttl, n_sessions=14, n_layers=1,
+                                 system_tokens=256, hist_range=(0, 1500), resident_p=0.5, threshold=128)
+    # some sessions end exactly on a block boundary so that keep_last bites
+    hashes = [orc.block_hashes(w.tokens[w.tok_off[s]:w.tok_off[s + 1]], 64) for s in range(w.n_sessions)]
+    allh = np.concatenate(hashes)
+    keys = np.unique(allh[w.resident])
+    expiry = np.random.default_rng(7).integers(0, 200, w.n_sessions) if ttl else None
+    flags = (orc.FILL_HOLES if fill_holes else 0) | (orc.KEEP_LAST if keep_last else 0)
+    got = orc.match(w.tokens, w.tok_off, 64, keys, allh, w.remote_blk, w.rem_off, w.threshold, w.free_blocks,
+                    flags=flags, expiry=expiry, now=100)
+    want, ps, pd = naive_match(orc, w.tokens, w.tok_off, 64, keys, allh, w.remote_blk, w.rem_off, w.threshold,
+                               w.free_blocks, fill_holes=bool(fill_holes), keep_last=bool(keep_last),
+                               expiry=expiry, now=100)
+    for k in ("local_hit", "remote_hit", "missing", "push"):
+        assert got[k].tolist() == want[k], k
+    assert got["pair_src"].tolist() == ps and got["pair_dst"].tolist() == pd
+
+
+def test_match_options_hand_cases(orc):
+    bs, n = 4, 8
+    toks, keys, remote = _session_case(orc, bs, n, 2, n, extra_resident=(4, 6))
+    args = (toks, [0, n * bs], bs, keys, remote, np.arange(10, 10 + n), [0, n], 1, np.arange(50, 60))
+    plain = orc.match(*args)
+    assert (plain["local_hit"][0], plain["remote_hit"][0], plain["missing"][0]) == (2, 8, 24)
+    assert plain["pair_src"].tolist() == [12, 13, 14, 15, 16, 17]
+    holes = orc.match(*args, flags=orc.FILL_HOLES)            # blocks 4 and 6 are reused in place
+    assert holes["missing"][0] == 16 and holes["pair_src"].tolist() == [12, 13, 15, 17]
+    assert holes["pair_dst"].tolist() == [50, 51, 52, 53]
+    last = orc.match(*args, flags=orc.KEEP_LAST)               # 32 tokens, all covered: last block recomputed
+    assert last["remote_hit"][0] == 7 and last["missing"][0] == 20
+    both = orc.match(*args, flags=orc.FILL_HOLES | orc.KEEP_LAST)
+    assert both["pair_src"].tolist() == [12, 13, 15]
+    expired = orc.match(*args, expiry=np.array([100]), now=100)
+    assert expired["remote_hit"][0] == 0 and expired["push"][0] == 0
+    alive = orc.match(*args, expiry=np.array([101]), now=100)
+    assert alive["remote_hit"][0] == 8
+    partial = orc.match(toks[:-1], [0, n * bs - 1], bs, keys, remote[:n - 1], np.arange(n - 1), [0, n - 1], 1,
+                        np.arange(9), flags=orc.KEEP_LAST)     # a partial last block is computed anyway
+    assert partial["remote_hit"][0] == 7
