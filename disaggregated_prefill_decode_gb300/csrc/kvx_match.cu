@@ -205,15 +205,26 @@ __global__ void kvx_table_lookup_kernel(TableView t, const uint64_t *keys, int64
 // Match
 // ------------------------------------------------------------------------------------------------
 
+// Options of the match on the device (kvx_match_opts plus the hole-filling scratch).
+struct MatchFlags {
+    int32_t flags;           // KVX_MATCH_*
+    const int64_t *expiry;   // per session, or NULL
+    int64_t now;
+    uint8_t *resident;       // FILL_HOLES: per published block, 1 if resident locally (scratch)
+};
+
 // One warp per session: hash block by block while either prefix (local hits, agreement with the
 // published remote hashes) is still open; stop once both have ended. Each lane keeps the hash of
 // one block of the current window of 32; at the end of a window the lanes look their blocks up in the
 // table and compare them with the published list in parallel, and ballots extend the two prefixes.
+// With FILL_HOLES the lookups go on while the remote prefix is open, residency is recorded for the
+// plan emission, and the non-resident blocks below the remote prefix are counted.
 __global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
                                                           int32_t n_sessions, int32_t bs, TableView table,
                                                           const uint64_t *remote_hash, const int64_t *rem_off,
                                                           int32_t threshold, int64_t n_tok_total, int64_t n_pub,
-                                                          kvx_match_result *out, int64_t *push_blocks, int32_t *err) {
+                                                          MatchFlags mf, kvx_match_result *out, int64_t *push_blocks,
+                                                          int32_t *err) {
     const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= n_sessions) return;
@@ -230,9 +241,12 @@ __global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens
         r0 = 0;
         n_rem = 0;
     }
+    if (mf.expiry && mf.now >= mf.expiry[s]) n_rem = 0;           // retention expired
+    const bool fill = (mf.flags & KVX_MATCH_FILL_HOLES) != 0;
     const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
-    int64_t l_loc = 0, l_rem = 0;
+    int64_t l_loc = 0, l_rem = 0, holes = 0;
     bool loc_open = true, rem_open = true;
+    unsigned last_hits = 0;                                       // residency bits of the last window
     uint64_t mine = 0;
     warp_chain(tokens + t0, n_full, bs, [&](int64_t j, uint64_t h) {
         if ((j & 31) == lane) mine = h;
@@ -241,9 +255,11 @@ __global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens
         const int n_valid = (int)(j - w0 + 1);
         const int64_t jb = w0 + lane;
         const bool valid = lane < n_valid;
+        const bool look = loc_open || (fill && rem_open);
+        const bool hit = look && valid && table_find(table, mine) >= 0;
+        const unsigned hits = __ballot_sync(kFull, hit);
         if (loc_open) {
-            const bool hit = valid && table_find(table, mine) >= 0;
-            const unsigned miss = ~__ballot_sync(kFull, hit);
+            const unsigned miss = ~hits;
             const int first_miss = miss ? __ffs(miss) - 1 : 32;  // lanes past n_valid always miss
             l_loc += min(first_miss, n_valid);
             loc_open = first_miss >= n_valid;
@@ -252,13 +268,26 @@ __global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens
             const bool same = valid && jb < n_rem && remote_hash[r0 + jb] == mine;
             const unsigned miss = ~__ballot_sync(kFull, same);
             const int first_miss = miss ? __ffs(miss) - 1 : 32;
-            l_rem += min(first_miss, n_valid);
+            const int n_in = min(first_miss, n_valid);              // blocks of this window in the prefix
+            if (fill) {
+                if (lane < n_in) mf.resident[r0 + jb] = hit ? 1 : 0;
+                const unsigned below = n_in >= 32 ? kFull : ((1u << n_in) - 1u);
+                holes += __popc(~hits & below);
+            }
+            l_rem += n_in;
             rem_open = first_miss >= n_valid;
         }
+        last_hits = hits;
         return loc_open || rem_open;
     });
     if (lane != 0) return;
-    const int64_t missing_blocks = l_rem > l_loc ? l_rem - l_loc : 0;
+    if ((mf.flags & KVX_MATCH_KEEP_LAST) && l_rem > 0 && l_rem * bs >= n_tok) {
+        // every token is covered (only when the session ends on a block boundary and the whole
+        // chain matched, so block l_rem - 1 is in the last window): recompute the last block
+        --l_rem;
+        if (fill && !((last_hits >> (l_rem & 31)) & 1u)) --holes;
+    }
+    const int64_t missing_blocks = fill ? holes : (l_rem > l_loc ? l_rem - l_loc : 0);
     const int64_t missing = missing_blocks * bs;
     if (missing > (int64_t)INT32_MAX || l_loc > (int64_t)INT32_MAX) atomicOr(err, 4);
     const int32_t push = (missing > 0 && missing >= threshold) ? 1 : 0;
@@ -413,6 +442,55 @@ __global__ void kvx_emit_pairs(const kvx_match_result *res, const int64_t *sess_
     int64_t starts = 1;
     if (i > 0) starts = (src == (int64_t)remote_blk[base + i - 1] + 1 && dst == (int64_t)free_blocks[k - 1] + 1) ? 0 : 1;
     flag[k] = starts;
+}
+
+// FILL_HOLES emission, step 1: published block k is pulled when its session pushes, it lies below
+// the session's remote prefix and it is not resident locally. Its session comes from a binary search
+// over the remote offsets, checked against the session's range (offsets of sessions flagged as
+// malformed never push).
+__device__ __forceinline__ int32_t session_of(const int64_t *rem_off, int32_t n_sessions, int64_t k) {
+    int32_t lo = 0, hi = n_sessions - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (rem_off[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void kvx_need_flags(const kvx_match_result *res, const int64_t *rem_off, int32_t n_sessions, int64_t n_pub,
+                               const uint8_t *resident, int64_t *need) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n_pub) return;
+    const int32_t s = session_of(rem_off, n_sessions, k);
+    const int64_t j = k - rem_off[s];
+    const bool mine = j >= 0 && k < rem_off[s + 1];
+    need[k] = (mine && res[s].push && j < res[s].remote_hit_blocks && !resident[k]) ? 1 : 0;
+}
+
+// Step 2: pulled block k goes to position npos[k] of the pair list (an exclusive scan of need), the
+// free-list entry of the same position; positions past the plan's block count are not emitted.
+__global__ void kvx_emit_pairs_holes(const int64_t *need, const int64_t *npos, const int64_t *total,
+                                     const int32_t *remote_blk, const int64_t *rem_off, int32_t n_sessions,
+                                     int64_t n_pub, const int32_t *free_blocks, int64_t *pair_src, int64_t *pair_dst,
+                                     int64_t *pair_sess, const int64_t *n_need, const int64_t *n_counted, int32_t *err) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // the flags must account for exactly the blocks the sessions counted
+    if (k == 0 && n_pub > 0 && *n_need != *n_counted) atomicOr(err, 32);
+    if (k >= n_pub || !need[k]) return;
+    const int64_t pos = npos[k];
+    if (pos >= *total) return;
+    pair_src[pos] = remote_blk[k];
+    pair_dst[pos] = free_blocks[pos];
+    pair_sess[pos] = session_of(rem_off, n_sessions, k);
+}
+
+// Step 3: a run starts at a new session or where either block id does not continue the previous.
+__global__ void kvx_run_flags(const int64_t *pair_src, const int64_t *pair_dst, const int64_t *pair_sess,
+                              const int64_t *total, int64_t *flag) {
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= *total) return;
+    flag[p] = (p == 0 || pair_sess[p] != pair_sess[p - 1] || pair_src[p] != pair_src[p - 1] + 1 ||
+               pair_dst[p] != pair_dst[p - 1] + 1) ? 1 : 0;
 }
 
 __global__ void kvx_run_starts(const int64_t *flag, const int64_t *run_idx, const int64_t *total, int64_t *run_start) {
@@ -610,8 +688,28 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
                             const int64_t *rem_off, int32_t threshold, const int32_t *free_blocks, int64_t n_free,
                             const kvx_pool *remote_pool, const kvx_pool *local_pool, kvx_match_result *out,
                             kvx_plan_t *out_plan, cudaStream_t stream) {
+    return kvx_match_prefix_ex(tokens, tok_off, n_sessions, block_size, table, remote_hash, remote_blk, rem_off,
+                               threshold, free_blocks, n_free, remote_pool, local_pool, nullptr, out, out_plan, stream);
+}
+
+kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t block_size,
+                               kvx_table_t table, const uint64_t *remote_hash, const int32_t *remote_blk,
+                               const int64_t *rem_off, int32_t threshold, const int32_t *free_blocks, int64_t n_free,
+                               const kvx_pool *remote_pool, const kvx_pool *local_pool, const kvx_match_opts *opts,
+                               kvx_match_result *out, kvx_plan_t *out_plan, cudaStream_t stream) {
     if (out_plan) *out_plan = nullptr;
     if (n_sessions < 0 || block_size < 1 || n_free < 0) return fail(KVX_EINVAL, "bad counts");
+    MatchFlags mf = {0, nullptr, 0, nullptr};
+    if (opts) {
+        if (opts->reserved0 || opts->reserved[0] || opts->reserved[1] || opts->reserved[2] || opts->reserved[3])
+            return fail(KVX_EINVAL, "kvx_match_opts.reserved must be 0");
+        if (opts->flags & ~(KVX_MATCH_FILL_HOLES | KVX_MATCH_KEEP_LAST))
+            return fail(KVX_EINVAL, "unknown kvx_match_opts.flags bits");
+        mf.flags = opts->flags;
+        mf.expiry = opts->expiry;
+        mf.now = opts->now;
+    }
+    const bool fill = (mf.flags & KVX_MATCH_FILL_HOLES) != 0;
     if (!table) return fail(KVX_EINVAL, "NULL table");
     if (n_sessions > 0 && (!tokens || !tok_off || !rem_off || !out || !remote_hash || !remote_blk))
         return fail(KVX_EINVAL, "NULL device array");
@@ -662,6 +760,9 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
     const size_t o_rstart = take(8 * B), o_tcount = take(8 * B), o_tstart = take(8 * B);
     const size_t o_part = take(8 * n_part), o_scal = take(8 * 8), o_err = take(sizeof(int32_t) * 4);
     const size_t o_rows = take(sizeof(int32_t) * 3 * B);
+    // hole filling: residency per published block, pull flags, their scan, each pair's session
+    const size_t o_res = fill ? take(B) : 0, o_need = fill ? take(8 * B) : 0, o_npos = fill ? take(8 * B) : 0;
+    const size_t o_psess = fill ? take(8 * B) : 0;
     void *scratch = nullptr;
     kvx_status st = pool_alloc(&scratch, off, stream);
     if (st) { delete pl; return st; }
@@ -680,6 +781,10 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
     m.scalars = reinterpret_cast<int64_t *>(sb + o_scal);
     m.err = reinterpret_cast<int32_t *>(sb + o_err);
     int32_t *rows = reinterpret_cast<int32_t *>(sb + o_rows);
+    int64_t *need = fill ? reinterpret_cast<int64_t *>(sb + o_need) : nullptr;
+    int64_t *npos = fill ? reinterpret_cast<int64_t *>(sb + o_npos) : nullptr;
+    int64_t *pair_sess = fill ? reinterpret_cast<int64_t *>(sb + o_psess) : nullptr;
+    if (fill) mf.resident = sb + o_res;
 
     auto cleanup = [&](kvx_status s) {
         cudaStreamSynchronize(stream);   // nothing may still use the buffers below
@@ -692,9 +797,10 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
     ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8, stream));
     ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
     count_launch();
+    if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
     kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                     table->view(), remote_hash, rem_off, threshold,
-                                                                    n_tok_total, n_pub, out, m.push_blocks, m.err);
+                                                                    n_tok_total, n_pub, mf, out, m.push_blocks, m.err);
     ok(cudaGetLastError());
     ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
     count_launch();
@@ -737,8 +843,23 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
         TileDesc *tiles = reinterpret_cast<TileDesc *>(dev + pl->off_tiles);
 
         count_launch(4);
-        kvx_emit_pairs<<<grid_for(B, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, remote_blk, rem_off,
-                                                             free_blocks, &m.scalars[4], m.pair_src, m.pair_dst, m.flag);
+        if (!fill) {
+            kvx_emit_pairs<<<grid_for(B, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, remote_blk, rem_off,
+                                                                 free_blocks, &m.scalars[4], m.pair_src, m.pair_dst,
+                                                                 m.flag);
+        } else {
+            count_launch(3);
+            kvx_need_flags<<<grid_for(B, 256), 256, 0, stream>>>(out, rem_off, n_sessions, n_pub, mf.resident, need);
+            ok(cudaGetLastError());
+            ok(exclusive_scan(need, npos, B, nullptr, m.partial, &m.scalars[5], stream));
+            kvx_emit_pairs_holes<<<grid_for(B, 256), 256, 0, stream>>>(need, npos, &m.scalars[4], remote_blk, rem_off,
+                                                                       n_sessions, n_pub, free_blocks, m.pair_src,
+                                                                       m.pair_dst, pair_sess, &m.scalars[5],
+                                                                       &m.scalars[0], m.err);
+            ok(cudaGetLastError());
+            kvx_run_flags<<<grid_for(B, 256), 256, 0, stream>>>(m.pair_src, m.pair_dst, pair_sess, &m.scalars[4],
+                                                                m.flag);
+        }
         ok(cudaGetLastError());
         ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.partial, &m.scalars[1], stream));
         kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start);
@@ -873,7 +994,8 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
         count_launch();
         kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                         table->view(), remote_hash, rem_off, threshold,
-                                                                        n_tok_total, n_pub, out, push_blocks, err);
+                                                                        n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr},
+                                                                        out, push_blocks, err);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);

@@ -55,6 +55,13 @@ class kvx_plan_info(ctypes.Structure):
                 ("src_pitch", c_i64), ("dst_pitch", c_i64)]
 
 
+class kvx_match_opts(ctypes.Structure):
+    _fields_ = [("flags", c_i32), ("reserved0", c_i32), ("expiry", c_vp), ("now", c_i64), ("reserved", c_i64 * 4)]
+
+
+KVX_MATCH_FILL_HOLES, KVX_MATCH_KEEP_LAST = 1, 2
+
+
 class kvx_match_result(ctypes.Structure):
     _fields_ = [("local_hit_blocks", c_i32), ("remote_hit_blocks", c_i32), ("missing_tokens", c_i32),
                 ("push", c_i32), ("dst_start", c_i64)]
@@ -91,6 +98,8 @@ _sig = {
     "kvx_table_destroy": (c_i32, [c_vp]),
     "kvx_match_prefix": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
                                  _P(kvx_pool), _P(kvx_pool), c_vp, _P(c_vp), c_vp]),
+    "kvx_match_prefix_ex": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
+                                    _P(kvx_pool), _P(kvx_pool), c_vp, c_vp, _P(c_vp), c_vp]),
     "kvx_match_prefix_static": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_i64, c_vp, c_vp]),
     "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp, c_vp]),
     "kvx_version": (ctypes.c_char_p, []),
@@ -343,14 +352,24 @@ def kvx_table_destroy(table: Table) -> None:
 
 def kvx_match_prefix(tokens, tok_off, n_sessions: int, block_size: int, table: Table, remote_hash, remote_blk,
                      rem_off, recompute_threshold_tokens: int, free_blocks, n_free: int, remote_pool: Optional[Pool],
-                     local_pool: Optional[Pool], out, want_plan: bool = True, stream=None):
-    """Returns (status, Plan or None). Status is KVX_OK or KVX_ENOMEM; other statuses raise."""
+                     local_pool: Optional[Pool], out, want_plan: bool = True, stream=None, flags: int = 0,
+                     expiry=None, now: int = 0):
+    """Returns (status, Plan or None). Status is KVX_OK or KVX_ENOMEM; other statuses raise. flags,
+    expiry (device int64 per session) and now go to kvx_match_prefix_ex when given."""
     plan = c_vp()
-    st = _lib.kvx_match_prefix(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, table.handle, _ptr(remote_hash),
-                               _ptr(remote_blk), _ptr(rem_off), recompute_threshold_tokens, _ptr(free_blocks), n_free,
-                               ctypes.byref(remote_pool.struct) if remote_pool else None,
-                               ctypes.byref(local_pool.struct) if local_pool else None, _ptr(out),
-                               ctypes.byref(plan) if want_plan else None, _stream(stream))
+    if flags or expiry is not None:
+        o = kvx_match_opts(int(flags), 0, _ptr(expiry) or None, int(now))
+        st = _lib.kvx_match_prefix_ex(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, table.handle,
+                                      _ptr(remote_hash), _ptr(remote_blk), _ptr(rem_off), recompute_threshold_tokens,
+                                      _ptr(free_blocks), n_free, ctypes.byref(remote_pool.struct) if remote_pool else None,
+                                      ctypes.byref(local_pool.struct) if local_pool else None, ctypes.byref(o),
+                                      _ptr(out), ctypes.byref(plan) if want_plan else None, _stream(stream))
+    else:
+        st = _lib.kvx_match_prefix(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, table.handle,
+                                   _ptr(remote_hash), _ptr(remote_blk), _ptr(rem_off), recompute_threshold_tokens,
+                                   _ptr(free_blocks), n_free, ctypes.byref(remote_pool.struct) if remote_pool else None,
+                                   ctypes.byref(local_pool.struct) if local_pool else None, _ptr(out),
+                                   ctypes.byref(plan) if want_plan else None, _stream(stream))
     if st not in (KVX_OK, KVX_ENOMEM):
         raise KvxError(st, "kvx_match_prefix")
     n_layers = remote_pool.geom.n_layers if remote_pool else 0

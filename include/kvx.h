@@ -334,6 +334,36 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
                             kvx_plan_t *out_plan, cudaStream_t stream);
 
 /*
+ * Options of kvx_match_prefix_ex (all off when opts is NULL; kvx_match_prefix is that case).
+ *  KVX_MATCH_FILL_HOLES: blocks of [0, L_rem) that are resident locally are reused even past the
+ *    first local miss (a chained hash certifies a block's whole prefix); only the non-resident
+ *    blocks of [0, L_rem) are pulled, in order: missing_tokens = their count * block_size.
+ *  KVX_MATCH_KEEP_LAST: when the L_rem matching blocks cover every token of a session, the last of
+ *    them is recomputed instead of pulled ([P2] section 3.1: the last token is always recomputed).
+ *  expiry / now: retention of the published spans ([P3] "Block Retention TTL": a turn that arrives
+ *    after the TTL falls back to normal prefill). expiry is a device array with one entry per
+ *    session (any clock; now is on the same clock); a session with now >= expiry[s] has nothing
+ *    published. NULL: spans never expire.
+ */
+#define KVX_MATCH_FILL_HOLES 1
+#define KVX_MATCH_KEEP_LAST 2
+
+typedef struct kvx_match_opts {
+    int32_t flags;
+    int32_t reserved0;             /* must be 0 */
+    const int64_t *expiry;
+    int64_t now;
+    int64_t reserved[4];           /* must be 0 */
+} kvx_match_opts;
+
+kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                               int32_t block_size, kvx_table_t local_table, const uint64_t *remote_hash,
+                               const int32_t *remote_blk, const int64_t *rem_off,
+                               int32_t recompute_threshold_tokens, const int32_t *free_blocks, int64_t n_free,
+                               const kvx_pool *remote_pool, const kvx_pool *local_pool, const kvx_match_opts *opts,
+                               kvx_match_result *out, kvx_plan_t *out_plan, cudaStream_t stream);
+
+/*
  * kvx_match_prefix_static -- the per-session decision of kvx_match_prefix (the same
  * kvx_match_result per session, dst_start included) without allocating any memory. The pages have
  * no counterpart: this entry point exists for callers that cannot allocate device memory on the

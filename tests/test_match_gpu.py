@@ -114,19 +114,20 @@ class Case:
         self.table = kvx.kvx_table_build(dev(self.keys, np.uint64), dev(np.arange(len(self.keys), dtype=np.int32),
                                                                         np.int32), len(self.keys))
 
-    def oracle_match(self, n_free=None):
+    def oracle_match(self, n_free=None, flags=0, expiry=None, now=0):
         w = self.w
         free = w.free_blocks if n_free is None else w.free_blocks[:n_free]
         return oracle.load().match(w.tokens, w.tok_off, w.block_size, self.keys, self.remote_hash, w.remote_blk,
-                                   w.rem_off, w.threshold, free)
+                                   w.rem_off, w.threshold, free, flags=flags, expiry=expiry, now=now)
 
-    def match(self, remote_pool=None, local_pool=None, n_free=None, want_plan=True):
+    def match(self, remote_pool=None, local_pool=None, n_free=None, want_plan=True, flags=0, expiry=None, now=0):
         w = self.w
         out = torch.zeros(max(w.n_sessions, 1) * 24, dtype=torch.uint8, device="cuda")
         nf = len(w.free_blocks) if n_free is None else n_free
         st, plan = kvx.kvx_match_prefix(self.t_tokens, self.t_tok_off, w.n_sessions, w.block_size, self.table, self.t_rh,
                                         self.t_rb, self.t_ro, w.threshold, self.t_free, nf, remote_pool, local_pool, out,
-                                        want_plan=want_plan)
+                                        want_plan=want_plan, flags=flags,
+                                        expiry=None if expiry is None else dev(expiry, np.int64), now=now)
         return st, plan, results(out, w.n_sessions)
 
     def close(self):
@@ -141,8 +142,22 @@ def assert_decisions(got, want):
     assert got["dst_start"].tolist() == want["dst_start"].tolist()
 
 
+def trim_to_blocks(w, sessions):
+    """Cut the given sessions' token streams to whole blocks (their published blocks are unchanged)."""
+    parts, offs = [], [0]
+    for s in range(w.n_sessions):
+        t = w.tokens[w.tok_off[s]:w.tok_off[s + 1]]
+        if s in sessions:
+            t = t[:len(t) // w.block_size * w.block_size]
+        parts.append(t)
+        offs.append(offs[-1] + len(t))
+    w.tokens = np.concatenate(parts).astype(np.uint32)
+    w.tok_off = np.asarray(offs, np.int64)
+
+
 def oracle_requests(c, want):
-    """The pushes the oracle's match implies: one request per pushing session."""
+    """The pushes the oracle's match implies: one request per pushing session (its pulled blocks in
+    order; with hole filling they need not be consecutive session blocks, which a copy ignores)."""
     w, reqs, k = c.w, [], 0
     for s in range(w.n_sessions):
         if want["push"][s]:
@@ -327,3 +342,36 @@ def test_bidir_full_scale_in_waves():
         check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")], reqs, [0, 23, 47])
         kvx.kvx_plan_destroy(plan)
     kvx.kvx_table_destroy(table)
+
+
+
+@pytest.mark.parametrize("flags,ttl", [(kvx.KVX_MATCH_FILL_HOLES, False), (kvx.KVX_MATCH_KEEP_LAST, False),
+                                       (0, True), (kvx.KVX_MATCH_FILL_HOLES | kvx.KVX_MATCH_KEEP_LAST, True)],
+                         ids=["holes", "keep_last", "ttl", "all"])
+def test_match_options_plan_and_push(flags, ttl):
+    w = kvx_inputs.bidir_mla_fp8(seed=25, n_sessions=20, n_layers=2, system_tokens=256, hist_range=(0, 2500),
+                                 resident_p=0.5, threshold=128)
+    trim_to_blocks(w, [0, 3, 7, 12])          # these end on a block boundary, so keep-last applies
+    c = Case(w, flip_frac=0.003, seed=6)
+    expiry = np.random.default_rng(8).integers(0, 200, w.n_sessions) if ttl else None
+    want = c.oracle_match(flags=flags, expiry=expiry, now=100)
+    assert want["status"] == 0 and want["push"].sum() > 2
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=5)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst), flags=flags, expiry=expiry, now=100)
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    orc = oracle.load()
+    reqs = oracle_requests(c, want)
+    wr = [orc.block_runs(r[1], r[2]) for r in reqs]
+    rs, rd, rl = kvx.kvx_plan_runs(plan)
+    assert rs.tolist() == (np.concatenate([x[0] for x in wr]) * 64).tolist()
+    assert rd.tolist() == (np.concatenate([x[1] for x in wr]) * 64).tolist()
+    assert rl.tolist() == (np.concatenate([x[2] for x in wr]) * 64).tolist()
+    side = torch.cuda.Stream()
+    for layer in range(2):
+        kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")], reqs, range(2))
+    kvx.kvx_plan_destroy(plan)
+    c.close()
