@@ -71,6 +71,24 @@ MATCH_RESULT_DTYPE = np.dtype([("local_hit_blocks", "<i4"), ("remote_hit_blocks"
                                ("push", "<i4"), ("dst_start", "<i8")])
 assert MATCH_RESULT_DTYPE.itemsize == ctypes.sizeof(kvx_match_result)
 
+class kvx_conn_config(ctypes.Structure):
+    _fields_ = [("defer_timeout_us", c_i64), ("transfer_timeout_us", c_i64), ("recv_abort_timeout_us", c_i64),
+                ("n_ranks", c_i32), ("reserved", c_i32)]
+
+
+class kvx_conn_event(ctypes.Structure):
+    _fields_ = [("req_id", c_i64), ("attempt", c_i32), ("state", c_i32)]
+
+
+class kvx_conn_info(ctypes.Structure):
+    _fields_ = [("attempt", c_i32), ("state", c_i32), ("n_tokens", c_i64), ("n_src", c_i32), ("n_dst", c_i32),
+                ("n_chunks", c_i32), ("ranks_sealed", c_i32), ("writes_issued", c_i64), ("writes_expected", c_i64),
+                ("writes_done", c_i64), ("writes_failed", c_i64), ("n_load_errors", c_i32), ("first_error", c_i32)]
+
+
+KVX_CONN_WAITING, KVX_CONN_DEFERRED, KVX_CONN_READY, KVX_CONN_IN_FLIGHT, KVX_CONN_DONE, KVX_CONN_FAILED, \
+    KVX_CONN_EXPIRED, KVX_CONN_TIMED_OUT, KVX_CONN_ABORTED = range(9)
+
 TILE_DTYPE = np.dtype([("src_off", "<i8"), ("dst_off", "<i8"), ("n", "<i4"), ("src_shard", "<i4"),
                        ("dst_shard", "<i4"), ("pad", "<i4")])
 
@@ -101,6 +119,20 @@ _sig = {
     "kvx_match_prefix_ex": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64,
                                     _P(kvx_pool), _P(kvx_pool), c_vp, c_vp, _P(c_vp), c_vp]),
     "kvx_match_prefix_static": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_i64, c_vp, c_vp]),
+    "kvx_conn_create": (c_i32, [_P(kvx_conn_config), _P(c_vp)]),
+    "kvx_conn_destroy": (c_i32, [c_vp]),
+    "kvx_conn_register": (c_i32, [c_vp, c_i64, c_i32, _P(c_i32), c_i32, c_i64]),
+    "kvx_conn_prefill": (c_i32, [c_vp, c_i64, c_i32, _P(c_i32), c_i32, c_i64, c_i32, c_i64]),
+    "kvx_conn_poll": (c_i32, [c_vp, c_i64, _P(kvx_conn_event), c_i32, _P(c_i32)]),
+    "kvx_conn_get": (c_i32, [c_vp, c_i64, _P(kvx_conn_info)]),
+    "kvx_conn_ids": (c_i32, [c_vp, c_i64, _P(c_i32), c_i32, _P(c_i32), c_i32]),
+    "kvx_conn_start": (c_i32, [c_vp, c_i64, c_i32, c_i64]),
+    "kvx_conn_write_issued": (c_i32, [c_vp, c_i64, c_i32, c_i32, c_i32]),
+    "kvx_conn_seal": (c_i32, [c_vp, c_i64, c_i32, c_i32]),
+    "kvx_conn_write_done": (c_i32, [c_vp, c_i64, c_i32, c_i32, _P(c_i32), c_i32, _P(c_i32), c_i32, c_i64]),
+    "kvx_conn_load_errors": (c_i32, [c_vp, c_i64, _P(c_i32), c_i32, _P(c_i32)]),
+    "kvx_conn_release": (c_i32, [c_vp, c_i64]),
+    "kvx_conn_size": (c_i64, [c_vp]),
     "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp, c_vp]),
     "kvx_version": (ctypes.c_char_p, []),
     "kvx_launch_count": (c_i64, []),
@@ -391,6 +423,113 @@ def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed:
                         done=None) -> None:
     _check(_lib.kvx_fixture_prefill(ctas, iters, _ptr(buf), n_bytes, seed & (2**64 - 1), _stream(stream),
                                     _event(done)), "kvx_fixture_prefill")
+
+
+# ---------------------------------------------------------------------------------------------
+# connector state machine (host only)
+# ---------------------------------------------------------------------------------------------
+
+class Conn:
+    def __init__(self, handle: int):
+        self.handle = handle
+
+
+def _conn(conn) -> int:
+    if conn is None or not conn.handle:
+        raise ValueError("connector was destroyed")
+    return conn.handle
+
+
+def _ids(a) -> tuple:
+    """Host int32 id array (kept alive by the caller's reference) and its count."""
+    a = np.ascontiguousarray(np.asarray(a if a is not None else [], dtype=np.int32))
+    return a, a.ctypes.data_as(_P(c_i32)) if len(a) else None, len(a)
+
+
+def kvx_conn_create(defer_timeout_us: int = 0, transfer_timeout_us: int = 0, recv_abort_timeout_us: int = 0,
+                    n_ranks: int = 0) -> Conn:
+    cfg = kvx_conn_config(defer_timeout_us, transfer_timeout_us, recv_abort_timeout_us, n_ranks, 0)
+    h = c_vp()
+    _check(_lib.kvx_conn_create(ctypes.byref(cfg), ctypes.byref(h)), "kvx_conn_create")
+    return Conn(h.value)
+
+
+def kvx_conn_destroy(conn: Conn) -> None:
+    if conn.handle:
+        _check(_lib.kvx_conn_destroy(conn.handle), "kvx_conn_destroy")
+        conn.handle = None
+
+
+def kvx_conn_register(conn: Conn, req_id: int, attempt: int, dst_ids, now_us: int) -> None:
+    a, p, n = _ids(dst_ids)
+    _check(_lib.kvx_conn_register(_conn(conn), req_id, attempt, p, n, now_us), "kvx_conn_register")
+
+
+def kvx_conn_prefill(conn: Conn, req_id: int, attempt: int, src_ids, n_tokens: int, last_chunk: bool,
+                     now_us: int) -> None:
+    a, p, n = _ids(src_ids)
+    _check(_lib.kvx_conn_prefill(_conn(conn), req_id, attempt, p, n, n_tokens, int(bool(last_chunk)), now_us),
+           "kvx_conn_prefill")
+
+
+def kvx_conn_poll(conn: Conn, now_us: int, cap: int = 1024) -> list:
+    """Events as (req_id, attempt, state) tuples, in the order they happened."""
+    out = (kvx_conn_event * max(cap, 1))()
+    n = c_i32()
+    _check(_lib.kvx_conn_poll(_conn(conn), now_us, out, cap, ctypes.byref(n)), "kvx_conn_poll")
+    return [(out[i].req_id, out[i].attempt, out[i].state) for i in range(n.value)]
+
+
+def kvx_conn_get(conn: Conn, req_id: int) -> dict:
+    info = kvx_conn_info()
+    _check(_lib.kvx_conn_get(_conn(conn), req_id, ctypes.byref(info)), "kvx_conn_get")
+    return {name: getattr(info, name) for name, _ in kvx_conn_info._fields_}
+
+
+def kvx_conn_ids(conn: Conn, req_id: int) -> tuple:
+    info = kvx_conn_get(conn, req_id)
+    src = np.zeros(max(info["n_src"], 1), np.int32)
+    dst = np.zeros(max(info["n_dst"], 1), np.int32)
+    _check(_lib.kvx_conn_ids(_conn(conn), req_id, src.ctypes.data_as(_P(c_i32)), info["n_src"],
+                             dst.ctypes.data_as(_P(c_i32)), info["n_dst"]), "kvx_conn_ids")
+    return src[:info["n_src"]], dst[:info["n_dst"]]
+
+
+def kvx_conn_start(conn: Conn, req_id: int, attempt: int, now_us: int) -> None:
+    _check(_lib.kvx_conn_start(_conn(conn), req_id, attempt, now_us), "kvx_conn_start")
+
+
+def kvx_conn_write_issued(conn: Conn, req_id: int, attempt: int, rank: int, n_writes: int) -> None:
+    _check(_lib.kvx_conn_write_issued(_conn(conn), req_id, attempt, rank, n_writes), "kvx_conn_write_issued")
+
+
+def kvx_conn_seal(conn: Conn, req_id: int, attempt: int, rank: int) -> None:
+    _check(_lib.kvx_conn_seal(_conn(conn), req_id, attempt, rank), "kvx_conn_seal")
+
+
+def kvx_conn_write_done(conn: Conn, req_id: int, attempt: int, rank: int, layer_states, failed_blocks=None,
+                        now_us: int = 0) -> None:
+    s, ps, ns = _ids(layer_states)
+    f, pf, nf = _ids(failed_blocks)
+    _check(_lib.kvx_conn_write_done(_conn(conn), req_id, attempt, rank, ps, ns, pf, nf, now_us),
+           "kvx_conn_write_done")
+
+
+def kvx_conn_load_errors(conn: Conn, req_id: int) -> np.ndarray:
+    n = c_i32()
+    _check(_lib.kvx_conn_load_errors(_conn(conn), req_id, None, 0, ctypes.byref(n)), "kvx_conn_load_errors")
+    out = np.zeros(max(n.value, 1), np.int32)
+    _check(_lib.kvx_conn_load_errors(_conn(conn), req_id, out.ctypes.data_as(_P(c_i32)), n.value, ctypes.byref(n)),
+           "kvx_conn_load_errors")
+    return out[:n.value]
+
+
+def kvx_conn_release(conn: Conn, req_id: int) -> None:
+    _check(_lib.kvx_conn_release(_conn(conn), req_id), "kvx_conn_release")
+
+
+def kvx_conn_size(conn: Conn) -> int:
+    return int(_lib.kvx_conn_size(_conn(conn)))
 
 
 def library_path() -> str:

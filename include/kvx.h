@@ -386,6 +386,144 @@ kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int64_t *tok_of
                                    kvx_match_result *out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * Connector state machine (host only; no CUDA call, usable without a GPU).
+ *
+ * The protocol around the push, one record per request id:
+ *   [P1] "Implementierungsdetails" step 1 (the consumer registers its destination blocks when it
+ *        allocates them), step 2 (registration and end of prefill meet in either order; whichever
+ *        comes second triggers the transfer; matching is by request id and copes with resent,
+ *        preempted and retried requests) and step 3 (one completion per producer rank; the KV
+ *        counts as received only when all expected completions are in);
+ *   [P2] section 3.2 (a write task whose destination ids have not arrived waits on a deferred list
+ *        and is given up after defer_timeout so the producer's blocks are freed; chunked prefill
+ *        collects blocks until the last chunk; wait_for_save seals the number of writes actually
+ *        queued), section 3.1 (failed loads are reported so those blocks are recomputed), section
+ *        5 (transfer_timeout, defer_timeout, recv_abort_timeout) and section 6 (the batch state is
+ *        judged over every layer's DONE / FAILED / PENDING; with consumer TP above producer TP,
+ *        consumer_tp / producer_tp acknowledgements complete a request).
+ *
+ * States of a record (the attempt it belongs to is part of every event):
+ *
+ *   WAITING --register + last prefill chunk--> READY --kvx_conn_start--> IN_FLIGHT --all ranks
+ *      |                                                                  sealed and reported-->
+ *      +--last prefill chunk, no registration--> DEFERRED --register--> READY      DONE | FAILED
+ *   DEFERRED --defer_timeout--> EXPIRED          IN_FLIGHT --transfer_timeout--> TIMED_OUT
+ *   registered, not DONE/FAILED --recv_abort_timeout (from registration)--> ABORTED
+ *
+ * Time is the caller's: every call that can change a state takes `now_us` (any monotonic
+ * microsecond clock; tests pass a fake one). Deadlines are checked by kvx_conn_poll only.
+ * A call naming an attempt older than the record's is stale and ignored (KVX_OK, no change); a
+ * newer attempt discards the record's state and starts over (a retried or preempted request).
+ * kvx_conn_* calls may come from several host threads; one mutex per connector orders them.
+ * Records stay until kvx_conn_release.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct kvx_conn_s *kvx_conn_t;
+
+typedef enum kvx_conn_state {
+    KVX_CONN_WAITING = 0,    /* nothing yet, or only the registration (held until prefill ends)  */
+    KVX_CONN_DEFERRED = 1,   /* prefill done, no registration yet: the producer holds its blocks */
+    KVX_CONN_READY = 2,      /* both halves in: the transfer may start                           */
+    KVX_CONN_IN_FLIGHT = 3,
+    KVX_CONN_DONE = 4,       /* every rank sealed and every write it queued reported, none failed */
+    KVX_CONN_FAILED = 5,     /* as DONE, but a write reported a FAILED layer: see load errors     */
+    KVX_CONN_EXPIRED = 6,    /* defer_timeout ran out while DEFERRED: free the producer's blocks  */
+    KVX_CONN_TIMED_OUT = 7,  /* transfer_timeout ran out while IN_FLIGHT                          */
+    KVX_CONN_ABORTED = 8     /* recv_abort_timeout ran out after registration                     */
+} kvx_conn_state;
+
+typedef struct kvx_conn_config {
+    int64_t defer_timeout_us;      /* 0 selects 60 s  */
+    int64_t transfer_timeout_us;   /* 0 selects 30 s  */
+    int64_t recv_abort_timeout_us; /* 0 selects 120 s */
+    int32_t n_ranks;               /* writer ranks (acknowledgements) that complete a request; 0 selects 1 */
+    int32_t reserved;              /* must be 0 */
+} kvx_conn_config;
+
+typedef struct kvx_conn_event {
+    int64_t req_id;
+    int32_t attempt;
+    int32_t state;                 /* READY, DONE, FAILED, EXPIRED, TIMED_OUT or ABORTED */
+} kvx_conn_event;
+
+typedef struct kvx_conn_info {
+    int32_t attempt;
+    int32_t state;                 /* kvx_conn_state */
+    int64_t n_tokens;              /* tokens the producer has computed (last kvx_conn_prefill) */
+    int32_t n_src;                 /* producer block ids collected over all chunks so far */
+    int32_t n_dst;                 /* registered consumer block ids */
+    int32_t n_chunks;              /* prefill chunks received */
+    int32_t ranks_sealed;
+    int64_t writes_issued;         /* over all ranks */
+    int64_t writes_expected;       /* over the sealed ranks */
+    int64_t writes_done;           /* writes reported (failed ones included) */
+    int64_t writes_failed;
+    int32_t n_load_errors;         /* distinct consumer block ids to recompute */
+    int32_t first_error;           /* position in the registered id list of the earliest failed block; -1 if none */
+} kvx_conn_info;
+
+/* cfg may be NULL (all defaults). KVX_EINVAL for negative values or reserved != 0. */
+kvx_status kvx_conn_create(const kvx_conn_config *cfg, kvx_conn_t *out);
+kvx_status kvx_conn_destroy(kvx_conn_t conn);   /* NULL is a no-op */
+
+/* Consumer side: register the destination block ids (host array, copied). A resent registration
+ * with the same ids is a no-op; with different ids, KVX_EINVAL. Completes the rendezvous (READY)
+ * when the last prefill chunk is already in. KVX_ETIMEDOUT when this attempt already EXPIRED: the
+ * producer gave up and the consumer must prefill the request itself. */
+kvx_status kvx_conn_register(kvx_conn_t conn, int64_t req_id, int32_t attempt, const int32_t *dst_ids,
+                             int32_t n_dst, int64_t now_us);
+
+/* Producer side: one prefill chunk finished. Its block ids (host array, copied) are appended to the
+ * request's; n_tokens is the request's computed length so far. Nothing can move before the last
+ * chunk (last_chunk != 0): only then does the request become READY (registration in) or DEFERRED
+ * (not yet). A chunk after the last one: KVX_EINVAL. */
+kvx_status kvx_conn_prefill(kvx_conn_t conn, int64_t req_id, int32_t attempt, const int32_t *src_ids,
+                            int32_t n_src, int64_t n_tokens, int32_t last_chunk, int64_t now_us);
+
+/* Applies every deadline that has passed at now_us, then hands out up to cap pending events in the
+ * order they happened (*n receives the count; the rest wait for the next poll). An event whose
+ * record was released or restarted since is dropped. */
+kvx_status kvx_conn_poll(kvx_conn_t conn, int64_t now_us, kvx_conn_event *out, int32_t cap, int32_t *n);
+
+/* Snapshot of one record; KVX_EINVAL for an unknown id. */
+kvx_status kvx_conn_get(kvx_conn_t conn, int64_t req_id, kvx_conn_info *out);
+
+/* The producer (src) and consumer (dst) block ids of a record, for kvx_plan. KVX_ERANGE when a cap
+ * is smaller than n_src / n_dst. */
+kvx_status kvx_conn_ids(kvx_conn_t conn, int64_t req_id, int32_t *src, int32_t src_cap, int32_t *dst,
+                        int32_t dst_cap);
+
+/* READY -> IN_FLIGHT (the transfer_timeout clock starts). KVX_EINVAL from any other state. */
+kvx_status kvx_conn_start(kvx_conn_t conn, int64_t req_id, int32_t attempt, int64_t now_us);
+
+/* Producer rank `rank` (0 <= rank < n_ranks) queued n_writes more writes (pushes) for the request.
+ * Only while IN_FLIGHT and before that rank sealed. */
+kvx_status kvx_conn_write_issued(kvx_conn_t conn, int64_t req_id, int32_t attempt, int32_t rank,
+                                 int32_t n_writes);
+
+/* Rank `rank` queued all its writes: its expected count becomes the number it issued (a second
+ * seal is a no-op). The request completes when every rank sealed and reported all its writes. */
+kvx_status kvx_conn_seal(kvx_conn_t conn, int64_t req_id, int32_t attempt, int32_t rank);
+
+/* One write of rank `rank` finished. layer_states: the per-layer states of the layers it covered
+ * (kvx_layer_state, e.g. from kvx_plan_layer_states). All DONE: a good write. Any FAILED, even
+ * among later DONE ones: a failed write, whose consumer blocks become load errors -- the
+ * failed_blocks given (consumer ids), or every registered block when n_failed == 0. Any IDLE or
+ * PENDING: KVX_EINVAL and nothing is counted. More reports than a sealed rank issued: KVX_EINVAL. */
+kvx_status kvx_conn_write_done(kvx_conn_t conn, int64_t req_id, int32_t attempt, int32_t rank,
+                               const int32_t *layer_states, int32_t n_layers, const int32_t *failed_blocks,
+                               int32_t n_failed, int64_t now_us);
+
+/* Consumer block ids whose KV did not arrive, in the order first reported (up to cap; *n receives
+ * the full count). The consumer recomputes them. */
+kvx_status kvx_conn_load_errors(kvx_conn_t conn, int64_t req_id, int32_t *blocks, int32_t cap, int32_t *n);
+
+/* Forget a record (after its blocks were freed or handed to decode). Unknown ids are a no-op. */
+kvx_status kvx_conn_release(kvx_conn_t conn, int64_t req_id);
+
+/* Number of records held. */
+int64_t kvx_conn_size(kvx_conn_t conn);
+
+/* ------------------------------------------------------------------------------------------------
  * Synthetic prefill fixture (tests and benchmark only; not part of the transfer path).
  * Occupies `ctas` CTAs of 128 threads with a dependent integer chain of `iters` steps per thread,
  * standing in for a layer's forward compute on the main stream. If `buf` is not NULL, the CTAs
