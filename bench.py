@@ -17,6 +17,7 @@ and the consumer KV read back each step (per-layer copies overlapped with the pu
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -43,13 +44,20 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="kvx", choices=["kvx", "reference"])
     p.add_argument("--workload", default="qwen3_32b_single", choices=sorted(kvx_inputs.PUSH_WORKLOADS))
+    p.add_argument("--layers", type=int, default=0,
+                   help="build the workload with this many layers (0: its own count); for small profiling captures")
     p.add_argument("--tile-bytes", type=int, default=0)
     p.add_argument("--threads", type=int, default=0)
     p.add_argument("--kernel", type=int, default=0, help="KVX_KERNEL_*: 0 auto, 1 tile, 2 persist, 3 bulk")
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--lanes", type=int, default=0, help="internal push streams (0: library default)")
+    p.add_argument("--bulk-stages", type=int, default=0, help="bulk kernel ring stages (0: library default)")
     p.add_argument("--fixture-ctas", type=int, default=8)
     p.add_argument("--fixture-iters", type=int, default=2000)
+    p.add_argument("--fixture-graph", action="store_true",
+                   help="replay the prefill fixture from one CUDA graph per step instead of launching it layer by layer")
+    p.add_argument("--timing-every", type=int, default=4,
+                   help="record per-push timing events on every n-th timed step (1: every step)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-match", action="store_true")
@@ -182,14 +190,15 @@ def run_kvx(args, rank, local_rank, world):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
 
-    w = kvx_inputs.PUSH_WORKLOADS[args.workload]()
+    make = kvx_inputs.PUSH_WORKLOADS[args.workload]
+    w = make(n_layers=args.layers) if args.layers > 0 else make()
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
     sp, dp = kvx.Pool(w.src, src), kvx.Pool(w.dst, dst)
     reqs = requests(w)
     opts = {"tile_bytes": args.tile_bytes, "threads": args.threads, "kernel": args.kernel,
-            "ctas_per_sm": args.ctas_per_sm, "lanes": args.lanes}
+            "ctas_per_sm": args.ctas_per_sm, "lanes": args.lanes, "bulk_stages": args.bulk_stages}
     # the synthetic prefill is the latency-critical path: its stream outranks the push stream, so the
     # copies fill the SMs the compute leaves free
     main = torch.cuda.Stream(priority=-1)
@@ -203,48 +212,71 @@ def run_kvx(args, rank, local_rank, world):
     blocks_step = sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L
 
     K, W = args.steps, args.warmup
-    opts["flags"] = kvx.KVX_PLAN_TIMING
+    every = max(1, args.timing_every)
+    timing_opts = dict(opts, flags=kvx.KVX_PLAN_TIMING)
     ready = [torch.cuda.Event() for _ in range(L)]
     for ev in ready:                                  # materialise the events so their handles exist
         ev.record(main)
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
-    lib = kvx._lib                                    # the C-ABI itself: two calls per layer in the loop
+    lib = kvx._lib                                    # the C-ABI itself, called directly in the loop
     push_raw_us, push_busy_us, issue_us = [], [], []
 
-    def issue():
-        """One step's plan and its per-layer issue: fixture then gated push, layer by layer."""
-        plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
-        for layer in range(L):
-            st = lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h, ready_h[layer])
-            st |= lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer])
-            if st:
-                raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
+    # The synthetic prefill: per layer a fixture kernel on the priority stream that records the
+    # layer's ready event, launched layer by layer from the host between the pushes (an engine
+    # issuing its forward pass); --fixture-graph captures the L launches once into a CUDA graph and
+    # replays it per step instead.
+    fixture_graph = None
+    if args.fixture_graph:
+        cap = torch.cuda.Stream(priority=-1)
+        fixture_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fixture_graph, stream=cap):
+            for layer in range(L):
+                if lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer,
+                                           int(cap.cuda_stream), ready_h[layer]):
+                    raise RuntimeError(f"fixture capture failed: {kvx.kvx_last_error()}")
+        torch.cuda.synchronize()
+
+    def issue(timing):
+        """One step: its plan, the prefill (graph replay or per-layer launches) and the gated pushes."""
+        plan = kvx.kvx_plan_ex(sp, dp, reqs, timing_opts if timing else opts)
+        if fixture_graph is not None:
+            fixture_graph.replay()                    # on the current stream: main
+            for layer in range(L):
+                if lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer]):
+                    raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
+        else:
+            for layer in range(L):
+                st = lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h,
+                                             ready_h[layer])
+                st |= lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer])
+                if st:
+                    raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
         return plan
 
-    def finish(plan, timed):
+    def finish(plan, timing):
         st = kvx.kvx_sync(plan, -1)
         if st != kvx.KVX_OK:
             raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
-        if timed:
+        if timing:
             s_us, e_us = kvx.kvx_plan_push_times(plan)
-            push_raw_us.extend((e_us - s_us).tolist())
-            push_busy_us.append(union_us(s_us, e_us))
+            push_raw_us.append((s_us, e_us))
         kvx.kvx_plan_destroy(plan)
 
     def run_steps(n, timed):
         """n steps, each synced after the next one is issued (one request in flight behind another)."""
         prev = None
-        for _ in range(n):
+        for i in range(n):
+            timing = timed and i % every == 0
             h0 = time.perf_counter()
-            plan = issue()
+            plan = issue(timing)
             if timed:
                 issue_us.append((time.perf_counter() - h0) * 1e6)
             if prev is not None:
-                finish(prev, timed)
-            prev = plan
+                finish(*prev)
+            prev = (plan, timing)
         if prev is not None:
-            finish(prev, timed)
+            finish(*prev)
 
     run_steps(W, False)
     torch.cuda.synchronize()
@@ -261,6 +293,8 @@ def run_kvx(args, rank, local_rank, world):
     launches0 = kvx.kvx_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    gc.collect()
+    gc.disable()                                      # no collector pauses inside the timed loop
     wall0 = time.perf_counter()
     t0.record(main)
     run_steps(K, True)
@@ -268,13 +302,19 @@ def run_kvx(args, rank, local_rank, world):
     t1.record(main)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    gc.enable()
     launches = kvx.kvx_launch_count() - launches0
+    if fixture_graph is not None:
+        launches += K * L                             # the fixture kernels the graph replays launched
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    assert len(push_raw_us) == K * L
+    assert len(push_raw_us) == -(-K // every)
+    for s_us, e_us in push_raw_us:
+        push_busy_us.append(union_us(s_us, e_us))
+    push_raw_us = [float(x) for s_us, e_us in push_raw_us for x in (e_us - s_us)]
     # pushes of consecutive layers may overlap (they run on separate lanes): the time the GPU spends
     # pushing is the union of their intervals; per launch that is union / launches
-    mean_push_ms = sum(push_busy_us) / (K * L) * 1e-3
+    mean_push_ms = sum(push_busy_us) / (len(push_busy_us) * L) * 1e-3
     raw_push_ms = statistics.fmean(push_raw_us) * 1e-3
     if world > 1:
         elapsed_ms, launches = reduce_over_ranks(elapsed_ms, launches, device)
@@ -302,12 +342,14 @@ def run_kvx(args, rank, local_rank, world):
             "requests": len(reqs), "tokens": int(sum(n for n, _, _ in reqs)),
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
-            "lanes": info["lanes"],
+            "lanes": info["lanes"], "bulk_stages": info["bulk_stages"],
             "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "auto (1 bulk / 2 persistent below 128 MiB per launch)",
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
-                      "stream "
-                      "records the layer's event; kvx_push_layer(priority 0 side stream, event) forks onto the push lanes and "
+                      "stream records the layer's event ("
+                      + (f"the {L} launches replayed from one CUDA graph per step, events as external graph nodes"
+                         if args.fixture_graph else "launched layer by layer from the host")
+                      + "); kvx_push_layer(priority 0 side stream, event) per layer forks onto the push lanes and "
                       "waits for it; a plan is built every step and synced after the next step is issued",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -315,10 +357,13 @@ def run_kvx(args, rank, local_rank, world):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-            "kernel": "kvx_copy_tiles (one launch per layer)",
+            "kernel": ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"][info["kernel"]]
+                      + " (one launch per layer)",
             "raw_launch_us_mean": round(raw_push_ms * 1e3, 3),
-            "timing": "KVX_PLAN_TIMING start/end events around every timed launch; mean_launch_us = union of the "
-                      "step's launch intervals (consecutive layers overlap on the push lanes) / launches",
+            "timing": ("KVX_PLAN_TIMING start/end events around every launch of "
+                       + ("every timed step" if every == 1 else f"every {every}th timed step")
+                       + "; mean_launch_us = union of the step's launch intervals (consecutive layers overlap on "
+                       "the push lanes) / launches"),
             "bytes_per_launch": 2 * info["bytes_per_layer"], "mean_launch_us": round(mean_push_ms * 1e3, 3),
             "traffic": ncu_traffic(args.workload),
         },
@@ -332,7 +377,9 @@ def run_kvx(args, rank, local_rank, world):
         if not args.no_e2e:
             result["e2e"] = run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world)
         if not args.no_match:
-            result["match"] = run_match(torch, kvx, device)
+            result["match"] = run_match(torch, kvx, device, {"kernel": args.kernel, "threads": args.threads,
+                                                             "ctas_per_sm": args.ctas_per_sm,
+                                                             "bulk_stages": args.bulk_stages})
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if world > 1:
@@ -428,7 +475,7 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
                    "host wall clock with device sync on both sides (rank 0)"}
 
 
-def run_match(torch, kvx, device):
+def run_match(torch, kvx, device, push_opts=None):
     """Prefix match of the bidirectional workload (256 sessions, 1024 shared + U[2k,32k] history tokens,
     block 64): decode publishes block hashes (kvx_block_hashes), prefill keeps a Bernoulli(0.4) subset
     in its table, kvx_match_prefix decides per session and builds the decode->prefill plan, which is
@@ -477,7 +524,8 @@ def run_match(torch, kvx, device):
     res = out.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
     info = kvx.kvx_plan_get_info(plan)
     side = torch.cuda.Stream()
-    kvx.kvx_plan_set_opts(plan, {"flags": kvx.KVX_PLAN_TIMING})
+    kvx.kvx_plan_set_opts(plan, dict(push_opts or {}, flags=kvx.KVX_PLAN_TIMING))
+    info = kvx.kvx_plan_get_info(plan)
     kvx.kvx_push_layer(plan, 0, side)
     kvx.kvx_sync(plan, -1)
     push_ms = []
@@ -499,6 +547,7 @@ def run_match(torch, kvx, device):
         "hashed_blocks": n_pub, "pushing_sessions": int(res["push"].sum()),
         "push_blocks": int(res["missing_tokens"].sum() // 64), "runs": info["n_runs"],
         "dp_push_gbs_one_layer": round(2 * info["bytes_per_layer"] / (statistics.median(push_ms) * 1e-3) / 1e9, 1),
+        "dp_push_kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]], "dp_push_tile_bytes": info["tile_bytes"],
         "how": "host wall clock per kvx_match_prefix call (it waits for its stream); hashes and push with CUDA events",
     }
 

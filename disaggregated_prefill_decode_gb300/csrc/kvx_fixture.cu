@@ -41,7 +41,13 @@ extern "C" kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "fixture launch");
     if (done) {
-        e = cudaEventRecord(done, stream);
+        // inside a stream capture the record becomes an event-record node of the graph, so that
+        // every replay records `done` where this launch sits
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing(fixture)");
+        e = cudaEventRecordWithFlags(done, stream,
+                                     cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fixture)");
     }
     return KVX_OK;

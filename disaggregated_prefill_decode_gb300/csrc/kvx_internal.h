@@ -93,8 +93,14 @@ struct LaunchShape {
     int32_t threads;
     int32_t tile_bytes;    // bulk: bytes per stage
     int32_t ctas_per_sm;   // 0: occupancy limit
+    int32_t stages;        // bulk: ring stages (2, 3, 4, 6 or 8)
 };
 cudaError_t launch_copy(const CopyArgs &args, int32_t n_layers, const LaunchShape &shape, cudaStream_t stream);
+
+// Bulk ring: stage counts with a kernel instantiation, and the most shared memory one ring may take
+// (two rings of an overlapping push then still fit an SM's 228 KiB only when each is <= 113 KiB).
+constexpr int64_t kBulkRingMax = 192 << 10;
+inline bool valid_stages(int32_t s) { return s == 0 || s == 2 || s == 3 || s == 4 || s == 6 || s == 8; }
 
 }  // namespace kvx
 
@@ -113,11 +119,14 @@ struct kvx_plan_s {
     int32_t vec = 16;
     int32_t width = 0;
     int32_t tile_bytes = 16384;
-    int32_t threads = 256;
+    int32_t threads = 256;                     // resolved threads per CTA of TILE / PERSIST
+    int32_t threads_req = 0;                   // threads asked for (0: by plan size)
     int32_t flags = 0;                         // KVX_PLAN_* bits
     int32_t kernel = 0;                        // resolved KVX_KERNEL_*
     int32_t ctas_per_sm = 0;                   // resident CTAs per SM of persistent kernels (0: by size)
     int32_t lanes = 4;                         // internal streams pushes fan out over
+    int32_t bulk_stages_req = 0;               // ring stages asked for (0: by plan kind)
+    int32_t bulk_stages = 4;                   // ring stages of the bulk kernel, resolved
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
     cudaStream_t lane_src = nullptr;           // caller stream the cached lanes below were chosen for

@@ -228,6 +228,25 @@ static void build_tiles(kvx_plan_s *pl, const std::vector<Pair> &pairs) {
     pl->n_tiles = (int64_t)pl->tiles.size();
 }
 
+// Default tile of a contiguous plan. Runs are cut at the block boundaries of both sides, so the usual
+// run is a whole number of "units" of min(block sizes) token rows. A unit above 16 KiB is split into
+// the fewest equal tiles of at most 16 KiB (a 36,864-byte MLA block: 3 x 12 KiB rather than
+// 16 + 16 + 4 KiB, whose short tail wastes a bulk-ring stage); smaller units are packed whole.
+static int32_t default_tile_bytes(const Geom &s, const Geom &d) {
+    constexpr int64_t kTarget = 16384;
+    const int64_t unit = (int64_t)std::min(s.block_size, d.block_size) * s.row_bytes();
+    int64_t t;
+    if (unit >= kTarget) {
+        const int64_t k = ceil_div(unit, kTarget);
+        t = ceil_div(unit, k);
+        t = ceil_div(t, 16) * 16;
+        if (t > kTarget) t = kTarget;
+    } else {
+        t = unit * std::max<int64_t>(1, kTarget / unit);
+    }
+    return (int32_t)std::max<int64_t>(16, t - t % 16);
+}
+
 kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl) {
     kvx_status st = read_geom(src, "producer", &pl->src, &pl->src_base);
     if (st) return st;
@@ -246,11 +265,12 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
     if (st) return st;
     if (opts) {
-        for (int i = 0; i < 2; ++i)
-            if (opts->reserved[i]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+        if (opts->reserved) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+        if (!valid_stages(opts->bulk_stages)) return fail(KVX_EINVAL, "bulk_stages must be 0, 2, 3, 4, 6 or 8");
         if (opts->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
         if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
         if (opts->threads) pl->threads = opts->threads;
+        pl->threads_req = opts->threads;
         pl->flags = opts->flags;
         if (opts->kernel < 0 || opts->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", opts->kernel);
         if (opts->ctas_per_sm < 0 || opts->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
@@ -258,6 +278,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         pl->kernel = opts->kernel;
         if (opts->ctas_per_sm) pl->ctas_per_sm = opts->ctas_per_sm;
         if (opts->lanes) pl->lanes = opts->lanes;
+        pl->bulk_stages_req = opts->bulk_stages;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
@@ -268,27 +289,44 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     pl->width = (int32_t)(pl->per_head ? s.head_bytes() : std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
     pl->src_pitch = pl->per_head ? s.token_pitch() : s.row_bytes();
     pl->dst_pitch = pl->per_head ? d.token_pitch() : d.row_bytes();
+    if (!(opts && opts->tile_bytes) && !pl->strided) pl->tile_bytes = default_tile_bytes(s, d);
     pl->layer_state.assign(s.n_layers, KVX_LAYER_IDLE);
     pl->inject.assign(s.n_layers, 0);
     pl->injected_pending.assign(s.n_layers, 0);
     return KVX_OK;
 }
 
-// Bulk copies need 16-byte aligned addresses and sizes and a stage that fits shared memory; the
-// automatic choice takes them whenever they apply (measured fastest with other work running).
-static int32_t resolve_kernel(const kvx_plan_s *pl) {
-    const bool bulk_ok = !pl->strided && pl->vec == 16 && pl->tile_bytes <= (48 << 10);
-    const int32_t k = pl->kernel == KVX_KERNEL_AUTO ? (bulk_ok ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
-    if (k == KVX_KERNEL_BULK && !bulk_ok) return KVX_KERNEL_PERSIST;
-    return k;
+// Bulk copies need 16-byte aligned addresses, sizes, widths and pitches (vec == 16), a ring that
+// fits shared memory and, for strided plans, a row that fits a stage. The automatic choice, measured
+// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at one CTA per SM
+// (it leaves room for the caller's compute and the next push), a larger one with the persistent
+// kernel at 128 threads per CTA and the occupancy limit of CTAs (many small independent CTAs).
+constexpr int64_t kLargeLayer = (int64_t)128 << 20;
+
+static void resolve_kernel(kvx_plan_s *pl) {
+    const bool bulk_ok = pl->vec == 16 && (int64_t)pl->tile_bytes * pl->bulk_stages <= kBulkRingMax &&
+                         (!pl->strided || pl->width <= pl->tile_bytes);
+    const bool large = pl->bytes_per_layer >= kLargeLayer;
+    const bool automatic = pl->kernel == KVX_KERNEL_AUTO;
+    int32_t k = automatic ? (bulk_ok && !large ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
+    if (k == KVX_KERNEL_BULK && !bulk_ok) k = KVX_KERNEL_PERSIST;
+    pl->kernel = k;
+    pl->threads = pl->threads_req ? pl->threads_req : (automatic && large ? 128 : 256);
+}
+
+// Default ring depth: measured on GB300, strided tiles (rows scattered on one side) run fastest with
+// a 3-stage ring (four CTAs per SM fit beside each other), contiguous ones with 4.
+static void resolve_stages(kvx_plan_s *pl) {
+    pl->bulk_stages = pl->bulk_stages_req ? pl->bulk_stages_req : (pl->strided ? 3 : 4);
 }
 
 void finish_plan_shape(kvx_plan_s *pl) {
     pl->vec = vector_bytes(pl, shard_pairs(pl->src, pl->dst));
-    pl->kernel = resolve_kernel(pl);
     int64_t toks = 0;
     for (int32_t n : pl->run_ntok) toks += n;
     pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
+    resolve_stages(pl);
+    resolve_kernel(pl);
 }
 
 }  // namespace kvx
@@ -384,7 +422,8 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     if (!pl || !o) return fail(KVX_EINVAL, "NULL argument");
     if (!pl->pending.empty()) return fail(KVX_EINVAL, "pushes are pending; kvx_sync first");
     if (o->tile_bytes && o->tile_bytes != pl->tile_bytes) return fail(KVX_EINVAL, "tile_bytes is fixed once tiles exist");
-    if (o->reserved[0] || o->reserved[1]) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+    if (o->reserved) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+    if (!valid_stages(o->bulk_stages)) return fail(KVX_EINVAL, "bulk_stages must be 0, 2, 3, 4, 6 or 8");
     if (o->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
     if (o->kernel < 0 || o->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", o->kernel);
     if (o->ctas_per_sm < 0 || o->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
@@ -398,13 +437,16 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     }
     pl->flags = o->flags;
     if (o->threads) pl->threads = o->threads;
+    pl->threads_req = o->threads;
     pl->ctas_per_sm = o->ctas_per_sm;
     pl->lanes = o->lanes ? o->lanes : 4;
+    pl->bulk_stages_req = o->bulk_stages;
+    resolve_stages(pl);
     pl->next_lane = 0;
     pl->lane_cache.clear();
     pl->lane_src = nullptr;
     pl->kernel = o->kernel;
-    pl->kernel = resolve_kernel(pl);
+    resolve_kernel(pl);
     return KVX_OK;
 }
 
@@ -432,7 +474,7 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->kernel = pl->kernel;
     out->threads = pl->kernel == KVX_KERNEL_BULK ? 32 : pl->threads;
     out->lanes = pl->lanes;
-    out->reserved = 0;
+    out->bulk_stages = pl->kernel == KVX_KERNEL_BULK ? pl->bulk_stages : 0;
     out->src_pitch = pl->src_pitch;
     out->dst_pitch = pl->dst_pitch;
     return KVX_OK;

@@ -140,14 +140,16 @@ __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_w
 }
 
 // ------------------------------------------------------------------------------------------------
-// KVX_KERNEL_BULK: bulk asynchronous copies through shared memory (contiguous, 16-byte aligned).
-// One thread per CTA drives a ring of kBulkStages stages: the load of an item lands in its stage
+// KVX_KERNEL_BULK: bulk asynchronous copies through shared memory (16-byte aligned).
+// One thread per CTA drives a ring of STAGES stages: the load of an item lands in its stage
 // and completes the stage's mbarrier (transaction count = bytes); the thread then issues the bulk
 // store of that stage and, once the store before it has finished reading its stage, the load of a
 // later item into that freed stage. Waits are bounded by the global timer.
+// A strided tile (rows of `width` bytes at each side's pitch) is packed densely in its stage: a side
+// whose pitch equals the width moves in one bulk copy, the other side row by row, all rows of a
+// load completing on the stage's one mbarrier and all row stores forming one bulk group.
 // ------------------------------------------------------------------------------------------------
 
-constexpr int kBulkStages = 4;
 constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -209,9 +211,11 @@ struct BulkItem {
     const uint8_t *src;
     uint8_t *dst;
     uint32_t bytes;    // 0: skipped (out of bounds or misaligned)
+    int32_t rows;      // strided tiles: rows of a.width bytes; contiguous tiles: 1
     int32_t layer;
 };
 
+template <bool STRIDED>
 __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int32_t stage_bytes) {
     int64_t tile, lp;
     BulkItem it;
@@ -220,21 +224,27 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     it.src = nullptr;
     it.dst = nullptr;
     it.bytes = 0;
-    if (!tile_in_bounds<false>(t, a) || t.n > stage_bytes) {
+    it.rows = STRIDED ? t.n : 1;
+    const int64_t bytes = STRIDED ? (int64_t)t.n * a.width : (int64_t)t.n;
+    if (!tile_in_bounds<STRIDED>(t, a) || bytes > stage_bytes) {
         if (t.n != 0) atomicOr(&a.err[it.layer], 1);
         return it;
     }
     it.src = a.src_base[lp * a.src_shards + t.s_shard] + t.src_off;
     it.dst = a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off;
-    if ((((uintptr_t)it.src) | ((uintptr_t)it.dst) | (uintptr_t)t.n) & 15) {
+    uintptr_t mis = ((uintptr_t)it.src) | ((uintptr_t)it.dst) | (uintptr_t)bytes;
+    if (STRIDED) mis |= (uintptr_t)a.width | (uintptr_t)a.src_pitch | (uintptr_t)a.dst_pitch;
+    if (mis & 15) {
         atomicOr(&a.err[it.layer], 1);
         return it;
     }
-    it.bytes = (uint32_t)t.n;
+    it.bytes = (uint32_t)bytes;
     return it;
 }
 
+template <int STAGES, bool STRIDED>
 __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, int32_t stage_bytes) {
+    constexpr int kBulkStages = STAGES;
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t bar[kBulkStages];
     if (threadIdx.x != 0) return;
@@ -244,11 +254,21 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     const int64_t n_mine = (int64_t)blockIdx.x < n_work ? (n_work - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     BulkItem items[kBulkStages];
     // item i of this CTA is work item blockIdx.x + i * gridDim.x, in stage i % kBulkStages
+    const bool src_packed = !STRIDED || a.src_pitch == a.width;    // one bulk copy per tile on that side
+    const bool dst_packed = !STRIDED || a.dst_pitch == a.width;
     auto issue = [&](int64_t i) {
         const int s = (int)(i % kBulkStages);
-        items[s] = bulk_item(a, blockIdx.x + i * gridDim.x, stage_bytes);
-        mbar_arrive_expect(&bar[s], items[s].bytes);
-        if (items[s].bytes) bulk_load(ring + (size_t)s * stage_bytes, items[s].src, items[s].bytes, &bar[s]);
+        const BulkItem it = bulk_item<STRIDED>(a, blockIdx.x + i * gridDim.x, stage_bytes);
+        items[s] = it;
+        mbar_arrive_expect(&bar[s], it.bytes);
+        if (!it.bytes) return;
+        uint8_t *stage = ring + (size_t)s * stage_bytes;
+        if (src_packed) {
+            bulk_load(stage, it.src, it.bytes, &bar[s]);
+        } else {
+            for (int32_t r = 0; r < it.rows; ++r)
+                bulk_load(stage + (size_t)r * a.width, it.src + (int64_t)r * a.src_pitch, (uint32_t)a.width, &bar[s]);
+        }
     };
     int64_t issued = 0;
     for (; issued < n_mine && issued < kBulkStages - 1; ++issued) issue(issued);
@@ -262,11 +282,17 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         }
         if (items[s].bytes) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            bulk_store(items[s].dst, ring + (size_t)s * stage_bytes, items[s].bytes);
+            const uint8_t *stage = ring + (size_t)s * stage_bytes;
+            if (dst_packed) {
+                bulk_store(items[s].dst, stage, items[s].bytes);
+            } else {
+                for (int32_t r = 0; r < items[s].rows; ++r)
+                    bulk_store(items[s].dst + (int64_t)r * a.dst_pitch, stage + (size_t)r * a.width, (uint32_t)a.width);
+            }
         }
         bulk_commit();
         if (issued < n_mine) {
-            bulk_wait_read_1();   // the store issued one item ago has read the stage the next load reuses
+            bulk_wait_read_1();   // the stores issued one item ago have read the stage the next load reuses
             issue(issued);
             ++issued;
         }
@@ -315,8 +341,9 @@ static cudaError_t resident_grid(const void *fn, int threads, int smem, int per_
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        if (smem > 48 * 1024) {
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (smem > 0) {
+            // one limit per kernel, large enough for every ring it may be launched with
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkRingMax);
             if (e != cudaSuccess) return e;
         }
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
@@ -326,6 +353,21 @@ static cudaError_t resident_grid(const void *fn, int threads, int smem, int per_
     const int sms = it->second / 1000, per_sm = it->second % 1000;
     *grid = sms * (per_sm_cap > 0 ? std::min(per_sm_cap, per_sm) : per_sm);
     return cudaSuccess;
+}
+
+template <bool STRIDED>
+static const void *bulk_fn_of(int stages) {
+    switch (stages) {
+        case 2: return (const void *)kvx_copy_bulk<2, STRIDED>;
+        case 3: return (const void *)kvx_copy_bulk<3, STRIDED>;
+        case 6: return (const void *)kvx_copy_bulk<6, STRIDED>;
+        case 8: return (const void *)kvx_copy_bulk<8, STRIDED>;
+        default: return (const void *)kvx_copy_bulk<4, STRIDED>;
+    }
+}
+
+static const void *bulk_fn(int stages, bool strided) {
+    return strided ? bulk_fn_of<true>(stages) : bulk_fn_of<false>(stages);
 }
 
 template <int VEC>
@@ -340,12 +382,16 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     int grid = 0;
     cudaError_t e;
     if (sh.kernel == KVX_KERNEL_BULK) {
-        const int smem = kBulkStages * sh.tile_bytes;
+        const int smem = sh.stages * sh.tile_bytes;
         const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 1 : 64);
-        e = resident_grid((const void *)kvx_copy_bulk, 32, smem, cap, &grid);
+        const void *fn = bulk_fn(sh.stages, sh.strided != 0);
+        e = resident_grid(fn, 32, smem, cap, &grid);
         if (e != cudaSuccess) return e;
-        kvx_copy_bulk<<<(unsigned)std::min<int64_t>(grid, n_work), 32, smem, st>>>(a, n_work, sh.tile_bytes);
-        return cudaGetLastError();
+        CopyArgs args_copy = a;
+        int64_t work = n_work;
+        int32_t stage_bytes = sh.tile_bytes;
+        void *args[] = {&args_copy, &work, &stage_bytes};
+        return cudaLaunchKernel(fn, dim3((unsigned)std::min<int64_t>(grid, n_work)), dim3(32), args, (size_t)smem, st);
     }
     // default resident CTAs: small launches stay small so that they overlap the caller's compute and
     // the next push; large ones take the whole GPU
@@ -609,7 +655,8 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
             return cuda_fail(e, "cudaEventRecord(push start)");
         }
     }
-    const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm};
+    const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
+                            pl->bulk_stages};
     e = launch_copy(plan_copy_args(pl, l0), l1 - l0, shape, stream);
     if (e != cudaSuccess) {
         if (start) pl->free_events.push_back(start);

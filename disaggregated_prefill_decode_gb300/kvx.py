@@ -41,7 +41,7 @@ class kvx_request(ctypes.Structure):
 
 class kvx_plan_opts(ctypes.Structure):
     _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("flags", c_i32), ("kernel", c_i32), ("ctas_per_sm", c_i32),
-                ("lanes", c_i32), ("reserved", c_i32 * 2)]
+                ("lanes", c_i32), ("bulk_stages", c_i32), ("reserved", c_i32)]
 
 
 KVX_PLAN_TIMING = 1
@@ -51,7 +51,7 @@ KVX_KERNEL_AUTO, KVX_KERNEL_TILE, KVX_KERNEL_PERSIST, KVX_KERNEL_BULK = range(4)
 class kvx_plan_info(ctypes.Structure):
     _fields_ = [("n_runs", c_i64), ("n_tiles", c_i64), ("bytes_per_layer", c_i64), ("vec_bytes", c_i32),
                 ("strided", c_i32), ("n_layers", c_i32), ("n_planes", c_i32), ("width", c_i32),
-                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("reserved", c_i32),
+                ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("bulk_stages", c_i32),
                 ("src_pitch", c_i64), ("dst_pitch", c_i64)]
 
 
@@ -263,12 +263,20 @@ def kvx_plan(src: Pool, dst: Pool, requests: Iterable) -> Plan:
     return kvx_plan_ex(src, dst, requests, None)
 
 
+_OPT_KEYS = ("tile_bytes", "threads", "flags", "kernel", "ctas_per_sm", "lanes", "bulk_stages")
+
+
+def _opts(opts: dict) -> kvx_plan_opts:
+    unknown = set(opts) - set(_OPT_KEYS)
+    if unknown:
+        raise ValueError(f"unknown plan options {sorted(unknown)}")
+    return kvx_plan_opts(*(int(opts.get(k, 0)) for k in _OPT_KEYS), 0)
+
+
 def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] = None) -> Plan:
     carr, n, _keep = _requests(requests)
     out = c_vp()
-    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0)), int(opts.get("flags", 0)),
-                      int(opts.get("kernel", 0)), int(opts.get("ctas_per_sm", 0)), int(opts.get("lanes", 0))) \
-        if opts else None
+    o = _opts(opts) if opts else None
     st = _lib.kvx_plan_ex(ctypes.byref(src.struct), ctypes.byref(dst.struct), carr, n,
                           ctypes.byref(o) if o is not None else None, ctypes.byref(out))
     _check(st, "kvx_plan")
@@ -276,8 +284,7 @@ def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] =
 
 
 def kvx_plan_set_opts(plan, opts: dict) -> None:
-    o = kvx_plan_opts(int(opts.get("tile_bytes", 0)), int(opts.get("threads", 0)), int(opts.get("flags", 0)),
-                      int(opts.get("kernel", 0)), int(opts.get("ctas_per_sm", 0)), int(opts.get("lanes", 0)))
+    o = _opts(opts)
     _check(_lib.kvx_plan_set_opts(_h(plan), ctypes.byref(o)), "kvx_plan_set_opts")
 
 

@@ -103,8 +103,12 @@ typedef struct kvx_plan_s *kvx_plan_t;
 
 /* Tuning knobs of a plan; zero fields take the defaults. */
 typedef struct kvx_plan_opts {
-    int32_t tile_bytes;       /* bytes one CTA copies per tile (default 16384; multiple of 16)  */
-    int32_t threads;          /* threads per CTA (default 256; multiple of 32, <= 1024)         */
+    int32_t tile_bytes;       /* bytes one CTA copies per tile (multiple of 16). Default: 16384 for
+                                 strided plans; for contiguous ones the block-row unit
+                                 (min block size x row bytes) split into the fewest equal tiles
+                                 of at most 16384 bytes, or whole units packed up to 16384     */
+    int32_t threads;          /* threads per CTA of TILE / PERSIST (multiple of 32, <= 1024;
+                                 default 256, or 128 where AUTO picks PERSIST for a large push) */
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
@@ -112,14 +116,20 @@ typedef struct kvx_plan_opts {
                                  with PERSIST, leaving room for the caller's compute and an
                                  overlapping push; the occupancy limit for larger launches) */
     int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
-    int32_t reserved[2];      /* must be 0 */
+    int32_t bulk_stages;      /* BULK: shared-memory ring stages of tile_bytes each, one of 2, 3, 4,
+                                 6, 8 with stages * tile_bytes <= 192 KiB (0: 4 for contiguous
+                                 plans, 3 for strided ones)                                     */
+    int32_t reserved;         /* must be 0 */
 } kvx_plan_opts;
 
 /* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
  * loading the next descriptor while it copies the current tile. BULK: the same walk with the bulk
- * asynchronous copy engine (global -> shared -> global through a ring of mbarrier-tracked stages);
- * contiguous plans with 16-byte alignment only, others fall back to PERSIST. AUTO picks BULK where it
- * applies and PERSIST elsewhere. */
+ * asynchronous copy engine (global -> shared -> global through a ring of mbarrier-tracked stages;
+ * strided tiles move row by row on a side whose rows are not adjacent); plans whose buffer bases,
+ * offsets, widths and pitches are all 16-byte aligned, with a row no larger than tile_bytes; others
+ * fall back to PERSIST. AUTO picks BULK where it applies to a plan that reads under 128 MiB per layer
+ * (one CTA per SM, leaving room for the caller's compute and the next push) and PERSIST with 128
+ * threads per CTA otherwise (measured fastest on GB300 for large layer pushes). */
 #define KVX_KERNEL_AUTO 0
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2
@@ -186,7 +196,7 @@ typedef struct kvx_plan_info {
     int32_t kernel;              /* the KVX_KERNEL_* the pushes use */
     int32_t threads;
     int32_t lanes;
-    int32_t reserved;
+    int32_t bulk_stages;         /* ring stages of the BULK kernel; 0 for the others */
     int64_t src_pitch;           /* strided plans: bytes between consecutive rows of a tile, producer */
     int64_t dst_pitch;           /* and consumer side */
 } kvx_plan_info;
@@ -529,6 +539,8 @@ int64_t kvx_conn_size(kvx_conn_t conn);
  * standing in for a layer's forward compute on the main stream. If `buf` is not NULL, the CTAs
  * then rewrite buf[0 .. n_bytes) (device, 16-byte aligned, n_bytes a multiple of 16) with a pattern
  * derived from `seed`, so a push that ran before the fixture finished would copy stale bytes.
+ * May be called while `stream` is being captured into a CUDA graph: `done` is then recorded by an
+ * external event-record node on every replay (the launch counter counts the capture only).
  * ---------------------------------------------------------------------------------------------- */
 kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes, uint64_t seed,
                                cudaStream_t stream, cudaEvent_t done /* recorded after it when not NULL */);

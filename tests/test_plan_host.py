@@ -245,11 +245,50 @@ def test_kernel_resolution():
     sp8 = kvx.Pool(g, [(1 << 40) + 8, (1 << 40) + 8 + (1 << 30)])
     assert kern({"kernel": kvx.KVX_KERNEL_BULK}, sp8, dp) == kvx.KVX_KERNEL_PERSIST                  # 8-byte aligned
     gs, gd = PoolGeom(1, 2, 2, 4, 128, 2, 16, 8), PoolGeom(1, 2, 1, 8, 128, 2, 16, 8)
-    assert kern({"kernel": kvx.KVX_KERNEL_BULK}, fake_pool(gs, 1 << 40), fake_pool(gd, 1 << 44)) == \
-        kvx.KVX_KERNEL_PERSIST                                                                       # strided
+    assert kern({}, fake_pool(gs, 1 << 40), fake_pool(gd, 1 << 44)) == kvx.KVX_KERNEL_BULK          # strided
+    p = kvx.kvx_plan_ex(fake_pool(gs, 1 << 40), fake_pool(gd, 1 << 44), [ok], None)
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 3                         # strided default ring
+    kvx.kvx_plan_destroy(p)
+    assert kern({"tile_bytes": 512}, fake_pool(gs, 1 << 40), fake_pool(gd, 1 << 44)) == \
+        kvx.KVX_KERNEL_PERSIST                                                  # a 1024-byte row exceeds the stage
+    gs8 = PoolGeom(1, 2, 2, 1, 4, 2, 16, 8)                                     # 8-byte rows: not 16-byte aligned
+    gd8 = PoolGeom(1, 2, 1, 2, 4, 2, 16, 8)
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK}, fake_pool(gs8, 1 << 40), fake_pool(gd8, 1 << 44)) == \
+        kvx.KVX_KERNEL_PERSIST
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"kernel": 9}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"ctas_per_sm": 99}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"lanes": 9}))
     p = kvx.kvx_plan(sp, dp, [ok])
     assert kvx.kvx_plan_get_info(p)["lanes"] == 4
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 4
+    kvx.kvx_plan_destroy(p)
+    # AUTO by size: a layer push reading >= 128 MiB runs PERSIST with 128 threads unless asked otherwise
+    gl = PoolGeom(1, 2, 1, 8, 128, 2, 16, 5000)
+    big = (40000, list(range(2500)), list(range(2500)))                        # 40000 x 2 KiB x 2 planes
+    def shape(opts):
+        p = kvx.kvx_plan_ex(fake_pool(gl, 1 << 40), fake_pool(gl, 1 << 44), [big], opts)
+        i = kvx.kvx_plan_get_info(p)
+        kvx.kvx_plan_destroy(p)
+        return i["kernel"], i["threads"], i["bytes_per_layer"]
+    assert shape(None) == (kvx.KVX_KERNEL_PERSIST, 128, 40000 * 2048 * 2)
+    assert shape({"threads": 512})[:2] == (kvx.KVX_KERNEL_PERSIST, 512)
+    assert shape({"kernel": kvx.KVX_KERNEL_BULK})[:2] == (kvx.KVX_KERNEL_BULK, 32)
+    assert shape({"kernel": kvx.KVX_KERNEL_PERSIST})[:2] == (kvx.KVX_KERNEL_PERSIST, 256)
+    small = (32767 // 2, list(range(2500)), list(range(2500)))                 # just under 128 MiB
+    p = kvx.kvx_plan_ex(fake_pool(gl, 1 << 40), fake_pool(gl, 1 << 44), [small], None)
+    assert kvx.kvx_plan_get_info(p)["kernel"] == kvx.KVX_KERNEL_BULK
+    kvx.kvx_plan_destroy(p)
+    # ring stages: only instantiated counts; a ring over 192 KiB leaves the bulk kernel
+    for bad in (1, 5, 7, 9, -1):
+        expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"bulk_stages": bad}))
+    assert kern({"bulk_stages": 8, "tile_bytes": 24576}) == kvx.KVX_KERNEL_BULK             # 192 KiB
+    assert kern({"bulk_stages": 8, "tile_bytes": 24592}) == kvx.KVX_KERNEL_PERSIST          # just over
+    assert kern({"bulk_stages": 2, "tile_bytes": 49152}) == kvx.KVX_KERNEL_BULK
+    p = kvx.kvx_plan_ex(sp, dp, [ok], {"bulk_stages": 6})
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 6
+    kvx.kvx_plan_set_opts(p, {"bulk_stages": 3})
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 3
+    kvx.kvx_plan_set_opts(p, {"kernel": kvx.KVX_KERNEL_PERSIST})
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 0                                     # not a bulk plan
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_set_opts(p, {"bulk_stages": 5}))
     kvx.kvx_plan_destroy(p)

@@ -81,7 +81,7 @@ def test_reduced_workloads_all_layers(make, kernel):
     w = make()
     info = run_workload(w, range(w.src.n_layers), opts={"kernel": KERNELS[kernel]})
     assert info["vec_bytes"] == 16
-    want = KERNELS[kernel] if not (kernel == "bulk" and info["strided"]) else KERNELS["persist"]
+    want = KERNELS[kernel]                                   # strided plans run the bulk kernel too
     assert info["kernel"] == want
 
 
@@ -90,6 +90,16 @@ def test_lanes(lanes):
     w = kvx_inputs.qwen3_32b_batched(n_layers=6, n_requests=4, len_range=(500, 3000))
     info = run_workload(w, range(6), opts={"lanes": lanes})
     assert info["lanes"] == lanes
+
+
+@pytest.mark.parametrize("stages,tile_bytes", [(2, 49152), (3, 16384), (6, 8192), (8, 24576), (8, 4096)])
+def test_bulk_ring_stages(stages, tile_bytes):
+    w = kvx_inputs.qwen3_32b_batched(n_layers=2, n_requests=4, len_range=(100, 2000))
+    info = run_workload(w, range(2), opts={"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": tile_bytes,
+                                           "bulk_stages": stages})
+    assert (info["kernel"], info["bulk_stages"]) == (kvx.KVX_KERNEL_BULK, stages)
+    run_workload(w, range(2), opts={"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": tile_bytes, "bulk_stages": stages},
+                 per_layer=False)
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -214,6 +224,41 @@ def test_push_ordered_after_prefill_rewrite():
     check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
                  range(4))
     kvx.kvx_plan_destroy(plan)
+
+
+def test_push_ordered_after_graph_replayed_prefill():
+    """The prefill captured once into a CUDA graph (each layer's ready event an external event-record
+    node) and replayed per step, the push of every layer gated on its event. Before each replay the
+    producer is zeroed and the consumer re-filled with canaries on the main stream, so a push that ran
+    ahead of the replay's rewrite would leave zeros behind; the consumer must equal the oracle."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=3)
+    src, src_big = device_pool(w.src, w.values, seed=w.seed)
+    dst, dst_big = device_pool(w.dst, "canary_" + w.values)
+    cap = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(3)]
+    for ev in ready:
+        ev.record()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for layer in range(3):
+            for b in layer_buffers(w.src, src, layer):
+                kvx.kvx_fixture_prefill(16, 20000, b, b.numel(), seed=500 + layer, stream=cap)
+            kvx.kvx_fixture_prefill(1, 1, stream=cap, done=ready[layer])
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(priority=-1)
+    for rep in range(3):
+        src_big.zero_()
+        kvx_inputs.fill_canary(dst_big, w.values)
+        g.replay()
+        plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+        for layer in range(3):
+            kvx.kvx_push_layer(plan, layer, side, ready[layer])
+        assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+        kvx.kvx_plan_destroy(plan)
+        main.synchronize()
+        assert not all(bool((b == 0).all()) for b in layer_buffers(w.src, src, 2))   # the replay rewrote it
+        check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)],
+                     reqs_of(w), range(3))
 
 
 def test_sync_timeout_then_completion():
