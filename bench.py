@@ -58,7 +58,7 @@ def parse():
                    help="replay the prefill fixture from one CUDA graph per step instead of launching it layer by layer")
     p.add_argument("--timing-every", type=int, default=4,
                    help="record per-push timing events on every n-th timed step (1: every step)")
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-match", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -421,43 +421,58 @@ def memcpy_ceiling(torch, device):
 
 
 def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world):
-    """Producer KV from pinned host memory, per layer: H2D copy, push, D2H of the consumer layer, on
-    three streams so the copies overlap the pushes; plan built and synced each step."""
+    """Producer KV from pinned host memory, per layer: H2D copy of the producer layer, push into the
+    consumer pool, gather of the pushed consumer blocks (a second kvx plan, consumer -> a dense staging
+    pool in request order) and D2H of that staging layer, on three streams so that copies in both
+    directions overlap the pushes; plans built and synced each step. The result read back is exactly
+    the pushed blocks; for equal layouts it must equal the producer blocks, which is checked."""
     L, P = w.src.n_layers, w.src.n_planes * w.src.n_shards
     bb_s = w.src.block_size * w.src.row_bytes
-    bb_d = w.dst.block_size * w.dst.row_bytes
     s_lo = min(int(r[1][:-(-r[0] // w.src.block_size)].min()) for r in reqs if r[0] > 0)
     s_hi = max(int(r[1][:-(-r[0] // w.src.block_size)].max()) for r in reqs if r[0] > 0) + 1
-    d_lo = min(int(r[2][:-(-r[0] // w.dst.block_size)].min()) for r in reqs if r[0] > 0)
-    d_hi = max(int(r[2][:-(-r[0] // w.dst.block_size)].max()) for r in reqs if r[0] > 0) + 1
-    s_rng, d_rng = (s_lo * bb_s, s_hi * bb_s), (d_lo * bb_d, d_hi * bb_d)
+    s_rng = (s_lo * bb_s, s_hi * bb_s)
+    # staging: the requests' consumer blocks, densely, in request order
+    nb = [-(-n // w.dst.block_size) for n, _, _ in reqs]
+    off = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+    stage_geom = w.dst.replace(n_blocks=int(off[-1]))
+    stage_reqs = [(n, d[:k], np.arange(off[i], off[i] + k, dtype=np.int32))
+                  for i, ((n, _, d), k) in enumerate(zip(reqs, nb))]
+    per = -(-stage_geom.buffer_bytes // 512) * 512
+    stage_big = torch.empty(per * stage_geom.n_buffers, dtype=torch.uint8, device=src[0].device)
+    stage = [stage_big[i * per:i * per + stage_geom.buffer_bytes] for i in range(stage_geom.n_buffers)]
+    stp = kvx.Pool(stage_geom, stage)
     host_src = [torch.empty(s_rng[1] - s_rng[0], dtype=torch.uint8, pin_memory=True) for _ in range(len(src))]
-    host_dst = [torch.empty(d_rng[1] - d_rng[0], dtype=torch.uint8, pin_memory=True) for _ in range(len(dst))]
+    host_dst = [torch.empty(stage_geom.buffer_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(len(stage))]
     for h, d in zip(host_src, src):
         h.copy_(d[s_rng[0]:s_rng[1]])
     h2d, side, d2h = torch.cuda.Stream(), torch.cuda.Stream(priority=-1), torch.cuda.Stream()
     ev_h = [torch.cuda.Event() for _ in range(L)]
     ev_p = [torch.cuda.Event() for _ in range(L)]
-    for ev in ev_h + ev_p:                              # materialise the event handles
+    ev_g = [torch.cuda.Event() for _ in range(L)]
+    for ev in ev_h + ev_p + ev_g:                       # materialise the event handles
         ev.record(h2d)
-    nd = w.dst.n_planes * w.dst.n_shards
+    nd = stage_geom.n_planes * stage_geom.n_shards
 
     def step():
         plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
+        gather = kvx.kvx_plan_ex(dp, stp, stage_reqs, opts)
         for layer in range(L):
             with torch.cuda.stream(h2d):
                 for i in range(layer * P, (layer + 1) * P):
                     src[i][s_rng[0]:s_rng[1]].copy_(host_src[i], non_blocking=True)
                 ev_h[layer].record(h2d)
             kvx.kvx_push_layer_notify(plan, layer, layer + 1, side, ev_h[layer], ev_p[layer])
+            kvx.kvx_push_layer_notify(gather, layer, layer + 1, side, ev_p[layer], ev_g[layer])
             with torch.cuda.stream(d2h):
-                d2h.wait_event(ev_p[layer])
+                d2h.wait_event(ev_g[layer])
                 for i in range(layer * nd, (layer + 1) * nd):
-                    host_dst[i].copy_(dst[i][d_rng[0]:d_rng[1]], non_blocking=True)
+                    host_dst[i].copy_(stage[i], non_blocking=True)
         st = kvx.kvx_sync(plan, -1)
+        st2 = kvx.kvx_sync(gather, -1)
         d2h.synchronize()
         kvx.kvx_plan_destroy(plan)
-        assert st == kvx.KVX_OK
+        kvx.kvx_plan_destroy(gather)
+        assert st == kvx.KVX_OK and st2 == kvx.KVX_OK
 
     for _ in range(2):
         step()
@@ -467,12 +482,21 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
         step()
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t) / args.e2e_steps
+    checked = None
+    if w.src == w.dst.replace(n_blocks=w.src.n_blocks) and all(
+            np.array_equal(np.asarray(r[1][:k]), np.arange(s_lo, s_lo + k)) for r, k in zip(reqs[:1], nb[:1])):
+        # equal layouts, first request's producer blocks contiguous from s_lo: its gathered tokens must
+        # equal those producer bytes, for the first and last buffer
+        n0 = int(reqs[0][0]) * w.src.row_bytes if w.src.layout == kvx_inputs.LAYOUT_NHD else 0
+        checked = all(torch.equal(host_dst[i][:n0], host_src[i][:n0]) for i in (0, len(host_dst) - 1))
+        assert checked, "e2e result read back differs from the producer KV"
     return {"value": round(bytes_step / dt / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": sum(h.numel() for h in host_src),
             "d2h_bytes_per_step": sum(h.numel() for h in host_dst),
-            "ms_per_step": round(dt * 1e3, 3), "steps": args.e2e_steps,
-            "how": "pinned host producer KV -> H2D per layer -> kvx_push_layer -> D2H consumer layer, 3 streams, "
-                   "host wall clock with device sync on both sides (rank 0)"}
+            "ms_per_step": round(dt * 1e3, 3), "steps": args.e2e_steps, "result_checked": checked,
+            "how": "pinned host producer KV -> H2D per layer -> kvx_push_layer -> kvx gather of the pushed consumer "
+                   "blocks into a dense staging pool -> D2H, 3 streams, each step synced before the next; host wall "
+                   "clock with device sync on both sides (rank 0)"}
 
 
 def run_match(torch, kvx, device, push_opts=None):
