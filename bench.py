@@ -63,6 +63,7 @@ def parse():
     p.add_argument("--no-match", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true", help="skip the short runs of the other push configs")
     return p.parse_args()
 
 
@@ -180,18 +181,12 @@ def alloc_pool(torch, geom, fill, seed, device):
     return [big[i * per:i * per + geom.buffer_bytes] for i in range(geom.n_buffers)], big
 
 
-def run_kvx(args, rank, local_rank, world):
-    import torch
-    import torch.distributed as dist
-    from disaggregated_prefill_decode_gb300 import kvx
-
-    device = torch.device(f"cuda:{local_rank}")
-    torch.cuda.set_device(device)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=device)
-
-    make = kvx_inputs.PUSH_WORKLOADS[args.workload]
-    w = make(n_layers=args.layers) if args.layers > 0 else make()
+def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, barrier=None):
+    """Allocates the workload's pools and times K steps of the per-layer push pattern after W untimed
+    ones. A step builds the requests' plan, runs the synthetic prefill (per layer a fixture kernel on
+    the priority stream that records the layer's ready event) and pushes every layer gated on its
+    event; each step is synced after the next one is issued. Per-push timing events are recorded on
+    every `every`-th timed step."""
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
@@ -208,11 +203,6 @@ def run_kvx(args, rank, local_rank, world):
     probe = kvx.kvx_plan_ex(sp, dp, reqs, opts)
     info = kvx.kvx_plan_get_info(probe)
     kvx.kvx_plan_destroy(probe)
-    bytes_step = 2 * info["bytes_per_layer"] * L                       # read + write
-    blocks_step = sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L
-
-    K, W = args.steps, args.warmup
-    every = max(1, args.timing_every)
     timing_opts = dict(opts, flags=kvx.KVX_PLAN_TIMING)
     ready = [torch.cuda.Event() for _ in range(L)]
     for ev in ready:                                  # materialise the events so their handles exist
@@ -220,10 +210,9 @@ def run_kvx(args, rank, local_rank, world):
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
     lib = kvx._lib                                    # the C-ABI itself, called directly in the loop
-    push_raw_us, push_busy_us, issue_us = [], [], []
+    push_times, issue_us = [], []
 
-    # The synthetic prefill: per layer a fixture kernel on the priority stream that records the
-    # layer's ready event, launched layer by layer from the host between the pushes (an engine
+    # The synthetic prefill is launched layer by layer from the host between the pushes (an engine
     # issuing its forward pass); --fixture-graph captures the L launches once into a CUDA graph and
     # replays it per step instead.
     fixture_graph = None
@@ -259,8 +248,7 @@ def run_kvx(args, rank, local_rank, world):
         if st != kvx.KVX_OK:
             raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
         if timing:
-            s_us, e_us = kvx.kvx_plan_push_times(plan)
-            push_raw_us.append((s_us, e_us))
+            push_times.append(kvx.kvx_plan_push_times(plan))
         kvx.kvx_plan_destroy(plan)
 
     def run_steps(n, timed):
@@ -280,16 +268,11 @@ def run_kvx(args, rank, local_rank, world):
 
     run_steps(W, False)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid)
-    clocks.start()
-    time.sleep(0.3)
+    if barrier:
+        barrier()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     launches0 = kvx.kvx_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -306,16 +289,72 @@ def run_kvx(args, rank, local_rank, world):
     launches = kvx.kvx_launch_count() - launches0
     if fixture_graph is not None:
         launches += K * L                             # the fixture kernels the graph replays launched
-    clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    assert len(push_raw_us) == -(-K // every)
-    for s_us, e_us in push_raw_us:
-        push_busy_us.append(union_us(s_us, e_us))
-    push_raw_us = [float(x) for s_us, e_us in push_raw_us for x in (e_us - s_us)]
+    clk = sampler.stop() if sampler else None
+    assert len(push_times) == -(-K // every)
     # pushes of consecutive layers may overlap (they run on separate lanes): the time the GPU spends
     # pushing is the union of their intervals; per launch that is union / launches
-    mean_push_ms = sum(push_busy_us) / (len(push_busy_us) * L) * 1e-3
-    raw_push_ms = statistics.fmean(push_raw_us) * 1e-3
+    busy_us = [union_us(s_us, e_us) for s_us, e_us in push_times]
+    raw_us = [float(x) for s_us, e_us in push_times for x in (e_us - s_us)]
+    torch.cuda.set_stream(torch.cuda.default_stream(device))
+    return {"w": w, "L": L, "src": src, "dst": dst, "sp": sp, "dp": dp, "reqs": reqs, "opts": opts, "info": info,
+            "bytes_step": 2 * info["bytes_per_layer"] * L,                     # read + write
+            "blocks_step": sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L,
+            "elapsed_ms": t0.elapsed_time(t1), "launches": launches, "clocks": clk, "wall": wall,
+            "mean_push_ms": sum(busy_us) / (len(busy_us) * L) * 1e-3, "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
+            "issue_us": issue_us}
+
+
+KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"]
+
+
+def per_config(args, torch, kvx, device):
+    """The other push configurations, briefly, in the same run: GB/s and blocks/s per step, the push
+    kernel's roofline fraction (union of push intervals, timing events on every step)."""
+    peak, _ = measured_peak()
+    out = []
+    for name, steps in (("tiny", 200), ("qwen3_32b_batched", 20), ("tp4_to_tp1_remap", 20),
+                        ("qwen3_32b_batched_hnd", 20)):
+        if name == args.workload:
+            continue
+        m = time_push_workload(args, torch, kvx, kvx_inputs.PUSH_WORKLOADS[name](), device, steps, 3, 1)
+        achieved = 2 * m["info"]["bytes_per_layer"] / (m["mean_push_ms"] * 1e-3) / 1e9
+        out.append({"workload": name, "steps": steps,
+                    "value": round(m["bytes_step"] * steps / (m["elapsed_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "blocks_per_s": round(m["blocks_step"] * steps / (m["elapsed_ms"] * 1e-3), 1),
+                    "roofline_frac": round(achieved / peak, 4), "mean_launch_us": round(m["mean_push_ms"] * 1e3, 3),
+                    "kernel": KERNEL_NAMES[m["info"]["kernel"]], "threads": m["info"]["threads"],
+                    "bytes_per_launch": 2 * m["info"]["bytes_per_layer"],
+                    "traffic": ncu_traffic(name)})
+        del m
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_kvx(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+    from disaggregated_prefill_decode_gb300 import kvx
+
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    make = kvx_inputs.PUSH_WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    every = max(1, args.timing_every)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    m = time_push_workload(args, torch, kvx, make(n_layers=args.layers) if args.layers > 0 else make(), device,
+                           K, W, every, sampler=ClockSampler(uuid), barrier=dist.barrier if world > 1 else None)
+    w, L, info, reqs = m["w"], m["L"], m["info"], m["reqs"]
+    src, dst, sp, dp, opts, bytes_step = m["src"], m["dst"], m["sp"], m["dp"], m["opts"], m["bytes_step"]
+    elapsed_ms, launches = m["elapsed_ms"], m["launches"]
+    mean_push_ms, raw_push_ms = m["mean_push_ms"], m["raw_push_ms"]
     if world > 1:
         elapsed_ms, launches = reduce_over_ranks(elapsed_ms, launches, device)
 
@@ -353,12 +392,11 @@ def run_kvx(args, rank, local_rank, world):
                       "waits for it; a plan is built every step and synced after the next step is issued",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "blocks_per_s": round(world * blocks_step * K / (elapsed_ms * 1e-3), 1),
+        "blocks_per_s": round(world * m["blocks_step"] * K / (elapsed_ms * 1e-3), 1),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-            "kernel": ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"][info["kernel"]]
-                      + " (one launch per layer)",
+            "kernel": KERNEL_NAMES[info["kernel"]] + " (one launch per layer)",
             "raw_launch_us_mean": round(raw_push_ms * 1e3, 3),
             "timing": ("KVX_PLAN_TIMING start/end events around every launch of "
                        + ("every timed step" if every == 1 else f"every {every}th timed step")
@@ -368,9 +406,9 @@ def run_kvx(args, rank, local_rank, world):
             "traffic": ncu_traffic(args.workload),
         },
         "gpu_launches": launches,
-        "clocks": clk,
-        "host_wall_s": round(wall, 4),
-        "host_issue_us_per_layer": round(statistics.fmean(issue_us) / L, 3),
+        "clocks": m["clocks"],
+        "host_wall_s": round(m["wall"], 4),
+        "host_issue_us_per_layer": round(statistics.fmean(m["issue_us"]) / L, 3),
     }
     if rank == 0:
         result["memcpy_ceiling"] = memcpy_ceiling(torch, device)
@@ -382,6 +420,9 @@ def run_kvx(args, rank, local_rank, world):
                                                              "bulk_stages": args.bulk_stages})
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        if not args.no_per_config:
+            del m, src, dst, sp, dp
+            result["per_config"] = per_config(args, torch, kvx, device)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
