@@ -56,8 +56,8 @@ def parse():
     p.add_argument("--fixture-iters", type=int, default=2000)
     p.add_argument("--fixture-graph", action="store_true",
                    help="replay the prefill fixture from one CUDA graph per step instead of launching it layer by layer")
-    p.add_argument("--timing-every", type=int, default=4,
-                   help="record per-push timing events on every n-th timed step (1: every step)")
+    p.add_argument("--timing-every", type=int, default=1,
+                   help="time the pushes of every n-th timed step only (1: every step)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-match", action="store_true")
@@ -248,7 +248,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
         if st != kvx.KVX_OK:
             raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
         if timing:
-            push_times.append(kvx.kvx_plan_push_times(plan))
+            push_times.append(kvx.kvx_plan_push_times_ns(plan))
         kvx.kvx_plan_destroy(plan)
 
     def run_steps(n, timed):
@@ -291,16 +291,21 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
         launches += K * L                             # the fixture kernels the graph replays launched
     clk = sampler.stop() if sampler else None
     assert len(push_times) == -(-K // every)
-    # pushes of consecutive layers may overlap (they run on separate lanes): the time the GPU spends
-    # pushing is the union of their intervals; per launch that is union / launches
-    busy_us = [union_us(s_us, e_us) for s_us, e_us in push_times]
-    raw_us = [float(x) for s_us, e_us in push_times for x in (e_us - s_us)]
+    # Pushes of consecutive layers (and of consecutive steps) may overlap: they run on separate lanes.
+    # The kernels stamp the GPU's one global timer, so all timed pushes share a timeline; the time the
+    # GPU spends pushing is the union of their intervals, per launch that union / launches.
+    all_s = np.concatenate([s_ns for s_ns, _ in push_times])
+    all_e = np.concatenate([e_ns for _, e_ns in push_times])
+    t_base = all_s.min()                              # int64 first: the timer's epoch is far from zero
+    all_s, all_e = (all_s - t_base) * 1e-3, (all_e - t_base) * 1e-3
+    busy_us = union_us(all_s, all_e)
+    raw_us = (all_e - all_s).tolist()
     torch.cuda.set_stream(torch.cuda.default_stream(device))
     return {"w": w, "L": L, "src": src, "dst": dst, "sp": sp, "dp": dp, "reqs": reqs, "opts": opts, "info": info,
             "bytes_step": 2 * info["bytes_per_layer"] * L,                     # read + write
             "blocks_step": sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L,
             "elapsed_ms": t0.elapsed_time(t1), "launches": launches, "clocks": clk, "wall": wall,
-            "mean_push_ms": sum(busy_us) / (len(busy_us) * L) * 1e-3, "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
+            "mean_push_ms": busy_us / (len(push_times) * L) * 1e-3, "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
             "issue_us": issue_us}
 
 
@@ -398,10 +403,11 @@ def run_kvx(args, rank, local_rank, world):
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "kernel": KERNEL_NAMES[info["kernel"]] + " (one launch per layer)",
             "raw_launch_us_mean": round(raw_push_ms * 1e3, 3),
-            "timing": ("KVX_PLAN_TIMING start/end events around every launch of "
+            "timing": ("KVX_PLAN_TIMING: each copy kernel stamps the GPU global timer (first CTA start, last "
+                       "CTA end) for every launch of "
                        + ("every timed step" if every == 1 else f"every {every}th timed step")
-                       + "; mean_launch_us = union of the step's launch intervals (consecutive layers overlap on "
-                       "the push lanes) / launches"),
+                       + "; mean_launch_us = union of all those launch intervals on that one timeline "
+                       "(consecutive layers and steps overlap on the push lanes) / launches"),
             "bytes_per_launch": 2 * info["bytes_per_layer"], "mean_launch_us": round(mean_push_ms * 1e3, 3),
             "traffic": ncu_traffic(args.workload),
         },

@@ -33,6 +33,8 @@ struct CopyArgs {
     int64_t dst_buf_bytes;
     int64_t src_pitch;                // producer row bytes
     int64_t dst_pitch;                // consumer row bytes
+    unsigned long long *ts_start;     // timing: atomicMin of %globaltimer at each CTA's start (or null)
+    unsigned long long *ts_end;       // timing: atomicMax of %globaltimer at each CTA's end
     int32_t width;                    // strided: bytes copied per row
     int32_t n_planes;
     int32_t src_shards;
@@ -59,9 +61,12 @@ struct Geom {
 
 struct PendingPush {
     cudaEvent_t done;
-    cudaEvent_t start;      // timing plans only
+    int32_t slot;           // timing plans: index of its global-timer stamps, -1 when not timed
     int32_t layer_begin, layer_end;
 };
+
+// Timing plans: pushes between two syncs that can carry global-timer stamps.
+constexpr int32_t kTimingSlots = 4096;
 
 // Head-shard pair: the contiguous head range one producer shard shares with one consumer shard, as
 // byte offsets inside a producer row and a consumer row.
@@ -149,6 +154,8 @@ struct kvx_plan_s {
     std::vector<kvx::PendingPush> pending;
     std::vector<cudaEvent_t> free_events;
     std::vector<float> push_start_us, push_end_us;   // timing plans: confirmed by the last sync
+    std::vector<int64_t> push_start_ns, push_end_ns; // the same, raw device global-timer values
+    unsigned long long *ts = nullptr;                // timing stamps: [kTimingSlots] starts, then ends
     std::vector<int32_t> layer_state;          // kvx_layer_state per layer
     std::vector<uint8_t> inject;               // host fault injection armed, per layer
     std::vector<uint8_t> injected_pending;     // injected failure waiting for sync, per layer

@@ -430,11 +430,6 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     if (o->lanes < 0 || o->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
     if (o->threads && (o->threads < 32 || o->threads > 1024 || o->threads % 32))
         return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
-    if ((o->flags ^ pl->flags) & KVX_PLAN_TIMING) {
-        // events are created with or without timing: hand the plan's spares back to the pool
-        for (cudaEvent_t ev : pl->free_events) event_give((pl->flags & KVX_PLAN_TIMING) != 0, ev);
-        pl->free_events.clear();
-    }
     pl->flags = o->flags;
     if (o->threads) pl->threads = o->threads;
     pl->threads_req = o->threads;
@@ -494,6 +489,17 @@ kvx_status kvx_plan_push_times(kvx_plan_t pl, float *start_us, float *end_us, in
     for (int32_t i = 0; i < *n && i < cap; ++i) {
         start_us[i] = pl->push_start_us[i];
         end_us[i] = pl->push_end_us[i];
+    }
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_push_times_ns(kvx_plan_t pl, int64_t *start_ns, int64_t *end_ns, int32_t cap, int32_t *n) {
+    if (!pl || !n || (cap > 0 && (!start_ns || !end_ns))) return fail(KVX_EINVAL, "NULL argument");
+    if (!(pl->flags & KVX_PLAN_TIMING)) return fail(KVX_EINVAL, "plan was built without KVX_PLAN_TIMING");
+    *n = (int32_t)pl->push_start_ns.size();
+    for (int32_t i = 0; i < *n && i < cap; ++i) {
+        start_ns[i] = pl->push_start_ns[i];
+        end_ns[i] = pl->push_end_ns[i];
     }
     return KVX_OK;
 }

@@ -93,6 +93,28 @@ __device__ __forceinline__ void copy_tile(const TileDesc &t, const uint8_t *src,
     }
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Timing plans: every CTA folds the device's global timer into its push's slot when it starts
+// (minimum) and when it is done (maximum), so a slot ends up holding the span from the first CTA's
+// start to the last CTA's end. One clock serves the whole GPU; no host call is involved.
+__device__ __forceinline__ void stamp_start(const CopyArgs &a) {
+    if (a.ts_start && threadIdx.x == 0) atomicMin(a.ts_start, (unsigned long long)global_ns());
+}
+
+// Called by every thread of the CTA (the test on a kernel argument is uniform). Each thread's stores
+// are made visible device-wide before the stamp, so the span covers them.
+__device__ __forceinline__ void stamp_end(const CopyArgs &a) {
+    if (!a.ts_end) return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(a.ts_end, (unsigned long long)global_ns());
+}
+
 // Work item w of a launch: tile w % n_tiles of plane (w / n_tiles) % n_planes of layer
 // layer0 + w / (n_tiles * n_planes). Consecutive items are consecutive tiles of one buffer pair.
 __device__ __forceinline__ void decode_item(const CopyArgs &a, int64_t w, int64_t *tile, int32_t *layer, int64_t *lp) {
@@ -106,15 +128,17 @@ __device__ __forceinline__ void decode_item(const CopyArgs &a, int64_t w, int64_
 // KVX_KERNEL_TILE: one CTA per (tile, plane, layer).
 template <int VEC, bool STRIDED>
 __global__ void __launch_bounds__(1024) kvx_copy_tiles(CopyArgs a) {
+    stamp_start(a);
     const TileDesc t = a.tiles[blockIdx.x];
     const int32_t layer = a.layer0 + (int32_t)blockIdx.z;
     const int64_t lp = (int64_t)layer * a.n_planes + blockIdx.y;
     if (!tile_in_bounds<STRIDED>(t, a)) {
         if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
-        return;
+    } else {
+        copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
+                                a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
     }
-    copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
-                            a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
+    stamp_end(a);
 }
 
 // KVX_KERNEL_PERSIST: a resident grid walks the work items; each CTA loads the next item's
@@ -123,6 +147,7 @@ template <int VEC, bool STRIDED>
 __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_work) {
     int64_t w = blockIdx.x;
     if (w >= n_work) return;
+    stamp_start(a);
     TileDesc next = a.tiles[w % a.n_tiles];
     for (; w < n_work; w += gridDim.x) {
         const TileDesc t = next;
@@ -137,6 +162,7 @@ __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_w
         copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
                                 a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
     }
+    stamp_end(a);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -153,12 +179,6 @@ __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_w
 constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
@@ -248,6 +268,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t bar[kBulkStages];
     if (threadIdx.x != 0) return;
+    stamp_start(a);
     for (int s = 0; s < kBulkStages; ++s) mbar_init(&bar[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
@@ -304,7 +325,8 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
             mbar_wait(&bar[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1));
         }
     }
-    bulk_wait_all();
+    bulk_wait_all();   // the stores have completed, not only read their stages
+    if (a.ts_end) atomicMax(a.ts_end, (unsigned long long)global_ns());
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -543,6 +565,8 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.src_base = reinterpret_cast<const uint8_t *const *>(base + pl->off_src);
     a.dst_base = reinterpret_cast<uint8_t *const *>(base + pl->off_dst);
     a.err = reinterpret_cast<int32_t *>(base + pl->off_err);
+    a.ts_start = nullptr;
+    a.ts_end = nullptr;
     a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();
@@ -595,14 +619,31 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     return KVX_OK;
 }
 
-// Timing plans use timing-enabled events for both ends of a push; other plans only need completion.
+// Stamp slots of a timing plan: kTimingSlots starts (set to all ones, folded with atomicMin) then
+// kTimingSlots ends (zero, folded with atomicMax), allocated and set on `stream` at the first timed push.
+static kvx_status reset_timing_slots(kvx_plan_s *pl, int32_t n, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(pl->ts, 0xFF, sizeof(unsigned long long) * (size_t)n, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(pl->ts + kTimingSlots, 0, sizeof(unsigned long long) * (size_t)n, stream);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e, "cudaMemsetAsync(timing slots)");
+}
+
+static kvx_status ensure_timing_slots(kvx_plan_s *pl, cudaStream_t stream) {
+    if (pl->ts) return KVX_OK;
+    void *p = nullptr;
+    kvx_status st = pool_alloc(&p, sizeof(unsigned long long) * 2 * (size_t)kTimingSlots, stream);
+    if (st) return st;
+    pl->ts = static_cast<unsigned long long *>(p);
+    return reset_timing_slots(pl, kTimingSlots, stream);
+}
+
+// Completion events; timing comes from the kernels' own global-timer stamps.
 static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
     if (!pl->free_events.empty()) {
         *ev = pl->free_events.back();
         pl->free_events.pop_back();
         return KVX_OK;
     }
-    return event_take((pl->flags & KVX_PLAN_TIMING) != 0, ev);
+    return event_take(false, ev);
 }
 
 extern "C" {
@@ -615,6 +656,14 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
     kvx_status st = ensure_device(pl, stream);
     if (st) return st;
     cudaError_t e;
+    // timing plans: the push's global-timer slot (stamps live in a buffer set up on the caller's
+    // stream before the fork, so every lane sees it initialised)
+    int32_t slot = -1;
+    if (pl->flags & KVX_PLAN_TIMING) {
+        st = ensure_timing_slots(pl, stream);
+        if (st) return st;
+        if ((int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
+    }
     if (pl->lanes > 1) {
         // fork: the lane waits for everything already on the caller's stream (the upload included)
         if (!pl->fork_evt) {
@@ -645,21 +694,15 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
         e = cudaStreamWaitEvent(stream, ready, 0);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(ready)");
     }
-    cudaEvent_t start = nullptr;
-    if (pl->flags & KVX_PLAN_TIMING) {
-        st = take_event(pl, &start);
-        if (st) return st;
-        e = cudaEventRecord(start, stream);
-        if (e != cudaSuccess) {
-            pl->free_events.push_back(start);
-            return cuda_fail(e, "cudaEventRecord(push start)");
-        }
-    }
     const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
                             pl->bulk_stages};
-    e = launch_copy(plan_copy_args(pl, l0), l1 - l0, shape, stream);
+    CopyArgs args = plan_copy_args(pl, l0);
+    if (slot >= 0) {
+        args.ts_start = pl->ts + slot;
+        args.ts_end = pl->ts + kTimingSlots + slot;
+    }
+    e = launch_copy(args, l1 - l0, shape, stream);
     if (e != cudaSuccess) {
-        if (start) pl->free_events.push_back(start);
         for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
         return cuda_fail(e, "copy kernel launch");
     }
@@ -669,18 +712,16 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
     e = cudaEventRecord(ev, stream);
     if (e != cudaSuccess) {
         pl->free_events.push_back(ev);
-        if (start) pl->free_events.push_back(start);
         return cuda_fail(e, "cudaEventRecord(push)");
     }
     if (done) {
         e = cudaEventRecord(done, stream);
         if (e != cudaSuccess) {
             pl->free_events.push_back(ev);
-            if (start) pl->free_events.push_back(start);
             return cuda_fail(e, "cudaEventRecord(done)");
         }
     }
-    pl->pending.push_back({ev, start, l0, l1});
+    pl->pending.push_back({ev, slot, l0, l1});
     for (int32_t l = l0; l < l1; ++l) {
         pl->layer_state[l] = KVX_LAYER_PENDING;
         if (pl->inject[l]) { pl->injected_pending[l] = 1; pl->inject[l] = 0; }
@@ -740,20 +781,38 @@ kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {
     bool failed = false;
     pl->push_start_us.clear();
     pl->push_end_us.clear();
-    for (size_t i = 0; i < sealed; ++i) {
-        const PendingPush &p = pl->pending[i];
-        if (p.start) {
-            float s_ms = 0.f, e_ms = 0.f;
-            e = cudaEventElapsedTime(&s_ms, pl->pending[0].start, p.start);
-            if (e == cudaSuccess) e = cudaEventElapsedTime(&e_ms, pl->pending[0].start, p.done);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime(push)");
-            pl->push_start_us.push_back(s_ms * 1000.f);
-            pl->push_end_us.push_back(e_ms * 1000.f);
+    pl->push_start_ns.clear();
+    pl->push_end_ns.clear();
+    int32_t n_slots = 0;
+    for (size_t i = 0; i < sealed; ++i) n_slots = std::max(n_slots, pl->pending[i].slot + 1);
+    if (n_slots > 0) {
+        // the kernels' global-timer stamps, then fresh slots for the next pushes
+        std::vector<unsigned long long> t0((size_t)n_slots), t1((size_t)n_slots);
+        e = cudaMemcpyAsync(t0.data(), pl->ts, sizeof(unsigned long long) * t0.size(), cudaMemcpyDeviceToHost, aux);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(t1.data(), pl->ts + kTimingSlots, sizeof(unsigned long long) * t1.size(),
+                                cudaMemcpyDeviceToHost, aux);
+        if (e != cudaSuccess) return cuda_fail(e, "reading push timing stamps");
+        kvx_status rs = reset_timing_slots(pl, n_slots, aux);
+        if (rs) return rs;
+        e = cudaStreamSynchronize(aux);
+        if (e != cudaSuccess) return cuda_fail(e, "reading push timing stamps");
+        unsigned long long base = ~0ull;
+        for (size_t i = 0; i < sealed; ++i) {
+            const int32_t k = pl->pending[i].slot;
+            if (k >= 0 && t0[k] != ~0ull) base = std::min(base, t0[k]);
+        }
+        for (size_t i = 0; i < sealed; ++i) {
+            const int32_t k = pl->pending[i].slot;
+            if (k < 0 || t0[k] == ~0ull) continue;   // untimed, or a launch with nothing to copy
+            pl->push_start_ns.push_back((int64_t)t0[k]);
+            pl->push_end_ns.push_back((int64_t)t1[k]);
+            pl->push_start_us.push_back((float)((double)(t0[k] - base) * 1e-3));
+            pl->push_end_us.push_back((float)((double)(t1[k] - base) * 1e-3));
         }
     }
     for (size_t i = 0; i < sealed; ++i) {
         const PendingPush &p = pl->pending[i];
-        if (p.start) pl->free_events.push_back(p.start);
         for (int32_t l = p.layer_begin; l < p.layer_end; ++l) {
             const bool bad = err[l] != 0 || pl->injected_pending[l];
             pl->layer_state[l] = bad ? KVX_LAYER_FAILED : KVX_LAYER_DONE;
@@ -773,17 +832,16 @@ kvx_status kvx_plan_destroy(kvx_plan_t pl) {
     for (const PendingPush &p : pl->pending) {
         cudaError_t e = cudaEventSynchronize(p.done);
         if (e != cudaSuccess && st == KVX_OK) st = cuda_fail(e, "cudaEventSynchronize(destroy)");
-        const bool timing = (pl->flags & KVX_PLAN_TIMING) != 0;
-        event_give(timing, p.done);
-        if (p.start) event_give(timing, p.start);
+        event_give(false, p.done);
     }
-    for (cudaEvent_t ev : pl->free_events) event_give((pl->flags & KVX_PLAN_TIMING) != 0, ev);
+    for (cudaEvent_t ev : pl->free_events) event_give(false, ev);
     if (pl->fork_evt) event_give(false, pl->fork_evt);
     if (pl->upload_evt) {
         cudaEventSynchronize(pl->upload_evt);
         event_give(false, pl->upload_evt);
     }
     if (pl->dev) pool_free(pl->dev);
+    if (pl->ts) pool_free(pl->ts);
     delete pl;
     return st;
 }

@@ -106,6 +106,7 @@ _sig = {
     "kvx_sync": (c_i32, [c_vp, c_i64]),
     "kvx_plan_layer_states": (c_i32, [c_vp, _P(c_i32), c_i32]),
     "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), _P(ctypes.c_float), c_i32, _P(c_i32)]),
+    "kvx_plan_push_times_ns": (c_i32, [c_vp, _P(c_i64), _P(c_i64), c_i32, _P(c_i32)]),
     "kvx_plan_inject_failure": (c_i32, [c_vp, c_i32]),
     "kvx_plan_destroy": (c_i32, [c_vp]),
     "kvx_status_str": (ctypes.c_char_p, [c_i32]),
@@ -340,12 +341,22 @@ def kvx_sync(plan, timeout_us: int = -1) -> int:
 
 
 def kvx_plan_push_times(plan, cap: int = 4096) -> tuple:
-    """(start_us, end_us) of each push confirmed by the last kvx_sync, relative to the first one's
-    start (timing plans)."""
+    """(start_us, end_us) of each push confirmed by the last kvx_sync, relative to the earliest start
+    among them (timing plans; the kernels' own global-timer stamps)."""
     s, e = np.zeros(cap, np.float32), np.zeros(cap, np.float32)
     n = c_i32()
     _check(_lib.kvx_plan_push_times(_h(plan), s.ctypes.data_as(_P(ctypes.c_float)), e.ctypes.data_as(_P(ctypes.c_float)),
                                     cap, ctypes.byref(n)), "kvx_plan_push_times")
+    k = min(n.value, cap)
+    return s[:k].copy(), e[:k].copy()
+
+
+def kvx_plan_push_times_ns(plan, cap: int = 4096) -> tuple:
+    """(start_ns, end_ns) of the same pushes as raw readings of the GPU's global timer."""
+    s, e = np.zeros(cap, np.int64), np.zeros(cap, np.int64)
+    n = c_i32()
+    _check(_lib.kvx_plan_push_times_ns(_h(plan), s.ctypes.data_as(_P(c_i64)), e.ctypes.data_as(_P(c_i64)),
+                                       cap, ctypes.byref(n)), "kvx_plan_push_times_ns")
     k = min(n.value, cap)
     return s[:k].copy(), e[:k].copy()
 

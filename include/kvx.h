@@ -135,10 +135,11 @@ typedef struct kvx_plan_opts {
 #define KVX_KERNEL_PERSIST 2
 #define KVX_KERNEL_BULK 3
 
-/* Record when every push starts and ends on the device (CUDA events around each launch); read
- * with kvx_plan_push_times after kvx_sync. This is the per-layer KV transfer time that the
- * bidirectional article's prefill-duration breakdown ([P3] "Leistungsdaten", Figs. 4 and 6)
- * separates from recompute time. */
+/* Record when every push starts and ends on the device; read with kvx_plan_push_times after
+ * kvx_sync. The copy kernels stamp the GPU's global timer themselves (the first CTA to start, the
+ * last CTA to finish), so timing adds no host call to a push. This is the per-layer KV transfer time
+ * that the bidirectional article's prefill-duration breakdown ([P3] "Leistungsdaten", Figs. 4 and 6)
+ * separates from recompute time. Up to 4096 pushes between two syncs are timed. */
 #define KVX_PLAN_TIMING 1
 
 /*
@@ -253,10 +254,15 @@ kvx_status kvx_push_layer_notify(kvx_plan_t plan, int32_t layer_begin, int32_t l
 kvx_status kvx_sync(kvx_plan_t plan, int64_t timeout_us);
 
 /* Plans built with KVX_PLAN_TIMING: for each push the last completed kvx_sync confirmed, in issue
- * order, its start and end in microseconds relative to the start of the first of them (up to cap
- * entries each; *n receives the count). A push starts when its stream has passed the push's
- * `ready` wait and ends with its kernel. Pushes on different lanes may overlap. */
+ * order, its start and end in microseconds relative to the earliest start among them (up to cap
+ * entries each; *n receives the count). A push starts when the first CTA of its kernel starts and
+ * ends when the last one has finished (its stores completed). Pushes on different lanes may overlap.
+ * A push with nothing to copy launches no kernel and has no entry. */
 kvx_status kvx_plan_push_times(kvx_plan_t plan, float *start_us, float *end_us, int32_t cap, int32_t *n);
+
+/* The same entries as raw readings of the GPU's global timer (nanoseconds). One clock serves the
+ * whole device, so the pushes of different plans can be placed on one timeline. */
+kvx_status kvx_plan_push_times_ns(kvx_plan_t plan, int64_t *start_ns, int64_t *end_ns, int32_t cap, int32_t *n);
 
 /* Per-layer states (out: n_layers entries of kvx_layer_state). */
 kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers);

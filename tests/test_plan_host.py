@@ -221,6 +221,7 @@ def test_timing_flag_validation():
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"flags": 2}))
     plain = kvx.kvx_plan(sp, dp, [ok])
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_push_times(plain))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_push_times_ns(plain))
     kvx.kvx_plan_destroy(plain)
     timed = kvx.kvx_plan_ex(sp, dp, [ok], {"flags": kvx.KVX_PLAN_TIMING})
     s, e = kvx.kvx_plan_push_times(timed)

@@ -298,17 +298,36 @@ def test_launch_count_grows():
     assert kvx.kvx_launch_count() >= n0 + 4                     # 2 fixtures + 2 pushes
 
 
-def test_push_times_of_timing_plan():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_push_times_of_timing_plan(kernel):
+    """Timing plans: the copy kernels stamp the GPU's global timer (first CTA start, last CTA end)."""
     w = kvx_inputs.qwen3_32b_single(n_layers=4)
     src, _ = device_pool(w.src, w.values, seed=w.seed)
     dst, _ = device_pool(w.dst, "canary_" + w.values)
-    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"flags": kvx.KVX_PLAN_TIMING})
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w),
+                           {"flags": kvx.KVX_PLAN_TIMING, "kernel": KERNELS[kernel]})
     assert push_all_layers(plan, 4) == kvx.KVX_OK
     s, e = kvx.kvx_plan_push_times(plan)
+    s_ns, e_ns = kvx.kvx_plan_push_times_ns(plan)
     t = e - s
-    assert len(t) == 4 and np.all(t > 0) and np.all(t < 1e5) and s[0] == 0
+    assert len(t) == 4 and np.all(t > 0) and np.all(t < 1e5) and s.min() == 0
+    assert np.allclose((e_ns - s_ns) * 1e-3, t, atol=0.01) and np.all(s_ns > 0)
     check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
                  range(4))
+    # a second round: fresh slots, stamped later on the same clock
+    assert push_all_layers(plan, 4) == kvx.KVX_OK
+    s2_ns, e2_ns = kvx.kvx_plan_push_times_ns(plan)
+    assert len(s2_ns) == 4 and s2_ns.min() > e_ns.max() and np.all(e2_ns > s2_ns)
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_timing_plan_with_nothing_to_copy_has_no_entries():
+    w = kvx_inputs.tiny()
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), [], {"flags": kvx.KVX_PLAN_TIMING})
+    assert push_all_layers(plan, w.src.n_layers) == kvx.KVX_OK
+    assert len(kvx.kvx_plan_push_times(plan)[0]) == 0 and len(kvx.kvx_plan_push_times_ns(plan)[0]) == 0
     kvx.kvx_plan_destroy(plan)
 
 
