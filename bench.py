@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -636,48 +637,98 @@ def oracle_sample(w, n_layers):
     return sg, src, dg, dst
 
 
-def cpu_baseline(w, seconds, n_layers=4):
+def oracle_layer(sg, src, dg, dst, layer):
+    """One layer of the host sample as a one-layer pool pair (views, no copies)."""
+    ps, pd = sg.n_planes * sg.n_shards, dg.n_planes * dg.n_shards
+    return (sg.replace(n_layers=1), src[layer * ps:(layer + 1) * ps], dg.replace(n_layers=1),
+            dst[layer * pd:(layer + 1) * pd])
+
+
+def oracle_threads():
+    """Host cores this process may run on (at most 32, which bounds the host sample's memory)."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        n = os.cpu_count() or 1
+    return max(1, min(32, n))
+
+
+def cpu_baseline(w, seconds):
+    """The oracle as it stands, on the host's cores: every thread pushes its own layer of a host
+    sample of the workload, concurrently (the oracle's calls release the interpreter lock), for about
+    `seconds`; then one thread alone, for comparison."""
+    import concurrent.futures as cf
     import oracle
     orc = oracle.load()
-    sg, src, dg, dst = oracle_sample(w, n_layers)
+    n_threads = oracle_threads()
+    sg, src, dg, dst = oracle_sample(w, n_threads)
     reqs = requests(w)
     per_layer = 2 * sum(n for n, _, _ in reqs) * sg.n_shards * sg.row_bytes * sg.n_planes
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        orc.push(sg, src, dg, dst, reqs)
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
+
+    def loop(layer, deadline):
+        views, n = oracle_layer(sg, src, dg, dst, layer), 0
+        while True:
+            orc.push(*views, reqs)
+            n += 1
+            if time.perf_counter() >= deadline:
+                return n
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(n_threads) as pool:
+        reps = sum(pool.map(lambda l: loop(l, t0 + 0.7 * seconds), range(n_threads)))
     dt = time.perf_counter() - t0
-    return {"value": round(per_layer * n_layers * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} oracle pushes of {n_layers} of {w.src.n_layers} layers of {w.name} "
-                      f"(host pools, single thread), {dt:.1f} s"}
+    t1 = time.perf_counter()
+    reps1 = loop(0, t1 + 0.3 * seconds)
+    dt1 = time.perf_counter() - t1
+    return {"value": round(per_layer * reps / dt / 1e9, 3), "unit": "GB/s", "cores": n_threads, "kind": "oracle",
+            "sample": f"{reps} oracle pushes of one layer of {w.name} (host pools), {n_threads} threads each on "
+                      f"its own layer, {dt:.1f} s",
+            "single_thread": {"value": round(per_layer * reps1 / dt1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps1} one-layer pushes, 1 thread, {dt1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle (there is no other implementation of this path), each step one
+    push of as many layers as the host has cores, one layer per thread, concurrently."""
     if rank != 0:
         return None
+    import concurrent.futures as cf
     import oracle
     orc = oracle.load()
     w = kvx_inputs.PUSH_WORKLOADS[args.workload]()
-    n_layers = 2
+    n_layers = n_threads = min(oracle_threads(), w.src.n_layers)
     sg, src, dg, dst = oracle_sample(w, n_layers)
     reqs = requests(w)
     bytes_step = 2 * sum(n for n, _, _ in reqs) * sg.n_shards * sg.row_bytes * sg.n_planes * n_layers
-    for _ in range(args.warmup):
-        orc.push(sg, src, dg, dst, reqs)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        orc.push(sg, src, dg, dst, reqs)
-    dt = time.perf_counter() - t0
+    views = [oracle_layer(sg, src, dg, dst, l) for l in range(n_layers)]
+    # each thread runs the warm-up and then the timed steps of its own layer back to back; the K steps
+    # are timed together, from a barrier after every warm-up to the last thread's end, so that no
+    # step waits for the slowest thread of the one before
+    start = threading.Barrier(n_threads + 1)
+
+    def worker(v):
+        for _ in range(args.warmup):
+            orc.push(*v, reqs)
+        start.wait()
+        for _ in range(args.steps):
+            orc.push(*v, reqs)
+
+    with cf.ThreadPoolExecutor(n_threads) as pool:
+        futs = [pool.submit(worker, v) for v in views]
+        start.wait()
+        t0 = time.perf_counter()
+        for f in futs:
+            f.result()
+        dt = time.perf_counter() - t0
     v = round(bytes_step * args.steps / dt / 1e9, 3)
-    sample = f"each step: oracle push of {n_layers} of {w.src.n_layers} layers of {w.name} on host pools, 1 thread"
+    sample = (f"each step: oracle push of {n_layers} of {w.src.n_layers} layers of {w.name} on host pools, "
+              f"{n_threads} threads, one layer each; the steps run back to back per thread")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic: seeded random bytes, same block ids as the kvx arm",
             "config": {"workload": args.workload, "layers_per_step": n_layers},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": n_threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
