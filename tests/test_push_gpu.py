@@ -374,3 +374,44 @@ def test_hnd_batched_workload_sampled():
     w = kvx_inputs.qwen3_32b_batched_hnd()
     info = run_workload(w, [0, 40, 63])
     assert info["strided"] == 1 and info["src_pitch"] == 256 and info["dst_pitch"] == 256
+
+
+def test_threads_push_their_own_plans_concurrently():
+    """kvx calls from several host threads, each with its own plan, pools and stream (the library's
+    lanes, event pool, device memory pool and status stream are shared): every consumer equals the
+    oracle on its producer."""
+    import threading
+    n_threads, reps = 4, 8
+    cases = []
+    for k in range(n_threads):
+        w = kvx_inputs.qwen3_32b_batched(seed=40 + k, n_layers=3, n_requests=3, len_range=(200, 1500))
+        src, _ = device_pool(w.src, w.values, seed=w.seed + k)
+        dst, _ = device_pool(w.dst, "canary_" + w.values)
+        cases.append((w, src, dst))
+    errors = []
+
+    def worker(k):
+        try:
+            w, src, dst = cases[k]
+            stream = torch.cuda.Stream()
+            for _ in range(reps):
+                plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w),
+                                       {"flags": kvx.KVX_PLAN_TIMING if k % 2 else 0})
+                for layer in range(w.src.n_layers):
+                    kvx.kvx_push_layer(plan, layer, stream)
+                assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+                kvx.kvx_plan_destroy(plan)
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(n_threads)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for w, src, dst in cases:
+        per = w.dst.n_planes * w.dst.n_shards
+        check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(per)],
+                     reqs_of(w), range(w.src.n_layers))
