@@ -186,8 +186,8 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     """Allocates the workload's pools and times K steps of the per-layer push pattern after W untimed
     ones. A step builds the requests' plan, runs the synthetic prefill (per layer a fixture kernel on
     the priority stream that records the layer's ready event) and pushes every layer gated on its
-    event; each step is synced after the next one is issued. Per-push timing events are recorded on
-    every `every`-th timed step."""
+    event; each step is synced after the next one is issued. The pushes of every `every`-th timed step
+    are timed (the kernels' own global-timer stamps)."""
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
@@ -315,7 +315,7 @@ KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_cop
 
 def per_config(args, torch, kvx, device):
     """The other push configurations, briefly, in the same run: GB/s and blocks/s per step, the push
-    kernel's roofline fraction (union of push intervals, timing events on every step)."""
+    kernel's roofline fraction (union of all push intervals on the kernels' global-timer stamps)."""
     peak, _ = measured_peak()
     out = []
     for name, steps in (("tiny", 200), ("qwen3_32b_batched", 20), ("tp4_to_tp1_remap", 20),

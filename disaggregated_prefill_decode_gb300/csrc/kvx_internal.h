@@ -87,8 +87,8 @@ void pool_free(void *ptr);
 kvx_status aux_stream(cudaStream_t *out);
 // Library-wide pool of events per (device, timing): plans rebuilt every step reuse them instead of
 // creating and destroying one or two per push.
-kvx_status event_take(bool timing, cudaEvent_t *ev);
-void event_give(bool timing, cudaEvent_t ev);
+kvx_status event_take(cudaEvent_t *ev);
+void event_give(cudaEvent_t ev);
 
 // Launches the tile copy for layers [args.layer0, args.layer0 + n_layers) (kvx_push.cu).
 struct LaunchShape {

@@ -896,7 +896,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
             if (e != cudaSuccess) return cleanup(cuda_fail(e, "reading plan runs"));
         }
         finish_plan_shape(pl);
-        st = event_take(false, &pl->upload_evt);
+        st = event_take(&pl->upload_evt);
         if (st) return cleanup(st);
         e = cudaEventRecord(pl->upload_evt, stream);
         if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventRecord(plan)"));

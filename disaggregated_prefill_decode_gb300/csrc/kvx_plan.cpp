@@ -1,4 +1,4 @@
-// Host side of kvx: error reporting, plan validation, run merging and tiling. No CUDA calls.
+// Host side of kvx: error reporting, plan validation, run merging and tiling. No device work.
 //
 // Follows the push-mode NIXL connector article (spke.com 3844), section "Threading-Modell" (block ids
 // are mapped to memory descriptors and contiguous blocks merged into larger regions) and

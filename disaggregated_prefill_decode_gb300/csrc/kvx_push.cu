@@ -445,35 +445,35 @@ static std::map<int, cudaMemPool_t> g_pools;
 static std::map<int, cudaStream_t> g_aux;
 static std::map<std::pair<int, int>, std::vector<cudaStream_t>> g_lanes;
 static std::mutex g_evt_mu;
-static std::map<std::pair<int, bool>, std::vector<cudaEvent_t>> g_events;
+static std::map<int, std::vector<cudaEvent_t>> g_events;   // per device, timing disabled
 
-kvx_status event_take(bool timing, cudaEvent_t *ev) {
+kvx_status event_take(cudaEvent_t *ev) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     {
         std::lock_guard<std::mutex> lk(g_evt_mu);
-        std::vector<cudaEvent_t> &v = g_events[std::make_pair(dev, timing)];
+        std::vector<cudaEvent_t> &v = g_events[dev];
         if (!v.empty()) {
             *ev = v.back();
             v.pop_back();
             return KVX_OK;
         }
     }
-    e = cudaEventCreateWithFlags(ev, timing ? cudaEventDefault : cudaEventDisableTiming);
+    e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
     return KVX_OK;
 }
 
 // Events go back to the pool of the current device; callers give back events of that device.
-void event_give(bool timing, cudaEvent_t ev) {
+void event_give(cudaEvent_t ev) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaEventDestroy(ev);
         return;
     }
     std::lock_guard<std::mutex> lk(g_evt_mu);
-    g_events[std::make_pair(dev, timing)].push_back(ev);
+    g_events[dev].push_back(ev);
 }
 
 // Lane `i` for the current device at `priority`: a non-blocking stream created on first use and kept
@@ -610,7 +610,7 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     memcpy(img + pl->off_dst, pl->dst_base.data(), sizeof(void *) * pl->dst_base.size());
     cudaError_t e = cudaMemcpyAsync(pl->dev, img, pl->dev_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan upload)");
-    st = event_take(false, &pl->upload_evt);
+    st = event_take(&pl->upload_evt);
     if (st) return st;
     e = cudaEventRecord(pl->upload_evt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(upload)");
@@ -643,7 +643,7 @@ static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
         pl->free_events.pop_back();
         return KVX_OK;
     }
-    return event_take(false, ev);
+    return event_take(ev);
 }
 
 extern "C" {
@@ -667,7 +667,7 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
     if (pl->lanes > 1) {
         // fork: the lane waits for everything already on the caller's stream (the upload included)
         if (!pl->fork_evt) {
-            st = event_take(false, &pl->fork_evt);
+            st = event_take(&pl->fork_evt);
             if (st) return st;
         }
         e = cudaEventRecord(pl->fork_evt, stream);
@@ -832,13 +832,13 @@ kvx_status kvx_plan_destroy(kvx_plan_t pl) {
     for (const PendingPush &p : pl->pending) {
         cudaError_t e = cudaEventSynchronize(p.done);
         if (e != cudaSuccess && st == KVX_OK) st = cuda_fail(e, "cudaEventSynchronize(destroy)");
-        event_give(false, p.done);
+        event_give(p.done);
     }
-    for (cudaEvent_t ev : pl->free_events) event_give(false, ev);
-    if (pl->fork_evt) event_give(false, pl->fork_evt);
+    for (cudaEvent_t ev : pl->free_events) event_give(ev);
+    if (pl->fork_evt) event_give(pl->fork_evt);
     if (pl->upload_evt) {
         cudaEventSynchronize(pl->upload_evt);
-        event_give(false, pl->upload_evt);
+        event_give(pl->upload_evt);
     }
     if (pl->dev) pool_free(pl->dev);
     if (pl->ts) pool_free(pl->ts);
