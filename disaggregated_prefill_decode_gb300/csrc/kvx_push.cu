@@ -1,5 +1,6 @@
-// The layer push: a tile-table driven gather/scatter copy kernel for sm_103a, the side-stream issue
-// path, completion counting and per-layer status.
+// The layer push on the host side: the library's device memory pool, status stream, push lanes and
+// event pool, the plan upload, the side-stream issue path, completion counting, per-layer status and
+// the read-back of the kernels' timing stamps. The copy kernels themselves are in kvx_copy.cu.
 //
 // Follows the push-mode NIXL connector article (spke.com 3844), "Implementierungsdetails" step 3
 // (write the KV blocks into the consumer's memory, one completion per write, the consumer counts
@@ -17,424 +18,6 @@
 #include <thread>
 
 namespace kvx {
-
-// ------------------------------------------------------------------------------------------------
-// Copy kernel
-// ------------------------------------------------------------------------------------------------
-
-template <int VEC> struct VecType;
-template <> struct VecType<16> { using T = uint4; };
-template <> struct VecType<8> { using T = uint2; };
-template <> struct VecType<4> { using T = uint32_t; };
-template <> struct VecType<2> { using T = uint16_t; };
-template <> struct VecType<1> { using T = uint8_t; };
-
-constexpr int kUnroll = 4;
-
-// Host-validated tables never fail this guard; device-built ones are checked here. An out-of-bounds
-// tile is skipped and its layer's error word set (no trap).
-template <bool STRIDED>
-__device__ __forceinline__ bool tile_in_bounds(const TileDesc &t, const CopyArgs &a) {
-    const int64_t src_end = STRIDED ? t.src_off + (int64_t)(t.n - 1) * a.src_pitch + a.width : t.src_off + t.n;
-    const int64_t dst_end = STRIDED ? t.dst_off + (int64_t)(t.n - 1) * a.dst_pitch + a.width : t.dst_off + t.n;
-    return t.n > 0 && t.src_off >= 0 && t.dst_off >= 0 && src_end <= a.src_buf_bytes && dst_end <= a.dst_buf_bytes &&
-           t.s_shard >= 0 && t.s_shard < a.src_shards && t.d_shard >= 0 && t.d_shard < a.dst_shards;
-}
-
-// Copies one tile with VEC-byte integer vectors, kUnroll independent loads in flight per thread
-// before their stores. Values are never converted.
-template <int VEC, bool STRIDED>
-__device__ __forceinline__ void copy_tile(const TileDesc &t, const uint8_t *src, uint8_t *dst, const CopyArgs &a) {
-    using V = typename VecType<VEC>::T;
-    if (!STRIDED) {
-        const V *s = reinterpret_cast<const V *>(src);
-        V *d = reinterpret_cast<V *>(dst);
-        const int32_t nv = t.n / VEC;
-        const int32_t step = (int32_t)blockDim.x;
-        for (int32_t i = threadIdx.x; i < nv; i += step * kUnroll) {
-            V r[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (i + u * step < nv) r[u] = s[i + u * step];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (i + u * step < nv) d[i + u * step] = r[u];
-        }
-    } else {
-        // Rows of `width` bytes at the two pitches. Threads are laid out as (row lane, column) once,
-        // so the loop has no per-element division.
-        const int32_t vpr = a.width / VEC;
-        if (vpr <= (int32_t)blockDim.x) {
-            const int32_t rpp = (int32_t)blockDim.x / vpr;          // rows per pass
-            const int32_t my_row = (int32_t)threadIdx.x / vpr;
-            const int32_t col = (int32_t)threadIdx.x - my_row * vpr;
-            if (my_row < rpp) {
-                for (int32_t row = my_row; row < t.n; row += rpp * kUnroll) {
-                    V r[kUnroll];
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
-                        const int32_t rr = row + u * rpp;
-                        if (rr < t.n) r[u] = reinterpret_cast<const V *>(src + (int64_t)rr * a.src_pitch)[col];
-                    }
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
-                        const int32_t rr = row + u * rpp;
-                        if (rr < t.n) reinterpret_cast<V *>(dst + (int64_t)rr * a.dst_pitch)[col] = r[u];
-                    }
-                }
-            }
-        } else {
-            for (int32_t row = 0; row < t.n; ++row) {
-                const V *s = reinterpret_cast<const V *>(src + (int64_t)row * a.src_pitch);
-                V *d = reinterpret_cast<V *>(dst + (int64_t)row * a.dst_pitch);
-                for (int32_t c = threadIdx.x; c < vpr; c += blockDim.x) d[c] = s[c];
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Timing plans: every CTA folds the device's global timer into its push's slot when it starts
-// (minimum) and when it is done (maximum), so a slot ends up holding the span from the first CTA's
-// start to the last CTA's end. One clock serves the whole GPU; no host call is involved.
-__device__ __forceinline__ void stamp_start(const CopyArgs &a) {
-    if (a.ts_start && threadIdx.x == 0) atomicMin(a.ts_start, (unsigned long long)global_ns());
-}
-
-// Called by every thread of the CTA (the test on a kernel argument is uniform). Each thread's stores
-// are made visible device-wide before the stamp, so the span covers them.
-__device__ __forceinline__ void stamp_end(const CopyArgs &a) {
-    if (!a.ts_end) return;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) atomicMax(a.ts_end, (unsigned long long)global_ns());
-}
-
-// Work item w of a launch: tile w % n_tiles of plane (w / n_tiles) % n_planes of layer
-// layer0 + w / (n_tiles * n_planes). Consecutive items are consecutive tiles of one buffer pair.
-__device__ __forceinline__ void decode_item(const CopyArgs &a, int64_t w, int64_t *tile, int32_t *layer, int64_t *lp) {
-    const int64_t rest = w / a.n_tiles;
-    *tile = w - rest * a.n_tiles;
-    const int32_t plane = (int32_t)(rest % a.n_planes);
-    *layer = a.layer0 + (int32_t)(rest / a.n_planes);
-    *lp = (int64_t)(*layer) * a.n_planes + plane;
-}
-
-// KVX_KERNEL_TILE: one CTA per (tile, plane, layer).
-template <int VEC, bool STRIDED>
-__global__ void __launch_bounds__(1024) kvx_copy_tiles(CopyArgs a) {
-    stamp_start(a);
-    const TileDesc t = a.tiles[blockIdx.x];
-    const int32_t layer = a.layer0 + (int32_t)blockIdx.z;
-    const int64_t lp = (int64_t)layer * a.n_planes + blockIdx.y;
-    if (!tile_in_bounds<STRIDED>(t, a)) {
-        if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
-    } else {
-        copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
-                                a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
-    }
-    stamp_end(a);
-}
-
-// KVX_KERNEL_PERSIST: a resident grid walks the work items; each CTA loads the next item's
-// descriptor before copying the current one, so the descriptor latency hides behind the copy.
-template <int VEC, bool STRIDED>
-__global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_work) {
-    int64_t w = blockIdx.x;
-    if (w >= n_work) return;
-    stamp_start(a);
-    TileDesc next = a.tiles[w % a.n_tiles];
-    for (; w < n_work; w += gridDim.x) {
-        const TileDesc t = next;
-        if (w + gridDim.x < n_work) next = a.tiles[(w + gridDim.x) % a.n_tiles];
-        int64_t tile, lp;
-        int32_t layer;
-        decode_item(a, w, &tile, &layer, &lp);
-        if (!tile_in_bounds<STRIDED>(t, a)) {
-            if (threadIdx.x == 0 && t.n != 0) atomicOr(&a.err[layer], 1);
-            continue;
-        }
-        copy_tile<VEC, STRIDED>(t, a.src_base[lp * a.src_shards + t.s_shard] + t.src_off,
-                                a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off, a);
-    }
-    stamp_end(a);
-}
-
-// ------------------------------------------------------------------------------------------------
-// KVX_KERNEL_BULK: bulk asynchronous copies through shared memory (16-byte aligned).
-// One thread per CTA drives a ring of STAGES stages: the load of an item lands in its stage
-// and completes the stage's mbarrier (transaction count = bytes); the thread then issues the bulk
-// store of that stage and, once the store before it has finished reading its stage, the load of a
-// later item into that freed stage. Waits are bounded by the global timer.
-// A strided tile (rows of `width` bytes at each side's pitch) is packed densely in its stage: a side
-// whose pitch equals the width moves in one bulk copy, the other side row by row, all rows of a
-// load completing on the stage's one mbarrier and all row stores forming one bulk group.
-// ------------------------------------------------------------------------------------------------
-
-constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// The single arrival of a stage's phase, announcing `bytes` of incoming transactions (0 for none).
-__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Bounded wait for a stage's phase; false when the deadline passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (!mbar_test(bar, parity))
-        if (global_ns() - t0 > kBulkWaitNs) return false;
-    return true;
-}
-
-__device__ __forceinline__ void bulk_load(void *stage, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_addr(stage)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void *dst, const void *stage, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(stage)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-struct BulkItem {
-    const uint8_t *src;
-    uint8_t *dst;
-    uint32_t bytes;    // 0: skipped (out of bounds or misaligned)
-    int32_t rows;      // strided tiles: rows of a.width bytes; contiguous tiles: 1
-    int32_t layer;
-};
-
-template <bool STRIDED>
-__device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int32_t stage_bytes) {
-    int64_t tile, lp;
-    BulkItem it;
-    decode_item(a, w, &tile, &it.layer, &lp);
-    const TileDesc t = a.tiles[tile];
-    it.src = nullptr;
-    it.dst = nullptr;
-    it.bytes = 0;
-    it.rows = STRIDED ? t.n : 1;
-    const int64_t bytes = STRIDED ? (int64_t)t.n * a.width : (int64_t)t.n;
-    if (!tile_in_bounds<STRIDED>(t, a) || bytes > stage_bytes) {
-        if (t.n != 0) atomicOr(&a.err[it.layer], 1);
-        return it;
-    }
-    it.src = a.src_base[lp * a.src_shards + t.s_shard] + t.src_off;
-    it.dst = a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off;
-    uintptr_t mis = ((uintptr_t)it.src) | ((uintptr_t)it.dst) | (uintptr_t)bytes;
-    if (STRIDED) mis |= (uintptr_t)a.width | (uintptr_t)a.src_pitch | (uintptr_t)a.dst_pitch;
-    if (mis & 15) {
-        atomicOr(&a.err[it.layer], 1);
-        return it;
-    }
-    it.bytes = (uint32_t)bytes;
-    return it;
-}
-
-template <int STAGES, bool STRIDED>
-__global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, int32_t stage_bytes) {
-    constexpr int kBulkStages = STAGES;
-    extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ __align__(8) uint64_t bar[kBulkStages];
-    if (threadIdx.x != 0) return;
-    stamp_start(a);
-    for (int s = 0; s < kBulkStages; ++s) mbar_init(&bar[s]);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-
-    const int64_t n_mine = (int64_t)blockIdx.x < n_work ? (n_work - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    BulkItem items[kBulkStages];
-    // item i of this CTA is work item blockIdx.x + i * gridDim.x, in stage i % kBulkStages
-    const bool src_packed = !STRIDED || a.src_pitch == a.width;    // one bulk copy per tile on that side
-    const bool dst_packed = !STRIDED || a.dst_pitch == a.width;
-    auto issue = [&](int64_t i) {
-        const int s = (int)(i % kBulkStages);
-        const BulkItem it = bulk_item<STRIDED>(a, blockIdx.x + i * gridDim.x, stage_bytes);
-        items[s] = it;
-        mbar_arrive_expect(&bar[s], it.bytes);
-        if (!it.bytes) return;
-        uint8_t *stage = ring + (size_t)s * stage_bytes;
-        if (src_packed) {
-            bulk_load(stage, it.src, it.bytes, &bar[s]);
-        } else {
-            for (int32_t r = 0; r < it.rows; ++r)
-                bulk_load(stage + (size_t)r * a.width, it.src + (int64_t)r * a.src_pitch, (uint32_t)a.width, &bar[s]);
-        }
-    };
-    int64_t issued = 0;
-    for (; issued < n_mine && issued < kBulkStages - 1; ++issued) issue(issued);
-    bool timed_out = false;
-    for (int64_t i = 0; i < n_mine; ++i) {
-        const int s = (int)(i % kBulkStages);
-        if (!mbar_wait(&bar[s], (uint32_t)((i / kBulkStages) & 1))) {
-            atomicOr(&a.err[items[s].layer], 2);
-            timed_out = true;
-            break;
-        }
-        if (items[s].bytes) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            const uint8_t *stage = ring + (size_t)s * stage_bytes;
-            if (dst_packed) {
-                bulk_store(items[s].dst, stage, items[s].bytes);
-            } else {
-                for (int32_t r = 0; r < items[s].rows; ++r)
-                    bulk_store(items[s].dst + (int64_t)r * a.dst_pitch, stage + (size_t)r * a.width, (uint32_t)a.width);
-            }
-        }
-        bulk_commit();
-        if (issued < n_mine) {
-            bulk_wait_read_1();   // the stores issued one item ago have read the stage the next load reuses
-            issue(issued);
-            ++issued;
-        }
-    }
-    if (timed_out) {
-        // give every load still in flight a bounded chance to land before the ring goes away
-        for (int64_t j = 0; j < kBulkStages && j < issued; ++j) {
-            const int64_t i = issued - 1 - j;
-            mbar_wait(&bar[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1));
-        }
-    }
-    bulk_wait_all();   // the stores have completed, not only read their stages
-    if (a.ts_end) atomicMax(a.ts_end, (unsigned long long)global_ns());
-}
-
-// ------------------------------------------------------------------------------------------------
-// Launch
-// ------------------------------------------------------------------------------------------------
-
-template <int VEC>
-static cudaError_t launch_vec(const CopyArgs &a, int32_t n_layers, const LaunchShape &sh, unsigned grid_persist,
-                              cudaStream_t st) {
-    const int64_t n_work = a.n_tiles * a.n_planes * n_layers;
-    if (sh.kernel == KVX_KERNEL_TILE) {
-        const dim3 grid((unsigned)a.n_tiles, (unsigned)a.n_planes, (unsigned)n_layers);
-        if (sh.strided) kvx_copy_tiles<VEC, true><<<grid, sh.threads, 0, st>>>(a);
-        else kvx_copy_tiles<VEC, false><<<grid, sh.threads, 0, st>>>(a);
-    } else {
-        if (sh.strided) kvx_copy_persist<VEC, true><<<grid_persist, sh.threads, 0, st>>>(a, n_work);
-        else kvx_copy_persist<VEC, false><<<grid_persist, sh.threads, 0, st>>>(a, n_work);
-    }
-    return cudaGetLastError();
-}
-
-// Resident CTAs per SM for a kernel (occupancy query), times the SM count; cached per key.
-static std::mutex g_grid_mu;
-static std::map<std::tuple<int, const void *, int, int>, int> g_resident;
-
-static cudaError_t resident_grid(const void *fn, int threads, int smem, int per_sm_cap, int *grid) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_grid_mu);
-    const auto key = std::make_tuple(dev, fn, threads, smem);
-    auto it = g_resident.find(key);
-    if (it == g_resident.end()) {
-        int sms = 0, per_sm = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (smem > 0) {
-            // one limit per kernel, large enough for every ring it may be launched with
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkRingMax);
-            if (e != cudaSuccess) return e;
-        }
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
-        if (e != cudaSuccess) return e;
-        it = g_resident.emplace(key, sms * 1000 + std::max(per_sm, 1)).first;
-    }
-    const int sms = it->second / 1000, per_sm = it->second % 1000;
-    *grid = sms * (per_sm_cap > 0 ? std::min(per_sm_cap, per_sm) : per_sm);
-    return cudaSuccess;
-}
-
-template <bool STRIDED>
-static const void *bulk_fn_of(int stages) {
-    switch (stages) {
-        case 2: return (const void *)kvx_copy_bulk<2, STRIDED>;
-        case 3: return (const void *)kvx_copy_bulk<3, STRIDED>;
-        case 6: return (const void *)kvx_copy_bulk<6, STRIDED>;
-        case 8: return (const void *)kvx_copy_bulk<8, STRIDED>;
-        default: return (const void *)kvx_copy_bulk<4, STRIDED>;
-    }
-}
-
-static const void *bulk_fn(int stages, bool strided) {
-    return strided ? bulk_fn_of<true>(stages) : bulk_fn_of<false>(stages);
-}
-
-template <int VEC>
-static const void *persist_fn(bool strided) {
-    return strided ? (const void *)kvx_copy_persist<VEC, true> : (const void *)kvx_copy_persist<VEC, false>;
-}
-
-cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &sh, cudaStream_t st) {
-    if (a.n_tiles <= 0 || n_layers <= 0) return cudaSuccess;
-    const int64_t n_work = a.n_tiles * a.n_planes * n_layers;
-    count_launch();
-    int grid = 0;
-    cudaError_t e;
-    if (sh.kernel == KVX_KERNEL_BULK) {
-        const int smem = sh.stages * sh.tile_bytes;
-        const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 1 : 64);
-        const void *fn = bulk_fn(sh.stages, sh.strided != 0);
-        e = resident_grid(fn, 32, smem, cap, &grid);
-        if (e != cudaSuccess) return e;
-        CopyArgs args_copy = a;
-        int64_t work = n_work;
-        int32_t stage_bytes = sh.tile_bytes;
-        void *args[] = {&args_copy, &work, &stage_bytes};
-        return cudaLaunchKernel(fn, dim3((unsigned)std::min<int64_t>(grid, n_work)), dim3(32), args, (size_t)smem, st);
-    }
-    // default resident CTAs: small launches stay small so that they overlap the caller's compute and
-    // the next push; large ones take the whole GPU
-    LaunchShape shape = sh;
-    if (shape.ctas_per_sm == 0) shape.ctas_per_sm = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20) ? 2 : 64;
-    if (sh.kernel == KVX_KERNEL_PERSIST) {
-        const void *fn = sh.vec == 16 ? persist_fn<16>(sh.strided) : sh.vec == 8 ? persist_fn<8>(sh.strided)
-                       : sh.vec == 4 ? persist_fn<4>(sh.strided) : sh.vec == 2 ? persist_fn<2>(sh.strided)
-                       : persist_fn<1>(sh.strided);
-        e = resident_grid(fn, sh.threads, 0, shape.ctas_per_sm, &grid);
-        if (e != cudaSuccess) return e;
-        grid = (int)std::min<int64_t>(grid, n_work);
-    }
-    switch (sh.vec) {
-        case 16: return launch_vec<16>(a, n_layers, sh, (unsigned)grid, st);
-        case 8: return launch_vec<8>(a, n_layers, sh, (unsigned)grid, st);
-        case 4: return launch_vec<4>(a, n_layers, sh, (unsigned)grid, st);
-        case 2: return launch_vec<2>(a, n_layers, sh, (unsigned)grid, st);
-        default: return launch_vec<1>(a, n_layers, sh, (unsigned)grid, st);
-    }
-}
 
 // ------------------------------------------------------------------------------------------------
 // Device memory pool and auxiliary stream
