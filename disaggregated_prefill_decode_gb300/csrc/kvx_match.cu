@@ -49,15 +49,16 @@ constexpr unsigned kFull = 0xffffffffu;
 // while the current ones are hashed, and every lane runs the same chain, taking each token from its
 // owner lane by shuffle. After each block every lane holds its hash h and calls on_block(j, h).
 // on_block returns false to stop early. All branches are uniform across the warp.
+// `parent` is the hash the first block chains to (0 for a session's first block).
 template <typename OnBlock>
-__device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, int32_t bs, OnBlock &&on_block) {
+__device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, int32_t bs, OnBlock &&on_block,
+                                           uint64_t parent = 0) {
     const int lane = threadIdx.x & 31;
     const int64_t total = n_full * bs;
     uint32_t nxt_a = 0, nxt_b = 0;
     if (2 * lane < total) nxt_a = tok[2 * lane];
     if (2 * lane + 1 < total) nxt_b = tok[2 * lane + 1];
     uint32_t lo = kFnvBasisLo, hi = kFnvBasisHi;
-    uint64_t parent = 0;
     int64_t j = 0;
     if ((bs & 63) == 0) {
         // block sizes that are multiples of 64: each chunk of 64 tokens lies inside one block, so the
@@ -213,79 +214,143 @@ struct MatchFlags {
     uint8_t *resident;       // FILL_HOLES: per published block, 1 if resident locally (scratch)
 };
 
-// One warp per session: hash block by block while either prefix (local hits, agreement with the
-// published remote hashes) is still open; stop once both have ended. Each lane keeps the hash of
-// one block of the current window of 32; at the end of a window the lanes look their blocks up in the
-// table and compare them with the published list in parallel, and ballots extend the two prefixes.
-// With FILL_HOLES the lookups go on while the remote prefix is open, residency is recorded for the
-// plan emission, and the non-resident blocks below the remote prefix are counted.
-__global__ void __launch_bounds__(128) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
-                                                          int32_t n_sessions, int32_t bs, TableView table,
-                                                          const uint64_t *remote_hash, const int64_t *rem_off,
-                                                          int32_t threshold, int64_t n_tok_total, int64_t n_pub,
-                                                          MatchFlags mf, kvx_match_result *out, int64_t *push_blocks,
-                                                          int32_t *err) {
-    const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
+// Hash of one block chained to `parent`: the 8 parent octets, then the block's token octets.
+__device__ __forceinline__ uint64_t block_hash(uint64_t parent, const uint32_t *tok, int32_t bs) {
+    uint32_t lo = kFnvBasisLo, hi = kFnvBasisHi;
+    fnv_word(lo, hi, (uint32_t)parent);
+    fnv_word(lo, hi, (uint32_t)(parent >> 32));
+#pragma unroll 8
+    for (int32_t i = 0; i < bs; ++i) fnv_word(lo, hi, __ldg(tok + i));
+    return ((uint64_t)hi << 32) | lo;
+}
+
+constexpr int kMatchThreads = 256;
+
+// One CTA per session. The remote prefix is found without walking the chain: block j is hashed from
+// the PUBLISHED hash of block j - 1 (its candidate c_j), and the first j where c_j differs from the
+// published hash is exactly the first j where the session's own chained hash h_j does: below it every
+// published parent equals the true one, so c_j = h_j, and at it the parent is still the true one,
+// so c_j = h_j there too. The candidates are independent, so the CTA hashes 256 of them at a time
+// (one per thread), each also looked up in the table; warp 0 then extends the two prefixes window by
+// window with ballots. Local hits can use candidates up to and including the first mismatch; if every
+// block to there is resident, warp 0 continues the true chain from that block, window by window, until
+// the first block that is not resident. With FILL_HOLES, residency inside the remote prefix is
+// recorded for the plan emission and the non-resident blocks there are counted.
+__global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
+                                                                    int32_t n_sessions, int32_t bs, TableView table,
+                                                                    const uint64_t *remote_hash, const int64_t *rem_off,
+                                                                    int32_t threshold, int64_t n_tok_total, int64_t n_pub,
+                                                                    MatchFlags mf, kvx_match_result *out,
+                                                                    int64_t *push_blocks, int32_t *err) {
+    __shared__ uint64_t cand[kMatchThreads];
+    __shared__ uint8_t flag[kMatchThreads];     // bit 0: equals the published hash, bit 1: resident
+    __shared__ int32_t go_on;
+    const int32_t s = (int32_t)blockIdx.x;
     if (s >= n_sessions) return;
+    const int tid = (int)threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
     int64_t r0 = rem_off[s], n_rem = rem_off[s + 1] - r0;
     // malformed offsets: flag them and treat the session as empty, so no array is read out of range
     if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total) {
-        if (lane == 0) atomicOr(err, 1);
+        if (tid == 0) atomicOr(err, 1);
         t0 = 0;
         n_tok = 0;
     }
     if (r0 < 0 || n_rem < 0 || r0 + n_rem > n_pub) {
-        if (lane == 0) atomicOr(err, 2);
+        if (tid == 0) atomicOr(err, 2);
         r0 = 0;
         n_rem = 0;
     }
     if (mf.expiry && mf.now >= mf.expiry[s]) n_rem = 0;           // retention expired
     const bool fill = (mf.flags & KVX_MATCH_FILL_HOLES) != 0;
     const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
+    const int64_t n_cand = min(n_full, n_rem + 1);                // the published blocks and the one after
+    const uint32_t *tk = tokens + t0;
+    // warp 0's state (uniform across its lanes)
     int64_t l_loc = 0, l_rem = 0, holes = 0;
-    bool loc_open = true, rem_open = true;
-    unsigned last_hits = 0;                                       // residency bits of the last window
-    uint64_t mine = 0;
-    warp_chain(tokens + t0, n_full, bs, [&](int64_t j, uint64_t h) {
-        if ((j & 31) == lane) mine = h;
-        if ((j & 31) != 31 && j != n_full - 1) return true;
-        const int64_t w0 = j & ~(int64_t)31;
-        const int n_valid = (int)(j - w0 + 1);
-        const int64_t jb = w0 + lane;
-        const bool valid = lane < n_valid;
-        const bool look = loc_open || (fill && rem_open);
-        const bool hit = look && valid && table_find(table, mine) >= 0;
-        const unsigned hits = __ballot_sync(kFull, hit);
-        if (loc_open) {
-            const unsigned miss = ~hits;
-            const int first_miss = miss ? __ffs(miss) - 1 : 32;  // lanes past n_valid always miss
-            l_loc += min(first_miss, n_valid);
-            loc_open = first_miss >= n_valid;
+    bool loc_open = true, rem_open = true, chain = false;
+    uint64_t chain_parent = 0;
+    for (int64_t base = 0; base < n_cand; base += kMatchThreads) {
+        const int64_t j = base + tid;
+        if (j < n_cand) {
+            const uint64_t c = block_hash(j == 0 ? 0 : remote_hash[r0 + j - 1], tk + j * bs, bs);
+            const bool same = j < n_rem && remote_hash[r0 + j] == c;
+            const bool res = table_find(table, c) >= 0;
+            cand[tid] = c;
+            flag[tid] = (uint8_t)((same ? 1 : 0) | (res ? 2 : 0));
         }
-        if (rem_open) {
-            const bool same = valid && jb < n_rem && remote_hash[r0 + jb] == mine;
-            const unsigned miss = ~__ballot_sync(kFull, same);
-            const int first_miss = miss ? __ffs(miss) - 1 : 32;
-            const int n_in = min(first_miss, n_valid);              // blocks of this window in the prefix
-            if (fill) {
-                if (lane < n_in) mf.resident[r0 + jb] = hit ? 1 : 0;
-                const unsigned below = n_in >= 32 ? kFull : ((1u << n_in) - 1u);
-                holes += __popc(~hits & below);
+        __syncthreads();
+        if (warp == 0) {
+            for (int w = 0; w < kMatchThreads / 32 && (rem_open || loc_open); ++w) {
+                const int64_t j0 = base + 32 * w;
+                const int p = 32 * w + lane;
+                const uint8_t f = j0 + lane < n_cand ? flag[p] : 0;   // past the candidates: both miss
+                const unsigned m1 = __ballot_sync(kFull, f & 2);
+                int loc_lim = 0;                                        // window positions local hits may use
+                int fr = 32;
+                bool closed_here = false;
+                if (rem_open) {
+                    const unsigned miss = ~__ballot_sync(kFull, f & 1);
+                    fr = miss ? __ffs(miss) - 1 : 32;
+                    if (fill) {
+                        if (lane < fr) mf.resident[r0 + j0 + lane] = (f & 2) ? 1 : 0;
+                        const unsigned below = fr >= 32 ? kFull : ((1u << fr) - 1u);
+                        holes += __popc(~m1 & below);
+                    }
+                    l_rem += fr;
+                    rem_open = fr == 32;
+                    closed_here = !rem_open;
+                    loc_lim = rem_open ? 32 : fr + 1;                   // the first mismatch still has its true hash
+                }
+                if (loc_open) {
+                    const unsigned lmiss = ~m1;
+                    const int fl = lmiss ? __ffs(lmiss) - 1 : 32;
+                    if (fl < loc_lim) {
+                        l_loc += fl;
+                        loc_open = false;
+                    } else {
+                        l_loc += loc_lim;
+                        if (closed_here) {                              // resident through the first mismatch,
+                            loc_open = false;                           // which is a candidate (fl > fr)
+                            chain = true;
+                            chain_parent = cand[32 * w + fr];
+                        } else if (!rem_open) {
+                            loc_open = false;
+                        }
+                    }
+                }
             }
-            l_rem += n_in;
-            rem_open = first_miss >= n_valid;
+            if (lane == 0) go_on = rem_open || loc_open;
         }
-        last_hits = hits;
-        return loc_open || rem_open;
-    });
+        __syncthreads();
+        if (!go_on) break;
+    }
+    if (warp != 0) return;
+    if (chain && l_loc < n_full) {
+        // beyond the first mismatch the published parents no longer hold: the true chain, from the
+        // candidate of that block, while the blocks stay resident (looked up 32 at a time)
+        uint64_t mine = 0;
+        const int64_t jb = l_loc;
+        bool open = true;
+        warp_chain(tk + jb * bs, n_full - jb, bs, [&](int64_t k, uint64_t h) {
+            if ((k & 31) == lane) mine = h;
+            if ((k & 31) != 31 && k != n_full - jb - 1) return true;
+            const int n_valid = (int)(k - (k & ~(int64_t)31) + 1);
+            const bool hit = lane < n_valid && table_find(table, mine) >= 0;
+            const unsigned miss = ~__ballot_sync(kFull, hit);
+            const int fl = miss ? __ffs(miss) - 1 : 32;
+            l_loc += min(fl, n_valid);
+            open = fl >= n_valid;
+            return open;
+        }, chain_parent);
+    }
+    __syncwarp();
     if (lane != 0) return;
     if ((mf.flags & KVX_MATCH_KEEP_LAST) && l_rem > 0 && l_rem * bs >= n_tok) {
-        // every token is covered (only when the session ends on a block boundary and the whole
-        // chain matched, so block l_rem - 1 is in the last window): recompute the last block
+        // every token is covered (the session ends on a block boundary and its whole chain matched):
+        // recompute the last block
         --l_rem;
-        if (fill && !((last_hits >> (l_rem & 31)) & 1u)) --holes;
+        if (fill && !mf.resident[r0 + l_rem]) --holes;
     }
     const int64_t missing_blocks = fill ? holes : (l_rem > l_loc ? l_rem - l_loc : 0);
     const int64_t missing = missing_blocks * bs;
@@ -798,9 +863,9 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
     count_launch();
     if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
-    kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
-                                                                    table->view(), remote_hash, rem_off, threshold,
-                                                                    n_tok_total, n_pub, mf, out, m.push_blocks, m.err);
+    kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                        table->view(), remote_hash, rem_off, threshold,
+                                                                        n_tok_total, n_pub, mf, out, m.push_blocks, m.err);
     ok(cudaGetLastError());
     ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
     count_launch();
@@ -992,10 +1057,10 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
     if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t) * 4, stream);
     if (e == cudaSuccess) {
         count_launch();
-        kvx_match_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
-                                                                        table->view(), remote_hash, rem_off, threshold,
-                                                                        n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr},
-                                                                        out, push_blocks, err);
+        kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                            table->view(), remote_hash, rem_off, threshold,
+                                                                            n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr},
+                                                                            out, push_blocks, err);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);

@@ -179,6 +179,28 @@ def test_match_decisions_and_plan_runs_reduced():
     c.close()
 
 
+@pytest.mark.parametrize("flags", [0, kvx.KVX_MATCH_FILL_HOLES, kvx.KVX_MATCH_KEEP_LAST])
+def test_local_hits_far_past_the_published_span(flags):
+    """Every block resident locally, the published spans cut early (flipped hashes) or absent
+    (expired sessions): the local prefix runs far past the remote one, over many windows of 32, so the
+    match has to continue the session's own chain there, from the first unmatched block."""
+    w = kvx_inputs.bidir_mla_fp8(seed=29, n_sessions=32, n_layers=1, system_tokens=512, hist_range=(2000, 12000),
+                                 resident_p=1.0, threshold=64)
+    trim_to_blocks(w, set(range(0, w.n_sessions, 3)))
+    c = Case(w, flip_frac=0.02, seed=11)
+    expiry = np.where(np.arange(w.n_sessions) % 2 == 0, 50, 500).astype(np.int64)   # even sessions expired
+    for exp in (None, expiry):
+        want = c.oracle_match(flags=flags, expiry=exp, now=100)
+        assert want["status"] == 0
+        n_full = (np.diff(w.tok_off) // w.block_size)
+        assert (want["local_hit"] == n_full).all()                           # all resident: to the end
+        assert (want["remote_hit"] < n_full - 40).sum() >= 8                 # many spans end far earlier
+        st, plan, got = c.match(want_plan=False, flags=flags, expiry=exp, now=100)
+        assert st in (kvx.KVX_OK, kvx.KVX_ENOMEM) and plan is None
+        assert_decisions(got, want)
+    c.close()
+
+
 def test_match_plan_and_push_reduced():
     w = kvx_inputs.bidir_mla_fp8(seed=22, n_sessions=16, n_layers=3, system_tokens=256, hist_range=(64, 2500),
                                  resident_p=0.5, threshold=128)
