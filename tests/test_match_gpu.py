@@ -201,6 +201,36 @@ def test_local_hits_far_past_the_published_span(flags):
     c.close()
 
 
+@pytest.mark.parametrize("bs", [16, 64, 256])
+def test_match_decisions_at_block_sizes(bs):
+    """Synthetic sessions at several block sizes (256 is past the shared-memory staging of the
+    match): published hashes from the oracle with some flipped, a random half of the blocks resident."""
+    rng = np.random.default_rng(bs)
+    lens = rng.integers(0, 40 * bs, 48)
+    lens[:4] = [0, bs - 1, bs, 3 * bs]                                       # empty, short, exact
+    tokens = rng.integers(0, 151936, int(lens.sum())).astype(np.uint32)
+    tok_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    orc = oracle.load()
+    hs = [orc.block_hashes(tokens[tok_off[s]:tok_off[s + 1]], bs) for s in range(len(lens))]
+    allh = np.concatenate(hs)
+    remote = allh.copy()
+    remote[rng.random(len(allh)) < 0.01] ^= np.uint64(1)
+    rem_off = np.concatenate([[0], np.cumsum([len(h) for h in hs])]).astype(np.int64)
+    remote_blk = np.arange(len(allh), dtype=np.int32)
+    keys = np.unique(allh[rng.random(len(allh)) < 0.5])
+    free = np.arange(len(allh), dtype=np.int32)
+    want = orc.match(tokens, tok_off, bs, keys, remote, remote_blk, rem_off, 2 * bs, free)
+    table = kvx.kvx_table_build(dev(keys, np.uint64), dev(np.arange(len(keys), dtype=np.int32), np.int32), len(keys))
+    out = torch.zeros(len(lens) * 24, dtype=torch.uint8, device="cuda")
+    st, plan = kvx.kvx_match_prefix(dev(tokens, np.uint32), dev(tok_off, np.int64), len(lens), bs, table,
+                                    dev(remote, np.uint64), dev(remote_blk, np.int32), dev(rem_off, np.int64), 2 * bs,
+                                    dev(free, np.int32), len(free), None, None, out, want_plan=False)
+    assert st == kvx.KVX_OK and want["status"] == 0
+    assert_decisions(results(out, len(lens)), want)
+    assert want["push"].sum() > 0 and (want["remote_hit"] < np.diff(rem_off)).sum() > 0
+    kvx.kvx_table_destroy(table)
+
+
 def test_match_plan_and_push_reduced():
     w = kvx_inputs.bidir_mla_fp8(seed=22, n_sessions=16, n_layers=3, system_tokens=256, hist_range=(64, 2500),
                                  resident_p=0.5, threshold=128)
