@@ -214,25 +214,30 @@ struct MatchFlags {
     uint8_t *resident;       // FILL_HOLES: per published block, 1 if resident locally (scratch)
 };
 
-// Hash of one block chained to `parent`: the 8 parent octets, then the block's token octets.
-template <bool SHARED>
+// Hash of one block chained to `parent`: the 8 parent octets, then the block's token octets. The
+// tokens are read 16 bytes at a time where aligned: a scalar head up to the first 16-byte boundary,
+// the aligned body, a scalar tail.
 __device__ __forceinline__ uint64_t block_hash(uint64_t parent, const uint32_t *tok, int32_t bs) {
     uint32_t lo = kFnvBasisLo, hi = kFnvBasisHi;
     fnv_word(lo, hi, (uint32_t)parent);
     fnv_word(lo, hi, (uint32_t)(parent >> 32));
-#pragma unroll 8
-    for (int32_t i = 0; i < bs; ++i) fnv_word(lo, hi, SHARED ? tok[i] : __ldg(tok + i));
+    const int32_t head = min(bs, (int32_t)((16 - ((uintptr_t)tok & 15)) & 15) >> 2);
+    for (int32_t i = 0; i < head; ++i) fnv_word(lo, hi, __ldg(tok + i));
+    const uint4 *v = reinterpret_cast<const uint4 *>(tok + head);
+    const int32_t n_vec = (bs - head) >> 2;
+#pragma unroll 4
+    for (int32_t i = 0; i < n_vec; ++i) {
+        const uint4 q = __ldg(v + i);
+        fnv_word(lo, hi, q.x);
+        fnv_word(lo, hi, q.y);
+        fnv_word(lo, hi, q.z);
+        fnv_word(lo, hi, q.w);
+    }
+    for (int32_t i = head + 4 * n_vec; i < bs; ++i) fnv_word(lo, hi, __ldg(tok + i));
     return ((uint64_t)hi << 32) | lo;
 }
 
 constexpr int kMatchThreads = 256;
-// Tokens of a round of candidates are staged in shared memory, one block per row of an odd number of
-// words (so the threads, each reading its own row, hit 32 different banks), for block sizes up to:
-constexpr int32_t kStagedMaxBs = 159;
-
-static inline size_t match_stage_bytes(int32_t bs) {
-    return bs <= kStagedMaxBs ? (size_t)kMatchThreads * (size_t)(bs | 1) * sizeof(uint32_t) : 0;
-}
 
 // One CTA per session. The remote prefix is found without walking the chain: block j is hashed from
 // the PUBLISHED hash of block j - 1 (its candidate c_j), and the first j where c_j differs from the
@@ -243,16 +248,13 @@ static inline size_t match_stage_bytes(int32_t bs) {
 // window with ballots. Local hits can use candidates up to and including the first mismatch; if every
 // block to there is resident, warp 0 continues the true chain from that block, window by window, until
 // the first block that is not resident. With FILL_HOLES, residency inside the remote prefix is
-// recorded for the plan emission and the non-resident blocks there are counted. STAGED: each round's
-// tokens are first copied into shared memory by whole warps (coalesced), then hashed from there.
-template <bool STAGED>
+// recorded for the plan emission and the non-resident blocks there are counted.
 __global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
                                                                     int32_t n_sessions, int32_t bs, TableView table,
                                                                     const uint64_t *remote_hash, const int64_t *rem_off,
                                                                     int32_t threshold, int64_t n_tok_total, int64_t n_pub,
                                                                     MatchFlags mf, kvx_match_result *out,
                                                                     int64_t *push_blocks, int32_t *err) {
-    extern __shared__ uint32_t stage[];         // STAGED: kMatchThreads rows of (bs | 1) words
     __shared__ uint64_t cand[kMatchThreads];
     __shared__ uint8_t flag[kMatchThreads];     // bit 0: equals the published hash, bit 1: resident
     __shared__ int32_t go_on;
@@ -281,22 +283,10 @@ __global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32
     int64_t l_loc = 0, l_rem = 0, holes = 0;
     bool loc_open = true, rem_open = true, chain = false;
     uint64_t chain_parent = 0;
-    const int32_t stride = bs | 1;
     for (int64_t base = 0; base < n_cand; base += kMatchThreads) {
         const int64_t j = base + tid;
-        if (STAGED) {
-            const int64_t n_round = min((int64_t)kMatchThreads, n_cand - base);
-            for (int64_t b = warp; b < n_round; b += kMatchThreads / 32) {
-                const uint32_t *g = tk + (base + b) * bs;
-                uint32_t *d = stage + b * stride;
-                for (int32_t i = lane; i < bs; i += 32) d[i] = __ldg(g + i);
-            }
-            __syncthreads();
-        }
         if (j < n_cand) {
-            const uint64_t parent = j == 0 ? 0 : remote_hash[r0 + j - 1];
-            const uint64_t c = STAGED ? block_hash<true>(parent, stage + tid * stride, bs)
-                                      : block_hash<false>(parent, tk + j * bs, bs);
+            const uint64_t c = block_hash(j == 0 ? 0 : remote_hash[r0 + j - 1], tk + j * bs, bs);
             const bool same = j < n_rem && remote_hash[r0 + j] == c;
             const bool res = table_find(table, c) >= 0;
             cand[tid] = c;
@@ -387,40 +377,6 @@ __global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32
     r.dst_start = -1;
     out[s] = r;
     push_blocks[s] = push ? missing_blocks : 0;
-}
-
-// One CTA per session; the staged variant for block sizes whose rows fit shared memory.
-static cudaError_t launch_match(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t bs,
-                                TableView table, const uint64_t *remote_hash, const int64_t *rem_off, int32_t threshold,
-                                int64_t n_tok_total, int64_t n_pub, MatchFlags mf, kvx_match_result *out,
-                                int64_t *push_blocks, int32_t *err, cudaStream_t stream) {
-    const size_t smem = match_stage_bytes(bs);
-    const dim3 grid((unsigned)max(n_sessions, 1));
-    if (smem) {
-        // the shared-memory limit is a property of the function in each device's context
-        static std::mutex mu;
-        static std::map<int, bool> done;
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        {
-            std::lock_guard<std::mutex> lk(mu);
-            if (!done[dev]) {
-                e = cudaFuncSetAttribute(kvx_match_sessions<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)match_stage_bytes(kStagedMaxBs));
-                if (e != cudaSuccess) return e;
-                done[dev] = true;
-            }
-        }
-        kvx_match_sessions<true><<<grid, kMatchThreads, smem, stream>>>(tokens, tok_off, n_sessions, bs, table, remote_hash,
-                                                                        rem_off, threshold, n_tok_total, n_pub, mf, out,
-                                                                        push_blocks, err);
-    } else {
-        kvx_match_sessions<false><<<grid, kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, bs, table, remote_hash,
-                                                                      rem_off, threshold, n_tok_total, n_pub, mf, out,
-                                                                      push_blocks, err);
-    }
-    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -920,8 +876,9 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
     count_launch();
     if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
-    ok(launch_match(tokens, tok_off, n_sessions, block_size, table->view(), remote_hash, rem_off, threshold, n_tok_total,
-                    n_pub, mf, out, m.push_blocks, m.err, stream));
+    kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                        table->view(), remote_hash, rem_off, threshold,
+                                                                        n_tok_total, n_pub, mf, out, m.push_blocks, m.err);
     ok(cudaGetLastError());
     ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
     count_launch();
@@ -1113,8 +1070,11 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
     if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t) * 4, stream);
     if (e == cudaSuccess) {
         count_launch();
-        e = launch_match(tokens, tok_off, n_sessions, block_size, table->view(), remote_hash, rem_off, threshold,
-                         n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr}, out, push_blocks, err, stream);
+        kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
+                                                                            table->view(), remote_hash, rem_off, threshold,
+                                                                            n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr},
+                                                                            out, push_blocks, err);
+        e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);
     if (e == cudaSuccess) {
