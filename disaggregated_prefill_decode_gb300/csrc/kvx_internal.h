@@ -165,6 +165,7 @@ namespace kvx {
 // Shared by host-built and device-built plans (kvx_plan.cpp).
 kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl);
 void finish_plan_shape(kvx_plan_s *pl);
+bool as_whole_block_copy(kvx_plan_s *pl);
 // Device layout and kernel arguments of a plan (kvx_push.cu).
 void plan_layout(kvx_plan_s *pl);
 CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0);

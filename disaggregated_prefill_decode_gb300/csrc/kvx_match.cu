@@ -804,9 +804,10 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
             delete pl;
             return fail(KVX_EINVAL, "pool block sizes must equal block_size");
         }
-        if (pl->per_head) {
+        if (pl->per_head && !as_whole_block_copy(pl)) {
             delete pl;
-            return fail(KVX_EUNSUPPORTED, "device-built plans need KVX_LAYOUT_NHD pools");
+            return fail(KVX_EUNSUPPORTED,
+                        "device-built plans need both pools NHD, or both HND with the same head partition");
         }
         if (std::max(pl->src.n_shards, pl->dst.n_shards) > 8) {
             delete pl;

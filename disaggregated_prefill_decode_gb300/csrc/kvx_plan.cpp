@@ -296,6 +296,23 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     return KVX_OK;
 }
 
+// A plan that only ever copies whole blocks between two head-major pools with the same head
+// partition and block size moves each block as one span of identical bytes: it is copied as a
+// contiguous plan. False (plan unchanged) for any other pair of layouts.
+bool as_whole_block_copy(kvx_plan_s *pl) {
+    const Geom &s = pl->src, &d = pl->dst;
+    if (s.layout != KVX_LAYOUT_HND || d.layout != KVX_LAYOUT_HND || s.n_shards != d.n_shards ||
+        s.heads_per_shard != d.heads_per_shard || s.block_size != d.block_size)
+        return false;
+    pl->per_head = 0;
+    pl->strided = 0;
+    pl->width = (int32_t)s.row_bytes();
+    pl->src_pitch = s.row_bytes();
+    pl->dst_pitch = d.row_bytes();
+    pl->tile_bytes = default_tile_bytes(s, d);
+    return true;
+}
+
 // Bulk copies need 16-byte aligned addresses, sizes, widths and pitches (vec == 16), a ring that
 // fits shared memory and, for strided plans, a row that fits a stage. The automatic choice, measured
 // on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at one CTA per SM

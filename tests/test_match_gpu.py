@@ -259,6 +259,37 @@ def test_match_plan_and_push_reduced():
     c.close()
 
 
+def test_match_plan_between_head_major_pools():
+    """The decode->prefill plan between two head-major K/V pools (8 heads of 128 bf16, the same head
+    partition): whole blocks are identical spans on both sides, so the device-built plan copies them
+    as such; the consumer equals the oracle's head-major push. Pools of different layouts are
+    refused before any device work."""
+    w = kvx_inputs.bidir_mla_fp8(seed=23, n_sessions=12, n_layers=2, system_tokens=256, hist_range=(64, 1500),
+                                 resident_p=0.5, threshold=128)
+    c = Case(w, flip_frac=0.005, seed=9)
+    want = c.oracle_match()
+    kv = dict(n_planes=2, heads_per_shard=8, head_dim=128, elem_bytes=2, layout=kvx_inputs.LAYOUT_HND)
+    dec, pre = w.decode.replace(**kv), w.prefill.replace(**kv)
+    src, _ = device_pool(dec, "bf16_normal", seed=12)
+    dst, _ = device_pool(pre, "canary_bf16_normal")
+    st, plan, got = c.match(kvx.Pool(dec, src), kvx.Pool(pre, dst))
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    assert kvx.kvx_plan_get_info(plan)["strided"] == 0
+    side = torch.cuda.Stream(priority=-1)
+    for layer in range(dec.n_layers):
+        kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(dec, src, pre, dst, lambda l: [canary_host(pre, "bf16_normal") for _ in range(2)],
+                 oracle_requests(c, want), range(dec.n_layers))
+    kvx.kvx_plan_destroy(plan)
+    nhd = pre.replace(layout=kvx_inputs.LAYOUT_NHD)
+    with pytest.raises(kvx.KvxError) as ei:
+        c.match(kvx.Pool(dec, src), kvx.Pool(nhd, dst))
+    assert ei.value.status == kvx.KVX_EUNSUPPORTED
+    c.close()
+
+
 def test_match_full_sessions_two_layers():
     """All 256 sessions of the bidirectional workload (1024 shared + U[2k,32k] history tokens each);
     the pool has 2 of its 48 layers so the whole push is checked against the oracle."""
