@@ -65,6 +65,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-config", action="store_true", help="skip the short runs of the other push configs")
+    p.add_argument("--no-overlap", action="store_true", help="skip the prefill / push overlap measurement")
     return p.parse_args()
 
 
@@ -310,6 +311,74 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
             "issue_us": issue_us}
 
 
+def measure_overlap(args, torch, kvx, m, steps=200):
+    """The pages' premise, measured: is the push off the prefill's critical path? Per step, the
+    synthetic prefill alone (the L fixture launches on the priority stream), the pushes alone (the L
+    layer pushes, no gate), and both (the benchmark's pattern: each push gated on its layer's event);
+    and how long the prefill chain itself takes inside the combined run. Twice: with the benchmark's
+    fixture (a prefill layer shorter than its push) and with one 8 times longer (a prefill layer longer
+    than its push, the regime of a real model, whose layers take far longer than their KV copy)."""
+    L, reqs, sp, dp = m["L"], m["reqs"], m["sp"], m["dp"]
+    opts = m["opts"]
+    lib = kvx._lib
+    main = torch.cuda.Stream(priority=-1)
+    side = torch.cuda.Stream(priority=0)
+    ready = [torch.cuda.Event() for _ in range(L)]
+    for ev in ready:
+        ev.record(main)
+    ready_h = [int(ev.cuda_event) for ev in ready]
+    main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
+
+    def run(prefill, push, n, iters):
+        prev, marks = None, []
+        for _ in range(n):
+            plan = kvx.kvx_plan_ex(sp, dp, reqs, opts) if push else None
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for layer in range(L):
+                if prefill:
+                    lib.kvx_fixture_prefill(args.fixture_ctas, iters, None, 0, layer, main_h, ready_h[layer])
+                if push:
+                    lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer] if prefill else None)
+            b.record(main)
+            marks.append((a, b))
+            if prev is not None:
+                assert kvx.kvx_sync(prev, -1) == kvx.KVX_OK
+                kvx.kvx_plan_destroy(prev)
+            prev = plan
+        if prev is not None:
+            assert kvx.kvx_sync(prev, -1) == kvx.KVX_OK
+            kvx.kvx_plan_destroy(prev)
+        return marks
+
+    def timed(prefill, push, iters):
+        run(prefill, push, 3, iters)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(main)
+        marks = run(prefill, push, steps, iters)
+        main.wait_stream(side)
+        t1.record(main)
+        torch.cuda.synchronize()
+        chain = statistics.median(a.elapsed_time(b) for a, b in marks) if prefill else None
+        return t0.elapsed_time(t1) / steps, chain
+
+    push_only, _ = timed(False, True, 0)
+    out = {"push_only_ms_per_step": round(push_only, 4)}
+    for name, iters in (("short_prefill", args.fixture_iters), ("long_prefill", 8 * args.fixture_iters)):
+        pre_only, chain_alone = timed(True, False, iters)
+        both, chain_with = timed(True, True, iters)
+        out[name] = {"fixture_iters": iters, "prefill_only_ms_per_step": round(pre_only, 4),
+                     "together_ms_per_step": round(both, 4),
+                     "hidden_frac": round((pre_only + push_only - both) / min(pre_only, push_only), 3),
+                     "prefill_chain_ms_alone": round(chain_alone, 4),
+                     "prefill_chain_ms_with_push": round(chain_with, 4),
+                     "prefill_slowdown": round(chain_with / chain_alone - 1, 4)}
+    out["how"] = (f"{steps} steps each; the prefill chain is the median time on its stream from a step's first "
+                  "fixture to its last; hidden_frac = (prefill + push - together) / min(prefill, push)")
+    return out
+
+
 KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"]
 
 
@@ -419,6 +488,8 @@ def run_kvx(args, rank, local_rank, world):
     }
     if rank == 0:
         result["memcpy_ceiling"] = memcpy_ceiling(torch, device)
+        if not args.no_overlap:
+            result["overlap"] = measure_overlap(args, torch, kvx, m)
         if not args.no_e2e:
             result["e2e"] = run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world)
         if not args.no_match:

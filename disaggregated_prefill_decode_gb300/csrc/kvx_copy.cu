@@ -201,13 +201,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for a stage's phase; false when the deadline passed.
+// Bounded wait for a stage's phase; false when the deadline passed. Each try_wait already suspends
+// the thread for a while when the phase is not complete; the global timer (a costly special register
+// to read, and issue slots taken from the SM's other warps) is read only every 64 tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_test(bar, parity))
-        if (global_ns() - t0 > kBulkWaitNs) return false;
-    return true;
+    for (uint32_t k = 1;; ++k) {
+        if (mbar_test(bar, parity)) return true;
+        if ((k & 63) == 0 && global_ns() - t0 > kBulkWaitNs) return false;
+    }
 }
 
 __device__ __forceinline__ void bulk_load(void *stage, const void *src, uint32_t bytes, uint64_t *bar) {
