@@ -488,6 +488,7 @@ def run_kvx(args, rank, local_rank, world):
     }
     if rank == 0:
         result["memcpy_ceiling"] = memcpy_ceiling(torch, device)
+        result["memcpy_ceiling"]["push_frac"] = round(achieved / result["memcpy_ceiling"]["value"], 4)
         if not args.no_overlap:
             result["overlap"] = measure_overlap(args, torch, kvx, m)
         if not args.no_e2e:
