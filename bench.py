@@ -1,17 +1,18 @@
-"""Benchmark of the kvx layer push (and the prefix match) on one GB300, or N independent replicas.
+"""Benchmark of the kvx layer push (and, on rank 0, the end-to-end path, the prefix match, the
+prefill/push overlap, the other push configurations and the oracle on the host's cores).
 
-Default workload: the Qwen3-32B-shaped single-request push (64 layers x {K,V}, 8 KV heads x 128 bf16,
-block 16, one 8192-token prompt = 512 blocks, pools of 615 blocks, destination ids chunked). One step
-is the whole hot path once: build the plan on the host, then for each layer run the synthetic prefill
-fixture on the main stream, record its event, push that layer on a high-priority side stream gated
-on the event, and finally kvx_sync. Inputs move 4.3 GB per step (larger than the 129 MB L2), so no
+One step = the whole push path for one batch of requests on the workload's pools: build the plan,
+then per layer run the synthetic prefill fixture on the priority stream (it records the layer's
+ready event) and kvx_push_layer gated on that event. Steps are issued with one step of look-ahead (a
+step's plan is synced after the next step has been issued). The pools are far larger than L2, so no
 flush is needed between steps.
 
-Printed: one JSON line (rank 0). value = read+write bytes of all pushes / device time of the timed
-steps (CUDA events on the main stream around all steps), summed over ranks / max over ranks.
-roofline.achieved = the same bytes per push launch / the mean push duration (CUDA events on the side
-stream around each launch). e2e = the same metric with the producer KV starting in pinned host memory
-and the consumer KV read back each step (per-layer copies overlapped with the pushes).
+value = read+write bytes of all timed steps / device time of the timed steps (CUDA events on the
+prefill stream around all steps), summed over ranks / max over ranks.
+roofline.achieved = the same bytes per push launch / the mean push duration, where the push
+durations are the copy kernels' own global-timer stamps (first CTA start, last CTA end) and the mean
+is the union of all timed launches on that one device clock / launches.
+
 --impl reference times the CPU oracle instead (rank 0 only), on bounded samples of the same workload.
 """
 from __future__ import annotations
