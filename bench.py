@@ -1,6 +1,9 @@
 """Benchmark of the kvx layer push (and, on rank 0, the end-to-end path, the prefix match, the
 prefill/push overlap, the other push configurations and the oracle on the host's cores).
 
+Default workload: the Qwen3-32B-shaped single-request push (64 layers x {K,V}, 8 KV heads x 128 bf16,
+block 16, one 8192-token prompt = 512 blocks, pools of 615 blocks, destination ids chunked).
+
 One step = the whole push path for one batch of requests on the workload's pools: build the plan,
 then per layer run the synthetic prefill fixture on the priority stream (it records the layer's
 ready event) and kvx_push_layer gated on that event. Steps are issued with one step of look-ahead (a
@@ -12,6 +15,8 @@ prefill stream around all steps), summed over ranks / max over ranks.
 roofline.achieved = the same bytes per push launch / the mean push duration, where the push
 durations are the copy kernels' own global-timer stamps (first CTA start, last CTA end) and the mean
 is the union of all timed launches on that one device clock / launches.
+e2e = the same metric with the producer KV starting in pinned host memory and the pushed consumer
+blocks gathered on the device and read back every step (per-layer copies overlapped with the pushes).
 
 --impl reference times the CPU oracle instead (rank 0 only), on bounded samples of the same workload.
 """
