@@ -162,6 +162,30 @@ def test_geometry_sweep(name, kernel):
     kvx.kvx_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_offsets_past_4gib(kernel):
+    """One 4.9 GB buffer per side (150,000 blocks of 32 KiB): runs that start and end beyond 2^32 bytes,
+    one that straddles it and one near the start; every copied block equals its source block and the
+    blocks around them keep their canary."""
+    g = PoolGeom(1, 1, 1, 8, 128, 2, 16, 150_000)
+    bb = 16 * g.row_bytes
+    src, _ = device_pool(g, "bf16_normal", seed=9)
+    dst, _ = device_pool(g, "canary_bf16_normal")
+    assert g.buffer_bytes > (1 << 32) + 8 * bb
+    edge = (1 << 32) // bb                                             # first block past 4 GiB: 131072
+    runs = [(edge - 3, edge + 1000, 7), (edge + 5000, edge - 2, 6), (10, 149_990, 4), (149_000, 20, 9)]
+    reqs = [(n * 16, np.arange(sb, sb + n), np.arange(db, db + n)) for sb, db, n in runs]
+    plan = kvx.kvx_plan_ex(kvx.Pool(g, src), kvx.Pool(g, dst), reqs, {"kernel": KERNELS[kernel]})
+    assert push_all_layers(plan, 1) == kvx.KVX_OK
+    kvx.kvx_plan_destroy(plan)
+    canary = torch.tensor(kvx_inputs.CANARY_BF16 - 0x10000, dtype=torch.int16, device="cuda")
+    s, d = src[0], dst[0]
+    for sb, db, n in runs:
+        assert torch.equal(d[db * bb:(db + n) * bb], s[sb * bb:(sb + n) * bb]), (sb, db, n)
+        for nb in (db - 1, db + n):                                    # the neighbours keep the canary
+            assert bool((d[nb * bb:(nb + 1) * bb].view(torch.int16) == canary).all()), nb
+
+
 def test_one_huge_run_equals_one_copy():
     g = PoolGeom(2, 2, 1, 8, 128, 2, 16, 1100)
     src, _ = device_pool(g, "bf16_normal", seed=3)
