@@ -68,6 +68,7 @@ using namespace kvx;
 namespace {
 
 constexpr int64_t kSecond = 1000 * 1000;
+constexpr int32_t kMaxRanks = 1 << 16;   // every record keeps one counter set per rank
 
 bool terminal(int32_t s) {
     return s == KVX_CONN_DONE || s == KVX_CONN_FAILED || s == KVX_CONN_EXPIRED || s == KVX_CONN_TIMED_OUT ||
@@ -156,8 +157,8 @@ kvx_status kvx_conn_create(const kvx_conn_config *cfg, kvx_conn_t *out) {
     if (cfg) {
         if (cfg->reserved) return fail(KVX_EINVAL, "kvx_conn_config.reserved must be 0");
         if (cfg->defer_timeout_us < 0 || cfg->transfer_timeout_us < 0 || cfg->recv_abort_timeout_us < 0 ||
-            cfg->n_ranks < 0)
-            return fail(KVX_EINVAL, "timeouts and n_ranks must be >= 0");
+            cfg->n_ranks < 0 || cfg->n_ranks > kMaxRanks)
+            return fail(KVX_EINVAL, "timeouts must be >= 0 and n_ranks in [0, %d]", kMaxRanks);
         if (cfg->defer_timeout_us) c.defer_timeout_us = cfg->defer_timeout_us;
         if (cfg->transfer_timeout_us) c.transfer_timeout_us = cfg->transfer_timeout_us;
         if (cfg->recv_abort_timeout_us) c.recv_abort_timeout_us = cfg->recv_abort_timeout_us;

@@ -453,7 +453,8 @@ typedef struct kvx_conn_config {
     int64_t defer_timeout_us;      /* 0 selects 60 s  */
     int64_t transfer_timeout_us;   /* 0 selects 30 s  */
     int64_t recv_abort_timeout_us; /* 0 selects 120 s */
-    int32_t n_ranks;               /* writer ranks (acknowledgements) that complete a request; 0 selects 1 */
+    int32_t n_ranks;               /* writer ranks (acknowledgements) that complete a request, at most
+                                      65536; 0 selects 1 */
     int32_t reserved;              /* must be 0 */
 } kvx_conn_config;
 

@@ -317,7 +317,7 @@ def test_poll_hands_out_events_in_order_up_to_cap(conn):
 
 
 def test_argument_checks():
-    bad_cfgs = [dict(defer_timeout_us=-1), dict(n_ranks=-2), dict(recv_abort_timeout_us=-5)]
+    bad_cfgs = [dict(defer_timeout_us=-1), dict(n_ranks=-2), dict(recv_abort_timeout_us=-5), dict(n_ranks=65537)]
     for cfg in bad_cfgs:
         with pytest.raises(kvx.KvxError) as ei:
             kvx.kvx_conn_create(**cfg)
