@@ -218,7 +218,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
     lib = kvx._lib                                    # the C-ABI itself, called directly in the loop
-    push_times, issue_us = [], []
+    push_times, issue_us, plan_us = [], [], []
 
     # The synthetic prefill is launched layer by layer from the host between the pushes (an engine
     # issuing its forward pass); --fixture-graph captures the L launches once into a CUDA graph and
@@ -236,7 +236,9 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
 
     def issue(timing):
         """One step: its plan, the prefill (graph replay or per-layer launches) and the gated pushes."""
+        p0 = time.perf_counter()
         plan = kvx.kvx_plan_ex(sp, dp, reqs, timing_opts if timing else opts)
+        plan_us.append((time.perf_counter() - p0) * 1e6)
         if fixture_graph is not None:
             fixture_graph.replay()                    # on the current stream: main
             for layer in range(L):
@@ -314,7 +316,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
             "blocks_step": sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L,
             "elapsed_ms": t0.elapsed_time(t1), "launches": launches, "clocks": clk, "wall": wall,
             "mean_push_ms": busy_us / (len(push_times) * L) * 1e-3, "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
-            "issue_us": issue_us}
+            "issue_us": issue_us, "plan_us": plan_us}
 
 
 def measure_overlap(args, torch, kvx, m, steps=200):
@@ -383,6 +385,36 @@ def measure_overlap(args, torch, kvx, m, steps=200):
     out["how"] = (f"{steps} steps each; the prefill chain is the median time on its stream from a step's first "
                   "fixture to its last; hidden_frac = (prefill + push - together) / min(prefill, push)")
     return out
+
+
+def connector_rate(kvx, n=20000):
+    """Requests per second through the host connector's whole protocol: registration, last prefill
+    chunk, poll (READY), start, one queued write, seal, its report (all layers DONE), poll (DONE),
+    release; alternate requests arrive in the other order (prefill first, deferred)."""
+    import numpy as np_
+    conn = kvx.kvx_conn_create()
+    ids = np_.arange(16, dtype=np_.int32)
+    states = np_.full(64, kvx.KVX_LAYER_DONE, np_.int32)
+    t0 = time.perf_counter()
+    for r in range(n):
+        if r & 1:
+            kvx.kvx_conn_prefill(conn, r, 0, ids, 256, True, r)
+            kvx.kvx_conn_register(conn, r, 0, ids, r)
+        else:
+            kvx.kvx_conn_register(conn, r, 0, ids, r)
+            kvx.kvx_conn_prefill(conn, r, 0, ids, 256, True, r)
+        kvx.kvx_conn_poll(conn, r, 8)
+        kvx.kvx_conn_start(conn, r, 0, r)
+        kvx.kvx_conn_write_issued(conn, r, 0, 0, 1)
+        kvx.kvx_conn_seal(conn, r, 0, 0)
+        kvx.kvx_conn_write_done(conn, r, 0, 0, states, now_us=r)
+        kvx.kvx_conn_poll(conn, r, 8)
+        kvx.kvx_conn_release(conn, r)
+    dt = time.perf_counter() - t0
+    kvx.kvx_conn_destroy(conn)
+    return {"requests_per_s": round(n / dt, 1), "calls_per_request": 10,
+            "how": f"{n} requests through the Python binding, one host thread: the figure is mostly the "
+                   "binding's per-call cost (about 4 us a call), not the native state machine's"}
 
 
 KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"]
@@ -491,12 +523,14 @@ def run_kvx(args, rank, local_rank, world):
         "clocks": m["clocks"],
         "host_wall_s": round(m["wall"], 4),
         "host_issue_us_per_layer": round(statistics.fmean(m["issue_us"]) / L, 3),
+        "plan_build_us": round(statistics.median(m["plan_us"]), 2),
     }
     if rank == 0:
         result["memcpy_ceiling"] = memcpy_ceiling(torch, device)
         result["memcpy_ceiling"]["push_frac"] = round(achieved / result["memcpy_ceiling"]["value"], 4)
         if not args.no_overlap:
             result["overlap"] = measure_overlap(args, torch, kvx, m)
+        result["connector"] = connector_rate(kvx)
         if not args.no_e2e:
             result["e2e"] = run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world)
         if not args.no_match:
