@@ -583,10 +583,18 @@ struct EmitShape {
     int32_t tile_bytes;
     int32_t rows_per_tile;
     int32_t n_pairs;
-    int32_t pad;
+    int32_t per_head;                    // a head-major side: tiles per (block, head)
     int32_t pair_s[8], pair_d[8];
     int64_t pair_soff[8], pair_doff[8];
+    // per_head: the head partition and layout of each side, the head's bytes and each side's token pitch
+    int32_t heads, hps_s, hps_d, layout_s, layout_d;
+    int64_t head_bytes, src_pitch, dst_pitch;
 };
+
+// Element index (in heads) of (block, slot 0, head) inside one buffer of a side's layout.
+__device__ __forceinline__ int64_t head_start(int32_t layout, int32_t hps, int32_t bs, int64_t blk, int32_t head) {
+    return layout == KVX_LAYOUT_HND ? (blk * hps + head) * (int64_t)bs : blk * (int64_t)bs * hps + head;
+}
 
 __global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, EmitShape sh, int64_t *tile_count) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -594,6 +602,10 @@ __global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, 
     if (r >= n_runs) return;
     const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
     const int64_t ntok = (k1 - run_start[r]) * sh.bs;
+    if (sh.per_head) {
+        tile_count[r] = (k1 - run_start[r]) * sh.heads * ((sh.bs + sh.rows_per_tile - 1) / sh.rows_per_tile);
+        return;
+    }
     const int64_t per = sh.strided ? (ntok + sh.rows_per_tile - 1) / sh.rows_per_tile
                                    : (ntok * sh.src_row_bytes + sh.tile_bytes - 1) / sh.tile_bytes;
     tile_count[r] = per * sh.n_pairs;
@@ -616,6 +628,27 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
     run_dst_row[r] = (int32_t)drow;
     run_ntok[r] = (int32_t)ntok;
     int64_t t = tile_start[r];
+    if (sh.per_head) {
+        // every block of the run, every head: bs rows at each side's token pitch
+        for (int64_t k = k0; k < k1; ++k)
+            for (int32_t g = 0; g < sh.heads; ++g) {
+                const int32_t ss = g / sh.hps_s, ds = g / sh.hps_d;
+                const int64_t s0 = head_start(sh.layout_s, sh.hps_s, sh.bs, pair_src[k], g % sh.hps_s) * sh.head_bytes;
+                const int64_t d0 = head_start(sh.layout_d, sh.hps_d, sh.bs, pair_dst[k], g % sh.hps_d) * sh.head_bytes;
+                for (int32_t r0 = 0; r0 < sh.bs; r0 += sh.rows_per_tile, ++t) {
+                    if (t >= tile_cap) { atomicOr(err, 16); return; }
+                    TileDesc d;
+                    d.src_off = s0 + r0 * sh.src_pitch;
+                    d.dst_off = d0 + r0 * sh.dst_pitch;
+                    d.n = min(sh.rows_per_tile, sh.bs - r0);
+                    d.s_shard = ss;
+                    d.d_shard = ds;
+                    d.pad = 0;
+                    tiles[t] = d;
+                }
+            }
+        return;
+    }
     if (!sh.strided) {
         const int64_t bytes = ntok * sh.src_row_bytes;
         const int64_t s0 = srow * sh.src_row_bytes, d0 = drow * sh.dst_row_bytes;
@@ -804,12 +837,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
             delete pl;
             return fail(KVX_EINVAL, "pool block sizes must equal block_size");
         }
-        if (pl->per_head && !as_whole_block_copy(pl)) {
-            delete pl;
-            return fail(KVX_EUNSUPPORTED,
-                        "device-built plans need both pools NHD, or both HND with the same head partition");
-        }
-        if (std::max(pl->src.n_shards, pl->dst.n_shards) > 8) {
+        if (pl->per_head) as_whole_block_copy(pl);                   // identical spans when the layouts agree
+        if (!pl->per_head && std::max(pl->src.n_shards, pl->dst.n_shards) > 8) {
             delete pl;
             return fail(KVX_EUNSUPPORTED, "device-built plans support at most 8 shard pairs");
         }
@@ -896,17 +925,28 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         sh.strided = pl->strided;
         sh.tile_bytes = pl->tile_bytes;
         sh.rows_per_tile = pl->strided ? std::max<int32_t>(1, pl->tile_bytes / pl->width) : 1;
-        sh.n_pairs = (int32_t)pairs.size();
-        for (size_t q = 0; q < pairs.size(); ++q) {
+        sh.n_pairs = pl->per_head ? 0 : (int32_t)pairs.size();
+        sh.per_head = pl->per_head;
+        sh.heads = pl->src.n_shards * pl->src.heads_per_shard;
+        sh.hps_s = pl->src.heads_per_shard;
+        sh.hps_d = pl->dst.heads_per_shard;
+        sh.layout_s = pl->src.layout;
+        sh.layout_d = pl->dst.layout;
+        sh.head_bytes = pl->src.head_bytes();
+        sh.src_pitch = pl->src_pitch;
+        sh.dst_pitch = pl->dst_pitch;
+        for (size_t q = 0; q < (size_t)sh.n_pairs; ++q) {
             sh.pair_s[q] = pairs[q].s;
             sh.pair_d[q] = pairs[q].d;
             sh.pair_soff[q] = pairs[q].src_seg_off;
             sh.pair_doff[q] = pairs[q].dst_seg_off;
         }
         // a run of L blocks has at most L times the tiles of one block
-        const int64_t per_block = pl->strided ? (block_size + sh.rows_per_tile - 1) / sh.rows_per_tile
-                                              : ((int64_t)block_size * sh.src_row_bytes + pl->tile_bytes - 1) / pl->tile_bytes;
-        const int64_t tile_cap = B * per_block * sh.n_pairs;
+        const int64_t per_block =
+            pl->per_head ? (int64_t)sh.heads * ((block_size + sh.rows_per_tile - 1) / sh.rows_per_tile)
+            : (pl->strided ? (block_size + sh.rows_per_tile - 1) / sh.rows_per_tile
+                           : ((int64_t)block_size * sh.src_row_bytes + pl->tile_bytes - 1) / pl->tile_bytes) * sh.n_pairs;
+        const int64_t tile_cap = B * per_block;
         pl->n_tiles = tile_cap;   // sizes the layout; the real count comes back below
         plan_layout(pl);
         st = pool_alloc(&pl->dev, pl->dev_bytes, stream);

@@ -335,9 +335,9 @@ typedef struct kvx_match_result {
  * free_blocks[dst_start + k].
  *
  * remote_pool is the producer (decode) pool, local_pool the consumer (prefill) pool; their
- * block_size must equal block_size, and either both use KVX_LAYOUT_NHD (head shards may then differ,
- * as in kvx_plan) or both use KVX_LAYOUT_HND with the same head partition (whole blocks are then
- * identical byte spans on both sides); other pairs return KVX_EUNSUPPORTED. If out_plan is not NULL it receives a plan (built on the
+ * block_size must equal block_size; their layouts and head partitions may differ as in kvx_plan
+ * (whole blocks between head-major pools of the same partition move as identical byte spans, other
+ * head-major pairs head by head). If out_plan is not NULL it receives a plan (built on the
  * device) whose pushes copy those blocks with kvx_push_layer / kvx_sync; NULL computes the
  * decisions only (the pools may then be NULL). The call waits for `stream` (it reads back the
  * totals). Block ids outside a pool make the affected layers FAILED at kvx_sync (the copy kernel

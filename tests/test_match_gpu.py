@@ -259,33 +259,57 @@ def test_match_plan_and_push_reduced():
     c.close()
 
 
-def test_match_plan_between_head_major_pools():
-    """The decode->prefill plan between two head-major K/V pools (8 heads of 128 bf16, the same head
-    partition): whole blocks are identical spans on both sides, so the device-built plan copies them
-    as such; the consumer equals the oracle's head-major push. Pools of different layouts are
-    refused before any device work."""
+PULL_LAYOUTS = {
+    # name: (decode side, prefill side) as (shards, heads per shard, layout); 8 heads of 128 bf16 each
+    "hnd_same": ((1, 8, 1), (1, 8, 1)),
+    "nhd_to_hnd": ((1, 8, 0), (1, 8, 1)),
+    "hnd_to_nhd": ((1, 8, 1), (1, 8, 0)),
+    "hnd_tp1_to_hnd_tp2": ((1, 8, 1), (2, 4, 1)),
+    "nhd_tp4_to_hnd_tp1": ((4, 2, 0), (1, 8, 1)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PULL_LAYOUTS))
+def test_match_plan_between_pools_of_other_layouts(name):
+    """The decode->prefill plan between K/V pools of different layouts or head partitions (8 heads of
+    128 bf16): identical spans when both sides are head-major alike, otherwise per-(block, head) tiles
+    built on the device; the consumer equals the oracle's push of the same pairs."""
     w = kvx_inputs.bidir_mla_fp8(seed=23, n_sessions=12, n_layers=2, system_tokens=256, hist_range=(64, 1500),
                                  resident_p=0.5, threshold=128)
     c = Case(w, flip_frac=0.005, seed=9)
     want = c.oracle_match()
-    kv = dict(n_planes=2, heads_per_shard=8, head_dim=128, elem_bytes=2, layout=kvx_inputs.LAYOUT_HND)
-    dec, pre = w.decode.replace(**kv), w.prefill.replace(**kv)
+    (ss, sh, sl), (ds, dh, dl) = PULL_LAYOUTS[name]
+    kv = dict(n_planes=2, head_dim=128, elem_bytes=2)
+    dec = w.decode.replace(n_shards=ss, heads_per_shard=sh, layout=sl, **kv)
+    pre = w.prefill.replace(n_shards=ds, heads_per_shard=dh, layout=dl, **kv)
     src, _ = device_pool(dec, "bf16_normal", seed=12)
     dst, _ = device_pool(pre, "canary_bf16_normal")
     st, plan, got = c.match(kvx.Pool(dec, src), kvx.Pool(pre, dst))
     assert st == kvx.KVX_OK
     assert_decisions(got, want)
-    assert kvx.kvx_plan_get_info(plan)["strided"] == 0
+    assert (kvx.kvx_plan_get_info(plan)["strided"] == 0) == (name == "hnd_same")
     side = torch.cuda.Stream(priority=-1)
     for layer in range(dec.n_layers):
         kvx.kvx_push_layer(plan, layer, side)
     assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
-    check_layers(dec, src, pre, dst, lambda l: [canary_host(pre, "bf16_normal") for _ in range(2)],
+    per = pre.n_planes * pre.n_shards
+    check_layers(dec, src, pre, dst, lambda l: [canary_host(pre, "bf16_normal") for _ in range(per)],
                  oracle_requests(c, want), range(dec.n_layers))
     kvx.kvx_plan_destroy(plan)
-    nhd = pre.replace(layout=kvx_inputs.LAYOUT_NHD)
+    c.close()
+
+
+def test_match_plan_refuses_shard_counts_that_do_not_divide():
+    w = kvx_inputs.bidir_mla_fp8(seed=24, n_sessions=4, n_layers=1, system_tokens=128, hist_range=(64, 600),
+                                 resident_p=0.5, threshold=64)
+    c = Case(w)
+    kv = dict(n_planes=2, head_dim=64, elem_bytes=2)
+    dec = w.decode.replace(n_shards=3, heads_per_shard=2, **kv)
+    pre = w.prefill.replace(n_shards=2, heads_per_shard=3, layout=kvx_inputs.LAYOUT_HND, **kv)
+    src, _ = device_pool(dec, "bf16_normal", seed=1)
+    dst, _ = device_pool(pre, "canary_bf16_normal")
     with pytest.raises(kvx.KvxError) as ei:
-        c.match(kvx.Pool(dec, src), kvx.Pool(nhd, dst))
+        c.match(kvx.Pool(dec, src), kvx.Pool(pre, dst))
     assert ei.value.status == kvx.KVX_EUNSUPPORTED
     c.close()
 
