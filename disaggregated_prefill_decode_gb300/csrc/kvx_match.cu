@@ -115,10 +115,11 @@ __device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, 
 }
 
 // One warp per session; hashes go out a window of 32 blocks at a time (lane k writes block k of the
-// window), coalesced.
+// window), coalesced. The first block chains to parent[s] (0 without a parent array).
 __global__ void __launch_bounds__(128) kvx_hash_sessions(const uint32_t *tokens, const int64_t *tok_off,
-                                                         int32_t n_sessions, int32_t bs, uint64_t *out,
-                                                         const int64_t *hash_off, int64_t n_tok_total, int32_t *err) {
+                                                         int32_t n_sessions, int32_t bs, const uint64_t *parent,
+                                                         uint64_t *out, const int64_t *hash_off, int64_t n_tok_total,
+                                                         int32_t *err) {
     const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= n_sessions) return;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(128) kvx_hash_sessions(const uint32_t *tokens,
             if (w0 + lane <= j) o[w0 + lane] = mine;
         }
         return true;
-    });
+    }, parent ? parent[s] : 0);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -704,6 +705,12 @@ extern "C" {
 
 kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t block_size,
                             uint64_t *out_hash, const int64_t *hash_off, cudaStream_t stream) {
+    return kvx_block_hashes_ex(tokens, tok_off, n_sessions, block_size, nullptr, out_hash, hash_off, stream);
+}
+
+kvx_status kvx_block_hashes_ex(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions, int32_t block_size,
+                               const uint64_t *parent, uint64_t *out_hash, const int64_t *hash_off,
+                               cudaStream_t stream) {
     if (n_sessions < 0 || block_size < 1) return fail(KVX_EINVAL, "n_sessions >= 0 and block_size >= 1");
     if (n_sessions == 0) return KVX_OK;
     if (!tokens || !tok_off || !out_hash || !hash_off) return fail(KVX_EINVAL, "NULL device array");
@@ -719,7 +726,7 @@ kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int3
     if (e == cudaSuccess) {
         count_launch();
         kvx_hash_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
-                                                                       out_hash, hash_off, n_tok_total, err);
+                                                                       parent, out_hash, hash_off, n_tok_total, err);
         e = cudaGetLastError();
     }
     int32_t h_err = 0;

@@ -112,6 +112,7 @@ _sig = {
     "kvx_status_str": (ctypes.c_char_p, [c_i32]),
     "kvx_last_error": (ctypes.c_char_p, []),
     "kvx_block_hashes": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "kvx_block_hashes_ex": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "kvx_table_build": (c_i32, [c_vp, c_vp, c_i64, c_vp, _P(c_vp)]),
     "kvx_table_lookup": (c_i32, [c_vp, c_vp, c_i64, c_vp, c_vp]),
     "kvx_table_destroy": (c_i32, [c_vp]),
@@ -382,6 +383,12 @@ def kvx_plan_destroy(plan) -> None:
 def kvx_block_hashes(tokens, tok_off, n_sessions: int, block_size: int, out_hash, hash_off, stream=None) -> None:
     _check(_lib.kvx_block_hashes(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, _ptr(out_hash), _ptr(hash_off),
                                  _stream(stream)), "kvx_block_hashes")
+
+
+def kvx_block_hashes_ex(tokens, tok_off, n_sessions: int, block_size: int, parent, out_hash, hash_off,
+                        stream=None) -> None:
+    _check(_lib.kvx_block_hashes_ex(_ptr(tokens), _ptr(tok_off), n_sessions, block_size, _ptr(parent), _ptr(out_hash),
+                                    _ptr(hash_off), _stream(stream)), "kvx_block_hashes_ex")
 
 
 def kvx_table_build(keys, vals, n: int, stream=None) -> Table:

@@ -300,6 +300,14 @@ kvx_status kvx_block_hashes(const uint32_t *tokens, const int64_t *tok_off, int3
                             int32_t block_size, uint64_t *out_hash, const int64_t *hash_off,
                             cudaStream_t stream);
 
+/* The same, continuing each session's chain: session s's first block chains to parent[s] (device
+ * array of n_sessions uint64; NULL means 0 for every session, which is kvx_block_hashes). A session's
+ * tokens then start at a block boundary of its whole stream and parent[s] is the hash of the block
+ * before them, so a turn's newly filled blocks are hashed without the blocks before them. */
+kvx_status kvx_block_hashes_ex(const uint32_t *tokens, const int64_t *tok_off, int32_t n_sessions,
+                               int32_t block_size, const uint64_t *parent, uint64_t *out_hash,
+                               const int64_t *hash_off, cudaStream_t stream);
+
 /* Device hash table of the prefill side's resident blocks: hash -> local block id. */
 typedef struct kvx_table_s *kvx_table_t;
 

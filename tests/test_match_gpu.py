@@ -57,6 +57,35 @@ def test_block_hashes_match_oracle(bs):
         assert np.array_equal(got[hash_off[s]:hash_off[s + 1]], orc.block_hashes(t, bs)), s
 
 
+def test_block_hashes_continue_from_a_parent():
+    """A turn's new blocks hashed from the hash of the block before them equal the tail of the whole
+    stream's chain: each session split at a random block boundary (empty halves included)."""
+    rng = np.random.default_rng(7)
+    bs, n = 64, 20
+    lens = rng.integers(0, 60, n) * bs + rng.integers(0, bs, n)
+    streams = [rng.integers(0, 151936, int(l)).astype(np.uint32) for l in lens]
+    orc = oracle.load()
+    full = [orc.block_hashes(t, bs) for t in streams]
+    cut = [int(rng.integers(0, len(h) + 1)) for h in full]                  # in blocks
+    head = [t[:k * bs] for t, k in zip(streams, cut)]
+    tail = [t[k * bs:] for t, k in zip(streams, cut)]
+    parent = np.array([h[k - 1] if k > 0 else 0 for h, k in zip(full, cut)], dtype=np.uint64)
+
+    def hashes(parts, par):
+        tok = np.concatenate(parts).astype(np.uint32) if parts else np.zeros(0, np.uint32)
+        off = np.concatenate([[0], np.cumsum([len(p) for p in parts])]).astype(np.int64)
+        hoff = np.concatenate([[0], np.cumsum([len(p) // bs for p in parts])]).astype(np.int64)
+        out = torch.zeros(max(int(hoff[-1]), 1), dtype=torch.int64, device="cuda")
+        kvx.kvx_block_hashes_ex(dev(tok, np.uint32), dev(off, np.int64), len(parts), bs,
+                                None if par is None else dev(par, np.uint64), out, dev(hoff, np.int64))
+        got = out.cpu().numpy().view(np.uint64)
+        return [got[hoff[i]:hoff[i + 1]] for i in range(len(parts))]
+
+    first, second = hashes(head, None), hashes(tail, parent)
+    for i in range(n):
+        assert np.array_equal(np.concatenate([first[i], second[i]]), full[i]), i
+
+
 def test_block_hashes_reject_short_output_range():
     tok_off = dev(np.array([0, 128], np.int64), np.int64)
     hash_off = dev(np.array([0, 1], np.int64), np.int64)       # 2 full blocks, room for 1
