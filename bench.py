@@ -659,6 +659,37 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
                    "clock with device sync on both sides (rank 0)"}
 
 
+def publish_turn(torch, kvx, w, hashes, d, turn_blocks):
+    """Incremental publishing: each session's last `turn_blocks` full blocks (one turn's new tokens)
+    hashed from the published hash of the block before them (kvx_block_hashes_ex), checked against
+    the tail of the from-scratch chain. Returns (median ms over 4 timed calls, blocks hashed)."""
+    bs = 64
+    n_full = np.diff(w.rem_off)
+    keep = np.minimum(n_full, turn_blocks)
+    first = n_full - keep                                     # first new block of each session
+    tok = [w.tokens[w.tok_off[s] + first[s] * bs: w.tok_off[s] + n_full[s] * bs] for s in range(w.n_sessions)]
+    tok_off = np.concatenate([[0], np.cumsum([len(t) for t in tok])]).astype(np.int64)
+    hash_off = np.concatenate([[0], np.cumsum(keep)]).astype(np.int64)
+    host_hash = hashes.cpu().numpy().view(np.uint64)
+    parent = np.array([host_hash[w.rem_off[s] + first[s] - 1] if first[s] > 0 else 0
+                       for s in range(w.n_sessions)], dtype=np.uint64)
+    want = np.concatenate([host_hash[w.rem_off[s] + first[s]: w.rem_off[s + 1]] for s in range(w.n_sessions)])
+    toks, toff, hoff, par = d(np.concatenate(tok)), d(tok_off), d(hash_off), d(parent)
+    out = torch.empty(max(int(hash_off[-1]), 1), dtype=torch.int64, device=hashes.device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for _ in range(5):
+        s.record()
+        kvx.kvx_block_hashes_ex(toks, toff, w.n_sessions, bs, par, out, hoff)
+        e.record()
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    got = out[:int(hash_off[-1])].cpu().numpy().view(np.uint64)
+    if not np.array_equal(got, want):
+        raise RuntimeError("incremental block hashes differ from the full chain's tail")
+    return statistics.median(ms[1:]), int(hash_off[-1])
+
+
 def run_match(torch, kvx, device, push_opts=None):
     """Prefix match of the bidirectional workload (256 sessions, 1024 shared + U[2k,32k] history tokens,
     block 64): decode publishes block hashes (kvx_block_hashes), prefill keeps a Bernoulli(0.4) subset
@@ -682,6 +713,7 @@ def run_match(torch, kvx, device, push_opts=None):
         e.record()
         e.synchronize()
         hash_ms.append(s.elapsed_time(e))
+    turn_ms, turn_blocks = publish_turn(torch, kvx, w, hashes, d, turn_blocks=8)
     resident = torch.from_numpy(w.resident).to(device)
     keys = torch.unique(hashes[resident])
     table = kvx.kvx_table_build(keys, torch.arange(keys.numel(), dtype=torch.int32, device=device), keys.numel())
@@ -728,6 +760,7 @@ def run_match(torch, kvx, device, push_opts=None):
         "block_compares_per_s": round(compares / (m_ms * 1e-3), 1),
         "match_ms": round(m_ms, 3), "match_and_plan_ms": round(statistics.median(plan_ms[1:]), 3),
         "hash_only_ms": round(statistics.median(hash_ms[1:]), 3),
+        "publish_turn_ms": round(turn_ms, 3), "publish_turn_blocks": turn_blocks,
         "hashed_blocks": n_pub, "pushing_sessions": int(res["push"].sum()),
         "push_blocks": int(res["missing_tokens"].sum() // 64), "runs": info["n_runs"],
         "dp_push_gbs_one_layer": round(2 * info["bytes_per_layer"] / (statistics.median(push_ms) * 1e-3) / 1e9, 1),
