@@ -284,30 +284,31 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
         args.ts_start = pl->ts + slot;
         args.ts_end = pl->ts + kTimingSlots + slot;
     }
-    e = launch_copy(args, l1 - l0, shape, stream);
-    if (e != cudaSuccess) {
-        for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
-        return cuda_fail(e, "copy kernel launch");
-    }
+    // the completion event is taken before the launch, so a launched push is always tracked
     cudaEvent_t ev;
     st = take_event(pl, &ev);
     if (st) return st;
-    e = cudaEventRecord(ev, stream);
+    e = launch_copy(args, l1 - l0, shape, stream);
     if (e != cudaSuccess) {
         pl->free_events.push_back(ev);
-        return cuda_fail(e, "cudaEventRecord(push)");
+        for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
+        return cuda_fail(e, "copy kernel launch");
     }
-    if (done) {
-        e = cudaEventRecord(done, stream);
-        if (e != cudaSuccess) {
-            pl->free_events.push_back(ev);
-            return cuda_fail(e, "cudaEventRecord(done)");
-        }
+    e = cudaEventRecord(ev, stream);
+    if (e != cudaSuccess) {
+        // launched but not trackable: the layers cannot be confirmed
+        pl->free_events.push_back(ev);
+        for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
+        return cuda_fail(e, "cudaEventRecord(push)");
     }
     pl->pending.push_back({ev, slot, l0, l1});
     for (int32_t l = l0; l < l1; ++l) {
         pl->layer_state[l] = KVX_LAYER_PENDING;
         if (pl->inject[l]) { pl->injected_pending[l] = 1; pl->inject[l] = 0; }
+    }
+    if (done) {
+        e = cudaEventRecord(done, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(done)");
     }
     return KVX_OK;
 }
