@@ -189,12 +189,15 @@ def alloc_pool(torch, geom, fill, seed, device):
     return [big[i * per:i * per + geom.buffer_bytes] for i in range(geom.n_buffers)], big
 
 
-def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, barrier=None):
+def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, barrier=None, all_layers=False,
+                       extra_opts=None):
     """Allocates the workload's pools and times K steps of the per-layer push pattern after W untimed
     ones. A step builds the requests' plan, runs the synthetic prefill (per layer a fixture kernel on
     the priority stream that records the layer's ready event) and pushes every layer gated on its
     event; each step is synced after the next one is issued. The pushes of every `every`-th timed step
-    are timed (the kernels' own global-timer stamps)."""
+    are timed (the kernels' own global-timer stamps). `all_layers`: one kvx_push_layers call per
+    step for all layers, gated on the last layer's event, instead of one kvx_push_layer per layer;
+    `extra_opts` are added to the plan options."""
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
@@ -202,6 +205,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     reqs = requests(w)
     opts = {"tile_bytes": args.tile_bytes, "threads": args.threads, "kernel": args.kernel,
             "ctas_per_sm": args.ctas_per_sm, "lanes": args.lanes, "bulk_stages": args.bulk_stages}
+    opts.update(extra_opts or {})
     # the synthetic prefill is the latency-critical path: its stream outranks the push stream, so the
     # copies fill the SMs the compute leaves free
     main = torch.cuda.Stream(priority=-1)
@@ -244,6 +248,14 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
             for layer in range(L):
                 if lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer]):
                     raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
+        elif all_layers:
+            st = 0
+            for layer in range(L):
+                st |= lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h,
+                                              ready_h[layer])
+            st |= lib.kvx_push_layers(plan.handle, 0, L, side_h, ready_h[L - 1])
+            if st:
+                raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
         else:
             for layer in range(L):
                 st = lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h,
@@ -315,7 +327,9 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
             "bytes_step": 2 * info["bytes_per_layer"] * L,                     # read + write
             "blocks_step": sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L,
             "elapsed_ms": t0.elapsed_time(t1), "launches": launches, "clocks": clk, "wall": wall,
-            "mean_push_ms": busy_us / (len(push_times) * L) * 1e-3, "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
+            "timed_steps": len(push_times), "timed_launches": len(raw_us),
+            "mean_push_ms": busy_us / len(raw_us) * 1e-3,
+            "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
             "issue_us": issue_us, "plan_us": plan_us}
 
 
@@ -425,19 +439,29 @@ def per_config(args, torch, kvx, device):
     kernel's roofline fraction (union of all push intervals on the kernels' global-timer stamps)."""
     peak, _ = measured_peak()
     out = []
-    for name, steps in (("tiny", 200), ("qwen3_32b_batched", 20), ("tp4_to_tp1_remap", 20),
-                        ("qwen3_32b_batched_hnd", 20)):
-        if name == args.workload:
+    per_layer_call = "one kvx_push_layer call per layer, gated on its layer"
+    one_call = "one kvx_push_layers call per step for all layers, after the prefill's last layer"
+    cases = (("tiny", 200, False, None, per_layer_call),
+             ("qwen3_32b_batched", 20, False, None, per_layer_call),
+             ("qwen3_32b_batched", 20, True, None, one_call + " (default: launches of about 256 MiB on the lanes)"),
+             ("qwen3_32b_batched", 20, True, {"layers_per_launch": 64}, one_call + " in a single launch"),
+             ("tp4_to_tp1_remap", 20, False, None, per_layer_call),
+             ("qwen3_32b_batched_hnd", 20, False, None, per_layer_call))
+    for name, steps, all_layers, extra, launch in cases:
+        if name == args.workload and not all_layers:
             continue
-        m = time_push_workload(args, torch, kvx, kvx_inputs.PUSH_WORKLOADS[name](), device, steps, 3, 1)
-        achieved = 2 * m["info"]["bytes_per_layer"] / (m["mean_push_ms"] * 1e-3) / 1e9
-        out.append({"workload": name, "steps": steps,
+        m = time_push_workload(args, torch, kvx, kvx_inputs.PUSH_WORKLOADS[name](), device, steps, 3, 1,
+                               all_layers=all_layers, extra_opts=extra)
+        bytes_launch = 2 * m["info"]["bytes_per_layer"] * m["L"] * m["timed_steps"] // m["timed_launches"]
+        achieved = bytes_launch / (m["mean_push_ms"] * 1e-3) / 1e9
+        out.append({"workload": name, "steps": steps, "launch": launch,
+                    "launches_per_step": m["timed_launches"] // m["timed_steps"],
                     "value": round(m["bytes_step"] * steps / (m["elapsed_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "blocks_per_s": round(m["blocks_step"] * steps / (m["elapsed_ms"] * 1e-3), 1),
                     "roofline_frac": round(achieved / peak, 4), "mean_launch_us": round(m["mean_push_ms"] * 1e3, 3),
                     "kernel": KERNEL_NAMES[m["info"]["kernel"]], "threads": m["info"]["threads"],
-                    "bytes_per_launch": 2 * m["info"]["bytes_per_layer"],
-                    "traffic": ncu_traffic(name)})
+                    "bytes_per_launch": bytes_launch,
+                    "traffic": None if all_layers else ncu_traffic(name)})
         del m
         gc.collect()
         torch.cuda.empty_cache()

@@ -68,6 +68,9 @@ struct PendingPush {
 // Timing plans: pushes between two syncs that can carry global-timer stamps.
 constexpr int32_t kTimingSlots = 4096;
 
+// Bytes moved (read + write) one launch of a multi-layer push aims at when it is split over lanes.
+constexpr int64_t kLaunchTargetBytes = (int64_t)256 << 20;
+
 // Head-shard pair: the contiguous head range one producer shard shares with one consumer shard, as
 // byte offsets inside a producer row and a consumer row.
 struct Pair { int32_t s, d; int64_t src_seg_off, dst_seg_off; };
@@ -132,6 +135,7 @@ struct kvx_plan_s {
     int32_t lanes = 4;                         // internal streams pushes fan out over
     int32_t bulk_stages_req = 0;               // ring stages asked for (0: by plan kind)
     int32_t bulk_stages = 4;                   // ring stages of the bulk kernel, resolved
+    int32_t layers_per_launch_req = 0;         // kvx_push_layers: layers per launch asked for (0: by size)
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
     cudaStream_t lane_src = nullptr;           // caller stream the cached lanes below were chosen for

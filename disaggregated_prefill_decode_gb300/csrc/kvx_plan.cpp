@@ -265,7 +265,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     st = check_overlap(pl->src_base, s.buf_bytes(), pl->dst_base, d.buf_bytes());
     if (st) return st;
     if (opts) {
-        if (opts->reserved) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+        if (opts->layers_per_launch < 0) return fail(KVX_EINVAL, "layers_per_launch must be >= 0");
         if (!valid_stages(opts->bulk_stages)) return fail(KVX_EINVAL, "bulk_stages must be 0, 2, 3, 4, 6 or 8");
         if (opts->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
         if (opts->tile_bytes) pl->tile_bytes = opts->tile_bytes;
@@ -279,6 +279,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         if (opts->ctas_per_sm) pl->ctas_per_sm = opts->ctas_per_sm;
         if (opts->lanes) pl->lanes = opts->lanes;
         pl->bulk_stages_req = opts->bulk_stages;
+        pl->layers_per_launch_req = opts->layers_per_launch;
     }
     if (pl->tile_bytes < 16 || pl->tile_bytes % 16 || pl->tile_bytes > (1 << 26))
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
@@ -439,7 +440,7 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     if (!pl || !o) return fail(KVX_EINVAL, "NULL argument");
     if (!pl->pending.empty()) return fail(KVX_EINVAL, "pushes are pending; kvx_sync first");
     if (o->tile_bytes && o->tile_bytes != pl->tile_bytes) return fail(KVX_EINVAL, "tile_bytes is fixed once tiles exist");
-    if (o->reserved) return fail(KVX_EINVAL, "kvx_plan_opts.reserved must be 0");
+    if (o->layers_per_launch < 0) return fail(KVX_EINVAL, "layers_per_launch must be >= 0");
     if (!valid_stages(o->bulk_stages)) return fail(KVX_EINVAL, "bulk_stages must be 0, 2, 3, 4, 6 or 8");
     if (o->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
     if (o->kernel < 0 || o->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", o->kernel);
@@ -453,6 +454,7 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     pl->ctas_per_sm = o->ctas_per_sm;
     pl->lanes = o->lanes ? o->lanes : 4;
     pl->bulk_stages_req = o->bulk_stages;
+    pl->layers_per_launch_req = o->layers_per_launch;
     resolve_stages(pl);
     pl->next_lane = 0;
     pl->lane_cache.clear();

@@ -229,54 +229,35 @@ static kvx_status take_event(kvx_plan_s *pl, cudaEvent_t *ev) {
     return event_take(ev);
 }
 
-extern "C" {
+// Layers one launch of a push over `n` layers covers: the plan's request, else with lanes a count
+// that moves about kLaunchTargetBytes per launch (long single launches of many layers ran slower on
+// GB300 than launches of a few hundred MiB overlapping on the lanes), else all of them.
+static int32_t layers_per_launch(const kvx_plan_s *pl, int32_t n) {
+    if (pl->layers_per_launch_req > 0) return std::min(n, pl->layers_per_launch_req);
+    if (pl->lanes <= 1) return n;
+    const int64_t per_layer = std::max<int64_t>(1, 2 * pl->bytes_per_layer);
+    return (int32_t)std::min<int64_t>(n, std::max<int64_t>(1, kLaunchTargetBytes / per_layer));
+}
 
-kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t ready,
-                                 cudaEvent_t done) {
-    if (!pl) return fail(KVX_EINVAL, "NULL plan");
-    if (l0 < 0 || l1 > pl->src.n_layers || l0 >= l1)
-        return fail(KVX_EINVAL, "layer range [%d, %d) outside [0, %d)", l0, l1, pl->src.n_layers);
-    kvx_status st = ensure_device(pl, stream);
-    if (st) return st;
-    cudaError_t e;
-    // timing plans: the push's global-timer slot (stamps live in a buffer set up on the caller's
-    // stream before the fork, so every lane sees it initialised)
-    int32_t slot = -1;
-    if (pl->flags & KVX_PLAN_TIMING) {
-        st = ensure_timing_slots(pl, stream);
+// Lanes at `stream`'s priority, looked up once per caller stream.
+static kvx_status lanes_for(kvx_plan_s *pl, cudaStream_t stream) {
+    if (pl->lane_src == stream && (int32_t)pl->lane_cache.size() == pl->lanes) return KVX_OK;
+    int prio = 0;
+    cudaError_t e = cudaStreamGetPriority(stream, &prio);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetPriority");
+    pl->lane_cache.assign(pl->lanes, nullptr);
+    for (int32_t i = 0; i < pl->lanes; ++i) {
+        kvx_status st = lane_stream(i, prio, &pl->lane_cache[i]);
         if (st) return st;
-        if ((int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
     }
-    if (pl->lanes > 1) {
-        // fork: the lane waits for everything already on the caller's stream (the upload included)
-        if (!pl->fork_evt) {
-            st = event_take(&pl->fork_evt);
-            if (st) return st;
-        }
-        e = cudaEventRecord(pl->fork_evt, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
-        if (pl->lane_src != stream || (int32_t)pl->lane_cache.size() != pl->lanes) {
-            // first push from this stream: look up its priority and the lanes that match it once
-            int prio = 0;
-            e = cudaStreamGetPriority(stream, &prio);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetPriority");
-            pl->lane_cache.assign(pl->lanes, nullptr);
-            for (int32_t i = 0; i < pl->lanes; ++i) {
-                st = lane_stream(i, prio, &pl->lane_cache[i]);
-                if (st) return st;
-            }
-            pl->lane_src = stream;
-        }
-        cudaStream_t lane = pl->lane_cache[pl->next_lane];
-        pl->next_lane = (pl->next_lane + 1) % pl->lanes;
-        e = cudaStreamWaitEvent(lane, pl->fork_evt, 0);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fork)");
-        stream = lane;
-    }
-    if (ready) {
-        e = cudaStreamWaitEvent(stream, ready, 0);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(ready)");
-    }
+    pl->lane_src = stream;
+    return KVX_OK;
+}
+
+// One copy launch for layers [l0, l1) on `stream`, tracked as a pending push.
+static kvx_status launch_tracked(kvx_plan_s *pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t *ev_out) {
+    int32_t slot = -1;
+    if ((pl->flags & KVX_PLAN_TIMING) && (int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
     const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
                             pl->bulk_stages};
     CopyArgs args = plan_copy_args(pl, l0);
@@ -286,9 +267,9 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
     }
     // the completion event is taken before the launch, so a launched push is always tracked
     cudaEvent_t ev;
-    st = take_event(pl, &ev);
+    kvx_status st = take_event(pl, &ev);
     if (st) return st;
-    e = launch_copy(args, l1 - l0, shape, stream);
+    cudaError_t e = launch_copy(args, l1 - l0, shape, stream);
     if (e != cudaSuccess) {
         pl->free_events.push_back(ev);
         for (int32_t l = l0; l < l1; ++l) pl->layer_state[l] = KVX_LAYER_FAILED;
@@ -306,8 +287,72 @@ kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStre
         pl->layer_state[l] = KVX_LAYER_PENDING;
         if (pl->inject[l]) { pl->injected_pending[l] = 1; pl->inject[l] = 0; }
     }
+    *ev_out = ev;
+    return KVX_OK;
+}
+
+extern "C" {
+
+kvx_status kvx_push_layer_notify(kvx_plan_t pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t ready,
+                                 cudaEvent_t done) {
+    if (!pl) return fail(KVX_EINVAL, "NULL plan");
+    if (l0 < 0 || l1 > pl->src.n_layers || l0 >= l1)
+        return fail(KVX_EINVAL, "layer range [%d, %d) outside [0, %d)", l0, l1, pl->src.n_layers);
+    kvx_status st = ensure_device(pl, stream);
+    if (st) return st;
+    cudaError_t e;
+    // timing plans: stamps live in a buffer set up on the caller's stream before the fork, so every
+    // lane sees it initialised
+    if (pl->flags & KVX_PLAN_TIMING) {
+        st = ensure_timing_slots(pl, stream);
+        if (st) return st;
+    }
+    if (pl->lanes > 1) {
+        // fork: each lane used below waits for everything already on the caller's stream (the
+        // upload included)
+        if (!pl->fork_evt) {
+            st = event_take(&pl->fork_evt);
+            if (st) return st;
+        }
+        e = cudaEventRecord(pl->fork_evt, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+        st = lanes_for(pl, stream);
+        if (st) return st;
+    }
+    const int32_t per = layers_per_launch(pl, l1 - l0);
+    cudaStream_t last = stream;
+    int32_t last_lane = -1;
+    cudaEvent_t lane_last[8] = {};   // this call's latest launch on each lane (lanes <= 8)
+    for (int32_t c0 = l0; c0 < l1; c0 += per) {
+        const int32_t c1 = std::min(l1, c0 + per);
+        cudaStream_t run = stream;
+        int32_t li = -1;
+        if (pl->lanes > 1) {
+            li = pl->next_lane;
+            run = pl->lane_cache[li];
+            pl->next_lane = (pl->next_lane + 1) % pl->lanes;
+            e = cudaStreamWaitEvent(run, pl->fork_evt, 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fork)");
+        }
+        if (ready) {
+            e = cudaStreamWaitEvent(run, ready, 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(ready)");
+        }
+        cudaEvent_t ev = nullptr;
+        st = launch_tracked(pl, c0, c1, run, &ev);
+        if (st) return st;
+        if (li >= 0) lane_last[li] = ev;
+        last = run;
+        last_lane = li;
+    }
     if (done) {
-        e = cudaEventRecord(done, stream);
+        // `done` follows every launch of the call: the last launch's stream joins the other lanes
+        for (int32_t i = 0; i < 8; ++i) {
+            if (!lane_last[i] || i == last_lane) continue;
+            e = cudaStreamWaitEvent(last, lane_last[i], 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(join)");
+        }
+        e = cudaEventRecord(done, last);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(done)");
     }
     return KVX_OK;

@@ -41,7 +41,7 @@ class kvx_request(ctypes.Structure):
 
 class kvx_plan_opts(ctypes.Structure):
     _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("flags", c_i32), ("kernel", c_i32), ("ctas_per_sm", c_i32),
-                ("lanes", c_i32), ("bulk_stages", c_i32), ("reserved", c_i32)]
+                ("lanes", c_i32), ("bulk_stages", c_i32), ("layers_per_launch", c_i32)]
 
 
 KVX_PLAN_TIMING = 1
@@ -265,14 +265,14 @@ def kvx_plan(src: Pool, dst: Pool, requests: Iterable) -> Plan:
     return kvx_plan_ex(src, dst, requests, None)
 
 
-_OPT_KEYS = ("tile_bytes", "threads", "flags", "kernel", "ctas_per_sm", "lanes", "bulk_stages")
+_OPT_KEYS = ("tile_bytes", "threads", "flags", "kernel", "ctas_per_sm", "lanes", "bulk_stages", "layers_per_launch")
 
 
 def _opts(opts: dict) -> kvx_plan_opts:
     unknown = set(opts) - set(_OPT_KEYS)
     if unknown:
         raise ValueError(f"unknown plan options {sorted(unknown)}")
-    return kvx_plan_opts(*(int(opts.get(k, 0)) for k in _OPT_KEYS), 0)
+    return kvx_plan_opts(*(int(opts.get(k, 0)) for k in _OPT_KEYS))
 
 
 def kvx_plan_ex(src: Pool, dst: Pool, requests: Iterable, opts: Optional[dict] = None) -> Plan:

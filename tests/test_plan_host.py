@@ -198,6 +198,7 @@ def test_validation_errors():
     expect(kvx.KVX_EUNSUPPORTED, lambda: kvx.kvx_plan(fake_pool(g.replace(layout=2), 1 << 40), dp, [ok]))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"tile_bytes": 24}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"threads": 48}))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"layers_per_launch": -1}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan(kvx.Pool(g, [0] * g.n_buffers), dp, [ok]))
     pl = kvx.kvx_plan(sp, dp, [ok])
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_inject_failure(pl, 2))

@@ -122,6 +122,51 @@ def test_all_layers_in_one_launch():
     run_workload(w, range(3), per_layer=False)
 
 
+@pytest.mark.parametrize("opts,launches", [({"layers_per_launch": 3}, [(0, 3), (3, 6), (6, 7)]),
+                                           ({}, [(0, 4), (4, 7)]),                 # 64 MiB a layer: 4 a launch
+                                           ({"lanes": 1}, [(0, 7)]),
+                                           ({"lanes": 1, "layers_per_launch": 2}, [(0, 2), (2, 4), (4, 6), (6, 7)])])
+def test_push_layers_split_into_launches(opts, launches):
+    """kvx_push_layers over 7 layers in launches of layers_per_launch layers (by default about
+    256 MiB moved per launch when lanes > 1): every layer lands, one timing entry per launch."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=7)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w),
+                           dict(opts, flags=kvx.KVX_PLAN_TIMING))
+    n0 = kvx.kvx_launch_count()
+    assert push_all_layers(plan, 7, per_layer=False) == kvx.KVX_OK
+    assert kvx.kvx_launch_count() - n0 == len(launches)
+    assert len(kvx.kvx_plan_push_times_ns(plan)[0]) == len(launches)
+    assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_DONE] * 7
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(7))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_push_layers_notify_follows_every_launch():
+    """The notification of a multi-layer push split over lanes is recorded after all its launches: a
+    consumer stream that waits on it reads every layer complete."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=7)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"layers_per_launch": 1})
+    side, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    done = torch.cuda.Event()
+    kvx.kvx_push_layer_notify(plan, 0, 7, side, None, done)
+    consumer.wait_event(done)
+    with torch.cuda.stream(consumer):
+        copies = [[b.clone() for b in layer_buffers(w.dst, dst, layer)] for layer in range(7)]
+    consumer.synchronize()
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    for layer in range(7):
+        for a, b in zip(copies[layer], layer_buffers(w.dst, dst, layer)):
+            assert torch.equal(a, b)
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(7))
+    kvx.kvx_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("tile_bytes,threads", [(16, 32), (4096, 128), (16384, 256), (65536, 1024), (2064, 96)])
 def test_launch_shapes(tile_bytes, threads):
     w = kvx_inputs.qwen3_32b_batched(n_layers=1, n_requests=3, len_range=(100, 900))
