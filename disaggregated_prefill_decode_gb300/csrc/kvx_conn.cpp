@@ -1,6 +1,6 @@
 // Host-side connector state machine around the push: rendezvous of the consumer's registration and
 // the producer's prefill, chunked-prefill gating, deferral with a timeout, sealed write counts per
-// producer rank, batch-state judgment of each write and load errors. No CUDA call: every call takes
+// producer rank, batch-state decision for each write and load errors. No CUDA call: every call takes
 // the caller's clock, so the protocol runs (and is tested) on any host.
 //
 // Follows the push-mode NIXL connector article (spke.com 3844), "Implementierungsdetails" steps 1-3,
@@ -343,7 +343,7 @@ kvx_status kvx_conn_write_done(kvx_conn_t k, int64_t id, int32_t attempt, int32_
     ConnRank &q = r->ranks[rank];
     if (q.done >= (q.expected >= 0 ? q.expected : q.issued))
         return fail(KVX_EINVAL, "request %lld rank %d: more writes reported than queued", (long long)id, rank);
-    // the write's state is judged over all its layers, not the last one reported
+    // the write's state is decided over all its layers, not the last one reported
     bool failed = false;
     for (int32_t l = 0; l < n_layers; ++l) {
         const int32_t s = layer_states[l];

@@ -43,7 +43,7 @@ typedef enum kvx_status {
     KVX_EFAILED = 8        /* a completed push reported FAILED for at least one layer             */
 } kvx_status;
 
-/* Per-layer state of a plan's pushes, [P2] section 6 ("failure handling": the batch state is judged
+/* Per-layer state of a plan's pushes, [P2] section 6 ("failure handling": the batch state is decided
  * over all layers' states DONE / FAILED / PENDING, because a middle layer can fail). */
 typedef enum kvx_layer_state {
     KVX_LAYER_IDLE = 0,     /* not pushed since the plan was built */
@@ -432,7 +432,7 @@ kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int64_t *tok_of
  *        collects blocks until the last chunk; wait_for_save seals the number of writes actually
  *        queued), section 3.1 (failed loads are reported so those blocks are recomputed), section
  *        5 (transfer_timeout, defer_timeout, recv_abort_timeout) and section 6 (the batch state is
- *        judged over every layer's DONE / FAILED / PENDING; with consumer TP above producer TP,
+ *        decided over every layer's DONE / FAILED / PENDING; with consumer TP above producer TP,
  *        consumer_tp / producer_tp acknowledgements complete a request).
  *
  * States of a record (the attempt it belongs to is part of every event):

@@ -248,7 +248,7 @@ def test_every_rank_must_seal_and_report():
     kvx.kvx_conn_destroy(c)
 
 
-def test_batch_state_is_judged_over_all_layers(conn):
+def test_batch_state_is_decided_over_all_layers(conn):
     kvx.kvx_conn_register(conn, 15, 0, [50, 51, 52, 53], now_us=0)
     kvx.kvx_conn_prefill(conn, 15, 0, [0, 1, 2, 3], 64, True, now_us=0)
     kvx.kvx_conn_start(conn, 15, 0, now_us=0)
