@@ -144,10 +144,13 @@ struct kvx_plan_s {
     int64_t bytes_per_layer = 0;
     std::vector<kvx::TileDesc> tiles;          // host-built plans; empty for device-built plans
 
-    // device copy: [tiles][src_base][dst_base][err]
+    // device copy: [tiles][src_base][dst_base][err][runs: device-built plans only]
     void *dev = nullptr;
     size_t dev_bytes = 0;
-    size_t off_tiles = 0, off_src = 0, off_dst = 0, off_err = 0;
+    size_t off_tiles = 0, off_src = 0, off_dst = 0, off_err = 0, off_runs = 0;
+    int64_t run_cap = 0;                       // device-built plans: run slots (src rows, dst rows, tokens)
+    int64_t n_runs_dev = -1;                   // device-built plans: runs held on the device until asked for
+    int64_t device_tokens = 0;                 // device-built plans: tokens copied per (layer, plane, shard)
     std::vector<uint8_t> upload_img;           // host image of the uploaded descriptor bytes
     bool uploaded = false;
     bool device_built = false;                 // descriptors were written on the device

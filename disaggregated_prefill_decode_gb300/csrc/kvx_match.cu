@@ -874,7 +874,6 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     const size_t o_ps = take(8 * B), o_pd = take(8 * B), o_flag = take(8 * B), o_ridx = take(8 * B);
     const size_t o_rstart = take(8 * B), o_tcount = take(8 * B), o_tstart = take(8 * B);
     const size_t o_part = take(8 * n_part), o_scal = take(8 * 8), o_err = take(sizeof(int32_t) * 4);
-    const size_t o_rows = take(sizeof(int32_t) * 3 * B);
     // hole filling: residency per published block, pull flags, their scan, each pair's session
     const size_t o_res = fill ? take(B) : 0, o_need = fill ? take(8 * B) : 0, o_npos = fill ? take(8 * B) : 0;
     const size_t o_psess = fill ? take(8 * B) : 0;
@@ -895,7 +894,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     m.partial = reinterpret_cast<int64_t *>(sb + o_part);
     m.scalars = reinterpret_cast<int64_t *>(sb + o_scal);
     m.err = reinterpret_cast<int32_t *>(sb + o_err);
-    int32_t *rows = reinterpret_cast<int32_t *>(sb + o_rows);
+    int32_t *rows = nullptr;   // the plan's run slots (src rows, dst rows, tokens), in its device block
     int64_t *need = fill ? reinterpret_cast<int64_t *>(sb + o_need) : nullptr;
     int64_t *npos = fill ? reinterpret_cast<int64_t *>(sb + o_npos) : nullptr;
     int64_t *pair_sess = fill ? reinterpret_cast<int64_t *>(sb + o_psess) : nullptr;
@@ -955,6 +954,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                            : ((int64_t)block_size * sh.src_row_bytes + pl->tile_bytes - 1) / pl->tile_bytes) * sh.n_pairs;
         const int64_t tile_cap = B * per_block;
         pl->n_tiles = tile_cap;   // sizes the layout; the real count comes back below
+        pl->run_cap = B;
         plan_layout(pl);
         st = pool_alloc(&pl->dev, pl->dev_bytes, stream);
         if (st) return cleanup(st);
@@ -967,6 +967,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                            stream));
         ok(cudaMemsetAsync(dev + pl->off_err, 0, sizeof(int32_t) * (size_t)pl->src.n_layers, stream));
         TileDesc *tiles = reinterpret_cast<TileDesc *>(dev + pl->off_tiles);
+        rows = reinterpret_cast<int32_t *>(dev + pl->off_runs);
 
         count_launch(4);
         if (!fill) {
@@ -998,7 +999,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                                                              rows + 2 * B, m.err);
         ok(cudaGetLastError());
     }
-    int64_t h_scal[3] = {0, 0, 0};
+    int64_t h_scal[5] = {0, 0, 0, 0, 0};
     int32_t h_err = 0;
     ok(cudaMemcpyAsync(h_scal, m.scalars, sizeof(h_scal), cudaMemcpyDeviceToHost, stream));
     ok(cudaMemcpyAsync(&h_err, m.err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
@@ -1009,18 +1010,11 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         return cleanup(fail(KVX_ENOMEM, "pushing sessions need %lld blocks, free list has %lld", (long long)h_scal[0],
                             (long long)n_free));
     if (pl) {
-        const int64_t n_runs = h_scal[1];
+        // the runs stay on the device (kvx_plan_runs reads them when asked); every pulled block is
+        // a whole block, so the tokens per layer are the pulled blocks times the block size
+        pl->n_runs_dev = h_scal[1];
         pl->n_tiles = h_scal[2];
-        pl->run_src_row.resize((size_t)n_runs);
-        pl->run_dst_row.resize((size_t)n_runs);
-        pl->run_ntok.resize((size_t)n_runs);
-        if (n_runs > 0) {
-            ok(cudaMemcpyAsync(pl->run_src_row.data(), rows, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
-            ok(cudaMemcpyAsync(pl->run_dst_row.data(), rows + B, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
-            ok(cudaMemcpyAsync(pl->run_ntok.data(), rows + 2 * B, sizeof(int32_t) * n_runs, cudaMemcpyDeviceToHost, stream));
-            ok(cudaStreamSynchronize(stream));
-            if (e != cudaSuccess) return cleanup(cuda_fail(e, "reading plan runs"));
-        }
+        pl->device_tokens = h_scal[4] * block_size;
         finish_plan_shape(pl);
         st = event_take(&pl->upload_evt);
         if (st) return cleanup(st);

@@ -340,7 +340,7 @@ static void resolve_stages(kvx_plan_s *pl) {
 
 void finish_plan_shape(kvx_plan_s *pl) {
     pl->vec = vector_bytes(pl, shard_pairs(pl->src, pl->dst));
-    int64_t toks = 0;
+    int64_t toks = pl->device_built ? pl->device_tokens : 0;
     for (int32_t n : pl->run_ntok) toks += n;
     pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
     resolve_stages(pl);
@@ -467,6 +467,20 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
 kvx_status kvx_plan_runs(kvx_plan_t pl, int64_t *n_runs, const int32_t **src_row, const int32_t **dst_row,
                          const int32_t **n_tokens) {
     if (!pl || !n_runs) return fail(KVX_EINVAL, "NULL argument");
+    if (pl->n_runs_dev > 0 && pl->run_ntok.empty()) {
+        // a device-built plan's runs stay on the device until asked for (the kernels that wrote
+        // them finished before kvx_match_prefix returned)
+        const size_t n = (size_t)pl->n_runs_dev;
+        std::vector<int32_t> s(n), d(n), t(n);
+        const int32_t *rows = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(pl->dev) + pl->off_runs);
+        cudaError_t e = cudaMemcpy(s.data(), rows, sizeof(int32_t) * n, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(d.data(), rows + pl->run_cap, sizeof(int32_t) * n, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(t.data(), rows + 2 * pl->run_cap, sizeof(int32_t) * n, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "reading plan runs");
+        pl->run_src_row.swap(s);
+        pl->run_dst_row.swap(d);
+        pl->run_ntok.swap(t);
+    }
     *n_runs = (int64_t)pl->run_ntok.size();
     if (src_row) *src_row = pl->run_src_row.data();
     if (dst_row) *dst_row = pl->run_dst_row.data();
@@ -476,7 +490,7 @@ kvx_status kvx_plan_runs(kvx_plan_t pl, int64_t *n_runs, const int32_t **src_row
 
 kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     if (!pl || !out) return fail(KVX_EINVAL, "NULL argument");
-    out->n_runs = (int64_t)pl->run_ntok.size();
+    out->n_runs = pl->n_runs_dev >= 0 ? pl->n_runs_dev : (int64_t)pl->run_ntok.size();
     out->n_tiles = pl->n_tiles;
     out->bytes_per_layer = pl->bytes_per_layer;
     out->vec_bytes = pl->vec;

@@ -138,7 +138,8 @@ void plan_layout(kvx_plan_s *pl) {
     pl->off_src = align_up(sizeof(TileDesc) * (size_t)pl->n_tiles, a);
     pl->off_dst = pl->off_src + align_up(sizeof(void *) * pl->src_base.size(), a);
     pl->off_err = pl->off_dst + align_up(sizeof(void *) * pl->dst_base.size(), a);
-    pl->dev_bytes = pl->off_err + align_up(sizeof(int32_t) * (size_t)pl->src.n_layers, a);
+    pl->off_runs = pl->off_err + align_up(sizeof(int32_t) * (size_t)pl->src.n_layers, a);
+    pl->dev_bytes = pl->off_runs + align_up(sizeof(int32_t) * 3 * (size_t)pl->run_cap, a);
 }
 
 CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {

@@ -179,7 +179,9 @@ kvx_status kvx_plan_ex(const kvx_pool *src, const kvx_pool *dst, const kvx_reque
 kvx_status kvx_plan_set_opts(kvx_plan_t plan, const kvx_plan_opts *opts);
 
 /* Introspection for tests: the plan's merged token runs (host arrays owned by the plan, valid
- * until kvx_plan_destroy). Rows are block * block_size + slot on each side. */
+ * until kvx_plan_destroy). Rows are block * block_size + slot on each side. A plan built by
+ * kvx_match_prefix keeps its runs on the device (no push needs them on the host); the first call
+ * here copies them back with a synchronous copy. */
 kvx_status kvx_plan_runs(kvx_plan_t plan, int64_t *n_runs, const int32_t **src_row,
                          const int32_t **dst_row, const int32_t **n_tokens);
 

@@ -384,6 +384,33 @@ def test_threshold_edges(l_rem, want_push):
     kvx.kvx_table_destroy(table)
 
 
+def test_match_plan_with_nothing_to_push():
+    """No session reaches the threshold, and a call with no sessions at all: each still returns a
+    plan, with no runs; pushing it is a no-op that syncs DONE and leaves the prefill pool as it was."""
+    w = kvx_inputs.bidir_mla_fp8(seed=26, n_sessions=6, n_layers=2, system_tokens=128, hist_range=(64, 900),
+                                 resident_p=0.5, threshold=1 << 30)
+    c = Case(w)
+    want = c.oracle_match()
+    assert want["push"].sum() == 0
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=2)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    before = [b.clone() for b in dst]
+    for n_sessions in (w.n_sessions, 0):
+        w.n_sessions = n_sessions
+        st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+        assert st == kvx.KVX_OK and plan is not None
+        if n_sessions:
+            assert_decisions(got, want)
+        assert kvx.kvx_plan_get_info(plan)["n_runs"] == 0
+        for layer in range(2):
+            kvx.kvx_push_layer(plan, layer, torch.cuda.current_stream())
+        assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+        assert kvx.kvx_plan_layer_states(plan).tolist() == [kvx.KVX_LAYER_DONE] * 2
+        kvx.kvx_plan_destroy(plan)
+    assert all(torch.equal(a, b) for a, b in zip(before, dst))
+    c.close()
+
+
 def test_free_list_too_short_is_enomem():
     w = kvx_inputs.bidir_mla_fp8(seed=23, n_sessions=8, n_layers=1, system_tokens=128, hist_range=(600, 1500),
                                  resident_p=0.3, threshold=64)
