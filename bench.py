@@ -103,9 +103,9 @@ def ncu_traffic(kernel_key):
 
 
 def csrc_sha():
-    """Hash of the copy kernels and the tile builder (the ncu counters are valid only for these)."""
+    """Hash of the copy kernels and the copy-shape builder (the ncu counters are valid only for these)."""
     h = hashlib.sha256()
-    for name in ("kvx_copy.cu", "kvx_plan.cpp"):
+    for name in ("kvx_copy.cu", "kvx_tiles.cpp"):
         with open(os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

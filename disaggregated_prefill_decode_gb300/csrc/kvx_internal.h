@@ -169,9 +169,14 @@ struct kvx_plan_s {
 };
 
 namespace kvx {
-// Shared by host-built and device-built plans (kvx_plan.cpp).
+// Shared by host-built and device-built plans: validation (kvx_plan.cpp) and the copy shape
+// (kvx_tiles.cpp).
 kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl);
+void init_copy_shape(kvx_plan_s *pl, bool tile_bytes_given);
+void request_runs(int64_t n_tok, int32_t bs_s, const int32_t *sids, int32_t bs_d, const int32_t *dids, kvx_plan_s *pl);
+void build_tiles(kvx_plan_s *pl);
 void finish_plan_shape(kvx_plan_s *pl);
+void resolve_launch(kvx_plan_s *pl);        // kernel, threads and ring stages from the plan's options
 bool as_whole_block_copy(kvx_plan_s *pl);
 // Device layout and kernel arguments of a plan (kvx_push.cu).
 void plan_layout(kvx_plan_s *pl);

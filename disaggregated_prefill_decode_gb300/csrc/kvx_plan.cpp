@@ -1,4 +1,5 @@
-// Host side of kvx: error reporting, plan validation, run merging and tiling. No device work.
+// Host side of kvx: error reporting, plan validation and the plan API. The runs, tiles and launch
+// shape a plan gets are built in kvx_tiles.cpp. No device work.
 //
 // Follows the push-mode NIXL connector article (spke.com 3844), section "Threading-Modell" (block ids
 // are mapped to memory descriptors and contiguous blocks merged into larger regions) and
@@ -87,165 +88,7 @@ static kvx_status check_overlap(const std::vector<void *> &src, int64_t src_byte
     return KVX_OK;
 }
 
-// Appends the maximal token runs of one request. Walks the segments between consecutive block
-// boundaries of either side (rows inside a segment advance together), and extends the previous run
-// when both sides continue it.
-static void request_runs(int64_t n_tok, int32_t bs_s, const int32_t *sids, int32_t bs_d, const int32_t *dids,
-                         kvx_plan_s *pl) {
-    const size_t first = pl->run_ntok.size();
-    int64_t t = 0;
-    while (t < n_tok) {
-        const int64_t is = t / bs_s, id = t / bs_d;
-        const int64_t end = std::min({(is + 1) * bs_s, (id + 1) * bs_d, n_tok});
-        const int64_t srow = (int64_t)sids[is] * bs_s + (t - is * bs_s);
-        const int64_t drow = (int64_t)dids[id] * bs_d + (t - id * bs_d);
-        const int32_t len = (int32_t)(end - t);
-        const size_t k = pl->run_ntok.size();
-        if (k > first && (int64_t)pl->run_src_row[k - 1] + pl->run_ntok[k - 1] == srow &&
-            (int64_t)pl->run_dst_row[k - 1] + pl->run_ntok[k - 1] == drow) {
-            pl->run_ntok[k - 1] += len;
-        } else {
-            pl->run_src_row.push_back((int32_t)srow);
-            pl->run_dst_row.push_back((int32_t)drow);
-            pl->run_ntok.push_back(len);
-        }
-        t = end;
-    }
-}
 
-// Head-shard pairs: the contiguous head ranges that one producer shard and one consumer shard share.
-std::vector<Pair> shard_pairs(const Geom &s, const Geom &d) {
-    std::vector<Pair> out;
-    const int64_t hb = s.head_bytes();
-    if (s.heads_per_shard == d.heads_per_shard) {
-        for (int32_t i = 0; i < s.n_shards; ++i) out.push_back({i, i, 0, 0});
-    } else if (s.heads_per_shard < d.heads_per_shard) {   // merge: several producer shards per consumer shard
-        for (int32_t i = 0; i < s.n_shards; ++i) {
-            const int32_t g0 = i * s.heads_per_shard;
-            const int32_t ds = g0 / d.heads_per_shard;
-            out.push_back({i, ds, 0, (int64_t)(g0 - ds * d.heads_per_shard) * hb});
-        }
-    } else {                                              // split: several consumer shards per producer shard
-        for (int32_t j = 0; j < d.n_shards; ++j) {
-            const int32_t g0 = j * d.heads_per_shard;
-            const int32_t ss = g0 / s.heads_per_shard;
-            out.push_back({ss, j, (int64_t)(g0 - ss * s.heads_per_shard) * hb, 0});
-        }
-    }
-    return out;
-}
-
-static int64_t gcd64(int64_t a, int64_t b) { return std::gcd(a < 0 ? -a : a, b < 0 ? -b : b); }
-
-// The widest vector (<= 16 bytes) dividing every address, offset and length the copy uses.
-static int32_t vector_bytes(const kvx_plan_s *pl, const std::vector<Pair> &pairs) {
-    int64_t g = 16;
-    for (void *p : pl->src_base) g = gcd64(g, (int64_t)((uintptr_t)p & 15));
-    for (void *p : pl->dst_base) g = gcd64(g, (int64_t)((uintptr_t)p & 15));
-    g = gcd64(g, pl->src.row_bytes());
-    g = gcd64(g, pl->dst.row_bytes());
-    if (pl->per_head) {
-        g = gcd64(g, pl->src.head_bytes());   // offsets, pitches and widths are multiples of it
-    } else if (pl->strided) {
-        g = gcd64(g, pl->width);
-        for (const Pair &q : pairs) g = gcd64(gcd64(g, q.src_seg_off), q.dst_seg_off);
-    } else {
-        g = gcd64(g, pl->tile_bytes);
-    }
-    return (int32_t)g;   // gcd with 16: one of 16, 8, 4, 2, 1
-}
-
-// Tiles of plans with an HND side: each run is cut at every block boundary of either side, and each
-// such segment is copied head by head (a head's tokens are rows at each side's token pitch). When
-// both sides are HND with the same block size and heads per shard, a stretch of whole blocks is one
-// contiguous span per shard on both sides and is copied as such.
-static void build_head_tiles(kvx_plan_s *pl) {
-    const Geom &s = pl->src, &d = pl->dst;
-    const int64_t hb = s.head_bytes();
-    const int64_t rows_per_tile = std::max<int64_t>(1, pl->tile_bytes / hb);
-    const int32_t heads = s.n_shards * s.heads_per_shard;
-    const bool same_hnd = s.layout == KVX_LAYOUT_HND && d.layout == KVX_LAYOUT_HND && s.block_size == d.block_size &&
-                          s.heads_per_shard == d.heads_per_shard;
-    auto emit = [&](int64_t soff, int64_t doff, int64_t rows, int32_t ss, int32_t ds) {
-        for (int64_t r0 = 0; r0 < rows; r0 += rows_per_tile)
-            pl->tiles.push_back({soff + r0 * pl->src_pitch, doff + r0 * pl->dst_pitch,
-                                 (int32_t)std::min(rows_per_tile, rows - r0), ss, ds, 0});
-    };
-    for (size_t r = 0; r < pl->run_ntok.size(); ++r) {
-        int64_t t = 0;
-        const int64_t n = pl->run_ntok[r];
-        while (t < n) {
-            const int64_t srow = (int64_t)pl->run_src_row[r] + t, drow = (int64_t)pl->run_dst_row[r] + t;
-            const int64_t sblk = srow / s.block_size, sslot = srow % s.block_size;
-            const int64_t dblk = drow / d.block_size, dslot = drow % d.block_size;
-            if (same_hnd && sslot == 0 && dslot == 0 && n - t >= s.block_size) {
-                const int64_t nblk = (n - t) / s.block_size;        // whole blocks, contiguous on both sides
-                for (int32_t sh = 0; sh < s.n_shards; ++sh)
-                    emit(s.head_index(sblk, 0, 0) * hb, d.head_index(dblk, 0, 0) * hb,
-                         nblk * s.block_size * s.heads_per_shard, sh, sh);
-                t += nblk * s.block_size;
-                continue;
-            }
-            const int64_t len = std::min({s.block_size - sslot, d.block_size - dslot, n - t});
-            for (int32_t g = 0; g < heads; ++g) {
-                const int32_t ss = g / s.heads_per_shard, hs = g % s.heads_per_shard;
-                const int32_t ds = g / d.heads_per_shard, hd = g % d.heads_per_shard;
-                emit(s.head_index(sblk, sslot, hs) * hb, d.head_index(dblk, dslot, hd) * hb, len, ss, ds);
-            }
-            t += len;
-        }
-    }
-    pl->n_tiles = (int64_t)pl->tiles.size();
-}
-
-static void build_tiles(kvx_plan_s *pl, const std::vector<Pair> &pairs) {
-    pl->tiles.clear();
-    if (pl->per_head) {
-        build_head_tiles(pl);
-        return;
-    }
-    const int64_t rb_s = pl->src.row_bytes(), rb_d = pl->dst.row_bytes();
-    const size_t nr = pl->run_ntok.size();
-    if (!pl->strided) {
-        for (size_t r = 0; r < nr; ++r) {
-            const int64_t bytes = (int64_t)pl->run_ntok[r] * rb_s;
-            const int64_t s0 = (int64_t)pl->run_src_row[r] * rb_s, d0 = (int64_t)pl->run_dst_row[r] * rb_d;
-            for (int64_t o = 0; o < bytes; o += pl->tile_bytes)
-                for (const Pair &q : pairs)
-                    pl->tiles.push_back({s0 + o, d0 + o, (int32_t)std::min<int64_t>(pl->tile_bytes, bytes - o),
-                                         q.s, q.d, 0});
-        }
-    } else {
-        const int64_t rpt = std::max<int64_t>(1, pl->tile_bytes / pl->width);
-        for (size_t r = 0; r < nr; ++r)
-            for (int64_t r0 = 0; r0 < pl->run_ntok[r]; r0 += rpt) {
-                const int32_t rows = (int32_t)std::min<int64_t>(rpt, pl->run_ntok[r] - r0);
-                for (const Pair &q : pairs)
-                    pl->tiles.push_back({((int64_t)pl->run_src_row[r] + r0) * rb_s + q.src_seg_off,
-                                         ((int64_t)pl->run_dst_row[r] + r0) * rb_d + q.dst_seg_off, rows, q.s, q.d, 0});
-            }
-    }
-    pl->n_tiles = (int64_t)pl->tiles.size();
-}
-
-// Default tile of a contiguous plan. Runs are cut at the block boundaries of both sides, so the usual
-// run is a whole number of "units" of min(block sizes) token rows. A unit above 16 KiB is split into
-// the fewest equal tiles of at most 16 KiB (a 36,864-byte MLA block: 3 x 12 KiB rather than
-// 16 + 16 + 4 KiB, whose short tail wastes a bulk-ring stage); smaller units are packed whole.
-static int32_t default_tile_bytes(const Geom &s, const Geom &d) {
-    constexpr int64_t kTarget = 16384;
-    const int64_t unit = (int64_t)std::min(s.block_size, d.block_size) * s.row_bytes();
-    int64_t t;
-    if (unit >= kTarget) {
-        const int64_t k = ceil_div(unit, kTarget);
-        t = ceil_div(unit, k);
-        t = ceil_div(t, 16) * 16;
-        if (t > kTarget) t = kTarget;
-    } else {
-        t = unit * std::max<int64_t>(1, kTarget / unit);
-    }
-    return (int32_t)std::max<int64_t>(16, t - t % 16);
-}
 
 kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl) {
     kvx_status st = read_geom(src, "producer", &pl->src, &pl->src_base);
@@ -285,66 +128,11 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         return fail(KVX_EINVAL, "tile_bytes must be a multiple of 16 in [16, 2^26]");
     if (pl->threads < 32 || pl->threads > 1024 || pl->threads % 32)
         return fail(KVX_EINVAL, "threads must be a multiple of 32 in [32, 1024]");
-    pl->per_head = (s.layout == KVX_LAYOUT_HND || d.layout == KVX_LAYOUT_HND) ? 1 : 0;
-    pl->strided = (pl->per_head || s.heads_per_shard != d.heads_per_shard) ? 1 : 0;
-    pl->width = (int32_t)(pl->per_head ? s.head_bytes() : std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
-    pl->src_pitch = pl->per_head ? s.token_pitch() : s.row_bytes();
-    pl->dst_pitch = pl->per_head ? d.token_pitch() : d.row_bytes();
-    if (!(opts && opts->tile_bytes) && !pl->strided) pl->tile_bytes = default_tile_bytes(s, d);
+    init_copy_shape(pl, opts && opts->tile_bytes);
     pl->layer_state.assign(s.n_layers, KVX_LAYER_IDLE);
     pl->inject.assign(s.n_layers, 0);
     pl->injected_pending.assign(s.n_layers, 0);
     return KVX_OK;
-}
-
-// A plan that only ever copies whole blocks between two head-major pools with the same head
-// partition and block size moves each block as one span of identical bytes: it is copied as a
-// contiguous plan. False (plan unchanged) for any other pair of layouts.
-bool as_whole_block_copy(kvx_plan_s *pl) {
-    const Geom &s = pl->src, &d = pl->dst;
-    if (s.layout != KVX_LAYOUT_HND || d.layout != KVX_LAYOUT_HND || s.n_shards != d.n_shards ||
-        s.heads_per_shard != d.heads_per_shard || s.block_size != d.block_size)
-        return false;
-    pl->per_head = 0;
-    pl->strided = 0;
-    pl->width = (int32_t)s.row_bytes();
-    pl->src_pitch = s.row_bytes();
-    pl->dst_pitch = d.row_bytes();
-    pl->tile_bytes = default_tile_bytes(s, d);
-    return true;
-}
-
-// Bulk copies need 16-byte aligned addresses, sizes, widths and pitches (vec == 16), a ring that
-// fits shared memory and, for strided plans, a row that fits a stage. The automatic choice, measured
-// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at one CTA per SM
-// (it leaves room for the caller's compute and the next push), a larger one with the persistent
-// kernel at 128 threads per CTA and the occupancy limit of CTAs (many small independent CTAs).
-constexpr int64_t kLargeLayer = (int64_t)128 << 20;
-
-static void resolve_kernel(kvx_plan_s *pl) {
-    const bool bulk_ok = pl->vec == 16 && (int64_t)pl->tile_bytes * pl->bulk_stages <= kBulkRingMax &&
-                         (!pl->strided || pl->width <= pl->tile_bytes);
-    const bool large = pl->bytes_per_layer >= kLargeLayer;
-    const bool automatic = pl->kernel == KVX_KERNEL_AUTO;
-    int32_t k = automatic ? (bulk_ok && !large ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
-    if (k == KVX_KERNEL_BULK && !bulk_ok) k = KVX_KERNEL_PERSIST;
-    pl->kernel = k;
-    pl->threads = pl->threads_req ? pl->threads_req : (automatic && large ? 128 : 256);
-}
-
-// Default ring depth: measured on GB300, strided tiles (rows scattered on one side) run fastest with
-// a 3-stage ring (four CTAs per SM fit beside each other), contiguous ones with 4.
-static void resolve_stages(kvx_plan_s *pl) {
-    pl->bulk_stages = pl->bulk_stages_req ? pl->bulk_stages_req : (pl->strided ? 3 : 4);
-}
-
-void finish_plan_shape(kvx_plan_s *pl) {
-    pl->vec = vector_bytes(pl, shard_pairs(pl->src, pl->dst));
-    int64_t toks = pl->device_built ? pl->device_tokens : 0;
-    for (int32_t n : pl->run_ntok) toks += n;
-    pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
-    resolve_stages(pl);
-    resolve_kernel(pl);
 }
 
 }  // namespace kvx
@@ -422,7 +210,7 @@ kvx_status kvx_plan_ex(const kvx_pool *src, const kvx_pool *dst, const kvx_reque
     for (int32_t r = 0; r < n_reqs; ++r)
         request_runs(reqs[r].n_tokens, s.block_size, reqs[r].src_block_ids, d.block_size, reqs[r].dst_block_ids, pl);
     finish_plan_shape(pl);
-    build_tiles(pl, shard_pairs(pl->src, pl->dst));
+    build_tiles(pl);
     if (pl->n_tiles > std::numeric_limits<int32_t>::max()) {
         delete pl;
         return fail(KVX_EUNSUPPORTED, "plan needs more than 2^31-1 tiles per layer; raise tile_bytes");
@@ -455,12 +243,11 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     pl->lanes = o->lanes ? o->lanes : 4;
     pl->bulk_stages_req = o->bulk_stages;
     pl->layers_per_launch_req = o->layers_per_launch;
-    resolve_stages(pl);
     pl->next_lane = 0;
     pl->lane_cache.clear();
     pl->lane_src = nullptr;
     pl->kernel = o->kernel;
-    resolve_kernel(pl);
+    resolve_launch(pl);
     return KVX_OK;
 }
 
