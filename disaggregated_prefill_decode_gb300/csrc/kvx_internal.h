@@ -136,6 +136,7 @@ struct kvx_plan_s {
     int32_t bulk_stages_req = 0;               // ring stages asked for (0: by plan kind)
     int32_t bulk_stages = 4;                   // ring stages of the bulk kernel, resolved
     int32_t layers_per_launch_req = 0;         // kvx_push_layers: layers per launch asked for (0: by size)
+    int32_t outside_device = -1;               // a pool buffer outside device memory (-1: not checked yet)
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
     cudaStream_t lane_src = nullptr;           // caller stream the cached lanes below were chosen for
@@ -169,6 +170,14 @@ struct kvx_plan_s {
 };
 
 namespace kvx {
+// The kernel a plan's pushes run: pools outside device memory (host memory over the chip-to-chip
+// link, managed memory) are copied with plain loads and stores, never by the bulk copy path.
+inline int32_t effective_kernel(const kvx_plan_s *pl) {
+    return pl->kernel == KVX_KERNEL_BULK && pl->outside_device == 1 ? KVX_KERNEL_PERSIST : pl->kernel;
+}
+// Checks where the pools' buffers live (first and last buffer of each side) and records it; refuses
+// pageable host memory the GPU cannot reach (kvx_push.cu).
+kvx_status check_pool_memory(kvx_plan_s *pl);
 // Shared by host-built and device-built plans: validation (kvx_plan.cpp) and the copy shape
 // (kvx_tiles.cpp).
 kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kvx_plan_opts *opts, kvx_plan_s *pl);

@@ -1016,6 +1016,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         pl->n_tiles = h_scal[2];
         pl->device_tokens = h_scal[4] * block_size;
         finish_plan_shape(pl);
+        st = check_pool_memory(pl);
+        if (st) return cleanup(st);
         st = event_take(&pl->upload_evt);
         if (st) return cleanup(st);
         e = cudaEventRecord(pl->upload_evt, stream);

@@ -286,10 +286,11 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->n_planes = pl->src.n_planes;
     out->width = pl->width;
     out->tile_bytes = pl->tile_bytes;
-    out->kernel = pl->kernel;
-    out->threads = pl->kernel == KVX_KERNEL_BULK ? 32 : pl->threads;
+    const int32_t k = effective_kernel(pl);
+    out->kernel = k;
+    out->threads = k == KVX_KERNEL_BULK ? 32 : pl->threads;
     out->lanes = pl->lanes;
-    out->bulk_stages = pl->kernel == KVX_KERNEL_BULK ? pl->bulk_stages : 0;
+    out->bulk_stages = k == KVX_KERNEL_BULK ? pl->bulk_stages : 0;
     out->src_pitch = pl->src_pitch;
     out->dst_pitch = pl->dst_pitch;
     return KVX_OK;

@@ -142,6 +142,28 @@ void plan_layout(kvx_plan_s *pl) {
     pl->dev_bytes = pl->off_runs + align_up(sizeof(int32_t) * 3 * (size_t)pl->run_cap, a);
 }
 
+kvx_status check_pool_memory(kvx_plan_s *pl) {
+    if (pl->outside_device >= 0) return KVX_OK;
+    const void *probe[4] = {pl->src_base.front(), pl->src_base.back(), pl->dst_base.front(), pl->dst_base.back()};
+    int32_t outside = 0;
+    for (const void *p : probe) {
+        cudaPointerAttributes a;
+        cudaError_t e = cudaPointerGetAttributes(&a, p);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(pool buffer)");
+        if (a.type == cudaMemoryTypeDevice) continue;
+        outside = 1;
+        if (a.type == cudaMemoryTypeUnregistered) {
+            int dev = 0, pageable = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(pageable memory access)");
+            if (!pageable) return fail(KVX_EINVAL, "a pool buffer is pageable host memory this GPU cannot access");
+        }
+    }
+    pl->outside_device = outside;
+    return KVX_OK;
+}
+
 CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     CopyArgs a;
     uint8_t *base = static_cast<uint8_t *>(pl->dev);
@@ -182,8 +204,10 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
         }
         return KVX_OK;
     }
+    kvx_status st = check_pool_memory(pl);
+    if (st) return st;
     plan_layout(pl);
-    kvx_status st = pool_alloc(&pl->dev, pl->dev_bytes, stream);
+    st = pool_alloc(&pl->dev, pl->dev_bytes, stream);
     if (st) return st;
     // one host image of the descriptor block, uploaded with a single copy; the plan keeps the image
     // until it is destroyed, so the copy never reads freed host memory
@@ -259,7 +283,7 @@ static kvx_status lanes_for(kvx_plan_s *pl, cudaStream_t stream) {
 static kvx_status launch_tracked(kvx_plan_s *pl, int32_t l0, int32_t l1, cudaStream_t stream, cudaEvent_t *ev_out) {
     int32_t slot = -1;
     if ((pl->flags & KVX_PLAN_TIMING) && (int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
-    const LaunchShape shape{pl->kernel, pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
+    const LaunchShape shape{effective_kernel(pl), pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
                             pl->bulk_stages};
     CopyArgs args = plan_copy_args(pl, l0);
     if (slot >= 0) {

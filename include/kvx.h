@@ -64,8 +64,12 @@ typedef enum kvx_layer_state {
  * of elem_bytes-byte elements. The two sides may use different layouts.
  * planes: 2 for separate K and V, 1 for a single latent (MLA). Shard s holds the global KV heads
  * [s * heads_per_shard, (s + 1) * heads_per_shard), i.e. the tensor-parallel head partition.
- * Values are moved as opaque bytes; elem_bytes only sizes them. `base` is a host array of device
- * pointers, copied by kvx_plan.
+ * Values are moved as opaque bytes; elem_bytes only sizes them. `base` is a host array of buffer
+ * pointers, copied by kvx_plan. Buffers are normally device memory; a pool may also live in pinned
+ * host memory (or pageable host memory where the GPU can reach it), which the copy kernels reach over
+ * the chip-to-chip link with plain loads and stores (the bulk copy path is kept to device memory;
+ * the first push checks the first and last buffer of each pool, and a pool's buffers are expected
+ * to be of one kind).
  */
 #define KVX_LAYOUT_NHD 0
 #define KVX_LAYOUT_HND 1

@@ -144,6 +144,28 @@ def test_push_layers_split_into_launches(opts, launches):
     kvx.kvx_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("side", ["src", "dst"])
+@pytest.mark.parametrize("kernel", ["auto", "bulk"])
+def test_pool_in_pinned_host_memory(side, kernel):
+    """One pool in pinned host memory, reached over the chip-to-chip link: the plan's pushes copy it
+    with plain loads and stores (the bulk copy path is kept to device memory, even when asked for),
+    byte for byte against the oracle."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=2)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    if side == "src":
+        src = [b.cpu().pin_memory() for b in src]
+    else:
+        dst = [b.cpu().pin_memory() for b in dst]
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w),
+                           {"kernel": KERNELS[kernel] if kernel != "auto" else 0})
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_PERSIST
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(2))
+    kvx.kvx_plan_destroy(plan)
+
+
 def test_push_layers_notify_follows_every_launch():
     """The notification of a multi-layer push split over lanes is recorded after all its launches: a
     consumer stream that waits on it reads every layer complete."""
