@@ -208,8 +208,8 @@ bool as_whole_block_copy(kvx_plan_s *pl) {
 
 // Bulk copies need 16-byte aligned addresses, sizes, widths and pitches (vec == 16), a ring that
 // fits shared memory and, for strided plans, a row that fits a stage. The automatic choice, measured
-// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at one CTA per SM
-// (it leaves room for the caller's compute and the next push), a larger one with the persistent
+// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at about one CTA
+// per SM (it leaves room for the caller's compute and the next push), a larger one with the persistent
 // kernel at 128 threads per CTA and the occupancy limit of CTAs (many small independent CTAs).
 constexpr int64_t kLargeLayer = (int64_t)128 << 20;
 
