@@ -118,11 +118,12 @@ __device__ __forceinline__ void warp_chain(const uint32_t *tok, int64_t n_full, 
 // window), coalesced. The first block chains to parent[s] (0 without a parent array).
 __global__ void __launch_bounds__(128) kvx_hash_sessions(const uint32_t *tokens, const int64_t *tok_off,
                                                          int32_t n_sessions, int32_t bs, const uint64_t *parent,
-                                                         uint64_t *out, const int64_t *hash_off, int64_t n_tok_total,
+                                                         uint64_t *out, const int64_t *hash_off,
                                                          int32_t *err) {
     const int32_t s = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= n_sessions) return;
+    const int64_t n_tok_total = tok_off[n_sessions];             // the CSR's own total bounds every read
     const int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
     const int64_t n_full = n_tok > 0 ? n_tok / bs : 0;
     if (t0 < 0 || n_tok < 0 || t0 + n_tok > n_tok_total || hash_off[s] < 0 || hash_off[s + 1] - hash_off[s] < n_full) {
@@ -253,8 +254,7 @@ constexpr int kMatchThreads = 256;
 __global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
                                                                     int32_t n_sessions, int32_t bs, TableView table,
                                                                     const uint64_t *remote_hash, const int64_t *rem_off,
-                                                                    int32_t threshold, int64_t n_tok_total, int64_t n_pub,
-                                                                    MatchFlags mf, kvx_match_result *out,
+                                                                    int32_t threshold, MatchFlags mf, kvx_match_result *out,
                                                                     int64_t *push_blocks, int32_t *err) {
     __shared__ uint64_t cand[kMatchThreads];
     __shared__ uint8_t flag[kMatchThreads];     // bit 0: equals the published hash, bit 1: resident
@@ -262,6 +262,8 @@ __global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32
     const int32_t s = (int32_t)blockIdx.x;
     if (s >= n_sessions) return;
     const int tid = (int)threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the two CSR totals bound every read of the token and published-hash arrays
+    const int64_t n_tok_total = tok_off[n_sessions], n_pub = rem_off[n_sessions];
     int64_t t0 = tok_off[s], n_tok = tok_off[s + 1] - t0;
     int64_t r0 = rem_off[s], n_rem = rem_off[s + 1] - r0;
     // malformed offsets: flag them and treat the session as empty, so no array is read out of range
@@ -450,9 +452,27 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_add(int64_t *out, int64
     if (i < n) out[i] += partial[blockIdx.x];
 }
 
+// The whole scan in one block, for n <= kScanThreads.
+__global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *in, int64_t *out, int64_t n_host,
+                                                                 const int64_t *n_dev, int64_t *sum) {
+    __shared__ int64_t ws[32];
+    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t i = threadIdx.x;
+    const int64_t v = i < n ? in[i] : 0;
+    int64_t total;
+    const int64_t inc = block_inclusive_scan(v, ws, &total);
+    if (i < n) out[i] = inc - v;
+    if (threadIdx.x == 0) *sum = total;
+}
+
 // Exclusive scan of in[0..n) into out, total into *sum. n_bound is a host upper bound on n.
 static cudaError_t exclusive_scan(const int64_t *in, int64_t *out, int64_t n_bound, const int64_t *n_dev,
                                   int64_t *partial, int64_t *sum, cudaStream_t st) {
+    if (n_bound <= kScanThreads) {
+        kvx_scan_single<<<1, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, sum);
+        count_launch(1);
+        return cudaGetLastError();
+    }
     const int64_t nb = std::max<int64_t>(1, (n_bound + kScanThreads - 1) / kScanThreads);
     kvx_scan_local<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, partial);
     kvx_scan_partials<<<1, kScanThreads, 0, st>>>(partial, nb, sum);
@@ -485,8 +505,9 @@ struct MatchScratch {
 // B bounds the scratch arrays: overlapping remote ranges (a malformed CSR) could otherwise claim more
 // pushed blocks than there are published ones.
 __global__ void kvx_assign_dst(kvx_match_result *out, const int64_t *sess_start, int32_t n_sessions,
-                               int64_t *scalars, int64_t n_free, int64_t B, int32_t *err) {
+                               int64_t *scalars, int64_t n_free, const int64_t *pub_total, int32_t *err) {
     const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t B = max(*pub_total, (int64_t)1);
     const bool fits = scalars[0] <= n_free;
     const bool sane = scalars[0] <= B;
     if (s == 0) {
@@ -714,19 +735,15 @@ kvx_status kvx_block_hashes_ex(const uint32_t *tokens, const int64_t *tok_off, i
     if (n_sessions < 0 || block_size < 1) return fail(KVX_EINVAL, "n_sessions >= 0 and block_size >= 1");
     if (n_sessions == 0) return KVX_OK;
     if (!tokens || !tok_off || !out_hash || !hash_off) return fail(KVX_EINVAL, "NULL device array");
-    int64_t n_tok_total = 0;
-    cudaError_t e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "reading tok_off");
     void *errp = nullptr;
     kvx_status st = pool_alloc(&errp, sizeof(int32_t), stream);
     if (st) return st;
     int32_t *err = static_cast<int32_t *>(errp);
-    e = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
     if (e == cudaSuccess) {
         count_launch();
         kvx_hash_sessions<<<grid_for((int64_t)n_sessions * 32, 128), 128, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
-                                                                       parent, out_hash, hash_off, n_tok_total, err);
+                                                                       parent, out_hash, hash_off, err);
         e = cudaGetLastError();
     }
     int32_t h_err = 0;
@@ -856,14 +873,17 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         return KVX_OK;
     }
 
-    // host bounds: published blocks (pushed blocks never exceed them) and tokens
-    int64_t n_pub = 0, n_tok_total = 0;
-    cudaError_t e = cudaMemcpyAsync(&n_pub, rem_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) { delete pl; return cuda_fail(e, "reading rem_off / tok_off"); }
-    if (n_pub < 0 || n_tok_total < 0) { delete pl; return fail(KVX_EINVAL, "offsets are not CSR offset arrays"); }
+    // The kernels bound their reads by the CSR totals themselves. Only a plan, or hole filling, needs
+    // the published-block count on the host, to size the per-block scratch; a decision-only call
+    // does not wait for it.
+    int64_t n_pub = 0;
+    cudaError_t e = cudaSuccess;
+    if (pl || fill) {
+        e = cudaMemcpyAsync(&n_pub, rem_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) { delete pl; return cuda_fail(e, "reading rem_off"); }
+        if (n_pub < 0) { delete pl; return fail(KVX_EINVAL, "rem_off is not a CSR offset array"); }
+    }
     const int64_t B = std::max<int64_t>(n_pub, 1);
     const int64_t n_part = std::max<int64_t>(1, (std::max<int64_t>(B, n_sessions) + kScanThreads - 1) / kScanThreads);
 
@@ -873,7 +893,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     const size_t o_push = take(sizeof(int64_t) * n_sessions), o_sess = take(sizeof(int64_t) * n_sessions);
     const size_t o_ps = take(8 * B), o_pd = take(8 * B), o_flag = take(8 * B), o_ridx = take(8 * B);
     const size_t o_rstart = take(8 * B), o_tcount = take(8 * B), o_tstart = take(8 * B);
-    const size_t o_part = take(8 * n_part), o_scal = take(8 * 8), o_err = take(sizeof(int32_t) * 4);
+    // scalars [8] and error words [4] side by side: one memset, one read-back
+    const size_t o_part = take(8 * n_part), o_scal = take(8 * 8 + sizeof(int32_t) * 4), o_err = o_scal + 8 * 8;
     // hole filling: residency per published block, pull flags, their scan, each pair's session
     const size_t o_res = fill ? take(B) : 0, o_need = fill ? take(8 * B) : 0, o_npos = fill ? take(8 * B) : 0;
     const size_t o_psess = fill ? take(8 * B) : 0;
@@ -908,18 +929,17 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     };
     auto ok = [&](cudaError_t x) { if (x != cudaSuccess && e == cudaSuccess) e = x; };
 
-    ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8, stream));
-    ok(cudaMemsetAsync(m.err, 0, sizeof(int32_t) * 4, stream));
+    ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8 + sizeof(int32_t) * 4, stream));
     count_launch();
     if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
     kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                         table->view(), remote_hash, rem_off, threshold,
-                                                                        n_tok_total, n_pub, mf, out, m.push_blocks, m.err);
+                                                                        mf, out, m.push_blocks, m.err);
     ok(cudaGetLastError());
     ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
     count_launch();
-    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free, B,
-                                                                  m.err);
+    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free,
+                                                                  rem_off + n_sessions, m.err);
     ok(cudaGetLastError());
 
     if (pl && e == cudaSuccess) {
@@ -999,11 +1019,11 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                                                              rows + 2 * B, m.err);
         ok(cudaGetLastError());
     }
-    int64_t h_scal[5] = {0, 0, 0, 0, 0};
-    int32_t h_err = 0;
-    ok(cudaMemcpyAsync(h_scal, m.scalars, sizeof(h_scal), cudaMemcpyDeviceToHost, stream));
-    ok(cudaMemcpyAsync(&h_err, m.err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
+    struct { int64_t scal[8]; int32_t err[4]; } back = {};
+    ok(cudaMemcpyAsync(&back, m.scalars, sizeof(back), cudaMemcpyDeviceToHost, stream));
     ok(cudaStreamSynchronize(stream));
+    const int64_t *h_scal = back.scal;
+    const int32_t h_err = back.err[0];
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "kvx_match_prefix"));
     if (h_err & ~8) return cleanup(fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err));
     if (h_err & 8)
@@ -1052,7 +1072,7 @@ constexpr size_t kStaticPushOff = 0;
 constexpr size_t kStaticSessOff = kStaticPushOff + sizeof(int64_t) * kStaticMaxSessions;
 constexpr size_t kStaticPartOff = kStaticSessOff + sizeof(int64_t) * kStaticMaxSessions;
 constexpr size_t kStaticScalOff = kStaticPartOff + sizeof(int64_t) * (kStaticMaxSessions / kScanThreads);
-constexpr size_t kStaticErrOff = kStaticScalOff + sizeof(int64_t) * 8;
+constexpr size_t kStaticErrOff = kStaticScalOff + sizeof(int64_t) * 8;   // right after the scalars
 constexpr size_t kStaticBytes = kStaticErrOff + sizeof(int32_t) * 4;
 
 static __device__ __align__(256) unsigned char g_match_scratch[kStaticBytes];
@@ -1100,38 +1120,29 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
     int64_t *scalars = reinterpret_cast<int64_t *>(sc + kStaticScalOff);
     int32_t *err = reinterpret_cast<int32_t *>(sc + kStaticErrOff);
 
-    // totals of the two CSR arrays bound every read the kernels make
-    int64_t n_pub = 0, n_tok_total = 0;
-    cudaError_t e = cudaMemcpyAsync(&n_pub, rem_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&n_tok_total, tok_off + n_sessions, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "reading rem_off / tok_off");
-    if (n_pub < 0 || n_tok_total < 0) return fail(KVX_EINVAL, "offsets are not CSR offset arrays");
-
-    // the array keeps the previous call's contents: the totals and error bits must start at zero
-    e = cudaMemsetAsync(scalars, 0, sizeof(int64_t) * 8, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t) * 4, stream);
+    // the kernels bound their reads by the two CSR totals themselves (no host round trip); the
+    // array keeps the previous call's contents: the totals and error bits must start at zero
+    cudaError_t e = cudaMemsetAsync(scalars, 0, sizeof(int64_t) * 8 + sizeof(int32_t) * 4, stream);
     if (e == cudaSuccess) {
         count_launch();
         kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                             table->view(), remote_hash, rem_off, threshold,
-                                                                            n_tok_total, n_pub, MatchFlags{0, nullptr, 0, nullptr},
-                                                                            out, push_blocks, err);
+                                                                            MatchFlags{0, nullptr, 0, nullptr}, out,
+                                                                            push_blocks, err);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);
     if (e == cudaSuccess) {
         count_launch();
         kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, sess_start, n_sessions, scalars, n_free,
-                                                                      n_pub, err);
+                                                                      rem_off + n_sessions, err);
         e = cudaGetLastError();
     }
-    int64_t need = 0;
-    int32_t h_err = 0;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&need, scalars, sizeof(int64_t), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_err, err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+    struct { int64_t scal[8]; int32_t err[4]; } back = {};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&back, scalars, sizeof(back), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    const int64_t need = back.scal[0];
+    const int32_t h_err = back.err[0];
     if (e != cudaSuccess) return cuda_fail(e, "kvx_match_prefix_static");
     if (h_err & ~8) return fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err);
     if (h_err & 8)

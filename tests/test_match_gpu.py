@@ -411,6 +411,38 @@ def test_match_plan_with_nothing_to_push():
     c.close()
 
 
+@pytest.mark.parametrize("entry", ["decisions", "plan", "static"])
+@pytest.mark.parametrize("bad", ["token_range_past_total", "negative_remote_total", "remote_ranges_overlap"])
+def test_match_rejects_malformed_offsets(entry, bad):
+    """CSR offsets that do not describe the arrays are refused with KVX_EINVAL: the kernels bound every
+    read by the CSR totals (read on the device), flag the session and read nothing out of range."""
+    bs, n = 4, 3
+    toks = np.arange(48, dtype=np.uint32)
+    tok_off = np.array([0, 16, 32, 48], np.int64)
+    rem_off = np.array([0, 4, 8, 12], np.int64)
+    if bad == "token_range_past_total":
+        tok_off = np.array([0, 16, 60, 48], np.int64)
+    elif bad == "negative_remote_total":
+        rem_off = np.array([0, 4, 8, -1], np.int64)
+    else:
+        rem_off = np.array([0, 8, 4, 12], np.int64)
+    remote = np.zeros(12, np.uint64)
+    table = kvx.kvx_table_build(None, None, 0)
+    out = torch.zeros(n * 24, dtype=torch.uint8, device="cuda")
+    args = (dev(toks, np.uint32), dev(tok_off, np.int64), n, bs, table, dev(remote, np.uint64))
+    with pytest.raises(kvx.KvxError) as ei:
+        if entry == "static":
+            kvx.kvx_match_prefix_static(*args, dev(rem_off, np.int64), 4, 100, out)
+        else:
+            g = PoolGeom(1, 1, 1, 1, 16, 1, bs, 64)
+            pools = [kvx.Pool(g, [torch.zeros(g.buffer_bytes, dtype=torch.uint8, device="cuda")]) for _ in range(2)]
+            kvx.kvx_match_prefix(*args, dev(np.arange(12, dtype=np.int32), np.int32), dev(rem_off, np.int64), 4,
+                                 dev(np.arange(64, dtype=np.int32), np.int32), 64, pools[0], pools[1], out,
+                                 want_plan=entry == "plan")
+    assert ei.value.status == kvx.KVX_EINVAL
+    kvx.kvx_table_destroy(table)
+
+
 def test_free_list_too_short_is_enomem():
     w = kvx_inputs.bidir_mla_fp8(seed=23, n_sessions=8, n_layers=1, system_tokens=128, hist_range=(600, 1500),
                                  resident_p=0.3, threshold=64)
