@@ -633,15 +633,20 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
     ev_h = [torch.cuda.Event() for _ in range(L)]
     ev_p = [torch.cuda.Event() for _ in range(L)]
     ev_g = [torch.cuda.Event() for _ in range(L)]
-    for ev in ev_h + ev_p + ev_g:                       # materialise the event handles
+    ev_d = [torch.cuda.Event() for _ in range(L)]
+    for ev in ev_h + ev_p + ev_g + ev_d:                # materialise the event handles
         ev.record(h2d)
     nd = stage_geom.n_planes * stage_geom.n_shards
 
-    def step():
+    def issue():
+        """One step, enqueued: per layer H2D -> push -> gather -> D2H. A layer's H2D waits for the
+        previous step's D2H of that layer (which came after its push and gather), so consecutive steps
+        pipeline layer by layer without overwriting a buffer still being read."""
         plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
         gather = kvx.kvx_plan_ex(dp, stp, stage_reqs, opts)
         for layer in range(L):
             with torch.cuda.stream(h2d):
+                h2d.wait_event(ev_d[layer])
                 for i in range(layer * P, (layer + 1) * P):
                     src[i][s_rng[0]:s_rng[1]].copy_(host_src[i], non_blocking=True)
                 ev_h[layer].record(h2d)
@@ -651,19 +656,29 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
                 d2h.wait_event(ev_g[layer])
                 for i in range(layer * nd, (layer + 1) * nd):
                     host_dst[i].copy_(stage[i], non_blocking=True)
-        st = kvx.kvx_sync(plan, -1)
-        st2 = kvx.kvx_sync(gather, -1)
-        d2h.synchronize()
-        kvx.kvx_plan_destroy(plan)
-        kvx.kvx_plan_destroy(gather)
-        assert st == kvx.KVX_OK and st2 == kvx.KVX_OK
+                ev_d[layer].record(d2h)
+        return plan, gather
 
-    for _ in range(2):
-        step()
+    def finish(plans):
+        for pl in plans:
+            assert kvx.kvx_sync(pl, -1) == kvx.KVX_OK
+            kvx.kvx_plan_destroy(pl)
+
+    def run(n):
+        """n steps, each finished (plans synced) after the next one is enqueued."""
+        prev = None
+        for _ in range(n):
+            cur = issue()
+            if prev is not None:
+                finish(prev)
+            prev = cur
+        finish(prev)
+        d2h.synchronize()
+
+    run(2)
     torch.cuda.synchronize()
     t = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        step()
+    run(args.e2e_steps)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t) / args.e2e_steps
     checked = None
@@ -679,8 +694,9 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
             "d2h_bytes_per_step": sum(h.numel() for h in host_dst),
             "ms_per_step": round(dt * 1e3, 3), "steps": args.e2e_steps, "result_checked": checked,
             "how": "pinned host producer KV -> H2D per layer -> kvx_push_layer -> kvx gather of the pushed consumer "
-                   "blocks into a dense staging pool -> D2H, 3 streams, each step synced before the next; host wall "
-                   "clock with device sync on both sides (rank 0)"}
+                   "blocks into a dense staging pool -> D2H, 3 streams; a layer's H2D waits for the previous step's "
+                   "D2H of that layer, each step's plans synced after the next step is enqueued; host wall clock "
+                   "with device sync on both sides (rank 0)"}
 
 
 def publish_turn(torch, kvx, w, hashes, d, turn_blocks):
