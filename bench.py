@@ -446,7 +446,8 @@ def per_config(args, torch, kvx, device):
              ("qwen3_32b_batched", 20, True, None, one_call + " (default: launches of about 256 MiB on the lanes)"),
              ("qwen3_32b_batched", 20, True, {"layers_per_launch": 64}, one_call + " in a single launch"),
              ("tp4_to_tp1_remap", 20, False, None, per_layer_call),
-             ("qwen3_32b_batched_hnd", 20, False, None, per_layer_call))
+             ("qwen3_32b_batched_hnd", 20, False, None, per_layer_call),
+             ("qwen3_32b_batched_nhd_to_hnd", 20, False, None, per_layer_call))
     for name, steps, all_layers, extra, launch in cases:
         if name == args.workload and not all_layers:
             continue

@@ -34,11 +34,26 @@ constexpr int kUnroll = 4;
 // tile is skipped and its layer's error word set (no trap).
 template <bool STRIDED>
 __device__ __forceinline__ bool tile_in_bounds(const TileDesc &t, const CopyArgs &a) {
-    const int64_t src_end = STRIDED ? t.src_off + (int64_t)(t.n - 1) * a.src_pitch + a.width : t.src_off + t.n;
-    const int64_t dst_end = STRIDED ? t.dst_off + (int64_t)(t.n - 1) * a.dst_pitch + a.width : t.dst_off + t.n;
-    return t.n > 0 && t.src_off >= 0 && t.dst_off >= 0 && src_end <= a.src_buf_bytes && dst_end <= a.dst_buf_bytes &&
-           t.s_shard >= 0 && t.s_shard < a.src_shards && t.d_shard >= 0 && t.d_shard < a.dst_shards;
+    const int64_t k = STRIDED ? (int64_t)max(t.heads, 1) - 1 : 0;     // heads after the first
+    const int64_t src_end =
+        STRIDED ? t.src_off + (int64_t)(t.n - 1) * a.src_pitch + k * a.src_head_pitch + a.width : t.src_off + t.n;
+    const int64_t dst_end =
+        STRIDED ? t.dst_off + (int64_t)(t.n - 1) * a.dst_pitch + k * a.dst_head_pitch + a.width : t.dst_off + t.n;
+    return t.n > 0 && t.heads >= 0 && t.src_off >= 0 && t.dst_off >= 0 && src_end <= a.src_buf_bytes &&
+           dst_end <= a.dst_buf_bytes && t.s_shard >= 0 && t.s_shard < a.src_shards && t.d_shard >= 0 &&
+           t.d_shard < a.dst_shards;
 }
+
+// Rows of a strided tile in head-major order: row r is row r % n of head r / n. A thread walks its
+// rows r0, r0 + step, ... keeping (head, row) by subtraction instead of dividing for every row.
+struct RowCursor {
+    int32_t h, t, n;
+    __device__ __forceinline__ RowCursor(int32_t r0, int32_t n_) : h(r0 / n_), t(r0 - (r0 / n_) * n_), n(n_) {}
+    __device__ __forceinline__ void advance(int32_t step) {
+        t += step;
+        while (t >= n) { t -= n; ++h; }
+    }
+};
 
 // Copies one tile with VEC-byte integer vectors, kUnroll independent loads in flight per thread
 // before their stores. Values are never converted.
@@ -60,32 +75,38 @@ __device__ __forceinline__ void copy_tile(const TileDesc &t, const uint8_t *src,
                 if (i + u * step < nv) d[i + u * step] = r[u];
         }
     } else {
-        // Rows of `width` bytes at the two pitches. Threads are laid out as (row lane, column) once,
-        // so the loop has no per-element division.
+        // Rows of `width` bytes at the two pitches, for each of the tile's heads. Threads are laid
+        // out as (row lane, column) once, so the loop has no per-element division.
         const int32_t vpr = a.width / VEC;
+        const int32_t rows = t.n * max(t.heads, 1);
         if (vpr <= (int32_t)blockDim.x) {
             const int32_t rpp = (int32_t)blockDim.x / vpr;          // rows per pass
             const int32_t my_row = (int32_t)threadIdx.x / vpr;
             const int32_t col = (int32_t)threadIdx.x - my_row * vpr;
             if (my_row < rpp) {
-                for (int32_t row = my_row; row < t.n; row += rpp * kUnroll) {
+                RowCursor c(my_row, t.n);
+                for (int32_t row = my_row; row < rows; row += rpp * kUnroll) {
                     V r[kUnroll];
+                    int64_t so[kUnroll], dof[kUnroll];
 #pragma unroll
                     for (int u = 0; u < kUnroll; ++u) {
-                        const int32_t rr = row + u * rpp;
-                        if (rr < t.n) r[u] = reinterpret_cast<const V *>(src + (int64_t)rr * a.src_pitch)[col];
+                        so[u] = (int64_t)c.h * a.src_head_pitch + (int64_t)c.t * a.src_pitch;
+                        dof[u] = (int64_t)c.h * a.dst_head_pitch + (int64_t)c.t * a.dst_pitch;
+                        c.advance(rpp);
                     }
 #pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
-                        const int32_t rr = row + u * rpp;
-                        if (rr < t.n) reinterpret_cast<V *>(dst + (int64_t)rr * a.dst_pitch)[col] = r[u];
-                    }
+                    for (int u = 0; u < kUnroll; ++u)
+                        if (row + u * rpp < rows) r[u] = reinterpret_cast<const V *>(src + so[u])[col];
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u)
+                        if (row + u * rpp < rows) reinterpret_cast<V *>(dst + dof[u])[col] = r[u];
                 }
             }
         } else {
-            for (int32_t row = 0; row < t.n; ++row) {
-                const V *s = reinterpret_cast<const V *>(src + (int64_t)row * a.src_pitch);
-                V *d = reinterpret_cast<V *>(dst + (int64_t)row * a.dst_pitch);
+            for (int32_t row = 0; row < rows; ++row) {
+                const int32_t h = row / t.n, tr = row - h * t.n;
+                const V *s = reinterpret_cast<const V *>(src + (int64_t)h * a.src_head_pitch + (int64_t)tr * a.src_pitch);
+                V *d = reinterpret_cast<V *>(dst + (int64_t)h * a.dst_head_pitch + (int64_t)tr * a.dst_pitch);
                 for (int32_t c = threadIdx.x; c < vpr; c += blockDim.x) d[c] = s[c];
             }
         }
@@ -233,7 +254,8 @@ struct BulkItem {
     const uint8_t *src;
     uint8_t *dst;
     uint32_t bytes;    // 0: skipped (out of bounds or misaligned)
-    int32_t rows;      // strided tiles: rows of a.width bytes; contiguous tiles: 1
+    int32_t n;         // strided tiles: rows of a.width bytes per head; contiguous tiles: 1
+    int32_t heads;     // strided tiles: heads (rows of head h follow those of head h - 1 in the stage)
     int32_t layer;
 };
 
@@ -246,8 +268,9 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     it.src = nullptr;
     it.dst = nullptr;
     it.bytes = 0;
-    it.rows = STRIDED ? t.n : 1;
-    const int64_t bytes = STRIDED ? (int64_t)t.n * a.width : (int64_t)t.n;
+    it.n = STRIDED ? t.n : 1;
+    it.heads = STRIDED ? max(t.heads, 1) : 1;
+    const int64_t bytes = STRIDED ? (int64_t)t.n * it.heads * a.width : (int64_t)t.n;
     if (!tile_in_bounds<STRIDED>(t, a) || bytes > stage_bytes) {
         if (t.n != 0) atomicOr(&a.err[it.layer], 1);
         return it;
@@ -255,7 +278,9 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     it.src = a.src_base[lp * a.src_shards + t.s_shard] + t.src_off;
     it.dst = a.dst_base[lp * a.dst_shards + t.d_shard] + t.dst_off;
     uintptr_t mis = ((uintptr_t)it.src) | ((uintptr_t)it.dst) | (uintptr_t)bytes;
-    if (STRIDED) mis |= (uintptr_t)a.width | (uintptr_t)a.src_pitch | (uintptr_t)a.dst_pitch;
+    if (STRIDED)
+        mis |= (uintptr_t)a.width | (uintptr_t)a.src_pitch | (uintptr_t)a.dst_pitch |
+               (it.heads > 1 ? (uintptr_t)(a.src_head_pitch | a.dst_head_pitch) : 0);
     if (mis & 15) {
         atomicOr(&a.err[it.layer], 1);
         return it;
@@ -276,9 +301,11 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
 
     const int64_t n_mine = (int64_t)blockIdx.x < n_work ? (n_work - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     BulkItem items[kBulkStages];
-    // item i of this CTA is work item blockIdx.x + i * gridDim.x, in stage i % kBulkStages
-    const bool src_packed = !STRIDED || a.src_pitch == a.width;    // one bulk copy per tile on that side
-    const bool dst_packed = !STRIDED || a.dst_pitch == a.width;
+    // item i of this CTA is work item blockIdx.x + i * gridDim.x, in stage i % kBulkStages. A side
+    // whose rows (and heads) are adjacent moves a tile in one bulk copy; the other row by row.
+    auto packed = [&](const BulkItem &it, int64_t pitch, int64_t head_pitch) {
+        return !STRIDED || (pitch == a.width && (it.heads == 1 || head_pitch == (int64_t)it.n * a.width));
+    };
     auto issue = [&](int64_t i) {
         const int s = (int)(i % kBulkStages);
         const BulkItem it = bulk_item<STRIDED>(a, blockIdx.x + i * gridDim.x, stage_bytes);
@@ -286,11 +313,14 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         mbar_arrive_expect(&bar[s], it.bytes);
         if (!it.bytes) return;
         uint8_t *stage = ring + (size_t)s * stage_bytes;
-        if (src_packed) {
+        if (packed(it, a.src_pitch, a.src_head_pitch)) {
             bulk_load(stage, it.src, it.bytes, &bar[s]);
         } else {
-            for (int32_t r = 0; r < it.rows; ++r)
-                bulk_load(stage + (size_t)r * a.width, it.src + (int64_t)r * a.src_pitch, (uint32_t)a.width, &bar[s]);
+            for (int32_t h = 0; h < it.heads; ++h)
+                for (int32_t r = 0; r < it.n; ++r)
+                    bulk_load(stage + (size_t)(h * it.n + r) * a.width,
+                              it.src + (int64_t)h * a.src_head_pitch + (int64_t)r * a.src_pitch, (uint32_t)a.width,
+                              &bar[s]);
         }
     };
     int64_t issued = 0;
@@ -306,11 +336,14 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         if (items[s].bytes) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint8_t *stage = ring + (size_t)s * stage_bytes;
-            if (dst_packed) {
-                bulk_store(items[s].dst, stage, items[s].bytes);
+            const BulkItem &it = items[s];
+            if (packed(it, a.dst_pitch, a.dst_head_pitch)) {
+                bulk_store(it.dst, stage, it.bytes);
             } else {
-                for (int32_t r = 0; r < items[s].rows; ++r)
-                    bulk_store(items[s].dst + (int64_t)r * a.dst_pitch, stage + (size_t)r * a.width, (uint32_t)a.width);
+                for (int32_t h = 0; h < it.heads; ++h)
+                    for (int32_t r = 0; r < it.n; ++r)
+                        bulk_store(it.dst + (int64_t)h * a.dst_head_pitch + (int64_t)r * a.dst_pitch,
+                                   stage + (size_t)(h * it.n + r) * a.width, (uint32_t)a.width);
             }
         }
         bulk_commit();

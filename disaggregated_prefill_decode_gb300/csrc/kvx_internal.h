@@ -11,14 +11,16 @@ namespace kvx {
 
 // One tile of copy work: a CTA moves it for one (layer, plane). Offsets are bytes into the
 // producer / consumer buffer of (layer, plane, shard). Contiguous plans: `n` is a byte count.
-// Strided plans (head-shard remap): `n` rows of CopyArgs::width bytes at the two row pitches.
+// Strided plans (head-shard remap): `n` rows of CopyArgs::width bytes at the two row pitches, for
+// each of `heads` heads (0 and 1 both mean one) at the two head pitches: row t of head h is at
+// off + h * head_pitch + t * pitch on each side.
 struct alignas(16) TileDesc {
     int64_t src_off;
     int64_t dst_off;
     int32_t n;
     int32_t s_shard;
     int32_t d_shard;
-    int32_t pad;
+    int32_t heads;
 };
 static_assert(sizeof(TileDesc) == 32, "TileDesc is two 16-byte words");
 
@@ -33,6 +35,8 @@ struct CopyArgs {
     int64_t dst_buf_bytes;
     int64_t src_pitch;                // producer row bytes
     int64_t dst_pitch;                // consumer row bytes
+    int64_t src_head_pitch;           // strided tiles of several heads: bytes from one head to the next
+    int64_t dst_head_pitch;
     unsigned long long *ts_start;     // timing: atomicMin of %globaltimer at each CTA's start (or null)
     unsigned long long *ts_end;       // timing: atomicMax of %globaltimer at each CTA's end
     int32_t width;                    // strided: bytes copied per row
@@ -124,6 +128,7 @@ struct kvx_plan_s {
     int32_t strided = 0;
     int32_t per_head = 0;                      // tiles are (block segment, head) pieces (an HND side)
     int64_t src_pitch = 0, dst_pitch = 0;      // strided tiles: row pitches
+    int64_t src_head_pitch = 0, dst_head_pitch = 0;   // per-head plans: head pitches of head-group tiles
     int32_t vec = 16;
     int32_t width = 0;
     int32_t tile_bytes = 16384;

@@ -608,9 +608,11 @@ struct EmitShape {
     int32_t per_head;                    // a head-major side: tiles per (block, head)
     int32_t pair_s[8], pair_d[8];
     int64_t pair_soff[8], pair_doff[8];
-    // per_head: the head partition and layout of each side, the head's bytes and each side's token pitch
-    int32_t heads, hps_s, hps_d, layout_s, layout_d;
-    int64_t head_bytes, src_pitch, dst_pitch;
+    // per_head: the head partition and layout of each side, the head's bytes, each side's token and
+    // head pitch, heads per tile and the head groups of one block (tiles per block = groups times the
+    // row chunks of a head)
+    int32_t heads, hps_s, hps_d, layout_s, layout_d, heads_per_tile, groups;
+    int64_t head_bytes, src_pitch, dst_pitch, src_head_pitch, dst_head_pitch;
 };
 
 // Element index (in heads) of (block, slot 0, head) inside one buffer of a side's layout.
@@ -625,7 +627,7 @@ __global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, 
     const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
     const int64_t ntok = (k1 - run_start[r]) * sh.bs;
     if (sh.per_head) {
-        tile_count[r] = (k1 - run_start[r]) * sh.heads * ((sh.bs + sh.rows_per_tile - 1) / sh.rows_per_tile);
+        tile_count[r] = (k1 - run_start[r]) * sh.groups * ((sh.bs + sh.rows_per_tile - 1) / sh.rows_per_tile);
         return;
     }
     const int64_t per = sh.strided ? (ntok + sh.rows_per_tile - 1) / sh.rows_per_tile
@@ -651,12 +653,14 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
     run_ntok[r] = (int32_t)ntok;
     int64_t t = tile_start[r];
     if (sh.per_head) {
-        // every block of the run, every head: bs rows at each side's token pitch
+        // every block of the run, by groups of heads that one shard pair shares (as many as fit a
+        // tile): bs rows per head at each side's token pitch, the group's heads a head pitch apart
         for (int64_t k = k0; k < k1; ++k)
-            for (int32_t g = 0; g < sh.heads; ++g) {
-                const int32_t ss = g / sh.hps_s, ds = g / sh.hps_d;
-                const int64_t s0 = head_start(sh.layout_s, sh.hps_s, sh.bs, pair_src[k], g % sh.hps_s) * sh.head_bytes;
-                const int64_t d0 = head_start(sh.layout_d, sh.hps_d, sh.bs, pair_dst[k], g % sh.hps_d) * sh.head_bytes;
+            for (int32_t g = 0; g < sh.heads;) {
+                const int32_t ss = g / sh.hps_s, hs = g % sh.hps_s, ds = g / sh.hps_d, hd = g % sh.hps_d;
+                const int32_t kh = min(sh.heads_per_tile, min(sh.hps_s - hs, sh.hps_d - hd));
+                const int64_t s0 = head_start(sh.layout_s, sh.hps_s, sh.bs, pair_src[k], hs) * sh.head_bytes;
+                const int64_t d0 = head_start(sh.layout_d, sh.hps_d, sh.bs, pair_dst[k], hd) * sh.head_bytes;
                 for (int32_t r0 = 0; r0 < sh.bs; r0 += sh.rows_per_tile, ++t) {
                     if (t >= tile_cap) { atomicOr(err, 16); return; }
                     TileDesc d;
@@ -665,9 +669,10 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
                     d.n = min(sh.rows_per_tile, sh.bs - r0);
                     d.s_shard = ss;
                     d.d_shard = ds;
-                    d.pad = 0;
+                    d.heads = kh > 1 ? kh : 0;
                     tiles[t] = d;
                 }
+                g += kh;
             }
         return;
     }
@@ -683,7 +688,7 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
                 d.n = (int32_t)min((int64_t)sh.tile_bytes, bytes - o);
                 d.s_shard = sh.pair_s[q];
                 d.d_shard = sh.pair_d[q];
-                d.pad = 0;
+                d.heads = 0;
                 tiles[t] = d;
             }
     } else {
@@ -696,7 +701,7 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
                 d.n = (int32_t)min((int64_t)sh.rows_per_tile, ntok - r0);
                 d.s_shard = sh.pair_s[q];
                 d.d_shard = sh.pair_d[q];
-                d.pad = 0;
+                d.heads = 0;
                 tiles[t] = d;
             }
     }
@@ -961,6 +966,13 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         sh.head_bytes = pl->src.head_bytes();
         sh.src_pitch = pl->src_pitch;
         sh.dst_pitch = pl->dst_pitch;
+        sh.src_head_pitch = pl->src_head_pitch;
+        sh.dst_head_pitch = pl->dst_head_pitch;
+        // head groups of one block, formed as the host plan builder forms them for a whole block
+        sh.heads_per_tile = (int32_t)std::max<int64_t>(1, sh.rows_per_tile / block_size);
+        sh.groups = 0;
+        for (int32_t g = 0; g < sh.heads; ++sh.groups)
+            g += std::min(sh.heads_per_tile, std::min(sh.hps_s - g % sh.hps_s, sh.hps_d - g % sh.hps_d));
         for (size_t q = 0; q < (size_t)sh.n_pairs; ++q) {
             sh.pair_s[q] = pairs[q].s;
             sh.pair_d[q] = pairs[q].d;
@@ -969,7 +981,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         }
         // a run of L blocks has at most L times the tiles of one block
         const int64_t per_block =
-            pl->per_head ? (int64_t)sh.heads * ((block_size + sh.rows_per_tile - 1) / sh.rows_per_tile)
+            pl->per_head ? (int64_t)sh.groups * ((block_size + sh.rows_per_tile - 1) / sh.rows_per_tile)
             : (pl->strided ? (block_size + sh.rows_per_tile - 1) / sh.rows_per_tile
                            : ((int64_t)block_size * sh.src_row_bytes + pl->tile_bytes - 1) / pl->tile_bytes) * sh.n_pairs;
         const int64_t tile_cap = B * per_block;

@@ -293,6 +293,8 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->bulk_stages = k == KVX_KERNEL_BULK ? pl->bulk_stages : 0;
     out->src_pitch = pl->src_pitch;
     out->dst_pitch = pl->dst_pitch;
+    out->src_head_pitch = pl->src_head_pitch;
+    out->dst_head_pitch = pl->dst_head_pitch;
     return KVX_OK;
 }
 

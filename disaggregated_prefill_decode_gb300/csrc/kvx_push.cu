@@ -178,6 +178,8 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.dst_buf_bytes = pl->dst.buf_bytes();
     a.src_pitch = pl->src_pitch;
     a.dst_pitch = pl->dst_pitch;
+    a.src_head_pitch = pl->src_head_pitch;
+    a.dst_head_pitch = pl->dst_head_pitch;
     a.width = pl->width;
     a.n_planes = pl->src.n_planes;
     a.src_shards = pl->src.n_shards;

@@ -85,9 +85,11 @@ static int32_t vector_bytes(const kvx_plan_s *pl, const std::vector<Pair> &pairs
 }
 
 // Tiles of plans with an HND side: each run is cut at every block boundary of either side, and each
-// such segment is copied head by head (a head's tokens are rows at each side's token pitch). When
-// both sides are HND with the same block size and heads per shard, a stretch of whole blocks is one
-// contiguous span per shard on both sides and is copied as such.
+// such segment is copied by groups of heads (a head's tokens are rows at each side's token pitch, and
+// the heads of a group, consecutive heads that one producer shard and one consumer shard share, are
+// a head pitch apart on each side): as many heads per tile as fit tile_bytes. When both sides are
+// HND with the same block size and heads per shard, a stretch of whole blocks is one contiguous span
+// per shard on both sides and is copied as such.
 static void build_head_tiles(kvx_plan_s *pl) {
     const Geom &s = pl->src, &d = pl->dst;
     const int64_t hb = s.head_bytes();
@@ -116,10 +118,17 @@ static void build_head_tiles(kvx_plan_s *pl) {
                 continue;
             }
             const int64_t len = std::min({s.block_size - sslot, d.block_size - dslot, n - t});
-            for (int32_t g = 0; g < heads; ++g) {
+            const int64_t per_tile = std::max<int64_t>(1, rows_per_tile / len);      // heads per tile
+            for (int32_t g = 0; g < heads;) {
                 const int32_t ss = g / s.heads_per_shard, hs = g % s.heads_per_shard;
                 const int32_t ds = g / d.heads_per_shard, hd = g % d.heads_per_shard;
-                emit(s.head_index(sblk, sslot, hs) * hb, d.head_index(dblk, dslot, hd) * hb, len, ss, ds);
+                const int32_t k = (int32_t)std::min<int64_t>({per_tile, s.heads_per_shard - hs, d.heads_per_shard - hd});
+                const int64_t so = s.head_index(sblk, sslot, hs) * hb, dof = d.head_index(dblk, dslot, hd) * hb;
+                if (k == 1)
+                    emit(so, dof, len, ss, ds);
+                else
+                    pl->tiles.push_back({so, dof, (int32_t)len, ss, ds, k});
+                g += k;
             }
             t += len;
         }
@@ -186,6 +195,9 @@ void init_copy_shape(kvx_plan_s *pl, bool tile_bytes_given) {
     pl->width = (int32_t)(pl->per_head ? s.head_bytes() : std::min(s.heads_per_shard, d.heads_per_shard) * s.head_bytes());
     pl->src_pitch = pl->per_head ? s.token_pitch() : s.row_bytes();
     pl->dst_pitch = pl->per_head ? d.token_pitch() : d.row_bytes();
+    // per-head plans: from a head to the next inside one shard, at the same token
+    pl->src_head_pitch = pl->per_head ? (s.layout == KVX_LAYOUT_HND ? s.block_size : 1) * s.head_bytes() : 0;
+    pl->dst_head_pitch = pl->per_head ? (d.layout == KVX_LAYOUT_HND ? d.block_size : 1) * d.head_bytes() : 0;
     if (!tile_bytes_given && !pl->strided) pl->tile_bytes = default_tile_bytes(s, d);
 }
 
@@ -202,6 +214,8 @@ bool as_whole_block_copy(kvx_plan_s *pl) {
     pl->width = (int32_t)s.row_bytes();
     pl->src_pitch = s.row_bytes();
     pl->dst_pitch = d.row_bytes();
+    pl->src_head_pitch = 0;
+    pl->dst_head_pitch = 0;
     pl->tile_bytes = default_tile_bytes(s, d);
     return true;
 }

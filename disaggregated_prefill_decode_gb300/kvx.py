@@ -52,7 +52,7 @@ class kvx_plan_info(ctypes.Structure):
     _fields_ = [("n_runs", c_i64), ("n_tiles", c_i64), ("bytes_per_layer", c_i64), ("vec_bytes", c_i32),
                 ("strided", c_i32), ("n_layers", c_i32), ("n_planes", c_i32), ("width", c_i32),
                 ("tile_bytes", c_i32), ("kernel", c_i32), ("threads", c_i32), ("lanes", c_i32), ("bulk_stages", c_i32),
-                ("src_pitch", c_i64), ("dst_pitch", c_i64)]
+                ("src_pitch", c_i64), ("dst_pitch", c_i64), ("src_head_pitch", c_i64), ("dst_head_pitch", c_i64)]
 
 
 class kvx_match_opts(ctypes.Structure):
@@ -90,7 +90,7 @@ KVX_CONN_WAITING, KVX_CONN_DEFERRED, KVX_CONN_READY, KVX_CONN_IN_FLIGHT, KVX_CON
     KVX_CONN_EXPIRED, KVX_CONN_TIMED_OUT, KVX_CONN_ABORTED = range(9)
 
 TILE_DTYPE = np.dtype([("src_off", "<i8"), ("dst_off", "<i8"), ("n", "<i4"), ("src_shard", "<i4"),
-                       ("dst_shard", "<i4"), ("pad", "<i4")])
+                       ("dst_shard", "<i4"), ("heads", "<i4")])
 
 _P = ctypes.POINTER
 _sig = {

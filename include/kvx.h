@@ -210,12 +210,14 @@ typedef struct kvx_plan_info {
     int32_t bulk_stages;         /* ring stages of the BULK kernel; 0 for the others */
     int64_t src_pitch;           /* strided plans: bytes between consecutive rows of a tile, producer */
     int64_t dst_pitch;           /* and consumer side */
+    int64_t src_head_pitch;      /* plans with a head-major side: bytes between consecutive heads of a */
+    int64_t dst_head_pitch;      /* tile (tiles then cover `heads` heads of n rows each), producer and consumer */
 } kvx_plan_info;
 kvx_status kvx_plan_get_info(kvx_plan_t plan, kvx_plan_info *out);
 
 /* Introspection for tests: the tile table of a host-built plan (host memory owned by the plan).
  * Entry layout, 32 bytes: { int64 src_off; int64 dst_off; int32 n; int32 src_shard;
- * int32 dst_shard; int32 pad }. Offsets are bytes into the (layer, plane, shard) buffers; every
+ * int32 dst_shard; int32 heads }; strided tiles copy n rows for each of max(heads, 1) heads. Offsets are bytes into the (layer, plane, shard) buffers; every
  * layer and plane uses the same table. Device-built plans report 0 entries here. */
 kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles);
 

@@ -188,12 +188,22 @@ def qwen3_32b_batched_hnd(seed: int = 3, n_layers: int = 64) -> PushWorkload:
     return w
 
 
+def qwen3_32b_batched_nhd_to_hnd(seed: int = 3, n_layers: int = 64) -> PushWorkload:
+    """The batched workload from a token-major producer ([block][slot][head][dim]) into a head-major
+    consumer ([block][head][slot][dim]): each block is transposed at head granularity."""
+    w = qwen3_32b_batched(seed=seed, n_layers=n_layers)
+    w.dst = w.dst.replace(layout=LAYOUT_HND)
+    w.name = "qwen3_32b_batched_nhd_to_hnd"
+    return w
+
+
 PUSH_WORKLOADS = {
     "tiny": tiny,
     "qwen3_32b_single": qwen3_32b_single,
     "qwen3_32b_batched": qwen3_32b_batched,
     "tp4_to_tp1_remap": tp4_to_tp1_remap,
     "qwen3_32b_batched_hnd": qwen3_32b_batched_hnd,
+    "qwen3_32b_batched_nhd_to_hnd": qwen3_32b_batched_nhd_to_hnd,
 }
 
 

@@ -90,8 +90,12 @@ def replay_tiles(plan, sg, src, dg, dst):
                     db[do:do + n] = sb[so:so + n]
                 else:
                     w, sp_, dp_ = info["width"], info["src_pitch"], info["dst_pitch"]
-                    for r in range(n):
-                        db[do + r * dp_:do + r * dp_ + w] = sb[so + r * sp_:so + r * sp_ + w]
+                    shp, dhp = info["src_head_pitch"], info["dst_head_pitch"]
+                    assert n * max(int(t["heads"]), 1) * w <= max(info["tile_bytes"], w)
+                    for h in range(max(int(t["heads"]), 1)):
+                        for r in range(n):
+                            s0, d0 = so + h * shp + r * sp_, do + h * dhp + r * dp_
+                            db[d0:d0 + w] = sb[s0:s0 + w]
     return out
 
 
@@ -108,6 +112,21 @@ CASES = {
     "nhd_to_hnd_merge": (PoolGeom(1, 2, 4, 1, 8, 2, 4, 10), PoolGeom(1, 2, 1, 4, 8, 2, 8, 6, 1)),
     "hnd_to_nhd_split": (PoolGeom(1, 1, 1, 4, 8, 2, 8, 5, 1), PoolGeom(1, 1, 2, 2, 8, 2, 2, 20)),
 }
+
+
+def test_head_major_plans_group_heads_per_tile():
+    """A plan with a head-major side copies groups of heads per tile (the heads one producer shard and
+    one consumer shard share, as many as fit tile_bytes), not one tile per head."""
+    sg = PoolGeom(1, 2, 1, 8, 128, 2, 16, 64)
+    dg = sg.replace(layout=1)
+    sp, dp = pools(sg, dg)
+    reqs = [(16 * 10, np.arange(10, dtype=np.int32), np.arange(20, 30, dtype=np.int32))]
+    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"tile_bytes": 16384})
+    info = kvx.kvx_plan_get_info(plan)
+    tiles = kvx.kvx_plan_tiles(plan)
+    assert info["src_head_pitch"] == 256 and info["dst_head_pitch"] == 16 * 256
+    assert len(tiles) == 10 * 2 and (tiles["heads"] == 4).all() and (tiles["n"] == 16).all()
+    kvx.kvx_plan_destroy(plan)
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
