@@ -361,10 +361,10 @@ typedef struct kvx_match_result {
  * remote_pool is the producer (decode) pool, local_pool the consumer (prefill) pool; their
  * block_size must equal block_size; their layouts and head partitions may differ as in kvx_plan
  * (whole blocks between head-major pools of the same partition move as identical byte spans, other
- * head-major pairs head by head). If out_plan is not NULL it receives a plan (built on the
+ * head-major pairs by groups of heads per block). If out_plan is not NULL it receives a plan (built on the
  * device) whose pushes copy those blocks with kvx_push_layer / kvx_sync; NULL computes the
- * decisions only (the pools may then be NULL). The call waits for `stream` (it reads back the
- * totals). Block ids outside a pool make the affected layers FAILED at kvx_sync (the copy kernel
+ * decisions only (the pools may then be NULL). The call waits for `stream` (it reads back its
+ * status; with a plan or hole filling also the published-block total first). Block ids outside a pool make the affected layers FAILED at kvx_sync (the copy kernel
  * skips them). If the pushing sessions need more than n_free blocks the decisions are still
  * written, no plan is made, and the call returns KVX_ENOMEM.
  */
