@@ -306,6 +306,13 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     auto packed = [&](const BulkItem &it, int64_t pitch, int64_t head_pitch) {
         return !STRIDED || (pitch == a.width && (it.heads == 1 || head_pitch == (int64_t)it.n * a.width));
     };
+    // Stage order of a head group: head-major (row t of head h at h * n + t) unless the producer keeps
+    // the group's heads of one token adjacent and the consumer does not; then token-major
+    // (t * heads + h), so that each token's heads load in one copy and the rows go out one by one
+    // (on GB300 row-by-row loads cost more than row-by-row stores).
+    auto token_major = [&](const BulkItem &it) {
+        return STRIDED && it.heads > 1 && a.src_head_pitch == a.width && a.dst_head_pitch != a.width;
+    };
     auto issue = [&](int64_t i) {
         const int s = (int)(i % kBulkStages);
         const BulkItem it = bulk_item<STRIDED>(a, blockIdx.x + i * gridDim.x, stage_bytes);
@@ -313,7 +320,15 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         mbar_arrive_expect(&bar[s], it.bytes);
         if (!it.bytes) return;
         uint8_t *stage = ring + (size_t)s * stage_bytes;
-        if (packed(it, a.src_pitch, a.src_head_pitch)) {
+        if (token_major(it)) {
+            const uint32_t span = (uint32_t)(it.heads * a.width);    // one token's heads
+            if (a.src_pitch == (int64_t)span) {
+                bulk_load(stage, it.src, it.bytes, &bar[s]);
+            } else {
+                for (int32_t r = 0; r < it.n; ++r)
+                    bulk_load(stage + (size_t)r * span, it.src + (int64_t)r * a.src_pitch, span, &bar[s]);
+            }
+        } else if (packed(it, a.src_pitch, a.src_head_pitch)) {
             bulk_load(stage, it.src, it.bytes, &bar[s]);
         } else {
             for (int32_t h = 0; h < it.heads; ++h)
@@ -337,7 +352,12 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint8_t *stage = ring + (size_t)s * stage_bytes;
             const BulkItem &it = items[s];
-            if (packed(it, a.dst_pitch, a.dst_head_pitch)) {
+            if (token_major(it)) {
+                for (int32_t h = 0; h < it.heads; ++h)
+                    for (int32_t r = 0; r < it.n; ++r)
+                        bulk_store(it.dst + (int64_t)h * a.dst_head_pitch + (int64_t)r * a.dst_pitch,
+                                   stage + (size_t)(r * it.heads + h) * a.width, (uint32_t)a.width);
+            } else if (packed(it, a.dst_pitch, a.dst_head_pitch)) {
                 bulk_store(it.dst, stage, it.bytes);
             } else {
                 for (int32_t h = 0; h < it.heads; ++h)
@@ -442,8 +462,9 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     if (sh.kernel == KVX_KERNEL_BULK) {
         // Launches that read under 128 MiB (a layer push) default to 5 CTAs per 4 SMs: measured on
         // GB300 in the per-layer push pattern, 1.25 CTAs per SM beat 1 (0.965 against 0.949 of the
-        // copy peak, consecutive launches overlapping on the lanes) and 2 (0.90). Larger launches
-        // take the occupancy limit.
+        // copy peak, consecutive launches overlapping on the lanes) and 2 (0.90). Head-group tiles,
+        // whose rows go out one bulk copy each, default to 2 per SM (0.947 against 0.890 at 1.25).
+        // Larger launches take the occupancy limit.
         const int smem = sh.stages * sh.tile_bytes;
         const bool small = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20);
         const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (small ? 2 : 64);
@@ -451,7 +472,7 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
         int sms = 0;
         e = resident_grid(fn, 32, smem, cap, &grid, &sms);
         if (e != cudaSuccess) return e;
-        if (!sh.ctas_per_sm && small) grid = std::min(grid, sms + sms / 4);
+        if (!sh.ctas_per_sm && small) grid = std::min(grid, sh.head_groups ? 2 * sms : sms + sms / 4);
         CopyArgs args_copy = a;
         int64_t work = n_work;
         int32_t stage_bytes = sh.tile_bytes;

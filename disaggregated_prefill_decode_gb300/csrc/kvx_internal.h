@@ -106,6 +106,7 @@ struct LaunchShape {
     int32_t tile_bytes;    // bulk: bytes per stage
     int32_t ctas_per_sm;   // 0: occupancy limit
     int32_t stages;        // bulk: ring stages (2, 3, 4, 6 or 8)
+    int32_t head_groups;   // tiles are head groups (a head-major side): many small row copies per tile
 };
 cudaError_t launch_copy(const CopyArgs &args, int32_t n_layers, const LaunchShape &shape, cudaStream_t stream);
 

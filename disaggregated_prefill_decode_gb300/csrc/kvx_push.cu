@@ -286,7 +286,7 @@ static kvx_status launch_tracked(kvx_plan_s *pl, int32_t l0, int32_t l1, cudaStr
     int32_t slot = -1;
     if ((pl->flags & KVX_PLAN_TIMING) && (int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
     const LaunchShape shape{effective_kernel(pl), pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
-                            pl->bulk_stages};
+                            pl->bulk_stages, pl->per_head};
     CopyArgs args = plan_copy_args(pl, l0);
     if (slot >= 0) {
         args.ts_start = pl->ts + slot;

@@ -209,6 +209,7 @@ GEOMS = {
     "hnd_tp4_to_nhd_tp1_bs64": (PoolGeom(1, 2, 4, 2, 128, 2, 16, 60, 1), PoolGeom(1, 2, 1, 8, 128, 2, 64, 15)),
     "nhd_to_hnd_bs16to32": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 1, 8, 128, 2, 32, 30, 1)),
     "hnd_odd_heads": (PoolGeom(1, 1, 1, 3, 3, 2, 8, 40, 1), PoolGeom(1, 1, 3, 1, 3, 2, 4, 80, 1)),
+    "nhd_tp1_to_hnd_tp2": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 2, 4, 128, 2, 16, 60, 1)),
 }
 
 
