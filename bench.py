@@ -186,6 +186,7 @@ def alloc_pool(torch, geom, fill, seed, device):
         kvx_inputs.fill_bf16_normal(big, seed) if geom.elem_bytes == 2 else kvx_inputs.fill_fp8_bytes(big, seed)
     else:
         kvx_inputs.fill_canary(big, "bf16_normal" if geom.elem_bytes == 2 else "fp8_bytes")
+    torch.cuda.synchronize(device)   # filled on the current stream; the pushes run on others
     return [big[i * per:i * per + geom.buffer_bytes] for i in range(geom.n_buffers)], big
 
 

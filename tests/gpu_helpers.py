@@ -22,6 +22,8 @@ def device_pool(geom, fill, seed=0, align=512):
         kvx_inputs.fill_canary(big, fill[len("canary_"):])
     else:
         raise ValueError(fill)
+    # the fill runs on the current stream; tests push from other streams, so it must be complete
+    torch.cuda.synchronize()
     return [big[i * per:i * per + geom.buffer_bytes] for i in range(geom.n_buffers)], big
 
 
