@@ -191,9 +191,10 @@ __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_w
 // and completes the stage's mbarrier (transaction count = bytes); the thread then issues the bulk
 // store of that stage and, once the store before it has finished reading its stage, the load of a
 // later item into that freed stage. Waits are bounded by the global timer.
-// A strided tile (rows of `width` bytes at each side's pitch) is packed densely in its stage: a side
-// whose pitch equals the width moves in one bulk copy, the other side row by row, all rows of a
-// load completing on the stage's one mbarrier and all row stores forming one bulk group.
+// A strided tile (rows of `width` bytes at each side's pitch, for each head of a head group) is packed
+// densely in its stage, head-major or token-major: a side whose rows lie adjacent in that order moves
+// in one bulk copy, the other piece by piece, all pieces of a load completing on the stage's one
+// mbarrier and all stores of a stage forming one bulk group.
 // ------------------------------------------------------------------------------------------------
 
 constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
@@ -255,7 +256,7 @@ struct BulkItem {
     uint8_t *dst;
     uint32_t bytes;    // 0: skipped (out of bounds or misaligned)
     int32_t n;         // strided tiles: rows of a.width bytes per head; contiguous tiles: 1
-    int32_t heads;     // strided tiles: heads (rows of head h follow those of head h - 1 in the stage)
+    int32_t heads;     // strided tiles: heads of the group (1 for a single head)
     int32_t layer;
 };
 
