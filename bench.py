@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import gc
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -103,11 +104,15 @@ def ncu_traffic(kernel_key):
 
 
 def csrc_sha():
-    """Hash of the copy kernels and the copy-shape builder (the ncu counters are valid only for these)."""
+    """Hash of the code of the copy kernels and the copy-shape builder, comments and blank space left
+    out (the ncu counters are valid only for this code)."""
     h = hashlib.sha256()
     for name in ("kvx_copy.cu", "kvx_tiles.cpp"):
-        with open(os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "disaggregated_prefill_decode_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
