@@ -239,19 +239,23 @@ __device__ __forceinline__ uint64_t block_hash(uint64_t parent, const uint32_t *
     return ((uint64_t)hi << 32) | lo;
 }
 
-constexpr int kMatchThreads = 256;
+// 512 threads: two CTAs per SM at 62 registers, so 304 sessions are resident at once; measured on
+// GB300 against 256 threads (one round of candidates fewer for sessions past 256 blocks: 0.054 ms
+// against 0.061 ms per 256-session call) and against two candidates per thread (0.063-0.064 ms: the
+// second chain doubles the work of the many sessions shorter than a round).
+constexpr int kMatchThreads = 512;
 
 // One CTA per session. The remote prefix is found without walking the chain: block j is hashed from
 // the PUBLISHED hash of block j - 1 (its candidate c_j), and the first j where c_j differs from the
 // published hash is exactly the first j where the session's own chained hash h_j does: below it every
 // published parent equals the true one, so c_j = h_j, and at it the parent is still the true one,
-// so c_j = h_j there too. The candidates are independent, so the CTA hashes 256 of them at a time
+// so c_j = h_j there too. The candidates are independent, so the CTA hashes 512 of them at a time
 // (one per thread), each also looked up in the table; warp 0 then extends the two prefixes window by
 // window with ballots. Local hits can use candidates up to and including the first mismatch; if every
 // block to there is resident, warp 0 continues the true chain from that block, window by window, until
 // the first block that is not resident. With FILL_HOLES, residency inside the remote prefix is
 // recorded for the plan emission and the non-resident blocks there are counted.
-__global__ void __launch_bounds__(kMatchThreads) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
+__global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uint32_t *tokens, const int64_t *tok_off,
                                                                     int32_t n_sessions, int32_t bs, TableView table,
                                                                     const uint64_t *remote_hash, const int64_t *rem_off,
                                                                     int32_t threshold, MatchFlags mf, kvx_match_result *out,
