@@ -250,8 +250,8 @@ constexpr int kMatchThreads = 512;
 // published hash is exactly the first j where the session's own chained hash h_j does: below it every
 // published parent equals the true one, so c_j = h_j, and at it the parent is still the true one,
 // so c_j = h_j there too. The candidates are independent, so the CTA hashes 512 of them at a time
-// (one per thread), each also looked up in the table; warp 0 then extends the two prefixes window by
-// window with ballots. Local hits can use candidates up to and including the first mismatch; if every
+// (one per thread), each also looked up in the table; each warp then summarises its window of 32
+// with ballots and warp 0 extends the two prefixes over the windows in one pass. Local hits can use candidates up to and including the first mismatch; if every
 // block to there is resident, warp 0 continues the true chain from that block, window by window, until
 // the first block that is not resident. With FILL_HOLES, residency inside the remote prefix is
 // recorded for the plan emission and the non-resident blocks there are counted.
@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
                                                                     int64_t *push_blocks, int32_t *err) {
     __shared__ uint64_t cand[kMatchThreads];
     __shared__ uint8_t flag[kMatchThreads];     // bit 0: equals the published hash, bit 1: resident
+    __shared__ int32_t win_fr[kMatchThreads / 32], win_fl[kMatchThreads / 32], win_holes[kMatchThreads / 32];
     __shared__ int32_t go_on;
     const int32_t s = (int32_t)blockIdx.x;
     if (s >= n_sessions) return;
@@ -300,44 +301,66 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
             flag[tid] = (uint8_t)((same ? 1 : 0) | (res ? 2 : 0));
         }
         __syncthreads();
+        // every warp summarises its window of 32 candidates: the first published-hash mismatch, the
+        // first block not resident, and (hole filling) the non-resident blocks before the mismatch
+        {
+            const int64_t j0 = base + 32 * warp;
+            const uint8_t f = j0 + lane < n_cand ? flag[tid] : 0;     // past the candidates: both miss
+            const unsigned hit = __ballot_sync(kFull, f & 2);
+            const unsigned rmiss = ~__ballot_sync(kFull, f & 1);
+            const int fr = rmiss ? __ffs(rmiss) - 1 : 32;
+            const int fl = ~hit ? __ffs(~hit) - 1 : 32;
+            // residency below the window's first mismatch. Every round that runs starts with the remote
+            // prefix open (once it closes, the local one has closed too); entries past the remote
+            // prefix are written as well and never read (the emission looks only below it)
+            if (fill && lane < fr) mf.resident[r0 + j0 + lane] = (f & 2) ? 1 : 0;
+            if (lane == 0) {
+                win_fr[warp] = fr;
+                win_fl[warp] = fl;
+                win_holes[warp] = __popc(~hit & (fr >= 32 ? kFull : ((1u << fr) - 1u)));
+            }
+        }
+        __syncthreads();
         if (warp == 0) {
-            for (int w = 0; w < kMatchThreads / 32 && (rem_open || loc_open); ++w) {
-                const int64_t j0 = base + 32 * w;
-                const int p = 32 * w + lane;
-                const uint8_t f = j0 + lane < n_cand ? flag[p] : 0;   // past the candidates: both miss
-                const unsigned m1 = __ballot_sync(kFull, f & 2);
-                int loc_lim = 0;                                        // window positions local hits may use
-                int fr = 32;
-                bool closed_here = false;
-                if (rem_open) {
-                    const unsigned miss = ~__ballot_sync(kFull, f & 1);
-                    fr = miss ? __ffs(miss) - 1 : 32;
-                    if (fill) {
-                        if (lane < fr) mf.resident[r0 + j0 + lane] = (f & 2) ? 1 : 0;
-                        const unsigned below = fr >= 32 ? kFull : ((1u << fr) - 1u);
-                        holes += __popc(~m1 & below);
-                    }
-                    l_rem += fr;
-                    rem_open = fr == 32;
-                    closed_here = !rem_open;
-                    loc_lim = rem_open ? 32 : fr + 1;                   // the first mismatch still has its true hash
+            // the windows in order, one lane each: the remote prefix runs to the first window with a
+            // mismatch; local hits run while resident, up to and including the first mismatch block
+            // (whose candidate is still its true hash)
+            constexpr int kWin = kMatchThreads / 32;
+            const bool valid = lane < kWin;
+            const int fr = valid ? win_fr[lane] : 32, fl = valid ? win_fl[lane] : 32;
+            const int hw = valid ? win_holes[lane] : 0;
+            int wr = kWin, fr_w = 32;                                   // first window with a mismatch
+            const bool rem_was_open = rem_open;
+            if (rem_open) {
+                const unsigned m = __ballot_sync(kFull, valid && fr < 32);
+                wr = m ? __ffs(m) - 1 : kWin;
+                fr_w = __shfl_sync(kFull, fr, wr < kWin ? wr : 0);
+                if (fill) {
+                    int h = lane <= wr ? hw : 0;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(kFull, h, o);
+                    holes += h;
                 }
-                if (loc_open) {
-                    const unsigned lmiss = ~m1;
-                    const int fl = lmiss ? __ffs(lmiss) - 1 : 32;
-                    if (fl < loc_lim) {
-                        l_loc += fl;
-                        loc_open = false;
-                    } else {
-                        l_loc += loc_lim;
-                        if (closed_here) {                              // resident through the first mismatch,
-                            loc_open = false;                           // which is a candidate (fl > fr)
-                            chain = true;
-                            chain_parent = cand[32 * w + fr];
-                        } else if (!rem_open) {
-                            loc_open = false;
-                        }
-                    }
+                l_rem += 32 * wr + (wr < kWin ? fr_w : 0);
+                rem_open = wr == kWin;
+            }
+            if (loc_open) {
+                // positions of window w local hits may use: all before wr, through the mismatch at wr
+                const int lim = !rem_was_open ? 0 : lane < wr ? 32 : (lane == wr ? fr_w + 1 : 0);
+                const unsigned m = __ballot_sync(kFull, valid && fl < lim);
+                const int wl = m ? __ffs(m) - 1 : kWin;
+                if (wl < kWin && wl <= wr) {
+                    l_loc += 32 * wl + __shfl_sync(kFull, fl, wl);
+                    loc_open = false;
+                } else if (!rem_was_open) {
+                    loc_open = false;
+                } else if (wr < kWin) {                                 // resident through the mismatch
+                    l_loc += 32 * wr + fr_w + 1;
+                    loc_open = false;
+                    chain = true;
+                    chain_parent = cand[32 * wr + fr_w];
+                } else {
+                    l_loc += 32 * kWin;
                 }
             }
             if (lane == 0) go_on = rem_open || loc_open;
