@@ -468,6 +468,14 @@ def test_hnd_batched_workload_sampled():
     assert info["strided"] == 1 and info["src_pitch"] == 256 and info["dst_pitch"] == 256
 
 
+def test_nhd_to_hnd_batched_workload_sampled():
+    """The batched Qwen3-32B-shaped workload from a token-major producer into a head-major consumer,
+    64 layers in the benchmark's launch pattern (head-group tiles), sampled layers checked whole."""
+    w = kvx_inputs.qwen3_32b_batched_nhd_to_hnd()
+    info = run_workload(w, [0, 33, 63])
+    assert info["strided"] == 1 and info["src_head_pitch"] == 256 and info["dst_head_pitch"] == 16 * 256
+
+
 def test_threads_push_their_own_plans_concurrently():
     """kvx calls from several host threads, each with its own plan, pools and stream (the library's
     lanes, event pool, device memory pool and status stream are shared): every consumer equals the
