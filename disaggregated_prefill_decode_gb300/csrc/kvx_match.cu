@@ -239,6 +239,39 @@ __device__ __forceinline__ uint64_t block_hash(uint64_t parent, const uint32_t *
     return ((uint64_t)hi << 32) | lo;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Scans: warp shuffles inside a warp, warp totals through shared memory, block totals through a
+// second level (reduce-then-scan over 1024-element blocks).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kScanThreads = 1024;
+
+// Inclusive scan of one value per thread across the block; returns it and the block total.
+__device__ __forceinline__ int64_t block_inclusive_scan(int64_t v, int64_t *warp_sums, int64_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < n_warps ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += warp_sums[warp - 1];
+    *total = warp_sums[n_warps - 1];
+    __syncthreads();
+    return v;
+}
+
 // 512 threads: two CTAs per SM at 62 registers, so 304 sessions are resident at once; measured on
 // GB300 against 256 threads (one round of candidates fewer for sessions past 256 blocks: 0.054 ms
 // against 0.061 ms per 256-session call) and against two candidates per thread (0.063-0.064 ms: the
@@ -259,13 +292,15 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
                                                                     int32_t n_sessions, int32_t bs, TableView table,
                                                                     const uint64_t *remote_hash, const int64_t *rem_off,
                                                                     int32_t threshold, MatchFlags mf, kvx_match_result *out,
-                                                                    int64_t *push_blocks, int32_t *err) {
+                                                                    int64_t *push_blocks, int64_t *sess_start,
+                                                                    int64_t *scalars, int64_t n_free, int32_t *err) {
     __shared__ uint64_t cand[kMatchThreads];
     __shared__ uint8_t flag[kMatchThreads];     // bit 0: equals the published hash, bit 1: resident
     __shared__ int32_t win_fr[kMatchThreads / 32], win_fl[kMatchThreads / 32], win_holes[kMatchThreads / 32];
-    __shared__ int32_t go_on;
+    __shared__ int32_t go_on, is_last;
+    __shared__ int64_t scan_ws[32];
     const int32_t s = (int32_t)blockIdx.x;
-    if (s >= n_sessions) return;
+    if (s >= n_sessions) return;                                  // never: the grid is one CTA per session
     const int tid = (int)threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the two CSR totals bound every read of the token and published-hash arrays
     const int64_t n_tok_total = tok_off[n_sessions], n_pub = rem_off[n_sessions];
@@ -368,8 +403,7 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
         __syncthreads();
         if (!go_on) break;
     }
-    if (warp != 0) return;
-    if (chain && l_loc < n_full) {
+    if (warp == 0 && chain && l_loc < n_full) {
         // beyond the first mismatch the published parents no longer hold: the true chain, from the
         // candidate of that block, while the blocks stay resident (looked up 32 at a time)
         uint64_t mine = 0;
@@ -387,59 +421,53 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
             return open;
         }, chain_parent);
     }
-    __syncwarp();
-    if (lane != 0) return;
-    if ((mf.flags & KVX_MATCH_KEEP_LAST) && l_rem > 0 && l_rem * bs >= n_tok) {
-        // every token is covered (the session ends on a block boundary and its whole chain matched):
-        // recompute the last block
-        --l_rem;
-        if (fill && !mf.resident[r0 + l_rem]) --holes;
-    }
-    const int64_t missing_blocks = fill ? holes : (l_rem > l_loc ? l_rem - l_loc : 0);
-    const int64_t missing = missing_blocks * bs;
-    if (missing > (int64_t)INT32_MAX || l_loc > (int64_t)INT32_MAX) atomicOr(err, 4);
-    const int32_t push = (missing > 0 && missing >= threshold) ? 1 : 0;
-    kvx_match_result r;
-    r.local_hit_blocks = (int32_t)l_loc;
-    r.remote_hit_blocks = (int32_t)l_rem;
-    r.missing_tokens = (int32_t)missing;
-    r.push = push;
-    r.dst_start = -1;
-    out[s] = r;
-    push_blocks[s] = push ? missing_blocks : 0;
-}
-
-// ------------------------------------------------------------------------------------------------
-// Scans: warp shuffles inside a warp, warp totals through shared memory, block totals through a
-// second level (reduce-then-scan over 1024-element blocks).
-// ------------------------------------------------------------------------------------------------
-
-constexpr int kScanThreads = 1024;
-
-// Inclusive scan of one value per thread across the block; returns it and the block total.
-__device__ __forceinline__ int64_t block_inclusive_scan(int64_t v, int64_t *warp_sums, int64_t *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = (blockDim.x + 31) >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_sums[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int64_t w = lane < n_warps ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t n = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += n;
+    if (tid == 0) {                                               // the session's result
+        if ((mf.flags & KVX_MATCH_KEEP_LAST) && l_rem > 0 && l_rem * bs >= n_tok) {
+            // every token is covered (the session ends on a block boundary and its whole chain matched):
+            // recompute the last block
+            --l_rem;
+            if (fill && !mf.resident[r0 + l_rem]) --holes;
         }
-        warp_sums[lane] = w;
+        const int64_t missing_blocks = fill ? holes : (l_rem > l_loc ? l_rem - l_loc : 0);
+        const int64_t missing = missing_blocks * bs;
+        if (missing > (int64_t)INT32_MAX || l_loc > (int64_t)INT32_MAX) atomicOr(err, 4);
+        const int32_t push = (missing > 0 && missing >= threshold) ? 1 : 0;
+        kvx_match_result r;
+        r.local_hit_blocks = (int32_t)l_loc;
+        r.remote_hit_blocks = (int32_t)l_rem;
+        r.missing_tokens = (int32_t)missing;
+        r.push = push;
+        r.dst_start = -1;
+        out[s] = r;
+        push_blocks[s] = push ? missing_blocks : 0;
+        __threadfence();                                              // visible before this CTA is counted
+        is_last = atomicAdd(reinterpret_cast<unsigned long long *>(&scalars[7]), 1ull) ==
+                  (unsigned long long)(n_sessions - 1);
     }
     __syncthreads();
-    if (warp > 0) v += warp_sums[warp - 1];
-    *total = warp_sums[n_warps - 1];
-    __syncthreads();
-    return v;
+    if (!is_last) return;
+    // The last CTA to finish: every session's pull count is in. It numbers the pulled blocks in
+    // session order (exclusive scan) and hands each pushing session its first free-list position.
+    __threadfence();
+    int64_t carry = 0;
+    for (int32_t b0 = 0; b0 < n_sessions; b0 += kMatchThreads) {
+        const int32_t i = b0 + tid;
+        const int64_t v = i < n_sessions ? push_blocks[i] : 0;
+        int64_t tot;
+        const int64_t inc = block_inclusive_scan(v, scan_ws, &tot);
+        if (i < n_sessions) sess_start[i] = carry + inc - v;
+        carry += tot;
+    }
+    for (int32_t i = tid; i < n_sessions; i += kMatchThreads)
+        if (out[i].push) out[i].dst_start = sess_start[i];
+    if (tid == 0) {
+        // the pulled blocks never exceed the published ones (else the remote offsets overlap)
+        const bool fits = carry <= n_free, sane = carry <= max(n_pub, (int64_t)1);
+        scalars[0] = carry;
+        scalars[4] = (fits && sane) ? carry : 0;
+        if (!sane) atomicOr(err, 2);
+        else if (!fits) atomicOr(err, 8);
+    }
 }
 
 // Phase 1: exclusive scan inside each 1024-element block; block totals to partial[].
@@ -513,7 +541,7 @@ static cudaError_t exclusive_scan(const int64_t *in, int64_t *out, int64_t n_bou
 // ------------------------------------------------------------------------------------------------
 
 // Scalars: [0] blocks the pushes need, [1] runs, [2] tiles, [4] blocks the plan emits ([0], or 0
-// when the free list is too short).
+// when the free list is too short), [5] hole-filling pull flags counted, [7] match CTAs finished.
 struct MatchScratch {
     int64_t *push_blocks;   // [n_sessions]
     int64_t *sess_start;    // [n_sessions] exclusive scan of push_blocks
@@ -529,21 +557,6 @@ struct MatchScratch {
     int32_t *err;           // [4] error bits
 };
 
-// B bounds the scratch arrays: overlapping remote ranges (a malformed CSR) could otherwise claim more
-// pushed blocks than there are published ones.
-__global__ void kvx_assign_dst(kvx_match_result *out, const int64_t *sess_start, int32_t n_sessions,
-                               int64_t *scalars, int64_t n_free, const int64_t *pub_total, int32_t *err) {
-    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t B = max(*pub_total, (int64_t)1);
-    const bool fits = scalars[0] <= n_free;
-    const bool sane = scalars[0] <= B;
-    if (s == 0) {
-        scalars[4] = (fits && sane) ? scalars[0] : 0;
-        if (!sane) atomicOr(err, 2);
-        else if (!fits) atomicOr(err, 8);
-    }
-    if (s < n_sessions && out[s].push) out[s].dst_start = sess_start[s];
-}
 
 // One thread per pushed block k: its session, its (decode, prefill) pair, and whether it starts a
 // run (first block of a session, or either id not its predecessor's + 1).
@@ -966,12 +979,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
     kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                         table->view(), remote_hash, rem_off, threshold,
-                                                                        mf, out, m.push_blocks, m.err);
-    ok(cudaGetLastError());
-    ok(exclusive_scan(m.push_blocks, m.sess_start, n_sessions, nullptr, m.partial, &m.scalars[0], stream));
-    count_launch();
-    kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, m.sess_start, n_sessions, m.scalars, n_free,
-                                                                  rem_off + n_sessions, m.err);
+                                                                        mf, out, m.push_blocks, m.sess_start,
+                                                                        m.scalars, n_free, m.err);
     ok(cudaGetLastError());
 
     if (pl && e == cudaSuccess) {
@@ -1109,8 +1118,7 @@ namespace kvx {
 constexpr int32_t kStaticMaxSessions = 65536;
 constexpr size_t kStaticPushOff = 0;
 constexpr size_t kStaticSessOff = kStaticPushOff + sizeof(int64_t) * kStaticMaxSessions;
-constexpr size_t kStaticPartOff = kStaticSessOff + sizeof(int64_t) * kStaticMaxSessions;
-constexpr size_t kStaticScalOff = kStaticPartOff + sizeof(int64_t) * (kStaticMaxSessions / kScanThreads);
+constexpr size_t kStaticScalOff = kStaticSessOff + sizeof(int64_t) * kStaticMaxSessions;
 constexpr size_t kStaticErrOff = kStaticScalOff + sizeof(int64_t) * 8;   // right after the scalars
 constexpr size_t kStaticBytes = kStaticErrOff + sizeof(int32_t) * 4;
 
@@ -1155,7 +1163,6 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
     if (st) return st;
     int64_t *push_blocks = reinterpret_cast<int64_t *>(sc + kStaticPushOff);
     int64_t *sess_start = reinterpret_cast<int64_t *>(sc + kStaticSessOff);
-    int64_t *partial = reinterpret_cast<int64_t *>(sc + kStaticPartOff);
     int64_t *scalars = reinterpret_cast<int64_t *>(sc + kStaticScalOff);
     int32_t *err = reinterpret_cast<int32_t *>(sc + kStaticErrOff);
 
@@ -1167,14 +1174,8 @@ extern "C" kvx_status kvx_match_prefix_static(const uint32_t *tokens, const int6
         kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
                                                                             table->view(), remote_hash, rem_off, threshold,
                                                                             MatchFlags{0, nullptr, 0, nullptr}, out,
-                                                                            push_blocks, err);
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) e = exclusive_scan(push_blocks, sess_start, n_sessions, nullptr, partial, &scalars[0], stream);
-    if (e == cudaSuccess) {
-        count_launch();
-        kvx_assign_dst<<<grid_for(n_sessions, 256), 256, 0, stream>>>(out, sess_start, n_sessions, scalars, n_free,
-                                                                      rem_off + n_sessions, err);
+                                                                            push_blocks, sess_start, scalars, n_free,
+                                                                            err);
         e = cudaGetLastError();
     }
     struct { int64_t scal[8]; int32_t err[4]; } back = {};
