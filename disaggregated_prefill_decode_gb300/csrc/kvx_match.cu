@@ -470,43 +470,6 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
     }
 }
 
-// Phase 1: exclusive scan inside each 1024-element block; block totals to partial[].
-// n is *n_dev when n_dev is not NULL, else n_host (the grid covers the host bound).
-__global__ void __launch_bounds__(kScanThreads) kvx_scan_local(const int64_t *in, int64_t *out, int64_t n_host,
-                                                                const int64_t *n_dev, int64_t *partial) {
-    __shared__ int64_t ws[32];
-    const int64_t n = n_dev ? *n_dev : n_host;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t v = i < n ? in[i] : 0;
-    int64_t total;
-    const int64_t inc = block_inclusive_scan(v, ws, &total);
-    if (i < n) out[i] = inc - v;
-    if (threadIdx.x == 0) partial[blockIdx.x] = total;
-}
-
-// Phase 2: one block scans the partials (any count, in passes of 1024 with a carry); *sum = total.
-__global__ void __launch_bounds__(kScanThreads) kvx_scan_partials(int64_t *partial, int64_t n_part, int64_t *sum) {
-    __shared__ int64_t ws[32];
-    int64_t carry = 0;
-    for (int64_t base = 0; base < n_part; base += blockDim.x) {
-        const int64_t i = base + threadIdx.x;
-        const int64_t v = i < n_part ? partial[i] : 0;
-        int64_t total;
-        const int64_t inc = block_inclusive_scan(v, ws, &total);
-        if (i < n_part) partial[i] = carry + inc - v;
-        carry += total;
-    }
-    if (threadIdx.x == 0) *sum = carry;
-}
-
-// Phase 3: add each block's offset.
-__global__ void __launch_bounds__(kScanThreads) kvx_scan_add(int64_t *out, int64_t n_host, const int64_t *n_dev,
-                                                              const int64_t *partial) {
-    const int64_t n = n_dev ? *n_dev : n_host;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) out[i] += partial[blockIdx.x];
-}
-
 // The whole scan in one block, for n <= kScanThreads.
 __global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *in, int64_t *out, int64_t n_host,
                                                                  const int64_t *n_dev, int64_t *sum) {
@@ -520,19 +483,76 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *i
     if (threadIdx.x == 0) *sum = total;
 }
 
-// Exclusive scan of in[0..n) into out, total into *sum. n_bound is a host upper bound on n.
+constexpr uint64_t kScanWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait on a predecessor
+
+__device__ __forceinline__ uint64_t scan_clock_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longer scans in one pass, with a look back over the tiles before: a CTA takes the next tile in
+// order by an atomic ticket (so every earlier tile belongs to a CTA already running, which never
+// waits on a later one), publishes its tile's total, then walks back over the earlier tiles adding
+// their totals until it meets one that has published its running prefix, and publishes its own.
+// state[t] holds 0 (nothing yet), total * 4 + 1 (the tile's total) or prefix * 4 + 2 (the prefix
+// through the tile); state[n_tiles] is the ticket counter; all zero before the launch. A wait is
+// bounded by the global timer: past the bound the scan sets error bit 64 and goes on (wrong sums,
+// reported by the caller).
+__global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t *in, int64_t *out, int64_t n_host,
+                                                                   const int64_t *n_dev, unsigned long long *state,
+                                                                   int64_t n_tiles, int64_t *sum, int32_t *err) {
+    __shared__ int64_t ws[32];
+    __shared__ int64_t tile_s, excl_s;
+    if (threadIdx.x == 0) tile_s = (int64_t)atomicAdd(&state[n_tiles], 1ull);
+    __syncthreads();
+    const int64_t tile = tile_s;
+    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t i = tile * blockDim.x + threadIdx.x;
+    const int64_t v = i < n ? in[i] : 0;
+    int64_t total;
+    const int64_t inc = block_inclusive_scan(v, ws, &total);
+    if (threadIdx.x == 0) {
+        int64_t excl = 0;
+        if (tile > 0) {
+            atomicExch(&state[tile], ((unsigned long long)total << 2) | 1ull);
+            uint64_t t0 = 0;
+            for (int64_t p = tile - 1;;) {
+                const unsigned long long f = __ldcg(&state[p]);             // from L2, where the writers publish
+                if ((f & 3ull) == 0) {
+                    if (t0 == 0) t0 = scan_clock_ns();
+                    else if (scan_clock_ns() - t0 > kScanWaitNs) { atomicOr(err, 64); break; }
+                    continue;
+                }
+                excl += (int64_t)(f >> 2);
+                if (f & 2ull) break;
+                --p;                                                    // tile 0 always publishes a prefix
+                t0 = 0;
+            }
+        }
+        atomicExch(&state[tile], ((unsigned long long)(excl + total) << 2) | 2ull);
+        excl_s = excl;
+        if (tile == n_tiles - 1) *sum = excl + total;
+    }
+    __syncthreads();
+    if (i < n) out[i] = excl_s + inc - v;
+}
+
+// Exclusive scan of in[0..n) into out, total into *sum. n_bound is a host upper bound on n; `state`
+// holds scan_state_words(n_bound) zeroed words (unused for n_bound <= kScanThreads).
+static int64_t scan_state_words(int64_t n_bound) {
+    return (n_bound + kScanThreads - 1) / kScanThreads + 1;
+}
+
 static cudaError_t exclusive_scan(const int64_t *in, int64_t *out, int64_t n_bound, const int64_t *n_dev,
-                                  int64_t *partial, int64_t *sum, cudaStream_t st) {
+                                  unsigned long long *state, int64_t *sum, int32_t *err, cudaStream_t st) {
+    count_launch(1);
     if (n_bound <= kScanThreads) {
         kvx_scan_single<<<1, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, sum);
-        count_launch(1);
         return cudaGetLastError();
     }
-    const int64_t nb = std::max<int64_t>(1, (n_bound + kScanThreads - 1) / kScanThreads);
-    kvx_scan_local<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, partial);
-    kvx_scan_partials<<<1, kScanThreads, 0, st>>>(partial, nb, sum);
-    kvx_scan_add<<<(unsigned)nb, kScanThreads, 0, st>>>(out, n_bound, n_dev, partial);
-    count_launch(3);
+    const int64_t nb = scan_state_words(n_bound) - 1;
+    kvx_scan_lookback<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, state, nb, sum, err);
     return cudaGetLastError();
 }
 
@@ -552,7 +572,7 @@ struct MatchScratch {
     int64_t *run_start;     // [B] first pushed block of each run
     int64_t *tile_count;    // [B] tiles of each run
     int64_t *tile_start;    // [B] exclusive scan of tile_count
-    int64_t *partial;       // scan partials
+    unsigned long long *scan_state;   // three regions of scan_state_words(B) words: the look-back scans
     int64_t *scalars;       // [8]
     int32_t *err;           // [4] error bits
 };
@@ -930,7 +950,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         if (n_pub < 0) { delete pl; return fail(KVX_EINVAL, "rem_off is not a CSR offset array"); }
     }
     const int64_t B = std::max<int64_t>(n_pub, 1);
-    const int64_t n_part = std::max<int64_t>(1, (std::max<int64_t>(B, n_sessions) + kScanThreads - 1) / kScanThreads);
+    const int64_t n_state = scan_state_words(B);
 
     // scratch, one allocation
     size_t off = 0;
@@ -939,7 +959,9 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     const size_t o_ps = take(8 * B), o_pd = take(8 * B), o_flag = take(8 * B), o_ridx = take(8 * B);
     const size_t o_rstart = take(8 * B), o_tcount = take(8 * B), o_tstart = take(8 * B);
     // scalars [8] and error words [4] side by side: one memset, one read-back
-    const size_t o_part = take(8 * n_part), o_scal = take(8 * 8 + sizeof(int32_t) * 4), o_err = o_scal + 8 * 8;
+    // scalars [8] and error words [4] side by side, then the scans' look-back state: one memset
+    const size_t o_scal = take(8 * 8 + sizeof(int32_t) * 4 + 8 * 3 * n_state), o_err = o_scal + 8 * 8;
+    const size_t o_state = o_err + sizeof(int32_t) * 4;
     // hole filling: residency per published block, pull flags, their scan, each pair's session
     const size_t o_res = fill ? take(B) : 0, o_need = fill ? take(8 * B) : 0, o_npos = fill ? take(8 * B) : 0;
     const size_t o_psess = fill ? take(8 * B) : 0;
@@ -957,7 +979,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     m.run_start = reinterpret_cast<int64_t *>(sb + o_rstart);
     m.tile_count = reinterpret_cast<int64_t *>(sb + o_tcount);
     m.tile_start = reinterpret_cast<int64_t *>(sb + o_tstart);
-    m.partial = reinterpret_cast<int64_t *>(sb + o_part);
+    m.scan_state = reinterpret_cast<unsigned long long *>(sb + o_state);
     m.scalars = reinterpret_cast<int64_t *>(sb + o_scal);
     m.err = reinterpret_cast<int32_t *>(sb + o_err);
     int32_t *rows = nullptr;   // the plan's run slots (src rows, dst rows, tokens), in its device block
@@ -974,7 +996,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     };
     auto ok = [&](cudaError_t x) { if (x != cudaSuccess && e == cudaSuccess) e = x; };
 
-    ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8 + sizeof(int32_t) * 4, stream));
+    ok(cudaMemsetAsync(m.scalars, 0, sizeof(int64_t) * 8 + sizeof(int32_t) * 4 + 8 * 3 * n_state, stream));
     count_launch();
     if (fill) ok(cudaMemsetAsync(mf.resident, 1, (size_t)B, stream));   // unmarked blocks are never pulled
     kvx_match_sessions<<<(unsigned)max(n_sessions, 1), kMatchThreads, 0, stream>>>(tokens, tok_off, n_sessions, block_size,
@@ -1046,7 +1068,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
             count_launch(3);
             kvx_need_flags<<<grid_for(B, 256), 256, 0, stream>>>(out, rem_off, n_sessions, n_pub, mf.resident, need);
             ok(cudaGetLastError());
-            ok(exclusive_scan(need, npos, B, nullptr, m.partial, &m.scalars[5], stream));
+            ok(exclusive_scan(need, npos, B, nullptr, m.scan_state, &m.scalars[5], m.err, stream));
             kvx_emit_pairs_holes<<<grid_for(B, 256), 256, 0, stream>>>(need, npos, &m.scalars[4], remote_blk, rem_off,
                                                                        n_sessions, n_pub, free_blocks, m.pair_src,
                                                                        m.pair_dst, pair_sess, &m.scalars[5],
@@ -1056,12 +1078,13 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                                                                 m.flag);
         }
         ok(cudaGetLastError());
-        ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.partial, &m.scalars[1], stream));
+        ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.scan_state + n_state, &m.scalars[1], m.err, stream));
         kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start);
         ok(cudaGetLastError());
         kvx_run_tiles<<<grid_for(B, 256), 256, 0, stream>>>(m.run_start, m.scalars, sh, m.tile_count);
         ok(cudaGetLastError());
-        ok(exclusive_scan(m.tile_count, m.tile_start, B, &m.scalars[1], m.partial, &m.scalars[2], stream));
+        ok(exclusive_scan(m.tile_count, m.tile_start, B, &m.scalars[1], m.scan_state + 2 * n_state, &m.scalars[2],
+                          m.err, stream));
         kvx_emit_tiles<<<grid_for(B, 128), 128, 0, stream>>>(m.run_start, m.tile_start, m.scalars, m.pair_src,
                                                              m.pair_dst, sh, tiles, tile_cap, rows, rows + B,
                                                              rows + 2 * B, m.err);
@@ -1073,6 +1096,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     const int64_t *h_scal = back.scal;
     const int32_t h_err = back.err[0];
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "kvx_match_prefix"));
+    if (h_err & 64) return cleanup(fail(KVX_ETIMEDOUT, "a plan scan waited past its bound for an earlier tile"));
     if (h_err & ~8) return cleanup(fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err));
     if (h_err & 8)
         return cleanup(fail(KVX_ENOMEM, "pushing sessions need %lld blocks, free list has %lld", (long long)h_scal[0],
@@ -1108,7 +1132,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
 // allow no device allocation on the request path afterwards: a cudaMalloc there can fail once the
 // pools are carved out, and cudaMalloc / cudaFree may synchronise the device and stall every other
 // stream. kvx_match_prefix_static serves such callers. Its scratch (per-session pushed-block
-// counts, their exclusive scan, scan partials, totals and error bits) is the file-scope array
+// counts, their exclusive scan, totals and error bits) is the file-scope array
 // below, sized for at most kStaticMaxSessions sessions per call (about 1 MiB, held by every GPU
 // that loads the library until the process exits).
 // ------------------------------------------------------------------------------------------------
