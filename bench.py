@@ -64,8 +64,9 @@ def parse():
     p.add_argument("--fixture-iters", type=int, default=2000)
     p.add_argument("--fixture-graph", action="store_true",
                    help="replay the prefill fixture from one CUDA graph per step instead of launching it layer by layer")
-    p.add_argument("--timing-every", type=int, default=1,
-                   help="time the pushes of every n-th timed step only (1: every step)")
+    p.add_argument("--timing-every", type=int, default=4,
+                   help="time the pushes of every n-th timed step only (1: every step; reading the stamps "
+                        "back costs the host about 25 us per timed step)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-match", action="store_true")
