@@ -788,6 +788,15 @@ def run_match(torch, kvx, device, push_opts=None):
         if i < n_calls - 1:
             kvx.kvx_plan_destroy(plan)
     res = out.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
+    # the hole-filling variant (resident blocks anywhere in the remote prefix are reused), decisions only
+    out2 = torch.empty_like(out)
+    holes_ms = []
+    for i in range(n_calls):
+        t = time.perf_counter()
+        kvx.kvx_match_prefix(tokens, tok_off, w.n_sessions, 64, table, hashes, rblk, rem_off, w.threshold, free,
+                             len(w.free_blocks), sp, dp, out2, want_plan=False, flags=kvx.KVX_MATCH_FILL_HOLES)
+        holes_ms.append((time.perf_counter() - t) * 1e3)
+    res_holes = out2.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
     info = kvx.kvx_plan_get_info(plan)
     side = torch.cuda.Stream()
     kvx.kvx_plan_set_opts(plan, dict(push_opts or {}, flags=kvx.KVX_PLAN_TIMING))
@@ -809,6 +818,8 @@ def run_match(torch, kvx, device, push_opts=None):
         "sessions_per_s": round(w.n_sessions / (m_ms * 1e-3), 1),
         "block_compares_per_s": round(compares / (m_ms * 1e-3), 1),
         "match_ms": round(m_ms, 3), "match_and_plan_ms": round(statistics.median(plan_ms[1:]), 3),
+        "match_fill_holes_ms": round(statistics.median(holes_ms[1:]), 3),
+        "fill_holes_push_blocks": int(res_holes["missing_tokens"].sum() // 64),
         "hash_only_ms": round(statistics.median(hash_ms[1:]), 3),
         "publish_turn_ms": round(turn_ms, 3), "publish_turn_blocks": turn_blocks,
         "hashed_blocks": n_pub, "pushing_sessions": int(res["push"].sum()),
