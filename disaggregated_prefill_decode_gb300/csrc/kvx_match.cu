@@ -240,8 +240,8 @@ __device__ __forceinline__ uint64_t block_hash(uint64_t parent, const uint32_t *
 }
 
 // ------------------------------------------------------------------------------------------------
-// Scans: warp shuffles inside a warp, warp totals through shared memory, block totals through a
-// second level (reduce-then-scan over 1024-element blocks).
+// Scans: warp shuffles inside a warp, warp totals through shared memory; across blocks a single
+// pass that looks back over the earlier tiles (kvx_scan_lookback, below).
 // ------------------------------------------------------------------------------------------------
 
 constexpr int kScanThreads = 1024;
@@ -1132,8 +1132,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
 // allow no device allocation on the request path afterwards: a cudaMalloc there can fail once the
 // pools are carved out, and cudaMalloc / cudaFree may synchronise the device and stall every other
 // stream. kvx_match_prefix_static serves such callers. Its scratch (per-session pushed-block
-// counts, their exclusive scan, totals and error bits) is the file-scope array
-// below, sized for at most kStaticMaxSessions sessions per call (about 1 MiB, held by every GPU
+// counts, their exclusive scan, totals and error bits) is the file-scope array below, sized for
+// at most kStaticMaxSessions sessions per call (about 1 MiB, held by every GPU
 // that loads the library until the process exits).
 // ------------------------------------------------------------------------------------------------
 
