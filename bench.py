@@ -344,9 +344,10 @@ def measure_overlap(args, torch, kvx, m, steps=200):
     """The pages' premise, measured: is the push off the prefill's critical path? Per step, the
     synthetic prefill alone (the L fixture launches on the priority stream), the pushes alone (the L
     layer pushes, no gate), and both (the benchmark's pattern: each push gated on its layer's event);
-    and how long the prefill chain itself takes inside the combined run. Twice: with the benchmark's
-    fixture (a prefill layer shorter than its push) and with one 8 times longer (a prefill layer longer
-    than its push, the regime of a real model, whose layers take far longer than their KV copy)."""
+    and how long the prefill chain itself takes inside the combined run. Three times: with the
+    benchmark's fixture (a prefill layer shorter than its push), with one 8 times longer (a prefill
+    layer longer than its push, the regime of a real model, whose layers take far longer than their KV
+    copy), and with layers of tensor-core work (one bf16 GEMM each) instead of the ALU fixture."""
     L, reqs, sp, dp = m["L"], m["reqs"], m["sp"], m["dp"]
     opts = m["opts"]
     lib = kvx._lib
@@ -358,6 +359,13 @@ def measure_overlap(args, torch, kvx, m, steps=200):
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
 
+    # a prefill layer made of tensor-core work instead of the ALU fixture: one bf16 GEMM of the
+    # layer's 8192 tokens by a 5120 x 5120 weight (a Qwen3-32B attention projection)
+    gemm = [torch.randn(8192, 5120, dtype=torch.bfloat16, device=main.device),
+            torch.randn(5120, 5120, dtype=torch.bfloat16, device=main.device)]
+    gemm.append(torch.empty(8192, 5120, dtype=torch.bfloat16, device=main.device))
+    torch.cuda.synchronize()
+
     def run(prefill, push, n, iters):
         prev, marks = None, []
         for _ in range(n):
@@ -365,7 +373,11 @@ def measure_overlap(args, torch, kvx, m, steps=200):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             for layer in range(L):
-                if prefill:
+                if prefill and iters < 0:
+                    with torch.cuda.stream(main):
+                        torch.matmul(gemm[0], gemm[1], out=gemm[2])
+                        ready[layer].record(main)
+                elif prefill:
                     lib.kvx_fixture_prefill(args.fixture_ctas, iters, None, 0, layer, main_h, ready_h[layer])
                 if push:
                     lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer] if prefill else None)
@@ -380,31 +392,34 @@ def measure_overlap(args, torch, kvx, m, steps=200):
             kvx.kvx_plan_destroy(prev)
         return marks
 
-    def timed(prefill, push, iters):
+    def timed(prefill, push, iters, n_steps=steps):
         run(prefill, push, 3, iters)
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(main)
-        marks = run(prefill, push, steps, iters)
+        marks = run(prefill, push, n_steps, iters)
         main.wait_stream(side)
         t1.record(main)
         torch.cuda.synchronize()
         chain = statistics.median(a.elapsed_time(b) for a, b in marks) if prefill else None
-        return t0.elapsed_time(t1) / steps, chain
+        return t0.elapsed_time(t1) / n_steps, chain
 
     push_only, _ = timed(False, True, 0)
     out = {"push_only_ms_per_step": round(push_only, 4)}
-    for name, iters in (("short_prefill", args.fixture_iters), ("long_prefill", 8 * args.fixture_iters)):
-        pre_only, chain_alone = timed(True, False, iters)
-        both, chain_with = timed(True, True, iters)
-        out[name] = {"fixture_iters": iters, "prefill_only_ms_per_step": round(pre_only, 4),
+    for name, iters in (("short_prefill", args.fixture_iters), ("long_prefill", 8 * args.fixture_iters),
+                        ("gemm_prefill", -1)):
+        pre_only, chain_alone = timed(True, False, iters, 50 if iters < 0 else steps)
+        both, chain_with = timed(True, True, iters, 50 if iters < 0 else steps)
+        out[name] = {"fixture_iters": iters if iters >= 0 else "bf16 GEMM 8192 x 5120 x 5120 per layer",
+                     "prefill_only_ms_per_step": round(pre_only, 4),
                      "together_ms_per_step": round(both, 4),
                      "hidden_frac": round((pre_only + push_only - both) / min(pre_only, push_only), 3),
                      "prefill_chain_ms_alone": round(chain_alone, 4),
                      "prefill_chain_ms_with_push": round(chain_with, 4),
                      "prefill_slowdown": round(chain_with / chain_alone - 1, 4)}
-    out["how"] = (f"{steps} steps each; the prefill chain is the median time on its stream from a step's first "
-                  "fixture to its last; hidden_frac = (prefill + push - together) / min(prefill, push)")
+    out["how"] = (f"{steps} steps each ({50} with the GEMM prefill); the prefill chain is the median time on its "
+                  "stream from a step's first layer to its last; hidden_frac = (prefill + push - together) / "
+                  "min(prefill, push)")
     return out
 
 
