@@ -18,6 +18,13 @@ is the union of all timed launches on that one device clock / launches.
 e2e = the same metric with the producer KV starting in pinned host memory and the pushed consumer
 blocks gathered on the device and read back every step (per-layer copies overlapped with the pushes).
 
+Also reported: per_config (the batched, remap, head-major and token-major -> head-major workloads,
+the batched one also as a single kvx_push_layers call per step), overlap (the push beside a short
+ALU prefill, a long one and a tensor-core GEMM prefill), match (block hashing, full and incremental;
+the prefix-match decision with and without hole filling; the device-built pull plan and one layer
+of its push), connector (requests per second through the host protocol), memcpy_ceiling and
+cpu_baseline.
+
 --impl reference times the CPU oracle instead (rank 0 only), on bounded samples of the same workload.
 """
 from __future__ import annotations
