@@ -243,14 +243,16 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
  * layers_per_launch layers each, on successive lanes, every one ordered after `stream` and `ready`
  * (measured on GB300: one launch for 64 layers of a 496 MB-per-layer batch reached 0.96-0.99 of the
  * copy peak, launches of about 256 MiB or one layer each 1.02-1.03, the heads of later launches
- * filling the tails of earlier ones); with lanes = 1 in one launch on `stream`.
+ * filling the tails of earlier ones); with lanes = 1 on `stream`, in one launch unless
+ * layers_per_launch asks for more.
  */
 kvx_status kvx_push_layer(kvx_plan_t plan, int32_t layer, cudaStream_t stream, cudaEvent_t ready);
 kvx_status kvx_push_layers(kvx_plan_t plan, int32_t layer_begin, int32_t layer_end, cudaStream_t stream,
                            cudaEvent_t ready);
 
 /* The same, and `done` (the caller's event, not NULL) is recorded right after the copy, on the
- * stream that runs it: a per-push completion notification ([P1] "Implementierungsdetails", step 3:
+ * stream that runs it (after every launch of a multi-layer push, the last one's lane first waiting
+ * for the others): a per-push completion notification ([P1] "Implementierungsdetails", step 3:
  * each write carries a completion notification). A consumer stream can wait on it before reading
  * the layer; kvx_sync still reports failures. */
 kvx_status kvx_push_layer_notify(kvx_plan_t plan, int32_t layer_begin, int32_t layer_end, cudaStream_t stream,
