@@ -288,6 +288,29 @@ def test_match_plan_and_push_reduced():
     c.close()
 
 
+def test_match_plan_pushed_as_multi_layer_launches():
+    """A device-built pull plan pushed with kvx_push_layers in launches of two layers each (the last
+    launch one layer) equals the oracle on every layer."""
+    w = kvx_inputs.bidir_mla_fp8(seed=27, n_sessions=12, n_layers=5, system_tokens=256, hist_range=(64, 2000),
+                                 resident_p=0.5, threshold=128)
+    c = Case(w, flip_frac=0.005, seed=6)
+    want = c.oracle_match()
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=8)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    kvx.kvx_plan_set_opts(plan, {"layers_per_launch": 2, "flags": kvx.KVX_PLAN_TIMING})
+    n0 = kvx.kvx_launch_count()
+    kvx.kvx_push_layers(plan, 0, 5, torch.cuda.Stream())
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    assert kvx.kvx_launch_count() - n0 == 3 and len(kvx.kvx_plan_push_times_ns(plan)[0]) == 3
+    check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")],
+                 oracle_requests(c, want), range(5))
+    kvx.kvx_plan_destroy(plan)
+    c.close()
+
+
 PULL_LAYOUTS = {
     # name: (decode side, prefill side) as (shards, heads per shard, layout); 8 heads of 128 bf16 each
     "hnd_same": ((1, 8, 1), (1, 8, 1)),

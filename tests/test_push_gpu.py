@@ -144,6 +144,21 @@ def test_push_layers_split_into_launches(opts, launches):
     kvx.kvx_plan_destroy(plan)
 
 
+def test_head_major_pool_in_pinned_host_memory():
+    """A head-major consumer pool in pinned host memory, fed from a token-major device pool: head-group
+    tiles written over the chip-to-chip link with plain stores, byte for byte against the oracle."""
+    w = kvx_inputs.qwen3_32b_batched_nhd_to_hnd(n_layers=2)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    dst = [b.cpu().pin_memory() for b in dst]
+    plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
+    assert push_all_layers(plan, 2) == kvx.KVX_OK
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_PERSIST
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(2))
+    kvx.kvx_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("side", ["src", "dst"])
 @pytest.mark.parametrize("kernel", ["auto", "bulk"])
 def test_pool_in_pinned_host_memory(side, kernel):
