@@ -47,6 +47,12 @@ MUTANTS = [
      "if (p->layout == 1) return (blk * p->block_size + slot) * p->heads_per_shard + head;"),
     ("hnd_slot_head_swapped", "if (p->layout == 1) return (blk * p->heads_per_shard + head) * p->block_size + slot;",
      "if (p->layout == 1) return (blk * p->heads_per_shard + slot) * p->block_size + head;"),
+    ("dst_block_from_src_bs", "int64_t dblk = dst_ids[r][t / dst->block_size];",
+     "int64_t dblk = dst_ids[r][t / src->block_size];"),
+    ("dst_head_is_src_head", "int32_t dh = g % dst->heads_per_shard;", "int32_t dh = h;"),
+    ("global_head_from_dst_split", "int32_t g = s * src->heads_per_shard + h;", "int32_t g = s * dst->heads_per_shard + h;"),
+    ("src_plane_dropped", "src->base[((int64_t)l * src->n_planes + p) * src->n_shards + s]",
+     "src->base[((int64_t)l * src->n_planes) * src->n_shards + s]"),
 ]
 
 CHILD = r"""
