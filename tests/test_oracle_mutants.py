@@ -53,6 +53,12 @@ MUTANTS = [
     ("global_head_from_dst_split", "int32_t g = s * src->heads_per_shard + h;", "int32_t g = s * dst->heads_per_shard + h;"),
     ("src_plane_dropped", "src->base[((int64_t)l * src->n_planes + p) * src->n_shards + s]",
      "src->base[((int64_t)l * src->n_planes) * src->n_shards + s]"),
+    ("remote_span_counts_all_matches",
+     "while (l_rem < n_full && l_rem < n_rem && h[l_rem] == remote_hash[rem_off[s] + l_rem]) ++l_rem;",
+     "for (int64_t q = 0; q < n_full && q < n_rem; ++q) l_rem += h[q] == remote_hash[rem_off[s] + q];"),
+    ("remote_span_ignores_published_count", "while (l_rem < n_full && l_rem < n_rem && h[l_rem]",
+     "while (l_rem < n_full && h[l_rem]"),
+    ("dst_start_session_index", "cursor += out_missing[s] / block_size;", "cursor += 1;"),
 ]
 
 CHILD = r"""
