@@ -456,8 +456,32 @@ def connector_rate(kvx, n=20000):
     dt = time.perf_counter() - t0
     kvx.kvx_conn_destroy(conn)
     return {"requests_per_s": round(n / dt, 1), "calls_per_request": 10,
+            "native_requests_per_s": connector_rate_native(),
             "how": f"{n} requests through the Python binding, one host thread: the figure is mostly the "
-                   "binding's per-call cost (about 4 us a call), not the native state machine's"}
+                   "binding's per-call cost (about 4 us a call); native_requests_per_s is the same protocol "
+                   "driven from C (tests/c/kvx_conn_rate.c, built with gcc here), 200000 requests"}
+
+
+def connector_rate_native():
+    """The connector's protocol driven from plain C against libkvx.so; None when no C compiler."""
+    import shutil
+    import tempfile
+    if not shutil.which("gcc"):
+        return None
+    pkg = os.path.join(ROOT, "disaggregated_prefill_decode_gb300")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "kvx_conn_rate")
+        r = subprocess.run(["gcc", "-std=c11", "-O2", os.path.join(ROOT, "tests", "c", "kvx_conn_rate.c"), "-o", exe,
+                            "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"), "-L", pkg, "-lkvx",
+                            "-L", os.path.join(cuda, "lib64"), "-lcudart",
+                            f"-Wl,-rpath,{pkg}:{os.path.join(cuda, 'lib64')}"], capture_output=True, text=True)
+        if r.returncode != 0:
+            return None
+        r = subprocess.run([exe, "200000"], capture_output=True, text=True, timeout=120)
+        if r.returncode != 0:
+            return None
+        return round(float(r.stdout.split()[-1]), 1)
 
 
 KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"]
