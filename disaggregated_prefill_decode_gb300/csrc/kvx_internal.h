@@ -75,6 +75,9 @@ constexpr int32_t kTimingSlots = 4096;
 // Bytes moved (read + write) one launch of a multi-layer push aims at when it is split over lanes.
 constexpr int64_t kLaunchTargetBytes = (int64_t)256 << 20;
 
+// Bulk copy launches that read at least this many bytes mark what they touch evict-first in L2.
+constexpr int64_t kStreamL2Bytes = (int64_t)8 << 20;
+
 // Head-shard pair: the contiguous head range one producer shard shares with one consumer shard, as
 // byte offsets inside a producer row and a consumer row.
 struct Pair { int32_t s, d; int64_t src_seg_off, dst_seg_off; };

@@ -117,9 +117,9 @@ typedef struct kvx_plan_opts {
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
                                  limit (0: for launches that read under 128 MiB 5 CTAs per 4 SMs
-                                 with BULK and 2 per SM with PERSIST, leaving room for the
-                                 caller's compute and an overlapping push; the occupancy limit
-                                 for larger launches) */
+                                 with BULK and 2 per SM with PERSIST (4 for head-group tiles),
+                                 leaving room for the caller's compute and an overlapping push;
+                                 the occupancy limit for larger launches) */
     int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
     int32_t bulk_stages;      /* BULK: shared-memory ring stages of tile_bytes each, one of 2, 3, 4,
                                  6, 8 with stages * tile_bytes <= 192 KiB (0: 4 for contiguous
@@ -135,9 +135,13 @@ typedef struct kvx_plan_opts {
  * asynchronous copy engine (global -> shared -> global through a ring of mbarrier-tracked stages;
  * strided tiles move row by row on a side whose rows are not adjacent); plans whose buffer bases,
  * offsets, widths and pitches are all 16-byte aligned, with a row no larger than tile_bytes; others
- * fall back to PERSIST. AUTO picks BULK where it applies to a plan that reads under 128 MiB per layer
- * (about one CTA per SM, leaving room for the caller's compute and the next push) and PERSIST with 128
- * threads per CTA otherwise (measured fastest on GB300 for large layer pushes). */
+ * fall back to PERSIST. Contiguous BULK launches that read at least 8 MiB mark the lines they touch
+ * evict-first in L2 (a cache hint only; the bytes copied are the same). AUTO picks BULK where it
+ * applies to a plan that reads under 128 MiB per layer (about one CTA per SM, leaving room for the
+ * caller's compute and the next push) and PERSIST with 128 threads per CTA otherwise (measured
+ * fastest on GB300 for large layer pushes); plans with one token-major and one head-major side, or
+ * two head-major sides with different block sizes or head splits, take PERSIST at any size (their
+ * tiles are many short rows). */
 #define KVX_KERNEL_AUTO 0
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2

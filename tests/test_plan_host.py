@@ -126,6 +126,16 @@ def test_head_major_plans_group_heads_per_tile():
     tiles = kvx.kvx_plan_tiles(plan)
     assert info["src_head_pitch"] == 256 and info["dst_head_pitch"] == 16 * 256
     assert len(tiles) == 10 * 2 and (tiles["heads"] == 4).all() and (tiles["n"] == 16).all()
+    # head-group tiles run the persistent kernel unless another is asked for; equal head-major
+    # layouts copy whole blocks and keep the bulk kernel
+    assert info["kernel"] == kvx.KVX_KERNEL_PERSIST
+    kvx.kvx_plan_destroy(plan)
+    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"tile_bytes": 16384, "kernel": kvx.KVX_KERNEL_BULK})
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
+    kvx.kvx_plan_destroy(plan)
+    hp, hq = pools(dg, dg)
+    plan = kvx.kvx_plan(hp, hq, reqs)
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
     kvx.kvx_plan_destroy(plan)
 
 
