@@ -230,8 +230,8 @@ bool as_whole_block_copy(kvx_plan_s *pl) {
 // per SM (it leaves room for the caller's compute and the next push), a larger one with the persistent
 // kernel at 128 threads per CTA and the occupancy limit of CTAs (many small independent CTAs). Plans
 // that map one head layout onto another (head-group tiles: dozens of row copies per tile, too many for
-// one issuing thread) take the persistent kernel at any size: 32 MiB-per-layer pushes of fragmented
-// requests ran at 0.78-0.79 of the copy peak against 0.59-0.64 with the bulk kernel. Two head-major
+// one issuing thread) take the persistent kernel at 128 threads per CTA at any size: 32 MiB-per-layer
+// pushes ran at 0.81 of the copy peak (256 threads 0.78-0.80) against 0.59-0.64 with the bulk kernel. Two head-major
 // sides alike copy whole blocks as single spans and keep the bulk kernel (0.94-0.95 against 0.76).
 constexpr int64_t kLargeLayer = (int64_t)128 << 20;
 
@@ -244,7 +244,7 @@ static void resolve_kernel(kvx_plan_s *pl) {
     int32_t k = automatic ? (bulk_ok && !large && !row_groups ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
     if (k == KVX_KERNEL_BULK && !bulk_ok) k = KVX_KERNEL_PERSIST;
     pl->kernel = k;
-    pl->threads = pl->threads_req ? pl->threads_req : (automatic && large ? 128 : 256);
+    pl->threads = pl->threads_req ? pl->threads_req : (automatic && (large || row_groups) ? 128 : 256);
 }
 
 // Default ring depth: measured on GB300, strided tiles (rows scattered on one side) run fastest with

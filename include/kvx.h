@@ -112,7 +112,8 @@ typedef struct kvx_plan_opts {
                                  (min block size x row bytes) split into the fewest equal tiles
                                  of at most 16384 bytes, or whole units packed up to 16384     */
     int32_t threads;          /* threads per CTA of TILE / PERSIST (multiple of 32, <= 1024;
-                                 default 256, or 128 where AUTO picks PERSIST for a large push) */
+                                 default 256, or 128 where AUTO picks PERSIST for a large push
+                                 or a head-group plan) */
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
