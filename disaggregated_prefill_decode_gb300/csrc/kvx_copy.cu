@@ -487,9 +487,10 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     if (sh.kernel == KVX_KERNEL_BULK) {
         // Launches that read under 128 MiB (a layer push) default to 5 CTAs per 4 SMs: measured on
         // GB300 in the per-layer push pattern, 1.25 CTAs per SM beat 1 (0.965 against 0.949 of the
-        // copy peak, consecutive launches overlapping on the lanes) and 2 (0.90). Head-group tiles,
-        // whose rows go out one bulk copy each, default to 2 per SM (0.947 against 0.890 at 1.25).
-        // Larger launches take the occupancy limit.
+        // copy peak, consecutive launches overlapping on the lanes) and 2 (0.90). Head-group plans
+        // (bulk only when asked for, or two head-major pools alike) default to 2 per SM: row-by-row
+        // copies leave one issuing thread per CTA busier (0.59 against 0.50 at 1 per SM on a
+        // token-major -> head-major push). Larger launches take the occupancy limit.
         const int smem = sh.stages * sh.tile_bytes;
         const bool small = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20);
         const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (small ? 2 : 64);
