@@ -63,6 +63,21 @@ struct Geom {
     int32_t n_buffers() const { return n_layers * n_planes * n_shards; }
 };
 
+// Makes `device` current for a scope and restores the caller's device after it; nothing happens
+// for -1 or when that device is already current.
+struct DeviceScope {
+    int prev = -1;
+    explicit DeviceScope(int device) {
+        if (device < 0 || cudaGetDevice(&prev) != cudaSuccess || prev == device || cudaSetDevice(device) != cudaSuccess)
+            prev = -1;
+    }
+    ~DeviceScope() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+};
+
 struct PendingPush {
     cudaEvent_t done;
     int32_t slot;           // timing plans: index of its global-timer stamps, -1 when not timed
@@ -163,6 +178,7 @@ struct kvx_plan_s {
     int64_t device_tokens = 0;                 // device-built plans: tokens copied per (layer, plane, shard)
     std::vector<uint8_t> upload_img;           // host image of the uploaded descriptor bytes
     bool uploaded = false;
+    int32_t device = -1;                       // device of the descriptors, set when they are uploaded
     bool device_built = false;                 // descriptors were written on the device
     cudaEvent_t upload_evt = nullptr;
     cudaStream_t upload_stream = nullptr;

@@ -784,6 +784,7 @@ struct kvx_table_s {
     int32_t shift = 0;
     int64_t n = 0;
     cudaEvent_t last_use = nullptr;   // recorded after each lookup; destroy waits for it
+    int32_t device = -1;              // device of the table, current while it is destroyed
     TableView view() const { return TableView{keys, vals, hdr, capacity - 1, shift}; }
 };
 
@@ -836,6 +837,7 @@ kvx_status kvx_table_build(const uint64_t *keys, const int32_t *vals, int64_t n,
     const size_t off_vals = align_up(sizeof(uint64_t) * cap, 256);
     const size_t off_hdr = off_vals + align_up(sizeof(int32_t) * cap, 256);
     const size_t bytes = off_hdr + 256;
+    if (cudaGetDevice(&t->device) != cudaSuccess) t->device = -1;
     kvx_status st = pool_alloc(&t->dev, bytes, stream);
     if (st) { delete t; return st; }
     t->keys = static_cast<uint64_t *>(t->dev);
@@ -872,6 +874,7 @@ kvx_status kvx_table_lookup(kvx_table_t t, const uint64_t *keys, int64_t n, int3
 
 kvx_status kvx_table_destroy(kvx_table_t t) {
     if (!t) return KVX_OK;
+    const DeviceScope on_device(t->device);
     cudaError_t e = cudaSuccess;
     if (t->last_use) {
         e = cudaEventSynchronize(t->last_use);
@@ -1115,6 +1118,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
         e = cudaEventRecord(pl->upload_evt, stream);
         if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventRecord(plan)"));
         pl->upload_stream = stream;
+        e = cudaGetDevice(&pl->device);
+        if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaGetDevice"));
         pl->uploaded = true;
         *out_plan = pl;
         pl = nullptr;

@@ -225,9 +225,13 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     e = cudaEventRecord(pl->upload_evt, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(upload)");
     pl->upload_stream = stream;
+    e = cudaGetDevice(&pl->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     pl->uploaded = true;
     return KVX_OK;
 }
+
+
 
 // Stamp slots of a timing plan: kTimingSlots starts (set to all ones, folded with atomicMin) then
 // kTimingSlots ends (zero, folded with atomicMax), allocated and set on `stream` at the first timed push.
@@ -395,6 +399,7 @@ kvx_status kvx_push_layer(kvx_plan_t pl, int32_t layer, cudaStream_t stream, cud
 
 kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {
     if (!pl) return fail(KVX_EINVAL, "NULL plan");
+    const DeviceScope on_device(pl->device);   // read-backs, the event pool and frees of the plan's device
     const size_t sealed = pl->pending.size();   // pushes issued so far
     if (sealed == 0) {
         for (int32_t s : pl->layer_state)
@@ -484,6 +489,7 @@ kvx_status kvx_sync(kvx_plan_t pl, int64_t timeout_us) {
 
 kvx_status kvx_plan_destroy(kvx_plan_t pl) {
     if (!pl) return KVX_OK;
+    const DeviceScope on_device(pl->device);   // read-backs, the event pool and frees of the plan's device
     kvx_status st = KVX_OK;
     for (const PendingPush &p : pl->pending) {
         cudaError_t e = cudaEventSynchronize(p.done);

@@ -294,7 +294,10 @@ kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers
  * device but is reported FAILED by kvx_sync. */
 kvx_status kvx_plan_inject_failure(kvx_plan_t plan, int32_t layer);
 
-/* Waits for any pending push, then frees the plan and its device descriptors. NULL is a no-op. */
+/* Waits for any pending push, then frees the plan and its device descriptors. NULL is a no-op.
+ * kvx_sync and kvx_plan_destroy make the plan's device (current at its first push, or at
+ * kvx_match_prefix for a device-built plan) current while they run and restore the caller's;
+ * kvx_table_destroy does the same with the device current at kvx_table_build. */
 kvx_status kvx_plan_destroy(kvx_plan_t plan);
 
 const char *kvx_status_str(kvx_status status);
