@@ -137,6 +137,15 @@ def test_head_major_plans_group_heads_per_tile():
     plan = kvx.kvx_plan(hp, hq, reqs)
     assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
     kvx.kvx_plan_destroy(plan)
+    # head-major -> token-major, and head-major pools of different block sizes: head groups again
+    for a, b in ((dg, sg), (dg, dg.replace(block_size=32, n_blocks=32))):
+        ap, bp = pools(a, b)
+        nd = 16 * 10 // b.block_size
+        rq = [(16 * 10, np.arange(10, dtype=np.int32), np.arange(10, 10 + nd, dtype=np.int32))]
+        plan = kvx.kvx_plan(ap, bp, rq)
+        i = kvx.kvx_plan_get_info(plan)
+        assert (i["kernel"], i["threads"]) == (kvx.KVX_KERNEL_PERSIST, 128)
+        kvx.kvx_plan_destroy(plan)
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
