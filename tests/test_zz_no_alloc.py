@@ -2,10 +2,12 @@
 request path (serving engines that hand nearly all free HBM to their KV pools at start-up, where a
 later allocation can fail and cudaMalloc / cudaFree can stall the other streams).
 
-Through the C-ABI, the allocation-free entry point must give exactly the decisions of
-kvx_match_prefix (integers: bit-exact) on two calls in a row, since both calls share one fixed
-scratch array that keeps the previous call's contents. This file sorts last so that a run stopping
-at its first failure has already run every other test; it also passes alone in a fresh process."""
+Through the C-ABI, the allocation-free entry point must give exactly the decisions of the oracle
+(integers: bit-exact, field by field) and of kvx_match_prefix, on two calls in a row, since both
+calls share one fixed scratch array that keeps the previous call's contents. The two entry points
+launch the same match kernel, so the oracle is the checker that a fault they share cannot pass.
+This file sorts last so that a run stopping at its first failure has already run every other test;
+it also passes alone in a fresh process."""
 import numpy as np
 import pytest
 
@@ -35,7 +37,20 @@ def workload(seed, n_sessions, threshold):
     remote[flip] ^= np.uint64(1)
     keys = np.unique(hs[w.resident])
     table = kvx.kvx_table_build(dev(keys), dev(np.arange(len(keys), dtype=np.int32)), len(keys))
-    return w, remote, table
+    return w, remote, table, keys
+
+
+def oracle_decisions(w, remote, keys, n_free):
+    """The oracle's decisions, with a free list of n_free blocks (the first n_free of the workload's)."""
+    return oracle.load().match(w.tokens, w.tok_off, 64, keys, remote, w.remote_blk, w.rem_off, w.threshold,
+                               w.free_blocks[:n_free])
+
+
+def assert_matches_oracle(got, want):
+    res = got.view(kvx.MATCH_RESULT_DTYPE)
+    for field, key in (("local_hit_blocks", "local_hit"), ("remote_hit_blocks", "remote_hit"),
+                       ("missing_tokens", "missing"), ("push", "push"), ("dst_start", "dst_start")):
+        assert res[field].tolist() == want[key].tolist(), field
 
 
 def decisions_with_allocation(w, remote, table, n_free):
@@ -56,21 +71,28 @@ def decisions_without_allocation(w, remote, table, n_free):
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")
 def test_static_scratch_matches_allocating_entry_point_twice():
     cases = [workload(31, 40, 256), workload(32, 300, 64)]     # second call: different size, same array
-    for w, remote, table in cases:
+    for w, remote, table, keys in cases:
         n_free = len(w.free_blocks)
+        ref = oracle_decisions(w, remote, keys, n_free)
+        assert ref["status"] == 0
         st_a, want = decisions_with_allocation(w, remote, table, n_free)
         st_b, got = decisions_without_allocation(w, remote, table, n_free)
         assert st_a == st_b == kvx.KVX_OK
+        assert_matches_oracle(got, ref)
         assert np.array_equal(got, want)
         res = got.view(kvx.MATCH_RESULT_DTYPE)
         assert res["push"].sum() > 0 and (res["push"] == 0).sum() > 0
-    # a free list too short for the pushes: same KVX_ENOMEM and the same decisions from both
-    w, remote, table = cases[1]
+    # a free list too short for the pushes: KVX_ENOMEM from both, and the oracle's decisions for that
+    # free list (its status 5: too short; the decisions and dst_start positions are still written)
+    w, remote, table, keys = cases[1]
+    ref = oracle_decisions(w, remote, keys, 5)
+    assert ref["status"] == 5
     st_a, want = decisions_with_allocation(w, remote, table, 5)
     st_b, got = decisions_without_allocation(w, remote, table, 5)
     assert st_a == st_b == kvx.KVX_ENOMEM
+    assert_matches_oracle(got, ref)
     assert np.array_equal(got, want)
-    for _, _, table in cases:
+    for _, _, table, _ in cases:
         kvx.kvx_table_destroy(table)
 
 
