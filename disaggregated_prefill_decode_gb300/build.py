@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvx.so")
 
-SOURCES = ["kvx_plan.cpp", "kvx_tiles.cpp", "kvx_conn.cpp", "kvx_copy.cu", "kvx_push.cu", "kvx_match.cu", "kvx_fixture.cu"]
+SOURCES = ["kvx_plan.cpp", "kvx_tiles.cpp", "kvx_conn.cpp", "kvx_copy.cu", "kvx_push.cu", "kvx_match.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I", INCLUDE, "-I", CSRC]
 

@@ -197,8 +197,6 @@ __global__ void __launch_bounds__(1024) kvx_copy_persist(CopyArgs a, int64_t n_w
 // mbarrier and all stores of a stage forming one bulk group.
 // ------------------------------------------------------------------------------------------------
 
-constexpr uint64_t kBulkWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate tile copy
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar) {
@@ -223,15 +221,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for a stage's phase; false when the deadline passed. Each try_wait already suspends
+// Bounded wait for a stage's phase; false when `limit_ns` passed. Each try_wait already suspends
 // the thread for a while when the phase is not complete; the global timer (a costly special register
 // to read, and issue slots taken from the SM's other warps) is read only every 64 tries.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t k = 1;; ++k) {
         if (mbar_test(bar, parity)) return true;
-        if ((k & 63) == 0 && global_ns() - t0 > kBulkWaitNs) return false;
+        if ((k & 63) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -366,10 +364,23 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     int64_t issued = 0;
     for (; issued < n_mine && issued < kBulkStages - 1; ++issued) issue(issued);
     bool timed_out = false;
+    bool stall = a.stall_layer >= 0 && blockIdx.x == 0;   // testing hook (kvx_plan_inject_stall)
     for (int64_t i = 0; i < n_mine; ++i) {
         const int s = (int)(i % kBulkStages);
-        if (!mbar_wait(&bar[s], (uint32_t)((i / kBulkStages) & 1))) {
-            atomicOr(&a.err[items[s].layer], 2);
+        const uint32_t parity = (uint32_t)((i / kBulkStages) & 1);
+        bool landed = mbar_wait(&bar[s], parity, a.wait_ns);
+        if (landed && stall && items[s].layer == a.stall_layer) {
+            // the hook: after the stage's loads have landed, wait for the stage's next phase, which
+            // nothing arms before this wait ends -- a wait that can only run out, with no copy in flight
+            stall = false;
+            landed = mbar_wait(&bar[s], parity ^ 1u, a.wait_ns);
+        }
+        if (!landed) {
+            // this CTA stops here: every layer of the work it had left (items i .. n_mine - 1, in
+            // layer order) is reported FAILED, not only the layer of the stage it waited for
+            const int32_t per_layer = (int32_t)(a.n_tiles * a.n_planes);
+            const int32_t l_last = a.layer0 + (int32_t)((blockIdx.x + (n_mine - 1) * gridDim.x) / per_layer);
+            for (int32_t l = items[s].layer; l <= l_last; ++l) atomicOr(&a.err[l], 2);
             timed_out = true;
             break;
         }
@@ -402,7 +413,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         // give every load still in flight a bounded chance to land before the ring goes away
         for (int64_t j = 0; j < kBulkStages && j < issued; ++j) {
             const int64_t i = issued - 1 - j;
-            mbar_wait(&bar[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1));
+            mbar_wait(&bar[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1), a.wait_ns);
         }
     }
     bulk_wait_all();   // the stores have completed, not only read their stages

@@ -39,6 +39,8 @@ struct CopyArgs {
     int64_t dst_head_pitch;
     unsigned long long *ts_start;     // timing: atomicMin of %globaltimer at each CTA's start (or null)
     unsigned long long *ts_end;       // timing: atomicMax of %globaltimer at each CTA's end
+    uint64_t wait_ns;                 // bulk: limit of one wait for a ring stage (kBulkWaitNs)
+    int32_t stall_layer;              // bulk, testing hook: this layer's first item on CTA 0 never completes (-1: none)
     int32_t width;                    // strided: bytes copied per row
     int32_t n_planes;
     int32_t src_shards;
@@ -83,6 +85,11 @@ struct PendingPush {
     int32_t slot;           // timing plans: index of its global-timer stamps, -1 when not timed
     int32_t layer_begin, layer_end;
 };
+
+// Bulk kernel: limit of one wait for a ring stage, far beyond any legitimate tile copy; and the
+// limit a push armed by kvx_plan_inject_stall runs with.
+constexpr uint64_t kBulkWaitNs = 2000000000ull;        // 2 s
+constexpr uint64_t kBulkStallWaitNs = 1000000ull;      // 1 ms
 
 // Timing plans: pushes between two syncs that can carry global-timer stamps.
 constexpr int32_t kTimingSlots = 4096;
@@ -192,6 +199,7 @@ struct kvx_plan_s {
     std::vector<int32_t> layer_state;          // kvx_layer_state per layer
     std::vector<uint8_t> inject;               // host fault injection armed, per layer
     std::vector<uint8_t> injected_pending;     // injected failure waiting for sync, per layer
+    std::vector<uint8_t> stall;                // kvx_plan_inject_stall armed, per layer
 };
 
 namespace kvx {

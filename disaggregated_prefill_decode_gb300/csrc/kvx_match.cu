@@ -1154,7 +1154,9 @@ constexpr size_t kStaticBytes = kStaticErrOff + sizeof(int32_t) * 4;
 static __device__ __align__(256) unsigned char g_match_scratch[kStaticBytes];
 
 // In host code g_match_scratch names a host-side stand-in, not device memory: the device address
-// is looked up once per device (with that device current) and cached.
+// is looked up once per device (with that device current) and cached. The cache lives as long as
+// the device's primary context; like the library's other per-device state (lanes, memory pool,
+// events) it does not survive a device reset, which the header states.
 static std::mutex g_static_mu;
 static std::map<int, unsigned char *> g_static_addr;
 

@@ -132,6 +132,7 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
     pl->layer_state.assign(s.n_layers, KVX_LAYER_IDLE);
     pl->inject.assign(s.n_layers, 0);
     pl->injected_pending.assign(s.n_layers, 0);
+    pl->stall.assign(s.n_layers, 0);
     return KVX_OK;
 }
 
@@ -338,6 +339,15 @@ kvx_status kvx_plan_inject_failure(kvx_plan_t pl, int32_t layer) {
     if (!pl) return fail(KVX_EINVAL, "NULL plan");
     if (layer < 0 || layer >= pl->src.n_layers) return fail(KVX_EINVAL, "layer %d out of range", layer);
     pl->inject[layer] = 1;
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_inject_stall(kvx_plan_t pl, int32_t layer) {
+    if (!pl) return fail(KVX_EINVAL, "NULL plan");
+    if (layer < 0 || layer >= pl->src.n_layers) return fail(KVX_EINVAL, "layer %d out of range", layer);
+    if (effective_kernel(pl) != KVX_KERNEL_BULK)
+        return fail(KVX_EUNSUPPORTED, "the stall hook needs a plan whose pushes run the bulk kernel");
+    pl->stall[layer] = 1;
     return KVX_OK;
 }
 

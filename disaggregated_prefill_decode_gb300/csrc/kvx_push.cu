@@ -173,6 +173,8 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.err = reinterpret_cast<int32_t *>(base + pl->off_err);
     a.ts_start = nullptr;
     a.ts_end = nullptr;
+    a.wait_ns = kBulkWaitNs;
+    a.stall_layer = -1;
     a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();
@@ -295,6 +297,13 @@ static kvx_status launch_tracked(kvx_plan_s *pl, int32_t l0, int32_t l1, cudaStr
     if (slot >= 0) {
         args.ts_start = pl->ts + slot;
         args.ts_end = pl->ts + kTimingSlots + slot;
+    }
+    for (int32_t l = l0; l < l1 && shape.kernel == KVX_KERNEL_BULK; ++l) {
+        if (!pl->stall[l]) continue;
+        args.stall_layer = l;              // testing hook: one stage of this layer never completes
+        args.wait_ns = kBulkStallWaitNs;
+        pl->stall[l] = 0;
+        break;
     }
     // the completion event is taken before the launch, so a launched push is always tracked
     cudaEvent_t ev;

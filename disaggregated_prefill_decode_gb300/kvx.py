@@ -108,6 +108,7 @@ _sig = {
     "kvx_plan_push_times": (c_i32, [c_vp, _P(ctypes.c_float), _P(ctypes.c_float), c_i32, _P(c_i32)]),
     "kvx_plan_push_times_ns": (c_i32, [c_vp, _P(c_i64), _P(c_i64), c_i32, _P(c_i32)]),
     "kvx_plan_inject_failure": (c_i32, [c_vp, c_i32]),
+    "kvx_plan_inject_stall": (c_i32, [c_vp, c_i32]),
     "kvx_plan_destroy": (c_i32, [c_vp]),
     "kvx_status_str": (ctypes.c_char_p, [c_i32]),
     "kvx_last_error": (ctypes.c_char_p, []),
@@ -135,7 +136,6 @@ _sig = {
     "kvx_conn_load_errors": (c_i32, [c_vp, c_i64, _P(c_i32), c_i32, _P(c_i32)]),
     "kvx_conn_release": (c_i32, [c_vp, c_i64]),
     "kvx_conn_size": (c_i64, [c_vp]),
-    "kvx_fixture_prefill": (c_i32, [c_i32, c_i64, c_vp, c_i64, c_u64, c_vp, c_vp]),
     "kvx_version": (ctypes.c_char_p, []),
     "kvx_launch_count": (c_i64, []),
 }
@@ -372,6 +372,10 @@ def kvx_plan_inject_failure(plan, layer: int) -> None:
     _check(_lib.kvx_plan_inject_failure(_h(plan), layer), "kvx_plan_inject_failure")
 
 
+def kvx_plan_inject_stall(plan, layer: int) -> None:
+    _check(_lib.kvx_plan_inject_stall(_h(plan), layer), "kvx_plan_inject_stall")
+
+
 def kvx_plan_destroy(plan) -> None:
     h = _h(plan)
     if h:
@@ -442,12 +446,6 @@ def kvx_match_prefix_static(tokens, tok_off, n_sessions: int, block_size: int, t
     if st not in (KVX_OK, KVX_ENOMEM):
         raise KvxError(st, "kvx_match_prefix_static")
     return st
-
-
-def kvx_fixture_prefill(ctas: int, iters: int, buf=None, n_bytes: int = 0, seed: int = 0, stream=None,
-                        done=None) -> None:
-    _check(_lib.kvx_fixture_prefill(ctas, iters, _ptr(buf), n_bytes, seed & (2**64 - 1), _stream(stream),
-                                    _event(done)), "kvx_fixture_prefill")
 
 
 # ---------------------------------------------------------------------------------------------

@@ -19,6 +19,11 @@
  *  - A plan or table is used by one host thread at a time. Different plans are independent.
  *  - Device work runs on the stream the caller passes (plus a library-owned non-blocking stream
  *    for small status read-backs).
+ *  - The library keeps per-device state for the life of the process: its push lanes (streams), a
+ *    stream-ordered memory pool, an event pool, the read-back stream and the device address of the
+ *    fixed scratch of kvx_match_prefix_static. All of it belongs to the device's primary context:
+ *    resetting the device (cudaDeviceReset) or otherwise destroying that context while the library
+ *    is loaded leaves it dangling, and later calls on that device are undefined.
  */
 #ifndef KVX_H
 #define KVX_H
@@ -294,6 +299,18 @@ kvx_status kvx_plan_layer_states(kvx_plan_t plan, int32_t *out, int32_t n_layers
  * device but is reported FAILED by kvx_sync. */
 kvx_status kvx_plan_inject_failure(kvx_plan_t plan, int32_t layer);
 
+/* Testing hook for the copy kernel's bounded device-side wait ([P2] section 3.1: failed loads are
+ * reported and those blocks recomputed; section 6: a middle layer can fail). The next push of
+ * `layer` runs with a 1 ms limit on each wait for a bulk ring stage instead of 2 s, and the
+ * launch's first CTA, once the loads of its first work item of that layer have landed, waits for a
+ * phase of that stage that nothing arms: a wait that can only run out, with no copy in flight. The
+ * CTA gives up at the limit, marks every layer of the work it had left FAILED, waits (at most the
+ * limit each) for its loads still in flight and returns; the other CTAs finish normally and nothing
+ * faults. kvx_sync then reports KVX_EFAILED and the layer
+ * FAILED; consumer bytes the CTA did not copy keep their prior contents. KVX_EUNSUPPORTED unless the
+ * plan's pushes run the bulk kernel. */
+kvx_status kvx_plan_inject_stall(kvx_plan_t plan, int32_t layer);
+
 /* Waits for any pending push, then frees the plan and its device descriptors. NULL is a no-op.
  * kvx_sync and kvx_plan_destroy make the plan's device (current at its first push, or at
  * kvx_match_prefix for a device-built plan) current while they run and restore the caller's;
@@ -426,8 +443,9 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
  * Arguments as in kvx_match_prefix; no plan is built (free_blocks is not read, n_free only bounds
  * the assignment). Its scratch is one fixed array of the library (about 1 MiB on every GPU that
  * loads it, held until the process exits), sized for at most 65536 sessions per call; more
- * return KVX_EINVAL. The first call on a device looks up that array's device address (make this
- * first call before any stream capture). Every call reuses the same array and leaves its contents
+ * return KVX_EINVAL. The first call on a device looks up that array's device address and keeps it
+ * for later calls (make this first call before any stream capture; a device reset invalidates it,
+ * see the conventions at the top). Every call reuses the same array and leaves its contents
  * behind; the call clears what must start at zero. Calls whose device work overlaps (on different
  * streams or host threads) race on the array. The call waits for `stream`. Returns KVX_OK, or
  * KVX_ENOMEM with the decisions written when the pushing sessions need more than n_free blocks.
@@ -575,18 +593,6 @@ kvx_status kvx_conn_release(kvx_conn_t conn, int64_t req_id);
 
 /* Number of records held. */
 int64_t kvx_conn_size(kvx_conn_t conn);
-
-/* ------------------------------------------------------------------------------------------------
- * Synthetic prefill fixture (tests and benchmark only; not part of the transfer path).
- * Occupies `ctas` CTAs of 128 threads with a dependent integer chain of `iters` steps per thread,
- * standing in for a layer's forward compute on the main stream. If `buf` is not NULL, the CTAs
- * then rewrite buf[0 .. n_bytes) (device, 16-byte aligned, n_bytes a multiple of 16) with a pattern
- * derived from `seed`, so a push that ran before the fixture finished would copy stale bytes.
- * May be called while `stream` is being captured into a CUDA graph: `done` is then recorded by an
- * external event-record node on every replay (the launch counter counts the capture only).
- * ---------------------------------------------------------------------------------------------- */
-kvx_status kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes, uint64_t seed,
-                               cudaStream_t stream, cudaEvent_t done /* recorded after it when not NULL */);
 
 /* Library version string and the number of kvx kernels launched by this process so far. */
 const char *kvx_version(void);

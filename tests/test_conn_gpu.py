@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 import kvx_inputs
+import prefill_fixture
 from gpu_helpers import canary_host, check_layers, device_pool, layer_buffers
 
 torch = pytest.importorskip("torch")
@@ -43,7 +44,7 @@ def forward_chunk(src_bufs, c, main, spin):
     events = []
     for layer in range(SRC.n_layers):
         for p, b in enumerate(layer_buffers(SRC, src_bufs, layer)):
-            kvx.kvx_fixture_prefill(16, spin, b[lo:hi], hi - lo, seed=1000 * c + 10 * layer + p, stream=main)
+            prefill_fixture.prefill(16, spin, b[lo:hi], hi - lo, seed=1000 * c + 10 * layer + p, stream=main)
         ev = torch.cuda.Event()
         ev.record(main)
         events.append(ev)
@@ -71,7 +72,7 @@ def run_chunked(bs, register_first, inject_layer=None, spin=20000):
     if register_first:
         kvx.kvx_conn_register(conn, rid, 0, dst_ids, now)
     plan, writes = None, []
-    launches_before = kvx.kvx_launch_count()
+    launches_before, fixtures_before = kvx.kvx_launch_count(), prefill_fixture.launch_count()
     for c in range(len(CHUNKS)):
         last = c == len(CHUNKS) - 1
         kvx.kvx_conn_prefill(conn, rid, 0, CHUNKS[c], N_TOKENS[c], last, now)
@@ -80,6 +81,7 @@ def run_chunked(bs, register_first, inject_layer=None, spin=20000):
             # the gate: nothing may move before the last chunk
             assert kvx.kvx_conn_get(conn, rid)["state"] == kvx.KVX_CONN_WAITING
             assert kvx.kvx_conn_poll(conn, now) == []
+            assert kvx.kvx_launch_count() == launches_before                  # no push launched yet
             continue
         if kvx.kvx_conn_get(conn, rid)["state"] == kvx.KVX_CONN_READY:
             # layer-wise: the pushes of the last chunk's forward, one per layer, gated on its event
@@ -91,8 +93,8 @@ def run_chunked(bs, register_first, inject_layer=None, spin=20000):
         else:
             assert kvx.kvx_conn_get(conn, rid)["state"] == kvx.KVX_CONN_DEFERRED
             deferred_after = events[-1]
-    # every fixture launch so far was ours; pushes counted only from the last chunk on
-    assert kvx.kvx_launch_count() - launches_before >= len(CHUNKS) * SRC.n_layers * SRC.n_planes
+    # one forward launch per (chunk, layer, plane), counted by the fixture's own library
+    assert prefill_fixture.launch_count() - fixtures_before == len(CHUNKS) * SRC.n_layers * SRC.n_planes
     if not register_first:
         # the deferred task: the registration arrives after the forward; all layers in one write,
         # gated on the event after the last layer (one stream: it follows every layer)

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import kvx_inputs
+import prefill_fixture
 import oracle
 from gpu_helpers import canary_host, check_layers, device_pool, host, layer_buffers
 
@@ -38,7 +39,7 @@ def push_all_layers(plan, n_layers, fixture_iters=2000, per_layer=True):
     side = torch.cuda.Stream(priority=-1)
     if per_layer:
         for layer in range(n_layers):
-            kvx.kvx_fixture_prefill(8, fixture_iters, stream=main)
+            prefill_fixture.prefill(8, fixture_iters, stream=main)
             ev = torch.cuda.Event()
             ev.record(main)
             kvx.kvx_push_layer(plan, layer, side, ev)
@@ -323,7 +324,7 @@ def test_push_ordered_after_prefill_rewrite():
     side = torch.cuda.Stream(priority=-1)
     for layer in range(4):
         for b in layer_buffers(w.src, src, layer):
-            kvx.kvx_fixture_prefill(16, 20000, b, b.numel(), seed=1000 + layer, stream=main)
+            prefill_fixture.prefill(16, 20000, b, b.numel(), seed=1000 + layer, stream=main)
         ev = torch.cuda.Event()
         ev.record(main)
         kvx.kvx_push_layer(plan, layer, side, ev)
@@ -349,8 +350,8 @@ def test_push_ordered_after_graph_replayed_prefill():
     with torch.cuda.graph(g, stream=cap):
         for layer in range(3):
             for b in layer_buffers(w.src, src, layer):
-                kvx.kvx_fixture_prefill(16, 20000, b, b.numel(), seed=500 + layer, stream=cap)
-            kvx.kvx_fixture_prefill(1, 1, stream=cap, done=ready[layer])
+                prefill_fixture.prefill(16, 20000, b, b.numel(), seed=500 + layer, stream=cap)
+            prefill_fixture.prefill(1, 1, stream=cap, done=ready[layer])
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream(priority=-1)
     for rep in range(3):
@@ -375,7 +376,7 @@ def test_sync_timeout_then_completion():
     dst, _ = device_pool(w.dst, "canary_" + w.values)
     plan = kvx.kvx_plan(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w))
     side = torch.cuda.Stream()
-    kvx.kvx_fixture_prefill(1, 30_000_000, stream=side)          # ~tens of ms of dependent integer work
+    prefill_fixture.prefill(1, 30_000_000, stream=side)          # ~tens of ms of dependent integer work
     kvx.kvx_push_layer(plan, 0, side)
     kvx.kvx_push_layer(plan, 1, side)
     assert kvx.kvx_sync(plan, 1000) == kvx.KVX_ETIMEDOUT
@@ -400,9 +401,10 @@ def test_injected_failure_reports_failed_layer():
 
 
 def test_launch_count_grows():
-    n0 = kvx.kvx_launch_count()
+    n0, f0 = kvx.kvx_launch_count(), prefill_fixture.launch_count()
     test_tiny_all_layers()
-    assert kvx.kvx_launch_count() >= n0 + 4                     # 2 fixtures + 2 pushes
+    assert kvx.kvx_launch_count() >= n0 + 2                     # 2 pushes
+    assert prefill_fixture.launch_count() == f0 + 2             # 2 fixtures, counted by their own library
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -530,3 +532,71 @@ def test_threads_push_their_own_plans_concurrently():
         per = w.dst.n_planes * w.dst.n_shards
         check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(per)],
                      reqs_of(w), range(w.src.n_layers))
+
+
+def assert_layer_states_truthful(w, src, dst, states, canary_elem):
+    """A layer that reads DONE equals the oracle byte for byte; a FAILED one holds, element by element,
+    either the oracle's value or its prior canary (nothing outside the pushed tokens moved)."""
+    orc = oracle.load()
+    sg1, dg1 = w.src.replace(n_layers=1), w.dst.replace(n_layers=1)
+    for layer, st in enumerate(states):
+        want = [canary_host(w.dst, w.values) for _ in range(w.dst.n_planes * w.dst.n_shards)]
+        orc.push(sg1, host(layer_buffers(w.src, src, layer)), dg1, want, reqs_of(w))
+        got = host(layer_buffers(w.dst, dst, layer))
+        for a, b in zip(got, want):
+            if st == kvx.KVX_LAYER_DONE:
+                assert np.array_equal(a, b), f"layer {layer} reads DONE but differs from the oracle"
+            else:
+                a16, b16 = a.view(np.uint16), b.view(np.uint16)
+                assert bool(((a16 == b16) | (a16 == canary_elem)).all()), f"layer {layer}: a byte moved outside the push"
+
+
+@pytest.mark.parametrize("multi_layer", [False, True], ids=["per_layer", "one_launch"])
+def test_bulk_wait_runs_out_and_reports_failed(multi_layer):
+    """kvx_plan_inject_stall: the bulk kernel's first CTA waits, after a stage's loads landed, for a
+    phase of that stage that nothing arms. The wait gives up at the hook's 1 ms limit (no hang, no
+    fault), every layer of the work that CTA had left reads FAILED at kvx_sync, layers read DONE only
+    when exact, and no consumer byte outside the pushed tokens changes. The hook fires once: the next
+    push of the same layers is complete and exact."""
+    w = kvx_inputs.qwen3_32b_single(n_layers=3)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    opts = {"layers_per_launch": 3} if multi_layer else None
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), opts)
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
+    side = torch.cuda.Stream()
+    if multi_layer:
+        kvx.kvx_plan_inject_stall(plan, 0)
+        kvx.kvx_push_layers(plan, 0, 3, side)
+    else:
+        kvx.kvx_plan_inject_stall(plan, 1)
+        for layer in range(3):
+            kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_EFAILED
+    states = kvx.kvx_plan_layer_states(plan).tolist()
+    if multi_layer:
+        # the stalled CTA held work in every layer of the one launch: all three are reported
+        assert states == [kvx.KVX_LAYER_FAILED] * 3
+    else:
+        assert states == [kvx.KVX_LAYER_DONE, kvx.KVX_LAYER_FAILED, kvx.KVX_LAYER_DONE]
+    assert_layer_states_truthful(w, src, dst, states, kvx_inputs.CANARY_BF16)
+    # the hook fired once
+    if multi_layer:
+        kvx.kvx_push_layers(plan, 0, 3, side)
+    else:
+        kvx.kvx_push_layer(plan, 1, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(3))
+    kvx.kvx_plan_destroy(plan)
+
+
+def test_stall_hook_needs_the_bulk_kernel():
+    w = kvx_inputs.tiny()
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"kernel": KERNELS["persist"]})
+    with pytest.raises(kvx.KvxError) as ei:
+        kvx.kvx_plan_inject_stall(plan, 0)
+    assert ei.value.status == kvx.KVX_EUNSUPPORTED
+    kvx.kvx_plan_destroy(plan)
