@@ -30,6 +30,7 @@ cpu_baseline.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import gc
 import hashlib
 import re
@@ -45,8 +46,10 @@ import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+sys.path.insert(1, os.path.join(ROOT, "tests"))   # the synthetic prefill fixture lives beside the tests
 
 import kvx_inputs  # noqa: E402
+import prefill_fixture  # noqa: E402
 
 METRIC = "KV push GB/s (read+write) and % of GB300 HBM roofline; blocks/s; prefix-match ops/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -69,13 +72,13 @@ def parse():
     p.add_argument("--bulk-stages", type=int, default=0, help="bulk kernel ring stages (0: library default)")
     p.add_argument("--fixture-ctas", type=int, default=8)
     p.add_argument("--fixture-iters", type=int, default=2000)
-    p.add_argument("--fixture-graph", action="store_true",
-                   help="replay the prefill fixture from one CUDA graph per step instead of launching it layer by layer")
     p.add_argument("--timing-every", type=int, default=4,
                    help="time the pushes of every n-th timed step only (1: every step; reading the stamps "
                         "back costs the host about 25 us per timed step)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-config-seconds", type=float, default=4.0,
+                   help="oracle time on each other configuration (all cores, then one)")
     p.add_argument("--no-match", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -147,6 +150,26 @@ def union_us(start, end):
 # clocks
 # ---------------------------------------------------------------------------------------------
 
+# The SM clock read through NVML every 2 ms in a child process (its own interpreter, so the sampling
+# takes nothing from the issuing thread), each sample stamped with the host's monotonic clock: fine
+# enough to tell the clock of each step of a short timed region.
+_NVML_POLLER = r"""
+import ctypes, sys, time
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(1)
+h = ctypes.c_void_p()
+if nv.nvmlDeviceGetHandleByUUID(sys.argv[1].encode(), ctypes.byref(h)) != 0:
+    sys.exit(1)
+clk = ctypes.c_uint()
+out = sys.stdout
+while True:
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:        # 1: the SM clock
+        out.write(f"{time.monotonic():.6f} {clk.value}\n")
+    time.sleep(0.002)
+"""
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -154,6 +177,7 @@ class ClockSampler:
 
     def __init__(self, device_uuid):
         self.proc = None
+        self.fine = None
         self.uuid = device_uuid
 
     def start(self):
@@ -164,10 +188,34 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.uuid:
+            try:
+                self.fine = subprocess.Popen([sys.executable, "-u", "-c", _NVML_POLLER, self.uuid], stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.fine = None
+
+    def stop_fine(self):
+        """(host monotonic time, SM MHz) samples of the NVML poller, or []."""
+        if not self.fine:
+            return []
+        self.fine.terminate()
+        out, _ = self.fine.communicate(timeout=10)
+        samples = []
+        for line in out.splitlines():
+            parts = line.split()
+            if len(parts) == 2:
+                try:
+                    samples.append((float(parts[0]), float(parts[1])))
+                except ValueError:
+                    pass
+        return samples
 
     def stop(self):
+        fine = self.stop_fine()
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0,
+                    "fine": fine}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         sm, smax, reasons = [], [], set()
@@ -185,7 +233,17 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "fine": fine}
+
+
+def clock_by_step(fine, step_host):
+    """Median NVML SM clock over each timed step's host issue window [start_i, start_{i+1}); None for
+    a step with no sample (the GPU runs up to a step behind the host, so this is approximate)."""
+    out = []
+    for a, b in zip(step_host[:-1], step_host[1:]):
+        v = [mhz for t, mhz in fine if a <= t < b]
+        out.append(statistics.median(v) if v else None)
+    return out
 
 
 # ---------------------------------------------------------------------------------------------
@@ -208,10 +266,12 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     """Allocates the workload's pools and times K steps of the per-layer push pattern after W untimed
     ones. A step builds the requests' plan, runs the synthetic prefill (per layer a fixture kernel on
     the priority stream that records the layer's ready event) and pushes every layer gated on its
-    event; each step is synced after the next one is issued. The pushes of every `every`-th timed step
-    are timed (the kernels' own global-timer stamps). `all_layers`: one kvx_push_layers call per
-    step for all layers, gated on the last layer's event, instead of one kvx_push_layer per layer;
-    `extra_opts` are added to the plan options."""
+    event; each step is synced after the next one is issued. The pushes of every `every`-th step are
+    timed (the kernels' own global-timer stamps); the warm-up steps follow the same pattern, so the
+    timed loop meets no first use. `all_layers`: one kvx_push_layers call per step for all layers,
+    gated on the last layer's event, instead of one kvx_push_layer per layer; `extra_opts` are added
+    to the plan options. `sampler` (clock sampling) runs from before the warm-up to the end of the
+    timed steps, so the GPU never idles between the two."""
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
@@ -229,104 +289,65 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     probe = kvx.kvx_plan_ex(sp, dp, reqs, opts)
     info = kvx.kvx_plan_get_info(probe)
     kvx.kvx_plan_destroy(probe)
-    timing_opts = dict(opts, flags=kvx.KVX_PLAN_TIMING)
     ready = [torch.cuda.Event() for _ in range(L)]
     for ev in ready:                                  # materialise the events so their handles exist
         ev.record(main)
     ready_h = [int(ev.cuda_event) for ev in ready]
     main_h, side_h = int(main.cuda_stream), int(side.cuda_stream)
-    lib = kvx._lib                                    # the C-ABI itself, called directly in the loop
-    push_times, issue_us, plan_us = [], [], []
-
-    # The synthetic prefill is launched layer by layer from the host between the pushes (an engine
-    # issuing its forward pass); --fixture-graph captures the L launches once into a CUDA graph and
-    # replays it per step instead.
-    fixture_graph = None
-    if args.fixture_graph:
-        cap = torch.cuda.Stream(priority=-1)
-        fixture_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(fixture_graph, stream=cap):
-            for layer in range(L):
-                if lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer,
-                                           int(cap.cuda_stream), ready_h[layer]):
-                    raise RuntimeError(f"fixture capture failed: {kvx.kvx_last_error()}")
-        torch.cuda.synchronize()
-
-    def issue(timing):
-        """One step: its plan, the prefill (graph replay or per-layer launches) and the gated pushes."""
-        p0 = time.perf_counter()
-        plan = kvx.kvx_plan_ex(sp, dp, reqs, timing_opts if timing else opts)
-        plan_us.append((time.perf_counter() - p0) * 1e6)
-        if fixture_graph is not None:
-            fixture_graph.replay()                    # on the current stream: main
-            for layer in range(L):
-                if lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer]):
-                    raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
-        elif all_layers:
-            st = 0
-            for layer in range(L):
-                st |= lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h,
-                                              ready_h[layer])
-            st |= lib.kvx_push_layers(plan.handle, 0, L, side_h, ready_h[L - 1])
-            if st:
-                raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
-        else:
-            for layer in range(L):
-                st = lib.kvx_fixture_prefill(args.fixture_ctas, args.fixture_iters, None, 0, layer, main_h,
-                                             ready_h[layer])
-                st |= lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer])
-                if st:
-                    raise RuntimeError(f"issue failed: {kvx.kvx_last_error()}")
-        return plan
-
-    def finish(plan, timing):
-        st = kvx.kvx_sync(plan, -1)
-        if st != kvx.KVX_OK:
-            raise RuntimeError(f"kvx_sync: {kvx.kvx_status_str(st)} {kvx.kvx_last_error()}")
-        if timing:
-            push_times.append(kvx.kvx_plan_push_times_ns(plan))
-        kvx.kvx_plan_destroy(plan)
+    fx = prefill_fixture.lib()                        # the synthetic prefill and the native engine loop
+    carr, n_req, _keep = kvx._requests(reqs)
+    o = kvx._opts(opts)
+    cap = 4096 * 64
+    s_ns, e_ns = np.zeros(cap, np.int64), np.zeros(cap, np.int64)
+    n_st = ctypes.c_int64(0)
+    ready_arr = (ctypes.c_void_p * L)(*ready_h)
 
     def run_steps(n, timed):
-        """n steps, each synced after the next one is issued (one request in flight behind another)."""
-        prev = None
-        for i in range(n):
-            timing = timed and i % every == 0
-            h0 = time.perf_counter()
-            plan = issue(timing)
-            if timed:
-                issue_us.append((time.perf_counter() - h0) * 1e6)
-            if prev is not None:
-                finish(*prev)
-            prev = (plan, timing)
-        if prev is not None:
-            finish(*prev)
+        """n steps of the engine loop, natively (the fixture library's kvx_fixture_run_steps, through the
+        kvx C-ABI): per step a plan (a timing plan when the step's index is a multiple of `every`, the
+        warm-up steps included, so the timed loop meets no first use), per layer the fixture and the
+        gated push; each step synced after the next one is issued. Timed runs record a CUDA event on
+        the prefill stream where each step starts and after the last sync."""
+        marks, marks_arr = None, None
+        if timed:
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            for m in marks:                           # materialise the handles
+                m.record(main)
+            torch.cuda.synchronize()
+            marks_arr = (ctypes.c_void_p * (n + 1))(*[int(m.cuda_event) for m in marks])
+        iss, pln = np.zeros(max(n, 1)), np.zeros(max(n, 1))
+        rc = fx.kvx_fixture_run_steps(ctypes.addressof(sp.struct), ctypes.addressof(dp.struct), ctypes.addressof(carr),
+                                      n_req, ctypes.addressof(o), every, n, int(all_layers), args.fixture_ctas,
+                                      args.fixture_iters, main_h, side_h, ctypes.addressof(ready_arr),
+                                      ctypes.addressof(marks_arr) if timed else None,
+                                      s_ns.ctypes.data if timed else None, e_ns.ctypes.data if timed else None, cap,
+                                      ctypes.addressof(n_st), iss.ctypes.data, pln.ctypes.data)
+        if rc:
+            raise RuntimeError(f"engine loop: {fx.kvx_fixture_last_error().decode()}")
+        return marks, iss[:n], pln[:n]
 
+    gc.collect()
+    gc.disable()                                      # no collector pauses in the warm-up or the timed loop
+    if sampler:
+        sampler.start()
     run_steps(W, False)
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
-    launches0 = kvx.kvx_launch_count()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kvx.kvx_launch_count() + prefill_fixture.launch_count()
     torch.cuda.synchronize()
-    gc.collect()
-    gc.disable()                                      # no collector pauses inside the timed loop
+    host0 = time.monotonic()
     wall0 = time.perf_counter()
-    t0.record(main)
-    run_steps(K, True)
-    main.wait_stream(side)
-    t1.record(main)
+    step_marks, issue_us, plan_us = run_steps(K, True)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    gc.enable()
-    launches = kvx.kvx_launch_count() - launches0
-    if fixture_graph is not None:
-        launches += K * L                             # the fixture kernels the graph replays launched
     clk = sampler.stop() if sampler else None
-    assert len(push_times) == -(-K // every)
+    gc.enable()
+    launches = kvx.kvx_launch_count() + prefill_fixture.launch_count() - launches0
+    step_host = np.concatenate([[0.0], np.cumsum(issue_us)]) * 1e-6 + host0
+    push_times = [(s_ns[:n_st.value], e_ns[:n_st.value])]
+    t0, t1 = step_marks[0], step_marks[-1]
+    step_ms = [a.elapsed_time(b) for a, b in zip(step_marks[:-1], step_marks[1:])]
     # Pushes of consecutive layers (and of consecutive steps) may overlap: they run on separate lanes.
     # The kernels stamp the GPU's one global timer, so all timed pushes share a timeline; the time the
     # GPU spends pushing is the union of their intervals, per launch that union / launches.
@@ -336,15 +357,18 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     all_s, all_e = (all_s - t_base) * 1e-3, (all_e - t_base) * 1e-3
     busy_us = union_us(all_s, all_e)
     raw_us = (all_e - all_s).tolist()
+    timed_step_ms = sum(step_ms[i] for i in range(0, K, every))
     torch.cuda.set_stream(torch.cuda.default_stream(device))
     return {"w": w, "L": L, "src": src, "dst": dst, "sp": sp, "dp": dp, "reqs": reqs, "opts": opts, "info": info,
             "bytes_step": 2 * info["bytes_per_layer"] * L,                     # read + write
             "blocks_step": sum(-(-n // w.src.block_size) for n, _, _ in reqs) * L,
             "elapsed_ms": t0.elapsed_time(t1), "launches": launches, "clocks": clk, "wall": wall,
-            "timed_steps": len(push_times), "timed_launches": len(raw_us),
+            "timed_steps": -(-K // every), "timed_launches": len(raw_us),
             "mean_push_ms": busy_us / len(raw_us) * 1e-3,
             "raw_push_ms": statistics.fmean(raw_us) * 1e-3,
-            "issue_us": issue_us, "plan_us": plan_us}
+            "step_ms": step_ms, "push_cover": busy_us * 1e-3 / timed_step_ms,
+            "step_host": step_host.tolist(),
+            "issue_us": issue_us.tolist(), "plan_us": plan_us.tolist()}
 
 
 def measure_overlap(args, torch, kvx, m, steps=200):
@@ -358,6 +382,7 @@ def measure_overlap(args, torch, kvx, m, steps=200):
     L, reqs, sp, dp = m["L"], m["reqs"], m["sp"], m["dp"]
     opts = m["opts"]
     lib = kvx._lib
+    fx = prefill_fixture.lib().kvx_fixture_prefill
     main = torch.cuda.Stream(priority=-1)
     side = torch.cuda.Stream(priority=0)
     ready = [torch.cuda.Event() for _ in range(L)]
@@ -385,7 +410,7 @@ def measure_overlap(args, torch, kvx, m, steps=200):
                         torch.matmul(gemm[0], gemm[1], out=gemm[2])
                         ready[layer].record(main)
                 elif prefill:
-                    lib.kvx_fixture_prefill(args.fixture_ctas, iters, None, 0, layer, main_h, ready_h[layer])
+                    fx(args.fixture_ctas, iters, None, 0, layer, main_h, ready_h[layer])
                 if push:
                     lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer] if prefill else None)
             b.record(main)
@@ -500,7 +525,9 @@ def per_config(args, torch, kvx, device):
              ("qwen3_32b_batched", 20, True, {"layers_per_launch": 64}, one_call + " in a single launch"),
              ("tp4_to_tp1_remap", 20, False, None, per_layer_call),
              ("qwen3_32b_batched_hnd", 20, False, None, per_layer_call),
-             ("qwen3_32b_batched_nhd_to_hnd", 20, False, None, per_layer_call))
+             ("qwen3_32b_batched_nhd_to_hnd", 20, False, None, per_layer_call),
+             ("qwen3_32b_single_nhd_to_hnd", 100, False, None, per_layer_call),
+             ("qwen3_32b_single_hnd_to_nhd", 100, False, None, per_layer_call))
     for name, steps, all_layers, extra, launch in cases:
         if name == args.workload and not all_layers:
             continue
@@ -519,6 +546,10 @@ def per_config(args, torch, kvx, device):
         del m
         gc.collect()
         torch.cuda.empty_cache()
+    out.append(bidir_full(torch, kvx, device, {"kernel": args.kernel, "threads": args.threads,
+                                                "ctas_per_sm": args.ctas_per_sm, "bulk_stages": args.bulk_stages}))
+    gc.collect()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -573,14 +604,15 @@ def run_kvx(args, rank, local_rank, world):
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
             "lanes": info["lanes"], "bulk_stages": info["bulk_stages"],
-            "threads": info["threads"], "ctas_per_sm": args.ctas_per_sm or "auto (1 bulk / 2 persistent below 128 MiB per launch)",
+            "threads": info["threads"],
+            "ctas_per_sm": args.ctas_per_sm or "auto (below 128 MiB per launch: 5 per 4 SMs bulk, 2 persistent, 4 "
+                                               "persistent on head groups; above: the occupancy limit)",
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
-                      "stream records the layer's event ("
-                      + (f"the {L} launches replayed from one CUDA graph per step, events as external graph nodes"
-                         if args.fixture_graph else "launched layer by layer from the host")
-                      + "); kvx_push_layer(priority 0 side stream, event) per layer forks onto the push lanes and "
-                      "waits for it; a plan is built every step and synced after the next step is issued",
+                      "stream records the layer's event, then kvx_push_layer(priority 0 side stream, event) forks "
+                      "onto the push lanes and waits for it; a plan is built every step and synced after the next "
+                      "step is issued; the engine loop issuing this runs natively (libkvx_fixture's "
+                      "kvx_fixture_run_steps, through the kvx C-ABI)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "blocks_per_s": round(world * m["blocks_step"] * K / (elapsed_ms * 1e-3), 1),
@@ -598,7 +630,8 @@ def run_kvx(args, rank, local_rank, world):
             "traffic": ncu_traffic(args.workload),
         },
         "gpu_launches": launches,
-        "clocks": m["clocks"],
+        "clocks": {k: v for k, v in (m["clocks"] or {}).items() if k != "fine"} or None,
+        "steps_detail": step_detail(m, K),
         "host_wall_s": round(m["wall"], 4),
         "host_issue_us_per_layer": round(statistics.fmean(m["issue_us"]) / L, 3),
         "plan_build_us": round(statistics.median(m["plan_us"]), 2),
@@ -617,6 +650,7 @@ def run_kvx(args, rank, local_rank, world):
                                                              "bulk_stages": args.bulk_stages})
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            result["cpu_baseline"]["per_config"] = cpu_baseline_per_config(args.cpu_config_seconds)
         if not args.no_per_config:
             del m, src, dst, sp, dp
             result["per_config"] = per_config(args, torch, kvx, device)
@@ -624,6 +658,25 @@ def run_kvx(args, rank, local_rank, world):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def step_detail(m, K):
+    """Per-step device times (CUDA events on the prefill stream where each timed step starts), the share
+    of the timed steps' time in which a push kernel was running, and the SM clock per step."""
+    ms = m["step_ms"]
+    fine = (m["clocks"] or {}).get("fine") or []
+    by_step = clock_by_step(fine, m["step_host"]) if fine else []
+    return {"median_ms": round(statistics.median(ms), 5), "first_ms": round(ms[0], 5),
+            "min_ms": round(min(ms), 5), "max_ms": round(max(ms), 5),
+            "ms": [round(x, 4) for x in ms] if K <= 64 else None,
+            "push_cover": round(m["push_cover"], 4),
+            "sm_mhz_by_step": by_step if K <= 64 else None,
+            "sm_mhz_fine_median": statistics.median(v for _, v in fine) if fine else None,
+            "sm_mhz_fine_min": min(v for _, v in fine) if fine else None,
+            "fine_samples": len(fine),
+            "how": "step i = CUDA event at the start of step i+1 (or the end event) - event at the start of step i, "
+                   "on the prefill stream; push_cover = union of the timed steps' push intervals / their step "
+                   "time; SM clock from NVML every 2 ms, binned by each step's host issue window"}
 
 
 def reduce_over_ranks(elapsed_ms, launches, device):
@@ -877,6 +930,99 @@ def run_match(torch, kvx, device, push_opts=None):
     }
 
 
+def bidir_full(torch, kvx, device, push_opts=None, reps=2, n_waves=4):
+    """Configuration 5 whole: 256 sessions, all 48 layers of the fp8 576-byte latent pools (decode about
+    130 GB, prefill about 87 GB), matched and pushed decode->prefill in waves of 64 sessions into one
+    recycled free region, as a prefill instance would pull each turn's reusable spans. The decode side
+    publishes its block hashes (kvx_block_hashes); the free region is sized by a decision-only pass
+    (the largest wave's need). Per wave: kvx_match_prefix with its device-built plan (host wall clock;
+    the call waits for its stream), then the 48 layer pushes on a side stream, their duration from
+    the kernels' own global-timer stamps (first start to last end of the wave). `reps` timed rounds
+    over all waves after one untimed round."""
+    w0 = kvx_inputs.bidir_mla_fp8(n_layers=48, free_blocks=1)
+    bs = w0.block_size
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        view = {np.uint32: np.int32, np.uint64: np.int64}.get(a.dtype.type, a.dtype.type)
+        return torch.from_numpy(a.view(view)).to(device)
+
+    tokens, tok_off, rem_off = d(w0.tokens), d(w0.tok_off), d(w0.rem_off)
+    hashes = torch.empty(int(w0.rem_off[-1]), dtype=torch.int64, device=device)
+    kvx.kvx_block_hashes(tokens, tok_off, w0.n_sessions, bs, hashes, rem_off)
+    keys = torch.unique(hashes[torch.from_numpy(w0.resident).to(device)])
+    table = kvx.kvx_table_build(keys, torch.arange(keys.numel(), dtype=torch.int32, device=device), keys.numel())
+    per = w0.n_sessions // n_waves
+    waves = []
+    for k in range(n_waves):
+        s0, s1 = k * per, (k + 1) * per
+        t0, t1, r0, r1 = (int(x) for x in (w0.tok_off[s0], w0.tok_off[s1], w0.rem_off[s0], w0.rem_off[s1]))
+        waves.append((tokens[t0:t1], d(w0.tok_off[s0:s1 + 1] - t0), hashes[r0:r1], d(w0.remote_blk[r0:r1]),
+                      d(w0.rem_off[s0:s1 + 1] - r0)))
+    out = torch.empty(per * 24, dtype=torch.uint8, device=device)
+    dummy = torch.zeros(1, dtype=torch.int32, device=device)
+    need = []
+    for tk, to, hs, rb, ro in waves:                  # decisions only: how many blocks each wave pulls
+        kvx.kvx_match_prefix(tk, to, per, bs, table, hs, rb, ro, w0.threshold, dummy, 0, None, None, out,
+                             want_plan=False)
+        res = out.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
+        need.append(int(res["missing_tokens"][res["push"] == 1].sum()) // bs)
+    w = kvx_inputs.bidir_mla_fp8(n_layers=48, free_blocks=max(need))
+    assert np.array_equal(w.remote_blk, w0.remote_blk) and np.array_equal(w.tokens, w0.tokens)
+    src, _ = alloc_pool(torch, w.decode, "src", w.seed, device)
+    dst, _ = alloc_pool(torch, w.prefill, "dst", 0, device)
+    sp, dp = kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst)
+    free = d(w.free_blocks)
+    side = torch.cuda.Stream()
+    match_ms, span_us, busy_us, launches, bytes_moved, blocks = [], [], [], 0, 0, 0
+    for rep in range(reps + 1):
+        for tk, to, hs, rb, ro in waves:
+            t = time.perf_counter()
+            st, plan = kvx.kvx_match_prefix(tk, to, per, bs, table, hs, rb, ro, w.threshold, free, len(w.free_blocks),
+                                            sp, dp, out, want_plan=True)
+            ms = (time.perf_counter() - t) * 1e3
+            if st != kvx.KVX_OK:
+                raise RuntimeError(f"kvx_match_prefix: {kvx.kvx_status_str(st)}")
+            kvx.kvx_plan_set_opts(plan, dict(push_opts or {}, flags=kvx.KVX_PLAN_TIMING))
+            info = kvx.kvx_plan_get_info(plan)
+            for layer in range(48):
+                kvx.kvx_push_layer(plan, layer, side)
+            if kvx.kvx_sync(plan, -1) != kvx.KVX_OK:
+                raise RuntimeError(f"kvx_sync: {kvx.kvx_last_error()}")
+            s_ns, e_ns = kvx.kvx_plan_push_times_ns(plan)
+            kvx.kvx_plan_destroy(plan)
+            if rep == 0:
+                continue
+            base = s_ns.min()
+            s_us, e_us = (s_ns - base) * 1e-3, (e_ns - base) * 1e-3
+            match_ms.append(ms)
+            span_us.append(float(e_us.max()))
+            busy_us.append(union_us(s_us, e_us))
+            launches += len(s_ns)
+            bytes_moved += 2 * info["bytes_per_layer"] * 48
+            res = out.cpu().numpy().view(kvx.MATCH_RESULT_DTYPE)
+            blocks += int(res["missing_tokens"][res["push"] == 1].sum()) // bs
+    kvx.kvx_table_destroy(table)
+    peak, _ = measured_peak()
+    span, busy = sum(span_us) * 1e-6, sum(busy_us) * 1e-6
+    result = {"workload": "bidir_mla_fp8_full", "sessions": w.n_sessions, "layers": 48, "waves": n_waves,
+              "timed_rounds": reps, "pull_blocks_per_round": blocks // reps, "wave_need_blocks": need,
+              "bytes_per_round": bytes_moved // reps,
+              "value": round(bytes_moved / span / 1e9, 2), "unit": "GB/s",
+              "blocks_per_s": round(blocks / span, 1),
+              "roofline_frac": round(bytes_moved / busy / 1e9 / peak, 4),
+              "push_ms_per_round": round(span * 1e3 / reps, 3),
+              "match_and_plan_ms_per_wave": round(statistics.median(match_ms), 3),
+              "launches": launches, "kernel": KERNEL_NAMES[info["kernel"]], "threads": info["threads"],
+              "how": "per round: 4 waves of 64 sessions, each kvx_match_prefix (decisions + device-built plan) "
+                     "then 48 kvx_push_layer on a side stream into the recycled free region; GB/s = read+write "
+                     "bytes / sum over waves of (last push end - first push start), kernel stamps; blocks/s = "
+                     "pulled blocks (each all 48 layers) / the same time; roofline_frac over the union of the "
+                     "push intervals"}
+    del src, dst, sp, dp
+    return result
+
+
 # ---------------------------------------------------------------------------------------------
 # oracle (CPU) timing: the cpu_baseline leg and the reference arm
 # ---------------------------------------------------------------------------------------------
@@ -938,6 +1084,137 @@ def cpu_baseline(w, seconds):
                       f"its own layer, {dt:.1f} s",
             "single_thread": {"value": round(per_layer * reps1 / dt1 / 1e9, 3), "unit": "GB/s", "cores": 1,
                               "sample": f"{reps1} one-layer pushes, 1 thread, {dt1:.1f} s"}}
+
+
+def oracle_push_rate(w, seconds, n_threads):
+    """The oracle as it stands pushing one layer of workload `w` (host pools: the producer layer shared,
+    one consumer copy per thread): all threads at once for 0.7 x `seconds`, then one thread for
+    0.3 x `seconds`. GB/s counts read + write bytes; blocks/s counts producer blocks (block-layers)."""
+    import concurrent.futures as cf
+    import oracle
+    orc = oracle.load()
+    sg, dg = w.src.replace(n_layers=1), w.dst.replace(n_layers=1)
+    rng = np.random.default_rng(w.seed)
+    src = [rng.integers(0, 256, sg.buffer_bytes, dtype=np.uint8) for _ in range(sg.n_buffers)]
+    dsts = [[np.full(dg.buffer_bytes, 0xAD, np.uint8) for _ in range(dg.n_buffers)] for _ in range(n_threads)]
+    reqs = requests(w)
+    per = 2 * sum(n for n, _, _ in reqs) * sg.n_shards * sg.row_bytes * sg.n_planes
+    blocks = sum(-(-n // sg.block_size) for n, _, _ in reqs)
+
+    def loop(dst, deadline):
+        n = 0
+        while True:
+            orc.push(sg, src, dg, dst, reqs)
+            n += 1
+            if time.perf_counter() >= deadline:
+                return n
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(n_threads) as pool:
+        reps = sum(pool.map(lambda dst: loop(dst, t0 + 0.7 * seconds), dsts))
+    dt = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    reps1 = loop(dsts[0], t1 + 0.3 * seconds)
+    dt1 = time.perf_counter() - t1
+    return {"workload": w.name, "value": round(per * reps / dt / 1e9, 3), "unit": "GB/s",
+            "blocks_per_s": round(blocks * reps / dt, 1), "cores": n_threads, "kind": "oracle",
+            "sample": f"{reps} oracle pushes of one layer ({per / 2e6:.1f} MB read), {n_threads} threads at once, "
+                      f"{dt:.1f} s",
+            "single_thread": {"value": round(per * reps1 / dt1 / 1e9, 3), "unit": "GB/s",
+                              "blocks_per_s": round(blocks * reps1 / dt1, 1), "cores": 1,
+                              "sample": f"{reps1} one-layer pushes, 1 thread, {dt1:.1f} s"}}
+
+
+def oracle_bidir(seconds, n_threads):
+    """The bidirectional workload on the oracle. Full scale (256 sessions): the match decision alone
+    (oracle_match hashes every session's blocks and decides), one thread. Reduced (16 sessions, the
+    same generator): end to end -- the published hashes, the match with its pairs, and the
+    decode->prefill push of the pulled blocks -- with the push timed per layer (one thread, and all
+    threads at once, one layer each) and the 48-layer figure composed from those times."""
+    import concurrent.futures as cf
+    import oracle
+    orc = oracle.load()
+    full = kvx_inputs.bidir_mla_fp8(n_layers=1)
+    hs = np.concatenate([orc.block_hashes(full.tokens[full.tok_off[s]:full.tok_off[s + 1]], 64)
+                         for s in range(full.n_sessions)])
+    keys = np.unique(hs[full.resident])
+    t = time.perf_counter()
+    n_match = 0
+    while True:
+        m = orc.match(full.tokens, full.tok_off, 64, keys, hs, full.remote_blk, full.rem_off, full.threshold,
+                      full.free_blocks)
+        n_match += 1
+        if time.perf_counter() - t >= 0.15 * seconds:
+            break
+    match_s = (time.perf_counter() - t) / n_match
+    compares = int(m["remote_hit"].sum())
+
+    w = kvx_inputs.bidir_mla_fp8(n_sessions=16, n_layers=1)
+    t = time.perf_counter()
+    hs16 = np.concatenate([orc.block_hashes(w.tokens[w.tok_off[s]:w.tok_off[s + 1]], 64) for s in range(w.n_sessions)])
+    keys16 = np.unique(hs16[w.resident])
+    m16 = orc.match(w.tokens, w.tok_off, 64, keys16, hs16, w.remote_blk, w.rem_off, w.threshold, w.free_blocks)
+    hash_match_s = time.perf_counter() - t
+    reqs, k = [], 0
+    for s in range(w.n_sessions):
+        if m16["push"][s]:
+            nb = int(m16["missing"][s]) // 64
+            reqs.append((nb * 64, m16["pair_src"][k:k + nb], m16["pair_dst"][k:k + nb]))
+            k += nb
+    pulled = k
+    rng = np.random.default_rng(w.seed)
+    src = [rng.integers(0, 255, w.decode.buffer_bytes, dtype=np.uint8)]
+    dsts = [[np.full(w.prefill.buffer_bytes, kvx_inputs.CANARY_FP8, np.uint8)] for _ in range(n_threads)]
+    per = 2 * pulled * 64 * 576
+
+    def loop(dst, deadline):
+        n = 0
+        while True:
+            orc.push(w.decode, src, w.prefill, dst, reqs)
+            n += 1
+            if time.perf_counter() >= deadline:
+                return n
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(n_threads) as pool:
+        reps = sum(pool.map(lambda dst: loop(dst, t0 + 0.5 * seconds), dsts))
+    dt = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    reps1 = loop(dsts[0], t1 + 0.3 * seconds)
+    dt1 = time.perf_counter() - t1
+    layer_all, layer_one = dt / reps, dt1 / reps1          # seconds per layer: aggregate, one thread
+    e2e_one = hash_match_s + 48 * layer_one
+    e2e_all = hash_match_s + 48 * layer_all
+    return {"workload": "bidir_mla_fp8", "kind": "oracle", "cores": n_threads,
+            "match_full": {"sessions_per_s": round(full.n_sessions / match_s, 1),
+                           "block_compares_per_s": round(compares / match_s, 1), "cores": 1,
+                           "sample": f"{n_match} oracle_match calls on all 256 sessions ({len(hs)} published "
+                                     f"blocks), 1 thread"},
+            "e2e_16_sessions": {"sessions": w.n_sessions, "pulled_blocks": pulled,
+                                "hash_and_match_ms": round(hash_match_s * 1e3, 3),
+                                "push_gbs_one_layer": {"all_cores": round(per / layer_all / 1e9, 3),
+                                                       "single_thread": round(per / layer_one / 1e9, 3)},
+                                "blocks_per_s": {"all_cores": round(pulled / (48 * layer_all), 1),
+                                                 "single_thread": round(pulled / (48 * layer_one), 1)},
+                                "ms_48_layers": {"all_cores": round(e2e_all * 1e3, 1),
+                                                 "single_thread": round(e2e_one * 1e3, 1)},
+                                "sample": f"hashes + match once, then {reps} one-layer pushes on {n_threads} threads "
+                                          f"({dt:.1f} s) and {reps1} on one ({dt1:.1f} s); 48-layer time = hash and "
+                                          "match + 48 x the per-layer push time"}}
+
+
+def cpu_baseline_per_config(seconds):
+    """The oracle on each configuration beside the headline one, in the same run, each on all the
+    host's cores and on one."""
+    n = oracle_threads()
+    out = []
+    for name in ("tiny", "qwen3_32b_batched", "tp4_to_tp1_remap", "qwen3_32b_single_nhd_to_hnd"):
+        out.append(oracle_push_rate(kvx_inputs.PUSH_WORKLOADS[name](n_layers=1) if name != "tiny"
+                                    else kvx_inputs.tiny(), seconds, n))
+        gc.collect()
+    out.append(oracle_bidir(seconds, n))
+    gc.collect()
+    return out
 
 
 def run_reference(args, rank, world):

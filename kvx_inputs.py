@@ -197,6 +197,23 @@ def qwen3_32b_batched_nhd_to_hnd(seed: int = 3, n_layers: int = 64) -> PushWorkl
     return w
 
 
+def qwen3_32b_single_nhd_to_hnd(seed: int = 2, n_layers: int = 64) -> PushWorkload:
+    """The single-request workload (one 8192-token prompt, 32 MiB per layer read) from a token-major
+    producer into a head-major consumer: a head-layout change at per-layer push sizes."""
+    w = qwen3_32b_single(seed=seed, n_layers=n_layers)
+    w.dst = w.dst.replace(layout=LAYOUT_HND)
+    w.name = "qwen3_32b_single_nhd_to_hnd"
+    return w
+
+
+def qwen3_32b_single_hnd_to_nhd(seed: int = 2, n_layers: int = 64) -> PushWorkload:
+    """The single-request workload from a head-major producer into a token-major consumer."""
+    w = qwen3_32b_single(seed=seed, n_layers=n_layers)
+    w.src = w.src.replace(layout=LAYOUT_HND)
+    w.name = "qwen3_32b_single_hnd_to_nhd"
+    return w
+
+
 PUSH_WORKLOADS = {
     "tiny": tiny,
     "qwen3_32b_single": qwen3_32b_single,
@@ -204,6 +221,8 @@ PUSH_WORKLOADS = {
     "tp4_to_tp1_remap": tp4_to_tp1_remap,
     "qwen3_32b_batched_hnd": qwen3_32b_batched_hnd,
     "qwen3_32b_batched_nhd_to_hnd": qwen3_32b_batched_nhd_to_hnd,
+    "qwen3_32b_single_nhd_to_hnd": qwen3_32b_single_nhd_to_hnd,
+    "qwen3_32b_single_hnd_to_nhd": qwen3_32b_single_hnd_to_nhd,
 }
 
 
