@@ -66,7 +66,8 @@ def parse():
                    help="build the workload with this many layers (0: its own count); for small profiling captures")
     p.add_argument("--tile-bytes", type=int, default=0)
     p.add_argument("--threads", type=int, default=0)
-    p.add_argument("--kernel", type=int, default=0, help="KVX_KERNEL_*: 0 auto, 1 tile, 2 persist, 3 bulk")
+    p.add_argument("--kernel", type=int, default=0, help="KVX_KERNEL_*: 0 auto, 1 tile, 2 persist, 3 bulk, 4 tensor, 5 staged")
+    p.add_argument("--max-ctas", type=int, default=0, help="upper bound on the CTAs of one copy launch (0: none)")
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--lanes", type=int, default=0, help="internal push streams (0: library default)")
     p.add_argument("--bulk-stages", type=int, default=0, help="bulk kernel ring stages (0: library default)")
@@ -84,6 +85,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-config", action="store_true", help="skip the short runs of the other push configs")
     p.add_argument("--no-overlap", action="store_true", help="skip the prefill / push overlap measurement")
+    p.add_argument("--overlap-narrow", default="32:6,64:4",
+                   help="push shapes beside the GEMM prefill, as max_ctas:bulk_stages pairs separated by commas")
     return p.parse_args()
 
 
@@ -278,7 +281,8 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     sp, dp = kvx.Pool(w.src, src), kvx.Pool(w.dst, dst)
     reqs = requests(w)
     opts = {"tile_bytes": args.tile_bytes, "threads": args.threads, "kernel": args.kernel,
-            "ctas_per_sm": args.ctas_per_sm, "lanes": args.lanes, "bulk_stages": args.bulk_stages}
+            "ctas_per_sm": args.ctas_per_sm, "lanes": args.lanes, "bulk_stages": args.bulk_stages,
+            "max_ctas": args.max_ctas}
     opts.update(extra_opts or {})
     # the synthetic prefill is the latency-critical path: its stream outranks the push stream, so the
     # copies fill the SMs the compute leaves free
@@ -398,10 +402,10 @@ def measure_overlap(args, torch, kvx, m, steps=200):
     gemm.append(torch.empty(8192, 5120, dtype=torch.bfloat16, device=main.device))
     torch.cuda.synchronize()
 
-    def run(prefill, push, n, iters):
+    def run(prefill, push, n, iters, push_opts=None):
         prev, marks = None, []
         for _ in range(n):
-            plan = kvx.kvx_plan_ex(sp, dp, reqs, opts) if push else None
+            plan = kvx.kvx_plan_ex(sp, dp, reqs, dict(opts, **(push_opts or {}))) if push else None
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             for layer in range(L):
@@ -424,12 +428,12 @@ def measure_overlap(args, torch, kvx, m, steps=200):
             kvx.kvx_plan_destroy(prev)
         return marks
 
-    def timed(prefill, push, iters, n_steps=steps):
-        run(prefill, push, 3, iters)
+    def timed(prefill, push, iters, n_steps=steps, push_opts=None):
+        run(prefill, push, 3, iters, push_opts)
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(main)
-        marks = run(prefill, push, n_steps, iters)
+        marks = run(prefill, push, n_steps, iters, push_opts)
         main.wait_stream(side)
         t1.record(main)
         torch.cuda.synchronize()
@@ -449,6 +453,23 @@ def measure_overlap(args, torch, kvx, m, steps=200):
                      "prefill_chain_ms_alone": round(chain_alone, 4),
                      "prefill_chain_ms_with_push": round(chain_with, 4),
                      "prefill_slowdown": round(chain_with / chain_alone - 1, 4)}
+        if iters < 0:
+            # the same GEMM prefill beside pushes bounded to a few CTAs with deep rings: the GEMM's CTAs
+            # take every register of an SM, so each SM a copy holds is an SM the GEMM waits for
+            out[name]["narrow_pushes"] = []
+            variants = []
+            for spec in args.overlap_narrow.split(","):
+                if spec.strip():
+                    c, st = (int(x) for x in spec.split(":"))
+                    variants.append({"max_ctas": c, "bulk_stages": st})
+            for v in variants:
+                p_only, _ = timed(False, True, 0, steps, v)
+                b, c_with = timed(True, True, iters, 50, v)
+                out[name]["narrow_pushes"].append(
+                    {"opts": v, "push_only_ms_per_step": round(p_only, 4), "together_ms_per_step": round(b, 4),
+                     "hidden_frac": round((pre_only + p_only - b) / min(pre_only, p_only), 3),
+                     "prefill_chain_ms_with_push": round(c_with, 4),
+                     "prefill_slowdown": round(c_with / chain_alone - 1, 4)})
     out["how"] = (f"{steps} steps each ({50} with the GEMM prefill); the prefill chain is the median time on its "
                   "stream from a step's first layer to its last; hidden_frac = (prefill + push - together) / "
                   "min(prefill, push)")
@@ -509,7 +530,9 @@ def connector_rate_native():
         return round(float(r.stdout.split()[-1]), 1)
 
 
-KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk"]
+KERNEL_NAMES = ["kvx_copy_tiles", "kvx_copy_tiles", "kvx_copy_persist", "kvx_copy_bulk", "kvx_copy_bulk (tensor maps)",
+                "kvx_copy_staged"]
+KERNEL_SHORT = ["auto", "tile", "persist", "bulk", "tensor", "staged"]
 
 
 def per_config(args, torch, kvx, device):
@@ -602,7 +625,7 @@ def run_kvx(args, rank, local_rank, world):
             "consumer": f"{w.dst.n_shards} x [{w.dst.n_blocks}][{w.dst.block_size}][{w.dst.heads_per_shard}][{w.dst.head_dim}] x {w.dst.elem_bytes} B",
             "requests": len(reqs), "tokens": int(sum(n for n, _, _ in reqs)),
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
-            "vec_bytes": info["vec_bytes"], "kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]],
+            "vec_bytes": info["vec_bytes"], "kernel": KERNEL_SHORT[info["kernel"]],
             "lanes": info["lanes"], "bulk_stages": info["bulk_stages"],
             "threads": info["threads"],
             "ctas_per_sm": args.ctas_per_sm or "auto (below 128 MiB per launch: 5 per 4 SMs bulk, 2 persistent, 4 "
@@ -924,7 +947,7 @@ def run_match(torch, kvx, device, push_opts=None):
         "hashed_blocks": n_pub, "pushing_sessions": int(res["push"].sum()),
         "push_blocks": int(res["missing_tokens"].sum() // 64), "runs": info["n_runs"],
         "dp_push_gbs_one_layer": round(2 * info["bytes_per_layer"] / (statistics.median(push_ms) * 1e-3) / 1e9, 1),
-        "dp_push_kernel": ["auto", "tile", "persist", "bulk"][info["kernel"]], "dp_push_tile_bytes": info["tile_bytes"],
+        "dp_push_kernel": KERNEL_SHORT[info["kernel"]], "dp_push_tile_bytes": info["tile_bytes"],
         "how": "host wall clock per kvx_match_prefix call (it waits for its stream), median of 100 calls; hashes and "
                "push with CUDA events",
     }

@@ -277,9 +277,33 @@ struct BulkItem {
     int32_t n;         // strided tiles: rows of a.width bytes per head; contiguous tiles: 1
     int32_t heads;     // strided tiles: heads of the group (1 for a single head)
     int32_t layer;
+    int32_t tensor;    // TENSOR: the tile is the maps' box and moves as one tensor copy each way
+    int32_t s_buf, d_buf;             // TENSOR: buffer (map) index on each side
+    int32_t sh, ss, sb, dh, ds, db;   // TENSOR: (head, slot, block) of the tile on each side
 };
 
-template <bool STRIDED>
+__device__ __forceinline__ int64_t div_by(int64_t x, int64_t d, int32_t shift) { return shift >= 0 ? x >> shift : x / d; }
+
+// (block, slot, head) of a byte offset into one side's buffer: the offset is head_index * head bytes,
+// head_index = (block * bs + slot) * hps + head (NHD) or (block * hps + head) * bs + slot (HND).
+__device__ __forceinline__ void side_coords(const TensorSide &g, int64_t off, int32_t *blk, int32_t *slot, int32_t *head) {
+    const int64_t idx = div_by(off, g.hb, g.sh_hb);
+    if (g.layout == KVX_LAYOUT_HND) {
+        const int64_t r = div_by(idx, g.bs, g.sh_bs);
+        const int64_t b = div_by(r, g.hps, g.sh_hps);
+        *slot = (int32_t)(idx - r * g.bs);
+        *head = (int32_t)(r - b * g.hps);
+        *blk = (int32_t)b;
+    } else {
+        const int64_t r = div_by(idx, g.hps, g.sh_hps);
+        const int64_t b = div_by(r, g.bs, g.sh_bs);
+        *head = (int32_t)(idx - r * g.hps);
+        *slot = (int32_t)(r - b * g.bs);
+        *blk = (int32_t)b;
+    }
+}
+
+template <bool STRIDED, bool TENSOR>
 __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int32_t stage_bytes) {
     int64_t tile, lp;
     BulkItem it;
@@ -288,6 +312,7 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     it.src = nullptr;
     it.dst = nullptr;
     it.bytes = 0;
+    it.tensor = 0;
     it.n = STRIDED ? t.n : 1;
     it.heads = STRIDED ? max(t.heads, 1) : 1;
     const int64_t bytes = STRIDED ? (int64_t)t.n * it.heads * a.width : (int64_t)t.n;
@@ -306,10 +331,41 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
         return it;
     }
     it.bytes = (uint32_t)bytes;
+    if (TENSOR && t.n == a.box_n && it.heads == a.box_k) {
+        // the maps' box: one tensor copy each way when it stays inside a block and a shard on both sides
+        side_coords(a.ts, t.src_off, &it.sb, &it.ss, &it.sh);
+        side_coords(a.td, t.dst_off, &it.db, &it.ds, &it.dh);
+        it.s_buf = (int32_t)(lp * a.src_shards + t.s_shard);
+        it.d_buf = (int32_t)(lp * a.dst_shards + t.d_shard);
+        it.tensor = it.ss + a.box_n <= a.ts.bs && it.sh + a.box_k <= a.ts.hps && it.ds + a.box_n <= a.td.bs &&
+                    it.dh + a.box_k <= a.td.hps;
+    }
     return it;
 }
 
-template <int STAGES, bool STRIDED>
+// Tensor-map copies of one box (rank 4: head bytes / 8, head, slot, block; x always 0). The load
+// completes on the stage's mbarrier; the store joins the thread's current bulk group.
+__device__ __forceinline__ void tensor_load(void *stage, const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tensor_store(const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk, const void *stage) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                 ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage))
+                 : "memory");
+}
+
+// The maps live in global memory, written by the plan upload; a CTA acquires each map for the tensor
+// proxy before its first use.
+__device__ __forceinline__ void map_acquire(const CUtensorMap *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+template <int STAGES, bool STRIDED, bool TENSOR>
 __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, int32_t stage_bytes,
                                                      int32_t stream_l2) {
     constexpr int kBulkStages = STAGES;
@@ -336,14 +392,19 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     auto token_major = [&](const BulkItem &it) {
         return STRIDED && it.heads > 1 && a.src_head_pitch == a.width && a.dst_head_pitch != a.width;
     };
+    const CUtensorMap *fenced_src = nullptr, *fenced_dst = nullptr;   // TENSOR: maps acquired so far
     auto issue = [&](int64_t i) {
         const int s = (int)(i % kBulkStages);
-        const BulkItem it = bulk_item<STRIDED>(a, blockIdx.x + i * gridDim.x, stage_bytes);
+        const BulkItem it = bulk_item<STRIDED, TENSOR>(a, blockIdx.x + i * gridDim.x, stage_bytes);
         items[s] = it;
         mbar_arrive_expect(&bar[s], it.bytes);
         if (!it.bytes) return;
         uint8_t *stage = ring + (size_t)s * stage_bytes;
-        if (token_major(it)) {
+        if (TENSOR && it.tensor) {
+            const CUtensorMap *map = a.src_maps + it.s_buf;
+            if (map != fenced_src) { map_acquire(map); fenced_src = map; }
+            tensor_load(stage, map, it.sh, it.ss, it.sb, &bar[s]);
+        } else if (token_major(it)) {
             const uint32_t span = (uint32_t)(it.heads * a.width);    // one token's heads
             if (a.src_pitch == (int64_t)span) {
                 bulk_load(stage, it.src, it.bytes, &bar[s], hint, policy);
@@ -388,7 +449,11 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint8_t *stage = ring + (size_t)s * stage_bytes;
             const BulkItem &it = items[s];
-            if (token_major(it)) {
+            if (TENSOR && it.tensor) {
+                const CUtensorMap *map = a.dst_maps + it.d_buf;
+                if (map != fenced_dst) { map_acquire(map); fenced_dst = map; }
+                tensor_store(map, it.dh, it.ds, it.db, stage);
+            } else if (token_major(it)) {
                 for (int32_t h = 0; h < it.heads; ++h)
                     for (int32_t r = 0; r < it.n; ++r)
                         bulk_store(it.dst + (int64_t)h * a.dst_head_pitch + (int64_t)r * a.dst_pitch,
@@ -418,6 +483,155 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
     }
     bulk_wait_all();   // the stores have completed, not only read their stages
     if (a.ts_end) atomicMax(a.ts_end, (unsigned long long)global_ns());
+}
+
+// ------------------------------------------------------------------------------------------------
+// KVX_KERNEL_STAGED: strided tiles loaded by the bulk copy engine into a shared-memory ring, then
+// stored to the consumer by the CTA's threads in the consumer's own layout.
+// A tile's load side is dense in one of two orders on the usual pools -- head-major (each head's n
+// rows adjacent, heads n rows apart: a head-major producer) or token-major (each token's heads
+// adjacent: a token-major producer) -- so it lands in one bulk copy (or one per token), in that order.
+// The threads then write each row to its place on the consumer side with 16-byte stores: a head
+// transpose costs no ring slot and no latency, since stores need no answer. Thread 0 issues the loads;
+// all threads wait on the stage's mbarrier (bounded), copy it out, meet at a barrier, and thread 0
+// refills the stage.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kStagedThreads = 128;
+
+struct StageInfo {
+    uint8_t *dst;      // consumer tile base
+    uint32_t bytes;    // 0: nothing staged (skipped item)
+    int32_t n;         // rows per head
+    int32_t heads;
+    int32_t order;     // 0: head-major (row h * n + t), 1: token-major (row t * heads + h)
+    int32_t layer;
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(kStagedThreads) kvx_copy_staged(CopyArgs a, int64_t n_work, int32_t stage_bytes) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t bar[STAGES];
+    __shared__ StageInfo info[STAGES];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        if (a.ts_start) atomicMin(a.ts_start, (unsigned long long)global_ns());
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s]);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int64_t n_mine = (int64_t)blockIdx.x < n_work ? (n_work - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+    // thread 0: item i of this CTA (work item blockIdx.x + i * gridDim.x) into stage i % STAGES
+    auto issue = [&](int64_t i) {
+        const int s = (int)(i % STAGES);
+        const BulkItem it = bulk_item<true, false>(a, blockIdx.x + i * gridDim.x, stage_bytes);
+        StageInfo &si = info[s];
+        si.dst = it.dst;
+        si.bytes = it.bytes;
+        si.n = it.n;
+        si.heads = it.heads;
+        si.layer = it.layer;
+        si.order = 0;
+        uint8_t *stage = ring + (size_t)s * stage_bytes;
+        if (!it.bytes) {
+            mbar_arrive_expect(&bar[s], 0);
+            return;
+        }
+        const bool dense_hm = a.src_pitch == a.width && (it.heads == 1 || a.src_head_pitch == (int64_t)it.n * a.width);
+        const bool tok_major = !dense_hm && it.heads > 1 && a.src_head_pitch == a.width;
+        si.order = tok_major ? 1 : 0;
+        mbar_arrive_expect(&bar[s], it.bytes);   // after si is written: the arrival releases it
+        if (dense_hm) {
+            bulk_load(stage, it.src, it.bytes, &bar[s], false, 0);
+        } else if (tok_major) {
+            const uint32_t span = (uint32_t)(it.heads * a.width);     // one token's heads
+            if (a.src_pitch == (int64_t)span) {
+                bulk_load(stage, it.src, it.bytes, &bar[s], false, 0);
+            } else {
+                for (int32_t r = 0; r < it.n; ++r)
+                    bulk_load(stage + (size_t)r * span, it.src + (int64_t)r * a.src_pitch, span, &bar[s], false, 0);
+            }
+        } else {
+            for (int32_t h = 0; h < it.heads; ++h)
+                for (int32_t r = 0; r < it.n; ++r)
+                    bulk_load(stage + (size_t)(h * it.n + r) * a.width,
+                              it.src + (int64_t)h * a.src_head_pitch + (int64_t)r * a.src_pitch, (uint32_t)a.width,
+                              &bar[s], false, 0);
+        }
+    };
+
+    if (tid == 0)
+        for (int64_t i = 0; i < n_mine && i < STAGES; ++i) issue(i);
+    const int32_t vpr = a.width >> 4;                 // 16-byte vectors per row
+    bool stall = a.stall_layer >= 0 && blockIdx.x == 0;   // testing hook (kvx_plan_inject_stall)
+    bool timed_out = false;
+    int64_t consumed = 0;
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int s = (int)(i % STAGES);
+        const uint32_t parity = (uint32_t)((i / STAGES) & 1);
+        bool landed = mbar_wait(&bar[s], parity, a.wait_ns);
+        const StageInfo si = info[s];
+        if (landed && stall && si.layer == a.stall_layer) {
+            // the hook: once the stage's loads landed, wait for its next phase, which nothing arms
+            stall = false;
+            landed = mbar_wait(&bar[s], parity ^ 1u, a.wait_ns);
+        }
+        if (__syncthreads_or(!landed)) {
+            if (tid == 0) {
+                const int32_t per_layer = (int32_t)(a.n_tiles * a.n_planes);
+                const int32_t l_last = a.layer0 + (int32_t)((blockIdx.x + (n_mine - 1) * gridDim.x) / per_layer);
+                for (int32_t l = si.layer; l <= l_last; ++l) atomicOr(&a.err[l], 2);
+            }
+            timed_out = true;
+            break;
+        }
+        consumed = i + 1;
+        if (si.bytes) {
+            const uint8_t *stage = ring + (size_t)s * stage_bytes;
+            const int32_t rows = si.n * si.heads;
+            const uint32_t split = si.order ? (uint32_t)si.heads : (uint32_t)si.n;   // inner extent of a row index
+            if (vpr <= kStagedThreads) {
+                const int32_t rpp = kStagedThreads / vpr;                  // rows per pass
+                const int32_t my = tid / vpr, col = tid - (tid / vpr) * vpr;
+                if (my < rpp) {
+                    for (int32_t row = my; row < rows; row += rpp * kUnroll) {
+                        uint4 v[kUnroll];
+                        int64_t off[kUnroll];
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const uint32_t r = (uint32_t)(row + u * rpp);
+                            if ((int32_t)r < rows) {
+                                const uint32_t hi = r / split, lo = r - hi * split;
+                                const int64_t h = si.order ? lo : hi, t = si.order ? hi : lo;
+                                off[u] = h * a.dst_head_pitch + t * a.dst_pitch + (int64_t)col * 16;
+                                v[u] = *reinterpret_cast<const uint4 *>(stage + (size_t)r * a.width + (size_t)col * 16);
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u)
+                            if (row + u * rpp < rows) *reinterpret_cast<uint4 *>(si.dst + off[u]) = v[u];
+                    }
+                }
+            } else {
+                for (int32_t r = 0; r < rows; ++r) {
+                    const uint32_t hi = (uint32_t)r / split, lo = (uint32_t)r - hi * split;
+                    const int64_t h = si.order ? lo : hi, t = si.order ? hi : lo;
+                    uint8_t *d = si.dst + h * a.dst_head_pitch + t * a.dst_pitch;
+                    for (int32_t c = tid; c < vpr; c += kStagedThreads)
+                        reinterpret_cast<uint4 *>(d)[c] = reinterpret_cast<const uint4 *>(stage + (size_t)r * a.width)[c];
+                }
+            }
+        }
+        __syncthreads();   // every thread has read stage s: it may be refilled
+        if (tid == 0 && i + STAGES < n_mine) issue(i + STAGES);
+    }
+    if (timed_out && tid == 0) {
+        // give every load still in flight a bounded chance to land before the ring goes away
+        const int64_t issued = n_mine < consumed + STAGES ? n_mine : consumed + STAGES;
+        for (int64_t j = consumed; j < issued; ++j) mbar_wait(&bar[j % STAGES], (uint32_t)((j / STAGES) & 1), a.wait_ns);
+    }
+    stamp_end(a);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -469,19 +683,29 @@ static cudaError_t resident_grid(const void *fn, int threads, int smem, int per_
     return cudaSuccess;
 }
 
-template <bool STRIDED>
+template <bool STRIDED, bool TENSOR>
 static const void *bulk_fn_of(int stages) {
     switch (stages) {
-        case 2: return (const void *)kvx_copy_bulk<2, STRIDED>;
-        case 3: return (const void *)kvx_copy_bulk<3, STRIDED>;
-        case 6: return (const void *)kvx_copy_bulk<6, STRIDED>;
-        case 8: return (const void *)kvx_copy_bulk<8, STRIDED>;
-        default: return (const void *)kvx_copy_bulk<4, STRIDED>;
+        case 2: return (const void *)kvx_copy_bulk<2, STRIDED, TENSOR>;
+        case 3: return (const void *)kvx_copy_bulk<3, STRIDED, TENSOR>;
+        case 6: return (const void *)kvx_copy_bulk<6, STRIDED, TENSOR>;
+        case 8: return (const void *)kvx_copy_bulk<8, STRIDED, TENSOR>;
+        default: return (const void *)kvx_copy_bulk<4, STRIDED, TENSOR>;
     }
 }
 
-static const void *bulk_fn(int stages, bool strided) {
-    return strided ? bulk_fn_of<true>(stages) : bulk_fn_of<false>(stages);
+static const void *staged_fn(int stages) {
+    switch (stages) {
+        case 2: return (const void *)kvx_copy_staged<2>;
+        case 3: return (const void *)kvx_copy_staged<3>;
+        case 6: return (const void *)kvx_copy_staged<6>;
+        case 8: return (const void *)kvx_copy_staged<8>;
+        default: return (const void *)kvx_copy_staged<4>;
+    }
+}
+
+static const void *bulk_fn(int stages, bool strided, bool tensor) {
+    return tensor ? bulk_fn_of<true, true>(stages) : strided ? bulk_fn_of<true, false>(stages) : bulk_fn_of<false, false>(stages);
 }
 
 template <int VEC>
@@ -495,24 +719,41 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
     count_launch();
     int grid = 0;
     cudaError_t e;
-    if (sh.kernel == KVX_KERNEL_BULK) {
-        // Launches that read under 128 MiB (a layer push) default to 5 CTAs per 4 SMs: measured on
-        // GB300 in the per-layer push pattern, 1.25 CTAs per SM beat 1 (0.965 against 0.949 of the
-        // copy peak, consecutive launches overlapping on the lanes) and 2 (0.90). Head-group plans
-        // (bulk only when asked for, or two head-major pools alike) default to 2 per SM: row-by-row
-        // copies leave one issuing thread per CTA busier (0.59 against 0.50 at 1 per SM on a
-        // token-major -> head-major push). Larger launches take the occupancy limit.
+    if (sh.kernel == KVX_KERNEL_STAGED) {
         const int smem = sh.stages * sh.tile_bytes;
         const bool small = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20);
         const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (small ? 2 : 64);
-        const void *fn = bulk_fn(sh.stages, sh.strided != 0);
-        int sms = 0;
-        e = resident_grid(fn, 32, smem, cap, &grid, &sms);
+        const void *fn = staged_fn(sh.stages);
+        e = resident_grid(fn, kStagedThreads, smem, cap, &grid);
         if (e != cudaSuccess) return e;
-        if (!sh.ctas_per_sm && small) grid = std::min(grid, sh.head_groups ? 2 * sms : sms + sms / 4);
+        if (sh.max_ctas > 0) grid = std::min(grid, sh.max_ctas);
         CopyArgs args_copy = a;
         int64_t work = n_work;
         int32_t stage_bytes = sh.tile_bytes;
+        void *args[] = {&args_copy, &work, &stage_bytes};
+        return cudaLaunchKernel(fn, dim3((unsigned)std::min<int64_t>(grid, n_work)), dim3(kStagedThreads), args,
+                                (size_t)smem, st);
+    }
+    if (ring_kernel(sh.kernel)) {
+        // Launches that read under 128 MiB (a layer push) default to 2 CTAs per SM with a 3-stage
+        // ring: measured on GB300, contiguous 64 MiB pushes ran at 0.999 of the copy peak in the
+        // per-layer step (consecutive launches overlapping on the lanes) and 0.81 alone, against
+        // 0.991 / 0.81 at 1.25 CTAs per SM with 4 stages and 0.94 / 0.85 at 2 per SM with 4 (the
+        // deeper ring leaves the next launch no room beside it). Larger launches take the occupancy
+        // limit. TENSOR stages are 128-byte aligned for the tensor copies.
+        const bool tensor = sh.kernel == KVX_KERNEL_TENSOR;
+        const int32_t stage_bytes_k = tensor ? (int32_t)align_up((size_t)sh.tile_bytes, 128) : sh.tile_bytes;
+        const int smem = sh.stages * stage_bytes_k;
+        const bool small = n_work * (int64_t)sh.tile_bytes < ((int64_t)128 << 20);
+        const int cap = sh.ctas_per_sm ? sh.ctas_per_sm : (small ? 2 : 64);
+        const void *fn = bulk_fn(sh.stages, sh.strided != 0, tensor);
+        int sms = 0;
+        e = resident_grid(fn, 32, smem, cap, &grid, &sms);
+        if (e != cudaSuccess) return e;
+        if (sh.max_ctas > 0) grid = std::min(grid, sh.max_ctas);
+        CopyArgs args_copy = a;
+        int64_t work = n_work;
+        int32_t stage_bytes = stage_bytes_k;
         // evict-first L2 hints for contiguous launches that stream at least kStreamL2Bytes. Smaller
         // ones keep the default policy (a 1 MB push whose blocks stay in L2 between steps ran 7 %
         // slower with it), and so do strided ones: rows written one by one into lines that other
@@ -534,6 +775,7 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
                        : persist_fn<1>(sh.strided);
         e = resident_grid(fn, sh.threads, 0, shape.ctas_per_sm, &grid);
         if (e != cudaSuccess) return e;
+        if (sh.max_ctas > 0) grid = std::min(grid, sh.max_ctas);
         grid = (int)std::min<int64_t>(grid, n_work);
     }
     switch (sh.vec) {

@@ -3,6 +3,8 @@
 
 #include "kvx.h"
 
+#include <cuda.h>   // CUtensorMap (the type; the encoder is fetched from the driver at run time)
+
 #include <atomic>
 #include <cstdint>
 #include <vector>
@@ -24,6 +26,14 @@ struct alignas(16) TileDesc {
 };
 static_assert(sizeof(TileDesc) == 32, "TileDesc is two 16-byte words");
 
+// TENSOR plans: what the kernel needs to turn a tile's byte offsets into tensor-map coordinates
+// (head, slot, block) on each side, and the maps' box (box_n token slots x box_k heads).
+struct TensorSide {
+    int64_t hb;                       // head bytes
+    int32_t layout, bs, hps;
+    int32_t sh_hb, sh_bs, sh_hps;     // log2 of hb / bs / hps when a power of two, else -1
+};
+
 // Kernel arguments of one push launch (passed by value).
 struct CopyArgs {
     const TileDesc *tiles;
@@ -41,6 +51,10 @@ struct CopyArgs {
     unsigned long long *ts_end;       // timing: atomicMax of %globaltimer at each CTA's end
     uint64_t wait_ns;                 // bulk: limit of one wait for a ring stage (kBulkWaitNs)
     int32_t stall_layer;              // bulk, testing hook: this layer's first item on CTA 0 never completes (-1: none)
+    const CUtensorMap *src_maps;      // TENSOR: one map per producer buffer (device, 64-byte aligned)
+    const CUtensorMap *dst_maps;      // TENSOR: one map per consumer buffer
+    TensorSide ts, td;                // TENSOR: producer / consumer geometry
+    int32_t box_n, box_k;             // TENSOR: the maps' box
     int32_t width;                    // strided: bytes copied per row
     int32_t n_planes;
     int32_t src_shards;
@@ -132,6 +146,7 @@ struct LaunchShape {
     int32_t ctas_per_sm;   // 0: occupancy limit
     int32_t stages;        // bulk: ring stages (2, 3, 4, 6 or 8)
     int32_t head_groups;   // tiles are head groups (a head-major side): many small row copies per tile
+    int32_t max_ctas;      // upper bound on the launch's CTAs (0: none)
 };
 cudaError_t launch_copy(const CopyArgs &args, int32_t n_layers, const LaunchShape &shape, cudaStream_t stream);
 
@@ -167,6 +182,9 @@ struct kvx_plan_s {
     int32_t bulk_stages_req = 0;               // ring stages asked for (0: by plan kind)
     int32_t bulk_stages = 4;                   // ring stages of the bulk kernel, resolved
     int32_t layers_per_launch_req = 0;         // kvx_push_layers: layers per launch asked for (0: by size)
+    int32_t max_ctas = 0;                      // upper bound on CTAs per copy launch (0: none)
+    int32_t box_n = 0, box_k = 0;              // TENSOR: token slots x heads of a tile the maps move at once
+    std::vector<CUtensorMap> maps;             // TENSOR: producer buffers' maps, then consumer buffers' (host)
     int32_t outside_device = -1;               // a pool buffer outside device memory (-1: not checked yet)
     int32_t next_lane = 0;
     cudaEvent_t fork_evt = nullptr;            // recorded on the caller's stream before each lane push
@@ -179,7 +197,7 @@ struct kvx_plan_s {
     // device copy: [tiles][src_base][dst_base][err][runs: device-built plans only]
     void *dev = nullptr;
     size_t dev_bytes = 0;
-    size_t off_tiles = 0, off_src = 0, off_dst = 0, off_err = 0, off_runs = 0;
+    size_t off_tiles = 0, off_src = 0, off_dst = 0, off_err = 0, off_runs = 0, off_maps = 0;
     int64_t run_cap = 0;                       // device-built plans: run slots (src rows, dst rows, tokens)
     int64_t n_runs_dev = -1;                   // device-built plans: runs held on the device until asked for
     int64_t device_tokens = 0;                 // device-built plans: tokens copied per (layer, plane, shard)
@@ -205,9 +223,22 @@ struct kvx_plan_s {
 namespace kvx {
 // The kernel a plan's pushes run: pools outside device memory (host memory over the chip-to-chip
 // link, managed memory) are copied with plain loads and stores, never by the bulk copy path.
+// TENSOR plans whose descriptors went up without tensor maps (the driver refused one, or the kernel
+// was chosen by kvx_plan_set_opts after the first push) run PERSIST.
 inline int32_t effective_kernel(const kvx_plan_s *pl) {
-    return pl->kernel == KVX_KERNEL_BULK && pl->outside_device == 1 ? KVX_KERNEL_PERSIST : pl->kernel;
+    const bool async_copy = pl->kernel == KVX_KERNEL_BULK || pl->kernel == KVX_KERNEL_TENSOR ||
+                            pl->kernel == KVX_KERNEL_STAGED;
+    if (async_copy && pl->outside_device == 1) return KVX_KERNEL_PERSIST;
+    if (pl->kernel == KVX_KERNEL_TENSOR && pl->uploaded && pl->maps.empty()) return KVX_KERNEL_PERSIST;
+    return pl->kernel;
 }
+// The ring kernels (BULK, TENSOR) run one issuing thread per 32-thread CTA; STAGED has the same
+// ring with 128 threads storing.
+inline bool ring_kernel(int32_t k) { return k == KVX_KERNEL_BULK || k == KVX_KERNEL_TENSOR; }
+inline bool staged_kernel(int32_t k) { return k == KVX_KERNEL_STAGED; }
+// TENSOR plans: encodes one tensor map per pool buffer into pl->maps (host); false when the driver
+// refuses a map (the plan then runs PERSIST) (kvx_push.cu).
+bool encode_tensor_maps(kvx_plan_s *pl);
 // Checks where the pools' buffers live (first and last buffer of each side) and records it; refuses
 // pageable host memory the GPU cannot reach (kvx_push.cu).
 kvx_status check_pool_memory(kvx_plan_s *pl);

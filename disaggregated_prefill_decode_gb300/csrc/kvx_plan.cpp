@@ -115,7 +115,9 @@ kvx_status init_plan_geometry(const kvx_pool *src, const kvx_pool *dst, const kv
         if (opts->threads) pl->threads = opts->threads;
         pl->threads_req = opts->threads;
         pl->flags = opts->flags;
-        if (opts->kernel < 0 || opts->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", opts->kernel);
+        if (opts->kernel < 0 || opts->kernel > KVX_KERNEL_STAGED) return fail(KVX_EINVAL, "unknown kernel %d", opts->kernel);
+        if (opts->max_ctas < 0) return fail(KVX_EINVAL, "max_ctas must be >= 0");
+        pl->max_ctas = opts->max_ctas;
         if (opts->ctas_per_sm < 0 || opts->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
         if (opts->lanes < 0 || opts->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
         pl->kernel = opts->kernel;
@@ -232,7 +234,8 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     if (o->layers_per_launch < 0) return fail(KVX_EINVAL, "layers_per_launch must be >= 0");
     if (!valid_stages(o->bulk_stages)) return fail(KVX_EINVAL, "bulk_stages must be 0, 2, 3, 4, 6 or 8");
     if (o->flags & ~KVX_PLAN_TIMING) return fail(KVX_EINVAL, "unknown kvx_plan_opts.flags bits");
-    if (o->kernel < 0 || o->kernel > KVX_KERNEL_BULK) return fail(KVX_EINVAL, "unknown kernel %d", o->kernel);
+    if (o->kernel < 0 || o->kernel > KVX_KERNEL_STAGED) return fail(KVX_EINVAL, "unknown kernel %d", o->kernel);
+    if (o->max_ctas < 0) return fail(KVX_EINVAL, "max_ctas must be >= 0");
     if (o->ctas_per_sm < 0 || o->ctas_per_sm > 64) return fail(KVX_EINVAL, "ctas_per_sm in [0, 64]");
     if (o->lanes < 0 || o->lanes > 8) return fail(KVX_EINVAL, "lanes in [0, 8]");
     if (o->threads && (o->threads < 32 || o->threads > 1024 || o->threads % 32))
@@ -244,6 +247,7 @@ kvx_status kvx_plan_set_opts(kvx_plan_t pl, const kvx_plan_opts *o) {
     pl->lanes = o->lanes ? o->lanes : 4;
     pl->bulk_stages_req = o->bulk_stages;
     pl->layers_per_launch_req = o->layers_per_launch;
+    pl->max_ctas = o->max_ctas;
     pl->next_lane = 0;
     pl->lane_cache.clear();
     pl->lane_src = nullptr;
@@ -289,9 +293,9 @@ kvx_status kvx_plan_get_info(kvx_plan_t pl, kvx_plan_info *out) {
     out->tile_bytes = pl->tile_bytes;
     const int32_t k = effective_kernel(pl);
     out->kernel = k;
-    out->threads = k == KVX_KERNEL_BULK ? 32 : pl->threads;
+    out->threads = ring_kernel(k) ? 32 : staged_kernel(k) ? 128 : pl->threads;
     out->lanes = pl->lanes;
-    out->bulk_stages = k == KVX_KERNEL_BULK ? pl->bulk_stages : 0;
+    out->bulk_stages = ring_kernel(k) || staged_kernel(k) ? pl->bulk_stages : 0;
     out->src_pitch = pl->src_pitch;
     out->dst_pitch = pl->dst_pitch;
     out->src_head_pitch = pl->src_head_pitch;
@@ -345,8 +349,9 @@ kvx_status kvx_plan_inject_failure(kvx_plan_t pl, int32_t layer) {
 kvx_status kvx_plan_inject_stall(kvx_plan_t pl, int32_t layer) {
     if (!pl) return fail(KVX_EINVAL, "NULL plan");
     if (layer < 0 || layer >= pl->src.n_layers) return fail(KVX_EINVAL, "layer %d out of range", layer);
-    if (effective_kernel(pl) != KVX_KERNEL_BULK)
-        return fail(KVX_EUNSUPPORTED, "the stall hook needs a plan whose pushes run the bulk kernel");
+    const int32_t k = effective_kernel(pl);
+    if (!ring_kernel(k) && !staged_kernel(k))
+        return fail(KVX_EUNSUPPORTED, "the stall hook needs a plan whose pushes run a shared-memory ring kernel");
     pl->stall[layer] = 1;
     return KVX_OK;
 }

@@ -139,7 +139,98 @@ void plan_layout(kvx_plan_s *pl) {
     pl->off_dst = pl->off_src + align_up(sizeof(void *) * pl->src_base.size(), a);
     pl->off_err = pl->off_dst + align_up(sizeof(void *) * pl->dst_base.size(), a);
     pl->off_runs = pl->off_err + align_up(sizeof(int32_t) * (size_t)pl->src.n_layers, a);
-    pl->dev_bytes = pl->off_runs + align_up(sizeof(int32_t) * 3 * (size_t)pl->run_cap, a);
+    pl->off_maps = pl->off_runs + align_up(sizeof(int32_t) * 3 * (size_t)pl->run_cap, a);
+    pl->dev_bytes = pl->off_maps + align_up(sizeof(CUtensorMap) * pl->maps.size(), a);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor maps (TENSOR plans)
+// ------------------------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encoder() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Maps already encoded, by (buffer base, side geometry, box): plans rebuilt every step over the same
+// pools find theirs here instead of encoding one per buffer again.
+using MapKey = std::tuple<uintptr_t, int32_t, int32_t, int32_t, int64_t, int64_t, int32_t, int32_t>;
+static std::mutex g_map_mu;
+static std::map<MapKey, CUtensorMap> g_map_cache;
+
+// One side's buffer as a rank-4 tensor of 8-byte elements: (head bytes / 8, head, token slot, block),
+// strides from the layout (NHD: a head's row follows the previous head's, a slot follows all heads;
+// HND: a slot's row follows the previous slot's, a head follows all slots). The box is
+// (head bytes / 8, box_k heads, box_n slots, 1 block): a load lands in shared memory slot-major,
+// heads inner, whichever the side's layout, and a store writes it back in the other side's layout.
+static bool encode_one(const Geom &g, void *base, int32_t box_n, int32_t box_k, CUtensorMap *out) {
+    const MapKey key{(uintptr_t)base, g.layout, g.block_size, g.heads_per_shard, g.head_bytes(), g.n_blocks, box_n,
+                     box_k};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_map_cache.find(key);
+        if (it != g_map_cache.end()) { *out = it->second; return true; }
+    }
+    EncodeTiledFn enc = encoder();
+    if (!enc || g.n_blocks < 1) return false;
+    const int64_t hb = g.head_bytes();
+    const cuuint64_t dim[4] = {(cuuint64_t)(hb / 8), (cuuint64_t)g.heads_per_shard, (cuuint64_t)g.block_size,
+                               (cuuint64_t)g.n_blocks};
+    const cuuint64_t row = (cuuint64_t)g.row_bytes(), blk = (cuuint64_t)g.block_size * row;
+    const cuuint64_t stride_nhd[3] = {(cuuint64_t)hb, row, blk};
+    const cuuint64_t stride_hnd[3] = {(cuuint64_t)(g.block_size * hb), (cuuint64_t)hb, blk};
+    const cuuint32_t box[4] = {(cuuint32_t)(hb / 8), (cuuint32_t)box_k, (cuuint32_t)box_n, 1};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, base, dim,
+                           g.layout == KVX_LAYOUT_HND ? stride_hnd : stride_nhd, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_map_cache.size() >= 65536) g_map_cache.clear();
+    g_map_cache.emplace(key, *out);
+    return true;
+}
+
+bool encode_tensor_maps(kvx_plan_s *pl) {
+    const size_t ns = pl->src_base.size(), nd = pl->dst_base.size();
+    pl->maps.resize(ns + nd);
+    for (size_t i = 0; i < ns; ++i)
+        if (!encode_one(pl->src, pl->src_base[i], pl->box_n, pl->box_k, &pl->maps[i])) { pl->maps.clear(); return false; }
+    for (size_t i = 0; i < nd; ++i)
+        if (!encode_one(pl->dst, pl->dst_base[i], pl->box_n, pl->box_k, &pl->maps[ns + i])) { pl->maps.clear(); return false; }
+    return true;
+}
+
+static int32_t log2_or_minus1(int64_t v) {
+    if (v <= 0 || (v & (v - 1))) return -1;
+    int32_t k = 0;
+    while ((int64_t)1 << k != v) ++k;
+    return k;
+}
+
+static TensorSide tensor_side(const Geom &g) {
+    TensorSide t;
+    t.hb = g.head_bytes();
+    t.layout = g.layout;
+    t.bs = g.block_size;
+    t.hps = g.heads_per_shard;
+    t.sh_hb = log2_or_minus1(t.hb);
+    t.sh_bs = log2_or_minus1(t.bs);
+    t.sh_hps = log2_or_minus1(t.hps);
+    return t;
 }
 
 kvx_status check_pool_memory(kvx_plan_s *pl) {
@@ -175,6 +266,14 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
     a.ts_end = nullptr;
     a.wait_ns = kBulkWaitNs;
     a.stall_layer = -1;
+    const CUtensorMap *maps =
+        pl->maps.empty() ? nullptr : reinterpret_cast<const CUtensorMap *>(base + pl->off_maps);
+    a.src_maps = maps;
+    a.dst_maps = maps ? maps + pl->src_base.size() : nullptr;
+    a.ts = tensor_side(pl->src);
+    a.td = tensor_side(pl->dst);
+    a.box_n = pl->box_n;
+    a.box_k = pl->box_k;
     a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();
@@ -210,6 +309,8 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     }
     kvx_status st = check_pool_memory(pl);
     if (st) return st;
+    // TENSOR plans encode a tensor map per buffer; a map the driver refuses sends the plan to PERSIST
+    if (effective_kernel(pl) == KVX_KERNEL_TENSOR && !encode_tensor_maps(pl)) pl->kernel = KVX_KERNEL_PERSIST;
     plan_layout(pl);
     st = pool_alloc(&pl->dev, pl->dev_bytes, stream);
     if (st) return st;
@@ -220,6 +321,7 @@ static kvx_status ensure_device(kvx_plan_s *pl, cudaStream_t stream) {
     if (pl->n_tiles) memcpy(img + pl->off_tiles, pl->tiles.data(), sizeof(TileDesc) * (size_t)pl->n_tiles);
     memcpy(img + pl->off_src, pl->src_base.data(), sizeof(void *) * pl->src_base.size());
     memcpy(img + pl->off_dst, pl->dst_base.data(), sizeof(void *) * pl->dst_base.size());
+    if (!pl->maps.empty()) memcpy(img + pl->off_maps, pl->maps.data(), sizeof(CUtensorMap) * pl->maps.size());
     cudaError_t e = cudaMemcpyAsync(pl->dev, img, pl->dev_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan upload)");
     st = event_take(&pl->upload_evt);
@@ -292,13 +394,13 @@ static kvx_status launch_tracked(kvx_plan_s *pl, int32_t l0, int32_t l1, cudaStr
     int32_t slot = -1;
     if ((pl->flags & KVX_PLAN_TIMING) && (int32_t)pl->pending.size() < kTimingSlots) slot = (int32_t)pl->pending.size();
     const LaunchShape shape{effective_kernel(pl), pl->vec, pl->strided, pl->threads, pl->tile_bytes, pl->ctas_per_sm,
-                            pl->bulk_stages, pl->per_head};
+                            pl->bulk_stages, pl->per_head, pl->max_ctas};
     CopyArgs args = plan_copy_args(pl, l0);
     if (slot >= 0) {
         args.ts_start = pl->ts + slot;
         args.ts_end = pl->ts + kTimingSlots + slot;
     }
-    for (int32_t l = l0; l < l1 && shape.kernel == KVX_KERNEL_BULK; ++l) {
+    for (int32_t l = l0; l < l1 && (ring_kernel(shape.kernel) || staged_kernel(shape.kernel)); ++l) {
         if (!pl->stall[l]) continue;
         args.stall_layer = l;              // testing hook: one stage of this layer never completes
         args.wait_ns = kBulkStallWaitNs;

@@ -190,6 +190,23 @@ static int32_t default_tile_bytes(const Geom &s, const Geom &d) {
     return (int32_t)std::max<int64_t>(16, t - t % 16);
 }
 
+// Default tile of a plan that maps one head layout onto another: a segment of min(block sizes)
+// tokens for the most heads a producer shard and a consumer shard share that fit kHeadTileTarget
+// bytes, the head count a divisor of the shared group so that every group splits into equal tiles
+// (each then one tensor-map copy per side; see tensor_box).
+constexpr int64_t kHeadTileTarget = 16384;
+
+static int32_t default_head_tile_bytes(const Geom &s, const Geom &d) {
+    const int64_t hb = s.head_bytes();
+    const int64_t n = std::min(s.block_size, d.block_size);
+    const int32_t group = std::min(s.heads_per_shard, d.heads_per_shard);
+    int32_t k = 1;
+    for (int32_t c = group; c >= 1; --c)
+        if (group % c == 0 && c * n * hb <= kHeadTileTarget) { k = c; break; }
+    const int64_t t = std::max<int64_t>(16, std::min<int64_t>((int64_t)k * n * hb, kHeadTileTarget));
+    return (int32_t)(t - t % 16);
+}
+
 // Copy shape from the two geometries: head-major sides copy per (block segment, head), unequal head
 // partitions copy strided rows of the shared head range, and the rest copies contiguous bytes.
 void init_copy_shape(kvx_plan_s *pl, bool tile_bytes_given) {
@@ -203,6 +220,7 @@ void init_copy_shape(kvx_plan_s *pl, bool tile_bytes_given) {
     pl->src_head_pitch = pl->per_head ? (s.layout == KVX_LAYOUT_HND ? s.block_size : 1) * s.head_bytes() : 0;
     pl->dst_head_pitch = pl->per_head ? (d.layout == KVX_LAYOUT_HND ? d.block_size : 1) * d.head_bytes() : 0;
     if (!tile_bytes_given && !pl->strided) pl->tile_bytes = default_tile_bytes(s, d);
+    if (!tile_bytes_given && pl->per_head && !same_head_major(s, d)) pl->tile_bytes = default_head_tile_bytes(s, d);
 }
 
 // A plan that only ever copies whole blocks between two head-major pools with the same head
@@ -235,22 +253,54 @@ bool as_whole_block_copy(kvx_plan_s *pl) {
 // sides alike copy whole blocks as single spans and keep the bulk kernel (0.94-0.95 against 0.76).
 constexpr int64_t kLargeLayer = (int64_t)128 << 20;
 
+// The box of a TENSOR plan's maps: tiles of box_n token slots for box_k heads go through the maps
+// (segments of min(block sizes) tokens, or tile_bytes / head_bytes of them when a head's segment is
+// longer than a tile; as many heads as build_head_tiles puts in such a tile).
+static void tensor_box(kvx_plan_s *pl) {
+    const int64_t hb = pl->src.head_bytes();
+    const int64_t rows = std::max<int64_t>(1, pl->tile_bytes / hb);
+    const int64_t seg = std::min(pl->src.block_size, pl->dst.block_size);
+    const int32_t group = std::min(pl->src.heads_per_shard, pl->dst.heads_per_shard);
+    pl->box_n = (int32_t)std::min<int64_t>(seg, rows);
+    pl->box_k = pl->box_n == seg ? (int32_t)std::min<int64_t>(group, std::max<int64_t>(1, rows / seg)) : 1;
+}
+
+// A TENSOR plan needs head rows the maps can describe (16..2048 bytes, 16-byte multiples, a box of
+// at most 256 per dimension that fits a ring stage) and host-built tiles.
+static bool tensor_ok(const kvx_plan_s *pl) {
+    const int64_t hb = pl->src.head_bytes();
+    return pl->per_head && !same_head_major(pl->src, pl->dst) && !pl->device_built && pl->vec == 16 && hb % 16 == 0 &&
+           hb <= 2048 && pl->box_n >= 1 && pl->box_n <= 256 && pl->box_k >= 1 && pl->box_k <= 256 &&
+           (int64_t)pl->box_n * pl->box_k * hb <= pl->tile_bytes &&
+           (int64_t)align_up((size_t)pl->tile_bytes, 128) * pl->bulk_stages <= kBulkRingMax;
+}
+
 static void resolve_kernel(kvx_plan_s *pl) {
     const bool bulk_ok = pl->vec == 16 && (int64_t)pl->tile_bytes * pl->bulk_stages <= kBulkRingMax &&
                          (!pl->strided || pl->width <= pl->tile_bytes);
+    // STAGED: strided tiles whose rows are whole 16-byte vectors (loads by the bulk engine, stores by
+    // the CTA's threads)
+    const bool staged_ok = bulk_ok && pl->strided && pl->width % 16 == 0;
     const bool large = pl->bytes_per_layer >= kLargeLayer;
     const bool automatic = pl->kernel == KVX_KERNEL_AUTO;
     const bool row_groups = pl->per_head && !same_head_major(pl->src, pl->dst);
-    int32_t k = automatic ? (bulk_ok && !large && !row_groups ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST) : pl->kernel;
+    tensor_box(pl);
+    int32_t k = pl->kernel;
+    if (automatic) k = row_groups ? (staged_ok ? KVX_KERNEL_STAGED : KVX_KERNEL_PERSIST)
+                                  : (bulk_ok && !large ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST);
+    if (k == KVX_KERNEL_TENSOR && !tensor_ok(pl)) k = row_groups ? KVX_KERNEL_PERSIST : KVX_KERNEL_BULK;
+    if (k == KVX_KERNEL_STAGED && !staged_ok) k = bulk_ok ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST;
     if (k == KVX_KERNEL_BULK && !bulk_ok) k = KVX_KERNEL_PERSIST;
     pl->kernel = k;
     pl->threads = pl->threads_req ? pl->threads_req : (automatic && (large || row_groups) ? 128 : 256);
 }
 
-// Default ring depth: measured on GB300, strided tiles (rows scattered on one side) run fastest with
-// a 3-stage ring (four CTAs per SM fit beside each other), contiguous ones with 4.
+// Default ring depth: 3 stages (measured on GB300: strided tiles, rows scattered on one side, ran
+// fastest with 3; contiguous ones at 2 CTAs per SM with 3 stages reached 0.999 of the copy peak in
+// the per-layer step and 0.81 for a launch alone, against 0.991 / 0.81 with 4 stages at 1.25 CTAs
+// per SM).
 static void resolve_stages(kvx_plan_s *pl) {
-    pl->bulk_stages = pl->bulk_stages_req ? pl->bulk_stages_req : (pl->strided ? 3 : 4);
+    pl->bulk_stages = pl->bulk_stages_req ? pl->bulk_stages_req : 3;
 }
 
 void resolve_launch(kvx_plan_s *pl) {

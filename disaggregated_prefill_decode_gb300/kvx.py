@@ -41,11 +41,11 @@ class kvx_request(ctypes.Structure):
 
 class kvx_plan_opts(ctypes.Structure):
     _fields_ = [("tile_bytes", c_i32), ("threads", c_i32), ("flags", c_i32), ("kernel", c_i32), ("ctas_per_sm", c_i32),
-                ("lanes", c_i32), ("bulk_stages", c_i32), ("layers_per_launch", c_i32)]
+                ("lanes", c_i32), ("bulk_stages", c_i32), ("layers_per_launch", c_i32), ("max_ctas", c_i32)]
 
 
 KVX_PLAN_TIMING = 1
-KVX_KERNEL_AUTO, KVX_KERNEL_TILE, KVX_KERNEL_PERSIST, KVX_KERNEL_BULK = range(4)
+KVX_KERNEL_AUTO, KVX_KERNEL_TILE, KVX_KERNEL_PERSIST, KVX_KERNEL_BULK, KVX_KERNEL_TENSOR, KVX_KERNEL_STAGED = range(6)
 
 
 class kvx_plan_info(ctypes.Structure):
@@ -265,7 +265,8 @@ def kvx_plan(src: Pool, dst: Pool, requests: Iterable) -> Plan:
     return kvx_plan_ex(src, dst, requests, None)
 
 
-_OPT_KEYS = ("tile_bytes", "threads", "flags", "kernel", "ctas_per_sm", "lanes", "bulk_stages", "layers_per_launch")
+_OPT_KEYS = ("tile_bytes", "threads", "flags", "kernel", "ctas_per_sm", "lanes", "bulk_stages", "layers_per_launch",
+             "max_ctas")
 
 
 def _opts(opts: dict) -> kvx_plan_opts:

@@ -134,7 +134,26 @@ typedef struct kvx_plan_opts {
                                  call spread over the lanes (0: as many as make about 256 MiB
                                  moved, read + write, per launch when lanes > 1, at least one;
                                  the whole range in one launch when lanes = 1)                   */
+    int32_t max_ctas;         /* upper bound on the CTAs of one copy launch (0: none). A push beside
+                                 a kernel that fills whole SMs -- a tensor-core GEMM holding every
+                                 register of an SM -- costs that kernel the SMs the copy occupies;
+                                 a few CTAs with a deep ring (bulk_stages) move the same bytes on
+                                 fewer SMs for longer                                            */
 } kvx_plan_opts;
+
+/* STAGED (strided plans with rows of whole 16-byte vectors): the bulk ring with 128 threads per
+ * CTA. A tile lands in its stage in the producer's row order (one bulk copy when the producer side
+ * of the tile is one span, else one per token or per row); the threads then store every row to its
+ * place in the consumer's layout with 16-byte stores, so a head transpose needs no ring slot on the
+ * store side.
+ * TENSOR (plans with one token-major and one head-major side, or head-major sides that differ in
+ * block size or head split): the bulk ring of BULK, but each tile of a head group is one tensor-map
+ * (TMA) load and one tensor-map store. Every pool buffer gets a tensor map of its own layout --
+ * dimensions (head bytes, head, token slot, block) with that layout's strides -- and both maps
+ * traverse a tile in the same order, so a token-major tile lands head-major (or back) in the copy
+ * itself, one bulk operation per side instead of one per row. Tiles of another shape (a partial last
+ * block) move row by row. Needs 16-byte aligned buffers and head rows of 16..2048 bytes in multiples
+ * of 16; host-built plans only; otherwise PERSIST. */
 
 /* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
  * loading the next descriptor while it copies the current tile. BULK: the same walk with the bulk
@@ -152,6 +171,8 @@ typedef struct kvx_plan_opts {
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2
 #define KVX_KERNEL_BULK 3
+#define KVX_KERNEL_TENSOR 4
+#define KVX_KERNEL_STAGED 5
 
 /* Record when every push starts and ends on the device; read with kvx_plan_push_times after
  * kvx_sync. The copy kernels stamp the GPU's global timer themselves (the first CTA to start, the

@@ -126,9 +126,23 @@ def test_head_major_plans_group_heads_per_tile():
     tiles = kvx.kvx_plan_tiles(plan)
     assert info["src_head_pitch"] == 256 and info["dst_head_pitch"] == 16 * 256
     assert len(tiles) == 10 * 2 and (tiles["heads"] == 4).all() and (tiles["n"] == 16).all()
-    # head-group tiles run the persistent kernel unless another is asked for; equal head-major
-    # layouts copy whole blocks and keep the bulk kernel
-    assert info["kernel"] == kvx.KVX_KERNEL_PERSIST
+    # head-group tiles run the staged kernel (bulk-engine loads, the threads' stores) unless another
+    # kernel is asked for; equal head-major layouts copy whole blocks and keep the bulk kernel
+    assert (info["kernel"], info["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
+    kvx.kvx_plan_destroy(plan)
+    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"kernel": kvx.KVX_KERNEL_TENSOR})
+    assert (kvx.kvx_plan_get_info(plan)["kernel"], kvx.kvx_plan_get_info(plan)["threads"]) == (kvx.KVX_KERNEL_TENSOR, 32)
+    kvx.kvx_plan_destroy(plan)
+    # the default tile of such a plan is a whole head group that divides the shared heads
+    plan = kvx.kvx_plan(sp, dp, reqs)
+    tiles = kvx.kvx_plan_tiles(plan)
+    assert kvx.kvx_plan_get_info(plan)["tile_bytes"] == 4 * 16 * 256 and (tiles["heads"] == 4).all()
+    kvx.kvx_plan_destroy(plan)
+    # head rows no tensor map can describe (24 bytes: not a multiple of 16) run the persistent kernel
+    s24, d24 = sg.replace(head_dim=12), dg.replace(head_dim=12)
+    p24, q24 = pools(s24, d24)
+    plan = kvx.kvx_plan(p24, q24, reqs)
+    assert (kvx.kvx_plan_get_info(plan)["kernel"], kvx.kvx_plan_get_info(plan)["threads"]) == (kvx.KVX_KERNEL_PERSIST, 128)
     kvx.kvx_plan_destroy(plan)
     plan = kvx.kvx_plan_ex(sp, dp, reqs, {"tile_bytes": 16384, "kernel": kvx.KVX_KERNEL_BULK})
     assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_BULK
@@ -144,7 +158,7 @@ def test_head_major_plans_group_heads_per_tile():
         rq = [(16 * 10, np.arange(10, dtype=np.int32), np.arange(10, 10 + nd, dtype=np.int32))]
         plan = kvx.kvx_plan(ap, bp, rq)
         i = kvx.kvx_plan_get_info(plan)
-        assert (i["kernel"], i["threads"]) == (kvx.KVX_KERNEL_PERSIST, 128)
+        assert (i["kernel"], i["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
         kvx.kvx_plan_destroy(plan)
 
 
@@ -278,10 +292,13 @@ def test_kernel_resolution():
         kvx.kvx_plan_destroy(p)
         return k
     assert kern({}) == kvx.KVX_KERNEL_BULK
-    assert kern({"tile_bytes": 65536}) == kvx.KVX_KERNEL_PERSIST
+    assert kern({"tile_bytes": 65536}) == kvx.KVX_KERNEL_BULK                       # 3 x 64 KiB ring fits
+    assert kern({"tile_bytes": 131072}) == kvx.KVX_KERNEL_PERSIST
     assert kern({"kernel": kvx.KVX_KERNEL_TILE}) == kvx.KVX_KERNEL_TILE
     assert kern({"kernel": kvx.KVX_KERNEL_BULK}) == kvx.KVX_KERNEL_BULK
-    assert kern({"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": 65536}) == kvx.KVX_KERNEL_PERSIST   # stage too big
+    assert kern({"kernel": kvx.KVX_KERNEL_BULK, "tile_bytes": 131072}) == kvx.KVX_KERNEL_PERSIST  # ring too big
+    assert kern({"kernel": kvx.KVX_KERNEL_TENSOR}) == kvx.KVX_KERNEL_BULK        # no head-major side: plain bulk
+    assert kern({"kernel": kvx.KVX_KERNEL_STAGED}) == kvx.KVX_KERNEL_BULK        # contiguous tiles: plain bulk
     sp8 = kvx.Pool(g, [(1 << 40) + 8, (1 << 40) + 8 + (1 << 30)])
     assert kern({"kernel": kvx.KVX_KERNEL_BULK}, sp8, dp) == kvx.KVX_KERNEL_PERSIST                  # 8-byte aligned
     gs, gd = PoolGeom(1, 2, 2, 4, 128, 2, 16, 8), PoolGeom(1, 2, 1, 8, 128, 2, 16, 8)
@@ -300,7 +317,7 @@ def test_kernel_resolution():
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"lanes": 9}))
     p = kvx.kvx_plan(sp, dp, [ok])
     assert kvx.kvx_plan_get_info(p)["lanes"] == 4
-    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 4
+    assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 3
     kvx.kvx_plan_destroy(p)
     # AUTO by size: a layer push reading >= 128 MiB runs PERSIST with 128 threads unless asked otherwise
     gl = PoolGeom(1, 2, 1, 8, 128, 2, 16, 5000)

@@ -69,7 +69,7 @@ def test_tiny_all_layers():
     run_workload(w, range(w.src.n_layers))
 
 
-KERNELS = {"tile": 1, "persist": 2, "bulk": 3}
+KERNELS = {"tile": 1, "persist": 2, "bulk": 3, "tensor": 4, "staged": 5}
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -82,7 +82,11 @@ def test_reduced_workloads_all_layers(make, kernel):
     w = make()
     info = run_workload(w, range(w.src.n_layers), opts={"kernel": KERNELS[kernel]})
     assert info["vec_bytes"] == 16
-    want = KERNELS[kernel]                                   # strided plans run the bulk kernel too
+    # strided plans run the bulk kernel too; TENSOR asked for on a plan with no head-major side is BULK,
+    # and so is STAGED on a contiguous plan
+    want = KERNELS[kernel]
+    if kernel == "tensor" or (kernel == "staged" and not info["strided"]):
+        want = kvx.KVX_KERNEL_BULK
     assert info["kernel"] == want
 
 
@@ -226,6 +230,12 @@ GEOMS = {
     "nhd_to_hnd_bs16to32": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 1, 8, 128, 2, 32, 30, 1)),
     "hnd_odd_heads": (PoolGeom(1, 1, 1, 3, 3, 2, 8, 40, 1), PoolGeom(1, 1, 3, 1, 3, 2, 4, 80, 1)),
     "nhd_tp1_to_hnd_tp2": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 2, 4, 128, 2, 16, 60, 1)),
+    # tensor-map boxes: heads and block sizes that are not powers of two (box of 3 heads x 12 slots),
+    # a head-major split with a block-size change, head rows of 16 and 2048 bytes
+    "nhd_to_hnd_nonpow2": (PoolGeom(1, 2, 1, 6, 128, 2, 12, 50), PoolGeom(1, 2, 1, 6, 128, 2, 12, 50, 1)),
+    "hnd_tp1_to_hnd_tp2_bs32": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60, 1), PoolGeom(1, 2, 2, 4, 128, 2, 32, 30, 1)),
+    "hnd_to_nhd_16byte_heads": (PoolGeom(2, 1, 1, 4, 8, 2, 16, 40, 1), PoolGeom(2, 1, 1, 4, 8, 2, 16, 40)),
+    "nhd_to_hnd_2kib_heads": (PoolGeom(1, 1, 2, 2, 1024, 2, 8, 30), PoolGeom(1, 1, 1, 4, 1024, 2, 8, 30, 1)),
 }
 
 
@@ -483,6 +493,40 @@ def test_hnd_batched_workload_sampled():
     w = kvx_inputs.qwen3_32b_batched_hnd()
     info = run_workload(w, [0, 40, 63])
     assert info["strided"] == 1 and info["src_pitch"] == 256 and info["dst_pitch"] == 256
+
+
+@pytest.mark.parametrize("kernel", ["auto", "tensor", "staged"])
+@pytest.mark.parametrize("name", ["qwen3_32b_single_nhd_to_hnd", "qwen3_32b_single_hnd_to_nhd"])
+def test_head_layout_change_per_layer_full_size(name, kernel):
+    """The per-layer head-layout changes at full size (64 layers, one 8192-token request, 32 MiB a
+    layer) in the benchmark's launch pattern: the automatic kernel (staged), and tensor-map copies."""
+    w = kvx_inputs.PUSH_WORKLOADS[name]()
+    info = run_workload(w, [0, 31, 63], opts={"kernel": KERNELS.get(kernel, 0)})
+    assert info["kernel"] == (kvx.KVX_KERNEL_TENSOR if kernel == "tensor" else kvx.KVX_KERNEL_STAGED)
+
+
+@pytest.mark.parametrize("kernel", ["tensor", "staged"])
+def test_head_layout_stall_reports_failed(kernel):
+    """The stall hook on a head-layout-changing plan: the waiting CTA gives up, the layer reads FAILED,
+    layers read DONE only when exact, and a second push completes."""
+    w = kvx_inputs.qwen3_32b_single_nhd_to_hnd(n_layers=3)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    plan = kvx.kvx_plan_ex(kvx.Pool(w.src, src), kvx.Pool(w.dst, dst), reqs_of(w), {"kernel": KERNELS[kernel]})
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == KERNELS[kernel]
+    side = torch.cuda.Stream()
+    kvx.kvx_plan_inject_stall(plan, 2)
+    for layer in range(3):
+        kvx.kvx_push_layer(plan, layer, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_EFAILED
+    states = kvx.kvx_plan_layer_states(plan).tolist()
+    assert states == [kvx.KVX_LAYER_DONE, kvx.KVX_LAYER_DONE, kvx.KVX_LAYER_FAILED]
+    assert_layer_states_truthful(w, src, dst, states, kvx_inputs.CANARY_BF16)
+    kvx.kvx_push_layer(plan, 2, side)
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(2)], reqs_of(w),
+                 range(3))
+    kvx.kvx_plan_destroy(plan)
 
 
 def test_nhd_to_hnd_batched_workload_sampled():
