@@ -273,8 +273,9 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     timed (the kernels' own global-timer stamps); the warm-up steps follow the same pattern, so the
     timed loop meets no first use. `all_layers`: one kvx_push_layers call per step for all layers,
     gated on the last layer's event, instead of one kvx_push_layer per layer; `extra_opts` are added
-    to the plan options. `sampler` (clock sampling) runs from before the warm-up to the end of the
-    timed steps, so the GPU never idles between the two."""
+    to the plan options. `sampler` (clock sampling, started by the caller before the pools are
+    allocated, since it takes a moment to start) is stopped after the timed steps; nothing idles the
+    GPU between the warm-up and the timed steps."""
     L = w.src.n_layers
     src, _ = alloc_pool(torch, w.src, "src", w.seed, device)
     dst, _ = alloc_pool(torch, w.dst, "dst", 0, device)
@@ -332,8 +333,6 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
 
     gc.collect()
     gc.disable()                                      # no collector pauses in the warm-up or the timed loop
-    if sampler:
-        sampler.start()
     run_steps(W, False)
     torch.cuda.synchronize()
     if barrier:
@@ -594,8 +593,10 @@ def run_kvx(args, rank, local_rank, world):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
         pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
     m = time_push_workload(args, torch, kvx, make(n_layers=args.layers) if args.layers > 0 else make(), device,
-                           K, W, every, sampler=ClockSampler(uuid), barrier=dist.barrier if world > 1 else None)
+                           K, W, every, sampler=sampler, barrier=dist.barrier if world > 1 else None)
     w, L, info, reqs = m["w"], m["L"], m["info"], m["reqs"]
     src, dst, sp, dp, opts, bytes_step = m["src"], m["dst"], m["sp"], m["dp"], m["opts"], m["bytes_step"]
     elapsed_ms, launches = m["elapsed_ms"], m["launches"]

@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *i
 }
 
 constexpr uint64_t kScanWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait on a predecessor
+constexpr uint64_t kScanStallWaitNs = 1000000ull;  // 1 ms: the bound under the testing hook
 
 __device__ __forceinline__ uint64_t scan_clock_ns() {
     uint64_t t;
@@ -497,11 +498,13 @@ __device__ __forceinline__ uint64_t scan_clock_ns() {
 // their totals until it meets one that has published its running prefix, and publishes its own.
 // state[t] holds 0 (nothing yet), total * 4 + 1 (the tile's total) or prefix * 4 + 2 (the prefix
 // through the tile); state[n_tiles] is the ticket counter; all zero before the launch. A wait is
-// bounded by the global timer: past the bound the scan sets error bit 64 and goes on (wrong sums,
-// reported by the caller).
+// bounded by the global timer (wait_ns): past the bound the scan sets error bit 64 and goes on (wrong
+// sums, reported by the caller). stall_tile (testing hook, -1 normally): that tile publishes nothing,
+// so the tile after it waits until the bound.
 __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t *in, int64_t *out, int64_t n_host,
                                                                    const int64_t *n_dev, unsigned long long *state,
-                                                                   int64_t n_tiles, int64_t *sum, int32_t *err) {
+                                                                   int64_t n_tiles, int64_t *sum, int32_t *err,
+                                                                   int64_t stall_tile, uint64_t wait_ns) {
     __shared__ int64_t ws[32];
     __shared__ int64_t tile_s, excl_s;
     if (threadIdx.x == 0) tile_s = (int64_t)atomicAdd(&state[n_tiles], 1ull);
@@ -514,14 +517,15 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t 
     const int64_t inc = block_inclusive_scan(v, ws, &total);
     if (threadIdx.x == 0) {
         int64_t excl = 0;
+        const bool publish = tile != stall_tile;
         if (tile > 0) {
-            atomicExch(&state[tile], ((unsigned long long)total << 2) | 1ull);
+            if (publish) atomicExch(&state[tile], ((unsigned long long)total << 2) | 1ull);
             uint64_t t0 = 0;
             for (int64_t p = tile - 1;;) {
                 const unsigned long long f = __ldcg(&state[p]);             // from L2, where the writers publish
                 if ((f & 3ull) == 0) {
                     if (t0 == 0) t0 = scan_clock_ns();
-                    else if (scan_clock_ns() - t0 > kScanWaitNs) { atomicOr(err, 64); break; }
+                    else if (scan_clock_ns() - t0 > wait_ns) { atomicOr(err, 64); break; }
                     continue;
                 }
                 excl += (int64_t)(f >> 2);
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t 
                 t0 = 0;
             }
         }
-        atomicExch(&state[tile], ((unsigned long long)(excl + total) << 2) | 2ull);
+        if (publish) atomicExch(&state[tile], ((unsigned long long)(excl + total) << 2) | 2ull);
         excl_s = excl;
         if (tile == n_tiles - 1) *sum = excl + total;
     }
@@ -544,15 +548,19 @@ static int64_t scan_state_words(int64_t n_bound) {
     return (n_bound + kScanThreads - 1) / kScanThreads + 1;
 }
 
+// stall (testing hook): the look-back scan's first tile publishes nothing and the waits are bounded
+// by 1 ms, so the second tile's wait runs out (no effect on a single-tile scan).
 static cudaError_t exclusive_scan(const int64_t *in, int64_t *out, int64_t n_bound, const int64_t *n_dev,
-                                  unsigned long long *state, int64_t *sum, int32_t *err, cudaStream_t st) {
+                                  unsigned long long *state, int64_t *sum, int32_t *err, cudaStream_t st,
+                                  bool stall = false) {
     count_launch(1);
     if (n_bound <= kScanThreads) {
         kvx_scan_single<<<1, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, sum);
         return cudaGetLastError();
     }
     const int64_t nb = scan_state_words(n_bound) - 1;
-    kvx_scan_lookback<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, state, nb, sum, err);
+    kvx_scan_lookback<<<(unsigned)nb, kScanThreads, 0, st>>>(in, out, n_bound, n_dev, state, nb, sum, err,
+                                                              stall ? 0 : -1, stall ? kScanStallWaitNs : kScanWaitNs);
     return cudaGetLastError();
 }
 
@@ -906,7 +914,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     if (opts) {
         if (opts->reserved0 || opts->reserved[0] || opts->reserved[1] || opts->reserved[2] || opts->reserved[3])
             return fail(KVX_EINVAL, "kvx_match_opts.reserved must be 0");
-        if (opts->flags & ~(KVX_MATCH_FILL_HOLES | KVX_MATCH_KEEP_LAST))
+        if (opts->flags & ~(KVX_MATCH_FILL_HOLES | KVX_MATCH_KEEP_LAST | KVX_MATCH_TEST_SCAN_STALL))
             return fail(KVX_EINVAL, "unknown kvx_match_opts.flags bits");
         mf.flags = opts->flags;
         mf.expiry = opts->expiry;
@@ -1081,7 +1089,8 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                                                                 m.flag);
         }
         ok(cudaGetLastError());
-        ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.scan_state + n_state, &m.scalars[1], m.err, stream));
+        ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.scan_state + n_state, &m.scalars[1], m.err, stream,
+                          (mf.flags & KVX_MATCH_TEST_SCAN_STALL) != 0));
         kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start);
         ok(cudaGetLastError());
         kvx_run_tiles<<<grid_for(B, 256), 256, 0, stream>>>(m.run_start, m.scalars, sh, m.tile_count);

@@ -244,13 +244,13 @@ bool as_whole_block_copy(kvx_plan_s *pl) {
 
 // Bulk copies need 16-byte aligned addresses, sizes, widths and pitches (vec == 16), a ring that
 // fits shared memory and, for strided plans, a row that fits a stage. The automatic choice, measured
-// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at about one CTA
-// per SM (it leaves room for the caller's compute and the next push), a larger one with the persistent
+// on GB300: a layer push that reads under 128 MiB runs fastest with the bulk kernel at two CTAs per
+// SM (it leaves room for the caller's compute and the next push), a larger one with the persistent
 // kernel at 128 threads per CTA and the occupancy limit of CTAs (many small independent CTAs). Plans
 // that map one head layout onto another (head-group tiles: dozens of row copies per tile, too many for
-// one issuing thread) take the persistent kernel at 128 threads per CTA at any size: 32 MiB-per-layer
-// pushes ran at 0.81 of the copy peak (256 threads 0.78-0.80) against 0.59-0.64 with the bulk kernel. Two head-major
-// sides alike copy whole blocks as single spans and keep the bulk kernel (0.94-0.95 against 0.76).
+// one issuing thread) take tensor-map copies (one TMA operation per tile and side) at any size, or
+// the persistent kernel at 128 threads per CTA where no tensor map fits. Two head-major sides alike
+// copy whole blocks as single spans and keep the bulk kernel (0.94-0.95 against 0.76).
 constexpr int64_t kLargeLayer = (int64_t)128 << 20;
 
 // The box of a TENSOR plan's maps: tiles of box_n token slots for box_k heads go through the maps
@@ -286,7 +286,15 @@ static void resolve_kernel(kvx_plan_s *pl) {
     const bool row_groups = pl->per_head && !same_head_major(pl->src, pl->dst);
     tensor_box(pl);
     int32_t k = pl->kernel;
-    if (automatic) k = row_groups ? (staged_ok ? KVX_KERNEL_STAGED : KVX_KERNEL_PERSIST)
+    // plans that map one head layout onto another: tensor-map copies with a 4-stage ring (measured on
+    // GB300, 32 MiB per layer: 0.84 of the copy peak in the per-layer step against 0.81 for PERSIST
+    // and 0.83-0.90 for STAGED, and 0.62 for a launch alone against 0.59-0.67 and 0.42-0.54; one
+    // 497 MB layer of the batched workload 0.990 against 0.968 for PERSIST, 0.87 for STAGED)
+    if (automatic && row_groups && tensor_ok(pl) && !pl->bulk_stages_req) {
+        pl->bulk_stages = 4;
+        if (!tensor_ok(pl)) pl->bulk_stages = 3;
+    }
+    if (automatic) k = row_groups ? (tensor_ok(pl) ? KVX_KERNEL_TENSOR : KVX_KERNEL_PERSIST)
                                   : (bulk_ok && !large ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST);
     if (k == KVX_KERNEL_TENSOR && !tensor_ok(pl)) k = row_groups ? KVX_KERNEL_PERSIST : KVX_KERNEL_BULK;
     if (k == KVX_KERNEL_STAGED && !staged_ok) k = bulk_ok ? KVX_KERNEL_BULK : KVX_KERNEL_PERSIST;

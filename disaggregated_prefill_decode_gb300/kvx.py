@@ -59,7 +59,7 @@ class kvx_match_opts(ctypes.Structure):
     _fields_ = [("flags", c_i32), ("reserved0", c_i32), ("expiry", c_vp), ("now", c_i64), ("reserved", c_i64 * 4)]
 
 
-KVX_MATCH_FILL_HOLES, KVX_MATCH_KEEP_LAST = 1, 2
+KVX_MATCH_FILL_HOLES, KVX_MATCH_KEEP_LAST, KVX_MATCH_TEST_SCAN_STALL = 1, 2, 256
 
 
 class kvx_match_result(ctypes.Structure):

@@ -118,18 +118,18 @@ typedef struct kvx_plan_opts {
                                  of at most 16384 bytes, or whole units packed up to 16384     */
     int32_t threads;          /* threads per CTA of TILE / PERSIST (multiple of 32, <= 1024;
                                  default 256, or 128 where AUTO picks PERSIST for a large push
-                                 or a head-group plan) */
+                                 or a head-group plan; BULK and TENSOR run 32, STAGED 128) */
     int32_t flags;            /* KVX_PLAN_* bits                                                 */
     int32_t kernel;           /* KVX_KERNEL_*; 0 lets the library choose                         */
     int32_t ctas_per_sm;      /* persistent kernels: resident CTAs per SM, capped at the occupancy
-                                 limit (0: for launches that read under 128 MiB 5 CTAs per 4 SMs
-                                 with BULK and 2 per SM with PERSIST (4 for head-group tiles),
-                                 leaving room for the caller's compute and an overlapping push;
-                                 the occupancy limit for larger launches) */
+                                 limit (0: for launches that read under 128 MiB 2 per SM with the
+                                 ring kernels (BULK, TENSOR, STAGED) and with PERSIST (4 for
+                                 head-group tiles), leaving room for the caller's compute and an
+                                 overlapping push; the occupancy limit for larger launches) */
     int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
-    int32_t bulk_stages;      /* BULK: shared-memory ring stages of tile_bytes each, one of 2, 3, 4,
-                                 6, 8 with stages * tile_bytes <= 192 KiB (0: 4 for contiguous
-                                 plans, 3 for strided ones)                                     */
+    int32_t bulk_stages;      /* ring kernels: shared-memory stages of tile_bytes each, one of 2, 3,
+                                 4, 6, 8 with stages * tile_bytes <= 192 KiB (0: 3; 4 for TENSOR
+                                 chosen by AUTO)                                                 */
     int32_t layers_per_launch; /* kvx_push_layers: layers one copy launch covers, the launches of a
                                  call spread over the lanes (0: as many as make about 256 MiB
                                  moved, read + write, per launch when lanes > 1, at least one;
@@ -162,11 +162,11 @@ typedef struct kvx_plan_opts {
  * offsets, widths and pitches are all 16-byte aligned, with a row no larger than tile_bytes; others
  * fall back to PERSIST. Contiguous BULK launches that read at least 8 MiB mark the lines they touch
  * evict-first in L2 (a cache hint only; the bytes copied are the same). AUTO picks BULK where it
- * applies to a plan that reads under 128 MiB per layer (about one CTA per SM, leaving room for the
- * caller's compute and the next push) and PERSIST with 128 threads per CTA otherwise (measured
- * fastest on GB300 for large layer pushes); plans with one token-major and one head-major side, or
- * two head-major sides with different block sizes or head splits, take PERSIST at any size (their
- * tiles are many short rows). */
+ * applies to a plan that reads under 128 MiB per layer (two CTAs per SM with a 3-stage ring, leaving
+ * room for the caller's compute and the next push) and PERSIST with 128 threads per CTA otherwise
+ * (measured fastest on GB300 for large layer pushes); plans with one token-major and one head-major
+ * side, or two head-major sides with different block sizes or head splits, take TENSOR with a
+ * 4-stage ring at any size when the tensor maps can describe them, else PERSIST. */
 #define KVX_KERNEL_AUTO 0
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2
@@ -437,6 +437,11 @@ kvx_status kvx_match_prefix(const uint32_t *tokens, const int64_t *tok_off, int3
  */
 #define KVX_MATCH_FILL_HOLES 1
 #define KVX_MATCH_KEEP_LAST 2
+/* Testing hook for the device-side bounded wait of the plan emission: the first tile of the
+ * look-back scan that numbers the plan's runs publishes nothing and the scan's waits are bounded by
+ * 1 ms, so the next tile's wait on it runs out (a scan of more than 1024 pulled blocks; nothing
+ * faults). The call then returns KVX_ETIMEDOUT with no plan. */
+#define KVX_MATCH_TEST_SCAN_STALL 256
 
 typedef struct kvx_match_opts {
     int32_t flags;

@@ -593,3 +593,30 @@ def test_match_options_plan_and_push(flags, ttl):
     check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")], reqs, range(2))
     kvx.kvx_plan_destroy(plan)
     c.close()
+
+
+def test_plan_scan_wait_runs_out_then_next_call_is_exact():
+    """KVX_MATCH_TEST_SCAN_STALL: the first tile of the look-back scan that numbers the plan's runs
+    publishes nothing, so the next tile's bounded wait (1 ms under the hook) runs out; the call returns
+    KVX_ETIMEDOUT with no plan and nothing faults. The same call without the hook then gives the
+    oracle's decisions and a plan whose pushed bytes equal the oracle's."""
+    w = kvx_inputs.bidir_mla_fp8(seed=26, n_sessions=24, n_layers=1, system_tokens=256, hist_range=(2000, 6000),
+                                 resident_p=0.3, threshold=64)
+    assert w.rem_off[-1] > 1024                                  # the run scan has more than one tile
+    c = Case(w)
+    src, _ = device_pool(w.decode, "fp8_bytes", seed=5)
+    dst, _ = device_pool(w.prefill, "canary_fp8_bytes")
+    with pytest.raises(kvx.KvxError) as ei:
+        c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst), flags=kvx.KVX_MATCH_TEST_SCAN_STALL)
+    assert ei.value.status == kvx.KVX_ETIMEDOUT
+    want = c.oracle_match()
+    assert want["status"] == 0 and want["push"].sum() > 1
+    st, plan, got = c.match(kvx.Pool(w.decode, src), kvx.Pool(w.prefill, dst))
+    assert st == kvx.KVX_OK
+    assert_decisions(got, want)
+    kvx.kvx_push_layer(plan, 0, torch.cuda.Stream())
+    assert kvx.kvx_sync(plan, -1) == kvx.KVX_OK
+    check_layers(w.decode, src, w.prefill, dst, lambda l: [canary_host(w.prefill, "fp8_bytes")],
+                 oracle_requests(c, want), range(1))
+    kvx.kvx_plan_destroy(plan)
+    c.close()

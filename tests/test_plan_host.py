@@ -126,12 +126,12 @@ def test_head_major_plans_group_heads_per_tile():
     tiles = kvx.kvx_plan_tiles(plan)
     assert info["src_head_pitch"] == 256 and info["dst_head_pitch"] == 16 * 256
     assert len(tiles) == 10 * 2 and (tiles["heads"] == 4).all() and (tiles["n"] == 16).all()
-    # head-group tiles run the staged kernel (bulk-engine loads, the threads' stores) unless another
-    # kernel is asked for; equal head-major layouts copy whole blocks and keep the bulk kernel
-    assert (info["kernel"], info["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
+    # head-group tiles move as tensor-map copies (4-stage ring) unless another kernel is asked for;
+    # equal head-major layouts copy whole blocks and keep the bulk kernel
+    assert (info["kernel"], info["threads"], info["bulk_stages"]) == (kvx.KVX_KERNEL_TENSOR, 32, 4)
     kvx.kvx_plan_destroy(plan)
-    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"kernel": kvx.KVX_KERNEL_TENSOR})
-    assert (kvx.kvx_plan_get_info(plan)["kernel"], kvx.kvx_plan_get_info(plan)["threads"]) == (kvx.KVX_KERNEL_TENSOR, 32)
+    plan = kvx.kvx_plan_ex(sp, dp, reqs, {"kernel": kvx.KVX_KERNEL_STAGED})
+    assert (kvx.kvx_plan_get_info(plan)["kernel"], kvx.kvx_plan_get_info(plan)["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
     kvx.kvx_plan_destroy(plan)
     # the default tile of such a plan is a whole head group that divides the shared heads
     plan = kvx.kvx_plan(sp, dp, reqs)
@@ -158,7 +158,7 @@ def test_head_major_plans_group_heads_per_tile():
         rq = [(16 * 10, np.arange(10, dtype=np.int32), np.arange(10, 10 + nd, dtype=np.int32))]
         plan = kvx.kvx_plan(ap, bp, rq)
         i = kvx.kvx_plan_get_info(plan)
-        assert (i["kernel"], i["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
+        assert (i["kernel"], i["threads"]) == (kvx.KVX_KERNEL_TENSOR, 32)
         kvx.kvx_plan_destroy(plan)
 
 

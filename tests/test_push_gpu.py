@@ -499,10 +499,10 @@ def test_hnd_batched_workload_sampled():
 @pytest.mark.parametrize("name", ["qwen3_32b_single_nhd_to_hnd", "qwen3_32b_single_hnd_to_nhd"])
 def test_head_layout_change_per_layer_full_size(name, kernel):
     """The per-layer head-layout changes at full size (64 layers, one 8192-token request, 32 MiB a
-    layer) in the benchmark's launch pattern: the automatic kernel (staged), and tensor-map copies."""
+    layer) in the benchmark's launch pattern: the automatic kernel (tensor-map copies), and staged."""
     w = kvx_inputs.PUSH_WORKLOADS[name]()
     info = run_workload(w, [0, 31, 63], opts={"kernel": KERNELS.get(kernel, 0)})
-    assert info["kernel"] == (kvx.KVX_KERNEL_TENSOR if kernel == "tensor" else kvx.KVX_KERNEL_STAGED)
+    assert info["kernel"] == (kvx.KVX_KERNEL_STAGED if kernel == "staged" else kvx.KVX_KERNEL_TENSOR)
 
 
 @pytest.mark.parametrize("kernel", ["tensor", "staged"])
