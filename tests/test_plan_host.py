@@ -349,3 +349,29 @@ def test_kernel_resolution():
     assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 0                                     # not a bulk plan
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_set_opts(p, {"bulk_stages": 5}))
     kvx.kvx_plan_destroy(p)
+
+
+def test_head_group_default_tiles_divide_the_shared_heads():
+    """Plans that map one head layout onto another cut each block segment into equal head groups: the
+    largest divisor of the heads a producer shard and a consumer shard share that fits 16 KiB, so
+    every group is one tensor-map box (6 shared heads of 256 B over 12-token blocks: 3 heads a tile;
+    a TP1 -> TP2 split with 4 shared heads: 4)."""
+    cases = [
+        (PoolGeom(1, 2, 1, 6, 128, 2, 12, 40), PoolGeom(1, 2, 1, 6, 128, 2, 12, 40, 1), 3, 12),
+        (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40), PoolGeom(1, 2, 2, 4, 128, 2, 16, 40, 1), 4, 16),
+        (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(1, 2, 1, 8, 128, 2, 32, 20), 4, 16),
+    ]
+    for sg, dg, k, n in cases:
+        sp, dp = pools(sg, dg)
+        n_tok = 4 * max(sg.block_size, dg.block_size)
+        reqs = [(n_tok, np.arange(n_tok // sg.block_size, dtype=np.int32),
+                 np.arange(3, 3 + n_tok // dg.block_size, dtype=np.int32))]
+        plan = kvx.kvx_plan(sp, dp, reqs)
+        info = kvx.kvx_plan_get_info(plan)
+        tiles = kvx.kvx_plan_tiles(plan)
+        assert info["kernel"] == kvx.KVX_KERNEL_TENSOR
+        assert info["tile_bytes"] == k * n * 256
+        assert (np.maximum(tiles["heads"], 1) == k).all() and (tiles["n"] == n).all()
+        total_heads = sg.n_shards * sg.heads_per_shard
+        assert len(tiles) == (n_tok // n) * (total_heads // k)
+        kvx.kvx_plan_destroy(plan)
