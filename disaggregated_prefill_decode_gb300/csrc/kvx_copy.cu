@@ -345,18 +345,34 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
 
 // Tensor-map copies of one box (rank 4: head bytes / 8, head, slot, block; x always 0). The load
 // completes on the stage's mbarrier; the store joins the thread's current bulk group.
+// With `hint` both carry the evict-first L2 policy (launches that stream 8 MiB or more: on GB300 a
+// 32 MiB-per-layer head-layout push went from 0.836-0.844 to 0.873-0.874 of the copy peak in the
+// per-layer step with it, 0.61-0.62 to 0.62-0.63 alone, a 497 MB layer unchanged at 0.99).
 __device__ __forceinline__ void tensor_load(void *stage, const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-        ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar))
-        : "memory");
+                                            uint64_t *bar, bool hint, uint64_t policy) {
+    if (hint)
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+            "[%1, {%2, %3, %4, %5}], [%6], %7;"
+            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar)), "l"(policy)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar))
+            : "memory");
 }
 
-__device__ __forceinline__ void tensor_store(const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk, const void *stage) {
-    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
-                 ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage))
-                 : "memory");
+__device__ __forceinline__ void tensor_store(const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk, const void *stage,
+                                             bool hint, uint64_t policy) {
+    if (hint)
+        asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4}], [%5], %6;"
+                     ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage)), "l"(policy)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                     ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage))
+                     : "memory");
 }
 
 // The maps live in global memory, written by the plan upload; a CTA acquires each map for the tensor
@@ -403,7 +419,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         if (TENSOR && it.tensor) {
             const CUtensorMap *map = a.src_maps + it.s_buf;
             if (map != fenced_src) { map_acquire(map); fenced_src = map; }
-            tensor_load(stage, map, it.sh, it.ss, it.sb, &bar[s]);
+            tensor_load(stage, map, it.sh, it.ss, it.sb, &bar[s], hint, policy);
         } else if (token_major(it)) {
             const uint32_t span = (uint32_t)(it.heads * a.width);    // one token's heads
             if (a.src_pitch == (int64_t)span) {
@@ -452,7 +468,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
             if (TENSOR && it.tensor) {
                 const CUtensorMap *map = a.dst_maps + it.d_buf;
                 if (map != fenced_dst) { map_acquire(map); fenced_dst = map; }
-                tensor_store(map, it.dh, it.ds, it.db, stage);
+                tensor_store(map, it.dh, it.ds, it.db, stage, hint, policy);
             } else if (token_major(it)) {
                 for (int32_t h = 0; h < it.heads; ++h)
                     for (int32_t r = 0; r < it.n; ++r)
@@ -754,12 +770,12 @@ cudaError_t launch_copy(const CopyArgs &a, int32_t n_layers, const LaunchShape &
         CopyArgs args_copy = a;
         int64_t work = n_work;
         int32_t stage_bytes = stage_bytes_k;
-        // evict-first L2 hints for contiguous launches that stream at least kStreamL2Bytes. Smaller
-        // ones keep the default policy (a 1 MB push whose blocks stay in L2 between steps ran 7 %
-        // slower with it), and so do strided ones: rows written one by one into lines that other
-        // items complete later ran 6-7 % slower with it (fragmented head-group pushes, 32 MiB per
-        // layer), 512-byte remap rows gained under 1 %.
-        int32_t stream_l2 = !sh.strided && n_work * (int64_t)sh.tile_bytes >= kStreamL2Bytes;
+        // evict-first L2 hints for contiguous and tensor-map launches that stream at least
+        // kStreamL2Bytes. Smaller ones keep the default policy (a 1 MB push whose blocks stay in L2
+        // between steps ran 7 % slower with it), and so do strided row-by-row ones: rows written
+        // one by one into lines that other items complete later ran 6-7 % slower with it
+        // (fragmented head-group pushes, 32 MiB per layer), 512-byte remap rows gained under 1 %.
+        int32_t stream_l2 = (!sh.strided || tensor) && n_work * (int64_t)sh.tile_bytes >= kStreamL2Bytes;
         void *args[] = {&args_copy, &work, &stage_bytes, &stream_l2};
         return cudaLaunchKernel(fn, dim3((unsigned)std::min<int64_t>(grid, n_work)), dim3(32), args, (size_t)smem, st);
     }
