@@ -375,3 +375,27 @@ def test_head_group_default_tiles_divide_the_shared_heads():
         total_heads = sg.n_shards * sg.heads_per_shard
         assert len(tiles) == (n_tok // n) * (total_heads // k)
         kvx.kvx_plan_destroy(plan)
+
+
+def test_stall_hook_argument_checks():
+    """kvx_plan_inject_stall needs a ring kernel and a layer of the plan; no CUDA call is made."""
+    g = PoolGeom(2, 2, 1, 8, 128, 2, 16, 40)
+    sp, dp = pools(g, g)
+    reqs = [(64, np.arange(4, dtype=np.int32), np.arange(10, 14, dtype=np.int32))]
+    for kernel, ok in ((kvx.KVX_KERNEL_BULK, True), (kvx.KVX_KERNEL_PERSIST, False), (kvx.KVX_KERNEL_TILE, False)):
+        plan = kvx.kvx_plan_ex(sp, dp, reqs, {"kernel": kernel})
+        if ok:
+            kvx.kvx_plan_inject_stall(plan, 1)
+        else:
+            expect(kvx.KVX_EUNSUPPORTED, lambda: kvx.kvx_plan_inject_stall(plan, 1))
+        kvx.kvx_plan_destroy(plan)
+    plan = kvx.kvx_plan(sp, dp, reqs)
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_inject_stall(plan, 2))
+    expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_inject_stall(plan, -1))
+    kvx.kvx_plan_destroy(plan)
+    hg, hd = PoolGeom(1, 2, 1, 8, 128, 2, 16, 40), PoolGeom(1, 2, 1, 8, 128, 2, 16, 40, 1)
+    hp, hq = pools(hg, hd)
+    for kernel in (kvx.KVX_KERNEL_TENSOR, kvx.KVX_KERNEL_STAGED):
+        plan = kvx.kvx_plan_ex(hp, hq, reqs, {"kernel": kernel})
+        kvx.kvx_plan_inject_stall(plan, 0)
+        kvx.kvx_plan_destroy(plan)
