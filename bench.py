@@ -716,23 +716,37 @@ def reduce_over_ranks(elapsed_ms, launches, device):
 
 
 def memcpy_ceiling(torch, device):
-    """cudaMemcpyAsync-class device-to-device copy of 2 GiB (torch copy_), read+write GB/s."""
+    """cudaMemcpyAsync-class device-to-device copy of 2 GiB (torch copy_), read+write GB/s; and, as the
+    same kind of yardstick for head-layout changes, torch's own copy of 2 GiB of whole Qwen3-32B-shaped
+    blocks from token-major to head-major ([block][16][8][128] -> [block][8][16][128], bf16)."""
     n = 1 << 31
     a = torch.empty(n, dtype=torch.uint8, device=device)
     b = torch.empty(n, dtype=torch.uint8, device=device)
     a.fill_(1)
-    for _ in range(3):
-        b.copy_(a)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    best = float("inf")
-    for _ in range(10):
-        s.record()
-        b.copy_(a)
-        e.record()
-        e.synchronize()
-        best = min(best, s.elapsed_time(e))
-    del a, b
-    return {"value": round(2 * n / (best * 1e-3) / 1e9, 1), "unit": "GB/s", "how": "torch copy_ of 2 GiB, best of 10"}
+
+    def best_of(fn, reps=10):
+        for _ in range(3):
+            fn()
+        best = float("inf")
+        for _ in range(reps):
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            best = min(best, s.elapsed_time(e))
+        return best
+
+    plain = best_of(lambda: b.copy_(a))
+    blocks = n // (16 * 8 * 128 * 2)
+    src = a.view(torch.bfloat16).view(blocks, 16, 8, 128)
+    dst = b.view(torch.bfloat16).view(blocks, 8, 16, 128)
+    xpose = best_of(lambda: dst.copy_(src.permute(0, 2, 1, 3)))
+    del a, b, src, dst
+    return {"value": round(2 * n / (plain * 1e-3) / 1e9, 1), "unit": "GB/s", "how": "torch copy_ of 2 GiB, best of 10",
+            "head_transpose": {"value": round(2 * n / (xpose * 1e-3) / 1e9, 1), "unit": "GB/s",
+                               "how": "torch copy_ of 2 GiB of [block][16][8][128] bf16 into [block][8][16][128] "
+                                      "(token-major -> head-major whole blocks), best of 10"}}
 
 
 def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world):
