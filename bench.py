@@ -239,13 +239,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "fine": fine}
 
 
-def clock_by_step(fine, step_host):
-    """Median NVML SM clock over each timed step's host issue window [start_i, start_{i+1}); None for
-    a step with no sample (the GPU runs up to a step behind the host, so this is approximate)."""
+def clock_by_step(fine, step_host, reach_s=0.003):
+    """NVML SM clock per timed step: the median of the samples inside the step's host issue window
+    [start_i, start_{i+1}), else the sample nearest the window's middle if one lies within reach_s
+    (samples come every few ms, steps last under one), else None. The GPU runs up to a step behind
+    the host, so this places clocks to within a step or two."""
     out = []
     for a, b in zip(step_host[:-1], step_host[1:]):
         v = [mhz for t, mhz in fine if a <= t < b]
-        out.append(statistics.median(v) if v else None)
+        if v:
+            out.append(statistics.median(v))
+            continue
+        mid = 0.5 * (a + b)
+        near = min(fine, key=lambda x: abs(x[0] - mid), default=None)
+        out.append(near[1] if near is not None and abs(near[0] - mid) <= reach_s else None)
     return out
 
 

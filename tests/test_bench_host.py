@@ -73,3 +73,13 @@ def test_reference_arm_under_torchrun_prints_once():
                    "--steps", "1", "--warmup", "3"])
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_clock_by_step_bins_and_nearest_sample():
+    fine = [(10.0000, 2070.0), (10.0021, 1980.0), (10.0100, 1500.0)]
+    steps = [9.9990, 10.0005, 10.0011, 10.0030, 10.0400, 10.0500]
+    got = bench.clock_by_step(fine, steps)
+    # step 0 holds the first sample; steps 1 and 2 take the nearest one (within 3 ms of their middle);
+    # step 3 holds the last sample; step 4's middle is 35 ms from every sample
+    assert got == [2070.0, 2070.0, 1980.0, 1500.0, None]
+    assert bench.clock_by_step([], steps) == [None] * 5
