@@ -86,7 +86,8 @@ def parse():
     p.add_argument("--no-per-config", action="store_true", help="skip the short runs of the other push configs")
     p.add_argument("--no-overlap", action="store_true", help="skip the prefill / push overlap measurement")
     p.add_argument("--overlap-narrow", default="32:6,64:4",
-                   help="push shapes beside the GEMM prefill, as max_ctas:bulk_stages pairs separated by commas")
+                   help="push shapes beside the GEMM prefill, separated by commas: max_ctas:bulk_stages pairs, "
+                        "or plan options as key=value;key=value")
     return p.parse_args()
 
 
@@ -465,7 +466,12 @@ def measure_overlap(args, torch, kvx, m, steps=200):
             out[name]["narrow_pushes"] = []
             variants = []
             for spec in args.overlap_narrow.split(","):
-                if spec.strip():
+                spec = spec.strip()
+                if not spec:
+                    continue
+                if "=" in spec:                       # key=value;key=value: any plan options
+                    variants.append({k: int(v) for k, v in (kv.split("=") for kv in spec.split(";"))})
+                else:                                 # max_ctas:bulk_stages
                     c, st = (int(x) for x in spec.split(":"))
                     variants.append({"max_ctas": c, "bulk_stages": st})
             for v in variants:
