@@ -447,21 +447,32 @@ def measure_overlap(args, torch, kvx, m, steps=200):
         chain = statistics.median(a.elapsed_time(b) for a, b in marks) if prefill else None
         return t0.elapsed_time(t1) / n_steps, chain
 
-    def interleaved(push_opts, n_pairs=24):
-        """GEMM prefill steps alternating without and with the pushes, each step on its own (the GPU
-        drained before the next), so clock and power drift falls on both alike: the median chain
-        time of each kind."""
-        alone, with_push = [], []
+    def interleaved(push_opts, iters=-1, n_pairs=24):
+        """Prefill steps (GEMM layers for iters < 0, else the ALU fixture) alternating without and with
+        the pushes, each step on its own (the GPU drained before the next), so clock and power drift
+        falls on both alike: the median chain time of each kind, and of the steps with pushes the median
+        span from the first layer to the end of the last copy (each lane's last push, in round-robin lane
+        order the last `lanes` layers, records an event after its copy)."""
+        alone, with_push, span = [], [], []
+        tail = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
+        for ev in tail:
+            ev.record(main)                           # torch creates an event at its first record
         for i in range(2 * (n_pairs + 2)):
             push = i % 2 == 1
             plan = kvx.kvx_plan_ex(sp, dp, reqs, dict(opts, **(push_opts or {}))) if push else None
+            n_tail = min(L, kvx.kvx_plan_get_info(plan)["lanes"]) if push else 0
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             for layer in range(L):
-                with torch.cuda.stream(main):
-                    torch.matmul(gemm[0], gemm[1], out=gemm[2])
-                    ready[layer].record(main)
-                if push:
+                if iters < 0:
+                    with torch.cuda.stream(main):
+                        torch.matmul(gemm[0], gemm[1], out=gemm[2])
+                        ready[layer].record(main)
+                else:
+                    fx(args.fixture_ctas, iters, None, 0, layer, main_h, ready_h[layer])
+                if push and layer >= L - n_tail:
+                    kvx.kvx_push_layer_notify(plan, layer, layer + 1, side, ready[layer], tail[layer])
+                elif push:
                     lib.kvx_push_layer(plan.handle, layer, side_h, ready_h[layer])
             b.record(main)
             if push:
@@ -470,7 +481,9 @@ def measure_overlap(args, torch, kvx, m, steps=200):
             torch.cuda.synchronize()
             if i >= 4:                                # the first two pairs warm up
                 (with_push if push else alone).append(a.elapsed_time(b))
-        return statistics.median(alone), statistics.median(with_push)
+                if push:
+                    span.append(max([a.elapsed_time(b)] + [a.elapsed_time(tail[l]) for l in range(L - n_tail, L)]))
+        return statistics.median(alone), statistics.median(with_push), statistics.median(span)
 
     push_only, _ = timed(False, True, 0)
     out = {"push_only_ms_per_step": round(push_only, 4)}
@@ -485,16 +498,18 @@ def measure_overlap(args, torch, kvx, m, steps=200):
                      "prefill_chain_ms_alone": round(chain_alone, 4),
                      "prefill_chain_ms_with_push": round(chain_with, 4),
                      "prefill_slowdown": round(chain_with / chain_alone - 1, 4)}
+        # the prefill chain's slowdown from steps alternating without and with the pushes: separate runs
+        # of a chain alone drift by up to a few per cent between themselves (clock and power under a
+        # 1.4 kW cap), as much as some of the effects measured, so the reported slowdown is this one
+        c0, c1, sp1 = interleaved(None, iters)
+        out[name]["separate_runs"] = {k: out[name][k] for k in (
+            "prefill_only_ms_per_step", "together_ms_per_step", "hidden_frac", "prefill_chain_ms_alone",
+            "prefill_chain_ms_with_push", "prefill_slowdown")}
+        out[name].update({"prefill_chain_ms_alone": round(c0, 4), "prefill_chain_ms_with_push": round(c1, 4),
+                          "prefill_slowdown": round(c1 / c0 - 1, 4), "step_ms_with_push": round(sp1, 4),
+                          "hidden_frac": round((c0 + push_only - sp1) / min(c0, push_only), 3)})
+        del out[name]["prefill_only_ms_per_step"], out[name]["together_ms_per_step"]
         if iters < 0:
-            # the GEMM chain's slowdown from steps alternating without and with the pushes: separate runs
-            # of the GEMM chain alone drift by up to a few per cent between themselves (clock and power
-            # under a 1.4 kW cap), as much as the effect measured, so the reported slowdown is this one
-            c0, c1 = interleaved(None)
-            out[name]["separate_runs"] = {"prefill_chain_ms_alone": out[name]["prefill_chain_ms_alone"],
-                                          "prefill_chain_ms_with_push": out[name]["prefill_chain_ms_with_push"],
-                                          "prefill_slowdown": out[name]["prefill_slowdown"]}
-            out[name].update({"prefill_chain_ms_alone": round(c0, 4), "prefill_chain_ms_with_push": round(c1, 4),
-                              "prefill_slowdown": round(c1 / c0 - 1, 4)})
             # the same GEMM prefill beside pushes bounded to a few CTAs with deep rings: the GEMM's CTAs
             # take every register of an SM, so each SM a copy holds is an SM the GEMM waits for
             out[name]["narrow_pushes"] = []
@@ -510,16 +525,19 @@ def measure_overlap(args, torch, kvx, m, steps=200):
                     variants.append({"max_ctas": c, "bulk_stages": st})
             for v in variants:
                 p_only, _ = timed(False, True, 0, steps, v)
-                c0, c1 = interleaved(v)
+                c0, c1, sp1 = interleaved(v)
                 out[name]["narrow_pushes"].append(
                     {"opts": v, "push_only_ms_per_step": round(p_only, 4),
                      "prefill_chain_ms_alone": round(c0, 4), "prefill_chain_ms_with_push": round(c1, 4),
-                     "prefill_slowdown": round(c1 / c0 - 1, 4)})
-    out["how"] = (f"{steps} steps each ({50} with the GEMM prefill); the prefill chain is the median time on its "
-                  "stream from a step's first layer to its last; hidden_frac = (prefill + push - together) / "
-                  "min(prefill, push); gemm_prefill's prefill_slowdown and its narrow_pushes: 24 steps without and "
-                  "24 with the pushes, alternating, each step drained before the next, medians compared (separately "
-                  "timed runs, kept under separate_runs, drift by a few per cent between themselves)")
+                     "prefill_slowdown": round(c1 / c0 - 1, 4), "step_ms_with_push": round(sp1, 4),
+                     "hidden_frac": round((c0 + p_only - sp1) / min(c0, p_only), 3)})
+    out["how"] = ("24 prefill steps without and 24 with the pushes, alternating, each step drained before the "
+                  "next, medians compared: the prefill chain is the time on its stream from a step's first layer to "
+                  "its last, step_ms_with_push runs to the end of the last copy, prefill_slowdown = chain with / "
+                  "chain alone - 1, hidden_frac = (chain alone + push alone - step with pushes) / min(chain alone, "
+                  f"push alone), push alone the median of {steps} pipelined push-only steps; separate_runs: the same "
+                  f"from separately timed pipelined runs ({steps} steps each, 50 with the GEMM prefill), which "
+                  "drift by a few per cent between themselves (clock and power)")
     return out
 
 

@@ -343,35 +343,36 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     return it;
 }
 
-// Tensor-map copies of one box (rank 4: head bytes / 8, head, slot, block; x always 0). The load
+// Tensor-map copies of one box (rank 4: head bytes / 8, then head and slot in the plan's box order,
+// block; x always 0; c1, c2 are the head and slot coordinates in that order). The load
 // completes on the stage's mbarrier; the store joins the thread's current bulk group.
 // With `hint` both carry the evict-first L2 policy (launches that stream 8 MiB or more: on GB300 a
 // 32 MiB-per-layer head-layout push went from 0.836-0.844 to 0.873-0.874 of the copy peak in the
 // per-layer step with it, 0.61-0.62 to 0.62-0.63 alone, a 497 MB layer unchanged at 0.99).
-__device__ __forceinline__ void tensor_load(void *stage, const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk,
+__device__ __forceinline__ void tensor_load(void *stage, const CUtensorMap *map, int32_t c1, int32_t c2, int32_t blk,
                                             uint64_t *bar, bool hint, uint64_t policy) {
     if (hint)
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
             "[%1, {%2, %3, %4, %5}], [%6], %7;"
-            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar)), "l"(policy)
+            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(c1), "r"(c2), "r"(blk), "r"(smem_addr(bar)), "l"(policy)
             : "memory");
     else
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(bar))
+            ::"r"(smem_addr(stage)), "l"(map), "r"(0), "r"(c1), "r"(c2), "r"(blk), "r"(smem_addr(bar))
             : "memory");
 }
 
-__device__ __forceinline__ void tensor_store(const CUtensorMap *map, int32_t h, int32_t slot, int32_t blk, const void *stage,
+__device__ __forceinline__ void tensor_store(const CUtensorMap *map, int32_t c1, int32_t c2, int32_t blk, const void *stage,
                                              bool hint, uint64_t policy) {
     if (hint)
         asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4}], [%5], %6;"
-                     ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage)), "l"(policy)
+                     ::"l"(map), "r"(0), "r"(c1), "r"(c2), "r"(blk), "r"(smem_addr(stage)), "l"(policy)
                      : "memory");
     else
         asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
-                     ::"l"(map), "r"(0), "r"(h), "r"(slot), "r"(blk), "r"(smem_addr(stage))
+                     ::"l"(map), "r"(0), "r"(c1), "r"(c2), "r"(blk), "r"(smem_addr(stage))
                      : "memory");
 }
 
@@ -416,10 +417,13 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
         mbar_arrive_expect(&bar[s], it.bytes);
         if (!it.bytes) return;
         uint8_t *stage = ring + (size_t)s * stage_bytes;
-        if (TENSOR && it.tensor) {
+        if (TENSOR && it.tensor && !a.ts.flat) {
             const CUtensorMap *map = a.src_maps + it.s_buf;
             if (map != fenced_src) { map_acquire(map); fenced_src = map; }
-            tensor_load(stage, map, it.sh, it.ss, it.sb, &bar[s], hint, policy);
+            const bool hnd = a.box_order == KVX_LAYOUT_HND;
+            tensor_load(stage, map, hnd ? it.ss : it.sh, hnd ? it.sh : it.ss, it.sb, &bar[s], hint, policy);
+        } else if (TENSOR && it.tensor) {
+            bulk_load(stage, it.src, it.bytes, &bar[s], hint, policy);   // the box is this side's span
         } else if (token_major(it)) {
             const uint32_t span = (uint32_t)(it.heads * a.width);    // one token's heads
             if (a.src_pitch == (int64_t)span) {
@@ -465,10 +469,13 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk(CopyArgs a, int64_t n_work, 
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint8_t *stage = ring + (size_t)s * stage_bytes;
             const BulkItem &it = items[s];
-            if (TENSOR && it.tensor) {
+            if (TENSOR && it.tensor && !a.td.flat) {
                 const CUtensorMap *map = a.dst_maps + it.d_buf;
                 if (map != fenced_dst) { map_acquire(map); fenced_dst = map; }
-                tensor_store(map, it.dh, it.ds, it.db, stage, hint, policy);
+                const bool hnd = a.box_order == KVX_LAYOUT_HND;
+                tensor_store(map, hnd ? it.ds : it.dh, hnd ? it.dh : it.ds, it.db, stage, hint, policy);
+            } else if (TENSOR && it.tensor) {
+                bulk_store(it.dst, stage, it.bytes, hint, policy);
             } else if (token_major(it)) {
                 for (int32_t h = 0; h < it.heads; ++h)
                     for (int32_t r = 0; r < it.n; ++r)

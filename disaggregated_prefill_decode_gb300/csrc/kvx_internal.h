@@ -27,11 +27,14 @@ struct alignas(16) TileDesc {
 static_assert(sizeof(TileDesc) == 32, "TileDesc is two 16-byte words");
 
 // TENSOR plans: what the kernel needs to turn a tile's byte offsets into tensor-map coordinates
-// (head, slot, block) on each side, and the maps' box (box_n token slots x box_k heads).
+// (head, slot, block) on each side, and the maps' box (box_n token slots x box_k heads, laid out in
+// shared memory in the plan's box order: KVX_LAYOUT_NHD slot-major, KVX_LAYOUT_HND head-major).
 struct TensorSide {
     int64_t hb;                       // head bytes
     int32_t layout, bs, hps;
     int32_t sh_hb, sh_bs, sh_hps;     // log2 of hb / bs / hps when a power of two, else -1
+    int32_t flat;                     // a box is one contiguous span on this side, in the box order:
+                                      // moved by one plain bulk copy instead of a tensor-map copy
 };
 
 // Kernel arguments of one push launch (passed by value).
@@ -55,6 +58,7 @@ struct CopyArgs {
     const CUtensorMap *dst_maps;      // TENSOR: one map per consumer buffer
     TensorSide ts, td;                // TENSOR: producer / consumer geometry
     int32_t box_n, box_k;             // TENSOR: the maps' box
+    int32_t box_order;                // TENSOR: KVX_LAYOUT_NHD or KVX_LAYOUT_HND (the box in shared memory)
     int32_t width;                    // strided: bytes copied per row
     int32_t n_planes;
     int32_t src_shards;
@@ -184,6 +188,8 @@ struct kvx_plan_s {
     int32_t layers_per_launch_req = 0;         // kvx_push_layers: layers per launch asked for (0: by size)
     int32_t max_ctas = 0;                      // upper bound on CTAs per copy launch (0: none)
     int32_t box_n = 0, box_k = 0;              // TENSOR: token slots x heads of a tile the maps move at once
+    int32_t box_order = KVX_LAYOUT_NHD;        // TENSOR: layout of the box in shared memory
+    bool head_tile_auto = false;               // head-group tiles of the library's default size
     std::vector<CUtensorMap> maps;             // TENSOR: producer buffers' maps, then consumer buffers' (host)
     int32_t outside_device = -1;               // a pool buffer outside device memory (-1: not checked yet)
     int32_t next_lane = 0;
@@ -239,6 +245,9 @@ inline bool staged_kernel(int32_t k) { return k == KVX_KERNEL_STAGED; }
 // TENSOR plans: encodes one tensor map per pool buffer into pl->maps (host); false when the driver
 // refuses a map (the plan then runs PERSIST) (kvx_push.cu).
 bool encode_tensor_maps(kvx_plan_s *pl);
+// TENSOR plans: whether a box (box_n slots x box_k heads, laid out in `order`) is one contiguous span
+// of a side with geometry g (kvx_tiles.cpp).
+bool tensor_side_flat(const Geom &g, int32_t order, int32_t box_n, int32_t box_k);
 // Checks where the pools' buffers live (first and last buffer of each side) and records it; refuses
 // pageable host memory the GPU cannot reach (kvx_push.cu).
 kvx_status check_pool_memory(kvx_plan_s *pl);

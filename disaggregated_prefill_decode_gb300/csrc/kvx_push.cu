@@ -164,20 +164,22 @@ static EncodeTiledFn encoder() {
     return fn;
 }
 
-// Maps already encoded, by (buffer base, side geometry, box): plans rebuilt every step over the same
-// pools find theirs here instead of encoding one per buffer again.
-using MapKey = std::tuple<uintptr_t, int32_t, int32_t, int32_t, int64_t, int64_t, int32_t, int32_t>;
+// Maps already encoded, by (buffer base, side geometry, box, box order): plans rebuilt every step over
+// the same pools find theirs here instead of encoding one per buffer again.
+using MapKey = std::tuple<uintptr_t, int32_t, int32_t, int32_t, int64_t, int64_t, int32_t, int32_t, int32_t>;
 static std::mutex g_map_mu;
 static std::map<MapKey, CUtensorMap> g_map_cache;
 
-// One side's buffer as a rank-4 tensor of 8-byte elements: (head bytes / 8, head, token slot, block),
-// strides from the layout (NHD: a head's row follows the previous head's, a slot follows all heads;
-// HND: a slot's row follows the previous slot's, a head follows all slots). The box is
-// (head bytes / 8, box_k heads, box_n slots, 1 block): a load lands in shared memory slot-major,
-// heads inner, whichever the side's layout, and a store writes it back in the other side's layout.
-static bool encode_one(const Geom &g, void *base, int32_t box_n, int32_t box_k, CUtensorMap *out) {
+// One side's buffer as a rank-4 tensor of 8-byte elements. In box order NHD the dimensions are
+// (head bytes / 8, head, token slot, block), in box order HND (head bytes / 8, token slot, head,
+// block); the strides come from the side's own layout (NHD: a head's row follows the previous head's,
+// a slot follows all heads; HND: a slot's row follows the previous slot's, a head follows all slots).
+// The box is (head bytes / 8, box_k heads, box_n slots, 1 block) in the order's dimensions, so a load
+// lands in shared memory in the box order whichever the side's layout, and a store writes the box
+// back in the side's layout.
+static bool encode_one(const Geom &g, void *base, int32_t box_n, int32_t box_k, int32_t order, CUtensorMap *out) {
     const MapKey key{(uintptr_t)base, g.layout, g.block_size, g.heads_per_shard, g.head_bytes(), g.n_blocks, box_n,
-                     box_k};
+                     box_k, order};
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_map_cache.find(key);
@@ -186,16 +188,19 @@ static bool encode_one(const Geom &g, void *base, int32_t box_n, int32_t box_k, 
     EncodeTiledFn enc = encoder();
     if (!enc || g.n_blocks < 1) return false;
     const int64_t hb = g.head_bytes();
-    const cuuint64_t dim[4] = {(cuuint64_t)(hb / 8), (cuuint64_t)g.heads_per_shard, (cuuint64_t)g.block_size,
-                               (cuuint64_t)g.n_blocks};
     const cuuint64_t row = (cuuint64_t)g.row_bytes(), blk = (cuuint64_t)g.block_size * row;
-    const cuuint64_t stride_nhd[3] = {(cuuint64_t)hb, row, blk};
-    const cuuint64_t stride_hnd[3] = {(cuuint64_t)(g.block_size * hb), (cuuint64_t)hb, blk};
-    const cuuint32_t box[4] = {(cuuint32_t)(hb / 8), (cuuint32_t)box_k, (cuuint32_t)box_n, 1};
+    // byte strides of one head and one slot in the side's layout
+    const cuuint64_t head_stride = g.layout == KVX_LAYOUT_HND ? (cuuint64_t)(g.block_size * hb) : (cuuint64_t)hb;
+    const cuuint64_t slot_stride = g.layout == KVX_LAYOUT_HND ? (cuuint64_t)hb : row;
+    const bool hnd = order == KVX_LAYOUT_HND;
+    const cuuint64_t dim[4] = {(cuuint64_t)(hb / 8), hnd ? (cuuint64_t)g.block_size : (cuuint64_t)g.heads_per_shard,
+                               hnd ? (cuuint64_t)g.heads_per_shard : (cuuint64_t)g.block_size, (cuuint64_t)g.n_blocks};
+    const cuuint64_t stride[3] = {hnd ? slot_stride : head_stride, hnd ? head_stride : slot_stride, blk};
+    const cuuint32_t box[4] = {(cuuint32_t)(hb / 8), (cuuint32_t)(hnd ? box_n : box_k), (cuuint32_t)(hnd ? box_k : box_n),
+                               1};
     const cuuint32_t elem[4] = {1, 1, 1, 1};
-    const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, base, dim,
-                           g.layout == KVX_LAYOUT_HND ? stride_hnd : stride_nhd, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, base, dim, stride, box, elem,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lk(g_map_mu);
@@ -208,9 +213,15 @@ bool encode_tensor_maps(kvx_plan_s *pl) {
     const size_t ns = pl->src_base.size(), nd = pl->dst_base.size();
     pl->maps.resize(ns + nd);
     for (size_t i = 0; i < ns; ++i)
-        if (!encode_one(pl->src, pl->src_base[i], pl->box_n, pl->box_k, &pl->maps[i])) { pl->maps.clear(); return false; }
+        if (!encode_one(pl->src, pl->src_base[i], pl->box_n, pl->box_k, pl->box_order, &pl->maps[i])) {
+            pl->maps.clear();
+            return false;
+        }
     for (size_t i = 0; i < nd; ++i)
-        if (!encode_one(pl->dst, pl->dst_base[i], pl->box_n, pl->box_k, &pl->maps[ns + i])) { pl->maps.clear(); return false; }
+        if (!encode_one(pl->dst, pl->dst_base[i], pl->box_n, pl->box_k, pl->box_order, &pl->maps[ns + i])) {
+            pl->maps.clear();
+            return false;
+        }
     return true;
 }
 
@@ -221,8 +232,9 @@ static int32_t log2_or_minus1(int64_t v) {
     return k;
 }
 
-static TensorSide tensor_side(const Geom &g) {
+static TensorSide tensor_side(const kvx_plan_s *pl, const Geom &g) {
     TensorSide t;
+    t.flat = tensor_side_flat(g, pl->box_order, pl->box_n, pl->box_k);
     t.hb = g.head_bytes();
     t.layout = g.layout;
     t.bs = g.block_size;
@@ -270,10 +282,11 @@ CopyArgs plan_copy_args(const kvx_plan_s *pl, int32_t layer0) {
         pl->maps.empty() ? nullptr : reinterpret_cast<const CUtensorMap *>(base + pl->off_maps);
     a.src_maps = maps;
     a.dst_maps = maps ? maps + pl->src_base.size() : nullptr;
-    a.ts = tensor_side(pl->src);
-    a.td = tensor_side(pl->dst);
+    a.ts = tensor_side(pl, pl->src);
+    a.td = tensor_side(pl, pl->dst);
     a.box_n = pl->box_n;
     a.box_k = pl->box_k;
+    a.box_order = pl->box_order;
     a.n_tiles = pl->n_tiles;
     a.src_buf_bytes = pl->src.buf_bytes();
     a.dst_buf_bytes = pl->dst.buf_bytes();

@@ -191,19 +191,24 @@ static int32_t default_tile_bytes(const Geom &s, const Geom &d) {
 }
 
 // Default tile of a plan that maps one head layout onto another: a segment of min(block sizes)
-// tokens for the most heads a producer shard and a consumer shard share that fit kHeadTileTarget
-// bytes, the head count a divisor of the shared group so that every group splits into equal tiles
-// (each then one tensor-map copy per side; see tensor_box).
+// tokens for the most heads a producer shard and a consumer shard share that fit `target` bytes, the
+// head count a divisor of the shared group so that every group splits into equal tiles (each then
+// one tensor-map box; see tensor_box). The target is kHeadTileTarget, or kTensorTileTarget for plans
+// that resolve to TENSOR (measured on GB300, 32 MiB per layer in the per-layer step, a consumer or
+// producer side moved by plain bulk copies: 16 KiB tiles in a 4-stage ring 0.886-0.888 of the copy
+// peak, 32 KiB tiles -- a whole block of 8 heads -- in a 2-stage ring 0.922-0.931, in a 3-stage ring
+// 0.85; alone 0.65-0.68 against 0.665 and 0.72).
 constexpr int64_t kHeadTileTarget = 16384;
+constexpr int64_t kTensorTileTarget = 32768;
 
-static int32_t default_head_tile_bytes(const Geom &s, const Geom &d) {
+static int32_t default_head_tile_bytes(const Geom &s, const Geom &d, int64_t target) {
     const int64_t hb = s.head_bytes();
     const int64_t n = std::min(s.block_size, d.block_size);
     const int32_t group = std::min(s.heads_per_shard, d.heads_per_shard);
     int32_t k = 1;
     for (int32_t c = group; c >= 1; --c)
-        if (group % c == 0 && c * n * hb <= kHeadTileTarget) { k = c; break; }
-    const int64_t t = std::max<int64_t>(16, std::min<int64_t>((int64_t)k * n * hb, kHeadTileTarget));
+        if (group % c == 0 && c * n * hb <= target) { k = c; break; }
+    const int64_t t = std::max<int64_t>(16, std::min<int64_t>((int64_t)k * n * hb, target));
     return (int32_t)(t - t % 16);
 }
 
@@ -220,7 +225,8 @@ void init_copy_shape(kvx_plan_s *pl, bool tile_bytes_given) {
     pl->src_head_pitch = pl->per_head ? (s.layout == KVX_LAYOUT_HND ? s.block_size : 1) * s.head_bytes() : 0;
     pl->dst_head_pitch = pl->per_head ? (d.layout == KVX_LAYOUT_HND ? d.block_size : 1) * d.head_bytes() : 0;
     if (!tile_bytes_given && !pl->strided) pl->tile_bytes = default_tile_bytes(s, d);
-    if (!tile_bytes_given && pl->per_head && !same_head_major(s, d)) pl->tile_bytes = default_head_tile_bytes(s, d);
+    pl->head_tile_auto = !tile_bytes_given && pl->per_head && !same_head_major(s, d);
+    if (pl->head_tile_auto) pl->tile_bytes = default_head_tile_bytes(s, d, kHeadTileTarget);
 }
 
 // A plan that only ever copies whole blocks between two head-major pools with the same head
@@ -256,6 +262,17 @@ constexpr int64_t kLargeLayer = (int64_t)128 << 20;
 // The box of a TENSOR plan's maps: tiles of box_n token slots for box_k heads go through the maps
 // (segments of min(block sizes) tokens, or tile_bytes / head_bytes of them when a head's segment is
 // longer than a tile; as many heads as build_head_tiles puts in such a tile).
+// The box order is the layout of the box in shared memory. A side whose layout is the box order and
+// whose box is one contiguous span (token-major: all of a shard's heads; head-major: all of a block's
+// slots) moves a box by one plain bulk copy, and only the other side through its map, which then does
+// the transpose. The consumer side is preferred (measured on GB300, 32 MiB per layer in the per-layer
+// step: head-major -> token-major 0.870 with maps on both sides against 0.917 with a plain store,
+// token-major -> head-major 0.871 against 0.893 with a plain load; the tensor-map load transposes
+// faster than the store).
+bool tensor_side_flat(const Geom &g, int32_t order, int32_t box_n, int32_t box_k) {
+    return g.layout == order && (order == KVX_LAYOUT_NHD ? box_k == g.heads_per_shard : box_n == g.block_size);
+}
+
 static void tensor_box(kvx_plan_s *pl) {
     const int64_t hb = pl->src.head_bytes();
     const int64_t rows = std::max<int64_t>(1, pl->tile_bytes / hb);
@@ -263,6 +280,12 @@ static void tensor_box(kvx_plan_s *pl) {
     const int32_t group = std::min(pl->src.heads_per_shard, pl->dst.heads_per_shard);
     pl->box_n = (int32_t)std::min<int64_t>(seg, rows);
     pl->box_k = pl->box_n == seg ? (int32_t)std::min<int64_t>(group, std::max<int64_t>(1, rows / seg)) : 1;
+    if (tensor_side_flat(pl->dst, pl->dst.layout, pl->box_n, pl->box_k))
+        pl->box_order = pl->dst.layout;
+    else if (tensor_side_flat(pl->src, pl->src.layout, pl->box_n, pl->box_k))
+        pl->box_order = pl->src.layout;
+    else
+        pl->box_order = KVX_LAYOUT_NHD;
 }
 
 // A TENSOR plan needs head rows the maps can describe (16..2048 bytes, 16-byte multiples, a box of
@@ -286,12 +309,12 @@ static void resolve_kernel(kvx_plan_s *pl) {
     const bool row_groups = pl->per_head && !same_head_major(pl->src, pl->dst);
     tensor_box(pl);
     int32_t k = pl->kernel;
-    // plans that map one head layout onto another: tensor-map copies with a 4-stage ring (measured on
-    // GB300, 32 MiB per layer: 0.84 of the copy peak in the per-layer step against 0.81 for PERSIST
-    // and 0.83-0.90 for STAGED, and 0.62 for a launch alone against 0.59-0.67 and 0.42-0.54; one
-    // 497 MB layer of the batched workload 0.990 against 0.968 for PERSIST, 0.87 for STAGED)
-    if (automatic && row_groups && tensor_ok(pl) && !pl->bulk_stages_req) {
-        pl->bulk_stages = 4;
+    // plans that map one head layout onto another: tensor-map copies (measured on GB300, 32 MiB per
+    // layer: 0.92-0.93 of the copy peak in the per-layer step against 0.81 for PERSIST and 0.83-0.90
+    // for STAGED; one 497 MB layer of the batched workload 1.00 against 0.968 for PERSIST, 0.87 for
+    // STAGED), in a 2-stage ring for tiles above 16 KiB, else 4 stages (3 where 4 do not fit)
+    if ((automatic || pl->kernel == KVX_KERNEL_TENSOR) && row_groups && tensor_ok(pl) && !pl->bulk_stages_req) {
+        pl->bulk_stages = pl->tile_bytes > kHeadTileTarget ? 2 : 4;
         if (!tensor_ok(pl)) pl->bulk_stages = 3;
     }
     if (automatic) k = row_groups ? (tensor_ok(pl) ? KVX_KERNEL_TENSOR : KVX_KERNEL_PERSIST)
@@ -321,8 +344,24 @@ void finish_plan_shape(kvx_plan_s *pl) {
     int64_t toks = pl->device_built ? pl->device_tokens : 0;
     for (int32_t n : pl->run_ntok) toks += n;
     pl->bytes_per_layer = toks * pl->src.row_bytes() * pl->src.n_shards * pl->src.n_planes;
+    const int32_t kernel_req = pl->kernel;   // as asked (resolve_kernel replaces it with the resolved one)
     resolve_stages(pl);
     resolve_kernel(pl);
+    // a TENSOR plan whose tile is the library's takes the larger TENSOR tile (its tiles are built
+    // after this), unless that tile no longer resolves to TENSOR
+    if (pl->kernel == KVX_KERNEL_TENSOR && pl->head_tile_auto && !pl->device_built) {
+        const int32_t small = pl->tile_bytes;
+        pl->tile_bytes = default_head_tile_bytes(pl->src, pl->dst, kTensorTileTarget);
+        pl->kernel = kernel_req;
+        resolve_stages(pl);
+        resolve_kernel(pl);
+        if (pl->kernel != KVX_KERNEL_TENSOR) {
+            pl->tile_bytes = small;
+            pl->kernel = kernel_req;
+            resolve_stages(pl);
+            resolve_kernel(pl);
+        }
+    }
 }
 
 }  // namespace kvx

@@ -131,13 +131,19 @@ def test_head_major_plans_group_heads_per_tile():
     assert (info["kernel"], info["threads"], info["bulk_stages"]) == (kvx.KVX_KERNEL_TENSOR, 32, 4)
     kvx.kvx_plan_destroy(plan)
     plan = kvx.kvx_plan_ex(sp, dp, reqs, {"kernel": kvx.KVX_KERNEL_STAGED})
-    assert (kvx.kvx_plan_get_info(plan)["kernel"], kvx.kvx_plan_get_info(plan)["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
+    info = kvx.kvx_plan_get_info(plan)
+    assert (info["kernel"], info["threads"]) == (kvx.KVX_KERNEL_STAGED, 128)
+    assert info["tile_bytes"] == 4 * 16 * 256                  # other kernels: head groups of up to 16 KiB
     kvx.kvx_plan_destroy(plan)
-    # the default tile of such a plan is a whole head group that divides the shared heads
-    plan = kvx.kvx_plan(sp, dp, reqs)
-    tiles = kvx.kvx_plan_tiles(plan)
-    assert kvx.kvx_plan_get_info(plan)["tile_bytes"] == 4 * 16 * 256 and (tiles["heads"] == 4).all()
-    kvx.kvx_plan_destroy(plan)
+    # the default tile of a TENSOR plan is a head group that divides the shared heads, up to 32 KiB
+    # (here a whole block of 8 heads), in a 2-stage ring; asked-for TENSOR takes the same
+    for opts in ({}, {"kernel": kvx.KVX_KERNEL_TENSOR}):
+        plan = kvx.kvx_plan_ex(sp, dp, reqs, opts)
+        tiles = kvx.kvx_plan_tiles(plan)
+        info = kvx.kvx_plan_get_info(plan)
+        assert (info["kernel"], info["tile_bytes"], info["bulk_stages"]) == (kvx.KVX_KERNEL_TENSOR, 8 * 16 * 256, 2)
+        assert (tiles["heads"] == 8).all() and (tiles["n"] == 16).all()
+        kvx.kvx_plan_destroy(plan)
     # head rows no tensor map can describe (24 bytes: not a multiple of 16) run the persistent kernel
     s24, d24 = sg.replace(head_dim=12), dg.replace(head_dim=12)
     p24, q24 = pools(s24, d24)
@@ -353,13 +359,14 @@ def test_kernel_resolution():
 
 def test_head_group_default_tiles_divide_the_shared_heads():
     """Plans that map one head layout onto another cut each block segment into equal head groups: the
-    largest divisor of the heads a producer shard and a consumer shard share that fits 16 KiB, so
-    every group is one tensor-map box (6 shared heads of 256 B over 12-token blocks: 3 heads a tile;
-    a TP1 -> TP2 split with 4 shared heads: 4)."""
+    largest divisor of the heads a producer shard and a consumer shard share that fits 32 KiB on the
+    tensor-map kernel, so every group is one tensor-map box (6 shared heads of 256 B over 12-token
+    blocks: all 6 in a tile; a TP1 -> TP2 split with 4 shared heads: 4; 8 heads of 512 B: 4)."""
     cases = [
-        (PoolGeom(1, 2, 1, 6, 128, 2, 12, 40), PoolGeom(1, 2, 1, 6, 128, 2, 12, 40, 1), 3, 12),
+        (PoolGeom(1, 2, 1, 6, 128, 2, 12, 40), PoolGeom(1, 2, 1, 6, 128, 2, 12, 40, 1), 6, 12),
         (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40), PoolGeom(1, 2, 2, 4, 128, 2, 16, 40, 1), 4, 16),
-        (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(1, 2, 1, 8, 128, 2, 32, 20), 4, 16),
+        (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(1, 2, 1, 8, 128, 2, 32, 20), 8, 16),
+        (PoolGeom(1, 2, 1, 8, 256, 2, 16, 40, 1), PoolGeom(1, 2, 1, 8, 256, 2, 16, 40), 4, 16),
     ]
     for sg, dg, k, n in cases:
         sp, dp = pools(sg, dg)
@@ -370,7 +377,7 @@ def test_head_group_default_tiles_divide_the_shared_heads():
         info = kvx.kvx_plan_get_info(plan)
         tiles = kvx.kvx_plan_tiles(plan)
         assert info["kernel"] == kvx.KVX_KERNEL_TENSOR
-        assert info["tile_bytes"] == k * n * 256
+        assert info["tile_bytes"] == k * n * sg.head_dim * sg.elem_bytes
         assert (np.maximum(tiles["heads"], 1) == k).all() and (tiles["n"] == n).all()
         total_heads = sg.n_shards * sg.heads_per_shard
         assert len(tiles) == (n_tok // n) * (total_heads // k)

@@ -256,6 +256,39 @@ def test_geometry_sweep(name, kernel):
     kvx.kvx_plan_destroy(plan)
 
 
+# Tensor-map plans: the box (box_n slots x box_k heads) is laid out in shared memory in the consumer's
+# layout when a box is one contiguous span of the consumer (token-major: all of a shard's heads;
+# head-major: all of a block's slots), else in the producer's when it is one of the producer's, else
+# token-major; a side whose layout that is and which holds the box contiguously moves it by a plain bulk
+# copy, the other through its tensor map. (name: src, dst, tile_bytes, the case it takes)
+BOX_CASES = {
+    "nhd_to_hnd_store_plain": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 40), PoolGeom(2, 2, 1, 8, 128, 2, 16, 40, 1), 0),
+    "hnd_to_nhd_store_plain": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(2, 2, 1, 8, 128, 2, 16, 40), 0),
+    "hnd_to_nhd_load_plain": (PoolGeom(2, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(2, 2, 1, 8, 128, 2, 16, 40), 16384),
+    "nhd_to_hnd_bs32_load_plain": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 1, 8, 128, 2, 32, 30, 1), 0),
+    "nhd_to_hnd_bs32_both_maps": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 60), PoolGeom(1, 2, 1, 8, 128, 2, 32, 30, 1), 16384),
+    "hnd_tp1_to_hnd_tp2_both_plain": (PoolGeom(1, 2, 1, 8, 128, 2, 16, 40, 1), PoolGeom(1, 2, 2, 4, 128, 2, 16, 40, 1), 0),
+    "nhd_to_hnd_6heads_store_plain": (PoolGeom(1, 2, 1, 6, 128, 2, 12, 50), PoolGeom(1, 2, 1, 6, 128, 2, 12, 50, 1), 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BOX_CASES))
+def test_tensor_box_orders(name):
+    from helpers import random_requests
+    sg, dg, tile_bytes = BOX_CASES[name]
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    reqs = random_requests(rng, sg, dg, 4, min(sg.n_blocks * sg.block_size, dg.n_blocks * dg.block_size) // 4)
+    src, _ = device_pool(sg, "bf16_normal", seed=11)
+    dst, _ = device_pool(dg, "canary_bf16_normal")
+    plan = kvx.kvx_plan_ex(kvx.Pool(sg, src), kvx.Pool(dg, dst), reqs, {"tile_bytes": tile_bytes})
+    assert kvx.kvx_plan_get_info(plan)["kernel"] == kvx.KVX_KERNEL_TENSOR
+    assert push_all_layers(plan, sg.n_layers) == kvx.KVX_OK
+    per = dg.n_planes * dg.n_shards
+    check_layers(sg, src, dg, dst, lambda l: [canary_host(dg, "bf16_normal") for _ in range(per)], reqs,
+                 range(sg.n_layers))
+    kvx.kvx_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 def test_offsets_past_4gib(kernel):
     """One 4.9 GB buffer per side (150,000 blocks of 32 KiB): runs that start and end beyond 2^32 bytes,
