@@ -694,9 +694,11 @@ def run_kvx(args, rank, local_rank, world):
             "runs": info["n_runs"], "tiles_per_layer_plane": info["n_tiles"], "tile_bytes": info["tile_bytes"],
             "vec_bytes": info["vec_bytes"], "kernel": KERNEL_SHORT[info["kernel"]],
             "lanes": info["lanes"], "bulk_stages": info["bulk_stages"],
+            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
             "threads": info["threads"],
-            "ctas_per_sm": args.ctas_per_sm or "auto (below 128 MiB per launch: 5 per 4 SMs bulk, 2 persistent, 4 "
-                                               "persistent on head groups; above: the occupancy limit)",
+            "ctas_per_sm": args.ctas_per_sm or "auto (below 128 MiB per launch: 2 per SM on the bulk and tensor-map "
+                                               "kernels, 2 persistent, 4 persistent on head groups; above: the "
+                                               "occupancy limit)",
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
                       "stream records the layer's event, then kvx_push_layer(priority 0 side stream, event) forks "
@@ -836,8 +838,13 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
     stage_big = torch.empty(per * stage_geom.n_buffers, dtype=torch.uint8, device=src[0].device)
     stage = [stage_big[i * per:i * per + stage_geom.buffer_bytes] for i in range(stage_geom.n_buffers)]
     stp = kvx.Pool(stage_geom, stage)
-    host_src = [torch.empty(s_rng[1] - s_rng[0], dtype=torch.uint8, pin_memory=True) for _ in range(len(src))]
-    host_dst = [torch.empty(stage_geom.buffer_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(len(stage))]
+    # one pinned allocation per side, cut into the buffers (16-byte aligned pieces)
+    hs_n = -(-(s_rng[1] - s_rng[0]) // 4096) * 4096
+    hd_n = -(-stage_geom.buffer_bytes // 4096) * 4096
+    host_src_big = torch.empty(hs_n * len(src), dtype=torch.uint8, pin_memory=True)
+    host_dst_big = torch.empty(hd_n * len(stage), dtype=torch.uint8, pin_memory=True)
+    host_src = [host_src_big[i * hs_n:i * hs_n + (s_rng[1] - s_rng[0])] for i in range(len(src))]
+    host_dst = [host_dst_big[i * hd_n:i * hd_n + stage_geom.buffer_bytes] for i in range(len(stage))]
     for h, d in zip(host_src, src):
         h.copy_(d[s_rng[0]:s_rng[1]])
     h2d, side, d2h = torch.cuda.Stream(), torch.cuda.Stream(priority=-1), torch.cuda.Stream()
@@ -1367,6 +1374,13 @@ def run_reference(args, rank, world):
 
 
 def main():
+    # 32 hardware work queues for this process's streams (read by the CUDA runtime when it creates the
+    # context, so set before any CUDA call; a caller's own setting wins). With the runtime's default of
+    # 8, the bench's streams and the library's lanes share queues in an order that depends on when each
+    # stream was created, and a lane that shares one with the prefill stream waits behind it: the same
+    # push measured 0.88 or 0.97 of the copy peak on alternate calls in one process. The library sizes
+    # its default lanes from the same variable.
+    os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     args = parse()
     if args.warmup < 3:
         args.warmup = 3

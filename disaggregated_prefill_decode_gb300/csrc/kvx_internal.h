@@ -182,7 +182,7 @@ struct kvx_plan_s {
     int32_t flags = 0;                         // KVX_PLAN_* bits
     int32_t kernel = 0;                        // resolved KVX_KERNEL_*
     int32_t ctas_per_sm = 0;                   // resident CTAs per SM of persistent kernels (0: by size)
-    int32_t lanes = 4;                         // internal streams pushes fan out over
+    int32_t lanes = 4;                         // internal streams pushes fan out over (default_lanes())
     int32_t bulk_stages_req = 0;               // ring stages asked for (0: by plan kind)
     int32_t bulk_stages = 4;                   // ring stages of the bulk kernel, resolved
     int32_t layers_per_launch_req = 0;         // kvx_push_layers: layers per launch asked for (0: by size)
@@ -242,6 +242,9 @@ inline int32_t effective_kernel(const kvx_plan_s *pl) {
 // ring with 128 threads storing.
 inline bool ring_kernel(int32_t k) { return k == KVX_KERNEL_BULK || k == KVX_KERNEL_TENSOR; }
 inline bool staged_kernel(int32_t k) { return k == KVX_KERNEL_STAGED; }
+// Lanes of a plan that asks for none: 4, or half the process's hardware work queues
+// (CUDA_DEVICE_MAX_CONNECTIONS) when that is fewer, at least 1 (kvx_plan.cpp).
+int32_t default_lanes();
 // TENSOR plans: encodes one tensor map per pool buffer into pl->maps (host); false when the driver
 // refuses a map (the plan then runs PERSIST) (kvx_push.cu).
 bool encode_tensor_maps(kvx_plan_s *pl);

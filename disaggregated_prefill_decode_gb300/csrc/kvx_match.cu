@@ -483,6 +483,14 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *i
     if (threadIdx.x == 0) *sum = total;
 }
 
+// Error bit 64: a look-back scan gave up waiting on an earlier tile, so the sums after it are wrong.
+// The kernels that consume scan results then do nothing (the call returns KVX_ETIMEDOUT): indexes
+// taken from wrong sums could point outside the arrays.
+constexpr int32_t kScanTimedOut = 64;
+__device__ __forceinline__ bool scan_failed(const int32_t *err) {
+    return (*(const volatile int32_t *)err & kScanTimedOut) != 0;
+}
+
 constexpr uint64_t kScanWaitNs = 1000000000ull;   // 1 s: far beyond any legitimate wait on a predecessor
 constexpr uint64_t kScanStallWaitNs = 1000000ull;  // 1 ms: the bound under the testing hook
 
@@ -499,7 +507,7 @@ __device__ __forceinline__ uint64_t scan_clock_ns() {
 // state[t] holds 0 (nothing yet), total * 4 + 1 (the tile's total) or prefix * 4 + 2 (the prefix
 // through the tile); state[n_tiles] is the ticket counter; all zero before the launch. A wait is
 // bounded by the global timer (wait_ns): past the bound the scan sets error bit 64 and goes on (wrong
-// sums, reported by the caller). stall_tile (testing hook, -1 normally): that tile publishes nothing,
+// sums, which the kernels after it then leave unused; the caller returns KVX_ETIMEDOUT). stall_tile (testing hook, -1 normally): that tile publishes nothing,
 // so the tile after it waits until the bound.
 __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t *in, int64_t *out, int64_t n_host,
                                                                    const int64_t *n_dev, unsigned long long *state,
@@ -525,7 +533,7 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t 
                 const unsigned long long f = __ldcg(&state[p]);             // from L2, where the writers publish
                 if ((f & 3ull) == 0) {
                     if (t0 == 0) t0 = scan_clock_ns();
-                    else if (scan_clock_ns() - t0 > wait_ns) { atomicOr(err, 64); break; }
+                    else if (scan_clock_ns() - t0 > wait_ns) { atomicOr(err, kScanTimedOut); break; }
                     continue;
                 }
                 excl += (int64_t)(f >> 2);
@@ -642,11 +650,12 @@ __global__ void kvx_emit_pairs_holes(const int64_t *need, const int64_t *npos, c
                                      int64_t n_pub, const int32_t *free_blocks, int64_t *pair_src, int64_t *pair_dst,
                                      int64_t *pair_sess, const int64_t *n_need, const int64_t *n_counted, int32_t *err) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (scan_failed(err)) return;
     // the flags must account for exactly the blocks the sessions counted
     if (k == 0 && n_pub > 0 && *n_need != *n_counted) atomicOr(err, 32);
     if (k >= n_pub || !need[k]) return;
     const int64_t pos = npos[k];
-    if (pos >= *total) return;
+    if (pos < 0 || pos >= *total) return;
     pair_src[pos] = remote_blk[k];
     pair_dst[pos] = free_blocks[pos];
     pair_sess[pos] = session_of(rem_off, n_sessions, k);
@@ -654,16 +663,22 @@ __global__ void kvx_emit_pairs_holes(const int64_t *need, const int64_t *npos, c
 
 // Step 3: a run starts at a new session or where either block id does not continue the previous.
 __global__ void kvx_run_flags(const int64_t *pair_src, const int64_t *pair_dst, const int64_t *pair_sess,
-                              const int64_t *total, int64_t *flag) {
+                              const int64_t *total, int64_t *flag, const int32_t *err) {
     const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (p >= *total) return;
+    if (p >= *total || scan_failed(err)) return;
     flag[p] = (p == 0 || pair_sess[p] != pair_sess[p - 1] || pair_src[p] != pair_src[p - 1] + 1 ||
                pair_dst[p] != pair_dst[p - 1] + 1) ? 1 : 0;
 }
 
-__global__ void kvx_run_starts(const int64_t *flag, const int64_t *run_idx, const int64_t *total, int64_t *run_start) {
+// run_idx[k] is the exclusive scan of the run flags, so a run's number lies in [0, total); one outside
+// is reported (bit 16) and not written.
+__global__ void kvx_run_starts(const int64_t *flag, const int64_t *run_idx, const int64_t *total, int64_t *run_start,
+                               int32_t *err) {
     const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k < *total && flag[k]) run_start[run_idx[k]] = k;
+    if (k >= *total || !flag[k] || scan_failed(err)) return;
+    const int64_t r = run_idx[k];
+    if (r < 0 || r >= *total) { atomicOr(err, 16); return; }
+    run_start[r] = k;
 }
 
 struct EmitShape {
@@ -688,11 +703,17 @@ __device__ __forceinline__ int64_t head_start(int32_t layout, int32_t hps, int32
     return layout == KVX_LAYOUT_HND ? (blk * hps + head) * (int64_t)bs : blk * (int64_t)bs * hps + head;
 }
 
-__global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, EmitShape sh, int64_t *tile_count) {
+// A run's blocks [run_start[r], run_start[r + 1]) must be a non-empty range inside [0, total): a run
+// that is not counts no tiles and is reported (bit 16).
+__device__ __forceinline__ bool run_ok(int64_t k0, int64_t k1, int64_t total) { return 0 <= k0 && k0 < k1 && k1 <= total; }
+
+__global__ void kvx_run_tiles(const int64_t *run_start, const int64_t *scalars, EmitShape sh, int64_t *tile_count,
+                              int32_t *err) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t n_runs = scalars[1], total = scalars[4];
-    if (r >= n_runs) return;
+    if (r >= n_runs || scan_failed(err)) return;
     const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
+    if (!run_ok(run_start[r], k1, total)) { tile_count[r] = 0; atomicOr(err, 16); return; }
     const int64_t ntok = (k1 - run_start[r]) * sh.bs;
     if (sh.per_head) {
         tile_count[r] = (k1 - run_start[r]) * sh.groups * ((sh.bs + sh.rows_per_tile - 1) / sh.rows_per_tile);
@@ -711,9 +732,10 @@ __global__ void kvx_emit_tiles(const int64_t *run_start, const int64_t *tile_sta
                                int32_t *err) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t n_runs = scalars[1], total = scalars[4];
-    if (r >= n_runs) return;
+    if (r >= n_runs || scan_failed(err)) return;
     const int64_t k0 = run_start[r];
     const int64_t k1 = r + 1 < n_runs ? run_start[r + 1] : total;
+    if (!run_ok(k0, k1, total) || tile_start[r] < 0) { atomicOr(err, 16); return; }
     const int64_t ntok = (k1 - k0) * sh.bs;
     const int64_t srow = pair_src[k0] * sh.bs, drow = pair_dst[k0] * sh.bs;
     run_src_row[r] = (int32_t)srow;
@@ -1086,14 +1108,14 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
                                                                        &m.scalars[0], m.err);
             ok(cudaGetLastError());
             kvx_run_flags<<<grid_for(B, 256), 256, 0, stream>>>(m.pair_src, m.pair_dst, pair_sess, &m.scalars[4],
-                                                                m.flag);
+                                                                m.flag, m.err);
         }
         ok(cudaGetLastError());
         ok(exclusive_scan(m.flag, m.run_idx, B, &m.scalars[4], m.scan_state + n_state, &m.scalars[1], m.err, stream,
                           (mf.flags & KVX_MATCH_TEST_SCAN_STALL) != 0));
-        kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start);
+        kvx_run_starts<<<grid_for(B, 256), 256, 0, stream>>>(m.flag, m.run_idx, &m.scalars[4], m.run_start, m.err);
         ok(cudaGetLastError());
-        kvx_run_tiles<<<grid_for(B, 256), 256, 0, stream>>>(m.run_start, m.scalars, sh, m.tile_count);
+        kvx_run_tiles<<<grid_for(B, 256), 256, 0, stream>>>(m.run_start, m.scalars, sh, m.tile_count, m.err);
         ok(cudaGetLastError());
         ok(exclusive_scan(m.tile_count, m.tile_start, B, &m.scalars[1], m.scan_state + 2 * n_state, &m.scalars[2],
                           m.err, stream));
@@ -1108,7 +1130,7 @@ kvx_status kvx_match_prefix_ex(const uint32_t *tokens, const int64_t *tok_off, i
     const int64_t *h_scal = back.scal;
     const int32_t h_err = back.err[0];
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "kvx_match_prefix"));
-    if (h_err & 64) return cleanup(fail(KVX_ETIMEDOUT, "a plan scan waited past its bound for an earlier tile"));
+    if (h_err & kScanTimedOut) return cleanup(fail(KVX_ETIMEDOUT, "a plan scan waited past its bound for an earlier tile"));
     if (h_err & ~8) return cleanup(fail(KVX_EINVAL, "malformed session or remote offsets (error bits %d)", h_err));
     if (h_err & 8)
         return cleanup(fail(KVX_ENOMEM, "pushing sessions need %lld blocks, free list has %lld", (long long)h_scal[0],

@@ -126,7 +126,13 @@ typedef struct kvx_plan_opts {
                                  ring kernels (BULK, TENSOR, STAGED) and with PERSIST (4 for
                                  head-group tiles), leaving room for the caller's compute and an
                                  overlapping push; the occupancy limit for larger launches) */
-    int32_t lanes;            /* internal streams pushes fan out over (0: default 4; 1: none)    */
+    int32_t lanes;            /* internal streams pushes fan out over (0: the default, 1: none):
+                                 4, or half the hardware work queues of the process
+                                 (CUDA_DEVICE_MAX_CONNECTIONS, 8 when unset) when that is fewer,
+                                 at least 1. Streams beyond the queues share them, and a lane that
+                                 shares a queue with the caller's compute stream waits behind it:
+                                 run with CUDA_DEVICE_MAX_CONNECTIONS >= 2 x (lanes + the caller's
+                                 own streams) so that pushes overlap as intended                 */
     int32_t bulk_stages;      /* ring kernels: shared-memory stages of tile_bytes each, one of 2, 3,
                                  4, 6, 8 with stages * tile_bytes <= 192 KiB (0: 3; 4 for TENSOR
                                  chosen by AUTO)                                                 */
@@ -261,7 +267,7 @@ kvx_status kvx_plan_tiles(kvx_plan_t plan, int64_t *n_tiles, const void **tiles)
  *
  * The push is ordered after everything already enqueued on `stream` and, if `ready` is not NULL,
  * after `ready`. The call only enqueues: it returns before the copy runs. Completion is what
- * kvx_sync reports, not stream order: with lanes > 1 (the default, 4) the copy runs on one of the
+ * kvx_sync reports, not stream order: with lanes > 1 (the default) the copy runs on one of the
  * library's internal high-priority streams ("lanes", forked from `stream` by an event), so
  * consecutive pushes of different layers can overlap on the GPU, the head of one hiding the tail
  * of the previous; work enqueued on `stream` later is not ordered after the copy. Lanes run at the

@@ -322,7 +322,7 @@ def test_kernel_resolution():
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"ctas_per_sm": 99}))
     expect(kvx.KVX_EINVAL, lambda: kvx.kvx_plan_ex(sp, dp, [ok], {"lanes": 9}))
     p = kvx.kvx_plan(sp, dp, [ok])
-    assert kvx.kvx_plan_get_info(p)["lanes"] == 4
+    assert kvx.kvx_plan_get_info(p)["lanes"] in (1, 2, 3, 4)                  # by the process's hardware queues
     assert kvx.kvx_plan_get_info(p)["bulk_stages"] == 3
     kvx.kvx_plan_destroy(p)
     # AUTO by size: a layer push reading >= 128 MiB runs PERSIST with 128 threads unless asked otherwise
@@ -406,3 +406,34 @@ def test_stall_hook_argument_checks():
         plan = kvx.kvx_plan_ex(hp, hq, reqs, {"kernel": kernel})
         kvx.kvx_plan_inject_stall(plan, 0)
         kvx.kvx_plan_destroy(plan)
+
+
+_LANES_PROBE = """
+import numpy as np
+from kvx_inputs import PoolGeom
+from disaggregated_prefill_decode_gb300 import kvx
+g = PoolGeom(2, 2, 1, 8, 128, 2, 16, 40)
+def pool(base):
+    return kvx.Pool(g, [base + i * (g.buffer_bytes + 256) for i in range(g.n_buffers)])
+reqs = [(64, np.arange(4, dtype=np.int32), np.arange(10, 14, dtype=np.int32))]
+p = kvx.kvx_plan(pool(1 << 40), pool(1 << 44), reqs)
+print(kvx.kvx_plan_get_info(p)["lanes"])
+kvx.kvx_plan_set_opts(p, {"lanes": 0})
+print(kvx.kvx_plan_get_info(p)["lanes"])
+"""
+
+
+@pytest.mark.parametrize("queues,lanes", [(None, 4), ("1", 1), ("2", 1), ("4", 2), ("6", 3), ("8", 4), ("32", 4)])
+def test_default_lanes_follow_the_hardware_queues(queues, lanes):
+    """The default lane count follows CUDA_DEVICE_MAX_CONNECTIONS as the process started: 4 lanes, or
+    half the queues when that is fewer, at least 1 (8 queues, the runtime's default: 4)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k != "CUDA_DEVICE_MAX_CONNECTIONS"}
+    if queues is not None:
+        env["CUDA_DEVICE_MAX_CONNECTIONS"] = queues
+    env["PYTHONPATH"] = os.pathsep.join([root, os.path.join(root, "tests"), env.get("PYTHONPATH", "")])
+    out = subprocess.run([sys.executable, "-c", _LANES_PROBE], env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(lanes), str(lanes)]
