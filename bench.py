@@ -736,6 +736,9 @@ def run_kvx(args, rank, local_rank, world):
         result["connector"] = connector_rate(kvx)
         if not args.no_e2e:
             result["e2e"] = run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world)
+            gc.collect()
+            torch.cuda.empty_cache()
+            result["e2e"]["host_pools"] = run_e2e_host_pools(args, torch, kvx, w, dst, dp, reqs, opts, bytes_step)
         if not args.no_match:
             result["match"] = run_match(torch, kvx, device, {"kernel": args.kernel, "threads": args.threads,
                                                              "ctas_per_sm": args.ctas_per_sm,
@@ -815,6 +818,79 @@ def memcpy_ceiling(torch, device):
             "head_transpose": {"value": round(2 * n / (xpose * 1e-3) / 1e9, 1), "unit": "GB/s",
                                "how": "torch copy_ of 2 GiB of [block][16][8][128] bf16 into [block][8][16][128] "
                                       "(token-major -> head-major whole blocks), best of 10"}}
+
+
+def run_e2e_host_pools(args, torch, kvx, w, dst, dp, reqs, opts, bytes_step):
+    """The end-to-end path through the C-ABI with host buffers and no separate copies: the producer
+    pool lives in pinned host memory and kvx_push_layer reads it over the chip-to-chip link into the
+    device consumer pool; a second plan gathers the pushed consumer blocks into a staging pool in pinned
+    host memory (the kernels write it over the link). Per layer push then gather, gated by an event;
+    plans built each step and synced after the next step is issued; host wall clock. The staged bytes
+    must equal the producer's for the first request (equal layouts), which is checked."""
+    L = w.src.n_layers
+    nb = [-(-n // w.dst.block_size) for n, _, _ in reqs]
+    off = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+    stage_geom = w.dst.replace(n_blocks=int(off[-1]))
+    stage_reqs = [(n, d[:k], np.arange(off[i], off[i] + k, dtype=np.int32))
+                  for i, ((n, _, d), k) in enumerate(zip(reqs, nb))]
+    ps = -(-w.src.buffer_bytes // 4096) * 4096
+    pd = -(-stage_geom.buffer_bytes // 4096) * 4096
+    hsrc_big = torch.empty(ps * w.src.n_buffers, dtype=torch.uint8, pin_memory=True)
+    hdst_big = torch.empty(pd * stage_geom.n_buffers, dtype=torch.uint8, pin_memory=True)
+    hsrc = [hsrc_big[i * ps:i * ps + w.src.buffer_bytes] for i in range(w.src.n_buffers)]
+    hdst = [hdst_big[i * pd:i * pd + stage_geom.buffer_bytes] for i in range(stage_geom.n_buffers)]
+    g = torch.Generator(device=dst[0].device).manual_seed(w.seed)
+    for h in hsrc:                                    # seeded bytes, drawn on the device, copied over
+        h.copy_(torch.randint(0, 256, (h.numel(),), dtype=torch.uint8, device=dst[0].device, generator=g))
+    hp, hs = kvx.Pool(w.src, hsrc), kvx.Pool(stage_geom, hdst)
+    side = torch.cuda.Stream(priority=-1)
+    ev_p = [torch.cuda.Event() for _ in range(L)]
+    for ev in ev_p:
+        ev.record(side)
+
+    def issue():
+        plan = kvx.kvx_plan_ex(hp, dp, reqs, opts)
+        gather = kvx.kvx_plan_ex(dp, hs, stage_reqs, opts)
+        for layer in range(L):
+            kvx.kvx_push_layer_notify(plan, layer, layer + 1, side, None, ev_p[layer])
+            kvx.kvx_push_layer(gather, layer, side, ev_p[layer])
+        return plan, gather
+
+    def finish(plans):
+        for pl in plans:
+            assert kvx.kvx_sync(pl, -1) == kvx.KVX_OK
+            kvx.kvx_plan_destroy(pl)
+
+    def run(n):
+        prev = None
+        for _ in range(n):
+            cur = issue()
+            if prev is not None:
+                finish(prev)
+            prev = cur
+        finish(prev)
+
+    run(2)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    run(args.e2e_steps)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t) / args.e2e_steps
+    n0, b0 = int(reqs[0][0]), [int(x) for x in reqs[0][1]]
+    checked = None
+    if w.src.layout == w.dst.layout == kvx_inputs.LAYOUT_NHD and w.src.block_size == w.dst.block_size and n0 > 0:
+        rb, bs = w.src.row_bytes, w.src.block_size
+        want = torch.cat([hsrc[0][b * bs * rb:(b + 1) * bs * rb] for b in b0])[:n0 * rb]
+        checked = bool(torch.equal(hdst[0][:n0 * rb], want))
+        assert checked, "host-pool e2e result differs from the producer KV"
+    return {"value": round(bytes_step / dt / 1e9, 2), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 3),
+            "steps": args.e2e_steps, "result_checked": checked,
+            "h2d_bytes_per_step": bytes_step // 2, "d2h_bytes_per_step": bytes_step // 2,
+            "how": "producer pool in pinned host memory, consumer pool on the device, staging pool in pinned host "
+                   "memory: per layer kvx_push_layer_notify host -> device and kvx_push_layer (gather) device -> host, "
+                   "both read or written over the chip-to-chip link by the copy kernel (the persistent plain-load "
+                   "kernel, which the library runs for pools outside device memory); no separate copies; host wall "
+                   "clock"}
 
 
 def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world):
