@@ -102,7 +102,9 @@ static kvx_status check_overlap(const std::vector<void *> &src, int64_t src_byte
 int32_t default_lanes() {
     static const int32_t lanes = [] {
         const char *e = std::getenv("CUDA_DEVICE_MAX_CONNECTIONS");
-        const long queues = e && *e ? std::strtol(e, nullptr, 10) : 8;
+        char *end = nullptr;
+        long queues = e ? std::strtol(e, &end, 10) : 8;
+        if (!e || end == e || queues < 1) queues = 8;       // unset or not a count: the runtime's default
         return (int32_t)std::max<long>(1, std::min<long>(4, queues / 2));
     }();
     return lanes;

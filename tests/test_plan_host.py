@@ -423,7 +423,8 @@ print(kvx.kvx_plan_get_info(p)["lanes"])
 """
 
 
-@pytest.mark.parametrize("queues,lanes", [(None, 4), ("1", 1), ("2", 1), ("4", 2), ("6", 3), ("8", 4), ("32", 4)])
+@pytest.mark.parametrize("queues,lanes", [(None, 4), ("1", 1), ("2", 1), ("4", 2), ("6", 3), ("8", 4), ("32", 4),
+                                          ("", 4), ("many", 4), ("0", 4)])
 def test_default_lanes_follow_the_hardware_queues(queues, lanes):
     """The default lane count follows CUDA_DEVICE_MAX_CONNECTIONS as the process started: 4 lanes, or
     half the queues when that is fewer, at least 1 (8 queues, the runtime's default: 4)."""
