@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kMatchThreads, 2) kvx_match_sessions(const uin
 __global__ void __launch_bounds__(kScanThreads) kvx_scan_single(const int64_t *in, int64_t *out, int64_t n_host,
                                                                  const int64_t *n_dev, int64_t *sum) {
     __shared__ int64_t ws[32];
-    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t n = n_dev ? min(*n_dev, n_host) : n_host;   // a device count never past the host bound
     const int64_t i = threadIdx.x;
     const int64_t v = i < n ? in[i] : 0;
     int64_t total;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kScanThreads) kvx_scan_lookback(const int64_t 
     if (threadIdx.x == 0) tile_s = (int64_t)atomicAdd(&state[n_tiles], 1ull);
     __syncthreads();
     const int64_t tile = tile_s;
-    const int64_t n = n_dev ? *n_dev : n_host;
+    const int64_t n = n_dev ? min(*n_dev, n_host) : n_host;   // a device count never past the host bound
     const int64_t i = tile * blockDim.x + threadIdx.x;
     const int64_t v = i < n ? in[i] : 0;
     int64_t total;
