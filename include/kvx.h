@@ -153,13 +153,15 @@ typedef struct kvx_plan_opts {
  * place in the consumer's layout with 16-byte stores, so a head transpose needs no ring slot on the
  * store side.
  * TENSOR (plans with one token-major and one head-major side, or head-major sides that differ in
- * block size or head split): the bulk ring of BULK, but each tile of a head group is one tensor-map
- * (TMA) load and one tensor-map store. Every pool buffer gets a tensor map of its own layout --
- * dimensions (head bytes, head, token slot, block) with that layout's strides -- and both maps
- * traverse a tile in the same order, so a token-major tile lands head-major (or back) in the copy
- * itself, one bulk operation per side instead of one per row. Tiles of another shape (a partial last
- * block) move row by row. Needs 16-byte aligned buffers and head rows of 16..2048 bytes in multiples
- * of 16; host-built plans only; otherwise PERSIST. */
+ * block size or head split): the bulk ring of BULK, but each tile of a head group is one box of a
+ * tensor map (TMA). Every pool buffer gets a map over its own layout's strides, with the box laid
+ * out in shared memory in one layout for both sides (the consumer's when a box is one contiguous
+ * span of the consumer, else the producer's when it is one of the producer's, else token-major). A
+ * side that holds the box as one span in that layout moves it with one plain bulk copy; the other
+ * side moves it with one tensor-map load or store, which does the transpose. Default tiles: the most
+ * shared heads of one block segment that fit 32 KiB, in a 2-stage ring. Tiles of another shape (a
+ * partial last block) move row by row. Needs 16-byte aligned buffers and head rows of 16..2048 bytes
+ * in multiples of 16; host-built plans only; otherwise PERSIST. */
 
 /* Copy kernels. TILE: one CTA per tile. PERSIST: a grid of (SMs x resident CTAs) walks the tiles,
  * loading the next descriptor while it copies the current tile. BULK: the same walk with the bulk
@@ -171,8 +173,8 @@ typedef struct kvx_plan_opts {
  * applies to a plan that reads under 128 MiB per layer (two CTAs per SM with a 3-stage ring, leaving
  * room for the caller's compute and the next push) and PERSIST with 128 threads per CTA otherwise
  * (measured fastest on GB300 for large layer pushes); plans with one token-major and one head-major
- * side, or two head-major sides with different block sizes or head splits, take TENSOR with a
- * 4-stage ring at any size when the tensor maps can describe them, else PERSIST. */
+ * side, or two head-major sides with different block sizes or head splits, take TENSOR (32 KiB
+ * tiles, 2-stage ring) at any size when the tensor maps can describe them, else PERSIST. */
 #define KVX_KERNEL_AUTO 0
 #define KVX_KERNEL_TILE 1
 #define KVX_KERNEL_PERSIST 2
