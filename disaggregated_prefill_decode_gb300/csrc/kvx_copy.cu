@@ -277,7 +277,8 @@ struct BulkItem {
     int32_t n;         // strided tiles: rows of a.width bytes per head; contiguous tiles: 1
     int32_t heads;     // strided tiles: heads of the group (1 for a single head)
     int32_t layer;
-    int32_t tensor;    // TENSOR: the tile is the maps' box and moves as one tensor copy each way
+    int32_t tensor;    // TENSOR: the tile is the maps' box: one copy each way (a plain bulk copy on a
+                       // side that holds the box as one span, else a tensor-map copy)
     int32_t s_buf, d_buf;             // TENSOR: buffer (map) index on each side
     int32_t sh, ss, sb, dh, ds, db;   // TENSOR: (head, slot, block) of the tile on each side
 };
@@ -332,7 +333,7 @@ __device__ __forceinline__ BulkItem bulk_item(const CopyArgs &a, int64_t w, int3
     }
     it.bytes = (uint32_t)bytes;
     if (TENSOR && t.n == a.box_n && it.heads == a.box_k) {
-        // the maps' box: one tensor copy each way when it stays inside a block and a shard on both sides
+        // the maps' box: one copy each way when it stays inside a block and a shard on both sides
         side_coords(a.ts, t.src_off, &it.sb, &it.ss, &it.sh);
         side_coords(a.td, t.dst_off, &it.db, &it.ds, &it.dh);
         it.s_buf = (int32_t)(lp * a.src_shards + t.s_shard);
