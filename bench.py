@@ -6,8 +6,8 @@ block 16, one 8192-token prompt = 512 blocks, pools of 615 blocks, destination i
 
 One step = the whole push path for one batch of requests on the workload's pools: build the plan,
 then per layer run the synthetic prefill fixture on the priority stream (it records the layer's
-ready event) and kvx_push_layer gated on that event. Steps are issued with one step of look-ahead (a
-step's plan is synced after the next step has been issued). The pools are far larger than L2, so no
+ready event) and kvx_push_layer gated on that event. Steps are issued with two steps of look-ahead (a
+step's plan is synced after the two steps after it have been issued). The pools are far larger than L2, so no
 flush is needed between steps.
 
 value = read+write bytes of all timed steps / device time of the timed steps (CUDA events on the
@@ -71,6 +71,8 @@ def parse():
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--lanes", type=int, default=0, help="internal push streams (0: library default)")
     p.add_argument("--bulk-stages", type=int, default=0, help="bulk kernel ring stages (0: library default)")
+    p.add_argument("--lookahead", type=int, default=2,
+                   help="engine loop: steps issued before the oldest one is synced (1: sync a step after the next is issued)")
     p.add_argument("--fixture-ctas", type=int, default=8)
     p.add_argument("--fixture-iters", type=int, default=2000)
     p.add_argument("--timing-every", type=int, default=4,
@@ -277,7 +279,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
     """Allocates the workload's pools and times K steps of the per-layer push pattern after W untimed
     ones. A step builds the requests' plan, runs the synthetic prefill (per layer a fixture kernel on
     the priority stream that records the layer's ready event) and pushes every layer gated on its
-    event; each step is synced after the next one is issued. The pushes of every `every`-th step are
+    event; each step is synced after `args.lookahead` later steps are issued. The pushes of every `every`-th step are
     timed (the kernels' own global-timer stamps); the warm-up steps follow the same pattern, so the
     timed loop meets no first use. `all_layers`: one kvx_push_layers call per step for all layers,
     gated on the last layer's event, instead of one kvx_push_layer per layer; `extra_opts` are added
@@ -319,7 +321,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
         """n steps of the engine loop, natively (the fixture library's kvx_fixture_run_steps, through the
         kvx C-ABI): per step a plan (a timing plan when the step's index is a multiple of `every`, the
         warm-up steps included, so the timed loop meets no first use), per layer the fixture and the
-        gated push; each step synced after the next one is issued. Timed runs record a CUDA event on
+        gated push; each step synced after `args.lookahead` later ones are issued. Timed runs record a CUDA event on
         the prefill stream where each step starts and after the last sync."""
         marks, marks_arr = None, None
         if timed:
@@ -334,7 +336,7 @@ def time_push_workload(args, torch, kvx, w, device, K, W, every, sampler=None, b
                                       args.fixture_iters, main_h, side_h, ctypes.addressof(ready_arr),
                                       ctypes.addressof(marks_arr) if timed else None,
                                       s_ns.ctypes.data if timed else None, e_ns.ctypes.data if timed else None, cap,
-                                      ctypes.addressof(n_st), iss.ctypes.data, pln.ctypes.data)
+                                      ctypes.addressof(n_st), iss.ctypes.data, pln.ctypes.data, args.lookahead)
         if rc:
             raise RuntimeError(f"engine loop: {fx.kvx_fixture_last_error().decode()}")
         return marks, iss[:n], pln[:n]
@@ -702,8 +704,8 @@ def run_kvx(args, rank, local_rank, world):
             "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read+written per step vs 129 MB L2; no flush",
             "launch": f"per layer: fixture ({args.fixture_ctas} CTAs x {args.fixture_iters} iters) on a priority -1 "
                       "stream records the layer's event, then kvx_push_layer(priority 0 side stream, event) forks "
-                      "onto the push lanes and waits for it; a plan is built every step and synced after the next "
-                      "step is issued; the engine loop issuing this runs natively (libkvx_fixture's "
+                      "onto the push lanes and waits for it; a plan is built every step and synced after "
+                      f"{args.lookahead} more steps are issued; the engine loop issuing this runs natively (libkvx_fixture's "
                       "kvx_fixture_run_steps, through the kvx C-ABI)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },

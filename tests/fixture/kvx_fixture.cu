@@ -8,6 +8,7 @@
 #include <atomic>
 #include <chrono>
 #include <cstdio>
+#include <deque>
 #include <vector>
 
 namespace {
@@ -98,8 +99,9 @@ extern "C" int kvx_fixture_run_steps(const kvx_pool *src, const kvx_pool *dst, c
                                      int32_t all_layers, int32_t fixture_ctas, int64_t fixture_iters,
                                      cudaStream_t main, cudaStream_t side, const cudaEvent_t *ready,
                                      const cudaEvent_t *marks, int64_t *start_ns, int64_t *end_ns, int64_t cap,
-                                     int64_t *n_stamps, double *issue_us, double *plan_us) {
-    if (!src || !dst || !ready || n_steps < 0 || every < 1) return fixture_fail("run_steps: bad arguments");
+                                     int64_t *n_stamps, double *issue_us, double *plan_us, int32_t lookahead) {
+    if (!src || !dst || !ready || n_steps < 0 || every < 1 || lookahead < 1)
+        return fixture_fail("run_steps: bad arguments");
     const int32_t n_layers = src->n_layers;
     kvx_plan_opts plain{}, timing{};
     if (opts) plain = *opts;
@@ -125,7 +127,19 @@ extern "C" int kvx_fixture_run_steps(const kvx_pool *src, const kvx_pool *dst, c
         return d == KVX_OK ? 0 : kvx_fail("kvx_plan_destroy", d);
     };
 
-    Issued prev;
+    std::deque<Issued> inflight;   // issued steps not yet synced, oldest first
+    auto drain = [&](size_t keep) -> int {
+        while (inflight.size() > keep) {
+            const Issued p = inflight.front();
+            inflight.pop_front();
+            if (finish(p)) {
+                for (const Issued &q : inflight) kvx_plan_destroy(q.plan);
+                inflight.clear();
+                return -1;
+            }
+        }
+        return 0;
+    };
     for (int32_t i = 0; i < n_steps; ++i) {
         const auto h0 = std::chrono::steady_clock::now();
         if (marks && cudaEventRecord(marks[i], main) != cudaSuccess) return fixture_fail("run_steps: mark record");
@@ -146,10 +160,10 @@ extern "C" int kvx_fixture_run_steps(const kvx_pool *src, const kvx_pool *dst, c
             if (st != KVX_OK) return kvx_fail("kvx_push_layers", st);
         }
         if (issue_us) issue_us[i] = us_since(h0);
-        if (prev.plan && finish(prev)) return -1;
-        prev = cur;
+        inflight.push_back(cur);
+        if (drain((size_t)lookahead)) return -1;
     }
-    if (prev.plan && finish(prev)) return -1;
+    if (drain(0)) return -1;
     if (marks && cudaEventRecord(marks[n_steps], main) != cudaSuccess) return fixture_fail("run_steps: mark record");
     return 0;
 }

@@ -33,8 +33,8 @@ int kvx_fixture_prefill(int32_t ctas, int64_t iters, void *buf, int64_t n_bytes,
  * i % every == 0 -- then per layer l: the fixture (fixture_ctas CTAs x fixture_iters) on `main`,
  * ready[l] recorded after it, and kvx_push_layer(plan, l, side, ready[l]) (with all_layers != 0: the
  * fixtures of every layer, then one kvx_push_layers over all of them gated on the last layer's
- * event). Each step's plan is synced (kvx_sync, no deadline) after the next step is issued, then
- * destroyed. marks, when not NULL, holds n_steps + 1 events: marks[i] is recorded on `main` where
+ * event). A step's plan is synced (kvx_sync, no deadline) once `lookahead` later steps have been
+ * issued (1: after the next one), then destroyed; the last ones after the loop. marks, when not NULL, holds n_steps + 1 events: marks[i] is recorded on `main` where
  * step i starts, marks[n_steps] after the last step's sync. The timed plans' push stamps (global
  * timer, ns) are appended to start_ns / end_ns (up to cap entries; *n_stamps receives the count);
  * issue_us[i] / plan_us[i] (may be NULL) receive the host time to issue step i and to build its
@@ -47,7 +47,8 @@ int kvx_fixture_run_steps(const struct kvx_pool *src, const struct kvx_pool *dst
                           int32_t n_reqs, const struct kvx_plan_opts *opts, int32_t every, int32_t n_steps,
                           int32_t all_layers, int32_t fixture_ctas, int64_t fixture_iters, cudaStream_t main,
                           cudaStream_t side, const cudaEvent_t *ready, const cudaEvent_t *marks, int64_t *start_ns,
-                          int64_t *end_ns, int64_t cap, int64_t *n_stamps, double *issue_us, double *plan_us);
+                          int64_t *end_ns, int64_t cap, int64_t *n_stamps, double *issue_us, double *plan_us,
+                          int32_t lookahead);
 
 /* Fixture kernels launched by this process so far. */
 int64_t kvx_fixture_launch_count(void);

@@ -58,7 +58,8 @@ def lib():
         P = ctypes.c_void_p
         l.kvx_fixture_run_steps.restype = ctypes.c_int
         l.kvx_fixture_run_steps.argtypes = [P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                            ctypes.c_int32, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int64, P, P, P]
+                                            ctypes.c_int32, ctypes.c_int64, P, P, P, P, P, P, ctypes.c_int64, P, P, P,
+                                            ctypes.c_int32]
         _lib = l
     return _lib
 
