@@ -195,9 +195,10 @@ static int32_t default_tile_bytes(const Geom &s, const Geom &d) {
 // head count a divisor of the shared group so that every group splits into equal tiles (each then
 // one tensor-map box; see tensor_box). The target is kHeadTileTarget, or kTensorTileTarget for plans
 // that resolve to TENSOR (measured on GB300, 32 MiB per layer in the per-layer step, a consumer or
-// producer side moved by plain bulk copies: 16 KiB tiles in a 4-stage ring 0.886-0.888 of the copy
-// peak, 32 KiB tiles -- a whole block of 8 heads -- in a 2-stage ring 0.922-0.931, in a 3-stage ring
-// 0.85; alone 0.65-0.68 against 0.665 and 0.72).
+// producer side moved by plain bulk copies, 2 CTAs per SM: 16 KiB tiles in a 4-stage ring 0.886-0.888
+// of the copy peak, 32 KiB tiles -- a whole block of 8 heads -- in a 2-stage ring 0.922-0.931, in a
+// 3-stage ring 0.85; alone 0.65-0.68 against 0.665 and 0.72; the 2-stage ring of 32 KiB tiles at up to
+// 3 CTAs per SM with every CTA taking 3 tiles: 0.954-0.958, alone 0.712).
 constexpr int64_t kHeadTileTarget = 16384;
 constexpr int64_t kTensorTileTarget = 32768;
 
@@ -310,7 +311,7 @@ static void resolve_kernel(kvx_plan_s *pl) {
     tensor_box(pl);
     int32_t k = pl->kernel;
     // plans that map one head layout onto another: tensor-map copies (measured on GB300, 32 MiB per
-    // layer: 0.92-0.93 of the copy peak in the per-layer step against 0.81 for PERSIST and 0.83-0.90
+    // layer: 0.95-0.96 of the copy peak in the per-layer step against 0.81 for PERSIST and 0.83-0.90
     // for STAGED; one 497 MB layer of the batched workload 1.00 against 0.968 for PERSIST, 0.87 for
     // STAGED), in a 2-stage ring for tiles above 16 KiB, else 4 stages (3 where 4 do not fit)
     if ((automatic || pl->kernel == KVX_KERNEL_TENSOR) && row_groups && tensor_ok(pl) && !pl->bulk_stages_req) {
