@@ -632,6 +632,9 @@ def per_config(args, torch, kvx, device):
                     "roofline_frac": round(achieved / peak, 4), "mean_launch_us": round(m["mean_push_ms"] * 1e3, 3),
                     "kernel": KERNEL_NAMES[m["info"]["kernel"]], "threads": m["info"]["threads"],
                     "bytes_per_launch": bytes_launch,
+                    "l2": (f"inputs larger than L2 ({m['bytes_step'] / 1e9:.2f} GB read+written per step); no flush"
+                           if m["bytes_step"] > (129 << 20) else
+                           f"fits in L2 ({m['bytes_step'] / 1e6:.1f} MB per step), not flushed: launch-bound, reported"),
                     "traffic": None if all_layers else ncu_traffic(name)})
         del m
         gc.collect()
