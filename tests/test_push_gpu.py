@@ -677,3 +677,39 @@ def test_stall_hook_needs_the_bulk_kernel():
         kvx.kvx_plan_inject_stall(plan, 0)
     assert ei.value.status == kvx.KVX_EUNSUPPORTED
     kvx.kvx_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("lookahead,all_layers", [(1, 0), (2, 0), (3, 1)])
+def test_native_engine_loop_pushes_exact_bytes(lookahead, all_layers):
+    """The benchmark's native engine loop (kvx_fixture_run_steps: a plan per step, per layer the prefill
+    fixture and the gated push, `lookahead` steps in flight, timing plans every other step) leaves the
+    consumer pool equal to the oracle's push on every layer, with every plan synced and destroyed."""
+    import ctypes
+    w = kvx_inputs.qwen3_32b_single(n_layers=4)
+    src, _ = device_pool(w.src, w.values, seed=w.seed)
+    dst, _ = device_pool(w.dst, "canary_" + w.values)
+    sp, dp = kvx.Pool(w.src, src), kvx.Pool(w.dst, dst)
+    carr, n_req, _keep = kvx._requests(reqs_of(w))
+    o = kvx._opts({})
+    main, side = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(w.src.n_layers)]
+    for ev in ready:
+        ev.record(main)
+    ready_arr = (ctypes.c_void_p * w.src.n_layers)(*[int(ev.cuda_event) for ev in ready])
+    cap = 4096
+    s_ns, e_ns = np.zeros(cap, np.int64), np.zeros(cap, np.int64)
+    n_st = ctypes.c_int64(0)
+    n_steps = 5
+    iss, pln = np.zeros(n_steps), np.zeros(n_steps)
+    fx = prefill_fixture.lib()
+    rc = fx.kvx_fixture_run_steps(ctypes.addressof(sp.struct), ctypes.addressof(dp.struct), ctypes.addressof(carr),
+                                  n_req, ctypes.addressof(o), 2, n_steps, all_layers, 8, 2000, int(main.cuda_stream),
+                                  int(side.cuda_stream), ctypes.addressof(ready_arr), None, s_ns.ctypes.data,
+                                  e_ns.ctypes.data, cap, ctypes.addressof(n_st), iss.ctypes.data, pln.ctypes.data,
+                                  lookahead)
+    assert rc == 0, fx.kvx_fixture_last_error().decode()
+    torch.cuda.synchronize()
+    assert n_st.value > 0 and (e_ns[:n_st.value] >= s_ns[:n_st.value]).all()   # timed steps carry stamps
+    per = w.dst.n_planes * w.dst.n_shards
+    check_layers(w.src, src, w.dst, dst, lambda l: [canary_host(w.dst, w.values) for _ in range(per)],
+                 reqs_of(w), range(w.src.n_layers))
