@@ -78,7 +78,7 @@ def parse():
     p.add_argument("--timing-every", type=int, default=4,
                    help="time the pushes of every n-th timed step only (1: every step; reading the stamps "
                         "back costs the host about 25 us per timed step)")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--cpu-config-seconds", type=float, default=4.0,
                    help="oracle time on each other configuration (all cores, then one)")
@@ -963,6 +963,8 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
             assert kvx.kvx_sync(pl, -1) == kvx.KVX_OK
             kvx.kvx_plan_destroy(pl)
 
+    done_at = []                                      # host time each step's plans were found complete
+
     def run(n):
         """n steps, each finished (plans synced) after the next one is enqueued."""
         prev = None
@@ -970,16 +972,21 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
             cur = issue()
             if prev is not None:
                 finish(prev)
+                done_at.append(time.perf_counter())
             prev = cur
         finish(prev)
         d2h.synchronize()
+        done_at.append(time.perf_counter())
 
     run(2)
     torch.cuda.synchronize()
     t = time.perf_counter()
+    done_at.clear()
     run(args.e2e_steps)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t) / args.e2e_steps
+    # interior intervals only: the first also holds the pipeline's fill, the last its drain
+    step_ms = [(b - a) * 1e3 for a, b in zip(done_at[:-2], done_at[1:-1])] or [dt * 1e3]
     checked = None
     if w.src == w.dst.replace(n_blocks=w.src.n_blocks) and all(
             np.array_equal(np.asarray(r[1][:k]), np.arange(s_lo, s_lo + k)) for r, k in zip(reqs[:1], nb[:1])):
@@ -992,6 +999,12 @@ def run_e2e(args, torch, kvx, w, src, dst, sp, dp, reqs, opts, bytes_step, world
             "h2d_bytes_per_step": sum(h.numel() for h in host_src),
             "d2h_bytes_per_step": sum(h.numel() for h in host_dst),
             "ms_per_step": round(dt * 1e3, 3), "steps": args.e2e_steps, "result_checked": checked,
+            "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
+                        "max": round(max(step_ms), 3),
+                        "how": "host time between consecutive steps found complete, the pipeline's fill and drain "
+                               "left out; "
+                               "the chip-to-chip link is shared with the host's other traffic, and runs saw "
+                               "stretches of slower copies"},
             "how": "pinned host producer KV -> H2D per layer -> kvx_push_layer -> kvx gather of the pushed consumer "
                    "blocks into a dense staging pool -> D2H, 3 streams; a layer's H2D waits for the previous step's "
                    "D2H of that layer, each step's plans synced after the next step is enqueued; host wall clock "
